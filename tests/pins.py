@@ -1,0 +1,432 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics fix.
+
+Each function takes an ``oracle.Oracle`` and raises AssertionError when the oracle
+disagrees with a closed form, an invariant, a special case that reduces to a textbook
+routine, or brute force on a tiny input.  The same functions run against the real oracle
+(all must pass) and against copies of it with one planted mistake (at least one must fail).
+
+Sources: paper summary page "Block Sparse Attention with Log-Linear Complexity"
+(Tang et al.): section "Core method" (eq. 21, the LSE block score; leaf level uses raw
+keys), section "Method step details" (step 1 pyramid eqs 10-15, step 2 selection with the
+eq. 22 head sum and SelectK, step 3 decode, step 4 attention), section "Prerequisites"
+(LSE Taylor form, GQA groups share one selected set); the blog post of the same title,
+section 3.3 (softmax over connected positions only; weights sum to one within 1e-3).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------
+def f2b(x) -> np.ndarray:
+    """float values that are exact in bf16 -> uint16 bit patterns (asserts exactness)."""
+    a = np.asarray(x, dtype=np.float32)
+    u = a.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def b2f(b) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def random_bf16(rng, shape, scale=1.0):
+    x = (rng.standard_normal(shape) * scale).astype(np.float32)
+    u = x.view(np.uint32)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def level_offsets(sizes):
+    off = [0]
+    for m in sizes[:-1]:
+        off.append(off[-1] + m)
+    return off
+
+
+def brute_leaf_lse(Qf, Kf, scale, t, C, causal=True):
+    """Exact LSE of every leaf for one query row: Qf [G, d], Kf [N, d] (float64).
+    Returns {leaf: sum over heads of LSE over the leaf's (causal) keys}."""
+    N = Kf.shape[0]
+    M1 = (N + C - 1) // C
+    z = scale * (Qf @ Kf.T)  # [G, N]
+    out = {}
+    for j in range(M1):
+        c0, c1 = j * C, min(N, j * C + C)
+        if causal:
+            if c0 > t:
+                continue
+            c1 = min(c1, t + 1)
+        zz = z[:, c0:c1]
+        m = zz.max(axis=1, keepdims=True)
+        out[j] = float(np.sum(m[:, 0] + np.log(np.exp(zz - m).sum(axis=1))))
+    return out
+
+
+# ------------------------------------------------------------------------------------
+# step 1: the pyramid
+# ------------------------------------------------------------------------------------
+def pin_level_sizes(o):
+    """Level sizes are the closed form of the pages' pyramid (golden table)."""
+    for row in read_golden("pyramid_levels.txt"):
+        n = int(row[0])
+        want = [int(x) for x in row[1:]]
+        assert o.level_sizes(n) == want, (n, o.level_sizes(n), want)
+        assert o.num_levels(n) == len(want)
+        assert o.pyramid_nodes(n) == sum(want)
+        # L = 1 + ceil(log2 M_1)
+        assert len(want) == 1 + math.ceil(math.log2(want[0]))
+
+
+def pin_bf16_rounding(o):
+    for xs, bs in read_golden("bf16_rounding.txt"):
+        assert o.f64_to_bf16(float.fromhex(xs)) == int(bs, 16), (xs, bs, hex(o.f64_to_bf16(float.fromhex(xs))))
+
+
+def pin_pyramid_constant_keys(o):
+    """Constant keys: every summary at every level equals that key (ragged nodes too)."""
+    d, C = 16, 64
+    for N in (1, 63, 337, 64 * 5 + 1, 1024):
+        vec = f2b(np.arange(d, dtype=np.float32) * 0.25 - 1.5)
+        K = np.tile(vec, (1, 2, N, 1)).astype(np.uint16)
+        P = o.build_pyramid(K, C=C)
+        sizes = o.level_sizes(N)
+        assert P.shape[2] == sum(sizes)
+        assert np.all(P == vec[None, None, None, :]), N
+
+
+def pin_pyramid_raw_mean(o):
+    """Each summary is within accumulated rounding of the mean of the raw keys it covers
+    (mean of means of equal-size groups = overall mean; each level adds <= 2^-8 relative)."""
+    rng = np.random.default_rng(1)
+    d, C = 32, 64
+    for N in (64 * 16, 64 * 13 + 5):
+        K = random_bf16(rng, (1, 1, N, d))
+        # a ramp so that a wrong child index shows up clearly
+        Kf = b2f(K[0, 0]) + np.linspace(-4, 4, N)[:, None]
+        K[0, 0] = f2b_round(Kf)
+        Kf = b2f(K[0, 0])
+        P = b2f(o.build_pyramid(K, C=C)[0, 0])
+        sizes = o.level_sizes(N)
+        off = level_offsets(sizes)
+        for l, m in enumerate(sizes, start=1):
+            span = C * 2 ** (l - 1)
+            for i in range(m):
+                c0, c1 = i * span, min(N, (i + 1) * span)
+                full = (c1 - c0) == span
+                raw = Kf[c0:c1].mean(axis=0)
+                got = P[off[l - 1] + i]
+                tol = l * 2.0 ** -8 * np.abs(Kf[c0:c1]).max(axis=0) + 1e-6
+                if full:
+                    assert np.all(np.abs(got - raw) <= tol), (N, l, i, np.abs(got - raw).max())
+
+
+def f2b_round(x):
+    a = np.asarray(x, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def pin_pyramid_ragged_leaf_mean(o):
+    """A ragged last leaf of n keys is the mean of those n keys (not divided by C)."""
+    d, C = 8, 64
+    N = 64 + 3
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 64:67] = f2b([[2.0] * d, [4.0] * d, [6.0] * d])
+    P = o.build_pyramid(K, C=C)
+    assert np.all(b2f(P[0, 0, 1]) == 4.0)       # leaf 1 = mean(2, 4, 6)
+    assert np.all(b2f(P[0, 0, 2]) == 2.0)       # root = mean(leaf0 = 0, leaf1 = 4)
+
+
+# ------------------------------------------------------------------------------------
+# step 2: scores and selection
+# ------------------------------------------------------------------------------------
+def _spike_case(o, t, K_sel=2):
+    """Two leaves (N=128), one query head, d=64, q = 8 e_0 so that logit = k[0] exactly."""
+    d, C, N = 64, 64, 128
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 0:64, 0] = f2b(1.0)                 # leaf 0: all logits 1
+    K[0, 0, 64 + 10, 0] = f2b(6.0)              # leaf 1: one logit 6 at key 74
+    P = o.build_pyramid(K)
+    r = o.select(Q, K, P, K_sel, np.array([[0, 0, t]]), scale=1.0 / 8.0)
+    return r
+
+
+def pin_leaf_lse_closed_forms(o):
+    g = {name: float(v) for name, v in read_golden("leaf_lse_closed_forms.txt")}
+    r = _spike_case(o, t=127)
+    cand, cs = r["cand"][0], r["cand_score"][0]
+    got = {int(j): s for j, s in zip(cand, cs) if j >= 0}
+    assert abs(got[0] - g["uniform_64_logit_1"]) < 1e-12, got
+    assert abs(got[1] - g["spike_6_in_64"]) < 1e-12, got
+    # causal: query at key 69 sees keys 64..69 of its own leaf (all logits 0); the spike at 74 is masked
+    r = _spike_case(o, t=69)
+    got = {int(j): s for j, s in zip(r["cand"][0], r["cand_score"][0]) if j >= 0}
+    assert abs(got[1] - g["prefix_6_of_zeros"]) < 1e-12, got
+
+
+def pin_gqa_head_sum(o):
+    """Two query heads share one KV head: the block score is the sum of per-head LSEs (eq. 22)."""
+    g = {name: float(v) for name, v in read_golden("leaf_lse_closed_forms.txt")}
+    d, C, N = 64, 64, 128
+    Q = np.zeros((1, N, 2, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    Q[0, :, 1, 1] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 64:128, 0] = f2b(1.0)               # head 0 sees logit 1 on all of leaf 1
+    K[0, 0, 64 + 10, 1] = f2b(6.0)              # head 1 sees a spike of 6 in leaf 1
+    P = o.build_pyramid(K)
+    r = o.select(Q, K, P, 2, np.array([[0, 0, 127]]), scale=1.0 / 8.0)
+    got = {int(j): s for j, s in zip(r["cand"][0], r["cand_score"][0]) if j >= 0}
+    assert abs(got[1] - g["two_heads_1_and_spike"]) < 1e-12, got
+    assert abs(got[0] - 2 * math.log(64)) < 1e-12, got
+
+
+def pin_lse_beats_mean(o):
+    """LSE scoring prefers a leaf with one sharp key over a leaf of uniformly moderate keys,
+    which mean-pooled scoring would rank the other way (Taylor view: the variance term)."""
+    d, C, N = 64, 64, 64 * 4
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 0:64, 0] = f2b(1.0)                 # leaf 0: mean logit 1.0, LSE = log 64 + 1 = 5.16
+    K[0, 0, 64 + 7, 0] = f2b(6.0)               # leaf 1: mean logit 0.09, LSE = 6.15
+    P = o.build_pyramid(K)
+    # K=2: own leaf (3) + the single best other leaf
+    r = o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0)
+    assert list(r["idx"][0]) == [1, 3], r["idx"]
+
+
+def pin_ties_lower_index(o):
+    """Identical keys everywhere: equal scores rank the lower block index first."""
+    d, C, N = 16, 64, 64 * 6
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, :] = f2b(np.full(d, 0.5))
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, :, :] = f2b(np.full(d, 0.25))
+    P = o.build_pyramid(K)
+    r = o.select(Q, K, P, 3, np.array([[0, 0, N - 1], [0, 0, 64 * 3 + 1]]))
+    assert list(r["idx"][0]) == [0, 1, 5], r["idx"]
+    assert list(r["idx"][1]) == [0, 1, 3], r["idx"]
+
+
+def _tiny_inputs(seed=3, N=1024, H_q=4, H_kv=1, d=64, offsets=True):
+    rng = np.random.default_rng(seed)
+    Q = random_bf16(rng, (1, N, H_q, d))
+    Kf = rng.standard_normal((1, H_kv, N, d))
+    if offsets:
+        M1 = (N + 63) // 64
+        off = 0.5 * rng.standard_normal((1, H_kv, M1, d))
+        Kf = Kf + np.repeat(off, 64, axis=2)[:, :, :N]
+    K = f2b_round(Kf)
+    V = random_bf16(rng, (1, H_kv, N, d))
+    return Q, K, V
+
+
+def pin_brute_force_topk(o):
+    """When the leaves fit (M_1 <= g K, so no level prunes), the selection is the exact top-K
+    of the leaf LSE over the eligible leaves, with the own leaf always kept (brute force)."""
+    for (N, H_q, H_kv, Ksel) in ((1024, 4, 1, 8), (64 * 11 + 9, 4, 2, 6)):
+        Q, K, V = _tiny_inputs(N=N, H_q=H_q, H_kv=H_kv)
+        P = o.build_pyramid(K)
+        G = H_q // H_kv
+        d = Q.shape[-1]
+        scale = 1.0 / math.sqrt(d)
+        rows = np.array([(0, g, t) for g in range(H_kv) for t in range(0, N, 7)])
+        r = o.select(Q, K, P, Ksel, rows)
+        for i, (b, g, t) in enumerate(rows):
+            Qf = b2f(Q[b, t, g * G:(g + 1) * G])
+            lse = brute_leaf_lse(Qf, b2f(K[b, g]), scale, t, 64)
+            own = t // 64
+            others = sorted((j for j in lse if j != own), key=lambda j: (-lse[j], j))
+            want = sorted([own] + others[:Ksel - 1])
+            got = [x for x in r["idx"][i] if x >= 0]
+            assert got == want, (N, t, got, want)
+            # cand scores equal the brute-force leaf LSE
+            for j, s in zip(r["cand"][i], r["cand_score"][i]):
+                if j >= 0:
+                    assert abs(s - lse[int(j)]) < 1e-9, (t, j, s, lse[int(j)])
+
+
+def pin_final_set_invariants(o):
+    """Final sets: ascending, unique, -1 padded at the end, own leaf present,
+    |I_t| = min(K, #eligible leaves) when no level prunes; <= gK candidates; |S2| <= K."""
+    Q, K, V = _tiny_inputs(seed=5)
+    P = o.build_pyramid(K)
+    N = Q.shape[1]
+    for Ksel in (1, 3, 16):
+        rows = np.array([(0, 0, t) for t in range(N)])
+        r = o.select(Q, K, P, Ksel, rows)
+        for t in range(N):
+            row = list(r["idx"][t])
+            val = [x for x in row if x >= 0]
+            assert row == val + [-1] * (Ksel - len(val))
+            assert val == sorted(set(val))
+            assert t // 64 in val
+            assert all(x * 64 <= t for x in val)
+            assert sum(1 for x in r["cand"][t] if x >= 0) <= 2 * Ksel
+            assert sum(1 for x in r["s2"][t] if x >= 0) <= Ksel
+            if Ksel >= 8:  # M_1 = 16 <= g K: every eligible leaf is a candidate
+                assert len(val) == min(Ksel, t // 64 + 1)
+
+
+def pin_walk_prunes_by_summary_lse(o):
+    """A hand-built 3-level case where the level walk must prune: 4 leaves, K=1.
+    Leaf summaries decide level 2; the subtree whose leaf summary has the larger logit wins."""
+    d, C, N = 64, 64, 64 * 4
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 0:64, 0] = f2b(-2.0)                # leaf 0 mean -2
+    K[0, 0, 64:128, 0] = f2b(-2.0)              # leaf 1 mean -2   -> node (level 2) 0
+    K[0, 0, 128:192, 0] = f2b(3.0)              # leaf 2 mean 3    -> node (level 2) 1
+    K[0, 0, 192:256, 0] = f2b(-2.0)             # leaf 3 mean -2
+    P = o.build_pyramid(K)
+    # K=2 at t in leaf 3: level 2 has candidates {0, 1} <= K, so both kept; leaves 0..3 candidates.
+    r = o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0)
+    assert list(r["idx"][0]) == [2, 3], r["idx"]
+    # 8 leaves, K=2: level 3 has 2 nodes (kept), level 2 has 4 candidates, scored by the LSE
+    # of their two leaf summaries (eq. 21).  Leaf logits (0..7): -3 3 | 1 1 | 1.5 1.5 | -3 -3.
+    # node 0 = LSE(-3,3) = 3.0025, node 1 = LSE(1,1) = 1.693, node 2 = LSE(1.5,1.5) = 2.193,
+    # node 3 = -2.307  ->  keep {0, 2} (gap 0.5).  Scoring a node by its own mean summary
+    # would keep {1, 2} instead.  Leaves 0,1,4,5 are candidates; the own leaf 7 is added; the
+    # best other leaf is 1 (logit 3, gap 1.5 to leaves 4/5).
+    N = 64 * 8
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    for leaf, v in enumerate([-3.0, 3.0, 1.0, 1.0, 1.5, 1.5, -3.0, -3.0]):
+        K[0, 0, 64 * leaf:64 * (leaf + 1), 0] = f2b(v)
+    P = o.build_pyramid(K)
+    r = o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0)
+    assert list(r["s2"][0]) == [0, 2], r["s2"]
+    assert list(r["cand"][0]) == [0, 1, 4, 5], r["cand"]
+    assert list(r["idx"][0]) == [1, 7], r["idx"]
+    assert abs(r["min_gap"][0] - 0.5) < 1e-12, r["min_gap"]
+
+
+# ------------------------------------------------------------------------------------
+# step 4: attention
+# ------------------------------------------------------------------------------------
+def pin_dense_equivalence(o):
+    """K >= M_1 selects every eligible leaf, so the output is dense causal attention
+    (textbook softmax over keys c <= t)."""
+    for H_kv in (1, 2):
+        Q, K, V = _tiny_inputs(seed=7, N=64 * 9 + 13, H_q=4, H_kv=H_kv)
+        N, H_q, d = Q.shape[1], Q.shape[2], Q.shape[3]
+        G = H_q // H_kv
+        Ksel = (N + 63) // 64
+        P = o.build_pyramid(K)
+        sel = o.select(Q, K, P, Ksel, np.array([(0, g, t) for g in range(H_kv) for t in range(N)]))
+        idx = sel["idx"].reshape(1, H_kv, N, Ksel)
+        rows = np.array([(0, t) for t in range(0, N, 5)])
+        O, LSE, ws = o.sparse_attention(Q, K, V, idx, rows)
+        scale = 1.0 / math.sqrt(d)
+        for i, (b, t) in enumerate(rows):
+            for h in range(H_q):
+                g = h // G
+                z = scale * (b2f(K[0, g, :t + 1]) @ b2f(Q[0, t, h]))
+                m = z.max()
+                w = np.exp(z - m)
+                lse = m + math.log(w.sum())
+                out = (w / w.sum()) @ b2f(V[0, g, :t + 1])
+                assert abs(LSE[i, h] - lse) < 1e-9, (t, h, LSE[i, h], lse)
+                assert np.abs(O[i, h] - out).max() < 1e-9, (t, h)
+
+
+def pin_weights_sum_to_one(o):
+    Q, K, V = _tiny_inputs(seed=9)
+    N = Q.shape[1]
+    P = o.build_pyramid(K)
+    sel = o.select(Q, K, P, 4, np.array([(0, 0, t) for t in range(N)]))
+    _, _, ws = o.sparse_attention(Q, K, V, sel["idx"].reshape(1, 1, N, 4), np.array([(0, t) for t in range(N)]))
+    assert np.all(np.abs(ws - 1.0) <= 1e-3)
+
+
+def pin_single_block_at_start(o):
+    """Only the own block selected and t its first key: the output is v_t itself."""
+    Q, K, V = _tiny_inputs(seed=11, N=64 * 4)
+    N = Q.shape[1]
+    idx = np.full((1, 1, N, 1), -1, np.int32)
+    idx[0, 0, :, 0] = np.arange(N) // 64
+    rows = np.array([(0, t) for t in (0, 64, 128, 192)])
+    O, LSE, _ = o.sparse_attention(Q, K, V, idx, rows)
+    for i, (b, t) in enumerate(rows):
+        for h in range(Q.shape[2]):
+            assert np.array_equal(O[i, h], b2f(V[0, 0, t])), (t, h)
+            z = (b2f(Q[0, t, h]) @ b2f(K[0, 0, t])) / math.sqrt(Q.shape[3])
+            assert abs(LSE[i, h] - z) < 1e-12
+
+
+# ------------------------------------------------------------------------------------
+# step 3: decode
+# ------------------------------------------------------------------------------------
+def pin_decode(o):
+    """Decode: the incrementally kept pyramid equals a full rebuild bit for bit, and each
+    step's output equals the prefill row T over the same T+1 tokens."""
+    rng = np.random.default_rng(13)
+    B, H_q, H_kv, d, Ksel = 2, 4, 2, 32, 3
+    N0, steps, N_cap = 60, 150, 256
+    G = H_q // H_kv
+    Kc = np.zeros((B, H_kv, N_cap, d), np.uint16)
+    Vc = np.zeros((B, H_kv, N_cap, d), np.uint16)
+    seq = np.array([N0, N0 + 5], np.int32)   # sequences of different lengths
+    Kc[:, :, :N0 + 5] = random_bf16(rng, (B, H_kv, N0 + 5, d))
+    Vc[:, :, :N0 + 5] = random_bf16(rng, (B, H_kv, N0 + 5, d))
+    for b in range(B):
+        Kc[b, :, seq[b]:] = 0
+        Vc[b, :, seq[b]:] = 0
+    Pc = np.concatenate([o.build_pyramid(Kc[b:b + 1], N=int(seq[b])) for b in range(B)])
+    Qs = random_bf16(rng, (steps, B, H_q, d))
+    ks = random_bf16(rng, (steps, B, H_kv, d))
+    vs = random_bf16(rng, (steps, B, H_kv, d))
+    for s in range(steps):
+        T = seq.copy()
+        out, lse, idx = o.decode_step(Qs[s], ks[s], vs[s], Kc, Vc, Pc, seq, Ksel)
+        assert list(seq) == list(T + 1)
+        for b in range(B):
+            n = int(T[b]) + 1
+            sizes = o.level_sizes(n)
+            off_cap = level_offsets(o.level_sizes(N_cap))
+            Pfull = o.build_pyramid(Kc[b:b + 1, :, :n].copy())
+            off_n = level_offsets(sizes)
+            for l, m in enumerate(sizes, start=1):
+                assert np.array_equal(Pc[b, :, off_cap[l - 1]:off_cap[l - 1] + m], Pfull[0, :, off_n[l - 1]:off_n[l - 1] + m]), (s, b, l)
+            if s % 37 == 0 or s == steps - 1:
+                Qp = np.zeros((1, n, H_q, d), np.uint16)
+                Qp[0, n - 1] = Qs[s, b]
+                Kp, Vp = Kc[b:b + 1, :, :n].copy(), Vc[b:b + 1, :, :n].copy()
+                sel = o.select(Qp, Kp, Pfull, Ksel, np.array([(0, g, n - 1) for g in range(H_kv)]))
+                assert np.array_equal(sel["idx"], idx[b]), (s, b)
+                idxf = np.full((1, H_kv, n, Ksel), -1, np.int32)
+                idxf[0, :, n - 1] = sel["idx"]
+                O, L, _ = o.sparse_attention(Qp, Kp, Vp, idxf, np.array([(0, n - 1)]))
+                assert np.array_equal(O[0], out[b]) and np.array_equal(L[0], lse[b]), (s, b)
+
+
+ALL_PINS = [
+    pin_level_sizes, pin_bf16_rounding, pin_pyramid_constant_keys, pin_pyramid_raw_mean,
+    pin_pyramid_ragged_leaf_mean, pin_leaf_lse_closed_forms, pin_gqa_head_sum, pin_lse_beats_mean,
+    pin_ties_lower_index, pin_brute_force_topk, pin_final_set_invariants, pin_walk_prunes_by_summary_lse,
+    pin_dense_equivalence, pin_weights_sum_to_one, pin_single_block_at_start, pin_decode,
+]

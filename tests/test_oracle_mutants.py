@@ -1,0 +1,94 @@
+"""Planted mistakes in the CPU oracle must each fail at least one pin.
+
+Each mutant is a copy of the oracle source with one plausible error (a dropped term, a
+wrong sign, index or mask, a missed rounding step), compiled into a temporary library and
+run against every pin in a child process (a mutant may also crash, which counts as caught).
+This shows the pins are sensitive enough that a mistake of that kind cannot pass.
+"""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+MUTANTS = {
+    "mean_instead_of_lse": [("return m + std::log(s);",
+                             "double mu = 0; for (double v : z) mu += v; return std::log((double)z.size()) + mu / z.size();")],
+    "leaf_causal_mask_dropped": [("if (!R.causal || c <= R.t) z.push_back(R.scale * dot_key(R, h, c));",
+                                  "z.push_back(R.scale * dot_key(R, h, c));")],
+    "level_mean_divides_by_g": [("      double cnt = (double)(r1 - r0);\n      for (int e = 0; e < d; ++e) Pbg[(off[l] + i) * d + e]",
+                                 "      double cnt = (double)g;\n      for (int e = 0; e < d; ++e) Pbg[(off[l] + i) * d + e]")],
+    "ragged_leaf_divides_by_C": [("    double cnt = (double)(c1 - c0);\n    for (int e = 0; e < d; ++e) Pbg[(off[1] + j) * d + e]",
+                                  "    double cnt = (double)C;\n    for (int e = 0; e < d; ++e) Pbg[(off[1] + j) * d + e]")],
+    "ties_to_higher_index": [("return ids[a] < ids[b];", "return ids[a] > ids[b];")],
+    "topk_ascending": [("if (sc[a] != sc[b]) return sc[a] > sc[b];", "if (sc[a] != sc[b]) return sc[a] < sc[b];")],
+    "own_block_not_forced": [("if (out.cand[s] >= 0 && out.cand[s] != own) {", "if (out.cand[s] >= 0) {"),
+                             ("fin = topk(ids, sc, R.causal ? R.K - 1 : R.K, &gap);", "fin = topk(ids, sc, R.K, &gap);"),
+                             ("  if (R.causal) fin.push_back(own);\n", "")],
+    "children_off_by_one": [("    for (long long r = R.g * p; r < R.g * p + R.g; ++r)\n      if (eligible(R, l, r)) out.push_back(r);",
+                             "    for (long long r = R.g * p + 1; r < R.g * p + R.g + 1; ++r)\n      if (eligible(R, l, r)) out.push_back(r);")],
+    "attention_scale_missing": [("      s.push_back(scale * z);", "      s.push_back(z);")],
+    "eligibility_by_last_key": [("return i * ipow(R.g, l - 1) * R.C <= R.t;",
+                                 "return ((i + 1) * ipow(R.g, l - 1) * R.C - 1) <= R.t;")],
+    "decode_skips_ancestors": [("      for (int l = 2; l <= lv.L; ++l) {\n        node /= g;",
+                                "      for (int l = 2; l <= 1; ++l) {\n        node /= g;")],
+    "attention_ignores_causal": [("      if (causal && c > t) continue;\n", "")],
+    "double_rounding_to_bf16": [("if (std::isfinite(f) && (double)f != x) {", "if (false) {")],
+    "leaf_scored_by_summary": [("if (!R.causal || c <= R.t) z.push_back(R.scale * dot_key(R, h, c));",
+                                "if (!R.causal || c <= R.t) z.push_back(R.scale * dot_node(R, h, 1, j));")],
+    "internal_scored_by_own_summary": [("if (eligible(R, l - 1, r)) z.push_back(R.scale * dot_node(R, h, l - 1, r));",
+                                        "if (eligible(R, l - 1, r)) z.push_back(R.scale * dot_node(R, h, l, i));")],
+    "walk_never_prunes": [("    if ((int)A.size() > R.K) {\n      std::vector<double> sc;\n      for (long long i : A) sc.push_back(score_internal(R, l, i));\n      double gap;",
+                           "    if (false) {\n      std::vector<double> sc;\n      for (long long i : A) sc.push_back(score_internal(R, l, i));\n      double gap;")],
+}
+
+# "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
+MUTANTS["head_sum_drops_heads"] = [
+    ("  double u = 0;\n  for (int h = 0; h < R.GQ; ++h) {\n    std::vector<double> z;\n    for (long long r",
+     "  double u = 0;\n  for (int h = 0; h < 1; ++h) {\n    std::vector<double> z;\n    for (long long r"),
+    ("  double u = 0;\n  for (int h = 0; h < R.GQ; ++h) {\n    std::vector<double> z;\n    for (long long c",
+     "  double u = 0;\n  for (int h = 0; h < 1; ++h) {\n    std::vector<double> z;\n    for (long long c"),
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+RUNNER = """
+import sys
+sys.path[:0] = [{root!r}, {here!r}]
+import oracle, pins
+o = oracle.Oracle({lib!r})
+failed = []
+for pin in pins.ALL_PINS:
+    try:
+        pin(o)
+    except Exception as e:
+        failed.append(pin.__name__)
+print("FAILED_PINS", ",".join(failed))
+"""
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, mutant_dir):
+    src = open(oracle.SRC).read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+        src = src.replace(old, new)
+    path = os.path.join(mutant_dir, f"{name}.cpp")
+    with open(path, "w") as f:
+        f.write(src)
+    lib = oracle.compile_source(path, os.path.join(mutant_dir, f"lib{name}.so"))
+    code = RUNNER.format(root=os.path.dirname(HERE), here=HERE, lib=lib)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    failed = [ln.split(" ", 1)[1] for ln in res.stdout.splitlines() if ln.startswith("FAILED_PINS ")]
+    caught = res.returncode != 0 or (failed and failed[0].strip() != "")
+    assert caught, f"no pin catches the planted mistake {name}: {res.stdout[-500:]}"
