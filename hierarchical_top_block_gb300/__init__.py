@@ -1,0 +1,235 @@
+"""GB300 (sm_103a) log-linear block-sparse attention with pyramid-LSE block selection.
+
+Python binding of the C ABI in ``include/pisa.h`` (library ``libpisa_gb300.so``).  The
+functions carry the C names and only marshal arguments: every step of the computation
+runs in the library's CUDA kernels.  PyTorch supplies device memory and the current
+stream.  If the library is missing, every call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpisa_gb300.so")
+
+PISA_OK = 0
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device wait timed out",
+           5: "bad block index", 6: "workspace too small"}
+
+
+class PisaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class pisa_params(ct.Structure):
+    _fields_ = [("C", ct.c_int), ("g", ct.c_int), ("K", ct.c_int), ("causal", ct.c_int), ("scale", ct.c_float)]
+
+
+class pisa_shape(ct.Structure):
+    _fields_ = [("B", ct.c_int), ("N", ct.c_int), ("H_q", ct.c_int), ("H_kv", ct.c_int), ("d", ct.c_int),
+                ("N_cap", ct.c_int)]
+
+
+_lib = None
+_P = ct.c_void_p
+
+
+def lib() -> ct.CDLL:
+    """Load the library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with hierarchical_top_block_gb300.build.build()")
+        L = ct.CDLL(LIB_PATH)
+        L.pisa_pyramid_levels.restype = ct.c_int
+        L.pisa_pyramid_levels.argtypes = [ct.c_longlong, ct.c_int, ct.c_int]
+        L.pisa_pyramid_nodes.restype = ct.c_longlong
+        L.pisa_pyramid_nodes.argtypes = [ct.c_longlong, ct.c_int, ct.c_int]
+        L.pisa_select_workspace_bytes.restype = ct.c_size_t
+        L.pisa_select_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_prefill_host_workspace_bytes.restype = ct.c_size_t
+        L.pisa_prefill_host_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_build_pyramid.restype = ct.c_int
+        L.pisa_build_pyramid.argtypes = [_P, _P, pisa_shape, pisa_params, _P]
+        L.pisa_select_prefill.restype = ct.c_int
+        L.pisa_select_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, ct.c_size_t, pisa_shape, pisa_params, _P]
+        L.pisa_sparse_attn_prefill.restype = ct.c_int
+        L.pisa_sparse_attn_prefill.argtypes = [_P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
+        L.pisa_prefill_host.restype = ct.c_int
+        L.pisa_prefill_host.argtypes = [_P, _P, _P, _P, _P, _P, _P, ct.c_size_t, pisa_shape, pisa_params, _P]
+        L.pisa_decode_step.restype = ct.c_int
+        L.pisa_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
+        L.pisa_status_string.restype = ct.c_char_p
+        L.pisa_status_string.argtypes = [ct.c_int]
+        L.pisa_get_last_device_error.restype = ct.c_int
+        L.pisa_get_last_device_error.argtypes = [_P]
+        L.pisa_version.restype = ct.c_char_p
+        L.pisa_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != PISA_OK:
+        raise PisaError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ct.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ct.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _bf16(t, name):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+
+
+def make_params(K: int, causal: bool = True, scale: float = 0.0, C: int = 64, g: int = 2) -> pisa_params:
+    return pisa_params(C, g, K, 1 if causal else 0, float(scale))
+
+
+def make_shape(B, N, H_q, H_kv, d, N_cap=0) -> pisa_shape:
+    return pisa_shape(B, N, H_q, H_kv, d, N_cap)
+
+
+# ---- geometry -------------------------------------------------------------------------
+def pisa_pyramid_levels(N: int, C: int = 64, g: int = 2) -> int:
+    return lib().pisa_pyramid_levels(N, C, g)
+
+
+def pisa_pyramid_nodes(N: int, C: int = 64, g: int = 2) -> int:
+    return int(lib().pisa_pyramid_nodes(N, C, g))
+
+
+def pisa_select_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
+    return int(lib().pisa_select_workspace_bytes(shape, params))
+
+
+def pisa_prefill_host_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
+    return int(lib().pisa_prefill_host_workspace_bytes(shape, params))
+
+
+def pisa_status_string(status: int) -> str:
+    return lib().pisa_status_string(status).decode()
+
+
+def pisa_version() -> str:
+    return lib().pisa_version().decode()
+
+
+def pisa_get_last_device_error(device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    return lib().pisa_get_last_device_error(ct.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+
+
+# ---- step 1 -----------------------------------------------------------------------------
+def pisa_build_pyramid(K: torch.Tensor, N: int | None = None, P: torch.Tensor | None = None) -> torch.Tensor:
+    """K [B, H_kv, N_cap, d] bf16 -> P [B, H_kv, nodes(N_cap), d]; levels built from the first N rows."""
+    _bf16(K, "K")
+    B, H_kv, N_cap, d = K.shape
+    N = N_cap if N is None else N
+    nodes = pisa_pyramid_nodes(N_cap)
+    if P is None:
+        P = torch.empty(B, H_kv, nodes, d, dtype=torch.bfloat16, device=K.device)
+    _bf16(P, "P")
+    shape = make_shape(B, N, H_kv, H_kv, d, N_cap)
+    _check(lib().pisa_build_pyramid(_ptr(K), _ptr(P), shape, make_params(1), _stream(K)), "pisa_build_pyramid")
+    return P
+
+
+# ---- step 2 -----------------------------------------------------------------------------
+def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float = 0.0, want_scores: bool = False,
+                        want_s2: bool = False, ws: torch.Tensor | None = None, idx: torch.Tensor | None = None):
+    """Returns idx [B, H_kv, N, K_sel] int32 (and leaf_score, s2 if asked)."""
+    for t, n in ((Q, "Q"), (K, "K"), (P, "P")):
+        _bf16(t, n)
+    B, N, H_q, d = Q.shape
+    H_kv = K.shape[1]
+    shape = make_shape(B, N, H_q, H_kv, d, N)
+    params = make_params(K_sel, causal, scale)
+    need = pisa_select_workspace_bytes(shape, params)
+    if need == 0 and B * N > 0:
+        raise PisaError(2, "pisa_select_prefill: unsupported shape or parameters")
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    if idx is None:
+        idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
+    score = torch.empty(B, H_kv, N, 2 * K_sel, dtype=torch.float32, device=Q.device) if want_scores else None
+    s2 = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device) if want_s2 else None
+    _check(lib().pisa_select_prefill(_ptr(Q), _ptr(K), _ptr(P), _ptr(idx), _ptr(score), _ptr(s2), _ptr(ws),
+                                     ws.numel(), shape, params, _stream(Q)), "pisa_select_prefill")
+    out = [idx]
+    if want_scores:
+        out.append(score)
+    if want_s2:
+        out.append(s2)
+    return out[0] if len(out) == 1 else tuple(out)
+
+
+# ---- step 4 -----------------------------------------------------------------------------
+def pisa_sparse_attn_prefill(Q, K, V, idx, causal: bool = True, scale: float = 0.0, O=None, LSE=None,
+                             want_lse: bool = True):
+    """Returns O [B, N, H_q, d] bf16 and LSE [B, H_q, N] fp32 (None if not wanted)."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _bf16(t, n)
+    if idx.dtype != torch.int32 or not idx.is_contiguous():
+        raise ValueError("idx must be contiguous int32")
+    B, N, H_q, d = Q.shape
+    H_kv = K.shape[1]
+    if O is None:
+        O = torch.empty_like(Q)
+    if want_lse and LSE is None:
+        LSE = torch.empty(B, H_q, N, dtype=torch.float32, device=Q.device)
+    shape = make_shape(B, N, H_q, H_kv, d, K.shape[2])
+    params = make_params(idx.shape[-1], causal, scale)
+    _check(lib().pisa_sparse_attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(O), _ptr(LSE if want_lse else None),
+                                          shape, params, _stream(Q)), "pisa_sparse_attn_prefill")
+    return O, (LSE if want_lse else None)
+
+
+def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, scale: float = 0.0, dev_ws=None,
+                      O_host=None, LSE_host=None, idx_host=None, device=None):
+    """Whole prefill from host (ideally pinned) tensors; copies happen inside the call."""
+    B, N, H_q, d = Q_host.shape
+    H_kv = K_host.shape[1]
+    shape = make_shape(B, N, H_q, H_kv, d, N)
+    params = make_params(K_sel, causal, scale)
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    need = pisa_prefill_host_workspace_bytes(shape, params)
+    if dev_ws is None or dev_ws.numel() < need:
+        dev_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    if O_host is None:
+        O_host = torch.empty_like(Q_host)
+    stream = ct.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    _check(lib().pisa_prefill_host(_ptr(Q_host), _ptr(K_host), _ptr(V_host), _ptr(O_host), _ptr(LSE_host),
+                                   _ptr(idx_host), _ptr(dev_ws), dev_ws.numel(), shape, params, stream),
+           "pisa_prefill_host")
+    return O_host
+
+
+# ---- step 3 -----------------------------------------------------------------------------
+def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.0, o=None, lse=None, idx_out=None):
+    """One decode step for every sequence; caches and seq_len are updated in place."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (Kc, "Kc"), (Vc, "Vc"), (Pc, "Pc")):
+        _bf16(t, n)
+    if seq_len.dtype != torch.int32 or not seq_len.is_cuda:
+        raise ValueError("seq_len must be an int32 CUDA tensor")
+    B, H_q, d = q.shape
+    H_kv = k.shape[1]
+    N_cap = Kc.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    shape = make_shape(B, 0, H_q, H_kv, d, N_cap)
+    _check(lib().pisa_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), _ptr(o),
+                                  _ptr(lse), _ptr(idx_out), shape, make_params(K_sel, True, scale), _stream(q)),
+           "pisa_decode_step")
+    return o

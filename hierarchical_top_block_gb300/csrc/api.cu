@@ -1,0 +1,395 @@
+// C ABI of the PISA library (declared in include/pisa.h): argument checks, workspace
+// carving, per-device state and the launch sequence of each entry point.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/pisa.h"
+#include "kernels.cuh"
+
+namespace pisa {
+
+// One error word per device: kernels OR ERR_* bits into it; the host reads and clears it.
+static __device__ uint32_t g_device_error;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* err = nullptr;  // device address of g_device_error on this device
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[MAX_DEVICES];
+
+// Per-device set-up, done once per device with that device current.
+pisa_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PISA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PISA_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return PISA_ERR_CUDA;
+    st.err = static_cast<uint32_t*>(p);
+    st.ready = true;
+  }
+  *out = &st;
+  return PISA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// level sizes for n tokens (C = 64, g = 2); offsets from the capacity layout
+Geometry make_geometry(long long n, long long n_cap) {
+  Geometry g{};
+  g.L = 0;
+  long long m = (n + 63) / 64;
+  if (n > 0) {
+    g.M[1] = (int)m;
+    g.L = 1;
+    while (m > 1 && g.L < MAX_LEVELS) {
+      m = (m + 1) / 2;
+      g.M[++g.L] = (int)m;
+    }
+  }
+  long long mc = (n_cap + 63) / 64, off = 0;
+  int l = 1;
+  if (n_cap > 0) {
+    while (true) {
+      g.off[l] = off;
+      off += mc;
+      if (mc <= 1 || l >= MAX_LEVELS) break;
+      mc = (mc + 1) / 2;
+      ++l;
+    }
+  }
+  g.nodes = off;
+  return g;
+}
+
+pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p) {
+  if (s.B < 0 || s.N < 0 || s.H_q <= 0 || s.H_kv <= 0 || s.d <= 0) return PISA_ERR_INVALID_ARG;
+  if (pr.C != 64 || pr.g != 2 || (s.d != 64 && s.d != 128)) return PISA_ERR_UNSUPPORTED;
+  if (pr.K < 1 || pr.K > 16) return PISA_ERR_UNSUPPORTED;
+  if (pr.causal != 0 && pr.causal != 1) return PISA_ERR_INVALID_ARG;
+  if (s.H_q % s.H_kv != 0) return PISA_ERR_INVALID_ARG;
+  const int gq = s.H_q / s.H_kv;
+  if (gq != 1 && gq != 2 && gq != 4 && gq != 8 && gq != 16) return PISA_ERR_UNSUPPORTED;
+  const long long ncap = s.N_cap == 0 ? s.N : s.N_cap;
+  if (ncap < s.N) return PISA_ERR_INVALID_ARG;
+  if (ncap >= (1LL << 25)) return PISA_ERR_UNSUPPORTED;                        // entry packing (t << 6)
+  if ((long long)s.B * ncap * s.H_q >= (1LL << 31)) return PISA_ERR_UNSUPPORTED;  // TMA coordinates
+  if (!(pr.scale == pr.scale)) return PISA_ERR_INVALID_ARG;
+  p->B = s.B;
+  p->N = s.N;
+  p->N_cap = (int)ncap;
+  p->H_q = s.H_q;
+  p->H_kv = s.H_kv;
+  p->d = s.d;
+  p->C = pr.C;
+  p->g = pr.g;
+  p->K = pr.K;
+  p->causal = pr.causal;
+  p->scale = pr.scale > 0.f ? pr.scale : 1.0f / sqrtf((float)s.d);
+  p->GQ = gq;
+  return PISA_OK;
+}
+
+struct SelectLayout {
+  size_t s2, score, counts, cursor, offsets, tile_off, block_sums, entries, tiles, totals, total_bytes;
+  ClusterBuffers cb;  // sizes only; pointers filled by carve()
+};
+
+SelectLayout select_layout(const Problem& p) {
+  SelectLayout L{};
+  const long long total = (long long)p.B * p.H_kv * p.N;
+  const Geometry g = make_geometry(p.N, p.N);
+  const int rpq = p.GQ < 8 ? 8 : p.GQ;
+  ClusterBuffers& cb = L.cb;
+  cb.qt = 128 / rpq;
+  long long win = (32LL << 20) / ((long long)p.GQ * p.d * 2);
+  win = win / 64 * 64;
+  if (win < 64) win = 64;
+  if (win > p.N) win = p.N > 0 ? p.N : 1;
+  cb.win = (int)win;
+  cb.nwin = p.N > 0 ? (int)((p.N + win - 1) / win) : 1;
+  cb.M2 = g.L >= 2 ? g.M[2] : 1;
+  cb.nkeys = (long long)p.B * p.H_kv * cb.nwin * cb.M2;
+  cb.nblocks = (int)((cb.nkeys + 4095) / 4096);
+  if (cb.nblocks < 1) cb.nblocks = 1;
+  cb.max_tiles = total * p.K / cb.qt + cb.nkeys + 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = round_up(o + bytes, 256);
+    return at;
+  };
+  L.s2 = take(sizeof(int32_t) * total * p.K);
+  L.score = take(sizeof(float) * total * 2 * p.K);
+  L.counts = take(sizeof(int32_t) * cb.nkeys);
+  L.cursor = take(sizeof(int32_t) * cb.nkeys);
+  L.offsets = take(sizeof(int32_t) * cb.nkeys);
+  L.tile_off = take(sizeof(int32_t) * cb.nkeys);
+  L.block_sums = take(sizeof(int32_t) * 2 * cb.nblocks);
+  L.entries = take(sizeof(int32_t) * total * p.K);
+  L.tiles = take(sizeof(int4) * cb.max_tiles);
+  L.totals = take(sizeof(int32_t) * 4);
+  L.total_bytes = o;
+  return L;
+}
+
+pisa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA; }
+
+pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx, float* leaf_score,
+                       int32_t* s2, void* ws, size_t ws_bytes, const Problem& p, DeviceState* st, cudaStream_t s) {
+  SelectLayout L = select_layout(p);
+  if (ws_bytes < L.total_bytes) return PISA_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* S2 = s2 ? s2 : reinterpret_cast<int32_t*>(w + L.s2);
+  float* score = leaf_score ? leaf_score : reinterpret_cast<float*>(w + L.score);
+  ClusterBuffers cb = L.cb;
+  cb.counts = reinterpret_cast<int32_t*>(w + L.counts);
+  cb.cursor = reinterpret_cast<int32_t*>(w + L.cursor);
+  cb.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  cb.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
+  cb.block_sums = reinterpret_cast<int32_t*>(w + L.block_sums);
+  cb.entries = reinterpret_cast<int32_t*>(w + L.entries);
+  cb.tiles = reinterpret_cast<int4*>(w + L.tiles);
+  cb.totals = reinterpret_cast<int32_t*>(w + L.totals);
+  const Geometry geo = make_geometry(p.N, p.N);
+  cudaError_t e;
+  if ((e = launch_stage1(Q, P, S2, p, geo, st->num_sms, st->err, s)) != cudaSuccess) return PISA_ERR_CUDA;
+  if ((e = launch_cluster(S2, cb, p, s)) != cudaSuccess) return PISA_ERR_CUDA;
+  if ((e = launch_leaf_lse(Q, K, cb, score, p, geo, st->num_sms, st->err, s)) != cudaSuccess) return PISA_ERR_CUDA;
+  if ((e = launch_topk(S2, score, idx, p, geo, s)) != cudaSuccess) return PISA_ERR_CUDA;
+  return PISA_OK;
+}
+
+}  // namespace
+
+bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace pisa
+
+using namespace pisa;
+
+extern "C" {
+
+int pisa_pyramid_levels(long long N, int C, int g) {
+  if (N <= 0 || C <= 0 || g < 2) return 0;
+  long long m = (N + C - 1) / C;
+  int L = 1;
+  while (m > 1) {
+    m = (m + g - 1) / g;
+    ++L;
+  }
+  return L;
+}
+
+long long pisa_pyramid_nodes(long long N, int C, int g) {
+  if (N <= 0 || C <= 0 || g < 2) return 0;
+  long long m = (N + C - 1) / C, s = m;
+  while (m > 1) {
+    m = (m + g - 1) / g;
+    s += m;
+  }
+  return s;
+}
+
+size_t pisa_select_workspace_bytes(pisa_shape shape, pisa_params params) {
+  Problem p;
+  if (check_params(shape, params, &p) != PISA_OK) return 0;
+  return select_layout(p).total_bytes;
+}
+
+pisa_status pisa_build_pyramid(const uint16_t* K, uint16_t* P, pisa_shape shape, pisa_params params,
+                               pisa_stream stream) {
+  Problem p;
+  pisa_status rc = check_params(shape, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.B == 0 || p.N == 0) return PISA_OK;
+  if (!K || !P || !aligned16(K) || !aligned16(P)) return PISA_ERR_INVALID_ARG;
+  const Geometry geo = make_geometry(p.N, p.N_cap);
+  return cuda_status(launch_pyramid(K, P, p, geo, static_cast<cudaStream_t>(stream)));
+}
+
+pisa_status pisa_select_prefill(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx,
+                                float* leaf_score, int32_t* s2, void* ws, size_t ws_bytes, pisa_shape shape,
+                                pisa_params params, pisa_stream stream) {
+  Problem p;
+  pisa_status rc = check_params(shape, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.N_cap != p.N) return PISA_ERR_INVALID_ARG;
+  if (p.B == 0 || p.N == 0) return PISA_OK;
+  if (!Q || !K || !P || !idx || !ws) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(P) || (reinterpret_cast<uintptr_t>(ws) & 255u)) return PISA_ERR_INVALID_ARG;
+  if ((leaf_score && !aligned16(leaf_score)) || (s2 && !aligned16(s2)) || !aligned16(idx)) return PISA_ERR_INVALID_ARG;
+  DeviceState* st;
+  if ((rc = device_state(&st)) != PISA_OK) return rc;
+  return run_select(Q, K, P, idx, leaf_score, s2, ws, ws_bytes, p, st, static_cast<cudaStream_t>(stream));
+}
+
+pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                                     uint16_t* O, float* LSE, pisa_shape shape, pisa_params params,
+                                     pisa_stream stream) {
+  Problem p;
+  pisa_status rc = check_params(shape, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.B == 0 || p.N == 0) return PISA_OK;
+  if (!Q || !K || !V || !idx || !O) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(idx)) return PISA_ERR_INVALID_ARG;
+  DeviceState* st;
+  if ((rc = device_state(&st)) != PISA_OK) return rc;
+  return cuda_status(launch_sparse_attn(Q, K, V, idx, O, LSE, p, st->num_sms, st->err, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params) {
+  Problem p;
+  if (check_params(shape, params, &p) != PISA_OK) return 0;
+  const size_t q = (size_t)p.B * p.N * p.H_q * p.d * 2;
+  const size_t kv = (size_t)p.B * p.H_kv * p.N * p.d * 2;
+  const size_t pyr = (size_t)p.B * p.H_kv * pisa_pyramid_nodes(p.N, 64, 2) * p.d * 2;
+  const size_t idx = (size_t)p.B * p.H_kv * p.N * p.K * 4;
+  const size_t lse = (size_t)p.B * p.H_q * p.N * 4;
+  return round_up(q, 256) * 2 + round_up(kv, 256) * 2 + round_up(pyr, 256) + round_up(idx, 256) + round_up(lse, 256) +
+         select_layout(p).total_bytes;
+}
+
+pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, const uint16_t* V_host,
+                              uint16_t* O_host, float* LSE_host, int32_t* idx_host, void* dev_ws, size_t ws_bytes,
+                              pisa_shape shape, pisa_params params, pisa_stream stream) {
+  Problem p;
+  pisa_status rc = check_params(shape, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.N_cap != p.N) return PISA_ERR_INVALID_ARG;
+  if (p.B == 0 || p.N == 0) return PISA_OK;
+  if (!Q_host || !K_host || !V_host || !O_host || !dev_ws) return PISA_ERR_INVALID_ARG;
+  if (ws_bytes < pisa_prefill_host_workspace_bytes(shape, params)) return PISA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(dev_ws) & 255u) return PISA_ERR_INVALID_ARG;
+  DeviceState* st;
+  if ((rc = device_state(&st)) != PISA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t q = (size_t)p.B * p.N * p.H_q * p.d * 2;
+  const size_t kv = (size_t)p.B * p.H_kv * p.N * p.d * 2;
+  const size_t pyr = (size_t)p.B * p.H_kv * pisa_pyramid_nodes(p.N, 64, 2) * p.d * 2;
+  const size_t idxb = (size_t)p.B * p.H_kv * p.N * p.K * 4;
+  const size_t lseb = (size_t)p.B * p.H_q * p.N * 4;
+  uint8_t* w = static_cast<uint8_t*>(dev_ws);
+  uint16_t* dQ = reinterpret_cast<uint16_t*>(w);
+  w += round_up(q, 256);
+  uint16_t* dO = reinterpret_cast<uint16_t*>(w);
+  w += round_up(q, 256);
+  uint16_t* dK = reinterpret_cast<uint16_t*>(w);
+  w += round_up(kv, 256);
+  uint16_t* dV = reinterpret_cast<uint16_t*>(w);
+  w += round_up(kv, 256);
+  uint16_t* dP = reinterpret_cast<uint16_t*>(w);
+  w += round_up(pyr, 256);
+  int32_t* dIdx = reinterpret_cast<int32_t*>(w);
+  w += round_up(idxb, 256);
+  float* dL = reinterpret_cast<float*>(w);
+  w += round_up(lseb, 256);
+  const size_t sel_bytes = select_layout(p).total_bytes;
+  if (cudaMemcpyAsync(dQ, Q_host, q, cudaMemcpyHostToDevice, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, s) != cudaSuccess) return PISA_ERR_CUDA;
+  const Geometry geo = make_geometry(p.N, p.N);
+  if (launch_pyramid(dK, dP, p, geo, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, p, st, s)) != PISA_OK) return rc;
+  if (launch_sparse_attn(dQ, dK, dV, dIdx, dO, dL, p, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaMemcpyAsync(O_host, dO, q, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (LSE_host && cudaMemcpyAsync(LSE_host, dL, lseb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (idx_host && cudaMemcpyAsync(idx_host, dIdx, idxb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
+                             uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
+                             pisa_shape shape, pisa_params params, pisa_stream stream) {
+  pisa_shape sh = shape;
+  if (sh.N_cap <= 0) return PISA_ERR_INVALID_ARG;
+  sh.N = 0;
+  Problem p;
+  pisa_status rc = check_params(sh, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.causal != 1) return PISA_ERR_UNSUPPORTED;
+  if (p.B == 0) return PISA_OK;
+  if (!q || !k || !v || !Kc || !Vc || !Pc || !seq_len || !o) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(Pc) ||
+      !aligned16(o))
+    return PISA_ERR_INVALID_ARG;
+  DeviceState* st;
+  if ((rc = device_state(&st)) != PISA_OK) return rc;
+  const Geometry geo_cap = make_geometry(p.N_cap, p.N_cap);
+  return cuda_status(
+      launch_decode(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, st->err, static_cast<cudaStream_t>(stream)));
+}
+
+const char* pisa_status_string(pisa_status status) {
+  switch (status) {
+    case PISA_OK: return "ok";
+    case PISA_ERR_INVALID_ARG: return "invalid argument";
+    case PISA_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case PISA_ERR_CUDA: return "CUDA runtime error";
+    case PISA_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case PISA_ERR_BAD_INDEX: return "a selected block index was out of range";
+    case PISA_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+pisa_status pisa_get_last_device_error(pisa_stream stream) {
+  DeviceState* st;
+  pisa_status rc = device_state(&st);
+  if (rc != PISA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0, zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&word, g_device_error, sizeof(word), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PISA_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PISA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (word & ERR_TIMEOUT) return PISA_ERR_TIMEOUT;
+  if (word & ERR_BAD_INDEX) return PISA_ERR_BAD_INDEX;
+  return PISA_OK;
+}
+
+const char* pisa_version(void) { return "pisa-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

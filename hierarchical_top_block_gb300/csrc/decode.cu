@@ -1,0 +1,496 @@
+// Step 3 of the method (summary page of "Block Sparse Attention with Log-Linear
+// Complexity", section "Method step details", step 3): one decode step per sequence in a
+// single fused kernel.  The pyramid cache is updated only along the new token's path
+// (its leaf from the raw keys, then every ancestor from its children, so the cache equals
+// a fresh build bit for bit), one kernel walks every level down to the leaves (eq. 21
+// scores, eq. 22 head sum, SelectK), scores the leaf candidates exactly, takes the final
+// top-K with the own block, and attends over the selected blocks (step 4).
+//
+// One CTA (4 warps) per (sequence, KV head).  The level walk runs in warp 0 with the
+// query group in mma.sync fragments and child summaries loaded straight into registers
+// (d permuted identically in both operands); the leaf scoring and the attention split
+// the blocks over the 4 warps; V blocks are staged in shared memory for ldmatrix.trans;
+// the 4 partial softmax states are merged in shared memory.  seq_len is advanced by a
+// second, one-thread-per-sequence kernel so that no CTA reads a length another changed.
+#include "kernels.cuh"
+
+namespace pisa {
+namespace {
+
+constexpr int WARPS = 4;
+constexpr int THREADS = 32 * WARPS;
+
+
+__device__ __forceinline__ float lse2_pair(float a, float b) {
+  const float m = fmaxf(a, b), n = fminf(a, b);
+  return m + fast_log2(1.0f + fast_exp2(n - m));
+}
+
+struct DecodeParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* Kc;
+  uint16_t* Vc;
+  uint16_t* Pc;
+  const int32_t* seq_len;
+  uint16_t* o;
+  float* lse;
+  int32_t* idx_out;
+  int H_q, H_kv, GQ, Ksel, N_cap;
+  float sl2;
+  long long nodes;          // P rows per (b, h_kv) in the capacity layout
+  long long off[MAX_LEVELS + 1];
+};
+
+// level sizes for n tokens (C = 64, g = 2)
+__device__ __forceinline__ int level_size(long long n, int l) {
+  long long m = (n + 63) >> 6;
+  for (int i = 1; i < l; ++i) m = (m + 1) >> 1;
+  return (int)m;
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_t* err) {
+  constexpr int NCH = D / 32;
+  constexpr int NDT = D / 8;
+  __shared__ int lst[32];
+  __shared__ int cand_leaf[32];
+  __shared__ float cand_score[32];
+  __shared__ int ncand_s, nsel_s;
+  __shared__ int sel[32];
+  __shared__ float part_m[WARPS][16], part_l[WARPS][16];
+  extern __shared__ __align__(1024) uint8_t vbuf_raw[];
+  uint8_t* vbuf = (uint8_t*)(((uintptr_t)vbuf_raw + 1023) & ~(uintptr_t)1023);  // [WARPS][64 x D bf16]
+
+  const int bh = blockIdx.x;
+  const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = lane >> 2, q = lane & 3;
+  const long long T = p.seq_len[b];
+  const long long n = T + 1;
+  uint16_t* Kb = p.Kc + (size_t)bh * p.N_cap * D;
+  uint16_t* Vb = p.Vc + (size_t)bh * p.N_cap * D;
+  uint16_t* Pb = p.Pc + (size_t)bh * p.nodes * D;
+
+  // ---- append k, v and update the pyramid path of the new token ----
+  if (tid < D) {
+    Kb[(size_t)T * D + tid] = p.k[(size_t)bh * D + tid];
+    Vb[(size_t)T * D + tid] = p.v[(size_t)bh * D + tid];
+  }
+  __syncthreads();
+  int L = 1;
+  while (level_size(n, L) > 1) ++L;
+  if (tid < D) {
+    const long long leaf = T >> 6;
+    float hi = 0.f, lo = 0.f;
+    for (long long c = leaf * 64; c <= T; ++c) {
+      float s, e;
+      two_sum(hi, bf16_to_f32(Kb[(size_t)c * D + tid]), s, e);
+      hi = s;
+      lo += e;
+    }
+    const double cnt = (double)(T - leaf * 64 + 1);
+    Pb[(size_t)(p.off[1] + leaf) * D + tid] = f64_to_bf16_rne(((double)hi + (double)lo) / cnt);
+    long long node = leaf;
+    for (int l = 2; l <= L; ++l) {
+      node >>= 1;
+      const long long c0 = 2 * node, c1 = min(2 * node + 2, (long long)level_size(n, l - 1));
+      double s = 0.0;
+      for (long long c = c0; c < c1; ++c) s += (double)bf16_to_f32(Pb[(size_t)(p.off[l - 1] + c) * D + tid]);
+      Pb[(size_t)(p.off[l] + node) * D + tid] = f64_to_bf16_rne(s / (double)(c1 - c0));
+    }
+  }
+  __syncthreads();
+
+  // query fragments, d permuted: chunk j of lane q holds d in [32j + 8q, 32j + 8q + 8)
+  uint4 qa[NCH], qb[NCH];
+  const uint16_t* qrow = p.q + ((size_t)b * p.H_q + (size_t)hk * p.GQ) * D;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    qa[j] = r < p.GQ ? ldg16(qrow + (size_t)r * D + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
+    qb[j] = r + 8 < p.GQ ? ldg16(qrow + (size_t)(r + 8) * D + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
+  }
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  // ---- level walk (warp 0) ----
+  if (warp == 0) {
+    int surv = lane == 0 ? 0 : -1, ns = 1;
+    for (int l = L - 1; l >= 2; --l) {
+      const int Ml = level_size(n, l);
+      const long long span = 64LL << (l - 1);
+      const int c0 = 2 * surv, c1 = 2 * surv + 1;
+      const bool e0 = lane < ns && c0 < Ml && (long long)c0 * span <= T;
+      const bool e1 = lane < ns && c1 < Ml && (long long)c1 * span <= T;
+      const unsigned b0 = __ballot_sync(0xffffffffu, e0), b1 = __ballot_sync(0xffffffffu, e1);
+      const int pos = __popc(b0 & lt_mask) + __popc(b1 & lt_mask);
+      const int nc = __popc(b0) + __popc(b1);
+      if (e0) lst[pos] = c0;
+      if (e1) lst[pos + (e0 ? 1 : 0)] = c1;
+      __syncwarp();
+      const int cand = lane < nc ? lst[lane] : -1;
+      __syncwarp();
+      if (nc <= p.Ksel) {
+        surv = cand;
+        ns = nc;
+        continue;
+      }
+      const long long cspan = 64LL << (l - 2);
+      const int Mc = level_size(n, l - 1);
+      float u[8];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int ci = 4 * nt + (r >> 1);
+        const int cnode = __shfl_sync(0xffffffffu, cand, ci);
+        const int child = 2 * cnode + (r & 1);
+        const bool valid = ci < nc && child < Mc && (long long)child * cspan <= T;
+        const uint16_t* prow = Pb + (size_t)(p.off[l - 1] + (valid ? child : 0)) * D;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const uint4 kv = valid ? ldg16(prow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
+          mma_bf16_16816(acc, qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
+          mma_bf16_16816(acc, qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+        }
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        const bool v0 = (vm >> (8 * q)) & 1u, v1 = (vm >> (8 * q + 4)) & 1u;
+        float part = 0.f;
+        if (v0) {
+          const float x1 = v1 ? acc[1] * p.sl2 : NEG_INF, y1 = v1 ? acc[3] * p.sl2 : NEG_INF;
+          if (r < p.GQ) part += lse2_pair(acc[0] * p.sl2, x1);
+          if (r + 8 < p.GQ) part += lse2_pair(acc[2] * p.sl2, y1);
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        part += __shfl_xor_sync(0xffffffffu, part, 8);
+        part += __shfl_xor_sync(0xffffffffu, part, 16);
+        u[nt] = v0 ? part : NEG_INF;
+      }
+      float my = NEG_INF;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const float v = __shfl_sync(0xffffffffu, u[nt], lane & 3);
+        if ((lane >> 2) == nt) my = v;
+      }
+      if (lane >= nc) my = NEG_INF;
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) {
+        const float uj = __shfl_sync(0xffffffffu, my, j);
+        rank += (uj > my || (uj == my && j < lane)) ? 1 : 0;
+      }
+      const bool keep = lane < nc && rank < p.Ksel;
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      if (keep) lst[__popc(km & lt_mask)] = cand;
+      __syncwarp();
+      ns = __popc(km);
+      surv = lane < ns ? lst[lane] : -1;
+      __syncwarp();
+    }
+    // leaf candidates: eligible children of the level-2 survivors, slot 2i + c
+    const int M1 = level_size(n, 1);
+    const int node = __shfl_sync(0xffffffffu, surv, (lane >> 1) & 31);
+    if (lane < 2 * p.Ksel) {
+      const int j = 2 * node + (lane & 1);
+      cand_leaf[lane] = (node >= 0 && j < M1 && (long long)j * 64 <= T) ? j : -1;
+    }
+    if (lane == 0) ncand_s = 2 * p.Ksel;
+  }
+  __syncthreads();
+
+  // ---- exact leaf LSE of the candidates (slots split over the warps) ----
+  const int nslots = ncand_s;
+  for (int sidx = warp; sidx < nslots; sidx += WARPS) {
+    const int leaf = cand_leaf[sidx];
+    if (leaf < 0) continue;
+    const long long key0 = (long long)leaf * 64;
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      const long long key = key0 + 8 * nt + r;
+      const bool vis = key <= T;
+      const uint16_t* krow = Kb + (size_t)(vis ? key : key0) * D;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const uint4 kv = vis ? ldg16(krow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
+        mma_bf16_16816(acc[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
+        mma_bf16_16816(acc[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+      }
+    }
+    // acc[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0, 1}
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const bool vis = key0 + 8 * nt + 2 * q + c <= T;
+        s0 += vis ? fast_exp2(acc[nt][c] * p.sl2) : 0.f;
+        s1 += vis ? fast_exp2(acc[nt][2 + c] * p.sl2) : 0.f;
+      }
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    float lse2_0, lse2_1;
+    if (s0 > 0.f && s0 < POS_INF && s1 > 0.f && s1 < POS_INF) {
+      lse2_0 = fast_log2(s0);
+      lse2_1 = fast_log2(s1);
+    } else {  // outside the fp32 exponent range: subtract the row maxima first
+      float m0 = NEG_INF, m1 = NEG_INF;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (key0 + 8 * nt + 2 * q + c <= T) {
+            m0 = fmaxf(m0, acc[nt][c] * p.sl2);
+            m1 = fmaxf(m1, acc[nt][2 + c] * p.sl2);
+          }
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+      s0 = s1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (key0 + 8 * nt + 2 * q + c <= T) {
+            s0 += fast_exp2(acc[nt][c] * p.sl2 - m0);
+            s1 += fast_exp2(acc[nt][2 + c] * p.sl2 - m1);
+          }
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      lse2_0 = m0 + fast_log2(s0);
+      lse2_1 = m1 + fast_log2(s1);
+    }
+    float part = (r < p.GQ ? lse2_0 : 0.f) + (r + 8 < p.GQ ? lse2_1 : 0.f);
+    if (q != 0) part = 0.f;
+    part += __shfl_xor_sync(0xffffffffu, part, 4);
+    part += __shfl_xor_sync(0xffffffffu, part, 8);
+    part += __shfl_xor_sync(0xffffffffu, part, 16);
+    if (lane == 0) cand_score[sidx] = part;
+  }
+  __syncthreads();
+
+  // ---- final top-K with the own block (warp 0) ----
+  if (warp == 0) {
+    const int own = (int)(T >> 6);
+    int leaf = lane < nslots ? cand_leaf[lane] : -1;
+    if (leaf == own) leaf = -1;
+    const float sc = leaf >= 0 ? cand_score[lane] : NEG_INF;
+    const unsigned valid = __ballot_sync(0xffffffffu, leaf >= 0);
+    int rank = 0;
+    for (int j = 0; j < 32; ++j) {
+      if (!((valid >> j) & 1u)) continue;
+      const float sj = __shfl_sync(0xffffffffu, sc, j);
+      const int lj = __shfl_sync(0xffffffffu, leaf, j);
+      rank += (leaf >= 0 && (sj > sc || (sj == sc && lj < leaf))) ? 1 : 0;
+    }
+    const bool keep = leaf >= 0 && rank < p.Ksel - 1;
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    int pos = 0, below = 0;
+    for (int j = 0; j < 32; ++j) {
+      if (!((km >> j) & 1u)) continue;
+      const int lj = __shfl_sync(0xffffffffu, leaf, j);
+      pos += (keep && lj < leaf) ? 1 : 0;
+      below += lj < own ? 1 : 0;
+    }
+    if (keep) sel[pos + (own < leaf ? 1 : 0)] = leaf;
+    if (lane == 0) {
+      sel[below] = own;
+      nsel_s = __popc(km) + 1;
+    }
+    __syncwarp();
+    if (p.idx_out && lane < p.Ksel) p.idx_out[(size_t)bh * p.Ksel + lane] = lane < nsel_s ? sel[lane] : -1;
+  }
+  __syncthreads();
+
+  // ---- attention over the selected blocks: warp w takes blocks w, w+4, ... ----
+  const int nsel = nsel_s;
+  // S uses the permuted-d Q fragments with direct K loads; P V uses ldmatrix.trans on V
+  // staged in shared memory (keys in natural order in both)
+  float o[NDT][4];
+#pragma unroll
+  for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+  uint8_t* vmine = vbuf + (size_t)warp * 64 * D * 2;
+  const uint32_t vs = smem_u32(vmine);
+  for (int si = warp; si < nsel; si += WARPS) {
+    const int blk = sel[si];
+    const long long key0 = (long long)blk * 64;
+    // stage V block (64 x D) in swizzled smem: row k, 16-byte chunk c at (c ^ (k & 7)) per 128-byte half
+    for (int i = lane; i < 64 * (D / 8); i += 32) {
+      const int k = i / (D / 8), c = i % (D / 8);
+      const long long key = key0 + k;
+      const uint4 val = key <= T ? ldg16(Vb + (size_t)key * D + 8 * c) : make_uint4(0, 0, 0, 0);
+      const int h = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(vmine + h * (64 * 128) + k * 128 + ((cc ^ (k & 7)) << 4)) = val;
+    }
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const long long key = key0 + 8 * nt + r;
+      const bool vis = key <= T;
+      const uint16_t* krow = Kb + (size_t)(vis ? key : key0) * D;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const uint4 kv = vis ? ldg16(krow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
+        mma_bf16_16816(s[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
+        mma_bf16_16816(s[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+      }
+    }
+    // s[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0,1}  (the n index maps key order 1:1)
+    float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const bool vis = key0 + 8 * nt + 2 * q + c <= T;
+        s[nt][c] = vis ? s[nt][c] * p.sl2 : NEG_INF;
+        s[nt][2 + c] = vis ? s[nt][2 + c] * p.sl2 : NEG_INF;
+        mx0 = fmaxf(mx0, s[nt][c]);
+        mx1 = fmaxf(mx1, s[nt][2 + c]);
+      }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+    const float c0 = nm0 == NEG_INF ? 1.f : fast_exp2(m0 - nm0);
+    const float c1 = nm1 == NEG_INF ? 1.f : fast_exp2(m1 - nm1);
+    m0 = nm0;
+    m1 = nm1;
+    l0 *= c0;
+    l1 *= c1;
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) {
+      o[i][0] *= c0;
+      o[i][1] *= c0;
+      o[i][2] *= c1;
+      o[i][3] *= c1;
+    }
+    uint32_t pa[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float p00 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][0] - m0);
+      const float p01 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][1] - m0);
+      const float p10 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][2] - m1);
+      const float p11 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][3] - m1);
+      l0 += p00 + p01;
+      l1 += p10 + p11;
+      const int kk = nt >> 1, hi = nt & 1;
+      pa[kk][hi ? 2 : 0] = pack_bf16x2(p00, p01);
+      pa[kk][hi ? 3 : 1] = pack_bf16x2(p10, p11);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+      for (int np = 0; np < NDT / 2; ++np) {
+        const int d0 = 8 * (2 * np + (lane >> 4));
+        const uint32_t addr = vs + (d0 >> 6) * (64 * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
+        mma_bf16_16816(o[2 * np + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+      }
+    }
+    __syncwarp();
+  }
+  // merge the per-warp softmax states (fixed order, deterministic)
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if (q == 0) {
+    part_m[warp][r] = m0;
+    part_l[warp][r] = l0;
+    part_m[warp][r + 8] = m1;
+    part_l[warp][r + 8] = l1;
+  }
+  __syncthreads();  // every warp is also done with its V staging buffer
+  float* po = reinterpret_cast<float*>(vbuf);  // [WARPS][16][D] fp32, reuses the V buffers
+  {
+    float mm0 = NEG_INF, mm1 = NEG_INF;
+    for (int w = 0; w < WARPS; ++w) {
+      mm0 = fmaxf(mm0, part_m[w][r]);
+      mm1 = fmaxf(mm1, part_m[w][r + 8]);
+    }
+    const float f0 = m0 == NEG_INF ? 0.f : fast_exp2(m0 - mm0);
+    const float f1 = m1 == NEG_INF ? 0.f : fast_exp2(m1 - mm1);
+#pragma unroll
+    for (int i = 0; i < NDT; ++i)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col = 8 * i + 2 * q + c;
+        po[((size_t)warp * 16 + r) * D + col] = o[i][c] * f0;
+        po[((size_t)warp * 16 + r + 8) * D + col] = o[i][2 + c] * f1;
+      }
+  }
+  __syncthreads();
+  for (int i = tid; i < p.GQ * D; i += THREADS) {
+    const int row = i / D, col = i - (i / D) * D;
+    float mm = NEG_INF;
+    for (int w = 0; w < WARPS; ++w) mm = fmaxf(mm, part_m[w][row]);
+    float lsum = 0.f, acc = 0.f;
+    for (int w = 0; w < WARPS; ++w) {
+      if (part_m[w][row] != NEG_INF) lsum += part_l[w][row] * fast_exp2(part_m[w][row] - mm);
+      acc += po[((size_t)w * 16 + row) * D + col];
+    }
+    const size_t orow = (size_t)b * p.H_q + (size_t)hk * p.GQ + row;
+    p.o[orow * D + col] = f32_to_bf16_rne(lsum > 0.f ? acc / lsum : 0.f);
+    if (col == 0 && p.lse) p.lse[orow] = lsum > 0.f ? (mm + fast_log2(lsum)) * LN2 : NEG_INF;
+  }
+  (void)err;
+}
+
+__global__ void advance_seq_len_kernel(int32_t* seq_len, int B) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) seq_len[b] += 1;
+}
+
+template <int D>
+cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
+                     uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out, const Problem& pr,
+                     const Geometry& geo_cap, uint32_t* err, cudaStream_t s) {
+  DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.Kc = Kc;
+  p.Vc = Vc;
+  p.Pc = Pc;
+  p.seq_len = seq_len;
+  p.o = o;
+  p.lse = lse;
+  p.idx_out = idx_out;
+  p.H_q = pr.H_q;
+  p.H_kv = pr.H_kv;
+  p.GQ = pr.GQ;
+  p.Ksel = pr.K;
+  p.N_cap = pr.N_cap;
+  p.sl2 = pr.scale * LOG2E;
+  p.nodes = geo_cap.nodes;
+  for (int l = 0; l <= MAX_LEVELS; ++l) p.off[l] = geo_cap.off[l];
+  const size_t smem = (size_t)WARPS * 64 * D * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<D><<<pr.B * pr.H_kv, THREADS, smem, s>>>(p, err);
+  advance_seq_len_kernel<<<(pr.B + 127) / 128, 128, 0, s>>>(seq_len, pr.B);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
+                          uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
+                          const Problem& p, const Geometry& geo_cap, uint32_t* err, cudaStream_t s) {
+  if (p.d == 128) return launch_d<128>(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, err, s);
+  return launch_d<64>(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, err, s);
+}
+
+}  // namespace pisa

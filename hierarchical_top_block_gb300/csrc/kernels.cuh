@@ -1,0 +1,60 @@
+// Internal launchers of the PISA kernels (one per translation unit), called by api.cu.
+#pragma once
+
+#include "common.cuh"
+
+namespace pisa {
+
+struct Problem {
+  int B, N, N_cap, H_q, H_kv, d;
+  int C, g, K, causal;
+  float scale;  // logit scale (already resolved; > 0)
+  int GQ;       // H_q / H_kv
+};
+
+// Builds pyramid levels 1..geo.L from the first N rows of K (layout capacity N_cap).
+cudaError_t launch_pyramid(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s);
+
+// Stage 1: level walk for every (b, h_kv, t); writes the level-2 survivors S2 [.., K].
+cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const Problem& p, const Geometry& geo,
+                          int num_sms, uint32_t* err, cudaStream_t s);
+
+// Clustering of (query, level-2 survivor) entries into per-(b, h_kv, window, node) lists
+// and Q tiles for Stage 2.
+struct ClusterBuffers {
+  int32_t* counts;      // [nkeys]
+  int32_t* cursor;      // [nkeys]
+  int32_t* offsets;     // [nkeys]  exclusive scan of counts
+  int32_t* tile_off;    // [nkeys]  exclusive scan of ceil(counts / qt)
+  int32_t* block_sums;  // [2 * nblocks]
+  int32_t* entries;     // [B * H_kv * N * K]   (t << 6) | slot
+  int4* tiles;          // [max_tiles]          {bh, node, entry start, entry count}
+  int32_t* totals;      // [4] {entries, tiles, ...}
+  long long nkeys;
+  int nwin, win, M2, qt, nblocks;
+  long long max_tiles;
+};
+cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Problem& p, cudaStream_t s);
+
+// Stage 2: exact leaf LSE of the candidate leaf pairs with tcgen05, head-summed.
+cudaError_t launch_leaf_lse(const uint16_t* Q, const uint16_t* K, const ClusterBuffers& cb, float* leaf_score,
+                            const Problem& p, const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s);
+
+// Final top-K with the own block kept; idx rows ascending, -1 padded.
+cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx, const Problem& p,
+                        const Geometry& geo, cudaStream_t s);
+
+// Block-sparse attention over idx.
+cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                               uint16_t* O, float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s);
+
+// Fused decode step.
+cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
+                          uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
+                          const Problem& p, const Geometry& geo_cap, uint32_t* err, cudaStream_t s);
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
+bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box);
+
+}  // namespace pisa

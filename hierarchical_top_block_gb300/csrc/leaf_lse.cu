@@ -1,0 +1,299 @@
+// Stage 2 of the two-stage selection (summary page of "Block Sparse Attention with
+// Log-Linear Complexity", section "Method step details", step 2; section "Core method",
+// eq. 21 at the leaf level): the exact LSE of every leaf candidate over its raw keys,
+// summed over the query heads of the GQA group.
+//
+// Work unit: a tile = up to qt queries (qt * max(G_Q, 8) = 128 rows) that all need the
+// same level-2 survivor, i.e. the same pair of sibling leaves (128 contiguous keys).
+//   D[128 rows, 128 keys] = Q_tile[128, d] . K_pair[128, d]^T   on tcgen05, fp32 in TMEM
+// then each epilogue thread owns one TMEM lane (one query head row) and reduces 64 keys
+// per leaf to log-sum-exp (causal mask inside the query's own block), and the G_Q rows of
+// a query are summed with lane shuffles in a fixed order.
+//
+// Persistent, warp-specialised CTA (one per SM):
+//   warp 0      TMA producer: K pair (3-D map, rows past N read as zero) into a 2-stage
+//               ring, reused across consecutive tiles of the same pair; Q rows of each
+//               query (2-D map, one box per 64 columns) into a 3-stage ring.
+//   warp 1      owns TMEM (2 x 128 columns, double-buffered accumulators); one thread
+//               issues the d/16 MMAs of a tile and commits to mbarriers.
+//   warps 2-9   epilogue: two warps per TMEM lane quarter, one per leaf of the pair.
+// Every wait is bounded; on timeout the error word is set and the CTA drains and exits.
+#include "kernels.cuh"
+
+namespace pisa {
+namespace {
+
+constexpr int NQS = 3;            // Q stages
+constexpr int NKS = 2;            // K-pair stages
+constexpr int ROWS = 128;         // MMA M (query-head rows)
+constexpr int KEYS = 128;         // MMA N (two leaves of 64 keys)
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t TMEM_COLS = 256;
+
+
+
+struct TileInfo {
+  int4 tile;   // bh, node, first entry, count
+  int ks;      // K stage holding the pair
+  int newk;    // 1 if the pair was loaded for this tile
+};
+
+struct Params {
+  const int4* tiles;
+  const int32_t* entries;
+  const int32_t* totals;
+  float* leaf_score;
+  int N, H_q, H_kv, GQ, RPQ, Ksel, M1, causal;
+  float sl2;  // scale * log2(e)
+};
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                              const __grid_constant__ CUtensorMap mapK, Params prm,
+                                                              uint32_t* err) {
+  constexpr int HALVES = D / 64;
+  constexpr uint32_t STAGE_BYTES = ROWS * D * 2;   // also the K-pair stage size (KEYS == ROWS)
+  constexpr int KSTEPS = D / 16;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + NQS * STAGE_BYTES;
+
+  __shared__ uint64_t q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[2], acc_empty[2];
+  __shared__ TileInfo info[NQS];
+  __shared__ int32_t ent[NQS][ROWS];
+  __shared__ uint32_t tmem_base_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NQS; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1 + EPI_WARPS);
+    }
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], EPI_WARPS);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, TMEM_COLS);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_s;
+  const int ntiles = prm.totals[1];
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    uint32_t kload = 0;
+    int prev_bh = -1, prev_node = -1, ks = 0;
+    for (int tile = blockIdx.x, it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+      const int qs = it % NQS;
+      if (!mbar_wait_warp(&q_empty[qs], ((it / NQS) & 1) ^ 1, err)) break;
+      const int4 tl = prm.tiles[tile];
+      const int bh = tl.x, node = tl.y, start = tl.z, cnt = tl.w;
+      const int newk = (bh != prev_bh || node != prev_node) ? 1 : 0;
+      if (newk) {
+        ks = kload % NKS;
+        if (!mbar_wait_warp(&k_empty[ks], ((kload / NKS) & 1) ^ 1, err)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&k_full[ks], STAGE_BYTES);
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h)
+            tma_load_3d(sK + ks * STAGE_BYTES + h * (KEYS * 128), &mapK, &k_full[ks], 64 * h, node * KEYS, bh);
+        }
+        ++kload;
+        prev_bh = bh;
+        prev_node = node;
+      }
+      const int b = bh / prm.H_kv, hk = bh - b * prm.H_kv;
+      int my_t[ROWS / 32 + 1];
+#pragma unroll
+      for (int k = 0; k * 32 < ROWS; ++k) {
+        const int i = lane + 32 * k;
+        my_t[k] = -1;
+        if (i < cnt) {
+          const int e = prm.entries[start + i];
+          ent[qs][i] = e;
+          my_t[k] = e >> 6;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        info[qs].tile = tl;
+        info[qs].ks = ks;
+        info[qs].newk = newk;
+        __threadfence_block();
+        mbar_arrive_expect_tx(&q_full[qs], (uint32_t)cnt * prm.RPQ * D * 2);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k * 32 < ROWS; ++k) {
+        const int i = lane + 32 * k;
+        if (i < cnt) {
+          const int row = (int)(((long long)b * prm.N + my_t[k]) * prm.H_q + (long long)hk * prm.GQ);
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h)
+            tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h,
+                        row);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(ROWS, KEYS);
+      uint32_t kload = 0;
+      int cur_ks = -1;
+      for (int tile = blockIdx.x, it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+        const int qs = it % NQS;
+        if (!mbar_wait(&q_full[qs], (it / NQS) & 1, err)) break;
+        const TileInfo ti = info[qs];
+        if (ti.newk) {
+          if (cur_ks >= 0) umma_commit(&k_empty[cur_ks]);
+          if (!mbar_wait(&k_full[ti.ks], (kload / NKS) & 1, err)) break;
+          ++kload;
+          cur_ks = ti.ks;
+        }
+        const int a = it & 1;
+        if (!mbar_wait(&acc_empty[a], ((it >> 1) & 1) ^ 1, err)) break;
+        tc_fence_after();
+        const uint32_t qbase = smem_u32(sQ + qs * STAGE_BYTES);
+        const uint32_t kbase = smem_u32(sK + ti.ks * STAGE_BYTES);
+#pragma unroll
+        for (int s = 0; s < KSTEPS; ++s) {
+          const uint32_t off = (s >> 2) * (ROWS * 128) + (s & 3) * 32;
+          umma_bf16(tmem_base + a * KEYS, smem_desc_sw128(qbase + off, 16, 1024),
+                    smem_desc_sw128(kbase + off, 16, 1024), idesc, s > 0 ? 1u : 0u);
+        }
+        umma_commit(&acc_full[a]);
+        umma_commit(&q_empty[qs]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int leaf_c = ew >> 2;  // which leaf of the pair this warp reduces
+    const int row = quarter * 32 + lane;
+    const int qi = row / prm.RPQ, h = row - qi * prm.RPQ;
+    const int twoK = 2 * prm.Ksel;
+    for (int tile = blockIdx.x, it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+      const int qs = it % NQS;
+      const int a = it & 1;
+      if (!mbar_wait_warp(&acc_full[a], (it >> 1) & 1, err)) break;
+      tc_fence_after();
+      const int4 tl = info[qs].tile;
+      const bool vq = qi < tl.w;
+      const int e = vq ? ent[qs][qi] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_empty[qs]);
+
+      uint32_t v[64];
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * KEYS + leaf_c * 64;
+      tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+
+      const int t = e >> 6, slot = e & 63;
+      const int bh = tl.x, node = tl.y;
+      const int leaf = 2 * node + leaf_c;
+      const long long key0 = (long long)leaf * 64;
+      const bool leaf_ok = vq && leaf < prm.M1 && (!prm.causal || key0 <= t);
+      // keys j <= lim of this leaf are visible (causal: key <= t; always: key < N)
+      long long lim = (long long)prm.N - 1 - key0;
+      if (prm.causal && (long long)t - key0 < lim) lim = (long long)t - key0;
+      float lse2 = NEG_INF;
+      if (leaf_ok && h < prm.GQ) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float x = __uint_as_float(v[j]) * prm.sl2;
+          s += (j <= lim) ? fast_exp2(x) : 0.f;
+        }
+        if (s > 0.f && s < POS_INF) {
+          lse2 = fast_log2(s);
+        } else {  // logits beyond the fp32 exponent range: subtract the max first
+          float m = NEG_INF;
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j <= lim) m = fmaxf(m, __uint_as_float(v[j]) * prm.sl2);
+          float s2 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j <= lim) s2 += fast_exp2(__uint_as_float(v[j]) * prm.sl2 - m);
+          lse2 = m + fast_log2(s2);
+        }
+      }
+      // sum over the G_Q head rows of each query (lanes of one query are contiguous)
+      float part = (leaf_ok && h < prm.GQ) ? lse2 : 0.f;
+      for (int o = 1; o < prm.RPQ; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (vq && h == 0)
+        prm.leaf_score[((size_t)bh * prm.N + t) * twoK + 2 * slot + leaf_c] = leaf_ok ? part * LN2 : NEG_INF;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers& cb, float* leaf_score,
+                     const Problem& p, const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s) {
+  const int RPQ = p.GQ < 8 ? 8 : p.GQ;
+  CUtensorMap mapQ, mapK;
+  {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.B * p.N * p.H_q};
+    const uint64_t strides[1] = {(uint64_t)D * 2};
+    const uint32_t box[2] = {64, (uint32_t)RPQ};
+    if (!encode_tensor_map(&mapQ, Q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.N, (uint64_t)p.B * p.H_kv};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.N * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)KEYS, 1};
+    if (!encode_tensor_map(&mapK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  Params prm;
+  prm.tiles = cb.tiles;
+  prm.entries = cb.entries;
+  prm.totals = cb.totals;
+  prm.leaf_score = leaf_score;
+  prm.N = p.N;
+  prm.H_q = p.H_q;
+  prm.H_kv = p.H_kv;
+  prm.GQ = p.GQ;
+  prm.RPQ = RPQ;
+  prm.Ksel = p.K;
+  prm.M1 = geo.M[1];
+  prm.causal = p.causal;
+  prm.sl2 = p.scale * LOG2E;
+  const size_t smem = (size_t)(NQS + NKS) * ROWS * D * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(leaf_lse_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  leaf_lse_kernel<D><<<num_sms, THREADS, smem, s>>>(mapQ, mapK, prm, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_leaf_lse(const uint16_t* Q, const uint16_t* K, const ClusterBuffers& cb, float* leaf_score,
+                            const Problem& p, const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s) {
+  if (p.d == 128) return launch_d<128>(Q, K, cb, leaf_score, p, geo, num_sms, err, s);
+  return launch_d<64>(Q, K, cb, leaf_score, p, geo, num_sms, err, s);
+}
+
+}  // namespace pisa

@@ -1,0 +1,144 @@
+// Step 1 of the method (summary page of "Block Sparse Attention with Log-Linear
+// Complexity", section "Method step details", eqs 10-15): the mean-pooled key pyramid.
+// Leaf j = mean of keys [jC, min(jC+C, N)); node i of level l+1 = mean of its <= g = 2
+// children.  Every node is rounded once to bf16 (nearest even) from an exact-to-2^-40
+// sum: leaves accumulate with error-free fp32 TwoSum pairs, the final division and the
+// level means run in fp64.
+//
+// HBM streaming: K is read once with 16-byte coalesced loads (one warp per leaf);
+// each CTA owns a 16-leaf subtree and writes levels 1..5 of it from shared memory; a
+// second small kernel builds the levels above (one CTA per (b, h_kv)).
+#include "kernels.cuh"
+
+namespace pisa {
+namespace {
+
+constexpr int LPB = 16;           // leaves per CTA subtree
+constexpr int SUB_LEVELS = 5;     // levels 1..5 of a 16-leaf subtree
+constexpr int THREADS = 256;
+
+template <int D>
+__global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t* __restrict__ K,
+                                                                 uint16_t* __restrict__ P, int N, int N_cap,
+                                                                 Geometry geo, int top_level) {
+  constexpr int LPR = D / 8;        // lanes per key row (16 bytes each)
+  constexpr int RPI = 32 / LPR;     // rows per warp iteration
+  __shared__ __align__(16) uint16_t buf[2][LPB][D];
+
+  const int bh = blockIdx.y;
+  const int sub = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint16_t* Kb = K + (size_t)bh * N_cap * D;
+  uint16_t* Pb = P + (size_t)bh * geo.nodes * D;
+  const int M1 = geo.M[1];
+  const int col = (lane % LPR) * 8;
+
+  for (int li = warp; li < LPB; li += THREADS / 32) {
+    const int leaf = sub * LPB + li;
+    if (leaf >= M1) break;
+    const int r0 = leaf * 64, r1 = min(N, r0 + 64);
+    float hi[8], lo[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hi[k] = lo[k] = 0.f;
+#pragma unroll 8
+    for (int r = r0 + lane / LPR; r < r1; r += RPI) {
+      uint4 v = ldg16(Kb + (size_t)r * D + col);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float s, e;
+        two_sum(hi[2 * k], bf16_lo(w[k]), s, e);
+        hi[2 * k] = s;
+        lo[2 * k] += e;
+        two_sum(hi[2 * k + 1], bf16_hi(w[k]), s, e);
+        hi[2 * k + 1] = s;
+        lo[2 * k + 1] += e;
+      }
+    }
+    // combine the partial sums of lanes that share a column
+#pragma unroll
+    for (int m = LPR; m < 32; m <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float oh = __shfl_xor_sync(0xffffffffu, hi[k], m);
+        float ol = __shfl_xor_sync(0xffffffffu, lo[k], m);
+        float s, e;
+        two_sum(hi[k], oh, s, e);
+        hi[k] = s;
+        lo[k] = lo[k] + ol + e;
+      }
+    }
+    if (lane < LPR) {
+      const double cnt = (double)(r1 - r0);
+      uint32_t packed[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint16_t a = f64_to_bf16_rne(((double)hi[2 * k] + (double)lo[2 * k]) / cnt);
+        uint16_t b = f64_to_bf16_rne(((double)hi[2 * k + 1] + (double)lo[2 * k + 1]) / cnt);
+        packed[k] = (uint32_t)a | ((uint32_t)b << 16);
+      }
+      uint4 out = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      *reinterpret_cast<uint4*>(Pb + (size_t)(geo.off[1] + leaf) * D + col) = out;
+      *reinterpret_cast<uint4*>(&buf[0][li][col]) = out;
+    }
+  }
+  __syncthreads();
+
+  // levels 2..top_level of this subtree, from shared memory
+  int cur = 0;
+  for (int l = 2; l <= top_level; ++l) {
+    const int per = LPB >> (l - 1);                  // nodes of this subtree at level l
+    const int first = (sub * LPB) >> (l - 1);        // global index of the first one
+    const int first_child = (sub * LPB) >> (l - 2);
+    for (int idx = threadIdx.x; idx < per * D; idx += THREADS) {
+      const int i = idx / D, e = idx % D;
+      const int node = first + i;
+      if (node >= geo.M[l]) continue;
+      const int c0 = 2 * node, c1 = min(2 * node + 2, geo.M[l - 1]);
+      double s = 0.0;
+      for (int c = c0; c < c1; ++c) s += (double)bf16_to_f32(buf[cur][c - first_child][e]);
+      const uint16_t v = f64_to_bf16_rne(s / (double)(c1 - c0));
+      Pb[(size_t)(geo.off[l] + node) * D + e] = v;
+      buf[cur ^ 1][i][e] = v;
+    }
+    __syncthreads();
+    cur ^= 1;
+  }
+}
+
+// Levels first_level..L for one (b, h_kv), each from the level below it in P.
+template <int D>
+__global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __restrict__ P, Geometry geo,
+                                                                int first_level) {
+  uint16_t* Pb = P + (size_t)blockIdx.x * geo.nodes * D;
+  for (int l = first_level; l <= geo.L; ++l) {
+    const int m = geo.M[l];
+    for (int idx = threadIdx.x; idx < m * D; idx += THREADS) {
+      const int node = idx / D, e = idx % D;
+      const int c0 = 2 * node, c1 = min(2 * node + 2, geo.M[l - 1]);
+      double s = 0.0;
+      for (int c = c0; c < c1; ++c) s += (double)bf16_to_f32(Pb[(size_t)(geo.off[l - 1] + c) * D + e]);
+      Pb[(size_t)(geo.off[l] + node) * D + e] = f64_to_bf16_rne(s / (double)(c1 - c0));
+    }
+    __syncthreads();
+  }
+}
+
+template <int D>
+cudaError_t launch_pyramid_d(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s) {
+  if (geo.L == 0) return cudaSuccess;
+  const int top = geo.L < SUB_LEVELS ? geo.L : SUB_LEVELS;
+  dim3 grid((geo.M[1] + LPB - 1) / LPB, p.B * p.H_kv);
+  pyramid_leaves_kernel<D><<<grid, THREADS, 0, s>>>(K, P, p.N, p.N_cap, geo, top);
+  if (geo.L > top) pyramid_upper_kernel<D><<<p.B * p.H_kv, THREADS, 0, s>>>(P, geo, top + 1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pyramid(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s) {
+  if (p.d == 128) return launch_pyramid_d<128>(K, P, p, geo, s);
+  return launch_pyramid_d<64>(K, P, p, geo, s);
+}
+
+}  // namespace pisa

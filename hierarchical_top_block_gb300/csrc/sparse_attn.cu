@@ -1,0 +1,312 @@
+// Step 4 of the method (summary page of "Block Sparse Attention with Log-Linear
+// Complexity", section "Method step details", step 4; section "Prerequisites", BSA:
+// attention on the raw K/V of the selected blocks only).  The softmax runs over the
+// connected positions only (blog post of the same title, section 3.3): for query t and
+// head h, the keys of the selected blocks of h's group, restricted to keys <= t.
+//
+// The G_Q heads of one query share the selected blocks, so one warp owns one query: its
+// G_Q rows (padded to 16) form the M = 16 side of m16n8k16 MMAs; different queries
+// select different blocks, so there is no larger dense tile without wasted work.  The
+// kernel is bound by moving the selected K/V blocks (16 KB each at d = 128) into the SM:
+// each warp runs its own ring of TMA-filled shared-memory slots (128-byte swizzle, one
+// 3-D box per block; rows past N read as zero) that keeps two blocks in flight ahead of
+// the one being multiplied, across query boundaries.  S = Q K^T and O += P V use ldmatrix
+// (.trans for V) on the swizzled slots; the softmax is online (running max and sum per
+// head row) in the exp2 domain.  All waits are bounded.
+#include "kernels.cuh"
+
+namespace pisa {
+namespace {
+
+constexpr int NW = 4;       // warps per CTA, one query each
+constexpr int NSLOT = 3;    // ring slots per warp (K and V blocks alternate)
+
+
+struct AttnParams {
+  const uint16_t* Q;
+  const int32_t* idx;
+  uint16_t* O;
+  float* LSE;
+  long long total;  // B * H_kv * N
+  int N, H_q, H_kv, GQ, Ksel, M1, causal;
+  float sl2;
+};
+
+// Walks the (query, selected block, K|V) load sequence of one warp.
+struct Cursor {
+  long long item;   // current (bh, t) item, or >= total when exhausted
+  unsigned mask;    // remaining valid idx positions of the item
+  int val;          // this lane's idx entry of the item
+  int kv;           // 0: K of the lowest remaining block next, 1: its V
+};
+
+__device__ __forceinline__ void load_item(Cursor& c, const AttnParams& p, long long item, uint32_t* err) {
+  const int lane = threadIdx.x & 31;
+  c.item = item;
+  c.kv = 0;
+  c.val = -1;
+  c.mask = 0;
+  if (item >= p.total) return;
+  const int t = (int)(item % p.N);
+  int v = lane < p.Ksel ? p.idx[item * p.Ksel + lane] : -1;
+  if (v >= p.M1) {
+    report_error(err, ERR_BAD_INDEX);
+    v = -1;
+  }
+  // a block that starts after t has no visible key: skip it
+  if (v >= 0 && p.causal && (long long)v * 64 > t) v = -1;
+  c.val = v;
+  c.mask = __ballot_sync(0xffffffffu, v >= 0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap mapK,
+                                                                 const __grid_constant__ CUtensorMap mapV,
+                                                                 AttnParams p, uint32_t* err) {
+  constexpr int HALVES = D / 64;
+  constexpr uint32_t SLOT = 64 * D * 2;
+  constexpr int KST = D / 16;        // k-steps of Q K^T
+  constexpr int NDT = D / 8;         // n-tiles of P V
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[NW][NSLOT];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, q = lane & 3;
+  uint8_t* ring = smem + (size_t)warp * NSLOT * SLOT;
+  if (lane == 0) {
+    for (int i = 0; i < NSLOT; ++i) mbar_init(&full[warp][i], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+
+  const long long gw = (long long)blockIdx.x * NW + warp;
+  const long long nwarps = (long long)gridDim.x * NW;
+
+  // ---- producer side of this warp's ring ----
+  Cursor pc;
+  load_item(pc, p, gw, err);
+  long long issued = 0, consumed = 0;
+  auto advance = [&](Cursor& c) {
+    if (c.kv == 0) {
+      c.kv = 1;
+      return;
+    }
+    c.kv = 0;
+    c.mask &= c.mask - 1;
+    while (c.mask == 0 && c.item < p.total) load_item(c, p, c.item + nwarps, err);
+  };
+  while (pc.mask == 0 && pc.item < p.total) load_item(pc, p, pc.item + nwarps, err);
+  auto issue_until = [&](long long limit) {
+    while (issued < limit && pc.item < p.total) {
+      const int slot = (int)(issued % NSLOT);
+      const int pos = __ffs(pc.mask) - 1;
+      const int blk = __shfl_sync(0xffffffffu, pc.val, pos);
+      const int bh = (int)(pc.item / p.N);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[warp][slot], SLOT);
+        const CUtensorMap* m = pc.kv == 0 ? &mapK : &mapV;
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h) tma_load_3d(ring + slot * SLOT + h * (64 * 128), m, &full[warp][slot], 64 * h, blk * 64, bh);
+      }
+      ++issued;
+      advance(pc);
+    }
+  };
+  issue_until(NSLOT);
+
+  bool ok = true;
+  for (long long item = gw; item < p.total && ok; item += nwarps) {
+    const int bh = (int)(item / p.N);
+    const int t = (int)(item - (long long)bh * p.N);
+    const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+    Cursor cc;
+    load_item(cc, p, item, nullptr);
+
+    // Q fragments (rows r, r+8 of the group; zero past G_Q)
+    uint32_t qa[KST][4];
+    const uint16_t* qrow = p.Q + (((size_t)b * p.N + t) * p.H_q + (size_t)hk * p.GQ) * D;
+#pragma unroll
+    for (int ks = 0; ks < KST; ++ks) {
+      const int c0 = 16 * ks + 2 * q;
+      qa[ks][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)r * D + c0) : 0u;
+      qa[ks][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)(r + 8) * D + c0) : 0u;
+      qa[ks][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)r * D + c0 + 8) : 0u;
+      qa[ks][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)(r + 8) * D + c0 + 8) : 0u;
+    }
+    float o[NDT][4];
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+    for (unsigned mask = cc.mask; mask && ok; mask &= mask - 1) {
+      const int blk = __shfl_sync(0xffffffffu, cc.val, __ffs(mask) - 1);
+      // ---------------- S = Q K^T over the block's 64 keys ----------------
+      int slot = (int)(consumed % NSLOT);
+      if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kb = smem_u32(ring + slot * SLOT);
+      float s[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        const int key = 8 * nt + (lane & 7);
+#pragma unroll
+        for (int kp = 0; kp < KST / 2; ++kp) {
+          const int d0 = 32 * kp + 8 * (lane >> 3);
+          const uint32_t addr = kb + (d0 >> 6) * (64 * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(addr, b0, b1, b2, b3);
+          mma_bf16_16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+          mma_bf16_16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+        }
+      }
+      ++consumed;
+      issue_until(consumed + NSLOT);
+
+      // ---------------- online softmax (log2 domain) ----------------
+      const long long kbase = (long long)blk * 64;
+      float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const long long key = kbase + 8 * nt + 2 * q + c;
+          const bool vis = key < p.N && (!p.causal || key <= t);
+          s[nt][c] = vis ? s[nt][c] * p.sl2 : NEG_INF;
+          s[nt][2 + c] = vis ? s[nt][2 + c] * p.sl2 : NEG_INF;
+          mx0 = fmaxf(mx0, s[nt][c]);
+          mx1 = fmaxf(mx1, s[nt][2 + c]);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+      const float c0 = nm0 == NEG_INF ? 1.f : fast_exp2(m0 - nm0);
+      const float c1 = nm1 == NEG_INF ? 1.f : fast_exp2(m1 - nm1);
+      m0 = nm0;
+      m1 = nm1;
+      l0 *= c0;
+      l1 *= c1;
+#pragma unroll
+      for (int i = 0; i < NDT; ++i) {
+        o[i][0] *= c0;
+        o[i][1] *= c0;
+        o[i][2] *= c1;
+        o[i][3] *= c1;
+      }
+      uint32_t pa[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const float p00 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][0] - m0);
+        const float p01 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][1] - m0);
+        const float p10 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][2] - m1);
+        const float p11 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][3] - m1);
+        l0 += p00 + p01;
+        l1 += p10 + p11;
+        const int kk = nt >> 1, hi = nt & 1;
+        pa[kk][hi ? 2 : 0] = pack_bf16x2(p00, p01);
+        pa[kk][hi ? 3 : 1] = pack_bf16x2(p10, p11);
+      }
+
+      // ---------------- O += P V ----------------
+      slot = (int)(consumed % NSLOT);
+      if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t vb = smem_u32(ring + slot * SLOT);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+        for (int np = 0; np < NDT / 2; ++np) {
+          const int d0 = 8 * (2 * np + (lane >> 4));
+          const uint32_t addr = vb + (d0 >> 6) * (64 * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
+          mma_bf16_16816(o[2 * np + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+        }
+      }
+      ++consumed;
+      issue_until(consumed + NSLOT);
+    }
+    if (!ok) break;
+
+    // ---------------- normalise and store ----------------
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    uint16_t* orow = p.O + (((size_t)b * p.N + t) * p.H_q + (size_t)hk * p.GQ) * D;
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) {
+      const int col = 8 * i + 2 * q;
+      if (r < p.GQ) *reinterpret_cast<uint32_t*>(orow + (size_t)r * D + col) = pack_bf16x2(o[i][0] * inv0, o[i][1] * inv0);
+      if (r + 8 < p.GQ)
+        *reinterpret_cast<uint32_t*>(orow + (size_t)(r + 8) * D + col) = pack_bf16x2(o[i][2] * inv1, o[i][3] * inv1);
+    }
+    if (p.LSE && q == 0) {
+      const size_t hbase = (size_t)b * p.H_q + (size_t)hk * p.GQ;
+      if (r < p.GQ) p.LSE[(hbase + r) * p.N + t] = l0 > 0.f ? (m0 + fast_log2(l0)) * LN2 : NEG_INF;
+      if (r + 8 < p.GQ) p.LSE[(hbase + r + 8) * p.N + t] = l1 > 0.f ? (m1 + fast_log2(l1)) * LN2 : NEG_INF;
+    }
+  }
+  // drain loads still in flight before the CTA's shared memory goes away (bounded)
+  while (consumed < issued) {
+    const int slot = (int)(consumed % NSLOT);
+    if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) break;
+    ++consumed;
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx, uint16_t* O,
+                     float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s) {
+  CUtensorMap mapK, mapV;
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.N, (uint64_t)p.B * p.H_kv};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.N_cap * D * 2};
+  const uint32_t box[3] = {64, 64, 1};
+  if (!encode_tensor_map(&mapK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  if (!encode_tensor_map(&mapV, V, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  AttnParams prm;
+  prm.Q = Q;
+  prm.idx = idx;
+  prm.O = O;
+  prm.LSE = LSE;
+  prm.total = (long long)p.B * p.H_kv * p.N;
+  prm.N = p.N;
+  prm.H_q = p.H_q;
+  prm.H_kv = p.H_kv;
+  prm.GQ = p.GQ;
+  prm.Ksel = p.K;
+  prm.M1 = (p.N + 63) / 64;
+  prm.causal = p.causal;
+  prm.sl2 = p.scale * LOG2E;
+  if (prm.total == 0) return cudaSuccess;
+  const size_t smem = (size_t)NW * NSLOT * 64 * D * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  long long blocks = (prm.total + NW - 1) / NW;
+  if (blocks > num_sms) blocks = num_sms;
+  sparse_attn_kernel<D><<<(int)blocks, 32 * NW, smem, s>>>(mapK, mapV, prm, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                               uint16_t* O, float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s) {
+  if (p.d == 128) return launch_d<128>(Q, K, V, idx, O, LSE, p, num_sms, err, s);
+  return launch_d<64>(Q, K, V, idx, O, LSE, p, num_sms, err, s);
+}
+
+}  // namespace pisa

@@ -1,0 +1,172 @@
+/*
+ * pisa.h - C ABI of the GB300 (sm_103a) library for log-linear block-sparse attention
+ * with pyramid-LSE block selection.
+ *
+ * Method: "Block Sparse Attention with Log-Linear Complexity" (Tang, Qin, Pan, Li, Liu),
+ * as described on its summary page:
+ *   - section "Prerequisites", BSA: keys/values are cut into contiguous blocks of C keys,
+ *     each query keeps K blocks and attends only to their raw K/V;
+ *   - section "Core method", eq. 21: a candidate block's score is the log-sum-exp of its
+ *     children's logits q.k/sqrt(d) (raw keys at the leaf level);
+ *   - section "Method step details": step 1 the mean-pooled key pyramid (eqs 10-15);
+ *     step 2 the coarse-to-fine walk that scores at most gK candidates per level, sums the
+ *     score over the GQA group (eq. 22), keeps K (SelectK), expands survivors to their
+ *     children, scores the leaf candidates exactly and takes a final top-K; step 3 the
+ *     decode step that updates the new token's leaf and ancestors and walks all levels in
+ *     one kernel; step 4 attention over the selected blocks.
+ * The softmax runs over the connected positions only (blog post of the same title, 3.3).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, unless a name ends in
+ *     _host.  The library allocates nothing: scratch memory is passed in as `ws`.
+ *   - bf16 tensors are passed as uint16_t bit patterns; every tensor is row-major with
+ *     the last dimension contiguous and a 16-byte aligned base.
+ *   - Layouts: Q, O [B][N][H_q][d];  K, V [B][H_kv][N_cap][d];
+ *              P (pyramid) [B][H_kv][pisa_pyramid_nodes(N_cap)][d], level l (1 = leaves)
+ *              starting at node offset sum_{l'<l} M_l'(N_cap);
+ *              idx [B][H_kv][N][K] int32; LSE [B][H_q][N] fp32 (natural log).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Argument errors are reported synchronously, before anything is launched.
+ *   - Supported: d in {64, 128}; C = 64; g = 2; 1 <= K <= 16; H_q % H_kv == 0 and
+ *     G_Q = H_q / H_kv in {1, 2, 4, 8, 16}.  Other values return PISA_ERR_UNSUPPORTED.
+ *   - Selected index rows are sorted ascending and padded with -1 at the end.
+ *   - Kernels never trap: waits are bounded and out-of-range indices are skipped; either
+ *     event sets a device error word that pisa_get_last_device_error() returns.
+ */
+#ifndef PISA_H
+#define PISA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PISA_API __attribute__((visibility("default")))
+#else
+#define PISA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PISA_OK = 0,
+  PISA_ERR_INVALID_ARG = 1,  /* NULL or misaligned pointer, bad size */
+  PISA_ERR_UNSUPPORTED = 2,  /* valid but not implemented shape or parameter */
+  PISA_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  PISA_ERR_TIMEOUT = 4,      /* a bounded device wait gave up (device error word) */
+  PISA_ERR_BAD_INDEX = 5,    /* a selected block index was out of range (device error word) */
+  PISA_ERR_WORKSPACE = 6     /* ws_bytes smaller than the *_workspace_bytes query */
+} pisa_status;
+
+/* Method parameters (summary page, "Reproducibility": C = 64, g = 2, K = 8 or 32). */
+typedef struct {
+  int C;        /* leaf block size in keys; must be 64 */
+  int g;        /* pooling factor per pyramid level; must be 2 */
+  int K;        /* blocks kept per query (SelectK and the final top-K) */
+  int causal;   /* 1: query t sees keys <= t and blocks starting <= t; own block kept */
+  float scale;  /* logit scale; <= 0 selects 1/sqrt(d) */
+} pisa_params;
+
+typedef struct {
+  int B;        /* batch (sequences) */
+  int N;        /* tokens per sequence (prefill) */
+  int H_q;      /* query heads */
+  int H_kv;     /* key/value heads; each serves G_Q = H_q / H_kv query heads */
+  int d;        /* head dimension */
+  int N_cap;    /* row capacity of the K/V/P layouts (>= N); 0 means N */
+} pisa_shape;
+
+typedef void* pisa_stream; /* cudaStream_t */
+
+/* ---- geometry --------------------------------------------------------------------- */
+
+/* Number of pyramid levels for N tokens: M_1 = ceil(N/C) leaves, M_{l+1} = ceil(M_l/g),
+ * up to the single root (summary page, step 1).  0 for N = 0. */
+PISA_API int pisa_pyramid_levels(long long N, int C, int g);
+
+/* Total pyramid nodes sum_l M_l for N tokens: the P row count per (b, h_kv). */
+PISA_API long long pisa_pyramid_nodes(long long N, int C, int g);
+
+/* Scratch bytes pisa_select_prefill needs for this shape (a multiple of 256). */
+PISA_API size_t pisa_select_workspace_bytes(pisa_shape shape, pisa_params params);
+
+/* ---- step 1: key pyramid ------------------------------------------------------------ */
+
+/* Builds levels 1..L(N) of P from the first N rows of K (summary page, step 1,
+ * eqs 10-15): leaf j = mean of keys [jC, min(jC+C, N)); node i of level l+1 = mean of
+ * its <= g children.  Sums are exact to well below bf16 resolution; each node is rounded
+ * once to bf16 (nearest even).  K: [B][H_kv][N_cap][d]; P: [B][H_kv][nodes(N_cap)][d]. */
+PISA_API pisa_status pisa_build_pyramid(const uint16_t* K, uint16_t* P, pisa_shape shape, pisa_params params,
+                               pisa_stream stream);
+
+/* ---- step 2: block selection for prefill ---------------------------------------------- */
+
+/* For every (b, h_kv, t): the coarse-to-fine level walk (scores <= gK candidates per level
+ * with eq. 21, sums over the G_Q heads of the group, eq. 22, keeps K), exact leaf LSE of
+ * the <= gK leaf candidates, and the final top-K (own block kept in causal mode; ties go
+ * to the lower block index).  Q, K, P as above (N_cap must equal N).
+ *   idx        [B][H_kv][N][K]   int32 out: selected leaf blocks, ascending, -1 padded.
+ *   leaf_score [B][H_kv][N][g*K] fp32 out, nullable: head-summed leaf LSE per candidate
+ *              slot (slot g*i + c = child c of the i-th level-2 survivor; -inf if empty).
+ *   s2         [B][H_kv][N][K]   int32 out, nullable: level-2 survivors, ascending.
+ *   ws         device scratch of at least pisa_select_workspace_bytes(); 256-B aligned. */
+PISA_API pisa_status pisa_select_prefill(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx,
+                                float* leaf_score, int32_t* s2, void* ws, size_t ws_bytes, pisa_shape shape,
+                                pisa_params params, pisa_stream stream);
+
+/* ---- step 4: attention over the selected blocks --------------------------------------- */
+
+/* o_{t,h} = sum over keys c of the selected blocks of head h's group (c <= t if causal) of
+ * softmax(scale q.k_c) v_c, with the softmax over those positions only; LSE = log of the
+ * softmax denominator.  Entries of idx < 0 are skipped; entries >= ceil(N/C) are skipped
+ * and flag PISA_ERR_BAD_INDEX.  A row with no position gives o = 0 and LSE = -inf.
+ *   O [B][N][H_q][d] bf16 (nearest even);  LSE [B][H_q][N] fp32, nullable. */
+PISA_API pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                                     uint16_t* O, float* LSE, pisa_shape shape, pisa_params params,
+                                     pisa_stream stream);
+
+/* ---- full prefill from host buffers (end-to-end path) --------------------------------- */
+
+/* Copies Q, K, V host -> device, builds the pyramid, selects, attends and copies O (and
+ * LSE, idx when non-NULL) device -> host, all on `stream`, then synchronises the stream.
+ * Host buffers should be pinned for full copy bandwidth.  dev_ws is device scratch of at
+ * least pisa_prefill_host_workspace_bytes().  N_cap must equal N. */
+PISA_API size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params);
+PISA_API pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, const uint16_t* V_host,
+                              uint16_t* O_host, float* LSE_host, int32_t* idx_host, void* dev_ws, size_t ws_bytes,
+                              pisa_shape shape, pisa_params params, pisa_stream stream);
+
+/* ---- step 3: decode ------------------------------------------------------------------- */
+
+/* One decode step for every sequence b, in one fused kernel (summary page, step 3):
+ * T = seq_len[b]; writes k, v at row T of the caches; recomputes leaf T/C from its raw
+ * keys and every ancestor from its children (so Pc equals pisa_build_pyramid of the first
+ * T+1 keys); selects for the query at T over T+1 tokens (level walk, exact leaf LSE,
+ * top-K with the own block); attends; and advances seq_len[b] by one.
+ *   q [B][H_q][d], k, v [B][H_kv][d] bf16 in;  Kc, Vc [B][H_kv][N_cap][d] and
+ *   Pc [B][H_kv][nodes(N_cap)][d] bf16 in/out;  seq_len [B] int32 in/out (device), each
+ *   entry < N_cap;  o [B][H_q][d] bf16 out;  lse [B][H_q] fp32 out, nullable;
+ *   idx_out [B][H_kv][K] int32 out, nullable.  shape.N is ignored; shape.N_cap is required.
+ * Causal mode only. */
+PISA_API pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
+                             uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
+                             pisa_shape shape, pisa_params params, pisa_stream stream);
+
+/* ---- status ---------------------------------------------------------------------------- */
+
+PISA_API const char* pisa_status_string(pisa_status status);
+
+/* Waits for `stream`, then returns and clears the current device's error word:
+ * PISA_ERR_TIMEOUT if a bounded wait gave up, PISA_ERR_BAD_INDEX if an index was out of
+ * range, PISA_OK otherwise (PISA_ERR_CUDA if the CUDA calls themselves fail). */
+PISA_API pisa_status pisa_get_last_device_error(pisa_stream stream);
+
+/* Library version string. */
+PISA_API const char* pisa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PISA_H */

@@ -1,0 +1,70 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry point of
+include/pisa.h; host-side geometry and argument checks (no compute launches)."""
+import ctypes as ct
+import os
+import re
+
+import pytest
+
+import hierarchical_top_block_gb300 as pisa
+from hierarchical_top_block_gb300.build import build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pisa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return pisa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pisa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("pisa_build_pyramid", "pisa_select_prefill", "pisa_sparse_attn_prefill", "pisa_decode_step",
+                 "pisa_prefill_host", "pisa_pyramid_nodes", "pisa_select_workspace_bytes",
+                 "pisa_get_last_device_error", "pisa_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} is declared in include/pisa.h but not exported"
+
+
+def test_python_binding_has_the_same_names():
+    for name in declared_functions():
+        assert hasattr(pisa, name), f"binding lacks {name}"
+
+
+def test_geometry_matches_the_oracle(lib, oracle_impl):
+    for n in (0, 1, 63, 64, 65, 1000, 4096, 32768, 131073, 262144):
+        assert pisa.pisa_pyramid_levels(n) == oracle_impl.num_levels(n)
+        assert pisa.pisa_pyramid_nodes(n) == oracle_impl.pyramid_nodes(n)
+
+
+def test_workspace_query(lib):
+    ok = pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 262144, 16, 1, 128), pisa.make_params(16))
+    assert ok > 0 and ok % 256 == 0
+    assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 16, 1, 96), pisa.make_params(16)) == 0
+    assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 16, 1, 128), pisa.make_params(17)) == 0
+    assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 12, 4, 128), pisa.make_params(8)) == 0
+
+
+def test_argument_errors_without_a_gpu(lib):
+    shape = pisa.make_shape(1, 128, 4, 1, 64)
+    # NULL pointers are rejected before anything touches the device
+    assert lib.pisa_build_pyramid(None, None, shape, pisa.make_params(4), None) == 1
+    assert lib.pisa_sparse_attn_prefill(None, None, None, None, None, None, shape, pisa.make_params(4), None) == 1
+    # unsupported head dim / group size / block size
+    assert lib.pisa_build_pyramid(None, None, pisa.make_shape(1, 128, 4, 1, 80), pisa.make_params(4), None) == 2
+    assert lib.pisa_build_pyramid(None, None, shape, pisa.make_params(4, C=32), None) == 2
+    # empty problems are a no-op
+    assert lib.pisa_build_pyramid(None, None, pisa.make_shape(0, 128, 4, 1, 64), pisa.make_params(4), None) == 0
+    assert lib.pisa_status_string(2).decode() == "unsupported shape or parameter"
+    assert b"sm_103a" in lib.pisa_version()

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import hierarchical_top_block_gb300 as pisa
+    from hierarchical_top_block_gb300.build import build as _build
+
+    _build()
+    import gpu_helpers as H
+
+
+def _inputs(w, device="cuda"):
+    return W.prefill_inputs(w, device)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _needs_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def test_generator_identical_on_gpu():
+    w = W.WORKLOADS["prefill_4k"].with_(B=2, N=777, H_kv=2, H_q=8)
+    for (a, b) in zip(W.prefill_inputs(w, "cuda"), W.prefill_inputs(w, "cpu")):
+        assert torch.equal(a.cpu().view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("K_sel", [4, 8, 16])
+def test_tiny_all_rows(oracle_impl, K_sel):
+    w = W.WORKLOADS["tiny"].with_(K=K_sel)
+    Q, K, V = _inputs(w)
+    rep = H.full_prefill_check(oracle_impl, Q, K, V, K_sel)
+    assert rep["rows"] == w.N
+
+
+@pytest.mark.parametrize("N,GQ,H_kv,d,K_sel", [
+    (1, 4, 1, 64, 4), (63, 4, 1, 64, 4), (64, 2, 2, 128, 2), (65, 8, 1, 128, 3), (130, 1, 2, 64, 1),
+    (64 * 37 + 11, 16, 1, 128, 5), (64 * 70 + 1, 8, 2, 64, 16), (2048 + 64 * 9 + 33, 16, 1, 128, 16),
+])
+def test_ragged_shapes_all_rows(oracle_impl, N, GQ, H_kv, d, K_sel):
+    w = W.WORKLOADS["prefill_4k"].with_(B=2, N=N, H_q=GQ * H_kv, H_kv=H_kv, d=d, K=K_sel, needles=min(3, max(0, N // 200)))
+    Q, K, V = _inputs(w)
+    rows = w.B * w.H_kv * w.N
+    H.full_prefill_check(oracle_impl, Q, K, V, K_sel, sample=None if rows <= 4096 else 1500, seed=N)
+
+
+def test_non_causal(oracle_impl):
+    w = W.WORKLOADS["tiny"].with_(N=64 * 20 + 7)
+    Q, K, V = _inputs(w)
+    H.full_prefill_check(oracle_impl, Q, K, V, 4, causal=False)
+
+
+def test_prefill_4k_sampled(oracle_impl):
+    w = W.WORKLOADS["prefill_4k"]
+    Q, K, V = _inputs(w)
+    rep = H.full_prefill_check(oracle_impl, Q, K, V, w.K, sample=768, seed=2)
+    assert rep["rows"] == 768
+
+
+def test_dense_when_K_covers_all_leaves(oracle_impl):
+    """K >= ceil(N/C): every eligible leaf is selected, so the output is dense causal attention."""
+    w = W.WORKLOADS["tiny"].with_(N=64 * 12 + 5, K=13)
+    Q, K, V = _inputs(w)
+    res = H.run_gpu_prefill(Q, K, V, 13)
+    N = w.N
+    for t in (0, 63, 64, 300, N - 1):
+        sel = [x for x in res["idx"][0, 0, t] if x >= 0]
+        assert sel == list(range(t // 64 + 1))
+    Qf, Kf, Vf = Q[0].double().cpu().numpy(), K[0, 0].double().cpu().numpy(), V[0, 0].double().cpu().numpy()
+    O = res["O"][0].float().cpu().numpy()
+    for t in (0, 100, N - 1):
+        for h in range(w.H_q):
+            z = Qf[t, h] @ Kf[: t + 1].T / math.sqrt(w.d)
+            p = np.exp(z - z.max())
+            ref = (p / p.sum()) @ Vf[: t + 1]
+            assert np.abs(O[t, h] - ref).max() <= H.ATTN_MAX_ABS
+
+
+def test_bad_index_is_reported_not_faulted():
+    w = W.WORKLOADS["tiny"]
+    Q, K, V = _inputs(w)
+    idx = torch.full((1, 1, w.N, 4), -1, dtype=torch.int32, device="cuda")
+    idx[..., 0] = torch.arange(w.N, device="cuda", dtype=torch.int32) // 64
+    idx[0, 0, 100, 1] = 10_000  # out of range
+    O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx)
+    torch.cuda.synchronize()
+    assert pisa.pisa_get_last_device_error() == 5
+    assert pisa.pisa_get_last_device_error() == 0  # cleared by the read
+    assert torch.isfinite(LSE).all()
+
+
+def test_argument_errors_are_synchronous():
+    w = W.WORKLOADS["tiny"]
+    Q, K, V = _inputs(w)
+    with pytest.raises(pisa.PisaError):
+        pisa.pisa_select_prefill(Q, K, pisa.pisa_build_pyramid(K), 17)  # K > 16 unsupported
+    assert pisa.pisa_get_last_device_error() == 0
+
+
+def test_prefill_32k_sampled(oracle_impl):
+    w = W.WORKLOADS["prefill_32k"]
+    Q, K, V = _inputs(w)
+    rep = H.full_prefill_check(oracle_impl, Q, K, V, w.K, sample=192, seed=3)
+    assert rep["rows"] == 192
+
+
+def test_prefill_256k_sampled(oracle_impl):
+    """Full selection-scale size, the launch configuration the benchmark times; the oracle
+    computes sampled rows one by one.  Q is generated on the GPU and, for the sampled rows
+    only, on the CPU; K and V are generated on both and compared bit for bit."""
+    w = W.WORKLOADS["prefill_256k"]
+    Q = W.make_q(w, "cuda")
+    K = W.make_kv(w, "K", "cuda")
+    V = W.make_kv(w, "V", "cuda")
+    res = H.run_gpu_prefill(Q, K, V, w.K)
+    Kc, Vc = W.make_kv(w, "K", "cpu"), W.make_kv(w, "V", "cpu")
+    assert torch.equal(K.cpu().view(torch.int16), Kc.view(torch.int16))
+    assert torch.equal(V.cpu().view(torch.int16), Vc.view(torch.int16))
+    Kb, Vb = W.bits(Kc), W.bits(Vc)
+    Pb = oracle_impl.build_pyramid(Kb)
+    assert np.array_equal(W.bits(res["P"]), Pb)
+    rng = np.random.default_rng(4)
+    ts = np.concatenate([[0, 63, 64, w.N - 1, w.N - 65], rng.integers(0, w.N, 91)]).astype(np.int64)
+    Qb = np.zeros((1, w.N, w.H_q, w.d), np.uint16)
+    qrows = W.q_rows(w, 0, ts)
+    Qb[0, ts] = W.bits(qrows)
+    assert torch.equal(Q[0, torch.as_tensor(ts, device="cuda")].cpu().view(torch.int16), qrows.view(torch.int16))
+    rows = np.stack([np.zeros_like(ts), np.zeros_like(ts), ts], 1)
+    H.check_selection(oracle_impl, Qb, Kb, Pb, w.K, rows, res["idx"][0, 0, ts], res["s2"][0, 0, ts],
+                      res["score"][0, 0, ts])
+    bt = np.unique(np.stack([np.zeros_like(ts), ts], 1), axis=0)
+    O = res["O"][0, torch.as_tensor(bt[:, 1], device="cuda")].float().cpu().numpy()
+    LSE = res["LSE"][0][:, bt[:, 1]].T
+    H.check_attention(oracle_impl, Qb, Kb, Vb, res["idx"], bt, O, LSE)
+
+
+def _decode_check(o, w, N0, steps, N_cap, pairs=None):
+    """Runs the GPU decode for `steps` steps from N0 cached tokens and checks every step on
+    the (sequence, KV head) pairs given: the pyramid cache (bit-exact), idx (gap rule) and
+    o / lse.  The oracle runs each pair as its own one-sequence, one-KV-head problem."""
+    B, H_q, H_kv, d, K_sel = w.B, w.H_q, w.H_kv, w.d, w.K
+    G = H_q // H_kv
+    wk = w.with_(N=N0)
+    Kc = torch.zeros(B, H_kv, N_cap, d, dtype=torch.bfloat16, device="cuda")
+    Vc = torch.zeros_like(Kc)
+    for b in range(B):
+        for g in range(H_kv):
+            Kc[b, g, :N0] = W.kv_slice(wk, "K", b, g, device="cuda")
+            Vc[b, g, :N0] = W.kv_slice(wk, "V", b, g, device="cuda")
+    Pc = pisa.pisa_build_pyramid(Kc, N=N0)
+    seq = torch.full((B,), N0, dtype=torch.int32, device="cuda")
+    pairs = [(b, g) for b in range(B) for g in range(H_kv)] if pairs is None else pairs
+    ref = {}
+    for b, g in pairs:
+        kc = np.zeros((1, 1, N_cap, d), np.uint16)
+        vc = np.zeros((1, 1, N_cap, d), np.uint16)
+        kc[0, 0, :N0] = W.bits(W.kv_slice(wk, "K", b, g))
+        vc[0, 0, :N0] = W.bits(W.kv_slice(wk, "V", b, g))
+        pc = o.build_pyramid(kc, N=N0)
+        assert np.array_equal(W.bits(Pc[b, g]), pc[0, 0]), "initial pyramid cache differs"
+        ref[(b, g)] = [kc, vc, pc, np.array([N0], np.int32)]
+    for s in range(steps):
+        q, k, v = W.decode_step_inputs(w, s, "cuda")
+        out = torch.empty(B, H_q, d, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, H_q, dtype=torch.float32, device="cuda")
+        idx = torch.empty(B, H_kv, K_sel, dtype=torch.int32, device="cuda")
+        pisa.pisa_decode_step(q, k, v, Kc, Vc, Pc, seq, K_sel, o=out, lse=lse, idx_out=idx)
+        torch.cuda.synchronize()
+        assert pisa.pisa_get_last_device_error() == 0
+        qn, kn, vn = W.bits(q), W.bits(k), W.bits(v)
+        for (b, g), (kc, vc, pc, sl) in ref.items():
+            T = int(sl[0])
+            ro, rl, ri = o.decode_step(qn[b:b + 1, g * G:(g + 1) * G].copy(), kn[b:b + 1, g:g + 1].copy(),
+                                       vn[b:b + 1, g:g + 1].copy(), kc, vc, pc, sl, K_sel)
+            assert np.array_equal(W.bits(Pc[b, g]), pc[0, 0]), f"pyramid cache differs at step {s}, pair {(b, g)}"
+            gi = idx[b, g].cpu().numpy()
+            if not np.array_equal(gi, ri[0, 0]):
+                n = T + 1
+                Qp = np.zeros((1, n, G, d), np.uint16)
+                Qp[0, T] = qn[b, g * G:(g + 1) * G]
+                Kp = kc[:, :, :n].copy()
+                H.check_selection(o, Qp, Kp, o.build_pyramid(Kp), K_sel, np.array([(0, 0, T)], np.int64), gi[None])
+            go = out[b, g * G:(g + 1) * G].float().cpu().numpy()
+            assert np.abs(go - ro[0]).max() <= H.ATTN_MAX_ABS, (s, b, g, np.abs(go - ro[0]).max())
+            assert H.rel_l2(go, ro[0]) <= H.ATTN_REL_L2
+            assert np.abs(lse[b, g * G:(g + 1) * G].cpu().numpy() - rl[0]).max() <= H.ATTN_MAX_ABS
+    assert torch.equal(seq.cpu(), torch.full((B,), N0 + steps, dtype=torch.int32))
+
+
+def test_decode_small_all_sequences(oracle_impl):
+    # 2040 cached tokens: the steps cross a leaf boundary (2048) and a level change (M_1 32 -> 33)
+    w = W.WORKLOADS["decode_128k"].with_(B=3, H_q=8, H_kv=2, K=6)
+    _decode_check(oracle_impl, w, N0=2040, steps=24, N_cap=2304)
+
+
+def test_decode_gq16_d64(oracle_impl):
+    w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=16, H_kv=1, d=64, K=16)
+    _decode_check(oracle_impl, w, N0=64 * 9 + 60, steps=10, N_cap=1024)
+
+
+def test_decode_fullsize_sampled(oracle_impl):
+    """The batched decode workload at full size (64 x 131072 cached tokens), two steps,
+    compared on sampled sequences."""
+    w = W.WORKLOADS["decode_128k"]
+    _decode_check(oracle_impl, w, N0=w.N, steps=2, N_cap=w.N + w.decode_steps, pairs=[(5, 3), (63, 7)])
