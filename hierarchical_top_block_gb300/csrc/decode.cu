@@ -69,6 +69,10 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_
   const int r = lane >> 2, q = lane & 3;
   const long long T = p.seq_len[b];
   const long long n = T + 1;
+  if (T < 0 || T >= p.N_cap) {  // no room in the caches: report, write nothing
+    if (tid == 0) report_error(err, ERR_BAD_INDEX);
+    return;
+  }
   uint16_t* Kb = p.Kc + (size_t)bh * p.N_cap * D;
   uint16_t* Vb = p.Vc + (size_t)bh * p.N_cap * D;
   uint16_t* Pb = p.Pc + (size_t)bh * p.nodes * D;
@@ -448,9 +452,9 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_
   (void)err;
 }
 
-__global__ void advance_seq_len_kernel(int32_t* seq_len, int B) {
+__global__ void advance_seq_len_kernel(int32_t* seq_len, int B, int N_cap) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) seq_len[b] += 1;
+  if (b < B && seq_len[b] >= 0 && seq_len[b] < N_cap) seq_len[b] += 1;
 }
 
 template <int D>
@@ -480,7 +484,7 @@ cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   decode_kernel<D><<<pr.B * pr.H_kv, THREADS, smem, s>>>(p, err);
-  advance_seq_len_kernel<<<(pr.B + 127) / 128, 128, 0, s>>>(seq_len, pr.B);
+  advance_seq_len_kernel<<<(pr.B + 127) / 128, 128, 0, s>>>(seq_len, pr.B, pr.N_cap);
   return cudaGetLastError();
 }
 
