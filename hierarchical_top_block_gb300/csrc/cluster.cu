@@ -172,6 +172,7 @@ cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Pr
   cudaError_t e;
   if ((e = cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cb.cursor, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(cb.totals, 0, sizeof(int32_t) * 4, s)) != cudaSuccess) return e;  // [2] = tile counter
   count_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.K, total);
   scan_local_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
   scan_blocks_kernel<<<1, SCAN_THREADS, 0, s>>>(cb);

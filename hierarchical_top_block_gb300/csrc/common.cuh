@@ -57,6 +57,28 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = (a - (s - bp)) + (b - bp);
 }
 
+// bf16 (nearest even) of (hi + lo) / cnt for an unevaluated fp32 pair hi + lo.  For a
+// power-of-two count the division is an exact scaling: the pair is renormalised with
+// TwoSum, scaled, folded into one fp32 with round-to-odd (truncate, then set the last bit
+// if anything was dropped) and rounded once to bf16, all in fp32.  Other counts (a ragged
+// last leaf) take the fp64 route.
+__device__ __forceinline__ uint16_t bf16_mean(float hi, float lo, int cnt) {
+  if ((cnt & (cnt - 1)) == 0) {
+    float s, e;
+    two_sum(hi, lo, s, e);
+    const float inv = 1.0f / (float)cnt;
+    s *= inv;
+    e *= inv;
+    uint32_t u = __float_as_uint(s);
+    if (e != 0.f) {
+      if ((e < 0.f) != (s < 0.f)) u -= 1u;  // s + e lies just inside |s|: truncate toward zero
+      u |= 1u;
+    }
+    return f32_to_bf16_rne(__uint_as_float(u));
+  }
+  return f64_to_bf16_rne(((double)hi + (double)lo) / (double)cnt);
+}
+
 // exp2 / log2 on the special-function unit.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -209,6 +231,9 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t saddr, uint32_t& r0, 
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(saddr));
 }
+
+// Fetch the 128-byte line holding p into L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 // 16-byte read-only global load.
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }

@@ -95,14 +95,16 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_
       lo += e;
     }
     const double cnt = (double)(T - leaf * 64 + 1);
-    Pb[(size_t)(p.off[1] + leaf) * D + tid] = f64_to_bf16_rne(((double)hi + (double)lo) / cnt);
+    Pb[(size_t)(p.off[1] + leaf) * D + tid] = bf16_mean(hi, lo, (int)cnt);
     long long node = leaf;
     for (int l = 2; l <= L; ++l) {
       node >>= 1;
       const long long c0 = 2 * node, c1 = min(2 * node + 2, (long long)level_size(n, l - 1));
-      double s = 0.0;
-      for (long long c = c0; c < c1; ++c) s += (double)bf16_to_f32(Pb[(size_t)(p.off[l - 1] + c) * D + tid]);
-      Pb[(size_t)(p.off[l] + node) * D + tid] = f64_to_bf16_rne(s / (double)(c1 - c0));
+      const float a = bf16_to_f32(Pb[(size_t)(p.off[l - 1] + c0) * D + tid]);
+      const float bb = c1 - c0 > 1 ? bf16_to_f32(Pb[(size_t)(p.off[l - 1] + c0 + 1) * D + tid]) : 0.f;
+      float s, err;
+      two_sum(a, bb, s, err);
+      Pb[(size_t)(p.off[l] + node) * D + tid] = bf16_mean(s, err, (int)(c1 - c0));
     }
   }
   __syncthreads();

@@ -13,7 +13,9 @@
 // Persistent, warp-specialised CTA (one per SM):
 //   warp 0      TMA producer: K pair (3-D map, rows past N read as zero) into a 2-stage
 //               ring, reused across consecutive tiles of the same pair; Q rows of each
-//               query (2-D map, one box per 64 columns) into a 3-stage ring.
+//               query (2-D map, one box per 64 columns) into a 4-stage ring.  Tiles
+//               come in runs of consecutive tiles from an atomic counter; a run's tile
+//               records and entries are staged in shared memory in one round trip.
 //   warp 1      owns TMEM (2 x 128 columns, double-buffered accumulators); one thread
 //               issues the d/16 MMAs of a tile and commits to mbarriers.
 //   warps 2-9   epilogue: two warps per TMEM lane quarter, one per leaf of the pair.
@@ -23,7 +25,7 @@
 namespace pisa {
 namespace {
 
-constexpr int NQS = 3;            // Q stages
+constexpr int NQS = 4;            // Q stages
 constexpr int NKS = 2;            // K-pair stages
 constexpr int ROWS = 128;         // MMA M (query-head rows)
 constexpr int KEYS = 128;         // MMA N (two leaves of 64 keys)
@@ -39,10 +41,13 @@ struct TileInfo {
   int newk;    // 1 if the pair was loaded for this tile
 };
 
+constexpr int SCHED_CHUNK = 8;    // tiles handed to a CTA per grab (consecutive: mostly one K pair)
+
 struct Params {
   const int4* tiles;
   const int32_t* entries;
   const int32_t* totals;
+  int32_t* sched;      // tile counter, zero at launch
   float* leaf_score;
   int N, H_q, H_kv, GQ, RPQ, Ksel, M1, causal;
   float sl2;  // scale * log2(e)
@@ -64,9 +69,13 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   __shared__ TileInfo info[NQS];
   __shared__ int32_t ent[NQS][ROWS];
   __shared__ uint32_t tmem_base_s;
+  __shared__ int done_it_s;  // iteration index of the end marker
+  __shared__ int4 chunk_tiles[SCHED_CHUNK];        // producer staging of the current chunk
+  __shared__ int32_t chunk_ent[SCHED_CHUNK * ROWS];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    done_it_s = 0x7fffffff;
     for (int i = 0; i < NQS; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1 + EPI_WARPS);
@@ -94,10 +103,38 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     // ------------------------------ producer ------------------------------
     uint32_t kload = 0;
     int prev_bh = -1, prev_node = -1, ks = 0;
-    for (int tile = blockIdx.x, it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+    int next_tile = 0, chunk_end = 0, chunk_base = 0, chunk_e0 = 0;
+    for (int it = 0;; ++it) {
       const int qs = it % NQS;
+      if (next_tile >= chunk_end) {
+        // grab the next run of consecutive tiles (mostly one K pair) and stage their tile
+        // records and entries in shared memory with one round trip each
+        int base = 0;
+        if (lane == 0) base = atomicAdd(prm.sched, SCHED_CHUNK);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        next_tile = chunk_base = base;
+        chunk_end = min(base + SCHED_CHUNK, ntiles);
+        if (base < ntiles) {
+          if (lane < chunk_end - base) chunk_tiles[lane] = prm.tiles[base + lane];
+          __syncwarp();
+          const int4 first = chunk_tiles[0], last = chunk_tiles[chunk_end - base - 1];
+          chunk_e0 = first.z;
+          const int ne = last.z + last.w - first.z;
+          for (int i = lane; i < ne; i += 32) chunk_ent[i] = prm.entries[chunk_e0 + i];
+          __syncwarp();
+        }
+      }
       if (!mbar_wait_warp(&q_empty[qs], ((it / NQS) & 1) ^ 1, err)) break;
-      const int4 tl = prm.tiles[tile];
+      if (next_tile >= ntiles) {  // no work left: pass an end marker down the pipeline
+        if (lane == 0) {
+          info[qs].tile = make_int4(0, 0, 0, -1);
+          __threadfence_block();
+          mbar_arrive(&q_full[qs]);
+        }
+        break;
+      }
+      const int4 tl = chunk_tiles[next_tile - chunk_base];
+      ++next_tile;
       const int bh = tl.x, node = tl.y, start = tl.z, cnt = tl.w;
       const int newk = (bh != prev_bh || node != prev_node) ? 1 : 0;
       if (newk) {
@@ -120,7 +157,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         const int i = lane + 32 * k;
         my_t[k] = -1;
         if (i < cnt) {
-          const int e = prm.entries[start + i];
+          const int e = chunk_ent[start - chunk_e0 + i];
           ent[qs][i] = e;
           my_t[k] = e >> 6;
         }
@@ -152,10 +189,18 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       constexpr uint32_t idesc = idesc_bf16_f32(ROWS, KEYS);
       uint32_t kload = 0;
       int cur_ks = -1;
-      for (int tile = blockIdx.x, it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+      for (int it = 0;; ++it) {
         const int qs = it % NQS;
         if (!mbar_wait(&q_full[qs], (it / NQS) & 1, err)) break;
         const TileInfo ti = info[qs];
+        if (ti.tile.w < 0) {  // end marker: tell the epilogue once its buffer is free
+          const int a = it & 1;
+          if (!mbar_wait(&acc_empty[a], ((it >> 1) & 1) ^ 1, err)) break;
+          done_it_s = it;
+          __threadfence_block();
+          mbar_arrive(&acc_full[a]);
+          break;
+        }
         if (ti.newk) {
           if (cur_ks >= 0) umma_commit(&k_empty[cur_ks]);
           if (!mbar_wait(&k_full[ti.ks], (kload / NKS) & 1, err)) break;
@@ -186,10 +231,11 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     const int row = quarter * 32 + lane;
     const int qi = row / prm.RPQ, h = row - qi * prm.RPQ;
     const int twoK = 2 * prm.Ksel;
-    for (int tile = blockIdx.x, it = 0; tile < ntiles; tile += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
       const int qs = it % NQS;
       const int a = it & 1;
       if (!mbar_wait_warp(&acc_full[a], (it >> 1) & 1, err)) break;
+      if (it >= *(volatile int*)&done_it_s) break;
       tc_fence_after();
       const int4 tl = info[qs].tile;
       const bool vq = qi < tl.w;
@@ -271,6 +317,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
   prm.tiles = cb.tiles;
   prm.entries = cb.entries;
   prm.totals = cb.totals;
+  prm.sched = cb.totals + 2;
   prm.leaf_score = leaf_score;
   prm.N = p.N;
   prm.H_q = p.H_q;

@@ -2,8 +2,9 @@
 // Complexity", section "Method step details", eqs 10-15): the mean-pooled key pyramid.
 // Leaf j = mean of keys [jC, min(jC+C, N)); node i of level l+1 = mean of its <= g = 2
 // children.  Every node is rounded once to bf16 (nearest even) from an exact-to-2^-40
-// sum: leaves accumulate with error-free fp32 TwoSum pairs, the final division and the
-// level means run in fp64.
+// sum: leaves accumulate with error-free fp32 TwoSum pairs and the level means are exact
+// TwoSum pairs; dividing by a power-of-two count is an exact scaling, folded to bf16 by
+// round-to-odd in fp32 (only a ragged last leaf divides in fp64, which is slow on GB300).
 //
 // HBM streaming: K is read once with 16-byte coalesced loads (one warp per leaf);
 // each CTA owns a 16-leaf subtree and writes levels 1..5 of it from shared memory; a
@@ -69,12 +70,12 @@ __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t*
       }
     }
     if (lane < LPR) {
-      const double cnt = (double)(r1 - r0);
+      const int cnt = r1 - r0;
       uint32_t packed[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint16_t a = f64_to_bf16_rne(((double)hi[2 * k] + (double)lo[2 * k]) / cnt);
-        uint16_t b = f64_to_bf16_rne(((double)hi[2 * k + 1] + (double)lo[2 * k + 1]) / cnt);
+        uint16_t a = bf16_mean(hi[2 * k], lo[2 * k], cnt);
+        uint16_t b = bf16_mean(hi[2 * k + 1], lo[2 * k + 1], cnt);
         packed[k] = (uint32_t)a | ((uint32_t)b << 16);
       }
       uint4 out = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -95,9 +96,11 @@ __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t*
       const int node = first + i;
       if (node >= geo.M[l]) continue;
       const int c0 = 2 * node, c1 = min(2 * node + 2, geo.M[l - 1]);
-      double s = 0.0;
-      for (int c = c0; c < c1; ++c) s += (double)bf16_to_f32(buf[cur][c - first_child][e]);
-      const uint16_t v = f64_to_bf16_rne(s / (double)(c1 - c0));
+      const float a = bf16_to_f32(buf[cur][c0 - first_child][e]);
+      const float b = c1 - c0 > 1 ? bf16_to_f32(buf[cur][c0 + 1 - first_child][e]) : 0.f;
+      float s, err;
+      two_sum(a, b, s, err);
+      const uint16_t v = bf16_mean(s, err, c1 - c0);
       Pb[(size_t)(geo.off[l] + node) * D + e] = v;
       buf[cur ^ 1][i][e] = v;
     }
@@ -116,9 +119,11 @@ __global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __rest
     for (int idx = threadIdx.x; idx < m * D; idx += THREADS) {
       const int node = idx / D, e = idx % D;
       const int c0 = 2 * node, c1 = min(2 * node + 2, geo.M[l - 1]);
-      double s = 0.0;
-      for (int c = c0; c < c1; ++c) s += (double)bf16_to_f32(Pb[(size_t)(geo.off[l - 1] + c) * D + e]);
-      Pb[(size_t)(geo.off[l] + node) * D + e] = f64_to_bf16_rne(s / (double)(c1 - c0));
+      const float a = bf16_to_f32(Pb[(size_t)(geo.off[l - 1] + c0) * D + e]);
+      const float b = c1 - c0 > 1 ? bf16_to_f32(Pb[(size_t)(geo.off[l - 1] + c0 + 1) * D + e]) : 0.f;
+      float s, err;
+      two_sum(a, b, s, err);
+      Pb[(size_t)(geo.off[l] + node) * D + e] = bf16_mean(s, err, c1 - c0);
     }
     __syncthreads();
   }

@@ -30,11 +30,12 @@ __device__ __forceinline__ float lse2_pair(float a, float b) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(THREADS) stage1_kernel(const uint16_t* __restrict__ Q,
+__global__ void __launch_bounds__(THREADS, D == 128 ? 2 : 3) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
                                                          float scale_log2, Geometry geo) {
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
+  constexpr int NB = 2;        // n-tiles (8 children each) whose loads are in flight together
   __shared__ int lists[THREADS / 32][32];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -86,14 +87,24 @@ __global__ void __launch_bounds__(THREADS) stage1_kernel(const uint16_t* __restr
       const long long cspan = 64LL << (l - 2);
       const long long lvl_off = geo.off[l - 1];
       const int Mc = geo.M[l - 1];
-      float u[8];
+      // start every child row of this level on its way to L1 before the batched loads, so
+      // the level costs one memory round trip instead of one per batch
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 kv[4][NCH];
-        bool valid[4];
+      for (int nt = 0; nt < 8; ++nt) {
+        const int ci = 4 * nt + (r >> 1);
+        const int cnode = __shfl_sync(0xffffffffu, cand, ci);
+        const int child = 2 * cnode + (r & 1);
+        const bool valid = ci < nc && child < Mc && (!causal || (long long)child * cspan <= t);
+        if (valid && 64 * (q >> 1) < D && (q & 1) == 0) prefetch_l1(Pb + (size_t)(lvl_off + child) * D + 64 * (q >> 1));
+      }
+      float my = NEG_INF;  // score of candidate `lane`
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int nt = half * 4 + k;
+      for (int half = 0; half < 8 / NB; ++half) {
+        uint4 kv[NB][NCH];
+        bool valid[NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+          const int nt = half * NB + k;
           const int ci = 4 * nt + (r >> 1);
           const int cnode = __shfl_sync(0xffffffffu, cand, ci);
           const int child = 2 * cnode + (r & 1);
@@ -103,7 +114,7 @@ __global__ void __launch_bounds__(THREADS) stage1_kernel(const uint16_t* __restr
           for (int j = 0; j < NCH; ++j) kv[k][j] = valid[k] ? ldg16(prow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < NB; ++k) {
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
@@ -123,15 +134,10 @@ __global__ void __launch_bounds__(THREADS) stage1_kernel(const uint16_t* __restr
           part += __shfl_xor_sync(0xffffffffu, part, 4);
           part += __shfl_xor_sync(0xffffffffu, part, 8);
           part += __shfl_xor_sync(0xffffffffu, part, 16);
-          u[half * 4 + k] = v0 ? part : NEG_INF;
+          // candidate 4nt+q's score to lane 4nt+q (lanes hold one candidate each)
+          const float val = __shfl_sync(0xffffffffu, v0 ? part : NEG_INF, lane & 3);
+          if ((lane >> 2) == half * NB + k) my = val;
         }
-      }
-      // candidate i's score to lane i
-      float my = NEG_INF;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const float v = __shfl_sync(0xffffffffu, u[nt], lane & 3);
-        if ((lane >> 2) == nt) my = v;
       }
       if (lane >= nc) my = NEG_INF;
       // SelectK: rank by (score desc, index asc)

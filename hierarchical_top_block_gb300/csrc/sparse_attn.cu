@@ -7,20 +7,22 @@
 // The G_Q heads of one query share the selected blocks, so one warp owns one query: its
 // G_Q rows (padded to 16) form the M = 16 side of m16n8k16 MMAs; different queries
 // select different blocks, so there is no larger dense tile without wasted work.  The
-// kernel is bound by moving the selected K/V blocks (16 KB each at d = 128) into the SM:
-// each warp runs its own ring of TMA-filled shared-memory slots (128-byte swizzle, one
-// 3-D box per block; rows past N read as zero) that keeps two blocks in flight ahead of
-// the one being multiplied, across query boundaries.  S = Q K^T and O += P V use ldmatrix
-// (.trans for V) on the swizzled slots; the softmax is online (running max and sum per
-// head row) in the exp2 domain.  All waits are bounded.
+// kernel is bound by moving the selected K/V blocks into the SM.  Each of the 8 warps of a
+// CTA runs its own ring of 3 shared-memory slots filled by TMA (one 4-D box per 32-key
+// half block: rows x both 64-column halves of d, 128-byte swizzle, rows past N read as
+// zero); the ring keeps two loads in flight ahead of the one being multiplied, across
+// block and query boundaries, and skips half blocks that hold no visible key.
+// S = Q K^T and O += P V use ldmatrix (.trans for V) on the swizzled slots; the softmax is
+// online in the exp2 domain, and the O rescale is skipped when no row maximum moved.
+// All waits are bounded.
 #include "kernels.cuh"
 
 namespace pisa {
 namespace {
 
-constexpr int NW = 4;       // warps per CTA, one query each
-constexpr int NSLOT = 3;    // ring slots per warp (K and V blocks alternate)
-
+constexpr int NW = 8;       // warps per CTA, one query each
+constexpr int NSLOT = 3;    // ring slots per warp
+constexpr int KS = 32;      // keys per slot (half a block)
 
 struct AttnParams {
   const uint16_t* Q;
@@ -29,34 +31,52 @@ struct AttnParams {
   float* LSE;
   long long total;  // B * H_kv * N
   int N, H_q, H_kv, GQ, Ksel, M1, causal;
+  int one_box;      // 1: the 4-D map loads both d halves in one box
   float sl2;
 };
 
-// Walks the (query, selected block, K|V) load sequence of one warp.
+// Walks the (query, selected block, half block, K|V) load sequence of one warp.
 struct Cursor {
   long long item;   // current (bh, t) item, or >= total when exhausted
   unsigned mask;    // remaining valid idx positions of the item
   int val;          // this lane's idx entry of the item
-  int kv;           // 0: K of the lowest remaining block next, 1: its V
+  int t;            // query position of the item
+  int blk, nsub, sub, kv;
 };
+
+__device__ __forceinline__ int half_blocks(const AttnParams& p, int blk, int t) {
+  const long long last = p.causal ? (long long)min(t, p.N - 1) : (long long)p.N - 1;
+  long long cnt = last - (long long)blk * 64 + 1;
+  if (cnt > 64) cnt = 64;
+  return (int)((cnt + KS - 1) / KS);
+}
+
+__device__ __forceinline__ void first_block(Cursor& c, const AttnParams& p) {
+  c.sub = 0;
+  c.kv = 0;
+  if (c.mask) {
+    c.blk = __shfl_sync(0xffffffffu, c.val, __ffs(c.mask) - 1);
+    c.nsub = half_blocks(p, c.blk, c.t);
+  }
+}
 
 __device__ __forceinline__ void load_item(Cursor& c, const AttnParams& p, long long item, uint32_t* err) {
   const int lane = threadIdx.x & 31;
   c.item = item;
-  c.kv = 0;
   c.val = -1;
   c.mask = 0;
   if (item >= p.total) return;
-  const int t = (int)(item % p.N);
+  c.t = (int)(item % p.N);
   int v = lane < p.Ksel ? p.idx[item * p.Ksel + lane] : -1;
   if (v >= p.M1) {
     report_error(err, ERR_BAD_INDEX);
     v = -1;
   }
   // a block that starts after t has no visible key: skip it
-  if (v >= 0 && p.causal && (long long)v * 64 > t) v = -1;
+  if (v >= 0 && p.causal && (long long)v * 64 > c.t) v = -1;
   c.val = v;
   c.mask = __ballot_sync(0xffffffffu, v >= 0);
+  first_block(c, p);
 }
 
 template <int D>
@@ -64,9 +84,10 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap mapV,
                                                                  AttnParams p, uint32_t* err) {
   constexpr int HALVES = D / 64;
-  constexpr uint32_t SLOT = 64 * D * 2;
-  constexpr int KST = D / 16;        // k-steps of Q K^T
-  constexpr int NDT = D / 8;         // n-tiles of P V
+  constexpr uint32_t SLOT = KS * D * 2;
+  constexpr uint32_t HALF = KS * 128;  // bytes of one 64-column half of a slot
+  constexpr int KST = D / 16;          // k-steps of Q K^T
+  constexpr int NDT = D / 8;           // n-tiles of P V
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[NW][NSLOT];
@@ -86,33 +107,38 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   // ---- producer side of this warp's ring ----
   Cursor pc;
   load_item(pc, p, gw, err);
-  long long issued = 0, consumed = 0;
-  auto advance = [&](Cursor& c) {
-    if (c.kv == 0) {
-      c.kv = 1;
-      return;
-    }
-    c.kv = 0;
-    c.mask &= c.mask - 1;
-    while (c.mask == 0 && c.item < p.total) load_item(c, p, c.item + nwarps, err);
-  };
   while (pc.mask == 0 && pc.item < p.total) load_item(pc, p, pc.item + nwarps, err);
+  long long issued = 0, consumed = 0;
   auto issue_until = [&](long long limit) {
     while (issued < limit && pc.item < p.total) {
       const int slot = (int)(issued % NSLOT);
-      const int pos = __ffs(pc.mask) - 1;
-      const int blk = __shfl_sync(0xffffffffu, pc.val, pos);
       const int bh = (int)(pc.item / p.N);
+      const int row = pc.blk * 64 + pc.sub * KS;
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&full[warp][slot], SLOT);
         const CUtensorMap* m = pc.kv == 0 ? &mapK : &mapV;
+        uint8_t* dst = ring + slot * SLOT;
+        if (p.one_box) {
+          asm volatile(
+              "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+              "%6}], [%2];" ::"r"(smem_u32(dst)),
+              "l"((uint64_t)m), "r"(smem_u32(&full[warp][slot])), "r"(0), "r"(row), "r"(0), "r"(bh)
+              : "memory");
+        } else {
 #pragma unroll
-        for (int h = 0; h < HALVES; ++h) tma_load_3d(ring + slot * SLOT + h * (64 * 128), m, &full[warp][slot], 64 * h, blk * 64, bh);
+          for (int h = 0; h < HALVES; ++h) tma_load_3d(dst + h * HALF, m, &full[warp][slot], 64 * h, row, bh);
+        }
       }
       ++issued;
-      advance(pc);
+      // advance: K then V of each half block, half blocks of each block, blocks of each item
+      pc.kv ^= 1;
+      if (pc.kv == 0 && ++pc.sub == pc.nsub) {
+        pc.mask &= pc.mask - 1;
+        first_block(pc, p);
+        while (pc.mask == 0 && pc.item < p.total) load_item(pc, p, pc.item + nwarps, err);
+      }
     }
   };
   issue_until(NSLOT);
@@ -141,24 +167,24 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
 
-    for (unsigned mask = cc.mask; mask && ok; mask &= mask - 1) {
-      const int blk = __shfl_sync(0xffffffffu, cc.val, __ffs(mask) - 1);
-      // ---------------- S = Q K^T over the block's 64 keys ----------------
+    while (cc.mask && ok) {
+      const long long kbase = (long long)cc.blk * 64 + cc.sub * KS;
+      // ---------------- S = Q K^T over KS keys ----------------
       int slot = (int)(consumed % NSLOT);
       if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) {
         ok = false;
         break;
       }
       const uint32_t kb = smem_u32(ring + slot * SLOT);
-      float s[8][4];
+      float s[KS / 8][4];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < KS / 8; ++nt) {
         s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
         const int key = 8 * nt + (lane & 7);
 #pragma unroll
         for (int kp = 0; kp < KST / 2; ++kp) {
           const int d0 = 32 * kp + 8 * (lane >> 3);
-          const uint32_t addr = kb + (d0 >> 6) * (64 * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          const uint32_t addr = kb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(addr, b0, b1, b2, b3);
           mma_bf16_16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
@@ -169,10 +195,9 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       issue_until(consumed + NSLOT);
 
       // ---------------- online softmax (log2 domain) ----------------
-      const long long kbase = (long long)blk * 64;
       float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < KS / 8; ++nt) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const long long key = kbase + 8 * nt + 2 * q + c;
@@ -188,22 +213,24 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-      const float c0 = nm0 == NEG_INF ? 1.f : fast_exp2(m0 - nm0);
-      const float c1 = nm1 == NEG_INF ? 1.f : fast_exp2(m1 - nm1);
+      const float c0 = (nm0 == NEG_INF || nm0 == m0) ? 1.f : fast_exp2(m0 - nm0);
+      const float c1 = (nm1 == NEG_INF || nm1 == m1) ? 1.f : fast_exp2(m1 - nm1);
       m0 = nm0;
       m1 = nm1;
-      l0 *= c0;
-      l1 *= c1;
+      if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+        l0 *= c0;
+        l1 *= c1;
 #pragma unroll
-      for (int i = 0; i < NDT; ++i) {
-        o[i][0] *= c0;
-        o[i][1] *= c0;
-        o[i][2] *= c1;
-        o[i][3] *= c1;
+        for (int i = 0; i < NDT; ++i) {
+          o[i][0] *= c0;
+          o[i][1] *= c0;
+          o[i][2] *= c1;
+          o[i][3] *= c1;
+        }
       }
-      uint32_t pa[4][4];
+      uint32_t pa[KS / 16][4];
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < KS / 8; ++nt) {
         const float p00 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][0] - m0);
         const float p01 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][1] - m0);
         const float p10 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][2] - m1);
@@ -223,12 +250,12 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       }
       const uint32_t vb = smem_u32(ring + slot * SLOT);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+      for (int kk = 0; kk < KS / 16; ++kk) {
         const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
         for (int np = 0; np < NDT / 2; ++np) {
           const int d0 = 8 * (2 * np + (lane >> 4));
-          const uint32_t addr = vb + (d0 >> 6) * (64 * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          const uint32_t addr = vb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4_trans(addr, b0, b1, b2, b3);
           mma_bf16_16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
@@ -237,6 +264,11 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       }
       ++consumed;
       issue_until(consumed + NSLOT);
+      // next half block / block
+      if (++cc.sub == cc.nsub) {
+        cc.mask &= cc.mask - 1;
+        first_block(cc, p);
+      }
     }
     if (!ok) break;
 
@@ -271,13 +303,24 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
 template <int D>
 cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx, uint16_t* O,
                      float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s) {
+  constexpr int HALVES = D / 64;
   CUtensorMap mapK, mapV;
-  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.N, (uint64_t)p.B * p.H_kv};
-  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.N_cap * D * 2};
-  const uint32_t box[3] = {64, 64, 1};
-  if (!encode_tensor_map(&mapK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  if (!encode_tensor_map(&mapV, V, 3, dims, strides, box)) return cudaErrorInvalidValue;
   AttnParams prm;
+  // one box per half block: dims (64 columns, rows, d half, b*h_kv); the d-half dimension is
+  // outermost in shared memory, giving two consecutive 128-byte-swizzled tiles
+  {
+    const uint64_t dims[4] = {64, (uint64_t)p.N, (uint64_t)HALVES, (uint64_t)p.B * p.H_kv};
+    const uint64_t strides[3] = {(uint64_t)D * 2, 128, (uint64_t)p.N_cap * D * 2};
+    const uint32_t box[4] = {64, (uint32_t)KS, (uint32_t)HALVES, 1};
+    prm.one_box = encode_tensor_map(&mapK, K, 4, dims, strides, box) && encode_tensor_map(&mapV, V, 4, dims, strides, box);
+  }
+  if (!prm.one_box) {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.N, (uint64_t)p.B * p.H_kv};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.N_cap * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)KS, 1};
+    if (!encode_tensor_map(&mapK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_tensor_map(&mapV, V, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   prm.Q = Q;
   prm.idx = idx;
   prm.O = O;
@@ -292,7 +335,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, co
   prm.causal = p.causal;
   prm.sl2 = p.scale * LOG2E;
   if (prm.total == 0) return cudaSuccess;
-  const size_t smem = (size_t)NW * NSLOT * 64 * D * 2 + 1024;
+  const size_t smem = (size_t)NW * NSLOT * KS * D * 2 + 1024;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   long long blocks = (prm.total + NW - 1) / NW;

@@ -36,6 +36,27 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
 
 
+def level_sizes(n, C=64):
+    out = []
+    m = (n + C - 1) // C
+    while m >= 1:
+        out.append(m)
+        if m == 1:
+            break
+        m = (m + 1) // 2
+    return out if n > 0 else []
+
+
+def pyramid_equal(P_gpu, P_ref, n, n_cap):
+    """Compare the rows that hold the pyramid of n tokens inside an n_cap layout [nodes, d]."""
+    off = 0
+    for l, (m, mcap) in enumerate(zip(level_sizes(n) + [0] * 64, level_sizes(n_cap))):
+        if m and not np.array_equal(P_gpu[off:off + m], P_ref[off:off + m]):
+            return False
+        off += mcap
+    return True
+
+
 def check_selection(o, Qb, Kb, Pb, K_sel, rows, gpu_idx, gpu_s2=None, gpu_score=None, causal=True):
     """rows: int64 [R, 3] (b, h_kv, t); gpu_*: arrays [R, ...].  Returns a small report dict."""
     ref = o.select(Qb, Kb, Pb, K_sel, rows, causal=causal)
@@ -55,7 +76,8 @@ def check_selection(o, Qb, Kb, Pb, K_sel, rows, gpu_idx, gpu_s2=None, gpu_score=
     if gpu_score is not None and gpu_s2 is not None:
         same_s2 = np.all(ref["s2"] == gpu_s2, axis=1)
         valid = (ref["cand"] >= 0) & same_s2[:, None]
-        diff = np.abs(np.where(valid, gpu_score - ref["cand_score"], 0.0))
+        with np.errstate(invalid="ignore"):
+            diff = np.abs(np.where(valid, gpu_score - ref["cand_score"], 0.0))
         assert diff.max() <= SCORE_TOL, f"leaf score differs by {diff.max()}"
     return dict(rows=len(rows), ambiguous=int(amb.size), clear=int(clear.sum()))
 

@@ -165,7 +165,7 @@ def _decode_check(o, w, N0, steps, N_cap, pairs=None):
         kc[0, 0, :N0] = W.bits(W.kv_slice(wk, "K", b, g))
         vc[0, 0, :N0] = W.bits(W.kv_slice(wk, "V", b, g))
         pc = o.build_pyramid(kc, N=N0)
-        assert np.array_equal(W.bits(Pc[b, g]), pc[0, 0]), "initial pyramid cache differs"
+        assert H.pyramid_equal(W.bits(Pc[b, g]), pc[0, 0], N0, N_cap), "initial pyramid cache differs"
         ref[(b, g)] = [kc, vc, pc, np.array([N0], np.int32)]
     for s in range(steps):
         q, k, v = W.decode_step_inputs(w, s, "cuda")
@@ -180,7 +180,7 @@ def _decode_check(o, w, N0, steps, N_cap, pairs=None):
             T = int(sl[0])
             ro, rl, ri = o.decode_step(qn[b:b + 1, g * G:(g + 1) * G].copy(), kn[b:b + 1, g:g + 1].copy(),
                                        vn[b:b + 1, g:g + 1].copy(), kc, vc, pc, sl, K_sel)
-            assert np.array_equal(W.bits(Pc[b, g]), pc[0, 0]), f"pyramid cache differs at step {s}, pair {(b, g)}"
+            assert H.pyramid_equal(W.bits(Pc[b, g]), pc[0, 0], T + 1, N_cap), f"pyramid cache differs at step {s}, pair {(b, g)}"
             gi = idx[b, g].cpu().numpy()
             if not np.array_equal(gi, ri[0, 0]):
                 n = T + 1
