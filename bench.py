@@ -1,0 +1,439 @@
+"""Benchmark of the PISA prefill hot path (pyramid + block selection + sparse attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pisa|reference] [--workload NAME]
+
+One step = one pass of the whole hot path over one batch of synthetic input: build the
+key pyramid, select blocks for every query (level walk, exact leaf LSE, top-K) and attend
+over the selected blocks.  The default workload is the selection-scale prefill
+(N = 262144 tokens, H_q = 16, H_kv = 1, d = 128, C = 64, g = 2, K = 16); its inputs (1.2 GB)
+are resident in HBM and larger than the 129 MB L2, so no flush is needed between steps.
+
+Under torchrun every rank runs its own replica on its own GPU (the path has no exchange
+step: weak scaling); the timed region is bracketed by a barrier and a synchronize, and
+rank 0 prints one JSON line with the maximum time over ranks.
+
+--impl reference times the CPU oracle (the plain statement of the method used by the
+tests) on a bounded sample of the same workload; only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (select + sparse attn)"
+UNIT = "tokens/s"
+KERNELS_PER_STEP = 12  # pyramid 2, stage 1, clustering 6, leaf LSE, top-K, attention
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="pisa", choices=["pisa", "reference"])
+    ap.add_argument("--workload", default="prefill_256k")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-secondary", action="store_true", help="skip the 32K prefill and decode measurements")
+    ap.add_argument("--cpu-sample-rows", type=int, default=32768)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ------------------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of the ranks' values (every rank gets it)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# algorithmic work of the attention step (counted from the realised selection)
+# ------------------------------------------------------------------------------------
+def attention_flops(idx, N, H_q, H_kv, d, C=64):
+    """4 d flops (QK^T and PV) per visible (query head, key) pair of the selected blocks."""
+    import torch
+
+    t = torch.arange(N, device=idx.device, dtype=torch.int64).view(1, 1, N, 1)
+    j = idx.to(torch.int64)
+    vis = torch.clamp(t - j * C + 1, min=0, max=C) * (j >= 0)
+    keys_per_group_query = vis.sum().item()  # over (b, h_kv, t)
+    return 4.0 * d * keys_per_group_query * (H_q // H_kv)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], tensor=p["bf16_tflops"], tensor_sustained=p.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, tensor=1900.0, tensor_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------------------------
+# the GPU path
+# ------------------------------------------------------------------------------------
+def run_pisa(args):
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+    import workloads as W
+
+    from hierarchical_top_block_gb300.build import build
+
+    build()  # no-op when the library is current
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    backend = "nccl" if world > 1 else "gloo"
+    init_dist(backend)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    assert w.decode_steps == 0, "the timed step is a prefill workload"
+
+    Q, K, V = W.prefill_inputs(w, dev)
+    P = torch.empty(w.B, w.H_kv, pisa.pisa_pyramid_nodes(w.N), w.d, dtype=torch.bfloat16, device=dev)
+    shape = pisa.make_shape(w.B, w.N, w.H_q, w.H_kv, w.d)
+    params = pisa.make_params(w.K)
+    ws = torch.empty(pisa.pisa_select_workspace_bytes(shape, params), dtype=torch.uint8, device=dev)
+    idx = torch.empty(w.B, w.H_kv, w.N, w.K, dtype=torch.int32, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(w.B, w.H_q, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(marks=None):
+        if marks is not None:
+            marks[0].record(stream)
+        pisa.pisa_build_pyramid(K, P=P)
+        pisa.pisa_select_prefill(Q, K, P, w.K, ws=ws, idx=idx)
+        if marks is not None:
+            marks[1].record(stream)
+        pisa.pisa_sparse_attn_prefill(Q, K, V, idx, O=O, LSE=LSE)
+        if marks is not None:
+            marks[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pisa.pisa_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    marks = [[ev(), ev(), ev()] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(marks[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    err = pisa.pisa_get_last_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error word {err} during the timed region")
+    ms_local = t0.elapsed_time(t1) / args.steps
+    ms = max_over_ranks(ms_local, world, dev if backend == "nccl" else None)
+    sel_ms = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
+    att_ms = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
+    tokens = w.B * w.N
+    value = tokens * world / (ms * 1e-3)
+
+    flops = attention_flops(idx, w.N, w.H_q, w.H_kv, w.d)
+    pk = peaks()
+    achieved_tf = flops / (att_ms * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; block-mean key offsets)",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "C": w.C,
+                   "g": w.g, "K": w.K, "causal": True, "parallelism": f"replicas x{world}",
+                   "l2": "inputs (1.2 GB) larger than L2, no flush"},
+        "breakdown_ms": {"pyramid+selection": sel_ms, "sparse_attention": att_ms},
+        "selection_only_tokens_per_s": tokens * world / (sel_ms * 1e-3),
+        "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": achieved_tf,
+                     "peak": pk["tensor"], "unit": "TFLOP/s", "frac": achieved_tf / pk["tensor"],
+                     "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "peak_source": pk["source"] + " bf16 dense burst"},
+        "clocks": clk,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+    }
+    if rank == 0:
+        out["e2e"] = run_e2e(args, w, dev)
+        if not args.no_secondary:
+            out["secondary"] = {"prefill_32k": secondary_prefill(W.WORKLOADS["prefill_32k"], dev),
+                                "decode_128k": secondary_decode(W.WORKLOADS["decode_128k"], dev)}
+        out["cpu_baseline"] = cpu_baseline(args, w)
+        print(json.dumps(out), flush=True)
+    barrier(world)
+
+
+def run_e2e(args, w, dev):
+    """Same metric through the host-buffer entry point: H2D of Q, K, V and D2H of O and LSE
+    inside the timed region, every step."""
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+    import workloads as W
+
+    Qh = W.make_q(w, dev).cpu().pin_memory()
+    Kh = W.make_kv(w, "K", dev).cpu().pin_memory()
+    Vh = W.make_kv(w, "V", dev).cpu().pin_memory()
+    Oh = torch.empty_like(Qh).pin_memory()
+    Lh = torch.empty(w.B, w.H_q, w.N, dtype=torch.float32).pin_memory()
+    shape = pisa.make_shape(w.B, w.N, w.H_q, w.H_kv, w.d)
+    params = pisa.make_params(w.K)
+    dws = torch.empty(pisa.pisa_prefill_host_workspace_bytes(shape, params), dtype=torch.uint8, device=dev)
+    pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, dev_ws=dws, O_host=Oh, LSE_host=Lh, device=dev.index)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, dev_ws=dws, O_host=Oh, LSE_host=Lh, device=dev.index)
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    h2d = Qh.numel() * 2 + Kh.numel() * 2 + Vh.numel() * 2
+    d2h = Oh.numel() * 2 + Lh.numel() * 4
+    return {"value": w.B * w.N / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": dt * 1e3, "steps": args.e2e_steps, "api": "pisa_prefill_host (pinned host buffers)"}
+
+
+def secondary_prefill(w, dev, steps=5):
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+    import workloads as W
+
+    Q, K, V = W.prefill_inputs(w, dev)
+    P = pisa.pisa_build_pyramid(K)
+    shape = pisa.make_shape(w.B, w.N, w.H_q, w.H_kv, w.d)
+    ws = torch.empty(pisa.pisa_select_workspace_bytes(shape, pisa.make_params(w.K)), dtype=torch.uint8, device=dev)
+    idx = torch.empty(w.B, w.H_kv, w.N, w.K, dtype=torch.int32, device=dev)
+    O = torch.empty_like(Q)
+    L = torch.empty(w.B, w.H_q, w.N, dtype=torch.float32, device=dev)
+
+    def step():
+        pisa.pisa_build_pyramid(K, P=P)
+        pisa.pisa_select_prefill(Q, K, P, w.K, ws=ws, idx=idx)
+        pisa.pisa_sparse_attn_prefill(Q, K, V, idx, O=O, LSE=L)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms_per_step": ms, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv}
+
+
+def secondary_decode(w, dev, steps=32, warmup=3):
+    """Batched decode: per-step latency of the fused decode kernel over all 64 sequences."""
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+    import workloads as W
+
+    N_cap = w.N + warmup + steps
+    Kc = torch.empty(w.B, w.H_kv, N_cap, w.d, dtype=torch.bfloat16, device=dev)
+    Vc = torch.empty_like(Kc)
+    for b in range(w.B):
+        for g in range(w.H_kv):
+            Kc[b, g, :w.N] = W.kv_slice(w, "K", b, g, device=dev)
+            Vc[b, g, :w.N] = W.kv_slice(w, "V", b, g, device=dev)
+    Pc = pisa.pisa_build_pyramid(Kc, N=w.N)
+    seq = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+    ins = [W.decode_step_inputs(w, s, dev) for s in range(warmup + steps)]
+    o = torch.empty(w.B, w.H_q, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H_q, dtype=torch.float32, device=dev)
+    for s in range(warmup):
+        pisa.pisa_decode_step(*ins[s], Kc, Vc, Pc, seq, w.K, o=o, lse=lse)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s in range(steps):
+        evs[s][0].record()
+        pisa.pisa_decode_step(*ins[warmup + s], Kc, Vc, Pc, seq, w.K, o=o, lse=lse)
+        evs[s][1].record()
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    del Kc, Vc, Pc
+    torch.cuda.empty_cache()
+    return {"step_us_mean": statistics.mean(us), "step_us_p50": us[len(us) // 2], "steps": steps,
+            "B": w.B, "cached_tokens": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "note": "steps 3..34 of 256"}
+
+
+# ------------------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+# ------------------------------------------------------------------------------------
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: the full pyramid, plus selection
+    and attention for a set of query positions spread over the sequence.  Inputs are
+    generated once (seeded, on the CPU); each run() is timed on its own."""
+
+    def __init__(self, w, max_rows, seed=7):
+        import numpy as np
+
+        import oracle
+        import workloads as W
+
+        self.w = w
+        self.o = oracle.Oracle()
+        self.Kb = W.bits(W.make_kv(w, "K", "cpu"))
+        self.Vb = W.bits(W.make_kv(w, "V", "cpu"))
+        rng = np.random.default_rng(seed)
+        self.ts_all = rng.permutation(w.N)[:max_rows].astype(np.int64)
+        self.Qb = np.zeros((w.B, w.N, w.H_q, w.d), np.uint16)
+        self.Qb[0, self.ts_all] = W.bits(W.q_rows(w, 0, self.ts_all))
+
+    def run(self, rows_n, offset=0):
+        import numpy as np
+
+        w = self.w
+        ts = np.sort(self.ts_all[offset:offset + rows_n])
+        t0 = time.perf_counter()
+        P = self.o.build_pyramid(self.Kb)
+        rows = np.stack([np.zeros_like(ts), np.zeros_like(ts), ts], 1)
+        sel = self.o.select(self.Qb, self.Kb, P, w.K, rows)
+        idx = np.full((w.B, w.H_kv, w.N, w.K), -1, np.int32)
+        idx[0, 0, ts] = sel["idx"]
+        self.o.sparse_attention(self.Qb, self.Kb, self.Vb, idx, np.stack([np.zeros_like(ts), ts], 1))
+        dt = time.perf_counter() - t0
+        return len(ts) / dt, dt
+
+
+def cpu_baseline(args, w):
+    try:
+        tps, dt = OracleSample(w, args.cpu_sample_rows).run(args.cpu_sample_rows)
+    except Exception as e:  # the baseline is informational
+        return {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "error": str(e)}
+    return {"value": tps, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"full pyramid + selection and attention for {args.cpu_sample_rows} query positions of "
+                      f"{w.name} (N={w.N}), {dt:.1f} s wall on {os.cpu_count()} threads"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    rows = max(16, args.cpu_sample_rows // 8)
+    sample = OracleSample(w, rows * (args.steps + 1))
+    for _ in range(args.warmup):
+        sample.run(8)
+    vals, dts = [], []
+    for s in range(args.steps):
+        v, dt = sample.run(rows, offset=rows * (s + 1))
+        vals.append(v)
+        dts.append(dt)
+    value = statistics.mean(vals)
+    desc = (f"per step: full pyramid + selection and attention for {rows} query positions of {w.name}, "
+            f"{os.cpu_count()} threads")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": statistics.mean(dts) * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, "B": w.B, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "K": w.K},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pisa(args)
+
+
+if __name__ == "__main__":
+    main()
