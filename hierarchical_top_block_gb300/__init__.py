@@ -59,6 +59,8 @@ def lib() -> ct.CDLL:
         L.pisa_build_pyramid.argtypes = [_P, _P, pisa_shape, pisa_params, _P]
         L.pisa_select_prefill.restype = ct.c_int
         L.pisa_select_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, ct.c_size_t, pisa_shape, pisa_params, _P]
+        L.pisa_select_prefill_noalloc.restype = ct.c_int
+        L.pisa_select_prefill_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
         L.pisa_sparse_attn_prefill.restype = ct.c_int
         L.pisa_sparse_attn_prefill.argtypes = [_P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
         L.pisa_prefill_host.restype = ct.c_int
@@ -173,6 +175,23 @@ def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float =
     if want_s2:
         out.append(s2)
     return out[0] if len(out) == 1 else tuple(out)
+
+
+def pisa_select_prefill_noalloc(Q, K, P, K_sel: int, causal: bool = True, scale: float = 0.0, idx=None,
+                                leaf_score=None, s2=None):
+    """pisa_select_prefill without a caller-supplied workspace: the library's fixed 32 MiB
+    device scratch is used instead (for callers that cannot allocate device memory).
+    Output tensors may be passed in so that the call itself allocates nothing."""
+    for t, n in ((Q, "Q"), (K, "K"), (P, "P")):
+        _bf16(t, n)
+    B, N, H_q, d = Q.shape
+    H_kv = K.shape[1]
+    if idx is None:
+        idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
+    _check(lib().pisa_select_prefill_noalloc(_ptr(Q), _ptr(K), _ptr(P), _ptr(idx), _ptr(leaf_score), _ptr(s2),
+                                             make_shape(B, N, H_q, H_kv, d, N), make_params(K_sel, causal, scale),
+                                             _stream(Q)), "pisa_select_prefill_noalloc")
+    return idx
 
 
 # ---- step 4 -----------------------------------------------------------------------------

@@ -115,6 +115,20 @@ PISA_API pisa_status pisa_select_prefill(const uint16_t* Q, const uint16_t* K, c
                                 float* leaf_score, int32_t* s2, void* ws, size_t ws_bytes, pisa_shape shape,
                                 pisa_params params, pisa_stream stream);
 
+/* pisa_select_prefill for callers that cannot allocate device memory (a host that owns
+ * the allocator, a pool they may not grow, a loop that must not call cudaMalloc).  The
+ * paper has no counterpart: this is a library convenience, not part of the method.
+ * Same arguments and results as pisa_select_prefill minus ws/ws_bytes: the scratch is one
+ * fixed 32 MiB array in device memory that every GPU loading the library holds until the
+ * process exits.  Shapes whose pisa_select_workspace_bytes() exceeds 32 MiB return
+ * PISA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's
+ * address with that device current, so make it before any stream capture.  All calls share
+ * the array (the selection clears what must start at zero): calls that overlap on the GPU
+ * race and must be serialised by the caller.  Allocates nothing. */
+PISA_API pisa_status pisa_select_prefill_noalloc(const uint16_t* Q, const uint16_t* K, const uint16_t* P,
+                                                 int32_t* idx, float* leaf_score, int32_t* s2, pisa_shape shape,
+                                                 pisa_params params, pisa_stream stream);
+
 /* ---- step 4: attention over the selected blocks --------------------------------------- */
 
 /* o_{t,h} = sum over keys c of the selected blocks of head h's group (c <= t if causal) of
