@@ -34,17 +34,38 @@ METRIC = "prefill tokens/s (select + sparse attn)"
 UNIT = "tokens/s"
 KERNELS_PER_STEP = 12  # pyramid 2, stage 1, clustering 6, leaf LSE, top-K, attention
 
+# DRAM traffic of the attention kernel per launch on the 256K prefill (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture, profiles/sparse_attn_kernel_prefill_256k.md), keyed
+# by a hash of the kernel's sources: when the sources change the figure is stale and is reported
+# as null until it is taken again.
+ATTN_TRAFFIC = {"sources_sha256": "57e79de6ef8b132ba9426c7b37ecad7d6d8c6e24520a4d33715cb4150845a4b6",
+                "workload": "prefill_256k", "bytes": 13988103424 + 1100957952}
+ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
+                "hierarchical_top_block_gb300/csrc/kernels.cuh"]
+
+
+def attn_sources_sha256():
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="pisa", choices=["pisa", "reference"])
     ap.add_argument("--workload", default="prefill_256k")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-secondary", action="store_true", help="skip the 32K prefill and decode measurements")
     ap.add_argument("--cpu-sample-rows", type=int, default=32768)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
     return ap.parse_args()
 
 
@@ -96,7 +117,7 @@ class ClockSampler:
         self.lines = []
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -136,15 +157,22 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------
 # algorithmic work of the attention step (counted from the realised selection)
 # ------------------------------------------------------------------------------------
-def attention_flops(idx, N, H_q, H_kv, d, C=64):
-    """4 d flops (QK^T and PV) per visible (query head, key) pair of the selected blocks."""
+def attention_work(idx, N, H_q, H_kv, d, C=64):
+    """Algorithmic work of one attention launch, counted from the realised selection.
+
+    flops: 4 d per visible (query head, key) pair of the selected blocks (QK^T and PV).
+    gather_bytes: the K and V rows of every selected, visible block, once per (query, KV head)
+    group (C keys x d x 2 bytes x 2 tensors per block): what the kernel reads from L2.
+    """
     import torch
 
     t = torch.arange(N, device=idx.device, dtype=torch.int64).view(1, 1, N, 1)
     j = idx.to(torch.int64)
     vis = torch.clamp(t - j * C + 1, min=0, max=C) * (j >= 0)
     keys_per_group_query = vis.sum().item()  # over (b, h_kv, t)
-    return 4.0 * d * keys_per_group_query * (H_q // H_kv)
+    blocks = (vis > 0).sum().item()
+    return {"flops": 4.0 * d * keys_per_group_query * (H_q // H_kv), "gather_bytes": blocks * C * d * 2 * 2,
+            "blocks": blocks}
 
 
 def peaks():
@@ -226,31 +254,37 @@ def run_pisa(args):
     tokens = w.B * w.N
     value = tokens * world / (ms * 1e-3)
 
-    flops = attention_flops(idx, w.N, w.H_q, w.H_kv, w.d)
+    work = attention_work(idx, w.N, w.H_q, w.H_kv, w.d)
+    flops = work["flops"]
     pk = peaks()
     achieved_tf = flops / (att_ms * 1e-3) / 1e12
+    io_bytes = sum(x.numel() * x.element_size() for x in (Q, K, V, O, LSE, P, idx))
+    traffic = ATTN_TRAFFIC["bytes"] if (ATTN_TRAFFIC["sources_sha256"] == attn_sources_sha256()
+                                        and ATTN_TRAFFIC["workload"] == w.name) else None
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; block-mean key offsets)",
         "config": {"workload": w.name, "B": w.B, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d, "C": w.C,
                    "g": w.g, "K": w.K, "causal": True, "parallelism": f"replicas x{world}",
-                   "l2": "inputs (1.2 GB) larger than L2, no flush"},
+                   "l2": f"inputs and outputs ({io_bytes / 1e9:.2f} GB) larger than L2 (129 MB), no flush"},
         "breakdown_ms": {"pyramid+selection": sel_ms, "sparse_attention": att_ms},
         "selection_only_tokens_per_s": tokens * world / (sel_ms * 1e-3),
         "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": achieved_tf,
                      "peak": pk["tensor"], "unit": "TFLOP/s", "frac": achieved_tf / pk["tensor"],
-                     "traffic": None, "algorithmic_flops_per_launch": flops,
-                     "peak_source": pk["source"] + " bf16 dense burst"},
+                     "traffic": traffic, "algorithmic_flops_per_launch": flops,
+                     "peak_source": pk["source"] + " bf16 dense burst",
+                     "l2_gather": {"bytes_per_launch": work["gather_bytes"], "blocks": work["blocks"],
+                                   "achieved_tbs": work["gather_bytes"] / (att_ms * 1e-3) / 1e12}},
         "clocks": clk,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
     }
     if rank == 0:
-        out["e2e"] = run_e2e(args, w, dev)
+        out["e2e"] = None if args.no_e2e else run_e2e(args, w, dev)
         if not args.no_secondary:
             out["secondary"] = {"prefill_32k": secondary_prefill(W.WORKLOADS["prefill_32k"], dev),
                                 "decode_128k": secondary_decode(W.WORKLOADS["decode_128k"], dev)}
-        out["cpu_baseline"] = cpu_baseline(args, w)
+        out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
         print(json.dumps(out), flush=True)
     barrier(world)
 

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
+    const uint64_t keep_policy = l2_evict_last_policy();  // K pairs are reused by later windows
     uint32_t kload = 0;
     int prev_bh = -1, prev_node = -1, ks = 0;
     int next_tile = 0, chunk_end = 0, chunk_base = 0, chunk_e0 = 0;
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           mbar_arrive_expect_tx(&k_full[ks], STAGE_BYTES);
 #pragma unroll
           for (int h = 0; h < HALVES; ++h)
-            tma_load_3d(sK + ks * STAGE_BYTES + h * (KEYS * 128), &mapK, &k_full[ks], 64 * h, node * KEYS, bh);
+            tma_load_3d_hint(sK + ks * STAGE_BYTES + h * (KEYS * 128), &mapK, &k_full[ks], 64 * h, node * KEYS, bh,
+                             keep_policy);
         }
         ++kload;
         prev_bh = bh;
@@ -258,16 +260,29 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       const long long key0 = (long long)leaf * 64;
       const bool leaf_ok = vq && leaf < prm.M1 && (!prm.causal || key0 <= t);
       // keys j <= lim of this leaf are visible (causal: key <= t; always: key < N)
-      long long lim = (long long)prm.N - 1 - key0;
-      if (prm.causal && (long long)t - key0 < lim) lim = (long long)t - key0;
+      long long lim64 = (long long)prm.N - 1 - key0;
+      if (prm.causal && (long long)t - key0 < lim64) lim64 = (long long)t - key0;
+      const int lim = (int)(lim64 < 63 ? lim64 : 63);
       float lse2 = NEG_INF;
       if (leaf_ok && h < prm.GQ) {
-        float s = 0.f;
+        // four independent partial sums; the mask is only needed inside the own block
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        if (lim >= 63) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float x = __uint_as_float(v[j]) * prm.sl2;
-          s += (j <= lim) ? fast_exp2(x) : 0.f;
+          for (int j = 0; j < 64; j += 4) {
+            p0 += fast_exp2(__uint_as_float(v[j]) * prm.sl2);
+            p1 += fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2);
+            p2 += fast_exp2(__uint_as_float(v[j + 2]) * prm.sl2);
+            p3 += fast_exp2(__uint_as_float(v[j + 3]) * prm.sl2);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            p0 += (j <= lim) ? fast_exp2(__uint_as_float(v[j]) * prm.sl2) : 0.f;
+            p1 += (j + 1 <= lim) ? fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2) : 0.f;
+          }
         }
+        const float s = (p0 + p1) + (p2 + p3);
         if (s > 0.f && s < POS_INF) {
           lse2 = fast_log2(s);
         } else {  // logits beyond the fp32 exponent range: subtract the max first

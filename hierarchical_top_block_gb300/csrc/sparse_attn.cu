@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   }
   __syncwarp();
 
+  // K/V blocks are re-read by many queries: keep them in L2; Q and O stream through once
+  const uint64_t keep_policy = l2_evict_last_policy();
+  const uint64_t stream_policy = l2_evict_first_policy();
   const long long gw = (long long)blockIdx.x * NW + warp;
   const long long nwarps = (long long)gridDim.x * NW;
 
@@ -121,14 +124,10 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
         const CUtensorMap* m = pc.kv == 0 ? &mapK : &mapV;
         uint8_t* dst = ring + slot * SLOT;
         if (p.one_box) {
-          asm volatile(
-              "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
-              "%6}], [%2];" ::"r"(smem_u32(dst)),
-              "l"((uint64_t)m), "r"(smem_u32(&full[warp][slot])), "r"(0), "r"(row), "r"(0), "r"(bh)
-              : "memory");
+          tma_load_4d_hint(dst, m, &full[warp][slot], 0, row, 0, bh, keep_policy);
         } else {
 #pragma unroll
-          for (int h = 0; h < HALVES; ++h) tma_load_3d(dst + h * HALF, m, &full[warp][slot], 64 * h, row, bh);
+          for (int h = 0; h < HALVES; ++h) tma_load_3d_hint(dst + h * HALF, m, &full[warp][slot], 64 * h, row, bh, keep_policy);
         }
       }
       ++issued;
@@ -157,10 +156,10 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
 #pragma unroll
     for (int ks = 0; ks < KST; ++ks) {
       const int c0 = 16 * ks + 2 * q;
-      qa[ks][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)r * D + c0) : 0u;
-      qa[ks][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)(r + 8) * D + c0) : 0u;
-      qa[ks][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)r * D + c0 + 8) : 0u;
-      qa[ks][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(qrow + (size_t)(r + 8) * D + c0 + 8) : 0u;
+      qa[ks][0] = r < p.GQ ? ld_b32_hint(qrow + (size_t)r * D + c0, stream_policy) : 0u;
+      qa[ks][1] = r + 8 < p.GQ ? ld_b32_hint(qrow + (size_t)(r + 8) * D + c0, stream_policy) : 0u;
+      qa[ks][2] = r < p.GQ ? ld_b32_hint(qrow + (size_t)r * D + c0 + 8, stream_policy) : 0u;
+      qa[ks][3] = r + 8 < p.GQ ? ld_b32_hint(qrow + (size_t)(r + 8) * D + c0 + 8, stream_policy) : 0u;
     }
     float o[NDT][4];
 #pragma unroll
@@ -178,12 +177,14 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       const uint32_t kb = smem_u32(ring + slot * SLOT);
       float s[KS / 8][4];
 #pragma unroll
-      for (int nt = 0; nt < KS / 8; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        const int key = 8 * nt + (lane & 7);
+      for (int nt = 0; nt < KS / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      // k outer, n-tiles inner: KS/8 independent accumulator chains interleave
 #pragma unroll
-        for (int kp = 0; kp < KST / 2; ++kp) {
-          const int d0 = 32 * kp + 8 * (lane >> 3);
+      for (int kp = 0; kp < KST / 2; ++kp) {
+        const int d0 = 32 * kp + 8 * (lane >> 3);
+#pragma unroll
+        for (int nt = 0; nt < KS / 8; ++nt) {
+          const int key = 8 * nt + (lane & 7);
           const uint32_t addr = kb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(addr, b0, b1, b2, b3);
@@ -282,9 +283,9 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < NDT; ++i) {
       const int col = 8 * i + 2 * q;
-      if (r < p.GQ) *reinterpret_cast<uint32_t*>(orow + (size_t)r * D + col) = pack_bf16x2(o[i][0] * inv0, o[i][1] * inv0);
+      if (r < p.GQ) st_b32_hint(orow + (size_t)r * D + col, pack_bf16x2(o[i][0] * inv0, o[i][1] * inv0), stream_policy);
       if (r + 8 < p.GQ)
-        *reinterpret_cast<uint32_t*>(orow + (size_t)(r + 8) * D + col) = pack_bf16x2(o[i][2] * inv1, o[i][3] * inv1);
+        st_b32_hint(orow + (size_t)(r + 8) * D + col, pack_bf16x2(o[i][2] * inv1, o[i][3] * inv1), stream_policy);
     }
     if (p.LSE && q == 0) {
       const size_t hbase = (size_t)b * p.H_q + (size_t)hk * p.GQ;

@@ -52,8 +52,9 @@ def test_ragged_shapes_all_rows(oracle_impl, N, GQ, H_kv, d, K_sel):
     H.full_prefill_check(oracle_impl, Q, K, V, K_sel, sample=None if rows <= 4096 else 1500, seed=N)
 
 
-def test_non_causal(oracle_impl):
-    w = W.WORKLOADS["tiny"].with_(N=64 * 20 + 7)
+@pytest.mark.parametrize("d,GQ", [(64, 4), (128, 16), (128, 4)])
+def test_non_causal(oracle_impl, d, GQ):
+    w = W.WORKLOADS["tiny"].with_(N=64 * 20 + 7, d=d, H_q=GQ, H_kv=1)
     Q, K, V = _inputs(w)
     H.full_prefill_check(oracle_impl, Q, K, V, 4, causal=False)
 
