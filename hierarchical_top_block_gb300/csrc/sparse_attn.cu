@@ -13,7 +13,10 @@
 // zero); the ring keeps two loads in flight ahead of the one being multiplied, across
 // block and query boundaries, and skips half blocks that hold no visible key.
 // S = Q K^T and O += P V use ldmatrix (.trans for V) on the swizzled slots; the softmax is
-// online in the exp2 domain, and the O rescale is skipped when no row maximum moved.
+// online in the exp2 domain against a lazy reference maximum per row: exact on the first half
+// block, then moved (and O and the running sum rescaled) only when a logit passes it by more
+// than 2^8, so most half blocks need no cross-lane maximum and no rescale.  Keys are masked
+// only in half blocks that reach past the last visible key.
 // All waits are bounded.
 #include "kernels.cuh"
 
@@ -23,6 +26,7 @@ namespace {
 constexpr int NW = 8;       // warps per CTA, one query each
 constexpr int NSLOT = 3;    // ring slots per warp
 constexpr int KS = 32;      // keys per slot (half a block)
+constexpr float RESCALE_MARGIN = 8.f;  // exp2 headroom before O and l are rescaled (P <= 2^8)
 
 struct AttnParams {
   const uint16_t* Q;
@@ -32,7 +36,8 @@ struct AttnParams {
   long long total;  // B * H_kv * N
   int N, H_q, H_kv, GQ, Ksel, M1, causal;
   int one_box;      // 1: the 4-D map loads both d halves in one box
-  float sl2;
+  float sl2;     // softmax scale x log2(e)
+  float margin;  // RESCALE_MARGIN / sl2: headroom of the reference maximum in raw logit units
 };
 
 // Walks the (query, selected block, half block, K|V) load sequence of one warp.
@@ -149,6 +154,16 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
     Cursor cc;
     load_item(cc, p, item, nullptr);
+    {  // move the next item's selection row and Q rows towards L2 while this one runs
+      const long long nitem = item + nwarps;
+      if (nitem < p.total) {
+        const int nbh = (int)(nitem / p.N), nt = (int)(nitem - (long long)nbh * p.N);
+        const int nb = nbh / p.H_kv, nhk = nbh - nb * p.H_kv;
+        const uint16_t* nq = p.Q + (((size_t)nb * p.N + nt) * p.H_q + (size_t)nhk * p.GQ) * D;
+        if (lane * 64 < p.GQ * D) prefetch_l2(nq + (size_t)lane * 64);  // 128 bytes per lane
+        if (lane == 31) prefetch_l2(p.idx + nitem * p.Ksel);
+      }
+    }
 
     // Q fragments (rows r, r+8 of the group; zero past G_Q)
     uint32_t qa[KST][4];
@@ -164,10 +179,14 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     float o[NDT][4];
 #pragma unroll
     for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    // m0/m1: reference row maxima in raw logit units (exact after the first half block, then
+    // raised only when a logit passes them by more than RESCALE_MARGIN in the exp2 domain)
     float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+    float th0 = NEG_INF, th1 = NEG_INF;  // rescale thresholds m + margin / sl2
+    const int last = p.causal ? min(t, p.N - 1) : p.N - 1;  // last visible key
 
     while (cc.mask && ok) {
-      const long long kbase = (long long)cc.blk * 64 + cc.sub * KS;
+      const int kbase = cc.blk * 64 + cc.sub * KS;
       // ---------------- S = Q K^T over KS keys ----------------
       int slot = (int)(consumed % NSLOT);
       if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) {
@@ -178,47 +197,63 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       float s[KS / 8][4];
 #pragma unroll
       for (int nt = 0; nt < KS / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      // k outer, n-tiles inner: KS/8 independent accumulator chains interleave
+      // per 32 columns of d: all n-tiles' fragments first, then two rounds of independent MMAs
 #pragma unroll
       for (int kp = 0; kp < KST / 2; ++kp) {
         const int d0 = 32 * kp + 8 * (lane >> 3);
+        uint32_t bk[KS / 8][4];
 #pragma unroll
         for (int nt = 0; nt < KS / 8; ++nt) {
           const int key = 8 * nt + (lane & 7);
           const uint32_t addr = kb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(addr, b0, b1, b2, b3);
-          mma_bf16_16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
-          mma_bf16_16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+          ldmatrix_x4(addr, bk[nt][0], bk[nt][1], bk[nt][2], bk[nt][3]);
         }
+#pragma unroll
+        for (int nt = 0; nt < KS / 8; ++nt)
+          mma_bf16_16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], bk[nt][0], bk[nt][1]);
+#pragma unroll
+        for (int nt = 0; nt < KS / 8; ++nt)
+          mma_bf16_16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], bk[nt][2],
+                         bk[nt][3]);
       }
       ++consumed;
       issue_until(consumed + NSLOT);
 
-      // ---------------- online softmax (log2 domain) ----------------
-      float mx0 = NEG_INF, mx1 = NEG_INF;
+      // ---------------- online softmax (exp2 domain, lazy reference maximum) ----------------
+      if (kbase + KS - 1 > last) {  // the half block holds invisible keys: mask them
 #pragma unroll
-      for (int nt = 0; nt < KS / 8; ++nt) {
+        for (int nt = 0; nt < KS / 8; ++nt) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const long long key = kbase + 8 * nt + 2 * q + c;
-          const bool vis = key < p.N && (!p.causal || key <= t);
-          s[nt][c] = vis ? s[nt][c] * p.sl2 : NEG_INF;
-          s[nt][2 + c] = vis ? s[nt][2 + c] * p.sl2 : NEG_INF;
-          mx0 = fmaxf(mx0, s[nt][c]);
-          mx1 = fmaxf(mx1, s[nt][2 + c]);
+          for (int c = 0; c < 2; ++c) {
+            const bool vis = kbase + 8 * nt + 2 * q + c <= last;
+            s[nt][c] = vis ? s[nt][c] : NEG_INF;
+            s[nt][2 + c] = vis ? s[nt][2 + c] : NEG_INF;
+          }
         }
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-      const float c0 = (nm0 == NEG_INF || nm0 == m0) ? 1.f : fast_exp2(m0 - nm0);
-      const float c1 = (nm1 == NEG_INF || nm1 == m1) ? 1.f : fast_exp2(m1 - nm1);
-      m0 = nm0;
-      m1 = nm1;
-      if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+      bool over = false;
+#pragma unroll
+      for (int nt = 0; nt < KS / 8; ++nt)
+        over |= (s[nt][0] > th0) | (s[nt][1] > th0) | (s[nt][2] > th1) | (s[nt][3] > th1);
+      if (__any_sync(0xffffffffu, over)) {
+        // exact row maxima of this half block; move the reference and rescale O and l
+        float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+        for (int nt = 0; nt < KS / 8; ++nt) {
+          mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+          mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+        const float c0 = (nm0 == NEG_INF || nm0 == m0) ? 1.f : fast_exp2((m0 - nm0) * p.sl2);
+        const float c1 = (nm1 == NEG_INF || nm1 == m1) ? 1.f : fast_exp2((m1 - nm1) * p.sl2);
+        m0 = nm0;
+        m1 = nm1;
+        th0 = m0 + p.margin;
+        th1 = m1 + p.margin;
         l0 *= c0;
         l1 *= c1;
 #pragma unroll
@@ -229,13 +264,15 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
           o[i][3] *= c1;
         }
       }
+      // every processed half block holds a visible key, so m0 and m1 are finite here
+      const float ms0 = -m0 * p.sl2, ms1 = -m1 * p.sl2;
       uint32_t pa[KS / 16][4];
 #pragma unroll
       for (int nt = 0; nt < KS / 8; ++nt) {
-        const float p00 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][0] - m0);
-        const float p01 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][1] - m0);
-        const float p10 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][2] - m1);
-        const float p11 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][3] - m1);
+        const float p00 = fast_exp2(fmaf(s[nt][0], p.sl2, ms0));
+        const float p01 = fast_exp2(fmaf(s[nt][1], p.sl2, ms0));
+        const float p10 = fast_exp2(fmaf(s[nt][2], p.sl2, ms1));
+        const float p11 = fast_exp2(fmaf(s[nt][3], p.sl2, ms1));
         l0 += p00 + p01;
         l1 += p10 + p11;
         const int kk = nt >> 1, hi = nt & 1;
@@ -289,8 +326,8 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     }
     if (p.LSE && q == 0) {
       const size_t hbase = (size_t)b * p.H_q + (size_t)hk * p.GQ;
-      if (r < p.GQ) p.LSE[(hbase + r) * p.N + t] = l0 > 0.f ? (m0 + fast_log2(l0)) * LN2 : NEG_INF;
-      if (r + 8 < p.GQ) p.LSE[(hbase + r + 8) * p.N + t] = l1 > 0.f ? (m1 + fast_log2(l1)) * LN2 : NEG_INF;
+      if (r < p.GQ) p.LSE[(hbase + r) * p.N + t] = l0 > 0.f ? (m0 * p.sl2 + fast_log2(l0)) * LN2 : NEG_INF;
+      if (r + 8 < p.GQ) p.LSE[(hbase + r + 8) * p.N + t] = l1 > 0.f ? (m1 * p.sl2 + fast_log2(l1)) * LN2 : NEG_INF;
     }
   }
   // drain loads still in flight before the CTA's shared memory goes away (bounded)
@@ -335,6 +372,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, co
   prm.M1 = (p.N + 63) / 64;
   prm.causal = p.causal;
   prm.sl2 = p.scale * LOG2E;
+  prm.margin = RESCALE_MARGIN / prm.sl2;
   if (prm.total == 0) return cudaSuccess;
   const size_t smem = (size_t)NW * NSLOT * KS * D * 2 + 1024;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
