@@ -8,34 +8,39 @@
 // candidates that Stage 2 scores exactly.
 //
 // One warp owns one (b, h_kv, t) at a time.  The group's G_Q query rows (padded to 16)
-// stay in registers as mma.sync A fragments for the whole walk; each scored level gathers
+// stay in registers as mma.sync B fragments for the whole walk; each scored level gathers
 // the <= 2K x 2 child summaries straight from L2/L1 into registers with 16-byte loads and
-// multiplies them with m16n8k16 (16 heads x 8 children per MMA).  The d index is permuted
-// identically in A and B so that each lane loads 8 contiguous values per child row.
-// Candidate lists, LSE, head sums and the rank-based SelectK stay in registers and warp
+// multiplies them with m16n8k16 (the two children of 8 candidates x 8 heads per MMA, so a
+// lane holds both children of one candidate and the pair LSE needs no exchange).  The d
+// index is permuted identically in A and B so that each lane loads 8 contiguous values per
+// row.  Candidate lists, LSE, head sums and a bitonic SelectK stay in registers and warp
 // shuffles: no query-key score matrix is materialised.
 #include "kernels.cuh"
 
 namespace pisa {
 namespace {
 
-constexpr int THREADS = 256;
+constexpr int THREADS = 128;
+// resident CTAs per SM the register budget is sized for (the walk is latency-bound: more
+// warps in flight hide the per-level L2 round trip and the MMA/shuffle dependency chains)
+constexpr int MIN_BLOCKS_128 = 5, MIN_BLOCKS_64 = 6;
 
 
-// log2(2^a + 2^b), with -inf inputs allowed (not both)
-__device__ __forceinline__ float lse2_pair(float a, float b) {
+// log2(2^(a s) + 2^(b s)) for s > 0; only a when b is absent
+__device__ __forceinline__ float lse2_scaled(float a, float b, bool has_b, float s) {
+  if (!has_b) return a * s;
   const float m = fmaxf(a, b);
   const float n = fminf(a, b);
-  return m + fast_log2(1.0f + fast_exp2(n - m));
+  return fmaf(m, s, fast_log2(1.0f + fast_exp2((n - m) * s)));
 }
 
 template <int D>
-__global__ void __launch_bounds__(THREADS, D == 128 ? 2 : 3) stage1_kernel(const uint16_t* __restrict__ Q,
+__global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCKS_64) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
                                                          float scale_log2, Geometry geo) {
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
-  constexpr int NB = 2;        // n-tiles (8 children each) whose loads are in flight together
+  constexpr int KH = NCH / 2;      // chunks loaded together
   __shared__ int lists[THREADS / 32][32];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -60,6 +65,7 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? 2 : 3) stage1_kernel(const
       qb[j] = r + 8 < GQ ? ldg16(qrow + (size_t)(r + 8) * D + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
     }
     const uint16_t* Pb = P + (size_t)bh * geo.nodes * D;
+    const bool two_tiles = GQ > 8;  // heads 8..15 exist
 
     int surv = lane == 0 ? 0 : -1;  // survivors of level l+1 (lane i holds the i-th, ascending)
     int ns = 1;
@@ -83,71 +89,87 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? 2 : 3) stage1_kernel(const
         continue;
       }
 
-      // score the nc candidates with their level-(l-1) children: slot 2i+c = child c of cand i
+      // score the nc candidates with their level-(l-1) children.  MMA rows are children
+      // (row r: child 0 of candidate 8m + r, row r + 8: its child 1), columns are heads, so
+      // lane (r, q) ends with both children of one candidate for heads 2q, 2q+1 (n-tile 0)
+      // and 8+2q, 9+2q (n-tile 1).
       const long long cspan = 64LL << (l - 2);
-      const long long lvl_off = geo.off[l - 1];
+      const uint16_t* Pl = Pb + (size_t)geo.off[l - 1] * D;
       const int Mc = geo.M[l - 1];
-      // start every child row of this level on its way to L1 before the batched loads, so
-      // the level costs one memory round trip instead of one per batch
+      // lane i starts candidate i's two (adjacent) child rows on their way to L1, so the level
+      // costs one memory round trip
+      if (lane < nc) {
+        const int ch = 2 * cand;
+        const bool v1 = ch + 1 < Mc && (!causal || (long long)(ch + 1) * cspan <= t);
+        const uint16_t* row = Pl + (size_t)ch * D;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int ci = 4 * nt + (r >> 1);
-        const int cnode = __shfl_sync(0xffffffffu, cand, ci);
-        const int child = 2 * cnode + (r & 1);
-        const bool valid = ci < nc && child < Mc && (!causal || (long long)child * cspan <= t);
-        if (valid && 64 * (q >> 1) < D && (q & 1) == 0) prefetch_l1(Pb + (size_t)(lvl_off + child) * D + 64 * (q >> 1));
+        for (int o = 0; o < (2 * D * 2) / 128; ++o)
+          if (o < (D * 2) / 128 || v1) prefetch_l1(row + o * 64);
       }
       float my = NEG_INF;  // score of candidate `lane`
+      const int nmt = (nc + 7) >> 3;
+      for (int mt = 0; mt < nmt; ++mt) {
+        const int ci = 8 * mt + r;
+        const int cnode = __shfl_sync(0xffffffffu, cand, ci);
+        const bool vc = ci < nc;
+        const int ch = 2 * cnode;
+        const bool v1 = vc && ch + 1 < Mc && (!causal || (long long)(ch + 1) * cspan <= t);
+        const uint16_t* row = Pl + (size_t)(vc ? ch : 0) * D;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int half = 0; half < 8 / NB; ++half) {
-        uint4 kv[NB][NCH];
-        bool valid[NB];
+        for (int jh = 0; jh < NCH; jh += KH) {  // KH chunks of both child rows per load group
+          uint4 k0[KH], k1[KH];
 #pragma unroll
-        for (int k = 0; k < NB; ++k) {
-          const int nt = half * NB + k;
-          const int ci = 4 * nt + (r >> 1);
-          const int cnode = __shfl_sync(0xffffffffu, cand, ci);
-          const int child = 2 * cnode + (r & 1);
-          valid[k] = ci < nc && child < Mc && (!causal || (long long)child * cspan <= t);
-          const uint16_t* prow = Pb + (size_t)(lvl_off + (valid[k] ? child : 0)) * D;
-#pragma unroll
-          for (int j = 0; j < NCH; ++j) kv[k][j] = valid[k] ? ldg16(prow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < NB; ++k) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < NCH; ++j) {
-            mma_bf16_16816(acc, qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv[k][j].x, kv[k][j].y);
-            mma_bf16_16816(acc, qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv[k][j].z, kv[k][j].w);
+          for (int u = 0; u < KH; ++u) {
+            k0[u] = vc ? ldg16(row + 32 * (jh + u) + 8 * q) : make_uint4(0, 0, 0, 0);
+            k1[u] = v1 ? ldg16(row + D + 32 * (jh + u) + 8 * q) : make_uint4(0, 0, 0, 0);
           }
-          // acc: (row r | r+8) x (col 2q | 2q+1) = heads x children 0/1 of candidate 4nt+q
-          const unsigned vm = __ballot_sync(0xffffffffu, valid[k]);
-          const bool v0 = (vm >> (8 * q)) & 1u, v1 = (vm >> (8 * q + 4)) & 1u;
-          float part = 0.f;
-          if (v0) {
-            const float x0 = acc[0] * scale_log2, x1 = v1 ? acc[1] * scale_log2 : NEG_INF;
-            const float y0 = acc[2] * scale_log2, y1 = v1 ? acc[3] * scale_log2 : NEG_INF;
-            if (r < GQ) part += lse2_pair(x0, x1);
-            if (r + 8 < GQ) part += lse2_pair(y0, y1);
+#pragma unroll
+          for (int u = 0; u < KH; ++u) {
+            mma_bf16_16816(a0, k0[u].x, k1[u].x, k0[u].y, k1[u].y, qa[jh + u].x, qa[jh + u].y);
+            mma_bf16_16816(a0, k0[u].z, k1[u].z, k0[u].w, k1[u].w, qa[jh + u].z, qa[jh + u].w);
           }
-          part += __shfl_xor_sync(0xffffffffu, part, 4);
-          part += __shfl_xor_sync(0xffffffffu, part, 8);
-          part += __shfl_xor_sync(0xffffffffu, part, 16);
-          // candidate 4nt+q's score to lane 4nt+q (lanes hold one candidate each)
-          const float val = __shfl_sync(0xffffffffu, v0 ? part : NEG_INF, lane & 3);
-          if ((lane >> 2) == half * NB + k) my = val;
+          if (two_tiles) {
+#pragma unroll
+            for (int u = 0; u < KH; ++u) {
+              mma_bf16_16816(a1, k0[u].x, k1[u].x, k0[u].y, k1[u].y, qb[jh + u].x, qb[jh + u].y);
+              mma_bf16_16816(a1, k0[u].z, k1[u].z, k0[u].w, k1[u].w, qb[jh + u].z, qb[jh + u].w);
+            }
+          }
         }
+        // per head: log2(2^x0 + 2^x1), x = logit * scale * log2(e); child 1 may be absent
+        float part = 0.f;
+        if (2 * q < GQ) part += lse2_scaled(a0[0], a0[2], v1, scale_log2);
+        if (2 * q + 1 < GQ) part += lse2_scaled(a0[1], a0[3], v1, scale_log2);
+        if (8 + 2 * q < GQ) part += lse2_scaled(a1[0], a1[2], v1, scale_log2);
+        if (9 + 2 * q < GQ) part += lse2_scaled(a1[1], a1[3], v1, scale_log2);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        // candidate 8mt + r's score (held by lanes 4r..4r+3) to lane 8mt + r
+        const float val = __shfl_sync(0xffffffffu, part, 4 * (lane & 7));
+        if ((lane >> 3) == mt) my = val;
       }
       if (lane >= nc) my = NEG_INF;
-      // SelectK: rank by (score desc, index asc)
-      int rank = 0;
-      for (int j = 0; j < nc; ++j) {
-        const float uj = __shfl_sync(0xffffffffu, my, j);
-        rank += (uj > my || (uj == my && j < lane)) ? 1 : 0;
+      // SelectK: bitonic sort of the 32 (score desc, index asc) pairs; the first Ksel lanes
+      // then hold the kept candidates
+      float sv = my;
+      int si = lane;
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, sv, j);
+          const int oi = __shfl_xor_sync(0xffffffffu, si, j);
+          const bool other_better = ov > sv || (ov == sv && oi < si);
+          const bool lower = (lane & j) == 0, desc = (lane & k) == 0;
+          if ((lower == desc) == other_better) {
+            sv = ov;
+            si = oi;
+          }
+        }
       }
-      const bool keep = lane < nc && rank < Ksel;
-      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      const unsigned km = __reduce_or_sync(0xffffffffu, lane < Ksel ? (1u << si) : 0u);
+      const bool keep = (km >> lane) & 1u;
       if (keep) lst[__popc(km & lt_mask)] = cand;
       __syncwarp();
       ns = __popc(km);
@@ -165,8 +187,15 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
   (void)err;
   const long long total = (long long)p.B * p.H_kv * p.N;
   if (total == 0) return cudaSuccess;
+  // persistent grid: exactly the CTAs that are resident at once, each walking items with a
+  // grid stride, so no second partial wave
+  const void* fn = p.d == 128 ? (const void*)stage1_kernel<128> : (const void*)stage1_kernel<64>;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, THREADS, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
   long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
-  const long long cap = (long long)num_sms * 8;
+  const long long cap = (long long)num_sms * per_sm;
   if (blocks > cap) blocks = cap;
   const float sl2 = p.scale * LOG2E;
   if (p.d == 128)

@@ -23,8 +23,10 @@
 namespace pisa {
 namespace {
 
-constexpr int NW = 8;       // warps per CTA, one query each
-constexpr int NSLOT = 3;    // ring slots per warp
+// Warps per CTA (one query each) and ring slots per warp.  The kernel is latency-bound, so
+// it runs as many warps as the register file holds, with the rest of shared memory as ring.
+constexpr int nw_for(int d) { return d == 128 ? 12 : 16; }
+constexpr int nslot_for(int d) { return d == 128 ? 2 : 3; }
 constexpr int KS = 32;      // keys per slot (half a block)
 constexpr float RESCALE_MARGIN = 8.f;  // exp2 headroom before O and l are rescaled (P <= 2^8)
 
@@ -84,7 +86,7 @@ __device__ __forceinline__ void load_item(Cursor& c, const AttnParams& p, long l
   first_block(c, p);
 }
 
-template <int D>
+template <int D, int NW = nw_for(D), int NSLOT = nslot_for(D)>
 __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap mapK,
                                                                  const __grid_constant__ CUtensorMap mapV,
                                                                  AttnParams p, uint32_t* err) {
@@ -116,10 +118,12 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   Cursor pc;
   load_item(pc, p, gw, err);
   while (pc.mask == 0 && pc.item < p.total) load_item(pc, p, pc.item + nwarps, err);
-  long long issued = 0, consumed = 0;
-  auto issue_until = [&](long long limit) {
-    while (issued < limit && pc.item < p.total) {
-      const int slot = (int)(issued % NSLOT);
+  // ring state: loads in flight, next slot to fill, next slot to consume and its parity
+  int in_flight = 0, islot = 0, cslot = 0;
+  uint32_t cphase = 0;
+  auto issue_fill = [&]() {
+    while (in_flight < NSLOT && pc.item < p.total) {
+      const int slot = islot;
       const int bh = (int)(pc.item / p.N);
       const int row = pc.blk * 64 + pc.sub * KS;
       fence_proxy_async();
@@ -135,7 +139,8 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
           for (int h = 0; h < HALVES; ++h) tma_load_3d_hint(dst + h * HALF, m, &full[warp][slot], 64 * h, row, bh, keep_policy);
         }
       }
-      ++issued;
+      islot = islot + 1 == NSLOT ? 0 : islot + 1;
+      ++in_flight;
       // advance: K then V of each half block, half blocks of each block, blocks of each item
       pc.kv ^= 1;
       if (pc.kv == 0 && ++pc.sub == pc.nsub) {
@@ -145,7 +150,14 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       }
     }
   };
-  issue_until(NSLOT);
+  issue_fill();
+  auto consume_next = [&]() {
+    if (++cslot == NSLOT) {
+      cslot = 0;
+      cphase ^= 1u;
+    }
+    --in_flight;
+  };
 
   bool ok = true;
   for (long long item = gw; item < p.total && ok; item += nwarps) {
@@ -188,12 +200,11 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     while (cc.mask && ok) {
       const int kbase = cc.blk * 64 + cc.sub * KS;
       // ---------------- S = Q K^T over KS keys ----------------
-      int slot = (int)(consumed % NSLOT);
-      if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) {
+      if (!mbar_wait_warp(&full[warp][cslot], cphase, err)) {
         ok = false;
         break;
       }
-      const uint32_t kb = smem_u32(ring + slot * SLOT);
+      const uint32_t kb = smem_u32(ring + cslot * SLOT);
       float s[KS / 8][4];
 #pragma unroll
       for (int nt = 0; nt < KS / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -216,8 +227,8 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
           mma_bf16_16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], bk[nt][2],
                          bk[nt][3]);
       }
-      ++consumed;
-      issue_until(consumed + NSLOT);
+      consume_next();
+      issue_fill();
 
       // ---------------- online softmax (exp2 domain, lazy reference maximum) ----------------
       if (kbase + KS - 1 > last) {  // the half block holds invisible keys: mask them
@@ -281,12 +292,11 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       }
 
       // ---------------- O += P V ----------------
-      slot = (int)(consumed % NSLOT);
-      if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) {
+      if (!mbar_wait_warp(&full[warp][cslot], cphase, err)) {
         ok = false;
         break;
       }
-      const uint32_t vb = smem_u32(ring + slot * SLOT);
+      const uint32_t vb = smem_u32(ring + cslot * SLOT);
 #pragma unroll
       for (int kk = 0; kk < KS / 16; ++kk) {
         const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
@@ -300,8 +310,8 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
           mma_bf16_16816(o[2 * np + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
         }
       }
-      ++consumed;
-      issue_until(consumed + NSLOT);
+      consume_next();
+      issue_fill();
       // next half block / block
       if (++cc.sub == cc.nsub) {
         cc.mask &= cc.mask - 1;
@@ -331,10 +341,9 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     }
   }
   // drain loads still in flight before the CTA's shared memory goes away (bounded)
-  while (consumed < issued) {
-    const int slot = (int)(consumed % NSLOT);
-    if (!mbar_wait_warp(&full[warp][slot], (uint32_t)((consumed / NSLOT) & 1), err)) break;
-    ++consumed;
+  while (in_flight > 0) {
+    if (!mbar_wait_warp(&full[warp][cslot], cphase, err)) break;
+    consume_next();
   }
 }
 
@@ -374,6 +383,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, co
   prm.sl2 = p.scale * LOG2E;
   prm.margin = RESCALE_MARGIN / prm.sl2;
   if (prm.total == 0) return cudaSuccess;
+  constexpr int NW = nw_for(D), NSLOT = nslot_for(D);
   const size_t smem = (size_t)NW * NSLOT * KS * D * 2 + 1024;
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
