@@ -11,11 +11,15 @@
 // a query are summed with lane shuffles in a fixed order.
 //
 // Persistent, warp-specialised CTA (one per SM):
-//   warp 0      TMA producer: K pair (3-D map, rows past N read as zero) into a 2-stage
-//               ring, reused across consecutive tiles of the same pair; Q rows of each
-//               query (2-D map, one box per 64 columns) into a 4-stage ring.  Tiles
-//               come in runs of consecutive tiles from an atomic counter; a run's tile
-//               records and entries are staged in shared memory in one round trip.
+//   warp 0      scheduler: tiles come in runs of consecutive tiles from an atomic counter
+//               (a run's tile records and entries are staged in shared memory in one round
+//               trip); per tile it publishes the record and the query list of a Q stage and
+//               loads the K pair by TMA (3-D map, rows past N read as zero) into a 2-stage
+//               ring, reused across consecutive tiles of the same pair.
+//   warps 10-13 Q loaders: one TMA box per query and d half (2-D map, RPQ rows x 64 columns,
+//               128-byte swizzle) into a 4-stage ring, the tile's queries spread over the
+//               four warps: with 2 KB per box the issue cost per box dominates, and one warp
+//               issuing all of them was the pipeline's bottleneck.
 //   warp 1      owns TMEM (2 x 128 columns, double-buffered accumulators); one thread
 //               issues the d/16 MMAs of a tile and commits to mbarriers.
 //   warps 2-9   epilogue: two warps per TMEM lane quarter, one per leaf of the pair.
@@ -30,7 +34,9 @@ constexpr int NKS = 2;            // K-pair stages
 constexpr int ROWS = 128;         // MMA M (query-head rows)
 constexpr int KEYS = 128;         // MMA N (two leaves of 64 keys)
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int LOAD_WARPS = 4;
+constexpr int LOAD_WARP0 = 2 + EPI_WARPS;
+constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * LOAD_WARPS;
 constexpr uint32_t TMEM_COLS = 256;
 
 
@@ -65,7 +71,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   uint8_t* sQ = smem;
   uint8_t* sK = smem + NQS * STAGE_BYTES;
 
-  __shared__ uint64_t q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[2], acc_empty[2];
+  __shared__ uint64_t q_info[NQS], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[2], acc_empty[2];
   __shared__ TileInfo info[NQS];
   __shared__ int32_t ent[NQS][ROWS];
   __shared__ uint32_t tmem_base_s;
@@ -77,7 +83,8 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   if (threadIdx.x == 0) {
     done_it_s = 0x7fffffff;
     for (int i = 0; i < NQS; ++i) {
-      mbar_init(&q_full[i], 1);
+      mbar_init(&q_info[i], 1);
+      mbar_init(&q_full[i], LOAD_WARPS);
       mbar_init(&q_empty[i], 1 + EPI_WARPS);
     }
     for (int i = 0; i < NKS; ++i) {
@@ -100,7 +107,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   const int ntiles = prm.totals[1];
 
   if (warp == 0) {
-    // ------------------------------ producer ------------------------------
+    // ------------------------------ scheduler ------------------------------
     const uint64_t keep_policy = l2_evict_last_policy();  // K pairs are reused by later windows
     uint32_t kload = 0;
     int prev_bh = -1, prev_node = -1, ks = 0;
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         if (lane == 0) {
           info[qs].tile = make_int4(0, 0, 0, -1);
           __threadfence_block();
-          mbar_arrive(&q_full[qs]);
+          mbar_arrive(&q_info[qs]);
         }
         break;
       }
@@ -138,8 +145,19 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       ++next_tile;
       const int bh = tl.x, node = tl.y, start = tl.z, cnt = tl.w;
       const int newk = (bh != prev_bh || node != prev_node) ? 1 : 0;
+      if (newk) ks = kload % NKS;
+      // publish the tile first: its Q loads need not wait for a free K stage
+      for (int i = lane; i < cnt; i += 32) ent[qs][i] = chunk_ent[start - chunk_e0 + i];
+      __syncwarp();
+      if (lane == 0) {
+        info[qs].tile = tl;
+        info[qs].ks = ks;
+        info[qs].newk = newk;
+        __threadfence_block();
+        mbar_arrive(&q_info[qs]);
+      }
+      __syncwarp();
       if (newk) {
-        ks = kload % NKS;
         if (!mbar_wait_warp(&k_empty[ks], ((kload / NKS) & 1) ^ 1, err)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&k_full[ks], STAGE_BYTES);
@@ -152,37 +170,30 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         prev_bh = bh;
         prev_node = node;
       }
+    }
+  } else if (warp >= LOAD_WARP0) {
+    // ------------------------------ Q loaders ------------------------------
+    // loader warp w issues the TMA boxes (RPQ rows x 64 columns, one per d half) of the tile's
+    // queries w, w + LOAD_WARPS, ...; each warp arrives on the stage's barrier with the bytes
+    // it expects, so the MMA issuer sees the stage full once every box has landed.
+    const int lw = warp - LOAD_WARP0;
+    for (int it = 0;; ++it) {
+      const int qs = it % NQS;
+      if (!mbar_wait_warp(&q_info[qs], (it / NQS) & 1, err)) break;
+      const int4 tl = info[qs].tile;
+      if (tl.w < 0) {  // end marker: pass it to the MMA issuer
+        if (lane == 0) mbar_arrive(&q_full[qs]);
+        break;
+      }
+      const int bh = tl.x, cnt = tl.w;
       const int b = bh / prm.H_kv, hk = bh - b * prm.H_kv;
-      int my_t[ROWS / 32 + 1];
-#pragma unroll
-      for (int k = 0; k * 32 < ROWS; ++k) {
-        const int i = lane + 32 * k;
-        my_t[k] = -1;
-        if (i < cnt) {
-          const int e = chunk_ent[start - chunk_e0 + i];
-          ent[qs][i] = e;
-          my_t[k] = e >> 6;
-        }
-      }
+      const int mine = cnt > lw ? (cnt - lw + LOAD_WARPS - 1) / LOAD_WARPS : 0;  // queries of this warp
+      if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)mine * prm.RPQ * D * 2);
       __syncwarp();
-      if (lane == 0) {
-        info[qs].tile = tl;
-        info[qs].ks = ks;
-        info[qs].newk = newk;
-        __threadfence_block();
-        mbar_arrive_expect_tx(&q_full[qs], (uint32_t)cnt * prm.RPQ * D * 2);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k * 32 < ROWS; ++k) {
-        const int i = lane + 32 * k;
-        if (i < cnt) {
-          const int row = (int)(((long long)b * prm.N + my_t[k]) * prm.H_q + (long long)hk * prm.GQ);
-#pragma unroll
-          for (int h = 0; h < HALVES; ++h)
-            tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h,
-                        row);
-        }
+      if (lane < mine * HALVES) {
+        const int i = lw + LOAD_WARPS * (lane / HALVES), h = lane % HALVES;
+        const int row = (int)(((long long)b * prm.N + (ent[qs][i] >> 6)) * prm.H_q + (long long)hk * prm.GQ);
+        tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h, row);
       }
     }
   } else if (warp == 1) {
