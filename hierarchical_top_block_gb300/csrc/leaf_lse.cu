@@ -6,7 +6,7 @@
 // Work unit: a tile = up to qt queries (qt * max(G_Q, 8) = 128 rows) that all need the
 // same level-2 survivor, i.e. the same pair of sibling leaves (128 contiguous keys).
 //   D[128 rows, 128 keys] = Q_tile[128, d] . K_pair[128, d]^T   on tcgen05, fp32 in TMEM
-// then each epilogue thread owns one TMEM lane (one query head row) and reduces 64 keys
+// then each epilogue thread owns one TMEM lane (one query head row) and reduces the 64 keys
 // per leaf to log-sum-exp (causal mask inside the query's own block), and the G_Q rows of
 // a query are summed with lane shuffles in a fixed order.
 //
@@ -22,7 +22,8 @@
 //               issuing all of them was the pipeline's bottleneck.
 //   warp 1      owns TMEM (2 x 128 columns, double-buffered accumulators); one thread
 //               issues the d/16 MMAs of a tile and commits to mbarriers.
-//   warps 2-9   epilogue: two warps per TMEM lane quarter, one per leaf of the pair.
+//   warps 2-9   epilogue: two groups of four (one warp per TMEM lane quarter) taking
+//               alternate tiles; each warp reduces both leaves of its rows.
 // Every wait is bounded; on timeout the error word is set and the CTA drains and exits.
 #include "kernels.cuh"
 
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     for (int i = 0; i < NQS; ++i) {
       mbar_init(&q_info[i], 1);
       mbar_init(&q_full[i], LOAD_WARPS);
-      mbar_init(&q_empty[i], 1 + EPI_WARPS);
+      mbar_init(&q_empty[i], 1 + EPI_WARPS / 2);
     }
     for (int i = 0; i < NKS; ++i) {
       mbar_init(&k_full[i], 1);
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], EPI_WARPS);
+      mbar_init(&acc_empty[i], EPI_WARPS / 2);
     }
     mbar_fence_init();
   }
@@ -206,12 +207,14 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         const int qs = it % NQS;
         if (!mbar_wait(&q_full[qs], (it / NQS) & 1, err)) break;
         const TileInfo ti = info[qs];
-        if (ti.tile.w < 0) {  // end marker: tell the epilogue once its buffer is free
-          const int a = it & 1;
-          if (!mbar_wait(&acc_empty[a], ((it >> 1) & 1) ^ 1, err)) break;
+        if (ti.tile.w < 0) {  // end marker: tell both epilogue groups once their buffers are free
           done_it_s = it;
           __threadfence_block();
-          mbar_arrive(&acc_full[a]);
+          for (int k = 0; k < 2; ++k) {
+            const int i2 = it + k, a = i2 & 1;
+            if (!mbar_wait(&acc_empty[a], ((i2 >> 1) & 1) ^ 1, err)) break;
+            mbar_arrive(&acc_full[a]);
+          }
           break;
         }
         if (ti.newk) {
@@ -238,15 +241,19 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     __syncwarp();
   } else {
     // ------------------------------ epilogue ------------------------------
+    // Two groups of four warps, one warp per TMEM lane quarter: group g takes the tiles
+    // g, g + 2, ... (accumulator buffer g) and reduces both leaves of each, so the two
+    // epilogue warps sharing a scheduler partition work on different tiles and keep its
+    // exponential unit busy across each other's TMEM loads and stores.
     const int ew = warp - 2;
+    const int grp = ew >> 2;
     const int quarter = warp & 3;
-    const int leaf_c = ew >> 2;  // which leaf of the pair this warp reduces
     const int row = quarter * 32 + lane;
     const int qi = row / prm.RPQ, h = row - qi * prm.RPQ;
     const int twoK = 2 * prm.Ksel;
-    for (int it = 0;; ++it) {
+    for (int it = grp;; it += 2) {
       const int qs = it % NQS;
-      const int a = it & 1;
+      const int a = grp;
       if (!mbar_wait_warp(&acc_full[a], (it >> 1) & 1, err)) break;
       if (it >= *(volatile int*)&done_it_s) break;
       tc_fence_after();
@@ -255,64 +262,67 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       const int e = vq ? ent[qs][qi] : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_empty[qs]);
-
-      uint32_t v[64];
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * KEYS + leaf_c * 64;
-      tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[a]);
-
       const int t = e >> 6, slot = e & 63;
       const int bh = tl.x, node = tl.y;
-      const int leaf = 2 * node + leaf_c;
-      const long long key0 = (long long)leaf * 64;
-      const bool leaf_ok = vq && leaf < prm.M1 && (!prm.causal || key0 <= t);
-      // keys j <= lim of this leaf are visible (causal: key <= t; always: key < N)
-      long long lim64 = (long long)prm.N - 1 - key0;
-      if (prm.causal && (long long)t - key0 < lim64) lim64 = (long long)t - key0;
-      const int lim = (int)(lim64 < 63 ? lim64 : 63);
-      float lse2 = NEG_INF;
-      if (leaf_ok && h < prm.GQ) {
-        // four independent partial sums; the mask is only needed inside the own block
-        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-        if (lim >= 63) {
+#pragma unroll 1
+      for (int leaf_c = 0; leaf_c < 2; ++leaf_c) {
+        uint32_t v[64];
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * KEYS + leaf_c * 64;
+        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_wait_ld();
+        if (leaf_c == 1) {  // the accumulator is read out: the MMA may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+        const int leaf = 2 * node + leaf_c;
+        const long long key0 = (long long)leaf * 64;
+        const bool leaf_ok = vq && leaf < prm.M1 && (!prm.causal || key0 <= t);
+        // keys j <= lim of this leaf are visible (causal: key <= t; always: key < N)
+        long long lim64 = (long long)prm.N - 1 - key0;
+        if (prm.causal && (long long)t - key0 < lim64) lim64 = (long long)t - key0;
+        const int lim = (int)(lim64 < 63 ? lim64 : 63);
+        float lse2 = NEG_INF;
+        if (leaf_ok && h < prm.GQ) {
+          // four independent partial sums; the mask is only needed inside the own block
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+          if (lim >= 63) {
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            p0 += fast_exp2(__uint_as_float(v[j]) * prm.sl2);
-            p1 += fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2);
-            p2 += fast_exp2(__uint_as_float(v[j + 2]) * prm.sl2);
-            p3 += fast_exp2(__uint_as_float(v[j + 3]) * prm.sl2);
+            for (int j = 0; j < 64; j += 4) {
+              p0 += fast_exp2(__uint_as_float(v[j]) * prm.sl2);
+              p1 += fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2);
+              p2 += fast_exp2(__uint_as_float(v[j + 2]) * prm.sl2);
+              p3 += fast_exp2(__uint_as_float(v[j + 3]) * prm.sl2);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+              p0 += (j <= lim) ? fast_exp2(__uint_as_float(v[j]) * prm.sl2) : 0.f;
+              p1 += (j + 1 <= lim) ? fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2) : 0.f;
+            }
           }
-        } else {
+          const float s = (p0 + p1) + (p2 + p3);
+          if (s > 0.f && s < POS_INF) {
+            lse2 = fast_log2(s);
+          } else {  // logits beyond the fp32 exponent range: subtract the max first
+            float m = NEG_INF;
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            p0 += (j <= lim) ? fast_exp2(__uint_as_float(v[j]) * prm.sl2) : 0.f;
-            p1 += (j + 1 <= lim) ? fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2) : 0.f;
+            for (int j = 0; j < 64; ++j)
+              if (j <= lim) m = fmaxf(m, __uint_as_float(v[j]) * prm.sl2);
+            float s2 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (j <= lim) s2 += fast_exp2(__uint_as_float(v[j]) * prm.sl2 - m);
+            lse2 = m + fast_log2(s2);
           }
         }
-        const float s = (p0 + p1) + (p2 + p3);
-        if (s > 0.f && s < POS_INF) {
-          lse2 = fast_log2(s);
-        } else {  // logits beyond the fp32 exponent range: subtract the max first
-          float m = NEG_INF;
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j <= lim) m = fmaxf(m, __uint_as_float(v[j]) * prm.sl2);
-          float s2 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j <= lim) s2 += fast_exp2(__uint_as_float(v[j]) * prm.sl2 - m);
-          lse2 = m + fast_log2(s2);
-        }
+        // sum over the G_Q head rows of each query (lanes of one query are contiguous)
+        float part = (leaf_ok && h < prm.GQ) ? lse2 : 0.f;
+        for (int o = 1; o < prm.RPQ; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (vq && h == 0)
+          prm.leaf_score[((size_t)bh * prm.N + t) * twoK + 2 * slot + leaf_c] = leaf_ok ? part * LN2 : NEG_INF;
       }
-      // sum over the G_Q head rows of each query (lanes of one query are contiguous)
-      float part = (leaf_ok && h < prm.GQ) ? lse2 : 0.f;
-      for (int o = 1; o < prm.RPQ; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (vq && h == 0)
-        prm.leaf_score[((size_t)bh * prm.N + t) * twoK + 2 * slot + leaf_c] = leaf_ok ? part * LN2 : NEG_INF;
     }
   }
   __syncthreads();
