@@ -36,26 +36,40 @@ struct AttnParams {
   uint16_t* O;
   float* LSE;
   long long total;  // B * H_kv * N
+  int BH;           // B * H_kv
   int N, H_q, H_kv, GQ, Ksel, M1, causal;
   int one_box;      // 1: the 4-D map loads both d halves in one box
   float sl2;     // softmax scale x log2(e)
   float margin;  // RESCALE_MARGIN / sl2: headroom of the reference maximum in raw logit units
 };
 
-// Walks the (query, selected block, half block, K|V) load sequence of one warp.
+// Walks the (query, selected block, half block, K|V) load sequence of one warp.  Items are
+// (bh, t) pairs visited with a grid stride; the stride is applied as (bh, t) increments.
 struct Cursor {
-  long long item;   // current (bh, t) item, or >= total when exhausted
+  int bh, t;        // current item; bh >= BH when exhausted
   unsigned mask;    // remaining valid idx positions of the item
   int val;          // this lane's idx entry of the item
-  int t;            // query position of the item
   int blk, nsub, sub, kv;
 };
 
+struct Stride {
+  int bh, t;  // the grid stride in items, as (bh, t) increments
+};
+
+__device__ __forceinline__ void step_item(int& bh, int& t, const Stride& st, int N) {
+  t += st.t;
+  bh += st.bh;
+  if (t >= N) {
+    t -= N;
+    ++bh;
+  }
+}
+
 __device__ __forceinline__ int half_blocks(const AttnParams& p, int blk, int t) {
-  const long long last = p.causal ? (long long)min(t, p.N - 1) : (long long)p.N - 1;
-  long long cnt = last - (long long)blk * 64 + 1;
+  const int last = p.causal ? min(t, p.N - 1) : p.N - 1;
+  int cnt = last - blk * 64 + 1;
   if (cnt > 64) cnt = 64;
-  return (int)((cnt + KS - 1) / KS);
+  return (cnt + KS - 1) / KS;
 }
 
 __device__ __forceinline__ void first_block(Cursor& c, const AttnParams& p) {
@@ -67,20 +81,20 @@ __device__ __forceinline__ void first_block(Cursor& c, const AttnParams& p) {
   }
 }
 
-__device__ __forceinline__ void load_item(Cursor& c, const AttnParams& p, long long item, uint32_t* err) {
+// Loads the selection row of item (c.bh, c.t) into the cursor.
+__device__ __forceinline__ void load_item(Cursor& c, const AttnParams& p, uint32_t* err) {
   const int lane = threadIdx.x & 31;
-  c.item = item;
   c.val = -1;
   c.mask = 0;
-  if (item >= p.total) return;
-  c.t = (int)(item % p.N);
+  if (c.bh >= p.BH) return;
+  const long long item = (long long)c.bh * p.N + c.t;
   int v = lane < p.Ksel ? p.idx[item * p.Ksel + lane] : -1;
   if (v >= p.M1) {
     report_error(err, ERR_BAD_INDEX);
     v = -1;
   }
   // a block that starts after t has no visible key: skip it
-  if (v >= 0 && p.causal && (long long)v * 64 > c.t) v = -1;
+  if (v >= 0 && p.causal && v * 64 > c.t) v = -1;
   c.val = v;
   c.mask = __ballot_sync(0xffffffffu, v >= 0);
   first_block(c, p);
@@ -113,20 +127,28 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   const uint64_t stream_policy = l2_evict_first_policy();
   const long long gw = (long long)blockIdx.x * NW + warp;
   const long long nwarps = (long long)gridDim.x * NW;
+  const Stride st{(int)(nwarps / p.N), (int)(nwarps % p.N)};
+  const int bh0 = (int)(gw / p.N), t0 = (int)(gw % p.N);
 
   // ---- producer side of this warp's ring ----
   Cursor pc;
-  load_item(pc, p, gw, err);
-  while (pc.mask == 0 && pc.item < p.total) load_item(pc, p, pc.item + nwarps, err);
+  pc.bh = bh0;
+  pc.t = t0;
+  load_item(pc, p, err);
+  while (pc.mask == 0 && pc.bh < p.BH) {
+    step_item(pc.bh, pc.t, st, p.N);
+    load_item(pc, p, err);
+  }
   // ring state: loads in flight, next slot to fill, next slot to consume and its parity
   int in_flight = 0, islot = 0, cslot = 0;
   uint32_t cphase = 0;
   auto issue_fill = [&]() {
-    while (in_flight < NSLOT && pc.item < p.total) {
+    while (in_flight < NSLOT && pc.bh < p.BH) {
       const int slot = islot;
-      const int bh = (int)(pc.item / p.N);
+      const int bh = pc.bh;
       const int row = pc.blk * 64 + pc.sub * KS;
-      fence_proxy_async();
+      // the slot's previous contents were read by ldmatrix whose results fed MMAs issued
+      // before this point, so the reads are complete when the copy is issued
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&full[warp][slot], SLOT);
@@ -146,7 +168,10 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       if (pc.kv == 0 && ++pc.sub == pc.nsub) {
         pc.mask &= pc.mask - 1;
         first_block(pc, p);
-        while (pc.mask == 0 && pc.item < p.total) load_item(pc, p, pc.item + nwarps, err);
+        while (pc.mask == 0 && pc.bh < p.BH) {
+          step_item(pc.bh, pc.t, st, p.N);
+          load_item(pc, p, err);
+        }
       }
     }
   };
@@ -160,16 +185,17 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   };
 
   bool ok = true;
-  for (long long item = gw; item < p.total && ok; item += nwarps) {
-    const int bh = (int)(item / p.N);
-    const int t = (int)(item - (long long)bh * p.N);
+  for (int bh = bh0, t = t0; bh < p.BH && ok; step_item(bh, t, st, p.N)) {
     const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
     Cursor cc;
-    load_item(cc, p, item, nullptr);
+    cc.bh = bh;
+    cc.t = t;
+    load_item(cc, p, nullptr);
     {  // move the next item's selection row and Q rows towards L2 while this one runs
-      const long long nitem = item + nwarps;
-      if (nitem < p.total) {
-        const int nbh = (int)(nitem / p.N), nt = (int)(nitem - (long long)nbh * p.N);
+      int nbh = bh, nt = t;
+      step_item(nbh, nt, st, p.N);
+      if (nbh < p.BH) {
+        const long long nitem = (long long)nbh * p.N + nt;
         const int nb = nbh / p.H_kv, nhk = nbh - nb * p.H_kv;
         const uint16_t* nq = p.Q + (((size_t)nb * p.N + nt) * p.H_q + (size_t)nhk * p.GQ) * D;
         if (lane * 64 < p.GQ * D) prefetch_l2(nq + (size_t)lane * 64);  // 128 bytes per lane
@@ -373,6 +399,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, co
   prm.O = O;
   prm.LSE = LSE;
   prm.total = (long long)p.B * p.H_kv * p.N;
+  prm.BH = p.B * p.H_kv;
   prm.N = p.N;
   prm.H_q = p.H_q;
   prm.H_kv = p.H_kv;
