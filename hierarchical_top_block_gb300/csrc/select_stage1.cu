@@ -47,13 +47,25 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
   const int r = lane >> 2, q = lane & 3;
   const unsigned lt_mask = (1u << lane) - 1u;
   int* lst = lists[warp];
-  const long long total = (long long)B * H_kv * N;
+  const int BH = B * H_kv;
+  // items (bh, t) with a grid stride, applied as (bh, t) increments
+  const long long gw = (long long)blockIdx.x * (THREADS / 32) + warp;
   const long long nwarps = (long long)gridDim.x * (THREADS / 32);
+  const int st_bh = (int)(nwarps / N), st_t = (int)(nwarps % N);
 
-  for (long long item = (long long)blockIdx.x * (THREADS / 32) + warp; item < total; item += nwarps) {
-    const int bh = (int)(item / N);
-    const int t = (int)(item - (long long)bh * N);
+  for (int bh = (int)(gw / N), t = (int)(gw % N); bh < BH;) {
+    const long long item = (long long)bh * N + t;
     const int b = bh / H_kv, hk = bh - b * H_kv;
+    int nbh = bh + st_bh, nt = t + st_t;  // the next item
+    if (nt >= N) {
+      nt -= N;
+      ++nbh;
+    }
+    if (nbh < BH) {  // move its Q rows towards L2 while this walk runs (128 bytes per lane)
+      const int nb = nbh / H_kv, nhk = nbh - nb * H_kv;
+      const uint16_t* nq = Q + (((size_t)nb * N + nt) * H_q + (size_t)nhk * GQ) * D;
+      if (lane * 64 < GQ * D) prefetch_l2(nq + (size_t)lane * 64);
+    }
 
     // query fragments: rows r and r+8 of the group (zero beyond G_Q), 8 contiguous d values
     // per chunk: chunk j of lane q covers d in [32j + 8q, 32j + 8q + 8)
@@ -71,10 +83,11 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
     int ns = 1;
     for (int l = geo.L - 1; l >= 2; --l) {
       // eligible children of the survivors, in ascending order
-      const long long span = 64LL << (l - 1);  // keys under one level-l node
+      // a level-l node covers 2^(l+5) keys and starts at key c * 2^(l+5): visible iff c <= t >> (l+5)
+      const int tl = t >> (l + 5);
       const int c0 = 2 * surv, c1 = 2 * surv + 1;
-      const bool e0 = lane < ns && c0 < geo.M[l] && (!causal || (long long)c0 * span <= t);
-      const bool e1 = lane < ns && c1 < geo.M[l] && (!causal || (long long)c1 * span <= t);
+      const bool e0 = lane < ns && c0 < geo.M[l] && (!causal || c0 <= tl);
+      const bool e1 = lane < ns && c1 < geo.M[l] && (!causal || c1 <= tl);
       const unsigned b0 = __ballot_sync(0xffffffffu, e0), b1 = __ballot_sync(0xffffffffu, e1);
       const int pos = __popc(b0 & lt_mask) + __popc(b1 & lt_mask);
       const int nc = __popc(b0) + __popc(b1);
@@ -93,14 +106,14 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       // (row r: child 0 of candidate 8m + r, row r + 8: its child 1), columns are heads, so
       // lane (r, q) ends with both children of one candidate for heads 2q, 2q+1 (n-tile 0)
       // and 8+2q, 9+2q (n-tile 1).
-      const long long cspan = 64LL << (l - 2);
+      const int tc = t >> (l + 4);  // the same for level-(l-1) nodes
       const uint16_t* Pl = Pb + (size_t)geo.off[l - 1] * D;
       const int Mc = geo.M[l - 1];
       // lane i starts candidate i's two (adjacent) child rows on their way to L1, so the level
       // costs one memory round trip
       if (lane < nc) {
         const int ch = 2 * cand;
-        const bool v1 = ch + 1 < Mc && (!causal || (long long)(ch + 1) * cspan <= t);
+        const bool v1 = ch + 1 < Mc && (!causal || ch + 1 <= tc);
         const uint16_t* row = Pl + (size_t)ch * D;
 #pragma unroll
         for (int o = 0; o < (2 * D * 2) / 128; ++o)
@@ -113,7 +126,10 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
         const int cnode = __shfl_sync(0xffffffffu, cand, ci);
         const bool vc = ci < nc;
         const int ch = 2 * cnode;
-        const bool v1 = vc && ch + 1 < Mc && (!causal || (long long)(ch + 1) * cspan <= t);
+        const bool v1 = vc && ch + 1 < Mc && (!causal || ch + 1 <= tc);
+        // rows are read unconditionally (an absent child 1 or candidate only feeds scores that
+        // are masked below); row ch + 1 <= Mc stays inside the pyramid: level l-1 is followed
+        // by level l
         const uint16_t* row = Pl + (size_t)(vc ? ch : 0) * D;
         float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -121,8 +137,8 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
           uint4 k0[KH], k1[KH];
 #pragma unroll
           for (int u = 0; u < KH; ++u) {
-            k0[u] = vc ? ldg16(row + 32 * (jh + u) + 8 * q) : make_uint4(0, 0, 0, 0);
-            k1[u] = v1 ? ldg16(row + D + 32 * (jh + u) + 8 * q) : make_uint4(0, 0, 0, 0);
+            k0[u] = ldg16(row + 32 * (jh + u) + 8 * q);
+            k1[u] = ldg16(row + D + 32 * (jh + u) + 8 * q);
           }
 #pragma unroll
           for (int u = 0; u < KH; ++u) {
@@ -177,6 +193,8 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       __syncwarp();
     }
     if (lane < Ksel) S2[item * Ksel + lane] = lane < ns ? surv : -1;
+    bh = nbh;
+    t = nt;
   }
 }
 
