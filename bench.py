@@ -35,11 +35,11 @@ UNIT = "tokens/s"
 KERNELS_PER_STEP = 12  # pyramid 2, stage 1, clustering 6, leaf LSE, top-K, attention
 
 # DRAM traffic of the attention kernel per launch on the 256K prefill (dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture, profiles/sparse_attn_kernel_prefill_256k.md), keyed
+# dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
 # as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "57e79de6ef8b132ba9426c7b37ecad7d6d8c6e24520a4d33715cb4150845a4b6",
-                "workload": "prefill_256k", "bytes": 13988103424 + 1100957952}
+ATTN_TRAFFIC = {"sources_sha256": "711831a769da5135e1a730c3d4c8e96889819dc26afde8a1bceb21a9d2d53e98",
+                "workload": "prefill_256k", "bytes": 16035273216 + 1299870208}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
