@@ -21,9 +21,11 @@ constexpr int WARPS = 4;
 constexpr int THREADS = 32 * WARPS;
 
 
-__device__ __forceinline__ float lse2_pair(float a, float b) {
+// log2(2^(a s) + 2^(b s)) for s > 0; only a when b is absent
+__device__ __forceinline__ float lse2_scaled(float a, float b, bool has_b, float s) {
+  if (!has_b) return a * s;
   const float m = fmaxf(a, b), n = fminf(a, b);
-  return m + fast_log2(1.0f + fast_exp2(n - m));
+  return fmaf(m, s, fast_log2(1.0f + fast_exp2((n - m) * s)));
 }
 
 struct DecodeParams {
@@ -50,18 +52,21 @@ __device__ __forceinline__ int level_size(long long n, int l) {
   return (int)m;
 }
 
+// 4 CTAs per SM (<= 128 registers, 33 KB of shared memory): a batch of 64 sequences x 8 KV
+// heads runs in one wave
 template <int D>
-__global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_t* err) {
+__global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint32_t* err) {
   constexpr int NCH = D / 32;
   constexpr int NDT = D / 8;
-  __shared__ int lst[32];
+  __shared__ int wlst[WARPS][32];
+  __shared__ float lvl_score[2][32];
   __shared__ int cand_leaf[32];
   __shared__ float cand_score[32];
   __shared__ int ncand_s, nsel_s;
   __shared__ int sel[32];
   __shared__ float part_m[WARPS][16], part_l[WARPS][16];
   extern __shared__ __align__(1024) uint8_t vbuf_raw[];
-  uint8_t* vbuf = (uint8_t*)(((uintptr_t)vbuf_raw + 1023) & ~(uintptr_t)1023);  // [WARPS][64 x D bf16]
+  uint8_t* vbuf = (uint8_t*)(((uintptr_t)vbuf_raw + 1023) & ~(uintptr_t)1023);  // [WARPS][32 x D bf16]
 
   const int bh = blockIdx.x;
   const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
@@ -86,25 +91,64 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_
   int L = 1;
   while (level_size(n, L) > 1) ++L;
   if (tid < D) {
+    // the new token's leaf: the mean of its <= 64 keys, summed in key order (the same
+    // arithmetic as the pyramid build, so the cache equals a fresh build bit for bit); the
+    // column is loaded in one batch first
     const long long leaf = T >> 6;
+    const int cnt = (int)(T - leaf * 64 + 1);
+    const uint16_t* kcol = Kb + (size_t)leaf * 64 * D + tid;
     float hi = 0.f, lo = 0.f;
-    for (long long c = leaf * 64; c <= T; ++c) {
-      float s, e;
-      two_sum(hi, bf16_to_f32(Kb[(size_t)c * D + tid]), s, e);
-      hi = s;
-      lo += e;
+#pragma unroll
+    for (int i0 = 0; i0 < 64; i0 += 32) {  // 32 rows per batch of loads
+      uint16_t kv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) kv[i] = i0 + i < cnt ? kcol[(size_t)(i0 + i) * D] : (uint16_t)0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (i0 + i < cnt) {
+          float s, e;
+          two_sum(hi, bf16_to_f32(kv[i]), s, e);
+          hi = s;
+          lo += e;
+        }
+      }
     }
-    const double cnt = (double)(T - leaf * 64 + 1);
-    Pb[(size_t)(p.off[1] + leaf) * D + tid] = bf16_mean(hi, lo, (int)cnt);
-    long long node = leaf;
-    for (int l = 2; l <= L; ++l) {
-      node >>= 1;
-      const long long c0 = 2 * node, c1 = min(2 * node + 2, (long long)level_size(n, l - 1));
-      const float a = bf16_to_f32(Pb[(size_t)(p.off[l - 1] + c0) * D + tid]);
-      const float bb = c1 - c0 > 1 ? bf16_to_f32(Pb[(size_t)(p.off[l - 1] + c0 + 1) * D + tid]) : 0.f;
-      float s, err;
-      two_sum(a, bb, s, err);
-      Pb[(size_t)(p.off[l] + node) * D + tid] = bf16_mean(s, err, (int)(c1 - c0));
+    uint16_t cur = bf16_mean(hi, lo, cnt);
+    Pb[(size_t)(p.off[1] + leaf) * D + tid] = cur;
+    // ancestors: each is the mean of its (one or two) children; the child off the path is
+    // unchanged by this step, so a chunk of levels' siblings is loaded first and the chain
+    // runs in registers
+    constexpr int CHUNK = 8;
+    long long size = (n + 63) >> 6;  // size of level l-1
+    for (int l0 = 2; l0 <= L; l0 += CHUNK) {
+      float sib[CHUNK];
+      long long sz = size;
+#pragma unroll
+      for (int u = 0; u < CHUNK; ++u) {
+        const int l = l0 + u;
+        if (l <= L) {
+          const long long child = leaf >> (l - 2);
+          sib[u] = (child | 1) < sz ? bf16_to_f32(Pb[(size_t)(p.off[l - 1] + (child ^ 1)) * D + tid]) : 0.f;
+          sz = (sz + 1) >> 1;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < CHUNK; ++u) {
+        const int l = l0 + u;
+        if (l <= L) {
+          const long long child = leaf >> (l - 2);
+          const bool pair = (child | 1) < size;
+          const float mine = bf16_to_f32(cur);
+          float s, e;
+          if (child & 1)
+            two_sum(sib[u], mine, s, e);
+          else
+            two_sum(mine, sib[u], s, e);
+          cur = bf16_mean(s, e, pair ? 2 : 1);
+          Pb[(size_t)(p.off[l] + (child >> 1)) * D + tid] = cur;
+          size = (size + 1) >> 1;
+        }
+      }
     }
   }
   __syncthreads();
@@ -119,86 +163,108 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_
   }
   const unsigned lt_mask = (1u << lane) - 1u;
 
-  // ---- level walk (warp 0) ----
-  if (warp == 0) {
-    int surv = lane == 0 ? 0 : -1, ns = 1;
+  // ---- level walk: every warp follows the same survivor list; a scored level's <= 32
+  // candidates are split over the 4 warps (8 each), scored with the two children of each
+  // candidate as MMA rows and the heads as columns, and meet in shared memory ----
+  {
+    int* mylst = wlst[warp];
+    int surv = lane == 0 ? 0 : -1, ns = 1, par = 0;
     for (int l = L - 1; l >= 2; --l) {
       const int Ml = level_size(n, l);
-      const long long span = 64LL << (l - 1);
+      const int tl = (int)(T >> (l + 5));  // level-l node c starts at key c * 2^(l+5)
       const int c0 = 2 * surv, c1 = 2 * surv + 1;
-      const bool e0 = lane < ns && c0 < Ml && (long long)c0 * span <= T;
-      const bool e1 = lane < ns && c1 < Ml && (long long)c1 * span <= T;
+      const bool e0 = lane < ns && c0 < Ml && c0 <= tl;
+      const bool e1 = lane < ns && c1 < Ml && c1 <= tl;
       const unsigned b0 = __ballot_sync(0xffffffffu, e0), b1 = __ballot_sync(0xffffffffu, e1);
       const int pos = __popc(b0 & lt_mask) + __popc(b1 & lt_mask);
       const int nc = __popc(b0) + __popc(b1);
-      if (e0) lst[pos] = c0;
-      if (e1) lst[pos + (e0 ? 1 : 0)] = c1;
+      if (e0) mylst[pos] = c0;
+      if (e1) mylst[pos + (e0 ? 1 : 0)] = c1;
       __syncwarp();
-      const int cand = lane < nc ? lst[lane] : -1;
+      const int cand = lane < nc ? mylst[lane] : -1;
       __syncwarp();
       if (nc <= p.Ksel) {
         surv = cand;
         ns = nc;
         continue;
       }
-      const long long cspan = 64LL << (l - 2);
       const int Mc = level_size(n, l - 1);
-      float u[8];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int ci = 4 * nt + (r >> 1);
+      const int tc = (int)(T >> (l + 4));
+      const uint16_t* Pl = Pb + (size_t)p.off[l - 1] * D;
+      if (8 * warp < nc) {
+        const int ci = 8 * warp + r;
         const int cnode = __shfl_sync(0xffffffffu, cand, ci);
-        const int child = 2 * cnode + (r & 1);
-        const bool valid = ci < nc && child < Mc && (long long)child * cspan <= T;
-        const uint16_t* prow = Pb + (size_t)(p.off[l - 1] + (valid ? child : 0)) * D;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool vc = ci < nc;
+        const int ch = 2 * cnode;
+        const bool v1 = vc && ch + 1 < Mc && ch + 1 <= tc;
+        // read unconditionally: rows of an absent child or candidate only feed masked
+        // scores, and row ch + 1 <= Mc lies inside the level's capacity or the next level
+        const uint16_t* row = Pl + (size_t)(vc ? ch : 0) * D;
+        uint4 k0[NCH], k1[NCH];
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          const uint4 kv = valid ? ldg16(prow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
-          mma_bf16_16816(acc, qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
-          mma_bf16_16816(acc, qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+          k0[j] = ldg16(row + 32 * j + 8 * q);
+          k1[j] = ldg16(row + D + 32 * j + 8 * q);
         }
-        const unsigned vm = __ballot_sync(0xffffffffu, valid);
-        const bool v0 = (vm >> (8 * q)) & 1u, v1 = (vm >> (8 * q + 4)) & 1u;
-        float part = 0.f;
-        if (v0) {
-          const float x1 = v1 ? acc[1] * p.sl2 : NEG_INF, y1 = v1 ? acc[3] * p.sl2 : NEG_INF;
-          if (r < p.GQ) part += lse2_pair(acc[0] * p.sl2, x1);
-          if (r + 8 < p.GQ) part += lse2_pair(acc[2] * p.sl2, y1);
-        }
-        part += __shfl_xor_sync(0xffffffffu, part, 4);
-        part += __shfl_xor_sync(0xffffffffu, part, 8);
-        part += __shfl_xor_sync(0xffffffffu, part, 16);
-        u[nt] = v0 ? part : NEG_INF;
-      }
-      float my = NEG_INF;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const float v = __shfl_sync(0xffffffffu, u[nt], lane & 3);
-        if ((lane >> 2) == nt) my = v;
+        for (int j = 0; j < NCH; ++j) {
+          mma_bf16_16816(a0, k0[j].x, k1[j].x, k0[j].y, k1[j].y, qa[j].x, qa[j].y);
+          mma_bf16_16816(a0, k0[j].z, k1[j].z, k0[j].w, k1[j].w, qa[j].z, qa[j].w);
+        }
+        if (p.GQ > 8) {
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            mma_bf16_16816(a1, k0[j].x, k1[j].x, k0[j].y, k1[j].y, qb[j].x, qb[j].y);
+            mma_bf16_16816(a1, k0[j].z, k1[j].z, k0[j].w, k1[j].w, qb[j].z, qb[j].w);
+          }
+        }
+        float part = 0.f;
+        if (2 * q < p.GQ) part += lse2_scaled(a0[0], a0[2], v1, p.sl2);
+        if (2 * q + 1 < p.GQ) part += lse2_scaled(a0[1], a0[3], v1, p.sl2);
+        if (8 + 2 * q < p.GQ) part += lse2_scaled(a1[0], a1[2], v1, p.sl2);
+        if (9 + 2 * q < p.GQ) part += lse2_scaled(a1[1], a1[3], v1, p.sl2);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (q == 0) lvl_score[par][ci] = vc ? part : NEG_INF;
       }
-      if (lane >= nc) my = NEG_INF;
-      int rank = 0;
-      for (int j = 0; j < nc; ++j) {
-        const float uj = __shfl_sync(0xffffffffu, my, j);
-        rank += (uj > my || (uj == my && j < lane)) ? 1 : 0;
+      __syncthreads();
+      // SelectK (every warp, same result): bitonic sort of (score desc, index asc)
+      float sv = lane < nc ? lvl_score[par][lane] : NEG_INF;
+      int si = lane;
+      par ^= 1;
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, sv, j);
+          const int oi = __shfl_xor_sync(0xffffffffu, si, j);
+          const bool other_better = ov > sv || (ov == sv && oi < si);
+          const bool lower = (lane & j) == 0, desc = (lane & k) == 0;
+          if ((lower == desc) == other_better) {
+            sv = ov;
+            si = oi;
+          }
+        }
       }
-      const bool keep = lane < nc && rank < p.Ksel;
-      const unsigned km = __ballot_sync(0xffffffffu, keep);
-      if (keep) lst[__popc(km & lt_mask)] = cand;
+      const unsigned km = __reduce_or_sync(0xffffffffu, lane < p.Ksel ? (1u << si) : 0u);
+      const bool keep = (km >> lane) & 1u;
+      if (keep) mylst[__popc(km & lt_mask)] = cand;
       __syncwarp();
       ns = __popc(km);
-      surv = lane < ns ? lst[lane] : -1;
+      surv = lane < ns ? mylst[lane] : -1;
       __syncwarp();
     }
-    // leaf candidates: eligible children of the level-2 survivors, slot 2i + c
-    const int M1 = level_size(n, 1);
-    const int node = __shfl_sync(0xffffffffu, surv, (lane >> 1) & 31);
-    if (lane < 2 * p.Ksel) {
-      const int j = 2 * node + (lane & 1);
-      cand_leaf[lane] = (node >= 0 && j < M1 && (long long)j * 64 <= T) ? j : -1;
+    if (warp == 0) {
+      // leaf candidates: eligible children of the level-2 survivors, slot 2i + c
+      const int M1 = level_size(n, 1);
+      const int node = __shfl_sync(0xffffffffu, surv, (lane >> 1) & 31);
+      if (lane < 2 * p.Ksel) {
+        const int j = 2 * node + (lane & 1);
+        cand_leaf[lane] = (node >= 0 && j < M1 && (long long)j * 64 <= T) ? j : -1;
+      }
+      if (lane == 0) ncand_s = 2 * p.Ksel;
     }
-    if (lane == 0) ncand_s = 2 * p.Ksel;
   }
   __syncthreads();
 
@@ -313,99 +379,108 @@ __global__ void __launch_bounds__(THREADS) decode_kernel(DecodeParams p, uint32_
   }
   __syncthreads();
 
-  // ---- attention over the selected blocks: warp w takes blocks w, w+4, ... ----
+  // ---- attention over the selected blocks in 32-key halves: warp w takes blocks w, w+4, ...
+  // The half's V rows are copied into the warp's swizzled shared buffer asynchronously
+  // while S = Q K^T runs on K rows loaded straight into registers; P V then uses
+  // ldmatrix.trans on the buffer.
   const int nsel = nsel_s;
-  // S uses the permuted-d Q fragments with direct K loads; P V uses ldmatrix.trans on V
-  // staged in shared memory (keys in natural order in both)
   float o[NDT][4];
 #pragma unroll
   for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-  uint8_t* vmine = vbuf + (size_t)warp * 64 * D * 2;
+  constexpr int HKEYS = 32;                 // keys per half block
+  constexpr uint32_t HSPAN = HKEYS * 128;  // bytes of one 64-column half of the buffer
+  uint8_t* vmine = vbuf + (size_t)warp * HKEYS * D * 2;
   const uint32_t vs = smem_u32(vmine);
   for (int si = warp; si < nsel; si += WARPS) {
     const int blk = sel[si];
-    const long long key0 = (long long)blk * 64;
-    // stage V block (64 x D) in swizzled smem: row k, 16-byte chunk c at (c ^ (k & 7)) per 128-byte half
-    for (int i = lane; i < 64 * (D / 8); i += 32) {
-      const int k = i / (D / 8), c = i % (D / 8);
-      const long long key = key0 + k;
-      const uint4 val = key <= T ? ldg16(Vb + (size_t)key * D + 8 * c) : make_uint4(0, 0, 0, 0);
-      const int h = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(vmine + h * (64 * 128) + k * 128 + ((cc ^ (k & 7)) << 4)) = val;
-    }
-    float s[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      const long long key = key0 + 8 * nt + r;
-      const bool vis = key <= T;
-      const uint16_t* krow = Kb + (size_t)(vis ? key : key0) * D;
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const uint4 kv = vis ? ldg16(krow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
-        mma_bf16_16816(s[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
-        mma_bf16_16816(s[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+#pragma unroll 1
+    for (int hb = 0; hb < 2; ++hb) {
+      const long long key0 = (long long)blk * 64 + HKEYS * hb;
+      if (key0 > T) break;
+      // V rows key0 .. key0 + 31 (rows past T become zero): row k, 16-byte chunk c at
+      // (c ^ (k & 7)) within its 128-byte half row
+      for (int i = lane; i < HKEYS * (D / 8); i += 32) {
+        const int k = i / (D / 8), c = i % (D / 8);
+        const long long key = key0 + k;
+        const bool in = key <= T;
+        cp_async16(vmine + (c >> 3) * HSPAN + k * 128 + (((c & 7) ^ (k & 7)) << 4),
+                   Vb + (size_t)(in ? key : key0) * D + 8 * c, in ? 16 : 0);
       }
-    }
-    // s[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0,1}  (the n index maps key order 1:1)
-    float mx0 = NEG_INF, mx1 = NEG_INF;
+      cp_async_commit();
+      float s[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+      for (int nt = 0; nt < 4; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        const long long key = key0 + 8 * nt + r;
+        const uint16_t* krow = Kb + (size_t)(key <= T ? key : key0) * D;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const bool vis = key0 + 8 * nt + 2 * q + c <= T;
-        s[nt][c] = vis ? s[nt][c] * p.sl2 : NEG_INF;
-        s[nt][2 + c] = vis ? s[nt][2 + c] * p.sl2 : NEG_INF;
-        mx0 = fmaxf(mx0, s[nt][c]);
-        mx1 = fmaxf(mx1, s[nt][2 + c]);
+        for (int j = 0; j < NCH; ++j) {
+          const uint4 kv = ldg16(krow + 32 * j + 8 * q);
+          mma_bf16_16816(s[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
+          mma_bf16_16816(s[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+        }
       }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-    const float c0 = nm0 == NEG_INF ? 1.f : fast_exp2(m0 - nm0);
-    const float c1 = nm1 == NEG_INF ? 1.f : fast_exp2(m1 - nm1);
-    m0 = nm0;
-    m1 = nm1;
-    l0 *= c0;
-    l1 *= c1;
+      // s[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0,1}  (the n index maps key order 1:1)
+      float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
-    for (int i = 0; i < NDT; ++i) {
-      o[i][0] *= c0;
-      o[i][1] *= c0;
-      o[i][2] *= c1;
-      o[i][3] *= c1;
-    }
-    uint32_t pa[4][4];
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p00 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][0] - m0);
-      const float p01 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][1] - m0);
-      const float p10 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][2] - m1);
-      const float p11 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][3] - m1);
-      l0 += p00 + p01;
-      l1 += p10 + p11;
-      const int kk = nt >> 1, hi = nt & 1;
-      pa[kk][hi ? 2 : 0] = pack_bf16x2(p00, p01);
-      pa[kk][hi ? 3 : 1] = pack_bf16x2(p10, p11);
-    }
-    __syncwarp();
+        for (int c = 0; c < 2; ++c) {
+          const bool vis = key0 + 8 * nt + 2 * q + c <= T;
+          s[nt][c] = vis ? s[nt][c] * p.sl2 : NEG_INF;
+          s[nt][2 + c] = vis ? s[nt][2 + c] * p.sl2 : NEG_INF;
+          mx0 = fmaxf(mx0, s[nt][c]);
+          mx1 = fmaxf(mx1, s[nt][2 + c]);
+        }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+      const float c0 = nm0 == NEG_INF ? 1.f : fast_exp2(m0 - nm0);
+      const float c1 = nm1 == NEG_INF ? 1.f : fast_exp2(m1 - nm1);
+      m0 = nm0;
+      m1 = nm1;
+      l0 *= c0;
+      l1 *= c1;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
-#pragma unroll
-      for (int np = 0; np < NDT / 2; ++np) {
-        const int d0 = 8 * (2 * np + (lane >> 4));
-        const uint32_t addr = vs + (d0 >> 6) * (64 * 128) + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-        mma_bf16_16816(o[2 * np + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+      for (int i = 0; i < NDT; ++i) {
+        o[i][0] *= c0;
+        o[i][1] *= c0;
+        o[i][2] *= c1;
+        o[i][3] *= c1;
       }
+      uint32_t pa[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float p00 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][0] - m0);
+        const float p01 = m0 == NEG_INF ? 0.f : fast_exp2(s[nt][1] - m0);
+        const float p10 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][2] - m1);
+        const float p11 = m1 == NEG_INF ? 0.f : fast_exp2(s[nt][3] - m1);
+        l0 += p00 + p01;
+        l1 += p10 + p11;
+        const int kk = nt >> 1, hi = nt & 1;
+        pa[kk][hi ? 2 : 0] = pack_bf16x2(p00, p01);
+        pa[kk][hi ? 3 : 1] = pack_bf16x2(p10, p11);
+      }
+      cp_async_wait_all();
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+        for (int np = 0; np < NDT / 2; ++np) {
+          const int d0 = 8 * (2 * np + (lane >> 4));
+          const uint32_t addr = vs + (d0 >> 6) * HSPAN + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
+          mma_bf16_16816(o[2 * np + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+        }
+      }
+      __syncwarp();  // every lane is done with the buffer before the next half overwrites it
     }
-    __syncwarp();
   }
   // merge the per-warp softmax states (fixed order, deterministic)
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -482,7 +557,8 @@ cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
   p.sl2 = pr.scale * LOG2E;
   p.nodes = geo_cap.nodes;
   for (int l = 0; l <= MAX_LEVELS; ++l) p.off[l] = geo_cap.off[l];
-  const size_t smem = (size_t)WARPS * 64 * D * 2 + 1024;
+  // V staging [WARPS][32 keys x D] bf16, also the merge buffer [WARPS][16][D] fp32
+  const size_t smem = (size_t)WARPS * 32 * D * 2 + 1024;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   decode_kernel<D><<<pr.B * pr.H_kv, THREADS, smem, s>>>(p, err);
