@@ -347,28 +347,35 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
   __syncthreads();
 
   // ---- final top-K with the own block (warp 0) ----
+  // The candidate slots hold their leaves in ascending order; rank the other leaves by
+  // (score desc, index asc) with a bitonic sort over the 32 lanes, keep K-1, and write the
+  // kept leaves plus the own block in ascending order.
   if (warp == 0) {
     const int own = (int)(T >> 6);
     int leaf = lane < nslots ? cand_leaf[lane] : -1;
     if (leaf == own) leaf = -1;
-    const float sc = leaf >= 0 ? cand_score[lane] : NEG_INF;
-    const unsigned valid = __ballot_sync(0xffffffffu, leaf >= 0);
-    int rank = 0;
-    for (int j = 0; j < 32; ++j) {
-      if (!((valid >> j) & 1u)) continue;
-      const float sj = __shfl_sync(0xffffffffu, sc, j);
-      const int lj = __shfl_sync(0xffffffffu, leaf, j);
-      rank += (leaf >= 0 && (sj > sc || (sj == sc && lj < leaf))) ? 1 : 0;
+    float sv = leaf >= 0 ? cand_score[lane] : NEG_INF;
+    int sl = leaf >= 0 ? leaf : 0x7fffffff, si = lane;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, sv, j);
+        const int ol = __shfl_xor_sync(0xffffffffu, sl, j);
+        const int oi = __shfl_xor_sync(0xffffffffu, si, j);
+        const bool other_better = ov > sv || (ov == sv && ol < sl);
+        const bool lower = (lane & j) == 0, desc = (lane & k) == 0;
+        if ((lower == desc) == other_better) {
+          sv = ov;
+          sl = ol;
+          si = oi;
+        }
+      }
     }
-    const bool keep = leaf >= 0 && rank < p.Ksel - 1;
-    const unsigned km = __ballot_sync(0xffffffffu, keep);
-    int pos = 0, below = 0;
-    for (int j = 0; j < 32; ++j) {
-      if (!((km >> j) & 1u)) continue;
-      const int lj = __shfl_sync(0xffffffffu, leaf, j);
-      pos += (keep && lj < leaf) ? 1 : 0;
-      below += lj < own ? 1 : 0;
-    }
+    const unsigned km = __reduce_or_sync(0xffffffffu, (lane < p.Ksel - 1 && sl != 0x7fffffff) ? (1u << si) : 0u);
+    const bool keep = (km >> lane) & 1u;
+    const int pos = __popc(km & lt_mask);
+    const int below = __popc(km & __ballot_sync(0xffffffffu, leaf >= 0 && leaf < own));
     if (keep) sel[pos + (own < leaf ? 1 : 0)] = leaf;
     if (lane == 0) {
       sel[below] = own;
