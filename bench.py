@@ -380,8 +380,27 @@ def secondary_decode(w, dev, steps=32, warmup=3):
     us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
     del Kc, Vc, Pc
     torch.cuda.empty_cache()
-    return {"step_us_mean": statistics.mean(us), "step_us_p50": us[len(us) // 2], "steps": steps,
-            "B": w.B, "cached_tokens": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "note": "steps 3..34 of 256"}
+    mean_us = statistics.mean(us)
+    hbm = decode_hbm_bytes(w)
+    pk = peaks()
+    return {"step_us_mean": mean_us, "step_us_p50": us[len(us) // 2], "steps": steps,
+            "B": w.B, "cached_tokens": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "note": "steps 3..34 of 256",
+            "roofline": {"bound": "hbm", "algorithmic_bytes_per_step": hbm,
+                         "achieved": hbm / (mean_us * 1e-6) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": hbm / (mean_us * 1e-6) / 1e9 / pk["hbm"], "peak_source": pk["source"] + " copy"}}
+
+
+def decode_hbm_bytes(w, C=64, g=2):
+    """Bytes one decode step must read at least, per (sequence, KV head): the child summaries
+    of every scored level (2K candidates x 2 children), the raw keys of the 2K leaf
+    candidates, and the raw keys and values of the K selected blocks; d bf16 values per row."""
+    n = w.N + 1
+    sizes = [-(-n // C)]
+    while sizes[-1] > 1:
+        sizes.append(-(-sizes[-1] // g))
+    scored = sum(1 for m in sizes[1:-1] if m > w.K)  # levels 2.. whose candidates exceed K
+    rows = scored * 2 * w.K * g + 2 * w.K * C + w.K * C * 2
+    return w.B * w.H_kv * rows * w.d * 2
 
 
 # ------------------------------------------------------------------------------------
