@@ -16,12 +16,16 @@ constexpr int THREADS = 256;
 
 __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict__ S2,
                                                        const float* __restrict__ score, int32_t* __restrict__ idx,
-                                                       long long total, int N, int Ksel, int M1, int causal) {
+                                                       int BH, int N, int Ksel, int M1, int causal) {
   const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const long long gw = (long long)blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5);
   const long long nwarps = (long long)gridDim.x * (THREADS / 32);
+  const int st_bh = (int)(nwarps / N), st_t = (int)(nwarps % N);  // grid stride as (bh, t) steps
   const int twoK = 2 * Ksel;
-  for (long long item = (long long)blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5); item < total; item += nwarps) {
-    const int t = (int)(item % N);
+  const int keep_n = causal ? Ksel - 1 : Ksel;
+  for (int bh = (int)(gw / N), t = (int)(gw % N); bh < BH;) {
+    const long long item = (long long)bh * N + t;
     const int own = causal ? t / 64 : -1;
     int leaf = -1;
     float sc = NEG_INF;
@@ -29,46 +33,46 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
       const int node = S2[item * Ksel + (lane >> 1)];
       if (node >= 0) {
         const int j = 2 * node + (lane & 1);
-        if (j < M1 && (!causal || (long long)j * 64 <= t) && j != own) {
+        if (j < M1 && (!causal || j <= t / 64) && j != own) {
           leaf = j;
           sc = score[item * twoK + lane];
         }
       }
     }
-    const unsigned valid = __ballot_sync(0xffffffffu, leaf >= 0);
-    // rank among the valid candidates: (score desc, block index asc)
-    int rank = 0;
-    for (int j = 0; j < 32; ++j) {
-      if (!((valid >> j) & 1u)) continue;
-      const float sj = __shfl_sync(0xffffffffu, sc, j);
-      const int lj = __shfl_sync(0xffffffffu, leaf, j);
-      rank += (leaf >= 0 && (sj > sc || (sj == sc && lj < leaf))) ? 1 : 0;
-    }
-    const int keep_n = causal ? Ksel - 1 : Ksel;
-    const bool keep = leaf >= 0 && rank < keep_n;
-    const unsigned km = __ballot_sync(0xffffffffu, keep);
-    // output position = number of kept blocks with a smaller index (+1 if the own block is smaller)
-    int pos = 0;
-    for (int j = 0; j < 32; ++j) {
-      if (!((km >> j) & 1u)) continue;
-      const int lj = __shfl_sync(0xffffffffu, leaf, j);
-      pos += (keep && lj < leaf) ? 1 : 0;
-    }
-    int32_t* out = idx + item * Ksel;
-    const int nkept = __popc(km);
-    if (keep) out[pos + ((causal && own < leaf) ? 1 : 0)] = leaf;
-    if (causal) {
-      // own block position: kept blocks below it
-      int below = 0;
-      for (int j = 0; j < 32; ++j) {
-        if (!((km >> j) & 1u)) continue;
-        const int lj = __shfl_sync(0xffffffffu, leaf, j);
-        below += lj < own ? 1 : 0;
+    // The survivors, hence the slots, are in ascending block order, so ranking by (score
+    // desc, slot asc) is ranking by (score desc, block index asc): bitonic sort over the lanes
+    float sv = sc;
+    int si = lane;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, sv, j);
+        const int oi = __shfl_xor_sync(0xffffffffu, si, j);
+        const bool other_better = ov > sv || (ov == sv && oi < si);
+        const bool lower = (lane & j) == 0, desc = (lane & k) == 0;
+        if ((lower == desc) == other_better) {
+          sv = ov;
+          si = oi;
+        }
       }
-      if (lane == 0) out[below] = own;
     }
-    const int filled = nkept + (causal ? 1 : 0);
+    const unsigned valid = __ballot_sync(0xffffffffu, leaf >= 0);
+    const unsigned km = __reduce_or_sync(0xffffffffu, lane < keep_n ? (1u << si) : 0u) & valid;
+    const bool keep = (km >> lane) & 1u;
+    // output position = kept blocks with a smaller index (+1 if the own block is smaller)
+    int32_t* out = idx + item * Ksel;
+    if (keep) out[__popc(km & lt_mask) + ((causal && own < leaf) ? 1 : 0)] = leaf;
+    const unsigned below = __ballot_sync(0xffffffffu, leaf >= 0 && leaf < own);  // eligible blocks under own
+    if (causal && lane == 0) out[__popc(km & below)] = own;
+    const int filled = __popc(km) + (causal ? 1 : 0);
     if (lane >= filled && lane < Ksel) out[lane] = -1;
+    t += st_t;
+    bh += st_bh;
+    if (t >= N) {
+      t -= N;
+      ++bh;
+    }
   }
 }
 
@@ -80,7 +84,7 @@ cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx
   if (total == 0) return cudaSuccess;
   long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, total, p.N, p.K, geo.M[1], p.causal);
+  topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.K, geo.M[1], p.causal);
   return cudaGetLastError();
 }
 

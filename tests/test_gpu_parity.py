@@ -212,3 +212,31 @@ def test_decode_fullsize_sampled(oracle_impl):
     compared on sampled sequences."""
     w = W.WORKLOADS["decode_128k"]
     _decode_check(oracle_impl, w, N0=w.N, steps=2, N_cap=w.N + w.decode_steps, pairs=[(5, 3), (63, 7)])
+
+
+def test_decode_gq16_d128(oracle_impl):
+    # both head tiles of the level walk (G_Q = 16) at d = 128, crossing a leaf boundary
+    w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=16, H_kv=1, d=128, K=16)
+    _decode_check(oracle_impl, w, N0=64 * 37 + 61, steps=6, N_cap=4096)
+
+
+def test_decode_full_cache_is_refused():
+    """A sequence whose cache is full is reported and left untouched; the others step."""
+    w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=8, H_kv=2, K=4)
+    N0, N_cap = 300, 320
+    Kc = torch.zeros(w.B, w.H_kv, N_cap, w.d, dtype=torch.bfloat16, device="cuda")
+    wk = w.with_(N=N_cap)
+    for b in range(w.B):
+        for g in range(w.H_kv):
+            Kc[b, g] = W.kv_slice(wk, "K", b, g, device="cuda")
+    Vc = Kc.clone()
+    Pc = pisa.pisa_build_pyramid(Kc, N=N_cap)
+    seq = torch.tensor([N_cap, N0], dtype=torch.int32, device="cuda")
+    K0, V0, P0 = Kc.clone(), Vc.clone(), Pc.clone()
+    q, k, v = W.decode_step_inputs(w, 0, "cuda")
+    pisa.pisa_decode_step(q, k, v, Kc, Vc, Pc, seq, w.K)
+    torch.cuda.synchronize()
+    assert pisa.pisa_get_last_device_error() == 5
+    assert torch.equal(Kc[0], K0[0]) and torch.equal(Vc[0], V0[0]) and torch.equal(Pc[0], P0[0])
+    assert torch.equal(Kc[1, :, N0], k[1].to(Kc.dtype)) and not torch.equal(Kc[1], K0[1])
+    assert seq.tolist() == [N_cap, N0 + 1]
