@@ -57,6 +57,7 @@ struct Params {
   int32_t* sched;      // tile counter, zero at launch
   float* leaf_score;
   int N, H_q, H_kv, GQ, RPQ, Ksel, M1, causal;
+  int qgrp;   // 1: one 4-D box per query, stage layout [query][8-row group][d half][8][64]
   float sl2;  // scale * log2(e)
 };
 
@@ -191,7 +192,13 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       const int mine = cnt > lw ? (cnt - lw + LOAD_WARPS - 1) / LOAD_WARPS : 0;  // queries of this warp
       if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)mine * prm.RPQ * D * 2);
       __syncwarp();
-      if (lane < mine * HALVES) {
+      if (prm.qgrp) {  // the query's 8-row groups with both d halves in one box
+        if (lane < mine) {
+          const int i = lw + LOAD_WARPS * lane;
+          const long long row = ((long long)b * prm.N + (ent[qs][i] >> 6)) * prm.H_q + (long long)hk * prm.GQ;
+          tma_load_4d(sQ + qs * STAGE_BYTES + i * prm.RPQ * 256, &mapQ, &q_full[qs], 0, 0, 0, (int)(row >> 3));
+        }
+      } else if (lane < mine * HALVES) {
         const int i = lw + LOAD_WARPS * (lane / HALVES), h = lane % HALVES;
         const int row = (int)(((long long)b * prm.N + (ent[qs][i] >> 6)) * prm.H_q + (long long)hk * prm.GQ);
         tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h, row);
@@ -231,7 +238,9 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
 #pragma unroll
         for (int s = 0; s < KSTEPS; ++s) {
           const uint32_t off = (s >> 2) * (ROWS * 128) + (s & 3) * 32;
-          umma_bf16(tmem_base + a * KEYS, smem_desc_sw128(qbase + off, 16, 1024),
+          // grouped Q: d half h of 8-row group g at g * 2048 + h * 1024
+          const uint32_t qoff = prm.qgrp ? (s >> 2) * 1024 + (s & 3) * 32 : off;
+          umma_bf16(tmem_base + a * KEYS, smem_desc_sw128(qbase + qoff, 16, prm.qgrp ? 2048 : 1024),
                     smem_desc_sw128(kbase + off, 16, 1024), idesc, s > 0 ? 1u : 0u);
         }
         umma_commit(&acc_full[a]);
@@ -337,8 +346,20 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
                      const Problem& p, const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s) {
   const int RPQ = p.GQ < 8 ? 8 : p.GQ;
   CUtensorMap mapQ, mapK;
-  {
-    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.B * p.N * p.H_q};
+  Params prm;
+  // d = 128 with G_Q a multiple of 8: one box per query, (64 columns, 8 rows, 2 d halves,
+  // G_Q / 8 row groups), lands as [row group][half][8 rows][64]: per d half the 8-row groups
+  // are 2 KB apart, a valid 128-byte-swizzled K-major operand; otherwise one 2-D box of RPQ
+  // rows per d half
+  const long long rows = (long long)p.B * p.N * p.H_q;
+  prm.qgrp = (D == 128 && p.GQ % 8 == 0 && p.H_q % 8 == 0) ? 1 : 0;
+  if (prm.qgrp) {
+    const uint64_t dims[4] = {64, 8, 2, (uint64_t)(rows / 8)};
+    const uint64_t strides[3] = {(uint64_t)D * 2, 128, (uint64_t)8 * D * 2};
+    const uint32_t box[4] = {64, 8, 2, (uint32_t)(p.GQ / 8)};
+    if (!encode_tensor_map(&mapQ, Q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)rows};
     const uint64_t strides[1] = {(uint64_t)D * 2};
     const uint32_t box[2] = {64, (uint32_t)RPQ};
     if (!encode_tensor_map(&mapQ, Q, 2, dims, strides, box)) return cudaErrorInvalidValue;
@@ -349,7 +370,6 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
     const uint32_t box[3] = {64, (uint32_t)KEYS, 1};
     if (!encode_tensor_map(&mapK, K, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  Params prm;
   prm.tiles = cb.tiles;
   prm.entries = cb.entries;
   prm.totals = cb.totals;
