@@ -16,14 +16,16 @@
 //               trip); per tile it publishes the record and the query list of a Q stage and
 //               loads the K pair by TMA (3-D map, rows past N read as zero) into a 2-stage
 //               ring, reused across consecutive tiles of the same pair.
-//   warps 10-13 Q loaders: one TMA box per query and d half (2-D map, RPQ rows x 64 columns,
-//               128-byte swizzle) into a 4-stage ring, the tile's queries spread over the
-//               four warps: with 2 KB per box the issue cost per box dominates, and one warp
-//               issuing all of them was the pipeline's bottleneck.
-//   warp 1      owns TMEM (2 x 128 columns, double-buffered accumulators); one thread
+//   warps 14-17 Q loaders: the tile's query rows by TMA into a 4-stage ring, the tile's
+//               queries spread over the four warps (with small boxes the issue cost per box
+//               dominates; one warp issuing all of them was the pipeline's bottleneck).  For
+//               d = 128 and G_Q a multiple of 8 one 4-D box per query (8-row groups with both
+//               d halves), else one 2-D box of RPQ rows per d half; 128-byte swizzle.
+//   warp 1      owns TMEM (3 x 128 columns of accumulators, one per epilogue group); one thread
 //               issues the d/16 MMAs of a tile and commits to mbarriers.
-//   warps 2-9   epilogue: two groups of four (one warp per TMEM lane quarter) taking
-//               alternate tiles; each warp reduces both leaves of its rows.
+//   warps 2-13  epilogue: three groups of four (one warp per TMEM lane quarter), group g
+//               taking tiles g, g+3, ... in its own accumulator; each warp reduces both
+//               leaves of its rows.
 // Every wait is bounded; on timeout the error word is set and the CTA drains and exits.
 #include "kernels.cuh"
 
@@ -34,11 +36,12 @@ constexpr int NQS = 4;            // Q stages
 constexpr int NKS = 2;            // K-pair stages
 constexpr int ROWS = 128;         // MMA M (query-head rows)
 constexpr int KEYS = 128;         // MMA N (two leaves of 64 keys)
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 12;
+constexpr int NACC = 3;           // accumulator buffers = epilogue groups
 constexpr int LOAD_WARPS = 4;
 constexpr int LOAD_WARP0 = 2 + EPI_WARPS;
 constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * LOAD_WARPS;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;
 
 
 
@@ -73,7 +76,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   uint8_t* sQ = smem;
   uint8_t* sK = smem + NQS * STAGE_BYTES;
 
-  __shared__ uint64_t q_info[NQS], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[2], acc_empty[2];
+  __shared__ uint64_t q_info[NQS], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[NACC], acc_empty[NACC];
   __shared__ TileInfo info[NQS];
   __shared__ int32_t ent[NQS][ROWS];
   __shared__ uint32_t tmem_base_s;
@@ -87,15 +90,15 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     for (int i = 0; i < NQS; ++i) {
       mbar_init(&q_info[i], 1);
       mbar_init(&q_full[i], LOAD_WARPS);
-      mbar_init(&q_empty[i], 1 + EPI_WARPS / 2);
+      mbar_init(&q_empty[i], 1 + 4);
     }
     for (int i = 0; i < NKS; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], EPI_WARPS / 2);
+      mbar_init(&acc_empty[i], 4);
     }
     mbar_fence_init();
   }
@@ -217,9 +220,9 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         if (ti.tile.w < 0) {  // end marker: tell both epilogue groups once their buffers are free
           done_it_s = it;
           __threadfence_block();
-          for (int k = 0; k < 2; ++k) {
-            const int i2 = it + k, a = i2 & 1;
-            if (!mbar_wait(&acc_empty[a], ((i2 >> 1) & 1) ^ 1, err)) break;
+          for (int k = 0; k < NACC; ++k) {
+            const int i2 = it + k, a = i2 % NACC;
+            if (!mbar_wait(&acc_empty[a], ((i2 / NACC) & 1) ^ 1, err)) break;
             mbar_arrive(&acc_full[a]);
           }
           break;
@@ -230,8 +233,8 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           ++kload;
           cur_ks = ti.ks;
         }
-        const int a = it & 1;
-        if (!mbar_wait(&acc_empty[a], ((it >> 1) & 1) ^ 1, err)) break;
+        const int a = it % NACC;
+        if (!mbar_wait(&acc_empty[a], ((it / NACC) & 1) ^ 1, err)) break;
         tc_fence_after();
         const uint32_t qbase = smem_u32(sQ + qs * STAGE_BYTES);
         const uint32_t kbase = smem_u32(sK + ti.ks * STAGE_BYTES);
@@ -250,20 +253,20 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     __syncwarp();
   } else {
     // ------------------------------ epilogue ------------------------------
-    // Two groups of four warps, one warp per TMEM lane quarter: group g takes the tiles
-    // g, g + 2, ... (accumulator buffer g) and reduces both leaves of each, so the two
-    // epilogue warps sharing a scheduler partition work on different tiles and keep its
-    // exponential unit busy across each other's TMEM loads and stores.
+    // Three groups of four warps, one warp per TMEM lane quarter: group g takes the tiles
+    // g, g + 3, ... (accumulator buffer g) and reduces both leaves of each, so the epilogue
+    // warps sharing a scheduler partition work on different tiles and hide each other's
+    // TMEM loads, shuffles and stores.
     const int ew = warp - 2;
     const int grp = ew >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int qi = row / prm.RPQ, h = row - qi * prm.RPQ;
     const int twoK = 2 * prm.Ksel;
-    for (int it = grp;; it += 2) {
+    for (int it = grp;; it += NACC) {
       const int qs = it % NQS;
       const int a = grp;
-      if (!mbar_wait_warp(&acc_full[a], (it >> 1) & 1, err)) break;
+      if (!mbar_wait_warp(&acc_full[a], (it / NACC) & 1, err)) break;
       if (it >= *(volatile int*)&done_it_s) break;
       tc_fence_after();
       const int4 tl = info[qs].tile;
