@@ -38,8 +38,8 @@ KERNELS_PER_STEP = 12  # pyramid 2, stage 1, clustering 6, leaf LSE, top-K, atte
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
 # as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "711831a769da5135e1a730c3d4c8e96889819dc26afde8a1bceb21a9d2d53e98",
-                "workload": "prefill_256k", "bytes": 16035273216 + 1299870208}
+ATTN_TRAFFIC = {"sources_sha256": "6f16dbffc13c80ccb36943510a860ba2e2dc51beb687620c7785e17281deeb27",
+                "workload": "prefill_256k", "bytes": 16032366336 + 1299501312}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
