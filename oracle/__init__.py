@@ -61,16 +61,16 @@ class Oracle:
         L.oracle_build_pyramid.argtypes = [_P, _P, _I, _I, _LL, _LL, _I, _I, _I, _I]
         L.oracle_select.restype = _I
         L.oracle_select.argtypes = [_P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _I, _P, _P, _P, _P, _P, _P,
-                                    _I]
+                                    _I, _I]
         L.oracle_selection_admissible.restype = _I
         L.oracle_selection_admissible.argtypes = [_P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _I, _P, _P,
-                                                  _D, _P, _I]
+                                                  _D, _P, _I, _I]
         L.oracle_sparse_attention.restype = _I
         L.oracle_sparse_attention.argtypes = [_P, _P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _D, _I, _P, _P, _P,
                                               _P, _I]
         L.oracle_decode_step.restype = _I
         L.oracle_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _P, _P,
-                                         _P, _I]
+                                         _P, _I, _I]
         L.oracle_f64_to_bf16.restype = ct.c_uint16
         L.oracle_f64_to_bf16.argtypes = [_D]
 
@@ -101,8 +101,9 @@ class Oracle:
         return P
 
     # ---- step 2 ---------------------------------------------------------------------
-    def select(self, Q, K, P, Ksel, rows, C=64, g=2, causal=True, scale=None):
-        """Q uint16 [B,N,H_q,d]; K [B,H_kv,N,d]; P [B,H_kv,nodes,d]; rows int64 [R,3] (b,h_kv,t)."""
+    def select(self, Q, K, P, Ksel, rows, C=64, g=2, causal=True, scale=None, scoring=0):
+        """Q uint16 [B,N,H_q,d]; K [B,H_kv,N,d]; P [B,H_kv,nodes,d]; rows int64 [R,3] (b,h_kv,t).
+        scoring: 0 LSE, 1 PISA-1 (log m + mean), 2 PISA-2 (log m + mean + var/2)."""
         B, N, H_q, d = Q.shape
         H_kv = K.shape[1]
         scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -114,11 +115,12 @@ class Oracle:
         cs = np.zeros((R, g * Ksel), np.float64)
         gap = np.zeros(R, np.float64)
         rc = self.lib.oracle_select(_ptr(Q), _ptr(K), _ptr(P), B, N, H_q, H_kv, d, C, g, Ksel, int(causal), scale, R,
-                                    _ptr(rows), _ptr(idx), _ptr(s2), _ptr(cand), _ptr(cs), _ptr(gap), self.nthreads)
+                                    _ptr(rows), _ptr(idx), _ptr(s2), _ptr(cand), _ptr(cs), _ptr(gap), self.nthreads,
+                                    int(scoring))
         assert rc == 0, rc
         return dict(idx=idx, s2=s2, cand=cand, cand_score=cs, min_gap=gap)
 
-    def admissible(self, Q, K, P, Ksel, rows, target_idx, tol=1e-3, C=64, g=2, causal=True, scale=None):
+    def admissible(self, Q, K, P, Ksel, rows, target_idx, tol=1e-3, C=64, g=2, causal=True, scale=None, scoring=0):
         B, N, H_q, d = Q.shape
         H_kv = K.shape[1]
         scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -127,7 +129,7 @@ class Oracle:
         ok = np.zeros(rows.shape[0], np.int32)
         self.lib.oracle_selection_admissible(_ptr(Q), _ptr(K), _ptr(P), B, N, H_q, H_kv, d, C, g, Ksel, int(causal),
                                              scale, rows.shape[0], _ptr(rows), _ptr(tgt), tol, _ptr(ok),
-                                             self.nthreads)
+                                             self.nthreads, int(scoring))
         return ok
 
     # ---- step 4 ---------------------------------------------------------------------
@@ -150,7 +152,7 @@ class Oracle:
         return O, LSE, ws
 
     # ---- step 3 ---------------------------------------------------------------------
-    def decode_step(self, q, k, v, Kc, Vc, Pc, seq_len, Ksel, C=64, g=2, scale=None):
+    def decode_step(self, q, k, v, Kc, Vc, Pc, seq_len, Ksel, C=64, g=2, scale=None, scoring=0):
         """In place on Kc, Vc, Pc (uint16) and seq_len (int32).  Returns o, lse, idx."""
         B, H_q, d = q.shape
         H_kv = k.shape[1]
@@ -166,6 +168,6 @@ class Oracle:
         v = np.ascontiguousarray(v, dtype=np.uint16)
         rc = self.lib.oracle_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), N_cap,
                                          B, H_q, H_kv, d, C, g, Ksel, scale, _ptr(o), _ptr(lse), _ptr(idx),
-                                         self.nthreads)
+                                         self.nthreads, int(scoring))
         assert rc == 0, rc
         return o, lse, idx

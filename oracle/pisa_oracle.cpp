@@ -31,6 +31,12 @@
 //     the cache pyramid equals a fresh build bit for bit.
 //  R9 scores are natural-log LSEs, summed over the group's heads without weights;
 //     logits are scale * q.k with scale = 1/sqrt(d) unless given.
+//  R10 the two ablation scorings are the first- and second-order truncations of the
+//     LSE's expansion around the mean of the block's m eligible child logits z ("Core
+//     method", eqs. 32-34): PISA-1 = log m + mean(z), PISA-2 = log m + mean(z) +
+//     Var(z) / 2 with the population variance (divisor m).  They replace the LSE at
+//     every scored level and at the exact leaf level; the head sum, SelectK and the
+//     final top-K are unchanged.
 //
 // Precision: bf16 inputs are widened exactly; every sum, exp and log is fp64.
 // Parallelism: independent rows are split across std::threads; every output element is
@@ -175,6 +181,7 @@ struct Row {
   int d, C, g, K, GQ;
   bool causal;
   double scale;
+  int scoring;                         // 0 LSE, 1 PISA-1, 2 PISA-2
   std::vector<double> q;               // GQ x d, widened
 };
 
@@ -207,7 +214,25 @@ double logsumexp(const std::vector<double>& z) {
   return m + std::log(s);
 }
 
-// eq. 21 for a level-l candidate (l >= 2): LSE over its eligible level-(l-1) children,
+// The score of one block from its m eligible child logits z: the LSE (eq. 21), or its
+// first- (PISA-1) or second-order (PISA-2) truncation around the mean (reading R10).
+double block_score(const std::vector<double>& z, int scoring) {
+  if (scoring == 0) return logsumexp(z);
+  if (z.empty()) return NEG_INF;
+  const double m = (double)z.size();
+  double mean = 0;
+  for (double v : z) mean += v;
+  mean /= m;
+  double s = std::log(m) + mean;
+  if (scoring == 2) {
+    double var = 0;
+    for (double v : z) var += (v - mean) * (v - mean);
+    s += 0.5 * var / m;
+  }
+  return s;
+}
+
+// eq. 21 for a level-l candidate (l >= 2): the score of its eligible level-(l-1) children,
 // summed over the group's heads (eq. 22).
 double score_internal(const Row& R, int l, long long i) {
   double u = 0;
@@ -215,7 +240,7 @@ double score_internal(const Row& R, int l, long long i) {
     std::vector<double> z;
     for (long long r = R.g * i; r < R.g * i + R.g; ++r)
       if (eligible(R, l - 1, r)) z.push_back(R.scale * dot_node(R, h, l - 1, r));
-    u += logsumexp(z);
+    u += block_score(z, R.scoring);
   }
   return u;
 }
@@ -229,7 +254,7 @@ double score_leaf(const Row& R, long long j) {
     std::vector<double> z;
     for (long long c = c0; c < c1; ++c)
       if (!R.causal || c <= R.t) z.push_back(R.scale * dot_key(R, h, c));
-    u += logsumexp(z);
+    u += block_score(z, R.scoring);
   }
   return u;
 }
@@ -400,8 +425,9 @@ int admissible_walk(const Row& R, int l, const std::vector<long long>& S, const 
 
 Row make_row(const uint16_t* Q_row /* GQ x d for this (b, t, group) */, const uint16_t* Kbg, const uint16_t* Pbg,
              const std::vector<long long>* off, long long n, long long t, int d, int C, int g, int K, int GQ,
-             int causal, double scale) {
+             int causal, double scale, int scoring) {
   Row R;
+  R.scoring = scoring;
   R.Kbg = Kbg;
   R.Pbg = Pbg;
   R.off = off;
@@ -502,8 +528,9 @@ int oracle_build_pyramid(const uint16_t* K, uint16_t* P, int B, int H_kv, long l
 //   min_gap: smallest K-th/(K+1)-th score gap met at any SelectK of the walk
 int oracle_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int B, long long N, int H_q, int H_kv,
                   int d, int C, int g, int Ksel, int causal, double scale, int nrows, const long long* rows,
-                  int32_t* idx, int32_t* s2, int32_t* cand, double* cand_score, double* min_gap, int nthreads) {
-  if (H_kv <= 0 || H_q % H_kv != 0 || Ksel < 1) return 1;
+                  int32_t* idx, int32_t* s2, int32_t* cand, double* cand_score, double* min_gap, int nthreads,
+                  int scoring) {
+  if (H_kv <= 0 || H_q % H_kv != 0 || Ksel < 1 || scoring < 0 || scoring > 2) return 1;
   int GQ = H_q / H_kv;
   std::vector<long long> off = level_offsets(N, C, g);
   long long nodes = oracle_pyramid_nodes(N, C, g);
@@ -517,7 +544,7 @@ int oracle_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int B
       }
       const uint16_t* qrow = Q + ((b * N + t) * H_q + hk * GQ) * d;
       Row R = make_row(qrow, K + (b * H_kv + hk) * N * d, P + (b * H_kv + hk) * nodes * d, &off, N, t, d, C, g, Ksel,
-                       GQ, causal, scale);
+                       GQ, causal, scale, scoring);
       Selection S = select_row(R);
       for (int i = 0; i < Ksel; ++i) idx[r * Ksel + i] = i < (int)S.final_set.size() ? (int32_t)S.final_set[i] : -1;
       if (s2)
@@ -538,7 +565,7 @@ int oracle_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int B
 int oracle_selection_admissible(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int B, long long N, int H_q,
                                 int H_kv, int d, int C, int g, int Ksel, int causal, double scale, int nrows,
                                 const long long* rows, const int32_t* target_idx, double tol, int32_t* ok,
-                                int nthreads) {
+                                int nthreads, int scoring) {
   int GQ = H_q / H_kv;
   std::vector<long long> off = level_offsets(N, C, g);
   long long nodes = oracle_pyramid_nodes(N, C, g);
@@ -547,7 +574,7 @@ int oracle_selection_admissible(const uint16_t* Q, const uint16_t* K, const uint
       long long b = rows[3 * r], hk = rows[3 * r + 1], t = rows[3 * r + 2];
       const uint16_t* qrow = Q + ((b * N + t) * H_q + hk * GQ) * d;
       Row R = make_row(qrow, K + (b * H_kv + hk) * N * d, P + (b * H_kv + hk) * nodes * d, &off, N, t, d, C, g, Ksel,
-                       GQ, causal, scale);
+                       GQ, causal, scale, scoring);
       std::vector<long long> target;
       for (int i = 0; i < Ksel; ++i)
         if (target_idx[r * Ksel + i] >= 0) target.push_back(target_idx[r * Ksel + i]);
@@ -595,7 +622,7 @@ int oracle_sparse_attention(const uint16_t* Q, const uint16_t* K, const uint16_t
 // idx_out [B][H_kv][Ksel] (nullable).  seq_len is advanced by one.
 int oracle_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
                        uint16_t* Pc, int32_t* seq_len, long long N_cap, int B, int H_q, int H_kv, int d, int C, int g,
-                       int Ksel, double scale, double* o, double* lse, int32_t* idx_out, int nthreads) {
+                       int Ksel, double scale, double* o, double* lse, int32_t* idx_out, int nthreads, int scoring) {
   if (H_kv <= 0 || H_q % H_kv != 0) return 1;
   for (int b = 0; b < B; ++b)
     if (seq_len[b] < 0 || seq_len[b] + 1 > N_cap) return 2;
@@ -635,7 +662,7 @@ int oracle_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
         for (int e2 = 0; e2 < d; ++e2) Pbg[(off[l] + node) * d + e2] = f64_to_bf16_rne(acc[e2] / (double)(r1 - r0));
       }
       // selection for the query at T
-      Row R = make_row(q + (b * H_q + hk * GQ) * d, Kbg, Pbg, &off, n, T, d, C, g, Ksel, GQ, 1, scale);
+      Row R = make_row(q + (b * H_q + hk * GQ) * d, Kbg, Pbg, &off, n, T, d, C, g, Ksel, GQ, 1, scale, scoring);
       Selection S = select_row(R);
       std::vector<int32_t> blocks(Ksel, -1);
       for (int i = 0; i < Ksel && i < (int)S.final_set.size(); ++i) blocks[i] = (int32_t)S.final_set[i];

@@ -217,6 +217,67 @@ def pin_lse_beats_mean(o):
     assert list(r["idx"][0]) == [1, 3], r["idx"]
 
 
+def _spike_case_scored(o, t, scoring, K_sel=2):
+    d, C, N = 64, 64, 128
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 0:64, 0] = f2b(1.0)
+    K[0, 0, 64 + 10, 0] = f2b(6.0)
+    P = o.build_pyramid(K)
+    r = o.select(Q, K, P, K_sel, np.array([[0, 0, t]]), scale=1.0 / 8.0, scoring=scoring)
+    return {int(j): s for j, s in zip(r["cand"][0], r["cand_score"][0]) if j >= 0}
+
+
+def pin_scoring_variants_closed_forms(o):
+    """PISA-1 and PISA-2 leaf scores are the first- and second-order truncations of the LSE
+    around the mean of the block's logits (golden closed forms, population variance)."""
+    g = {name: float(v) for name, v in read_golden("scoring_variants.txt")}
+    p1, p2 = _spike_case_scored(o, 127, 1), _spike_case_scored(o, 127, 2)
+    assert abs(p1[0] - g["pisa1_uniform_64_logit_1"]) < 1e-12, p1
+    assert abs(p2[0] - g["pisa1_uniform_64_logit_1"]) < 1e-12, p2  # zero variance
+    assert abs(p1[1] - g["pisa1_spike_6_in_64"]) < 1e-12, p1
+    assert abs(p2[1] - g["pisa2_spike_6_in_64"]) < 1e-12, p2
+    for sc in (1, 2):  # causal prefix of 6 zero logits in the own leaf
+        got = _spike_case_scored(o, 69, sc)
+        assert abs(got[1] - g["pisa12_prefix_6_of_zeros"]) < 1e-12, (sc, got)
+
+
+def pin_scoring_variants_order(o):
+    """On random inputs where no level prunes (the candidate slots are the same for every
+    scoring): PISA-1 <= LSE (Jensen: log mean exp >= mean) and PISA-1 <= PISA-2 (variance
+    >= 0), slot by slot; a single visible key gives the same score under all three."""
+    Q, K, V = _tiny_inputs(seed=21, N=64 * 6)
+    P = o.build_pyramid(K)
+    N = Q.shape[1]
+    rows = np.array([[0, 0, t] for t in range(0, N, 37)], np.int64)
+    r = [o.select(Q, K, P, 4, rows, scoring=s) for s in (0, 1, 2)]
+    assert np.array_equal(r[0]["cand"], r[1]["cand"]) and np.array_equal(r[0]["cand"], r[2]["cand"])
+    m = r[0]["cand"] >= 0
+    lse, p1, p2 = (x["cand_score"][m] for x in r)
+    assert np.all(p1 <= lse + 1e-12) and np.all(p1 <= p2 + 1e-12)
+    assert np.any(p1 < lse - 1e-6) and np.any(p2 > p1 + 1e-6)
+    # query at the first key of a leaf: its own leaf has one visible key
+    t = 64 * 5
+    own = [o.select(Q, K, P, 4, np.array([[0, 0, t]]), scoring=s) for s in (0, 1, 2)]
+    vals = [x["cand_score"][0][list(x["cand"][0]).index(5)] for x in own]
+    assert abs(vals[0] - vals[1]) < 1e-12 and abs(vals[0] - vals[2]) < 1e-12, vals
+
+
+def pin_mean_scoring_ranks_like_the_mean(o):
+    """The case where LSE prefers the sharp leaf: first-order (PISA-1) scoring is the mean
+    logit plus log m, so it keeps the uniformly moderate leaf instead."""
+    d, C, N = 64, 64, 64 * 4
+    Q = np.zeros((1, N, 1, d), np.uint16)
+    Q[0, :, 0, 0] = f2b(8.0)
+    K = np.zeros((1, 1, N, d), np.uint16)
+    K[0, 0, 0:64, 0] = f2b(1.0)
+    K[0, 0, 64 + 7, 0] = f2b(6.0)
+    P = o.build_pyramid(K)
+    assert list(o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0, scoring=1)["idx"][0]) == [0, 3]
+    assert list(o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0, scoring=0)["idx"][0]) == [1, 3]
+
+
 def pin_ties_lower_index(o):
     """Identical keys everywhere: equal scores rank the lower block index first."""
     d, C, N = 16, 64, 64 * 6
@@ -429,4 +490,5 @@ ALL_PINS = [
     pin_pyramid_ragged_leaf_mean, pin_leaf_lse_closed_forms, pin_gqa_head_sum, pin_lse_beats_mean,
     pin_ties_lower_index, pin_brute_force_topk, pin_final_set_invariants, pin_walk_prunes_by_summary_lse,
     pin_dense_equivalence, pin_weights_sum_to_one, pin_single_block_at_start, pin_decode,
+    pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,
 ]

@@ -47,6 +47,12 @@ MUTANTS = {
                            "    if (false) {\n      std::vector<double> sc;\n      for (long long i : A) sc.push_back(score_internal(R, l, i));\n      double gap;")],
 }
 
+# the ablation scorings (PISA-1 / PISA-2)
+MUTANTS["variant_drops_log_m"] = [("  double s = std::log(m) + mean;", "  double s = mean;")]
+MUTANTS["variance_sample_divisor"] = [("    s += 0.5 * var / m;", "    s += 0.5 * var / (m > 1 ? m - 1 : 1);")]
+MUTANTS["variance_not_halved"] = [("    s += 0.5 * var / m;", "    s += var / m;")]
+MUTANTS["pisa1_adds_variance"] = [("  if (scoring == 2) {", "  if (scoring >= 1) {")]
+
 # "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
 MUTANTS["head_sum_drops_heads"] = [
     ("  double u = 0;\n  for (int h = 0; h < R.GQ; ++h) {\n    std::vector<double> z;\n    for (long long r",
