@@ -279,6 +279,8 @@ def run_pisa(args):
         "clocks": clk,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
     }
+    if rank == 0 and not args.no_secondary:
+        out["scoring_variants"] = scoring_variants(Q, K, P, w, ws, idx)
     if rank == 0:
         out["e2e"] = None if args.no_e2e else run_e2e(args, w, dev)
         if not args.no_secondary:
@@ -287,6 +289,34 @@ def run_pisa(args):
         out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
         print(json.dumps(out), flush=True)
     barrier(world)
+
+
+def scoring_variants(Q, K, P, w, ws, idx, steps=10, warmup=3):
+    """Selection-only time (pyramid + selection) on the same inputs for the three block
+    scorings: the LSE (PISA) and its first- and second-order truncations (PISA-1, PISA-2)."""
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+
+    res = {}
+    for name in ("lse", "pisa1", "pisa2"):
+        def sel():
+            pisa.pisa_build_pyramid(K, P=P)
+            pisa.pisa_select_prefill(Q, K, P, w.K, ws=ws, idx=idx, scoring=name)
+        for _ in range(warmup):
+            sel()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            sel()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        res[name] = {"select_ms": ms, "selection_tokens_per_s": w.B * w.N / (ms * 1e-3)}
+    if pisa.pisa_get_last_device_error() != 0:
+        raise RuntimeError("device error word set while timing the scoring variants")
+    return res
 
 
 def run_e2e(args, w, dev):

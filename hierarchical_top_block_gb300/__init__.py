@@ -28,7 +28,8 @@ class PisaError(RuntimeError):
 
 
 class pisa_params(ct.Structure):
-    _fields_ = [("C", ct.c_int), ("g", ct.c_int), ("K", ct.c_int), ("causal", ct.c_int), ("scale", ct.c_float)]
+    _fields_ = [("C", ct.c_int), ("g", ct.c_int), ("K", ct.c_int), ("causal", ct.c_int), ("scale", ct.c_float),
+                ("scoring", ct.c_int)]
 
 
 class pisa_shape(ct.Structure):
@@ -95,8 +96,14 @@ def _bf16(t, name):
         raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
 
 
-def make_params(K: int, causal: bool = True, scale: float = 0.0, C: int = 64, g: int = 2) -> pisa_params:
-    return pisa_params(C, g, K, 1 if causal else 0, float(scale))
+# block scores: the LSE (PISA) or its first- / second-order truncations (PISA-1, PISA-2)
+SCORING = {"lse": 0, "pisa1": 1, "pisa2": 2}
+
+
+def make_params(K: int, causal: bool = True, scale: float = 0.0, C: int = 64, g: int = 2,
+                scoring: int | str = 0) -> pisa_params:
+    sc = SCORING[scoring] if isinstance(scoring, str) else int(scoring)
+    return pisa_params(C, g, K, 1 if causal else 0, float(scale), sc)
 
 
 def make_shape(B, N, H_q, H_kv, d, N_cap=0) -> pisa_shape:
@@ -150,14 +157,15 @@ def pisa_build_pyramid(K: torch.Tensor, N: int | None = None, P: torch.Tensor | 
 
 # ---- step 2 -----------------------------------------------------------------------------
 def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float = 0.0, want_scores: bool = False,
-                        want_s2: bool = False, ws: torch.Tensor | None = None, idx: torch.Tensor | None = None):
+                        want_s2: bool = False, ws: torch.Tensor | None = None, idx: torch.Tensor | None = None,
+                        scoring: int | str = 0):
     """Returns idx [B, H_kv, N, K_sel] int32 (and leaf_score, s2 if asked)."""
     for t, n in ((Q, "Q"), (K, "K"), (P, "P")):
         _bf16(t, n)
     B, N, H_q, d = Q.shape
     H_kv = K.shape[1]
     shape = make_shape(B, N, H_q, H_kv, d, N)
-    params = make_params(K_sel, causal, scale)
+    params = make_params(K_sel, causal, scale, scoring=scoring)
     need = pisa_select_workspace_bytes(shape, params)
     if need == 0 and B * N > 0:
         raise PisaError(2, "pisa_select_prefill: unsupported shape or parameters")
@@ -178,7 +186,7 @@ def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float =
 
 
 def pisa_select_prefill_noalloc(Q, K, P, K_sel: int, causal: bool = True, scale: float = 0.0, idx=None,
-                                leaf_score=None, s2=None):
+                                leaf_score=None, s2=None, scoring: int | str = 0):
     """pisa_select_prefill without a caller-supplied workspace: the library's fixed 32 MiB
     device scratch is used instead (for callers that cannot allocate device memory).
     Output tensors may be passed in so that the call itself allocates nothing."""
@@ -189,7 +197,8 @@ def pisa_select_prefill_noalloc(Q, K, P, K_sel: int, causal: bool = True, scale:
     if idx is None:
         idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
     _check(lib().pisa_select_prefill_noalloc(_ptr(Q), _ptr(K), _ptr(P), _ptr(idx), _ptr(leaf_score), _ptr(s2),
-                                             make_shape(B, N, H_q, H_kv, d, N), make_params(K_sel, causal, scale),
+                                             make_shape(B, N, H_q, H_kv, d, N),
+                                             make_params(K_sel, causal, scale, scoring=scoring),
                                              _stream(Q)), "pisa_select_prefill_noalloc")
     return idx
 
@@ -216,12 +225,12 @@ def pisa_sparse_attn_prefill(Q, K, V, idx, causal: bool = True, scale: float = 0
 
 
 def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, scale: float = 0.0, dev_ws=None,
-                      O_host=None, LSE_host=None, idx_host=None, device=None):
+                      O_host=None, LSE_host=None, idx_host=None, device=None, scoring: int | str = 0):
     """Whole prefill from host (ideally pinned) tensors; copies happen inside the call."""
     B, N, H_q, d = Q_host.shape
     H_kv = K_host.shape[1]
     shape = make_shape(B, N, H_q, H_kv, d, N)
-    params = make_params(K_sel, causal, scale)
+    params = make_params(K_sel, causal, scale, scoring=scoring)
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     need = pisa_prefill_host_workspace_bytes(shape, params)
     if dev_ws is None or dev_ws.numel() < need:
@@ -236,7 +245,8 @@ def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, s
 
 
 # ---- step 3 -----------------------------------------------------------------------------
-def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.0, o=None, lse=None, idx_out=None):
+def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.0, o=None, lse=None, idx_out=None,
+                     scoring: int | str = 0):
     """One decode step for every sequence; caches and seq_len are updated in place."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (Kc, "Kc"), (Vc, "Vc"), (Pc, "Pc")):
         _bf16(t, n)
@@ -249,6 +259,7 @@ def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.
         o = torch.empty_like(q)
     shape = make_shape(B, 0, H_q, H_kv, d, N_cap)
     _check(lib().pisa_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), _ptr(o),
-                                  _ptr(lse), _ptr(idx_out), shape, make_params(K_sel, True, scale), _stream(q)),
+                                  _ptr(lse), _ptr(idx_out), shape, make_params(K_sel, True, scale, scoring=scoring),
+                                  _stream(q)),
            "pisa_decode_step")
     return o

@@ -92,6 +92,7 @@ pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p)
   if (pr.C != 64 || pr.g != 2 || (s.d != 64 && s.d != 128)) return PISA_ERR_UNSUPPORTED;
   if (pr.K < 1 || pr.K > 16) return PISA_ERR_UNSUPPORTED;
   if (pr.causal != 0 && pr.causal != 1) return PISA_ERR_INVALID_ARG;
+  if (pr.scoring < 0 || pr.scoring > 2) return PISA_ERR_INVALID_ARG;
   if (s.H_q % s.H_kv != 0) return PISA_ERR_INVALID_ARG;
   const int gq = s.H_q / s.H_kv;
   if (gq != 1 && gq != 2 && gq != 4 && gq != 8 && gq != 16) return PISA_ERR_UNSUPPORTED;
@@ -110,6 +111,7 @@ pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p)
   p->g = pr.g;
   p->K = pr.K;
   p->causal = pr.causal;
+  p->scoring = pr.scoring;
   p->scale = pr.scale > 0.f ? pr.scale : 1.0f / sqrtf((float)s.d);
   p->GQ = gq;
   return PISA_OK;

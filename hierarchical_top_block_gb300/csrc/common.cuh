@@ -96,6 +96,22 @@ constexpr float NEG_INF = -__builtin_huge_valf();
 constexpr float POS_INF = __builtin_huge_valf();
 constexpr float LN2 = 0.6931471805599453f;
 
+// Score of a block with one or two eligible children of logits a, b (raw q.k; s = scale *
+// log2(e) > 0), in log2 units: scoring 0 log2(2^(as) + 2^(bs)); 1 log2 m + mean; 2 adds the
+// variance term Var(z)/2 of the natural-log form, which is ln(2)/2 * Var(x) for x = logit * s.
+__device__ __forceinline__ float pair_score(float a, float b, bool has_b, float s, int scoring) {
+  if (!has_b) return a * s;
+  if (scoring == 0) {
+    const float m = fmaxf(a, b);
+    const float n = fminf(a, b);
+    return fmaf(m, s, fast_log2(1.0f + fast_exp2((n - m) * s)));
+  }
+  const float xa = a * s, xb = b * s;
+  float r = 1.0f + 0.5f * (xa + xb);
+  if (scoring == 2) r += 0.125f * LN2 * (xa - xb) * (xa - xb);
+  return r;
+}
+
 // ---- mbarrier --------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -21,13 +21,6 @@ constexpr int WARPS = 4;
 constexpr int THREADS = 32 * WARPS;
 
 
-// log2(2^(a s) + 2^(b s)) for s > 0; only a when b is absent
-__device__ __forceinline__ float lse2_scaled(float a, float b, bool has_b, float s) {
-  if (!has_b) return a * s;
-  const float m = fmaxf(a, b), n = fminf(a, b);
-  return fmaf(m, s, fast_log2(1.0f + fast_exp2((n - m) * s)));
-}
-
 struct DecodeParams {
   const uint16_t* q;
   const uint16_t* k;
@@ -40,6 +33,7 @@ struct DecodeParams {
   float* lse;
   int32_t* idx_out;
   int H_q, H_kv, GQ, Ksel, N_cap;
+  int scoring;  // 0 LSE, 1 log m + mean, 2 log m + mean + variance / 2
   float sl2;
   long long nodes;          // P rows per (b, h_kv) in the capacity layout
   long long off[MAX_LEVELS + 1];
@@ -220,10 +214,10 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
           }
         }
         float part = 0.f;
-        if (2 * q < p.GQ) part += lse2_scaled(a0[0], a0[2], v1, p.sl2);
-        if (2 * q + 1 < p.GQ) part += lse2_scaled(a0[1], a0[3], v1, p.sl2);
-        if (8 + 2 * q < p.GQ) part += lse2_scaled(a1[0], a1[2], v1, p.sl2);
-        if (9 + 2 * q < p.GQ) part += lse2_scaled(a1[1], a1[3], v1, p.sl2);
+        if (2 * q < p.GQ) part += pair_score(a0[0], a0[2], v1, p.sl2, p.scoring);
+        if (2 * q + 1 < p.GQ) part += pair_score(a0[1], a0[3], v1, p.sl2, p.scoring);
+        if (8 + 2 * q < p.GQ) part += pair_score(a1[0], a1[2], v1, p.sl2, p.scoring);
+        if (9 + 2 * q < p.GQ) part += pair_score(a1[1], a1[3], v1, p.sl2, p.scoring);
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         if (q == 0) lvl_score[par][ci] = vc ? part : NEG_INF;
@@ -289,6 +283,46 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       }
     }
     // acc[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0, 1}
+    float lse2_0, lse2_1;
+    if (p.scoring != 0) {
+      // truncated forms over the m visible keys, log2 units: log2 m + mean (+ ln2/2 Var)
+      const int m = (int)min(T - key0 + 1, 64LL);
+      float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (key0 + 8 * nt + 2 * q + c <= T) {
+            m0 += acc[nt][c] * p.sl2;
+            m1 += acc[nt][2 + c] * p.sl2;
+          }
+      m0 += __shfl_xor_sync(0xffffffffu, m0, 1);
+      m0 += __shfl_xor_sync(0xffffffffu, m0, 2);
+      m1 += __shfl_xor_sync(0xffffffffu, m1, 1);
+      m1 += __shfl_xor_sync(0xffffffffu, m1, 2);
+      m0 /= (float)m;
+      m1 /= (float)m;
+      lse2_0 = fast_log2((float)m) + m0;
+      lse2_1 = fast_log2((float)m) + m1;
+      if (p.scoring == 2) {
+        float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            if (key0 + 8 * nt + 2 * q + c <= T) {
+              const float d0 = acc[nt][c] * p.sl2 - m0, d1 = acc[nt][2 + c] * p.sl2 - m1;
+              v0 = fmaf(d0, d0, v0);
+              v1 = fmaf(d1, d1, v1);
+            }
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+        lse2_0 += 0.5f * LN2 * v0 / (float)m;
+        lse2_1 += 0.5f * LN2 * v1 / (float)m;
+      }
+    } else {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -303,7 +337,6 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
     s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
     s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
     s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-    float lse2_0, lse2_1;
     if (s0 > 0.f && s0 < POS_INF && s1 > 0.f && s1 < POS_INF) {
       lse2_0 = fast_log2(s0);
       lse2_1 = fast_log2(s1);
@@ -336,6 +369,7 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
       lse2_0 = m0 + fast_log2(s0);
       lse2_1 = m1 + fast_log2(s1);
+    }
     }
     float part = (r < p.GQ ? lse2_0 : 0.f) + (r + 8 < p.GQ ? lse2_1 : 0.f);
     if (q != 0) part = 0.f;
@@ -560,6 +594,7 @@ cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
   p.H_kv = pr.H_kv;
   p.GQ = pr.GQ;
   p.Ksel = pr.K;
+  p.scoring = pr.scoring;
   p.N_cap = pr.N_cap;
   p.sl2 = pr.scale * LOG2E;
   p.nodes = geo_cap.nodes;

@@ -8,6 +8,7 @@ namespace pisa {
 struct Problem {
   int B, N, N_cap, H_q, H_kv, d;
   int C, g, K, causal;
+  int scoring;  // 0 LSE, 1 log m + mean, 2 log m + mean + variance / 2
   float scale;  // logit scale (already resolved; > 0)
   int GQ;       // H_q / H_kv
 };

@@ -61,6 +61,7 @@ struct Params {
   float* leaf_score;
   int N, H_q, H_kv, GQ, RPQ, Ksel, M1, causal;
   int qgrp;   // 1: one 4-D box per query, stage layout [query][8-row group][d half][8][64]
+  int scoring;  // 0 LSE, 1 log m + mean, 2 log m + mean + variance / 2
   float sl2;  // scale * log2(e)
 };
 
@@ -296,7 +297,29 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         if (prm.causal && (long long)t - key0 < lim64) lim64 = (long long)t - key0;
         const int lim = (int)(lim64 < 63 ? lim64 : 63);
         float lse2 = NEG_INF;
-        if (leaf_ok && h < prm.GQ) {
+        if (leaf_ok && h < prm.GQ && prm.scoring != 0) {
+          // truncated forms over the m = lim + 1 visible keys, log2 units: log2 m + mean,
+          // plus ln2/2 * Var for the second order
+          const float inv_m = 1.f / (float)(lim + 1);
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            a0 += (j <= lim) ? __uint_as_float(v[j]) * prm.sl2 : 0.f;
+            a1 += (j + 1 <= lim) ? __uint_as_float(v[j + 1]) * prm.sl2 : 0.f;
+          }
+          const float mean = (a0 + a1) * inv_m;
+          lse2 = fast_log2((float)(lim + 1)) + mean;
+          if (prm.scoring == 2) {
+            float q0 = 0.f, q1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+              const float d0 = __uint_as_float(v[j]) * prm.sl2 - mean, d1 = __uint_as_float(v[j + 1]) * prm.sl2 - mean;
+              q0 += (j <= lim) ? d0 * d0 : 0.f;
+              q1 += (j + 1 <= lim) ? d1 * d1 : 0.f;
+            }
+            lse2 += 0.5f * LN2 * (q0 + q1) * inv_m;
+          }
+        } else if (leaf_ok && h < prm.GQ) {
           // four independent partial sums; the mask is only needed inside the own block
           float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
           if (lim >= 63) {
@@ -386,6 +409,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
   prm.Ksel = p.K;
   prm.M1 = geo.M[1];
   prm.causal = p.causal;
+  prm.scoring = p.scoring;
   prm.sl2 = p.scale * LOG2E;
   const size_t smem = (size_t)(NQS + NKS) * ROWS * D * 2 + 1024;
   cudaError_t e = cudaFuncSetAttribute(leaf_lse_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

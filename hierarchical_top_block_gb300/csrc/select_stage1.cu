@@ -26,19 +26,11 @@ constexpr int THREADS = 128;
 constexpr int MIN_BLOCKS_128 = 5, MIN_BLOCKS_64 = 6;
 
 
-// log2(2^(a s) + 2^(b s)) for s > 0; only a when b is absent
-__device__ __forceinline__ float lse2_scaled(float a, float b, bool has_b, float s) {
-  if (!has_b) return a * s;
-  const float m = fmaxf(a, b);
-  const float n = fminf(a, b);
-  return fmaf(m, s, fast_log2(1.0f + fast_exp2((n - m) * s)));
-}
-
 template <int D>
 __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCKS_64) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
-                                                         float scale_log2, Geometry geo) {
+                                                         int scoring, float scale_log2, Geometry geo) {
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
   constexpr int KH = NCH / 2;      // chunks loaded together
   __shared__ int lists[THREADS / 32][32];
@@ -153,12 +145,12 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
             }
           }
         }
-        // per head: log2(2^x0 + 2^x1), x = logit * scale * log2(e); child 1 may be absent
+        // per head: the pair score (LSE or one of its truncations), log2 units; child 1 may be absent
         float part = 0.f;
-        if (2 * q < GQ) part += lse2_scaled(a0[0], a0[2], v1, scale_log2);
-        if (2 * q + 1 < GQ) part += lse2_scaled(a0[1], a0[3], v1, scale_log2);
-        if (8 + 2 * q < GQ) part += lse2_scaled(a1[0], a1[2], v1, scale_log2);
-        if (9 + 2 * q < GQ) part += lse2_scaled(a1[1], a1[3], v1, scale_log2);
+        if (2 * q < GQ) part += pair_score(a0[0], a0[2], v1, scale_log2, scoring);
+        if (2 * q + 1 < GQ) part += pair_score(a0[1], a0[3], v1, scale_log2, scoring);
+        if (8 + 2 * q < GQ) part += pair_score(a1[0], a1[2], v1, scale_log2, scoring);
+        if (9 + 2 * q < GQ) part += pair_score(a1[1], a1[3], v1, scale_log2, scoring);
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         // candidate 8mt + r's score (held by lanes 4r..4r+3) to lane 8mt + r
@@ -217,9 +209,11 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
   if (blocks > cap) blocks = cap;
   const float sl2 = p.scale * LOG2E;
   if (p.d == 128)
-    stage1_kernel<128><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, sl2, geo);
+    stage1_kernel<128><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scoring, sl2,
+                                                       geo);
   else
-    stage1_kernel<64><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, sl2, geo);
+    stage1_kernel<64><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scoring, sl2,
+                                                       geo);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,11 @@ typedef struct {
   int K;        /* blocks kept per query (SelectK and the final top-K) */
   int causal;   /* 1: query t sees keys <= t and blocks starting <= t; own block kept */
   float scale;  /* logit scale; <= 0 selects 1/sqrt(d) */
+  int scoring;  /* block score from a block's m eligible child logits z (summary page,
+                   "Core method", eq. 21 and its expansion, eqs. 32-34): 0 = PISA, the LSE;
+                   1 = PISA-1, log m + mean(z); 2 = PISA-2, log m + mean(z) + Var(z)/2
+                   (population variance).  Used at every scored level and at the leaf level;
+                   the head sum, SelectK and the final top-K are the same for all three. */
 } pisa_params;
 
 typedef struct {

@@ -57,9 +57,9 @@ def pyramid_equal(P_gpu, P_ref, n, n_cap):
     return True
 
 
-def check_selection(o, Qb, Kb, Pb, K_sel, rows, gpu_idx, gpu_s2=None, gpu_score=None, causal=True):
+def check_selection(o, Qb, Kb, Pb, K_sel, rows, gpu_idx, gpu_s2=None, gpu_score=None, causal=True, scoring=0):
     """rows: int64 [R, 3] (b, h_kv, t); gpu_*: arrays [R, ...].  Returns a small report dict."""
-    ref = o.select(Qb, Kb, Pb, K_sel, rows, causal=causal)
+    ref = o.select(Qb, Kb, Pb, K_sel, rows, causal=causal, scoring=scoring)
     clear = ref["min_gap"] >= GAP_TOL
     same_idx = np.all(ref["idx"] == gpu_idx, axis=1)
     bad_clear = np.where(clear & ~same_idx)[0]
@@ -71,7 +71,7 @@ def check_selection(o, Qb, Kb, Pb, K_sel, rows, gpu_idx, gpu_s2=None, gpu_score=
         assert bad.size == 0, f"S2 differs on clear-gap row {rows[bad[0]]}: gpu {gpu_s2[bad[0]]} oracle {ref['s2'][bad[0]]}"
     amb = np.where(~same_idx)[0]
     if amb.size:
-        ok = o.admissible(Qb, Kb, Pb, K_sel, rows[amb], gpu_idx[amb], tol=GAP_TOL, causal=causal)
+        ok = o.admissible(Qb, Kb, Pb, K_sel, rows[amb], gpu_idx[amb], tol=GAP_TOL, causal=causal, scoring=scoring)
         assert np.all(ok == 1), f"{int(np.sum(ok != 1))} ambiguous rows are not admissible: {rows[amb][ok != 1][:3]}"
     if gpu_score is not None and gpu_s2 is not None:
         same_s2 = np.all(ref["s2"] == gpu_s2, axis=1)
@@ -97,21 +97,22 @@ def check_attention(o, Qb, Kb, Vb, idx_np, rows_bt, gpu_O, gpu_LSE, causal=True)
     return dict(max_abs_O=float(err_o), max_abs_LSE=float(err_l))
 
 
-def run_gpu_prefill(Q, K, V, K_sel, causal=True):
+def run_gpu_prefill(Q, K, V, K_sel, causal=True, scoring=0):
     """Runs pyramid, selection and attention; returns CPU copies."""
     P = pisa.pisa_build_pyramid(K)
-    idx, score, s2 = pisa.pisa_select_prefill(Q, K, P, K_sel, causal=causal, want_scores=True, want_s2=True)
+    idx, score, s2 = pisa.pisa_select_prefill(Q, K, P, K_sel, causal=causal, want_scores=True, want_s2=True,
+                                              scoring=scoring)
     O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx, causal=causal)
     torch.cuda.synchronize()
     assert pisa.pisa_get_last_device_error() == 0
     return dict(P=P, idx=idx.cpu().numpy(), score=score.cpu().numpy(), s2=s2.cpu().numpy(), O=O, LSE=LSE.cpu().numpy())
 
 
-def full_prefill_check(o, Q, K, V, K_sel, causal=True, sample=None, seed=0):
+def full_prefill_check(o, Q, K, V, K_sel, causal=True, sample=None, seed=0, scoring=0):
     """Q, K, V on the GPU; the oracle gets bit-identical CPU copies."""
     B, N, H_q, d = Q.shape
     H_kv = K.shape[1]
-    res = run_gpu_prefill(Q, K, V, K_sel, causal)
+    res = run_gpu_prefill(Q, K, V, K_sel, causal, scoring)
     Qb, Kb, Vb = to_np_bits(Q), to_np_bits(K), to_np_bits(V)
     Pb = o.build_pyramid(Kb)
     assert np.array_equal(to_np_bits(res["P"]), Pb), "pyramid differs from the oracle"
@@ -125,7 +126,7 @@ def full_prefill_check(o, Q, K, V, K_sel, causal=True, sample=None, seed=0):
     gi = res["idx"][rows[:, 0], rows[:, 1], rows[:, 2]]
     gs2 = res["s2"][rows[:, 0], rows[:, 1], rows[:, 2]]
     gsc = res["score"][rows[:, 0], rows[:, 1], rows[:, 2]]
-    rep = check_selection(o, Qb, Kb, Pb, K_sel, rows, gi, gs2, gsc, causal=causal)
+    rep = check_selection(o, Qb, Kb, Pb, K_sel, rows, gi, gs2, gsc, causal=causal, scoring=scoring)
     bt = np.unique(rows[:, [0, 2]], axis=0)
     O = res["O"].float().cpu().numpy()[bt[:, 0], bt[:, 1]]
     LSE = np.transpose(res["LSE"], (0, 2, 1))[bt[:, 0], bt[:, 1]]

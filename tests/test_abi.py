@@ -64,6 +64,8 @@ def test_argument_errors_without_a_gpu(lib):
     # unsupported head dim / group size / block size
     assert lib.pisa_build_pyramid(None, None, pisa.make_shape(1, 128, 4, 1, 80), pisa.make_params(4), None) == 2
     assert lib.pisa_build_pyramid(None, None, shape, pisa.make_params(4, C=32), None) == 2
+    # a scoring other than LSE / PISA-1 / PISA-2 is an argument error
+    assert lib.pisa_build_pyramid(None, None, shape, pisa.make_params(4, scoring=3), None) == 1
     # empty problems are a no-op
     assert lib.pisa_build_pyramid(None, None, pisa.make_shape(0, 128, 4, 1, 64), pisa.make_params(4), None) == 0
     assert lib.pisa_status_string(2).decode() == "unsupported shape or parameter"

@@ -143,7 +143,7 @@ def test_prefill_256k_sampled(oracle_impl):
     H.check_attention(oracle_impl, Qb, Kb, Vb, res["idx"], bt, O, LSE)
 
 
-def _decode_check(o, w, N0, steps, N_cap, pairs=None):
+def _decode_check(o, w, N0, steps, N_cap, pairs=None, scoring=0):
     """Runs the GPU decode for `steps` steps from N0 cached tokens and checks every step on
     the (sequence, KV head) pairs given: the pyramid cache (bit-exact), idx (gap rule) and
     o / lse.  The oracle runs each pair as its own one-sequence, one-KV-head problem."""
@@ -173,14 +173,14 @@ def _decode_check(o, w, N0, steps, N_cap, pairs=None):
         out = torch.empty(B, H_q, d, dtype=torch.bfloat16, device="cuda")
         lse = torch.empty(B, H_q, dtype=torch.float32, device="cuda")
         idx = torch.empty(B, H_kv, K_sel, dtype=torch.int32, device="cuda")
-        pisa.pisa_decode_step(q, k, v, Kc, Vc, Pc, seq, K_sel, o=out, lse=lse, idx_out=idx)
+        pisa.pisa_decode_step(q, k, v, Kc, Vc, Pc, seq, K_sel, o=out, lse=lse, idx_out=idx, scoring=scoring)
         torch.cuda.synchronize()
         assert pisa.pisa_get_last_device_error() == 0
         qn, kn, vn = W.bits(q), W.bits(k), W.bits(v)
         for (b, g), (kc, vc, pc, sl) in ref.items():
             T = int(sl[0])
             ro, rl, ri = o.decode_step(qn[b:b + 1, g * G:(g + 1) * G].copy(), kn[b:b + 1, g:g + 1].copy(),
-                                       vn[b:b + 1, g:g + 1].copy(), kc, vc, pc, sl, K_sel)
+                                       vn[b:b + 1, g:g + 1].copy(), kc, vc, pc, sl, K_sel, scoring=scoring)
             assert H.pyramid_equal(W.bits(Pc[b, g]), pc[0, 0], T + 1, N_cap), f"pyramid cache differs at step {s}, pair {(b, g)}"
             gi = idx[b, g].cpu().numpy()
             if not np.array_equal(gi, ri[0, 0]):
@@ -188,7 +188,8 @@ def _decode_check(o, w, N0, steps, N_cap, pairs=None):
                 Qp = np.zeros((1, n, G, d), np.uint16)
                 Qp[0, T] = qn[b, g * G:(g + 1) * G]
                 Kp = kc[:, :, :n].copy()
-                H.check_selection(o, Qp, Kp, o.build_pyramid(Kp), K_sel, np.array([(0, 0, T)], np.int64), gi[None])
+                H.check_selection(o, Qp, Kp, o.build_pyramid(Kp), K_sel, np.array([(0, 0, T)], np.int64), gi[None],
+                                  scoring=scoring)
             go = out[b, g * G:(g + 1) * G].float().cpu().numpy()
             assert np.abs(go - ro[0]).max() <= H.ATTN_MAX_ABS, (s, b, g, np.abs(go - ro[0]).max())
             assert H.rel_l2(go, ro[0]) <= H.ATTN_REL_L2
@@ -240,3 +241,32 @@ def test_decode_full_cache_is_refused():
     assert torch.equal(Kc[0], K0[0]) and torch.equal(Vc[0], V0[0]) and torch.equal(Pc[0], P0[0])
     assert torch.equal(Kc[1, :, N0], k[1].to(Kc.dtype)) and not torch.equal(Kc[1], K0[1])
     assert seq.tolist() == [N_cap, N0 + 1]
+
+
+# ---- the ablation scorings: PISA-1 (log m + mean) and PISA-2 (+ variance / 2) ----------------
+@pytest.mark.parametrize("scoring", [1, 2])
+def test_scoring_variants_tiny_all_rows(oracle_impl, scoring):
+    w = W.WORKLOADS["tiny"]
+    Q, K, V = _inputs(w)
+    H.full_prefill_check(oracle_impl, Q, K, V, 8, scoring=scoring)
+
+
+@pytest.mark.parametrize("scoring", [1, 2])
+def test_scoring_variants_prefill_4k_sampled(oracle_impl, scoring):
+    w = W.WORKLOADS["prefill_4k"]
+    Q, K, V = _inputs(w)
+    rep = H.full_prefill_check(oracle_impl, Q, K, V, w.K, sample=512, seed=5 + scoring, scoring=scoring)
+    assert rep["rows"] == 512
+
+
+def test_scoring_variant_ragged_d128(oracle_impl):
+    N, GQ, H_kv, d, K_sel = 64 * 37 + 11, 8, 2, 128, 5
+    w = W.WORKLOADS["tiny"].with_(N=N, H_q=GQ * H_kv, H_kv=H_kv, d=d, K=K_sel)
+    Q, K, V = _inputs(w)
+    H.full_prefill_check(oracle_impl, Q, K, V, K_sel, sample=1200, seed=N, scoring=2)
+
+
+@pytest.mark.parametrize("scoring", [1, 2])
+def test_decode_scoring_variants(oracle_impl, scoring):
+    w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=8, H_kv=2, K=6)
+    _decode_check(oracle_impl, w, N0=2040, steps=12, N_cap=2304, scoring=scoring)
