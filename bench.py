@@ -285,7 +285,8 @@ def run_pisa(args):
         out["e2e"] = None if args.no_e2e else run_e2e(args, w, dev)
         if not args.no_secondary:
             out["secondary"] = {"prefill_32k": secondary_prefill(W.WORKLOADS["prefill_32k"], dev),
-                                "decode_128k": secondary_decode(W.WORKLOADS["decode_128k"], dev)}
+                                "decode_128k": secondary_decode(W.WORKLOADS["decode_128k"], dev),
+                                "selection_quality_32k": selection_quality_section(W.WORKLOADS["prefill_32k"], dev)}
         out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
         print(json.dumps(out), flush=True)
     barrier(world)
@@ -377,6 +378,32 @@ def secondary_prefill(w, dev, steps=5):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms_per_step": ms, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv}
+
+
+def selection_quality_section(w, dev, samples=96, seed=11):
+    """Recall@K against the exact leaf-LSE top-K and kept dense-attention mass, on the seeded
+    needle workload, for each block scoring and K = 8 (the pages' setting) and the workload's K."""
+    import numpy as np
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+    from hierarchical_top_block_gb300 import quality
+    import workloads as W
+
+    Q, K, V = W.prefill_inputs(w, dev)
+    P = pisa.pisa_build_pyramid(K)
+    rng = np.random.default_rng(seed)
+    rows = sorted((int(rng.integers(0, w.B)), int(t)) for t in rng.integers(64, w.N, samples))
+    res = {"samples": samples, "workload": w.name,
+           "reference": "exact top-K of the head-summed leaf LSE over all eligible blocks (own block kept)"}
+    for K_sel in sorted({8, w.K}):
+        for name in ("lse", "pisa1", "pisa2"):
+            idx = pisa.pisa_select_prefill(Q, K, P, K_sel, scoring=name)
+            torch.cuda.synchronize()
+            res[f"K{K_sel}_{name}"] = quality.selection_quality(Q, K, idx, K_sel, rows)
+    del Q, K, V, P
+    torch.cuda.empty_cache()
+    return res
 
 
 def secondary_decode(w, dev, steps=32, warmup=3):

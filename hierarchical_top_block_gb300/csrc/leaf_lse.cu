@@ -298,26 +298,49 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         const int lim = (int)(lim64 < 63 ? lim64 : 63);
         float lse2 = NEG_INF;
         if (leaf_ok && h < prm.GQ && prm.scoring != 0) {
-          // truncated forms over the m = lim + 1 visible keys, log2 units: log2 m + mean,
-          // plus ln2/2 * Var for the second order
-          const float inv_m = 1.f / (float)(lim + 1);
-          float a0 = 0.f, a1 = 0.f;
+          // truncated forms over the m = lim + 1 visible keys, log2 units: log2 m + mean(x),
+          // plus ln2/2 * Var(x) for the second order; x = logit * sl2, so the sums run on the
+          // raw logits and are scaled once (Var by sl2^2)
+          const float m = (float)(lim + 1);
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          if (lim >= 63) {
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            a0 += (j <= lim) ? __uint_as_float(v[j]) * prm.sl2 : 0.f;
-            a1 += (j + 1 <= lim) ? __uint_as_float(v[j + 1]) * prm.sl2 : 0.f;
-          }
-          const float mean = (a0 + a1) * inv_m;
-          lse2 = fast_log2((float)(lim + 1)) + mean;
-          if (prm.scoring == 2) {
-            float q0 = 0.f, q1 = 0.f;
+            for (int j = 0; j < 64; j += 4) {
+              a0 += __uint_as_float(v[j]);
+              a1 += __uint_as_float(v[j + 1]);
+              a2 += __uint_as_float(v[j + 2]);
+              a3 += __uint_as_float(v[j + 3]);
+            }
+          } else {
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
-              const float d0 = __uint_as_float(v[j]) * prm.sl2 - mean, d1 = __uint_as_float(v[j + 1]) * prm.sl2 - mean;
-              q0 += (j <= lim) ? d0 * d0 : 0.f;
-              q1 += (j + 1 <= lim) ? d1 * d1 : 0.f;
+              a0 += (j <= lim) ? __uint_as_float(v[j]) : 0.f;
+              a1 += (j + 1 <= lim) ? __uint_as_float(v[j + 1]) : 0.f;
             }
-            lse2 += 0.5f * LN2 * (q0 + q1) * inv_m;
+          }
+          const float mean = ((a0 + a1) + (a2 + a3)) / m;  // raw logits
+          lse2 = fast_log2(m) + mean * prm.sl2;
+          if (prm.scoring == 2) {
+            float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;
+            if (lim >= 63) {
+#pragma unroll
+              for (int j = 0; j < 64; j += 4) {
+                const float d0 = __uint_as_float(v[j]) - mean, d1 = __uint_as_float(v[j + 1]) - mean;
+                const float d2 = __uint_as_float(v[j + 2]) - mean, d3 = __uint_as_float(v[j + 3]) - mean;
+                q0 = fmaf(d0, d0, q0);
+                q1 = fmaf(d1, d1, q1);
+                q2 = fmaf(d2, d2, q2);
+                q3 = fmaf(d3, d3, q3);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 64; j += 2) {
+                const float d0 = __uint_as_float(v[j]) - mean, d1 = __uint_as_float(v[j + 1]) - mean;
+                q0 += (j <= lim) ? d0 * d0 : 0.f;
+                q1 += (j + 1 <= lim) ? d1 * d1 : 0.f;
+              }
+            }
+            lse2 += 0.5f * LN2 * prm.sl2 * prm.sl2 * ((q0 + q1) + (q2 + q3)) / m;
           }
         } else if (leaf_ok && h < prm.GQ) {
           // four independent partial sums; the mask is only needed inside the own block
