@@ -68,6 +68,9 @@ class Oracle:
         L.oracle_sparse_attention.restype = _I
         L.oracle_sparse_attention.argtypes = [_P, _P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _D, _I, _P, _P, _P,
                                               _P, _I]
+        L.oracle_sparse_attention_backward.restype = _I
+        L.oracle_sparse_attention_backward.argtypes = [_P, _P, _P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _D, _P,
+                                                       _P, _P, _I]
         L.oracle_decode_step.restype = _I
         L.oracle_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _P, _P,
                                          _P, _I, _I]
@@ -150,6 +153,24 @@ class Oracle:
                                               self.nthreads)
         assert rc == 0, rc
         return O, LSE, ws
+
+    def sparse_attention_backward(self, Q, K, V, idx, dO, C=64, causal=True, scale=None):
+        """Gradients of the step-4 output: Q, dO uint16 [B,N,H_q,d]; K, V [B,H_kv,N,d];
+        idx int32 [B,H_kv,N,Ksel] -> dQ [B,N,H_q,d], dK, dV [B,H_kv,N,d] (fp64)."""
+        B, N, H_q, d = Q.shape
+        H_kv = K.shape[1]
+        Ksel = idx.shape[-1]
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        dQ = np.zeros((B, N, H_q, d), np.float64)
+        dK = np.zeros((B, H_kv, N, d), np.float64)
+        dV = np.zeros((B, H_kv, N, d), np.float64)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        dO = np.ascontiguousarray(dO, dtype=np.uint16)
+        rc = self.lib.oracle_sparse_attention_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(dO), B, N, H_q,
+                                                       H_kv, d, C, Ksel, int(causal), scale, _ptr(dQ), _ptr(dK),
+                                                       _ptr(dV), self.nthreads)
+        assert rc == 0, rc
+        return dQ, dK, dV
 
     # ---- step 3 ---------------------------------------------------------------------
     def decode_step(self, q, k, v, Kc, Vc, Pc, seq_len, Ksel, C=64, g=2, scale=None, scoring=0):

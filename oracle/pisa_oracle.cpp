@@ -483,6 +483,53 @@ double attend(const uint16_t* qh, const uint16_t* Kbg, const uint16_t* Vbg, long
   return lse;
 }
 
+// Backward of attend() for one query head (the gradient of the forward function; the pages
+// give no backward): with the forward's visible positions c, s_c = scale q.k_c,
+// P_c = exp(s_c - lse), O = sum P_c v_c, D = dO.O, dP_c = dO.v_c, dS_c = P_c (dP_c - D):
+// dq += scale sum dS_c k_c, dk_c += scale dS_c q, dv_c += P_c dO.  dO is d values (fp64).
+void attend_backward(const uint16_t* qh, const uint16_t* Kbg, const uint16_t* Vbg, long long n, long long t, int d,
+                     int C, bool causal, double scale, const int32_t* blocks, int nb, const double* dO, double* dq,
+                     double* dK, double* dV) {
+  std::vector<long long> bl;
+  long long M1 = (n + C - 1) / C;
+  for (int i = 0; i < nb; ++i)
+    if (blocks[i] >= 0 && blocks[i] < M1) bl.push_back(blocks[i]);
+  std::sort(bl.begin(), bl.end());
+  bl.erase(std::unique(bl.begin(), bl.end()), bl.end());
+  std::vector<double> q(d);
+  for (int e = 0; e < d; ++e) q[e] = bf16_to_f64(qh[e]);
+  std::vector<long long> pos;
+  std::vector<double> s;
+  for (long long j : bl)
+    for (long long c = j * C; c < std::min<long long>(n, j * C + C); ++c) {
+      if (causal && c > t) continue;
+      double z = 0;
+      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);
+      pos.push_back(c);
+      s.push_back(scale * z);
+    }
+  if (pos.empty()) return;
+  const double lse = logsumexp(s);
+  std::vector<double> P(pos.size()), o(d, 0.0);
+  for (size_t i = 0; i < pos.size(); ++i) {
+    P[i] = std::exp(s[i] - lse);
+    for (int e = 0; e < d; ++e) o[e] += P[i] * bf16_to_f64(Vbg[pos[i] * d + e]);
+  }
+  double D = 0;
+  for (int e = 0; e < d; ++e) D += dO[e] * o[e];
+  for (size_t i = 0; i < pos.size(); ++i) {
+    const long long c = pos[i];
+    double dP = 0;
+    for (int e = 0; e < d; ++e) dP += dO[e] * bf16_to_f64(Vbg[c * d + e]);
+    const double dS = P[i] * (dP - D);
+    for (int e = 0; e < d; ++e) {
+      dq[e] += scale * dS * bf16_to_f64(Kbg[c * d + e]);
+      dK[c * d + e] += scale * dS * q[e];
+      dV[c * d + e] += P[i] * dO[e];
+    }
+  }
+}
+
 }  // namespace
 
 // =======================================================================================
@@ -610,6 +657,34 @@ int oracle_sparse_attention(const uint16_t* Q, const uint16_t* K, const uint16_t
         LSE[r * H_q + h] = l;
         if (wsum) wsum[r * H_q + h] = ws;
       }
+    }
+  });
+  return 0;
+}
+
+// Backward of step 4 for every query (the gradient of the forward; the pages specify none).
+// dO bf16 [B][N][H_q][d] (same layout as Q).  Outputs fp64, overwritten: dQ [B][N][H_q][d],
+// dK, dV [B][H_kv][N][d].  Work is split by (b, h_kv), so each thread owns its dK/dV rows.
+int oracle_sparse_attention_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                                     const uint16_t* dO, int B, long long N, int H_q, int H_kv, int d, int C, int Ksel,
+                                     int causal, double scale, double* dQ, double* dK, double* dV, int nthreads) {
+  if (H_kv <= 0 || H_q % H_kv != 0) return 1;
+  const int GQ = H_q / H_kv;
+  std::fill(dQ, dQ + (size_t)B * N * H_q * d, 0.0);
+  std::fill(dK, dK + (size_t)B * H_kv * N * d, 0.0);
+  std::fill(dV, dV + (size_t)B * H_kv * N * d, 0.0);
+  run_parallel((long long)B * H_kv, nthreads, [&](long long a, long long e) {
+    std::vector<double> go(d);
+    for (long long bg = a; bg < e; ++bg) {
+      const long long b = bg / H_kv, hk = bg % H_kv;
+      for (long long t = 0; t < N; ++t)
+        for (int g = 0; g < GQ; ++g) {
+          const long long h = hk * GQ + g;
+          const size_t row = ((size_t)(b * N + t) * H_q + h) * d;
+          for (int x = 0; x < d; ++x) go[x] = bf16_to_f64(dO[row + x]);
+          attend_backward(Q + row, K + bg * N * d, V + bg * N * d, N, t, d, C, causal != 0, scale,
+                          idx + (bg * N + t) * Ksel, Ksel, go.data(), dQ + row, dK + bg * N * d, dV + bg * N * d);
+        }
     }
   });
   return 0;

@@ -278,6 +278,106 @@ def pin_mean_scoring_ranks_like_the_mean(o):
     assert list(o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0, scoring=0)["idx"][0]) == [1, 3]
 
 
+# ------------------------------------------------------------------------------------
+# backward of step 4 (the gradient of the forward; the pages give none)
+# ------------------------------------------------------------------------------------
+def _bwd_case(seed, N=128, H_q=2, H_kv=1, d=16, K_sel=1):
+    rng = np.random.default_rng(seed)
+    Q, K, V = (random_bf16(rng, s, 0.5) for s in ((1, N, H_q, d), (1, H_kv, N, d), (1, H_kv, N, d)))
+    dO = random_bf16(rng, (1, N, H_q, d))
+    return Q, K, V, dO
+
+
+def pin_backward_dense_autograd(o):
+    """K >= M_1 keeps every eligible block, so step 4 is dense causal attention: its
+    gradients equal PyTorch's autograd of the textbook formula (fp64)."""
+    import torch
+    Q, K, V, dO = _bwd_case(41, N=130, H_q=4, H_kv=2, d=16)
+    N, H_q, H_kv, d = 130, 4, 2, 16
+    P = o.build_pyramid(K)
+    K_sel = 3                                     # M_1 = 3 leaves
+    rows = np.array([[0, g, t] for g in range(H_kv) for t in range(N)], np.int64)
+    idx = o.select(Q, K, P, K_sel, rows)["idx"].reshape(1, H_kv, N, K_sel)
+    dQ, dK, dV = o.sparse_attention_backward(Q, K, V, idx, dO)
+    q = torch.tensor(b2f(Q), dtype=torch.float64, requires_grad=True)
+    k = torch.tensor(b2f(K), dtype=torch.float64, requires_grad=True)
+    v = torch.tensor(b2f(V), dtype=torch.float64, requires_grad=True)
+    G = H_q // H_kv
+    kk, vv = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)          # [1, H_q, N, d]
+    s_ = torch.einsum("bthd,bhnd->bhtn", q, kk) / math.sqrt(d)
+    s_ = s_.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), -math.inf)
+    out = torch.einsum("bhtn,bhnd->bthd", torch.softmax(s_, dim=-1), vv)
+    out.backward(torch.tensor(b2f(dO)))
+    assert np.abs(dQ - q.grad.numpy()).max() < 1e-10
+    assert np.abs(dK - k.grad.numpy()).max() < 1e-10
+    assert np.abs(dV - v.grad.numpy()).max() < 1e-10
+
+
+def pin_backward_finite_differences(o):
+    """Sparse selection (K=1: the own block only in causal mode, other blocks absent): the
+    gradients match central differences of the oracle's own forward of L = sum(O * dO),
+    Richardson-extrapolated (steps 2^-6 and 2^-5, both exact in bf16 around the chosen
+    entries), for entries of Q, K and V."""
+    Q, K, V, dO = _bwd_case(43)
+    N, H_q, H_kv, d = 128, 2, 1, 16
+    idx = np.zeros((1, H_kv, N, 2), np.int32)
+    idx[0, 0, :, 0] = np.arange(N) // 64                 # own block
+    idx[0, 0, :, 1] = np.where(np.arange(N) >= 64, 0, -1)  # and block 0 for the second block
+    dQ, dK, dV = o.sparse_attention_backward(Q, K, V, idx, dO)
+    rows = np.array([[0, t] for t in range(N)], np.int64)
+    w = b2f(dO)[0]
+
+    def loss(Qx, Kx, Vx):
+        O, _, _ = o.sparse_attention(Qx, Kx, Vx, idx, rows)
+        return float((O * w).sum())
+
+    def fd(arr, pos, which):
+        base = arr.copy()
+        x0 = b2f(base[pos])
+
+        def at(delta):
+            a2 = base.copy()
+            a2[pos] = f2b(np.float32(x0 + delta))
+            args = {"Q": Q, "K": K, "V": V}
+            args[which] = a2
+            return loss(args["Q"], args["K"], args["V"])
+        h = 2.0 ** -6
+        d1 = (at(h) - at(-h)) / (2 * h)
+        d2 = (at(2 * h) - at(-2 * h)) / (4 * h)
+        return (4 * d1 - d2) / 3
+
+    rng = np.random.default_rng(5)
+    for which, arr, grad in (("Q", Q, dQ), ("K", K, dK), ("V", V, dV)):
+        for _ in range(4):
+            pos = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            x0 = float(b2f(arr[pos]))
+            arr_c = arr.copy()
+            arr_c[pos] = f2b(np.float32(np.round(x0 * 8) / 8))   # a value on a 2^-3 grid, so +-h stay exact
+            g = {"Q": Q, "K": K, "V": V}
+            g[which] = arr_c
+            ref = o.sparse_attention_backward(g["Q"], g["K"], g["V"], idx, dO)["QKV".index(which)][pos]
+            num = fd(arr_c, pos, which)
+            assert abs(ref - num) <= 2e-5 + 1e-4 * abs(num), (which, pos, ref, num)
+
+
+def pin_backward_sums(o):
+    """Per (sequence, KV head): sum over keys of dV = sum over the group's queries and heads
+    of dO (each softmax row sums to one), and sum over keys of dK = 0 (each row of dS sums
+    to zero), on a pruned selection."""
+    Q, K, V, dO = _bwd_case(47, N=64 * 6, H_q=4, H_kv=2, d=16)
+    N, H_q, H_kv = 64 * 6, 4, 2
+    P = o.build_pyramid(K)
+    rows = np.array([[0, g, t] for g in range(H_kv) for t in range(N)], np.int64)
+    idx = o.select(Q, K, P, 2, rows)["idx"].reshape(1, H_kv, N, 2)
+    dQ, dK, dV = o.sparse_attention_backward(Q, K, V, idx, dO)
+    w = b2f(dO)[0]                                   # [N, H_q, d]
+    G = H_q // H_kv
+    for g in range(H_kv):
+        assert np.abs(dV[0, g].sum(0) - w[:, g * G:(g + 1) * G].sum((0, 1))).max() < 1e-9
+        assert np.abs(dK[0, g].sum(0)).max() < 1e-9
+    assert np.abs(dK).max() > 1e-3
+
+
 def pin_ties_lower_index(o):
     """Identical keys everywhere: equal scores rank the lower block index first."""
     d, C, N = 16, 64, 64 * 6
@@ -491,4 +591,5 @@ ALL_PINS = [
     pin_ties_lower_index, pin_brute_force_topk, pin_final_set_invariants, pin_walk_prunes_by_summary_lse,
     pin_dense_equivalence, pin_weights_sum_to_one, pin_single_block_at_start, pin_decode,
     pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,
+    pin_backward_dense_autograd, pin_backward_finite_differences, pin_backward_sums,
 ]

@@ -32,12 +32,14 @@ MUTANTS = {
                              ("  if (R.causal) fin.push_back(own);\n", "")],
     "children_off_by_one": [("    for (long long r = R.g * p; r < R.g * p + R.g; ++r)\n      if (eligible(R, l, r)) out.push_back(r);",
                              "    for (long long r = R.g * p + 1; r < R.g * p + R.g + 1; ++r)\n      if (eligible(R, l, r)) out.push_back(r);")],
-    "attention_scale_missing": [("      s.push_back(scale * z);", "      s.push_back(z);")],
+    "attention_scale_missing": [("      s.push_back(scale * z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;",
+                                 "      s.push_back(z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;")],
     "eligibility_by_last_key": [("return i * ipow(R.g, l - 1) * R.C <= R.t;",
                                  "return ((i + 1) * ipow(R.g, l - 1) * R.C - 1) <= R.t;")],
     "decode_skips_ancestors": [("      for (int l = 2; l <= lv.L; ++l) {\n        node /= g;",
                                 "      for (int l = 2; l <= 1; ++l) {\n        node /= g;")],
-    "attention_ignores_causal": [("      if (causal && c > t) continue;\n", "")],
+    "attention_ignores_causal": [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;",
+                                  "      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;")],
     "double_rounding_to_bf16": [("if (std::isfinite(f) && (double)f != x) {", "if (false) {")],
     "leaf_scored_by_summary": [("if (!R.causal || c <= R.t) z.push_back(R.scale * dot_key(R, h, c));",
                                 "if (!R.causal || c <= R.t) z.push_back(R.scale * dot_node(R, h, 1, j));")],
@@ -52,6 +54,13 @@ MUTANTS["variant_drops_log_m"] = [("  double s = std::log(m) + mean;", "  double
 MUTANTS["variance_sample_divisor"] = [("    s += 0.5 * var / m;", "    s += 0.5 * var / (m > 1 ? m - 1 : 1);")]
 MUTANTS["variance_not_halved"] = [("    s += 0.5 * var / m;", "    s += var / m;")]
 MUTANTS["pisa1_adds_variance"] = [("  if (scoring == 2) {", "  if (scoring >= 1) {")]
+
+# the backward of step 4
+MUTANTS["backward_drops_D"] = [("    const double dS = P[i] * (dP - D);", "    const double dS = P[i] * dP;")]
+MUTANTS["backward_dk_without_scale"] = [("      dK[c * d + e] += scale * dS * q[e];", "      dK[c * d + e] += dS * q[e];")]
+MUTANTS["backward_dv_uses_dS"] = [("      dV[c * d + e] += P[i] * dO[e];", "      dV[c * d + e] += dS * dO[e];")]
+MUTANTS["backward_ignores_causal"] = [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;",
+                                       "      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;")]
 
 # "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
 MUTANTS["head_sum_drops_heads"] = [
