@@ -281,6 +281,7 @@ def run_pisa(args):
     }
     if rank == 0 and not args.no_secondary:
         out["scoring_variants"] = scoring_variants(Q, K, P, w, ws, idx)
+        out["backward"] = backward_section(Q, K, V, idx, O, LSE, w, work)
     if rank == 0:
         out["e2e"] = None if args.no_e2e else run_e2e(args, w, dev)
         if not args.no_secondary:
@@ -290,6 +291,43 @@ def run_pisa(args):
         out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
         print(json.dumps(out), flush=True)
     barrier(world)
+
+
+def backward_section(Q, K, V, idx, O, LSE, w, work, steps=5, warmup=3):
+    """The attention backward (dQ, dK, dV over the selected blocks) on the bench inputs with a
+    seeded upstream gradient.  Algorithmic flops: per visible (query head, key) pair,
+    2d each for S, dP and dQ (dQ kernel) and for S^T, dP^T, dV and dK (dK/dV kernel)."""
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+
+    gen = torch.Generator(device="cpu").manual_seed(99)
+    dO = (torch.randn(Q.shape, generator=gen) * 0.5).to(torch.bfloat16).to(Q.device)
+    B, N, H_q, d = Q.shape
+    shape = pisa.make_shape(B, N, H_q, K.shape[1], d, K.shape[2])
+    ws = torch.empty(pisa.pisa_attn_backward_workspace_bytes(shape, pisa.make_params(w.K)), dtype=torch.uint8,
+                     device=Q.device)
+    dQ = torch.empty(Q.shape, dtype=torch.float32, device=Q.device)
+    dK = torch.empty(K.shape, dtype=torch.float32, device=Q.device)
+    dV = torch.empty_like(dK)
+    run = lambda: pisa.pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, ws=ws, dQ=dQ, dK=dK, dV=dV)  # noqa: E731
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    if pisa.pisa_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the backward")
+    ms = a.elapsed_time(b) / steps
+    flops = work["flops"] / 4.0 * 14.0   # forward counts 4d per pair; the backward 14d
+    del dO, ws, dQ, dK, dV
+    torch.cuda.empty_cache()
+    return {"ms": ms, "tokens_per_s": B * N / (ms * 1e-3), "algorithmic_tflop": flops / 1e12,
+            "achieved_tflops": flops / (ms * 1e-3) / 1e12}
 
 
 def scoring_variants(Q, K, P, w, ws, idx, steps=10, warmup=3):

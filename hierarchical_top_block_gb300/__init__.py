@@ -54,6 +54,10 @@ def lib() -> ct.CDLL:
         L.pisa_pyramid_nodes.argtypes = [ct.c_longlong, ct.c_int, ct.c_int]
         L.pisa_select_workspace_bytes.restype = ct.c_size_t
         L.pisa_select_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_attn_backward_workspace_bytes.restype = ct.c_size_t
+        L.pisa_attn_backward_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_sparse_attn_backward.restype = ct.c_int
+        L.pisa_sparse_attn_backward.argtypes = [_P] * 10 + [_P, ct.c_size_t, pisa_shape, pisa_params, _P]
         L.pisa_prefill_host_workspace_bytes.restype = ct.c_size_t
         L.pisa_prefill_host_workspace_bytes.argtypes = [pisa_shape, pisa_params]
         L.pisa_build_pyramid.restype = ct.c_int
@@ -222,6 +226,37 @@ def pisa_sparse_attn_prefill(Q, K, V, idx, causal: bool = True, scale: float = 0
     _check(lib().pisa_sparse_attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(O), _ptr(LSE if want_lse else None),
                                           shape, params, _stream(Q)), "pisa_sparse_attn_prefill")
     return O, (LSE if want_lse else None)
+
+
+def pisa_attn_backward_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
+    return lib().pisa_attn_backward_workspace_bytes(shape, params)
+
+
+def pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal: bool = True, scale: float = 0.0, ws=None,
+                              dQ=None, dK=None, dV=None):
+    """Gradients of pisa_sparse_attn_prefill: returns dQ [B, N, H_q, d], dK, dV [B, H_kv, N_cap, d] (fp32)."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
+        _bf16(t, n)
+    if idx.dtype != torch.int32 or not idx.is_contiguous():
+        raise ValueError("idx must be contiguous int32")
+    if LSE.dtype != torch.float32 or not LSE.is_contiguous():
+        raise ValueError("LSE must be contiguous fp32")
+    B, N, H_q, d = Q.shape
+    H_kv, N_cap = K.shape[1], K.shape[2]
+    shape = make_shape(B, N, H_q, H_kv, d, N_cap)
+    params = make_params(idx.shape[-1], causal, scale)
+    need = pisa_attn_backward_workspace_bytes(shape, params)
+    if need == 0 and B * N > 0:
+        raise PisaError(2, "pisa_sparse_attn_backward: unsupported shape or parameters")
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    dQ = torch.empty(B, N, H_q, d, dtype=torch.float32, device=Q.device) if dQ is None else dQ
+    dK = torch.empty(B, H_kv, N_cap, d, dtype=torch.float32, device=Q.device) if dK is None else dK
+    dV = torch.empty(B, H_kv, N_cap, d, dtype=torch.float32, device=Q.device) if dV is None else dV
+    _check(lib().pisa_sparse_attn_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(O), _ptr(LSE), _ptr(dO),
+                                           _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), shape, params,
+                                           _stream(Q)), "pisa_sparse_attn_backward")
+    return dQ, dK, dV
 
 
 def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, scale: float = 0.0, dev_ws=None,

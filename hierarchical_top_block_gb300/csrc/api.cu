@@ -280,6 +280,31 @@ pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t* K, const
   return cuda_status(launch_sparse_attn(Q, K, V, idx, O, LSE, p, st->num_sms, st->err, static_cast<cudaStream_t>(stream)));
 }
 
+size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params) {
+  Problem p;
+  if (check_params(shape, params, &p) != PISA_OK) return 0;
+  return attn_backward_workspace_bytes(p);
+}
+
+pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                                      const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
+                                      float* dV, void* ws, size_t ws_bytes, pisa_shape shape, pisa_params params,
+                                      pisa_stream stream) {
+  Problem p;
+  pisa_status rc = check_params(shape, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.B == 0 || p.N == 0) return PISA_OK;
+  if (!Q || !K || !V || !idx || !O || !LSE || !dO || !dQ || !dK || !dV || !ws) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+      !aligned16(dK) || !aligned16(dV) || ((uintptr_t)ws & 255))
+    return PISA_ERR_INVALID_ARG;
+  if (ws_bytes < attn_backward_workspace_bytes(p)) return PISA_ERR_WORKSPACE;
+  DeviceState* st;
+  if ((rc = device_state(&st)) != PISA_OK) return rc;
+  return cuda_status(launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params) {
   Problem p;
   if (check_params(shape, params, &p) != PISA_OK) return 0;

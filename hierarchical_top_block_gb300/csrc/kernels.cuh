@@ -49,6 +49,12 @@ cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx
 cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
                                uint16_t* O, float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s);
 
+// Backward of the attention over the selected blocks (dQ, dK, dV).
+size_t attn_backward_workspace_bytes(const Problem& p);
+cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                                 const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
+                                 float* dV, void* ws, const Problem& p, int num_sms, cudaStream_t s);
+
 // Fused decode step.
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
                           uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,

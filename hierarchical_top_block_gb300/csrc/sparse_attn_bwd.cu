@@ -1,0 +1,529 @@
+// Backward of step 4 (the attention over the selected blocks; summary page of "Block Sparse
+// Attention with Log-Linear Complexity", section "Method step details", step 4; the softmax
+// covers the connected positions only, blog post of the same title, section 3.3).  The pages
+// give no backward: this is the gradient of the forward function.  For query t, head h and
+// the visible keys c of its selected blocks, with the forward's LSE:
+//   P_c = exp(scale q.k_c - LSE),  D = dO . O,  dP_c = dO . v_c,  dS_c = P_c (dP_c - D)
+//   dq = scale sum_c dS_c k_c,   dk_c += scale dS_c q,   dv_c += P_c dO
+// (dk_c and dv_c summed over every query head of the group that selected c's block).
+//
+// Kernels: (1) D per (b, t, h) from the stored O and dO; (2) an inverse index, block ->
+// the queries that selected it, cut into chunks of at most QC queries; (3) dQ, one warp per
+// query over its selected blocks in 32-key halves (the forward's structure, with dP = dO V^T
+// and dQ += dS K in place of P V); (4) dK and dV, one 4-warp CTA per chunk, each warp owning
+// 16 keys of the block and accumulating over the chunk's queries, then adding into fp32 dK
+// and dV (a block selected by many queries spans several chunks).
+#include "kernels.cuh"
+
+namespace pisa {
+namespace {
+
+constexpr int QC = 64;      // queries per dK/dV chunk
+constexpr int HK = 32;      // keys per half block (dQ kernel)
+constexpr int DQ_WARPS = 8;
+constexpr int KV_WARPS = 4;
+
+struct BwdParams {
+  const uint16_t *Q, *K, *V, *O, *dO;
+  const int32_t* idx;
+  const float* LSE;
+  float *dQ, *dK, *dV, *Dsum;
+  int32_t *counts, *cursor, *offsets, *entries;
+  int4* chunks;
+  int32_t* nchunks;
+  int B, N, N_cap, H_q, H_kv, GQ, Ksel, M1, causal;
+  float scale, sl2;
+};
+
+// swizzled [half][rows][64] bf16 tile: byte offset of row k, 16-byte chunk c (8 columns)
+__device__ __forceinline__ uint32_t swz(int half_bytes, int k, int c) {
+  return (c >> 3) * half_bytes + k * 128 + ((((c & 7) ^ (k & 7))) << 4);
+}
+
+// (1) D[b][h][t] = sum_e dO[b,t,h,e] O[b,t,h,e]
+template <int D>
+__global__ void bwd_dsum_kernel(BwdParams p) {
+  const long long rows = (long long)p.B * p.N * p.H_q;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += (long long)gridDim.x * blockDim.x) {
+    const uint4* a = reinterpret_cast<const uint4*>(p.dO + i * D);
+    const uint4* o = reinterpret_cast<const uint4*>(p.O + i * D);
+    float s = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < D / 8; ++j) {
+      const uint4 x = __ldg(a + j), y = __ldg(o + j);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s += bf16_lo(xs[u]) * bf16_lo(ys[u]) + bf16_hi(xs[u]) * bf16_hi(ys[u]);
+    }
+    const long long h = i % p.H_q, bt = i / p.H_q, t = bt % p.N, b = bt / p.N;
+    p.Dsum[(b * p.H_q + h) * p.N + t] = s;
+  }
+}
+
+__device__ __forceinline__ bool valid_block(const BwdParams& p, int blk, int t) {
+  return blk >= 0 && blk < p.M1 && (!p.causal || blk * 64 <= t);
+}
+
+// (2a) per (bh, block): how many queries selected it
+__global__ void bwd_count_kernel(BwdParams p) {
+  const long long total = (long long)p.B * p.H_kv * p.N * p.Ksel;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const long long item = i / p.Ksel;
+    const int t = (int)(item % p.N), bh = (int)(item / p.N);
+    const int blk = p.idx[i];
+    if (valid_block(p, blk, t)) atomicAdd(&p.counts[(long long)bh * p.M1 + blk], 1);
+  }
+}
+
+// (2b) exclusive scans of the counts and of the per-block chunk counts (one CTA)
+__global__ void bwd_scan_kernel(BwdParams p, int nkeys, int32_t* chunk_off) {
+  __shared__ int32_t carry_s[2];
+  __shared__ int32_t warp_s[2][32];
+  if (threadIdx.x == 0) carry_s[0] = carry_s[1] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < nkeys; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int c = i < nkeys ? p.counts[i] : 0;
+    const int ch = (c + QC - 1) / QC;
+    int a = c, b = ch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+      if (lane >= o) {
+        a += ya;
+        b += yb;
+      }
+    }
+    if (lane == 31) {
+      warp_s[0][warp] = a;
+      warp_s[1][warp] = b;
+    }
+    __syncthreads();
+    int pa = 0, pb = 0;
+    for (int w = 0; w < warp; ++w) {
+      pa += warp_s[0][w];
+      pb += warp_s[1][w];
+    }
+    const int ca = carry_s[0], cb = carry_s[1];
+    if (i < nkeys) {
+      p.offsets[i] = ca + pa + a - c;
+      chunk_off[i] = cb + pb + b - ch;
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) {
+      carry_s[0] = ca + pa + a;
+      carry_s[1] = cb + pb + b;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.offsets[nkeys] = carry_s[0];
+    *p.nchunks = carry_s[1];
+  }
+}
+
+// (2c) each selection entry's query position into its block's list
+__global__ void bwd_scatter_kernel(BwdParams p) {
+  const long long total = (long long)p.B * p.H_kv * p.N * p.Ksel;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const long long item = i / p.Ksel;
+    const int t = (int)(item % p.N), bh = (int)(item / p.N);
+    const int blk = p.idx[i];
+    if (!valid_block(p, blk, t)) continue;
+    const long long key = (long long)bh * p.M1 + blk;
+    p.entries[p.offsets[key] + atomicAdd(&p.cursor[key], 1)] = t;
+  }
+}
+
+// (2d) chunk records {bh, block, first entry, count}
+__global__ void bwd_chunks_kernel(BwdParams p, int nkeys, const int32_t* chunk_off) {
+  for (int key = blockIdx.x * blockDim.x + threadIdx.x; key < nkeys; key += gridDim.x * blockDim.x) {
+    const int c = p.counts[key];
+    const int bh = key / p.M1, blk = key - bh * p.M1;
+    for (int j = 0; j * QC < c; ++j)
+      p.chunks[chunk_off[key] + j] = make_int4(bh, blk, p.offsets[key] + j * QC, min(QC, c - j * QC));
+  }
+}
+
+// (3) dQ: one warp per (b, h_kv, t)
+template <int D>
+__global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
+  constexpr int KST = D / 16, NDT = D / 8, CPR = D / 8;
+  constexpr int HALF = HK * 128;             // bytes of one 64-column half of a slot
+  constexpr int SLOT = HK * D * 2;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
+  uint8_t* ks = smem + (size_t)warp * 2 * SLOT;
+  uint8_t* vs = ks + SLOT;
+  const uint32_t kb = smem_u32(ks), vb = smem_u32(vs);
+  const long long total = (long long)p.B * p.H_kv * p.N;
+  for (long long item = (long long)blockIdx.x * DQ_WARPS + warp; item < total; item += (long long)gridDim.x * DQ_WARPS) {
+    const int bh = (int)(item / p.N), t = (int)(item - (long long)bh * p.N);
+    const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+    const int last = p.causal ? min(t, p.N - 1) : p.N - 1;
+    int v = lane < p.Ksel ? p.idx[item * p.Ksel + lane] : -1;
+    if (!valid_block(p, v, t)) v = -1;
+    unsigned mask = __ballot_sync(0xffffffffu, v >= 0);
+    // A fragments of Q and dO (rows r, r+8 of the group; zero past G_Q)
+    const size_t row0 = ((size_t)b * p.N + t) * p.H_q + (size_t)hk * p.GQ;
+    uint32_t qa[KST][4], da[KST][4];
+#pragma unroll
+    for (int s = 0; s < KST; ++s) {
+      const int c0 = 16 * s + 2 * q;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int rr = r + 8 * (u & 1), cc = c0 + 8 * (u >> 1);
+        const bool in = rr < p.GQ;
+        qa[s][u] = in ? *reinterpret_cast<const uint32_t*>(p.Q + (row0 + rr) * D + cc) : 0u;
+        da[s][u] = in ? *reinterpret_cast<const uint32_t*>(p.dO + (row0 + rr) * D + cc) : 0u;
+      }
+    }
+    // per row: log2-domain LSE (+inf zeroes P on padded or empty rows) and D
+    float lse2[2], dsum[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int rr = r + 8 * u;
+      const size_t li = ((size_t)b * p.H_q + (size_t)hk * p.GQ + rr) * p.N + t;
+      const float l = rr < p.GQ ? p.LSE[li] : NEG_INF;
+      lse2[u] = l == NEG_INF ? POS_INF : l * LOG2E;
+      dsum[u] = rr < p.GQ ? p.Dsum[li] : 0.f;
+    }
+    float dq[NDT][4];
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
+    for (; mask; mask &= mask - 1) {
+      const int blk = __shfl_sync(0xffffffffu, v, __ffs(mask) - 1);
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {
+        const int kbase = blk * 64 + HK * hb;
+        if (kbase > last) break;
+        // K and V rows kbase .. kbase + 31 (rows past the last visible key become zero)
+        const uint16_t* Kg = p.K + ((size_t)bh * p.N_cap) * D;
+        const uint16_t* Vg = p.V + ((size_t)bh * p.N_cap) * D;
+        for (int i = lane; i < HK * CPR; i += 32) {
+          const int k = i / CPR, c = i - k * CPR;
+          const int key = kbase + k;
+          const bool in = key <= last;
+          const size_t off = (size_t)(in ? key : kbase) * D + 8 * c;
+          cp_async16(ks + swz(HALF, k, c), Kg + off, in ? 16 : 0);
+          cp_async16(vs + swz(HALF, k, c), Vg + off, in ? 16 : 0);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncwarp();
+        // S = Q K^T and dP = dO V^T over 32 keys (4 n-tiles)
+        float sacc[4][4], pacc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) sacc[nt][u] = pacc[nt][u] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < KST / 2; ++kp) {
+          const int d0 = 32 * kp + 8 * (lane >> 3);
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            const int key = 8 * nt + (lane & 7);
+            const uint32_t off = (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(kb + off, b0, b1, b2, b3);
+            mma_bf16_16816(sacc[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+            mma_bf16_16816(sacc[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+            ldmatrix_x4(vb + off, b0, b1, b2, b3);
+            mma_bf16_16816(pacc[nt], da[2 * kp][0], da[2 * kp][1], da[2 * kp][2], da[2 * kp][3], b0, b1);
+            mma_bf16_16816(pacc[nt], da[2 * kp + 1][0], da[2 * kp + 1][1], da[2 * kp + 1][2], da[2 * kp + 1][3], b2, b3);
+          }
+        }
+        // dS = P (dP - D), packed as bf16 A fragments (keys are the k index of dQ += dS K)
+        uint32_t sa[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          float ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int key = kbase + 8 * nt + 2 * q + (u & 1);
+            const int rr = u >> 1;
+            const float pr = key <= last ? fast_exp2(fmaf(sacc[nt][u], p.sl2, -lse2[rr])) : 0.f;
+            ds[u] = pr * (pacc[nt][u] - dsum[rr]);
+          }
+          const int kk = nt >> 1, hi = nt & 1;
+          sa[kk][hi ? 2 : 0] = pack_bf16x2(ds[0], ds[1]);
+          sa[kk][hi ? 3 : 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        // dQ += dS K (K^T fragments by ldmatrix.trans on the K slot)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+          for (int np = 0; np < NDT / 2; ++np) {
+            const int d0 = 8 * (2 * np + (lane >> 4));
+            const uint32_t addr = kb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+            mma_bf16_16816(dq[2 * np], sa[kk][0], sa[kk][1], sa[kk][2], sa[kk][3], b0, b1);
+            mma_bf16_16816(dq[2 * np + 1], sa[kk][0], sa[kk][1], sa[kk][2], sa[kk][3], b2, b3);
+          }
+        }
+        __syncwarp();  // every lane is done with the slots before the next copy
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) {
+      const int col = 8 * i + 2 * q;
+      if (r < p.GQ)
+        *reinterpret_cast<float2*>(p.dQ + (row0 + r) * D + col) = make_float2(dq[i][0] * p.scale, dq[i][1] * p.scale);
+      if (r + 8 < p.GQ)
+        *reinterpret_cast<float2*>(p.dQ + (row0 + r + 8) * D + col) =
+            make_float2(dq[i][2] * p.scale, dq[i][3] * p.scale);
+    }
+  }
+}
+
+__device__ __forceinline__ void red_add(float* a, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(a), "f"(v) : "memory");
+}
+
+// (4) dK, dV: one CTA of 4 warps per chunk; warp w owns keys 16w .. 16w + 15 of the block
+template <int D>
+__global__ void __launch_bounds__(32 * KV_WARPS) bwd_dkv_kernel(BwdParams p) {
+  constexpr int KST = D / 16, NDT = D / 8, CPR = D / 8;
+  constexpr int KHALF = 64 * 128;            // K/V tiles: [half][64 keys][64]
+  constexpr int QHALF = 16 * 128;            // Q/dO tiles: [half][16 heads][64]
+  constexpr int KTILE = 64 * D * 2, QTILE = 16 * D * 2;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* Ks = smem;
+  uint8_t* Vs = Ks + KTILE;
+  uint8_t* Qs = Vs + KTILE;                  // [2][QTILE]
+  uint8_t* dOs = Qs + 2 * QTILE;             // [2][QTILE]
+  __shared__ float lse2_s[2][16], dsum_s[2][16];
+  __shared__ int t_s[2];
+  if (blockIdx.x >= *p.nchunks) return;
+  const int4 ch = p.chunks[blockIdx.x];
+  const int bh = ch.x, blk = ch.y, first = ch.z, cnt = ch.w;
+  const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
+  const int key0 = blk * 64;
+  // the block's K and V (rows past N become zero)
+  {
+    const uint16_t* Kg = p.K + ((size_t)bh * p.N_cap) * D;
+    const uint16_t* Vg = p.V + ((size_t)bh * p.N_cap) * D;
+    for (int i = threadIdx.x; i < 64 * CPR; i += blockDim.x) {
+      const int k = i / CPR, c = i - k * CPR;
+      const bool in = key0 + k < p.N;
+      const size_t off = (size_t)(in ? key0 + k : key0) * D + 8 * c;
+      cp_async16(Ks + swz(KHALF, k, c), Kg + off, in ? 16 : 0);
+      cp_async16(Vs + swz(KHALF, k, c), Vg + off, in ? 16 : 0);
+    }
+  }
+  // one query's Q and dO rows (heads past G_Q become zero), log2 LSE and D, into buffer bf
+  auto stage = [&](int i, int bf) {
+    const int t = p.entries[first + i];
+    const size_t row0 = ((size_t)b * p.N + t) * p.H_q + (size_t)hk * p.GQ;
+    for (int j = threadIdx.x; j < 16 * CPR; j += blockDim.x) {
+      const int h = j / CPR, c = j - h * CPR;
+      const bool in = h < p.GQ;
+      const size_t off = (row0 + (in ? h : 0)) * D + 8 * c;
+      cp_async16(Qs + bf * QTILE + swz(QHALF, h, c), p.Q + off, in ? 16 : 0);
+      cp_async16(dOs + bf * QTILE + swz(QHALF, h, c), p.dO + off, in ? 16 : 0);
+    }
+    if (threadIdx.x < 16) {
+      const int h = threadIdx.x;
+      const size_t li = ((size_t)b * p.H_q + (size_t)hk * p.GQ + h) * p.N + t;
+      const float l = h < p.GQ ? p.LSE[li] : NEG_INF;
+      lse2_s[bf][h] = l == NEG_INF ? POS_INF : l * LOG2E;
+      dsum_s[bf][h] = h < p.GQ ? p.Dsum[li] : 0.f;
+    }
+    if (threadIdx.x == 0) t_s[bf] = t;
+  };
+  stage(0, 0);
+  cp_async_commit();
+  float dk[NDT][4], dv[NDT][4];
+#pragma unroll
+  for (int i = 0; i < NDT; ++i)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dk[i][u] = dv[i][u] = 0.f;
+  const uint32_t ksa = smem_u32(Ks), vsa = smem_u32(Vs);
+  for (int i = 0; i < cnt; ++i) {
+    const int bf = i & 1;
+    if (i + 1 < cnt) {
+      stage(i + 1, bf ^ 1);
+      cp_async_commit();
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      cp_async_wait_all();
+    }
+    __syncthreads();
+    const int t = t_s[bf];
+    const int last = p.causal ? min(t, p.N - 1) : p.N - 1;
+    const uint32_t qsa = smem_u32(Qs + bf * QTILE), dsa = smem_u32(dOs + bf * QTILE);
+    // S^T [16 keys x 16 heads] = K_w Q^T and dP^T = V_w dO^T
+    float sacc[2][4], pacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sacc[nt][u] = pacc[nt][u] = 0.f;
+#pragma unroll
+    for (int s = 0; s < KST; ++s) {
+      const int m = lane >> 3;
+      // A: rows 16w + 8 (m & 1) + (lane & 7), columns 16 s + 8 (m >> 1)
+      const int ak = 16 * warp + 8 * (m & 1) + (lane & 7), ac = 2 * s + (m >> 1);
+      uint32_t k0, k1, k2, k3, v0, v1, v2, v3;
+      ldmatrix_x4(ksa + swz(KHALF, ak, ac), k0, k1, k2, k3);
+      ldmatrix_x4(vsa + swz(KHALF, ak, ac), v0, v1, v2, v3);
+      // B: heads 8 (m >> 1) + (lane & 7), columns 16 s + 8 (m & 1)
+      const int bh8 = 8 * (m >> 1) + (lane & 7), bc = 2 * s + (m & 1);
+      uint32_t q0, q1, q2, q3, o0, o1, o2, o3;
+      ldmatrix_x4(qsa + swz(QHALF, bh8, bc), q0, q1, q2, q3);
+      ldmatrix_x4(dsa + swz(QHALF, bh8, bc), o0, o1, o2, o3);
+      mma_bf16_16816(sacc[0], k0, k1, k2, k3, q0, q1);
+      mma_bf16_16816(sacc[1], k0, k1, k2, k3, q2, q3);
+      mma_bf16_16816(pacc[0], v0, v1, v2, v3, o0, o1);
+      mma_bf16_16816(pacc[1], v0, v1, v2, v3, o2, o3);
+    }
+    // P^T and dS^T (rows: keys 16w + r, + 8; columns: heads 8 nt + 2q + {0, 1})
+    uint32_t pa[4], sa[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float pv[4], dsv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int key = key0 + 16 * warp + r + 8 * (u >> 1);
+        const int h = 8 * nt + 2 * q + (u & 1);
+        const float pr = key <= last ? fast_exp2(fmaf(sacc[nt][u], p.sl2, -lse2_s[bf][h])) : 0.f;
+        pv[u] = pr;
+        dsv[u] = pr * (pacc[nt][u] - dsum_s[bf][h]);
+      }
+      pa[nt ? 2 : 0] = pack_bf16x2(pv[0], pv[1]);
+      pa[nt ? 3 : 1] = pack_bf16x2(pv[2], pv[3]);
+      sa[nt ? 2 : 0] = pack_bf16x2(dsv[0], dsv[1]);
+      sa[nt ? 3 : 1] = pack_bf16x2(dsv[2], dsv[3]);
+    }
+    // dV_w += P^T dO and dK_w += dS^T Q (B fragments by ldmatrix.trans: k = head, n = d)
+#pragma unroll
+    for (int np = 0; np < NDT / 2; ++np) {
+      const int h = 8 * ((lane >> 3) & 1) + (lane & 7);
+      const int c = 2 * np + (lane >> 4);
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4_trans(dsa + swz(QHALF, h, c), b0, b1, b2, b3);
+      mma_bf16_16816(dv[2 * np], pa[0], pa[1], pa[2], pa[3], b0, b1);
+      mma_bf16_16816(dv[2 * np + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
+      ldmatrix_x4_trans(qsa + swz(QHALF, h, c), b0, b1, b2, b3);
+      mma_bf16_16816(dk[2 * np], sa[0], sa[1], sa[2], sa[3], b0, b1);
+      mma_bf16_16816(dk[2 * np + 1], sa[0], sa[1], sa[2], sa[3], b2, b3);
+    }
+    __syncthreads();  // the buffer is restaged two queries later
+  }
+  // add this chunk's contribution (keys past N carry none)
+  float* dKg = p.dK + ((size_t)bh * p.N_cap) * D;
+  float* dVg = p.dV + ((size_t)bh * p.N_cap) * D;
+#pragma unroll
+  for (int u2 = 0; u2 < 2; ++u2) {
+    const int key = key0 + 16 * warp + r + 8 * u2;
+    if (key >= p.N) continue;
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) {
+      const int col = 8 * i + 2 * q;
+      red_add(dKg + (size_t)key * D + col, dk[i][2 * u2] * p.scale);
+      red_add(dKg + (size_t)key * D + col + 1, dk[i][2 * u2 + 1] * p.scale);
+      red_add(dVg + (size_t)key * D + col, dv[i][2 * u2]);
+      red_add(dVg + (size_t)key * D + col + 1, dv[i][2 * u2 + 1]);
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_chunks, int num_sms, cudaStream_t s) {
+  cudaError_t e;
+  const long long rows = (long long)p.B * p.N * p.H_q;
+  const long long ents = (long long)p.B * p.H_kv * p.N * p.Ksel;
+  const int g1 = (int)std::min<long long>((rows + 255) / 256, (long long)num_sms * 16);
+  const int g2 = (int)std::min<long long>((ents + 255) / 256, (long long)num_sms * 16);
+  bwd_dsum_kernel<D><<<g1 > 0 ? g1 : 1, 256, 0, s>>>(p);
+  bwd_count_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
+  bwd_scan_kernel<<<1, 1024, 0, s>>>(p, nkeys, chunk_off);
+  bwd_scatter_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
+  bwd_chunks_kernel<<<(nkeys + 255) / 256, 256, 0, s>>>(p, nkeys, chunk_off);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t smem_q = (size_t)DQ_WARPS * 2 * HK * D * 2 + 1024;
+  if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q)) != cudaSuccess)
+    return e;
+  const long long items = (long long)p.B * p.H_kv * p.N;
+  const long long gq = std::min<long long>((items + DQ_WARPS - 1) / DQ_WARPS, (long long)num_sms);
+  bwd_dq_kernel<D><<<(int)gq, 32 * DQ_WARPS, smem_q, s>>>(p);
+  const size_t smem_kv = (size_t)2 * 64 * D * 2 + (size_t)4 * 16 * D * 2 + 1024;
+  if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) !=
+      cudaSuccess)
+    return e;
+  if (max_chunks > 0) bwd_dkv_kernel<D><<<(int)max_chunks, 32 * KV_WARPS, smem_kv, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_backward_workspace_bytes(const Problem& p) {
+  const long long M1 = (p.N + 63) / 64;
+  const long long nkeys = (long long)p.B * p.H_kv * M1;
+  const long long ents = (long long)p.B * p.H_kv * p.N * p.K;
+  const long long max_chunks = nkeys + ents / QC + 1;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + up((size_t)(nkeys + 1) * 4) +
+         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4);
+}
+
+cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
+                                 const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
+                                 float* dV, void* ws, const Problem& pr, int num_sms, cudaStream_t s) {
+  BwdParams p;
+  p.Q = Q;
+  p.K = K;
+  p.V = V;
+  p.O = O;
+  p.dO = dO;
+  p.idx = idx;
+  p.LSE = LSE;
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.B = pr.B;
+  p.N = pr.N;
+  p.N_cap = pr.N_cap;
+  p.H_q = pr.H_q;
+  p.H_kv = pr.H_kv;
+  p.GQ = pr.GQ;
+  p.Ksel = pr.K;
+  p.M1 = (pr.N + 63) / 64;
+  p.causal = pr.causal;
+  p.scale = pr.scale;
+  p.sl2 = pr.scale * LOG2E;
+  const long long nkeys = (long long)pr.B * pr.H_kv * p.M1;
+  const long long ents = (long long)pr.B * pr.H_kv * pr.N * pr.K;
+  const long long max_chunks = nkeys + ents / QC + 1;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.Dsum = reinterpret_cast<float*>(w);
+  w += up((size_t)pr.B * pr.H_q * pr.N * 4);
+  p.counts = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)(nkeys + 1) * 4);
+  p.cursor = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)(nkeys + 1) * 4);
+  p.offsets = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)(nkeys + 1) * 4);
+  int32_t* chunk_off = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)(nkeys + 1) * 4);
+  p.entries = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)ents * 4);
+  p.chunks = reinterpret_cast<int4*>(w);
+  w += up((size_t)max_chunks * 16);
+  p.nchunks = reinterpret_cast<int32_t*>(w);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(p.counts, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.cursor, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dK, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dV, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
+  if (pr.d == 128) return launch_d<128>(p, (int)nkeys, chunk_off, max_chunks, num_sms, s);
+  return launch_d<64>(p, (int)nkeys, chunk_off, max_chunks, num_sms, s);
+}
+
+}  // namespace pisa

@@ -145,6 +145,24 @@ PISA_API pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t*
                                      uint16_t* O, float* LSE, pisa_shape shape, pisa_params params,
                                      pisa_stream stream);
 
+/* Backward of the attention over the selected blocks: the gradient of pisa_sparse_attn_prefill
+ * with respect to Q, K and V for an upstream gradient dO (the pages give no backward; this is
+ * the derivative of the forward).  With the forward's LSE, for the visible keys c of the
+ * selected blocks: P_c = exp(scale q.k_c - LSE), D = dO.O, dS_c = P_c (dO.v_c - D);
+ * dq = scale sum dS_c k_c, dk_c += scale dS_c q, dv_c += P_c dO, the last two summed over
+ * every query head of the group that selected c's block.  idx, causal and scale as in the
+ * forward; only params.K, causal and scale are used.
+ *   O, dO [B][N][H_q][d] bf16 (O and LSE from the forward);  LSE [B][H_q][N] fp32.
+ *   dQ [B][N][H_q][d] fp32 out;  dK, dV [B][H_kv][N_cap][d] fp32 out (rows >= N are zero).
+ *   ws  device scratch of at least pisa_attn_backward_workspace_bytes(); 256-B aligned.
+ * dK and dV accumulate with fp32 atomic adds, so their last bits may vary between runs. */
+PISA_API size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params);
+PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                               const int32_t* idx, const uint16_t* O, const float* LSE,
+                                               const uint16_t* dO, float* dQ, float* dK, float* dV, void* ws,
+                                               size_t ws_bytes, pisa_shape shape, pisa_params params,
+                                               pisa_stream stream);
+
 /* ---- full prefill from host buffers (end-to-end path) --------------------------------- */
 
 /* Copies Q, K, V host -> device, builds the pyramid, selects, attends and copies O (and
