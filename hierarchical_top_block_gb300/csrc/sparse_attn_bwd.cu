@@ -11,17 +11,19 @@
 // the queries that selected it, cut into chunks of at most QC queries; (3) dQ, one warp per
 // query over its selected blocks in 32-key halves (the forward's structure, with dP = dO V^T
 // and dQ += dS K in place of P V); (4) dK and dV, one 4-warp CTA per chunk, each warp owning
-// 16 keys of the block and accumulating over the chunk's queries, then adding into fp32 dK
-// and dV (a block selected by many queries spans several chunks).
+// 16 keys of the block and accumulating over the chunk's queries (their Q and dO rows staged
+// three ahead in a 4-buffer ring), then adding into fp32 dK and dV (a block selected by many
+// queries spans several chunks).
 #include "kernels.cuh"
 
 namespace pisa {
 namespace {
 
-constexpr int QC = 64;      // queries per dK/dV chunk
+constexpr int QC = 256;     // queries per dK/dV chunk
 constexpr int HK = 32;      // keys per half block (dQ kernel)
 constexpr int DQ_WARPS = 8;
 constexpr int KV_WARPS = 4;
+constexpr int KV_NBUF = 4;  // staged queries per dK/dV CTA (three prefetched ahead)
 
 struct BwdParams {
   const uint16_t *Q, *K, *V, *O, *dO;
@@ -295,10 +297,10 @@ __global__ void __launch_bounds__(32 * KV_WARPS) bwd_dkv_kernel(BwdParams p) {
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* Ks = smem;
   uint8_t* Vs = Ks + KTILE;
-  uint8_t* Qs = Vs + KTILE;                  // [2][QTILE]
-  uint8_t* dOs = Qs + 2 * QTILE;             // [2][QTILE]
-  __shared__ float lse2_s[2][16], dsum_s[2][16];
-  __shared__ int t_s[2];
+  uint8_t* Qs = Vs + KTILE;                  // [KV_NBUF][QTILE]
+  uint8_t* dOs = Qs + KV_NBUF * QTILE;       // [KV_NBUF][QTILE]
+  __shared__ float lse2_s[KV_NBUF][16], dsum_s[KV_NBUF][16];
+  __shared__ int t_s[KV_NBUF];
   if (blockIdx.x >= *p.nchunks) return;
   const int4 ch = p.chunks[blockIdx.x];
   const int bh = ch.x, blk = ch.y, first = ch.z, cnt = ch.w;
@@ -337,8 +339,12 @@ __global__ void __launch_bounds__(32 * KV_WARPS) bwd_dkv_kernel(BwdParams p) {
     }
     if (threadIdx.x == 0) t_s[bf] = t;
   };
-  stage(0, 0);
-  cp_async_commit();
+  // the K/V copies join the first group; every iteration commits one (possibly empty) group,
+  // so waiting until KV_NBUF - 1 groups remain in flight completes the current query's
+  for (int j = 0; j < KV_NBUF - 1; ++j) {
+    if (j < cnt) stage(j, j);
+    cp_async_commit();
+  }
   float dk[NDT][4], dv[NDT][4];
 #pragma unroll
   for (int i = 0; i < NDT; ++i)
@@ -346,14 +352,10 @@ __global__ void __launch_bounds__(32 * KV_WARPS) bwd_dkv_kernel(BwdParams p) {
     for (int u = 0; u < 4; ++u) dk[i][u] = dv[i][u] = 0.f;
   const uint32_t ksa = smem_u32(Ks), vsa = smem_u32(Vs);
   for (int i = 0; i < cnt; ++i) {
-    const int bf = i & 1;
-    if (i + 1 < cnt) {
-      stage(i + 1, bf ^ 1);
-      cp_async_commit();
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      cp_async_wait_all();
-    }
+    const int bf = i % KV_NBUF;
+    if (i + KV_NBUF - 1 < cnt) stage(i + KV_NBUF - 1, (i + KV_NBUF - 1) % KV_NBUF);
+    cp_async_commit();
+    asm volatile("cp.async.wait_group %0;" ::"n"(KV_NBUF - 1) : "memory");
     __syncthreads();
     const int t = t_s[bf];
     const int last = p.causal ? min(t, p.N - 1) : p.N - 1;
@@ -413,8 +415,9 @@ __global__ void __launch_bounds__(32 * KV_WARPS) bwd_dkv_kernel(BwdParams p) {
       mma_bf16_16816(dk[2 * np], sa[0], sa[1], sa[2], sa[3], b0, b1);
       mma_bf16_16816(dk[2 * np + 1], sa[0], sa[1], sa[2], sa[3], b2, b3);
     }
-    __syncthreads();  // the buffer is restaged two queries later
+    __syncthreads();  // the buffer is restaged KV_NBUF - 1 queries later
   }
+  cp_async_wait_all();
   // add this chunk's contribution (keys past N carry none)
   float* dKg = p.dK + ((size_t)bh * p.N_cap) * D;
   float* dVg = p.dV + ((size_t)bh * p.N_cap) * D;
@@ -452,7 +455,7 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   const long long items = (long long)p.B * p.H_kv * p.N;
   const long long gq = std::min<long long>((items + DQ_WARPS - 1) / DQ_WARPS, (long long)num_sms);
   bwd_dq_kernel<D><<<(int)gq, 32 * DQ_WARPS, smem_q, s>>>(p);
-  const size_t smem_kv = (size_t)2 * 64 * D * 2 + (size_t)4 * 16 * D * 2 + 1024;
+  const size_t smem_kv = (size_t)2 * 64 * D * 2 + (size_t)2 * KV_NBUF * 16 * D * 2 + 1024;
   if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) !=
       cudaSuccess)
     return e;
