@@ -288,7 +288,8 @@ __device__ __forceinline__ void red_add(float* a, float v) {
 
 // (4) dK, dV: one CTA of 4 warps per chunk; warp w owns keys 16w .. 16w + 15 of the block
 template <int D>
-__global__ void __launch_bounds__(32 * KV_WARPS) bwd_dkv_kernel(BwdParams p) {
+// 3 CTAs per SM (<= 168 registers): the per-query chain is latency-bound, more warps hide it
+__global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) {
   constexpr int KST = D / 16, NDT = D / 8, CPR = D / 8;
   constexpr int KHALF = 64 * 128;            // K/V tiles: [half][64 keys][64]
   constexpr int QHALF = 16 * 128;            // Q/dO tiles: [half][16 heads][64]
