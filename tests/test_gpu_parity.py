@@ -270,3 +270,24 @@ def test_scoring_variant_ragged_d128(oracle_impl):
 def test_decode_scoring_variants(oracle_impl, scoring):
     w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=8, H_kv=2, K=6)
     _decode_check(oracle_impl, w, N0=2040, steps=12, N_cap=2304, scoring=scoring)
+
+
+def test_prefill_host_matches_the_device_path():
+    """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
+    what the device-resident calls return on the same inputs."""
+    w = W.WORKLOADS["prefill_4k"].with_(B=2)
+    Q, K, V = _inputs(w)
+    P = pisa.pisa_build_pyramid(K)
+    idx = pisa.pisa_select_prefill(Q, K, P, w.K)
+    O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx)
+    torch.cuda.synchronize()
+    Qh, Kh, Vh = (x.cpu().pin_memory() for x in (Q, K, V))
+    Oh = torch.empty(Q.shape, dtype=torch.bfloat16).pin_memory()
+    Lh = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
+    Ih = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+    pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, O_host=Oh, LSE_host=Lh, idx_host=Ih)
+    torch.cuda.synchronize()
+    assert pisa.pisa_get_last_device_error() == 0
+    assert torch.equal(Ih, idx.cpu())
+    assert torch.equal(Oh, O.cpu())
+    assert torch.equal(Lh, LSE.cpu())
