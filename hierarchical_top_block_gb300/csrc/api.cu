@@ -17,10 +17,22 @@ namespace {
 
 constexpr int MAX_DEVICES = 64;
 
+// Streams and events of the host-buffer prefill pipeline (created on first use).
+constexpr int PIPE_MAX_CHUNKS = 16;
+constexpr int PIPE_EVENTS = 4 + 2 * PIPE_MAX_CHUNKS;
+
+struct HostPipe {
+  bool ready = false;
+  std::mutex run;                   // one host-buffer prefill at a time per device
+  cudaStream_t in = nullptr, out = nullptr;  // host->device and device->host copies
+  cudaEvent_t ev[PIPE_EVENTS] = {};
+};
+
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   uint32_t* err = nullptr;  // device address of g_device_error on this device
+  HostPipe pipe;
 };
 
 std::mutex g_mutex;
@@ -40,6 +52,20 @@ pisa_status device_state(DeviceState** out) {
     st.ready = true;
   }
   *out = &st;
+  return PISA_OK;
+}
+
+pisa_status host_pipe(DeviceState* st, HostPipe** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  HostPipe& hp = st->pipe;
+  if (!hp.ready) {
+    if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
+    for (cudaEvent_t& e : hp.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return PISA_ERR_CUDA;
+    hp.ready = true;
+  }
+  *out = &hp;
   return PISA_OK;
 }
 
@@ -114,6 +140,8 @@ pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p)
   p->scoring = pr.scoring;
   p->scale = pr.scale > 0.f ? pr.scale : 1.0f / sqrtf((float)s.d);
   p->GQ = gq;
+  p->t_lo = 0;
+  p->t_hi = s.N;
   return PISA_OK;
 }
 
@@ -330,6 +358,9 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   if (reinterpret_cast<uintptr_t>(dev_ws) & 255u) return PISA_ERR_INVALID_ARG;
   DeviceState* st;
   if ((rc = device_state(&st)) != PISA_OK) return rc;
+  HostPipe* hp;
+  if ((rc = host_pipe(st, &hp)) != PISA_OK) return rc;
+  std::lock_guard<std::mutex> hold(hp->run);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t q = (size_t)p.B * p.N * p.H_q * p.d * 2;
   const size_t kv = (size_t)p.B * p.H_kv * p.N * p.d * 2;
@@ -352,17 +383,79 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   float* dL = reinterpret_cast<float*>(w);
   w += round_up(lseb, 256);
   const size_t sel_bytes = select_layout(p).total_bytes;
-  if (cudaMemcpyAsync(dQ, Q_host, q, cudaMemcpyHostToDevice, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if (cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if (cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, s) != cudaSuccess) return PISA_ERR_CUDA;
+
+  // Query chunks: selection and attention of chunk j need Q rows of chunk j only (plus all
+  // of K and V), so the copy-in of chunk j+1 and the copy-out of chunk j-1 overlap the
+  // compute of chunk j.  Q and O are [B][N][H_q][d]: a chunk is one row band per sequence.
+  long long chunk = ((long long)p.N + PIPE_MAX_CHUNKS - 1) / PIPE_MAX_CHUNKS;
+  if (chunk < 16384) chunk = 16384;
+  chunk = (chunk + 63) / 64 * 64;
+  const int nchunks = (int)(((long long)p.N + chunk - 1) / chunk);
+  cudaEvent_t* ev = hp->ev;
+  cudaEvent_t e_start = ev[0], e_k = ev[1], e_v = ev[2], e_end = ev[3];
+  cudaEvent_t* e_q = ev + 4;
+  cudaEvent_t* e_attn = ev + 4 + PIPE_MAX_CHUNKS;
+  const size_t q_row = (size_t)p.H_q * p.d * 2;  // bytes of one query position, all heads
+  auto copy_q = [&](int j) {
+    const long long lo = j * chunk, hi = lo + chunk < p.N ? lo + chunk : p.N;
+    return cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(dQ) + lo * q_row, p.N * q_row,
+                             reinterpret_cast<const uint8_t*>(Q_host) + lo * q_row, p.N * q_row, (hi - lo) * q_row, p.B,
+                             cudaMemcpyHostToDevice, hp->in);
+  };
+  bool ok = true;
+  auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
+  // the copy-in stream starts after whatever the caller queued on `stream` before this call
+  chk(cudaEventRecord(e_start, s));
+  chk(cudaStreamWaitEvent(hp->in, e_start, 0));
+  chk(cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, hp->in));
+  chk(cudaEventRecord(e_k, hp->in));
+  chk(copy_q(0));
+  chk(cudaEventRecord(e_q[0], hp->in));
+  chk(cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, hp->in));
+  chk(cudaEventRecord(e_v, hp->in));
+  for (int j = 1; j < nchunks && ok; ++j) {
+    chk(copy_q(j));
+    chk(cudaEventRecord(e_q[j], hp->in));
+  }
   const Geometry geo = make_geometry(p.N, p.N);
-  if (launch_pyramid(dK, dP, p, geo, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, p, st, s)) != PISA_OK) return rc;
-  if (launch_sparse_attn(dQ, dK, dV, dIdx, dO, dL, p, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if (cudaMemcpyAsync(O_host, dO, q, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if (LSE_host && cudaMemcpyAsync(LSE_host, dL, lseb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if (idx_host && cudaMemcpyAsync(idx_host, dIdx, idxb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PISA_ERR_CUDA;
-  return cuda_status(cudaStreamSynchronize(s));
+  chk(cudaStreamWaitEvent(s, e_k, 0));
+  if (ok) chk(launch_pyramid(dK, dP, p, geo, s));
+  for (int j = 0; j < nchunks && ok; ++j) {
+    Problem pc = p;
+    pc.t_lo = (int)(j * chunk);
+    pc.t_hi = (int)(pc.t_lo + chunk < p.N ? pc.t_lo + chunk : p.N);
+    chk(cudaStreamWaitEvent(s, e_q[j], 0));
+    if (!ok) break;
+    if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, pc, st, s)) != PISA_OK) {
+      ok = false;
+      break;
+    }
+    if (j == 0) chk(cudaStreamWaitEvent(s, e_v, 0));
+    if (ok) chk(launch_sparse_attn(dQ, dK, dV, dIdx, dO, dL, pc, st->num_sms, st->err, s));
+    chk(cudaEventRecord(e_attn[j], s));
+    // copy-out of chunk j: O rows, and the LSE / selection columns of every head
+    const size_t nq = (size_t)(pc.t_hi - pc.t_lo), t0 = (size_t)pc.t_lo;
+    chk(cudaStreamWaitEvent(hp->out, e_attn[j], 0));
+    chk(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(O_host) + t0 * q_row, p.N * q_row,
+                          reinterpret_cast<const uint8_t*>(dO) + t0 * q_row, p.N * q_row, nq * q_row, p.B,
+                          cudaMemcpyDeviceToHost, hp->out));
+    if (LSE_host)
+      chk(cudaMemcpy2DAsync(LSE_host + t0, (size_t)p.N * 4, dL + t0, (size_t)p.N * 4, nq * 4, (size_t)p.B * p.H_q,
+                            cudaMemcpyDeviceToHost, hp->out));
+    if (idx_host)
+      chk(cudaMemcpy2DAsync(idx_host + t0 * p.K, (size_t)p.N * p.K * 4, dIdx + t0 * p.K, (size_t)p.N * p.K * 4,
+                            nq * p.K * 4, (size_t)p.B * p.H_kv, cudaMemcpyDeviceToHost, hp->out));
+  }
+  // the call returns once all three streams are idle (also after an error, so that no copy
+  // is still writing into the caller's buffers)
+  const cudaError_t e_rec = cudaEventRecord(e_end, hp->out);
+  if (e_rec == cudaSuccess) cudaStreamWaitEvent(s, e_end, 0);
+  const cudaError_t e_in = cudaStreamSynchronize(hp->in), e_out = cudaStreamSynchronize(hp->out);
+  const cudaError_t e_s = cudaStreamSynchronize(s);
+  if (rc != PISA_OK) return rc;
+  if (!ok || e_rec != cudaSuccess || e_in != cudaSuccess || e_out != cudaSuccess || e_s != cudaSuccess)
+    return PISA_ERR_CUDA;
+  return PISA_OK;
 }
 
 pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,

@@ -25,13 +25,14 @@ __device__ __forceinline__ long long key_of(int bh, int t, int node, const Clust
   return ((long long)bh * cb.nwin + t / cb.win) * cb.M2 + node;
 }
 
-__global__ void count_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int Ksel, long long total) {
+__global__ void count_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int t_lo, int nq, int Ksel,
+                             long long total) {
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total * Ksel;
        e += (long long)gridDim.x * blockDim.x) {
-    const int node = S2[e];
-    if (node < 0) continue;
     const long long item = e / Ksel;
-    const int bh = (int)(item / N), t = (int)(item % N);
+    const int bh = (int)(item / nq), t = t_lo + (int)(item % nq);
+    const int node = S2[((long long)bh * N + t) * Ksel + (e - item * Ksel)];
+    if (node < 0) continue;
     atomicAdd(&cb.counts[key_of(bh, t, node, cb)], 1);
   }
 }
@@ -132,14 +133,15 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_add_kernel(ClusterBuffers c
   }
 }
 
-__global__ void scatter_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int Ksel, long long total) {
+__global__ void scatter_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int t_lo, int nq, int Ksel,
+                               long long total) {
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total * Ksel;
        e += (long long)gridDim.x * blockDim.x) {
-    const int node = S2[e];
-    if (node < 0) continue;
     const long long item = e / Ksel;
     const int slot = (int)(e - item * Ksel);
-    const int bh = (int)(item / N), t = (int)(item % N);
+    const int bh = (int)(item / nq), t = t_lo + (int)(item % nq);
+    const int node = S2[((long long)bh * N + t) * Ksel + slot];
+    if (node < 0) continue;
     const long long key = key_of(bh, t, node, cb);
     const int pos = cb.offsets[key] + atomicAdd(&cb.cursor[key], 1);
     cb.entries[pos] = (t << 6) | slot;
@@ -168,16 +170,17 @@ inline int grid_for(long long work, int threads, int cap = 4096) {
 }  // namespace
 
 cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Problem& p, cudaStream_t s) {
-  const long long total = (long long)p.B * p.H_kv * p.N;
+  const int nq = p.t_hi - p.t_lo;
+  const long long total = (long long)p.B * p.H_kv * (nq > 0 ? nq : 0);
   cudaError_t e;
   if ((e = cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cb.cursor, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cb.totals, 0, sizeof(int32_t) * 4, s)) != cudaSuccess) return e;  // [2] = tile counter
-  count_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.K, total);
+  count_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.t_lo, nq, p.K, total);
   scan_local_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
   scan_blocks_kernel<<<1, SCAN_THREADS, 0, s>>>(cb);
   scan_add_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
-  scatter_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.K, total);
+  scatter_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.t_lo, nq, p.K, total);
   tiles_kernel<<<grid_for(cb.nkeys, THREADS), THREADS, 0, s>>>(cb);
   return cudaGetLastError();
 }

@@ -11,6 +11,9 @@ struct Problem {
   int scoring;  // 0 LSE, 1 log m + mean, 2 log m + mean + variance / 2
   float scale;  // logit scale (already resolved; > 0)
   int GQ;       // H_q / H_kv
+  // queries processed by the per-query kernels (Stage 1, clustering, top-K, attention):
+  // t in [t_lo, t_hi); every buffer keeps its full-length layout and is indexed by t
+  int t_lo, t_hi;
 };
 
 // Builds pyramid levels 1..geo.L from the first N rows of K (layout capacity N_cap).

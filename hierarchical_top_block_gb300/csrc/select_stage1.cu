@@ -30,7 +30,7 @@ template <int D>
 __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCKS_64) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
-                                                         int scoring, float scale_log2, Geometry geo) {
+                                                         int scoring, float scale_log2, int t_lo, int nq, Geometry geo) {
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
   constexpr int KH = NCH / 2;      // chunks loaded together
   __shared__ int lists[THREADS / 32][32];
@@ -40,17 +40,18 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
   const unsigned lt_mask = (1u << lane) - 1u;
   int* lst = lists[warp];
   const int BH = B * H_kv;
-  // items (bh, t) with a grid stride, applied as (bh, t) increments
+  // items (bh, t), t in [t_lo, t_lo + nq), with a grid stride applied as (bh, t) increments
   const long long gw = (long long)blockIdx.x * (THREADS / 32) + warp;
   const long long nwarps = (long long)gridDim.x * (THREADS / 32);
-  const int st_bh = (int)(nwarps / N), st_t = (int)(nwarps % N);
+  const int st_bh = (int)(nwarps / nq), st_t = (int)(nwarps % nq);
+  const int t_end = t_lo + nq;
 
-  for (int bh = (int)(gw / N), t = (int)(gw % N); bh < BH;) {
+  for (int bh = (int)(gw / nq), t = t_lo + (int)(gw % nq); bh < BH;) {
     const long long item = (long long)bh * N + t;
     const int b = bh / H_kv, hk = bh - b * H_kv;
     int nbh = bh + st_bh, nt = t + st_t;  // the next item
-    if (nt >= N) {
-      nt -= N;
+    if (nt >= t_end) {
+      nt -= nq;
       ++nbh;
     }
     if (nbh < BH) {  // move its Q rows towards L2 while this walk runs (128 bytes per lane)
@@ -195,8 +196,9 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
 cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const Problem& p, const Geometry& geo,
                           int num_sms, uint32_t* err, cudaStream_t s) {
   (void)err;
-  const long long total = (long long)p.B * p.H_kv * p.N;
-  if (total == 0) return cudaSuccess;
+  const int nq = p.t_hi - p.t_lo;
+  const long long total = (long long)p.B * p.H_kv * nq;
+  if (total <= 0) return cudaSuccess;
   // persistent grid: exactly the CTAs that are resident at once, each walking items with a
   // grid stride, so no second partial wave
   const void* fn = p.d == 128 ? (const void*)stage1_kernel<128> : (const void*)stage1_kernel<64>;
@@ -210,10 +212,10 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
   const float sl2 = p.scale * LOG2E;
   if (p.d == 128)
     stage1_kernel<128><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scoring, sl2,
-                                                       geo);
+                                                       p.t_lo, nq, geo);
   else
     stage1_kernel<64><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scoring, sl2,
-                                                       geo);
+                                                       p.t_lo, nq, geo);
   return cudaGetLastError();
 }
 

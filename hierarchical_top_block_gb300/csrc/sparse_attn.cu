@@ -35,16 +35,18 @@ struct AttnParams {
   const int32_t* idx;
   uint16_t* O;
   float* LSE;
-  long long total;  // B * H_kv * N
+  long long total;  // B * H_kv * (queries in [t_lo, t_hi))
   int BH;           // B * H_kv
   int N, H_q, H_kv, GQ, Ksel, M1, causal;
+  int t_lo, nq;     // queries t_lo .. t_lo + nq - 1 are attended
   int one_box;      // 1: the 4-D map loads both d halves in one box
   float sl2;     // softmax scale x log2(e)
   float margin;  // RESCALE_MARGIN / sl2: headroom of the reference maximum in raw logit units
 };
 
 // Walks the (query, selected block, half block, K|V) load sequence of one warp.  Items are
-// (bh, t) pairs visited with a grid stride; the stride is applied as (bh, t) increments.
+// (bh, t) pairs, t in [t_lo, t_lo + nq), visited with a grid stride; the stride is applied
+// as (bh, t) increments.
 struct Cursor {
   int bh, t;        // current item; bh >= BH when exhausted
   unsigned mask;    // remaining valid idx positions of the item
@@ -53,14 +55,15 @@ struct Cursor {
 };
 
 struct Stride {
-  int bh, t;  // the grid stride in items, as (bh, t) increments
+  int bh, t;     // the grid stride in items, as (bh, t) increments
+  int t_end, nq;  // the query range ends at t_end and holds nq queries
 };
 
-__device__ __forceinline__ void step_item(int& bh, int& t, const Stride& st, int N) {
+__device__ __forceinline__ void step_item(int& bh, int& t, const Stride& st) {
   t += st.t;
   bh += st.bh;
-  if (t >= N) {
-    t -= N;
+  if (t >= st.t_end) {
+    t -= st.nq;
     ++bh;
   }
 }
@@ -127,8 +130,8 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   const uint64_t stream_policy = l2_evict_first_policy();
   const long long gw = (long long)blockIdx.x * NW + warp;
   const long long nwarps = (long long)gridDim.x * NW;
-  const Stride st{(int)(nwarps / p.N), (int)(nwarps % p.N)};
-  const int bh0 = (int)(gw / p.N), t0 = (int)(gw % p.N);
+  const Stride st{(int)(nwarps / p.nq), (int)(nwarps % p.nq), p.t_lo + p.nq, p.nq};
+  const int bh0 = (int)(gw / p.nq), t0 = p.t_lo + (int)(gw % p.nq);
 
   // ---- producer side of this warp's ring ----
   Cursor pc;
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   pc.t = t0;
   load_item(pc, p, err);
   while (pc.mask == 0 && pc.bh < p.BH) {
-    step_item(pc.bh, pc.t, st, p.N);
+    step_item(pc.bh, pc.t, st);
     load_item(pc, p, err);
   }
   // ring state: loads in flight, next slot to fill, next slot to consume and its parity
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
         pc.mask &= pc.mask - 1;
         first_block(pc, p);
         while (pc.mask == 0 && pc.bh < p.BH) {
-          step_item(pc.bh, pc.t, st, p.N);
+          step_item(pc.bh, pc.t, st);
           load_item(pc, p, err);
         }
       }
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   };
 
   bool ok = true;
-  for (int bh = bh0, t = t0; bh < p.BH && ok; step_item(bh, t, st, p.N)) {
+  for (int bh = bh0, t = t0; bh < p.BH && ok; step_item(bh, t, st)) {
     const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
     Cursor cc;
     cc.bh = bh;
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
     load_item(cc, p, nullptr);
     {  // move the next item's selection row and Q rows towards L2 while this one runs
       int nbh = bh, nt = t;
-      step_item(nbh, nt, st, p.N);
+      step_item(nbh, nt, st);
       if (nbh < p.BH) {
         const long long nitem = (long long)nbh * p.N + nt;
         const int nb = nbh / p.H_kv, nhk = nbh - nb * p.H_kv;
@@ -398,7 +401,9 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const uint16_t* V, co
   prm.idx = idx;
   prm.O = O;
   prm.LSE = LSE;
-  prm.total = (long long)p.B * p.H_kv * p.N;
+  prm.t_lo = p.t_lo;
+  prm.nq = p.t_hi - p.t_lo;
+  prm.total = prm.nq > 0 ? (long long)p.B * p.H_kv * prm.nq : 0;
   prm.BH = p.B * p.H_kv;
   prm.N = p.N;
   prm.H_q = p.H_q;

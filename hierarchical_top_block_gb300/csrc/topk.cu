@@ -16,15 +16,15 @@ constexpr int THREADS = 256;
 
 __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict__ S2,
                                                        const float* __restrict__ score, int32_t* __restrict__ idx,
-                                                       int BH, int N, int Ksel, int M1, int causal) {
+                                                       int BH, int N, int t_lo, int nq, int Ksel, int M1, int causal) {
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
   const long long gw = (long long)blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5);
   const long long nwarps = (long long)gridDim.x * (THREADS / 32);
-  const int st_bh = (int)(nwarps / N), st_t = (int)(nwarps % N);  // grid stride as (bh, t) steps
+  const int st_bh = (int)(nwarps / nq), st_t = (int)(nwarps % nq);  // grid stride as (bh, t) steps
   const int twoK = 2 * Ksel;
   const int keep_n = causal ? Ksel - 1 : Ksel;
-  for (int bh = (int)(gw / N), t = (int)(gw % N); bh < BH;) {
+  for (int bh = (int)(gw / nq), t = t_lo + (int)(gw % nq); bh < BH;) {
     const long long item = (long long)bh * N + t;
     const int own = causal ? t / 64 : -1;
     int leaf = -1;
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
     if (lane >= filled && lane < Ksel) out[lane] = -1;
     t += st_t;
     bh += st_bh;
-    if (t >= N) {
-      t -= N;
+    if (t >= t_lo + nq) {
+      t -= nq;
       ++bh;
     }
   }
@@ -80,11 +80,12 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
 
 cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx, const Problem& p,
                         const Geometry& geo, cudaStream_t s) {
-  const long long total = (long long)p.B * p.H_kv * p.N;
-  if (total == 0) return cudaSuccess;
+  const int nq = p.t_hi - p.t_lo;
+  const long long total = (long long)p.B * p.H_kv * nq;
+  if (total <= 0) return cudaSuccess;
   long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
   if (blocks > 65535LL * 8) blocks = 65535LL * 8;
-  topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.K, geo.M[1], p.causal);
+  topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1], p.causal);
   return cudaGetLastError();
 }
 

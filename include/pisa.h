@@ -166,9 +166,16 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
 /* ---- full prefill from host buffers (end-to-end path) --------------------------------- */
 
 /* Copies Q, K, V host -> device, builds the pyramid, selects, attends and copies O (and
- * LSE, idx when non-NULL) device -> host, all on `stream`, then synchronises the stream.
- * Host buffers should be pinned for full copy bandwidth.  dev_ws is device scratch of at
- * least pisa_prefill_host_workspace_bytes().  N_cap must equal N. */
+ * LSE, idx when non-NULL) device -> host; returns when all of it has finished.  The work runs
+ * in query chunks (at most 16, of at least 16384 positions) so that the host -> device copy
+ * of the next chunk's Q and the device -> host copy of the last chunk's O overlap the compute
+ * of the current one: kernels run on `stream`, the copies on two streams of the library's own
+ * (ordered after the work queued on `stream` before the call), and `stream` is idle again on
+ * return.  Results equal those of pisa_build_pyramid + pisa_select_prefill +
+ * pisa_sparse_attn_prefill on the same inputs.  One call at a time per device (calls from
+ * several threads are serialised).  Host buffers should be pinned for full copy bandwidth
+ * and concurrent copies.  dev_ws is device scratch of at least
+ * pisa_prefill_host_workspace_bytes().  N_cap must equal N. */
 PISA_API size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params);
 PISA_API pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, const uint16_t* V_host,
                               uint16_t* O_host, float* LSE_host, int32_t* idx_host, void* dev_ws, size_t ws_bytes,

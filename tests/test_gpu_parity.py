@@ -272,10 +272,16 @@ def test_decode_scoring_variants(oracle_impl, scoring):
     _decode_check(oracle_impl, w, N0=2040, steps=12, N_cap=2304, scoring=scoring)
 
 
-def test_prefill_host_matches_the_device_path():
+@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked"])
+def test_prefill_host_matches_the_device_path(case):
     """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
-    what the device-resident calls return on the same inputs."""
-    w = W.WORKLOADS["prefill_4k"].with_(B=2)
+    what the device-resident calls return on the same inputs.  The second case runs as three
+    query chunks (16384, 16384 and a ragged 2232) with two sequences per batch, so the chunked
+    copies of Q, O, LSE and the selection rows are all strided."""
+    if case == "4k_b2":
+        w = W.WORKLOADS["prefill_4k"].with_(B=2)
+    else:
+        w = W.WORKLOADS["prefill_32k"].with_(B=2, N=35000, H_q=8, H_kv=2)
     Q, K, V = _inputs(w)
     P = pisa.pisa_build_pyramid(K)
     idx = pisa.pisa_select_prefill(Q, K, P, w.K)
