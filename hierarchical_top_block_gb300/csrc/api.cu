@@ -19,14 +19,36 @@ constexpr int MAX_DEVICES = 64;
 
 // Streams and events of the host-buffer prefill pipeline (created on first use).
 constexpr int PIPE_MAX_CHUNKS = 16;
-constexpr int PIPE_EVENTS = 4 + 2 * PIPE_MAX_CHUNKS;
+constexpr int PIPE_EVENTS = 4 + 3 * PIPE_MAX_CHUNKS;
 
 struct HostPipe {
   bool ready = false;
-  std::mutex run;                   // one host-buffer prefill at a time per device
-  cudaStream_t in = nullptr, out = nullptr;  // host->device and device->host copies
+  std::mutex run;                                    // one host-buffer prefill at a time per device
+  cudaStream_t in = nullptr, out = nullptr;          // host->device and device->host copies
+  cudaStream_t attn = nullptr;                       // attention of chunk j beside selection of j+1
   cudaEvent_t ev[PIPE_EVENTS] = {};
 };
+
+// Query chunks of the host-buffer prefill: a short first chunk (the copy-in that precedes
+// any compute) and a short last chunk (the copy-out that follows it), growing threefold in
+// between up to a quarter of the sequence.  Sizes are multiples of 64 except the remainder.
+int plan_chunks(long long N, long long* bounds) {
+  long long lo = (N / 32 + 63) / 64 * 64;
+  if (lo < 4096) lo = 4096;
+  long long cap = N / 4 / 64 * 64;
+  if (cap < lo) cap = lo;
+  int n = 0;
+  long long t = 0, c = lo;
+  bounds[0] = 0;
+  while (t + c + lo < N && n < PIPE_MAX_CHUNKS - 2) {
+    t += c;
+    bounds[++n] = t;
+    c = 3 * c < cap ? 3 * c : cap;
+  }
+  if (N - t > lo) bounds[++n] = N - lo;
+  bounds[++n] = N;
+  return n;
+}
 
 struct DeviceState {
   bool ready = false;
@@ -61,6 +83,7 @@ pisa_status host_pipe(DeviceState* st, HostPipe** out) {
   if (!hp.ready) {
     if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&hp.attn, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
     for (cudaEvent_t& e : hp.ev)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return PISA_ERR_CUDA;
     hp.ready = true;
@@ -386,27 +409,31 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
 
   // Query chunks: selection and attention of chunk j need Q rows of chunk j only (plus all
   // of K and V), so the copy-in of chunk j+1 and the copy-out of chunk j-1 overlap the
-  // compute of chunk j.  Q and O are [B][N][H_q][d]: a chunk is one row band per sequence.
-  long long chunk = ((long long)p.N + PIPE_MAX_CHUNKS - 1) / PIPE_MAX_CHUNKS;
-  if (chunk < 16384) chunk = 16384;
-  chunk = (chunk + 63) / 64 * 64;
-  const int nchunks = (int)(((long long)p.N + chunk - 1) / chunk);
+  // compute of chunk j; attention of chunk j (its own stream) also overlaps selection of
+  // chunk j+1, which fills the tail of each persistent kernel with the next one's CTAs.
+  // The two share only idx, whose rows of different chunks are disjoint; selection scratch
+  // is reused from chunk to chunk in the order of `stream`.  Q and O are [B][N][H_q][d]: a
+  // chunk is one row band per sequence.
+  long long bounds[PIPE_MAX_CHUNKS + 1];
+  const int nchunks = plan_chunks(p.N, bounds);
   cudaEvent_t* ev = hp->ev;
   cudaEvent_t e_start = ev[0], e_k = ev[1], e_v = ev[2], e_end = ev[3];
   cudaEvent_t* e_q = ev + 4;
-  cudaEvent_t* e_attn = ev + 4 + PIPE_MAX_CHUNKS;
+  cudaEvent_t* e_sel = ev + 4 + PIPE_MAX_CHUNKS;
+  cudaEvent_t* e_attn = ev + 4 + 2 * PIPE_MAX_CHUNKS;
   const size_t q_row = (size_t)p.H_q * p.d * 2;  // bytes of one query position, all heads
   auto copy_q = [&](int j) {
-    const long long lo = j * chunk, hi = lo + chunk < p.N ? lo + chunk : p.N;
+    const long long lo = bounds[j], hi = bounds[j + 1];
     return cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(dQ) + lo * q_row, p.N * q_row,
                              reinterpret_cast<const uint8_t*>(Q_host) + lo * q_row, p.N * q_row, (hi - lo) * q_row, p.B,
                              cudaMemcpyHostToDevice, hp->in);
   };
   bool ok = true;
   auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
-  // the copy-in stream starts after whatever the caller queued on `stream` before this call
+  // the library's streams start after whatever the caller queued on `stream` before this call
   chk(cudaEventRecord(e_start, s));
   chk(cudaStreamWaitEvent(hp->in, e_start, 0));
+  chk(cudaStreamWaitEvent(hp->attn, e_start, 0));
   chk(cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, hp->in));
   chk(cudaEventRecord(e_k, hp->in));
   chk(copy_q(0));
@@ -420,19 +447,21 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   const Geometry geo = make_geometry(p.N, p.N);
   chk(cudaStreamWaitEvent(s, e_k, 0));
   if (ok) chk(launch_pyramid(dK, dP, p, geo, s));
+  chk(cudaStreamWaitEvent(hp->attn, e_v, 0));
   for (int j = 0; j < nchunks && ok; ++j) {
     Problem pc = p;
-    pc.t_lo = (int)(j * chunk);
-    pc.t_hi = (int)(pc.t_lo + chunk < p.N ? pc.t_lo + chunk : p.N);
+    pc.t_lo = (int)bounds[j];
+    pc.t_hi = (int)bounds[j + 1];
     chk(cudaStreamWaitEvent(s, e_q[j], 0));
     if (!ok) break;
     if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, pc, st, s)) != PISA_OK) {
       ok = false;
       break;
     }
-    if (j == 0) chk(cudaStreamWaitEvent(s, e_v, 0));
-    if (ok) chk(launch_sparse_attn(dQ, dK, dV, dIdx, dO, dL, pc, st->num_sms, st->err, s));
-    chk(cudaEventRecord(e_attn[j], s));
+    chk(cudaEventRecord(e_sel[j], s));
+    chk(cudaStreamWaitEvent(hp->attn, e_sel[j], 0));
+    if (ok) chk(launch_sparse_attn(dQ, dK, dV, dIdx, dO, dL, pc, st->num_sms, st->err, hp->attn));
+    chk(cudaEventRecord(e_attn[j], hp->attn));
     // copy-out of chunk j: O rows, and the LSE / selection columns of every head
     const size_t nq = (size_t)(pc.t_hi - pc.t_lo), t0 = (size_t)pc.t_lo;
     chk(cudaStreamWaitEvent(hp->out, e_attn[j], 0));
@@ -446,14 +475,15 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
       chk(cudaMemcpy2DAsync(idx_host + t0 * p.K, (size_t)p.N * p.K * 4, dIdx + t0 * p.K, (size_t)p.N * p.K * 4,
                             nq * p.K * 4, (size_t)p.B * p.H_kv, cudaMemcpyDeviceToHost, hp->out));
   }
-  // the call returns once all three streams are idle (also after an error, so that no copy
+  // the call returns once all four streams are idle (also after an error, so that no copy
   // is still writing into the caller's buffers)
   const cudaError_t e_rec = cudaEventRecord(e_end, hp->out);
   if (e_rec == cudaSuccess) cudaStreamWaitEvent(s, e_end, 0);
-  const cudaError_t e_in = cudaStreamSynchronize(hp->in), e_out = cudaStreamSynchronize(hp->out);
-  const cudaError_t e_s = cudaStreamSynchronize(s);
+  const cudaError_t e_in = cudaStreamSynchronize(hp->in), e_at = cudaStreamSynchronize(hp->attn);
+  const cudaError_t e_out = cudaStreamSynchronize(hp->out), e_s = cudaStreamSynchronize(s);
   if (rc != PISA_OK) return rc;
-  if (!ok || e_rec != cudaSuccess || e_in != cudaSuccess || e_out != cudaSuccess || e_s != cudaSuccess)
+  if (!ok || e_rec != cudaSuccess || e_in != cudaSuccess || e_at != cudaSuccess || e_out != cudaSuccess ||
+      e_s != cudaSuccess)
     return PISA_ERR_CUDA;
   return PISA_OK;
 }

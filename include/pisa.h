@@ -167,11 +167,12 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
 
 /* Copies Q, K, V host -> device, builds the pyramid, selects, attends and copies O (and
  * LSE, idx when non-NULL) device -> host; returns when all of it has finished.  The work runs
- * in query chunks (at most 16, of at least 16384 positions) so that the host -> device copy
- * of the next chunk's Q and the device -> host copy of the last chunk's O overlap the compute
- * of the current one: kernels run on `stream`, the copies on two streams of the library's own
- * (ordered after the work queued on `stream` before the call), and `stream` is idle again on
- * return.  Results equal those of pisa_build_pyramid + pisa_select_prefill +
+ * in query chunks (at most 16; the first and last about N/32 positions, at least 4096, the
+ * ones between growing threefold up to N/4) so that the host -> device copy of the next
+ * chunk's Q, the device -> host copy of the previous chunk's O and the attention of one chunk
+ * overlap the selection of the next: selection runs on `stream`, attention and the copies on
+ * three streams of the library's own (ordered after the work queued on `stream` before the
+ * call), and all of them are idle again on return.  Results equal those of pisa_build_pyramid + pisa_select_prefill +
  * pisa_sparse_attn_prefill on the same inputs.  One call at a time per device (calls from
  * several threads are serialised).  Host buffers should be pinned for full copy bandwidth
  * and concurrent copies.  dev_ws is device scratch of at least

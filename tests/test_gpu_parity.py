@@ -275,9 +275,9 @@ def test_decode_scoring_variants(oracle_impl, scoring):
 @pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked"])
 def test_prefill_host_matches_the_device_path(case):
     """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
-    what the device-resident calls return on the same inputs.  The second case runs as three
-    query chunks (16384, 16384 and a ragged 2232) with two sequences per batch, so the chunked
-    copies of Q, O, LSE and the selection rows are all strided."""
+    what the device-resident calls return on the same inputs.  The second case runs as six
+    query chunks (4096, 8704, 8704, 8704, 696, 4096) with two sequences per batch, so the
+    chunked copies of Q, O, LSE and the selection rows are all strided."""
     if case == "4k_b2":
         w = W.WORKLOADS["prefill_4k"].with_(B=2)
     else:
