@@ -26,11 +26,14 @@ constexpr int THREADS = 128;
 constexpr int MIN_BLOCKS_128 = 5, MIN_BLOCKS_64 = 6;
 
 
-template <int D>
+// SC: the block score (0 LSE, 1 log m + mean, 2 log m + mean + variance / 2), fixed at compile
+// time so that the pair score carries no branch
+template <int D, int SC>
 __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCKS_64) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
-                                                         int scoring, float scale_log2, int t_lo, int nq, Geometry geo) {
+                                                         float scale_log2, int t_lo, int nq, Geometry geo) {
+  constexpr int scoring = SC;
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
   constexpr int KH = NCH / 2;      // chunks loaded together
   __shared__ int lists[THREADS / 32][32];
@@ -160,13 +163,17 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       }
       if (lane >= nc) my = NEG_INF;
       // SelectK: bitonic sort of the 32 (score desc, index asc) pairs; the first Ksel lanes
-      // then hold the kept candidates
+      // then hold the kept candidates.  For Ksel = 16 the network stops after the first merge
+      // step of the last stage: the two sorted halves then face each other, so each of lanes
+      // 0..15 holds the better of a pair whose partners rank i and 15-i, i.e. the best 16 as
+      // a set (their order is not needed)
       float sv = my;
       int si = lane;
 #pragma unroll
       for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
+          if (k == 32 && j < 16 && Ksel == 16) break;
           const float ov = __shfl_xor_sync(0xffffffffu, sv, j);
           const int oi = __shfl_xor_sync(0xffffffffu, si, j);
           const bool other_better = ov > sv || (ov == sv && oi < si);
@@ -201,22 +208,26 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
   if (total <= 0) return cudaSuccess;
   // persistent grid: exactly the CTAs that are resident at once, each walking items with a
   // grid stride, so no second partial wave
-  const void* fn = p.d == 128 ? (const void*)stage1_kernel<128> : (const void*)stage1_kernel<64>;
-  int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, THREADS, 0);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
-  const long long cap = (long long)num_sms * per_sm;
-  if (blocks > cap) blocks = cap;
-  const float sl2 = p.scale * LOG2E;
-  if (p.d == 128)
-    stage1_kernel<128><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scoring, sl2,
-                                                       p.t_lo, nq, geo);
-  else
-    stage1_kernel<64><<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scoring, sl2,
-                                                       p.t_lo, nq, geo);
-  return cudaGetLastError();
+  auto go = [&](auto kern) -> cudaError_t {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
+    const long long cap = (long long)num_sms * per_sm;
+    if (blocks > cap) blocks = cap;
+    kern<<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scale * LOG2E, p.t_lo,
+                                         nq, geo);
+    return cudaGetLastError();
+  };
+  if (p.d == 128) {
+    if (p.scoring == 1) return go(stage1_kernel<128, 1>);
+    if (p.scoring == 2) return go(stage1_kernel<128, 2>);
+    return go(stage1_kernel<128, 0>);
+  }
+  if (p.scoring == 1) return go(stage1_kernel<64, 1>);
+  if (p.scoring == 2) return go(stage1_kernel<64, 2>);
+  return go(stage1_kernel<64, 0>);
 }
 
 }  // namespace pisa

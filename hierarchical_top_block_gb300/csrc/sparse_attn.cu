@@ -234,9 +234,14 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
         break;
       }
       const uint32_t kb = smem_u32(ring + cslot * SLOT);
-      float s[KS / 8][4];
+      // even and odd k-steps accumulate separately (s, s2) and are added at the end: two
+      // chains of four dependent MMAs per n-tile instead of one of eight, so the warp waits
+      // less on the MMA latency
+      float s[KS / 8][4], s2[KS / 8][4];
 #pragma unroll
-      for (int nt = 0; nt < KS / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int nt = 0; nt < KS / 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[nt][c] = s2[nt][c] = 0.f;
       // per 32 columns of d: all n-tiles' fragments first, then two rounds of independent MMAs
 #pragma unroll
       for (int kp = 0; kp < KST / 2; ++kp) {
@@ -253,9 +258,13 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
           mma_bf16_16816(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], bk[nt][0], bk[nt][1]);
 #pragma unroll
         for (int nt = 0; nt < KS / 8; ++nt)
-          mma_bf16_16816(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], bk[nt][2],
+          mma_bf16_16816(s2[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], bk[nt][2],
                          bk[nt][3]);
       }
+#pragma unroll
+      for (int nt = 0; nt < KS / 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[nt][c] += s2[nt][c];
       consume_next();
       issue_fill();
 
