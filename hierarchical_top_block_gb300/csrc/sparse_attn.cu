@@ -119,6 +119,17 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, q = lane & 3;
   uint8_t* ring = smem + (size_t)warp * NSLOT * SLOT;
+  // per-lane byte offsets of the ldmatrix rows inside a 128-byte-swizzled slot (16-byte
+  // chunk c of key row k sits at chunk c ^ (k & 7)): K fragments at d chunk lane/8 (+4 for
+  // odd 32-column groups), V fragments at key lane%16 and d chunk 2j + lane/16; every
+  // address below is one of these plus a compile-time constant
+  const uint32_t llo = lane & 7;
+  const uint32_t koff0 = llo * 128 + ((((uint32_t)lane >> 3) ^ llo) << 4);
+  const uint32_t koff1 = llo * 128 + (((4u ^ ((uint32_t)lane >> 3)) ^ llo) << 4);
+  uint32_t voff[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    voff[j] = ((((uint32_t)lane >> 3) & 1u) * 8 + llo) * 128 + (((2u * j) ^ ((uint32_t)lane >> 4) ^ llo) << 4);
   if (lane == 0) {
     for (int i = 0; i < NSLOT; ++i) mbar_init(&full[warp][i], 1);
     mbar_fence_init();
@@ -245,12 +256,10 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       // per 32 columns of d: all n-tiles' fragments first, then two rounds of independent MMAs
 #pragma unroll
       for (int kp = 0; kp < KST / 2; ++kp) {
-        const int d0 = 32 * kp + 8 * (lane >> 3);
         uint32_t bk[KS / 8][4];
 #pragma unroll
         for (int nt = 0; nt < KS / 8; ++nt) {
-          const int key = 8 * nt + (lane & 7);
-          const uint32_t addr = kb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          const uint32_t addr = kb + ((kp & 1) ? koff1 : koff0) + (kp >> 1) * HALF + nt * 1024;
           ldmatrix_x4(addr, bk[nt][0], bk[nt][1], bk[nt][2], bk[nt][3]);
         }
 #pragma unroll
@@ -337,11 +346,9 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       const uint32_t vb = smem_u32(ring + cslot * SLOT);
 #pragma unroll
       for (int kk = 0; kk < KS / 16; ++kk) {
-        const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
         for (int np = 0; np < NDT / 2; ++np) {
-          const int d0 = 8 * (2 * np + (lane >> 4));
-          const uint32_t addr = vb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+          const uint32_t addr = vb + voff[np & 3] + (np >> 2) * HALF + kk * 2048;
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4_trans(addr, b0, b1, b2, b3);
           mma_bf16_16816(o[2 * np], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
