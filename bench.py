@@ -38,8 +38,8 @@ KERNELS_PER_STEP = 12  # pyramid 2, stage 1, clustering 6, leaf LSE, top-K, atte
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
 # as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "6f16dbffc13c80ccb36943510a860ba2e2dc51beb687620c7785e17281deeb27",
-                "workload": "prefill_256k", "bytes": 16032366336 + 1299501312}
+ATTN_TRAFFIC = {"sources_sha256": "0783c6a21a10bb45b2a795beb54334a9d5d847fe8f609d335b7154223d39b26d",
+                "workload": "prefill_256k", "bytes": 14336186880 + 1093362432}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
