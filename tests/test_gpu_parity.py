@@ -272,26 +272,31 @@ def test_decode_scoring_variants(oracle_impl, scoring):
     _decode_check(oracle_impl, w, N0=2040, steps=12, N_cap=2304, scoring=scoring)
 
 
-@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked"])
+@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked", "35000_noncausal_pisa2_chunked"])
 def test_prefill_host_matches_the_device_path(case):
     """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
-    what the device-resident calls return on the same inputs.  The second case runs as six
+    what the device-resident calls return on the same inputs.  The chunked cases run as six
     query chunks (4096, 8704, 8704, 8704, 696, 4096) with two sequences per batch, so the
-    chunked copies of Q, O, LSE and the selection rows are all strided."""
+    chunked copies of Q, O, LSE and the selection rows are all strided; the last one also
+    selects without the causal mask (every block of the sequence is a candidate for every
+    chunk) and with the PISA-2 block score."""
+    causal, scoring = True, 0
     if case == "4k_b2":
         w = W.WORKLOADS["prefill_4k"].with_(B=2)
     else:
         w = W.WORKLOADS["prefill_32k"].with_(B=2, N=35000, H_q=8, H_kv=2)
+        if case == "35000_noncausal_pisa2_chunked":
+            causal, scoring = False, 2
     Q, K, V = _inputs(w)
     P = pisa.pisa_build_pyramid(K)
-    idx = pisa.pisa_select_prefill(Q, K, P, w.K)
-    O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx)
+    idx = pisa.pisa_select_prefill(Q, K, P, w.K, causal=causal, scoring=scoring)
+    O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx, causal=causal)
     torch.cuda.synchronize()
     Qh, Kh, Vh = (x.cpu().pin_memory() for x in (Q, K, V))
     Oh = torch.empty(Q.shape, dtype=torch.bfloat16).pin_memory()
     Lh = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
     Ih = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
-    pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, O_host=Oh, LSE_host=Lh, idx_host=Ih)
+    pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, causal=causal, O_host=Oh, LSE_host=Lh, idx_host=Ih, scoring=scoring)
     torch.cuda.synchronize()
     assert pisa.pisa_get_last_device_error() == 0
     assert torch.equal(Ih, idx.cpu())
