@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s (select + sparse attn)"
 UNIT = "tokens/s"
-KERNELS_PER_STEP = 12  # pyramid 2, stage 1, clustering 6, leaf LSE, top-K, attention
+KERNELS_PER_STEP = 11  # pyramid 2, stage 1 (with the clustering histogram), clustering 5, leaf LSE, top-K, attention
 
 # DRAM traffic of the attention kernel per launch on the 256K prefill (dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed

@@ -230,7 +230,8 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   cb.tiles = reinterpret_cast<int4*>(w + L.tiles);
   cb.totals = reinterpret_cast<int32_t*>(w + L.totals);
   const Geometry geo = make_geometry(p.N, p.N);
-  if (launch_stage1(Q, P, S2, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * cb.nkeys, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (launch_stage1(Q, P, S2, cb, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_cluster(S2, cb, p, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_leaf_lse(Q, K, cb, score, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_topk(S2, score, idx, p, geo, s) != cudaSuccess) return PISA_ERR_CUDA;

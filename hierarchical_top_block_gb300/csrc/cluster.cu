@@ -5,7 +5,8 @@
 // (query t, survivor slot i) becomes an entry in the list of key (b, h_kv, window, node).
 // Windows of consecutive queries keep the Q rows a tile gathers resident in L2.
 //
-//   count   : histogram of entries per key                 (atomics)
+//   count   : histogram of entries per key (atomics; accumulated by the Stage 1 walk as it
+//             writes each query's survivors, into counts zeroed before it)
 //   scan    : exclusive scans of counts and of ceil(count / qt) (three small kernels)
 //   scatter : entries[offset[key] + k] = (t << 6) | slot   (order within a key arbitrary)
 //   tiles   : {bh, node, first entry, entry count <= qt} for every tile
@@ -23,18 +24,6 @@ constexpr int SCAN_CHUNK = SCAN_THREADS * SCAN_PER_THREAD;
 
 __device__ __forceinline__ long long key_of(int bh, int t, int node, const ClusterBuffers& cb) {
   return ((long long)bh * cb.nwin + t / cb.win) * cb.M2 + node;
-}
-
-__global__ void count_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int t_lo, int nq, int Ksel,
-                             long long total) {
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total * Ksel;
-       e += (long long)gridDim.x * blockDim.x) {
-    const long long item = e / Ksel;
-    const int bh = (int)(item / nq), t = t_lo + (int)(item % nq);
-    const int node = S2[((long long)bh * N + t) * Ksel + (e - item * Ksel)];
-    if (node < 0) continue;
-    atomicAdd(&cb.counts[key_of(bh, t, node, cb)], 1);
-  }
 }
 
 // block-local exclusive scan of (count, tiles) pairs; writes block totals
@@ -173,10 +162,8 @@ cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Pr
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * (nq > 0 ? nq : 0);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cb.cursor, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cb.totals, 0, sizeof(int32_t) * 4, s)) != cudaSuccess) return e;  // [2] = tile counter
-  count_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.t_lo, nq, p.K, total);
   scan_local_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
   scan_blocks_kernel<<<1, SCAN_THREADS, 0, s>>>(cb);
   scan_add_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);

@@ -19,10 +19,6 @@ struct Problem {
 // Builds pyramid levels 1..geo.L from the first N rows of K (layout capacity N_cap).
 cudaError_t launch_pyramid(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s);
 
-// Stage 1: level walk for every (b, h_kv, t); writes the level-2 survivors S2 [.., K].
-cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const Problem& p, const Geometry& geo,
-                          int num_sms, uint32_t* err, cudaStream_t s);
-
 // Clustering of (query, level-2 survivor) entries into per-(b, h_kv, window, node) lists
 // and Q tiles for Stage 2.
 struct ClusterBuffers {
@@ -38,6 +34,12 @@ struct ClusterBuffers {
   int nwin, win, M2, qt, nblocks;
   long long max_tiles;
 };
+// Stage 1: level walk for every (b, h_kv, t); writes the level-2 survivors S2 [.., K] and adds
+// each survivor to the clustering histogram cb.counts (zeroed by the caller).
+cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const ClusterBuffers& cb, const Problem& p,
+                          const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s);
+
+// The rest of the clustering: scans of the histogram, scatter of the entries, tile list.
 cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Problem& p, cudaStream_t s);
 
 // Stage 2: exact leaf LSE of the candidate leaf pairs with tcgen05, head-summed.

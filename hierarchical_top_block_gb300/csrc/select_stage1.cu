@@ -31,6 +31,7 @@ constexpr int MIN_BLOCKS_128 = 5, MIN_BLOCKS_64 = 6;
 template <int D, int SC>
 __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCKS_64) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
+                                                         ClusterBuffers cb,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
                                                          float scale_log2, int t_lo, int nq, Geometry geo) {
   constexpr int scoring = SC;
@@ -193,6 +194,8 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       __syncwarp();
     }
     if (lane < Ksel) S2[item * Ksel + lane] = lane < ns ? surv : -1;
+    // the clustering histogram: one entry per survivor in the list of key (b, h_kv, window, node)
+    if (lane < ns) atomicAdd(&cb.counts[((long long)bh * cb.nwin + t / cb.win) * cb.M2 + surv], 1);
     bh = nbh;
     t = nt;
   }
@@ -200,8 +203,8 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
 
 }  // namespace
 
-cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const Problem& p, const Geometry& geo,
-                          int num_sms, uint32_t* err, cudaStream_t s) {
+cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const ClusterBuffers& cb, const Problem& p,
+                          const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s) {
   (void)err;
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * nq;
@@ -216,7 +219,7 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
     long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
     const long long cap = (long long)num_sms * per_sm;
     if (blocks > cap) blocks = cap;
-    kern<<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scale * LOG2E, p.t_lo,
+    kern<<<(int)blocks, THREADS, 0, s>>>(Q, P, S2, cb, p.B, p.N, p.H_q, p.H_kv, p.GQ, p.K, p.causal, p.scale * LOG2E, p.t_lo,
                                          nq, geo);
     return cudaGetLastError();
   };

@@ -272,10 +272,10 @@ def test_decode_scoring_variants(oracle_impl, scoring):
     _decode_check(oracle_impl, w, N0=2040, steps=12, N_cap=2304, scoring=scoring)
 
 
-@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked", "35000_noncausal_pisa2_chunked"])
+@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked", "35000_noncausal_pisa2_chunked", "20000_d64_k4_chunked"])
 def test_prefill_host_matches_the_device_path(case):
     """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
-    what the device-resident calls return on the same inputs.  The chunked cases run as six
+    what the device-resident calls return on the same inputs.  The 35000-token cases run as six
     query chunks (4096, 8704, 8704, 8704, 696, 4096) with two sequences per batch, so the
     chunked copies of Q, O, LSE and the selection rows are all strided; the last one also
     selects without the causal mask (every block of the sequence is a candidate for every
@@ -283,6 +283,8 @@ def test_prefill_host_matches_the_device_path(case):
     causal, scoring = True, 0
     if case == "4k_b2":
         w = W.WORKLOADS["prefill_4k"].with_(B=2)
+    elif case == "20000_d64_k4_chunked":  # d = 64, G_Q = 4, K = 4: chunks 4096, 4992, 4992, 1824, 4096
+        w = W.WORKLOADS["tiny"].with_(N=20000)
     else:
         w = W.WORKLOADS["prefill_32k"].with_(B=2, N=35000, H_q=8, H_kv=2)
         if case == "35000_noncausal_pisa2_chunked":
