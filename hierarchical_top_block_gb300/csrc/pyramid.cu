@@ -109,21 +109,49 @@ __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t*
   }
 }
 
-// Levels first_level..L for one (b, h_kv), each from the level below it in P.
+// Levels first_level..L for one (b, h_kv), each from the level below it in P.  A thread takes
+// 16-byte chunks (8 values of one row) in batches: all loads of a batch are issued before its
+// stores, so a level costs about one memory round trip per batch instead of one per value.
 template <int D>
 __global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __restrict__ P, Geometry geo,
                                                                 int first_level) {
+  constexpr int CH = D / 8;   // chunks per row
+  constexpr int BATCH = 8;
   uint16_t* Pb = P + (size_t)blockIdx.x * geo.nodes * D;
   for (int l = first_level; l <= geo.L; ++l) {
-    const int m = geo.M[l];
-    for (int idx = threadIdx.x; idx < m * D; idx += THREADS) {
-      const int node = idx / D, e = idx % D;
-      const int c0 = 2 * node, c1 = min(2 * node + 2, geo.M[l - 1]);
-      const float a = bf16_to_f32(Pb[(size_t)(geo.off[l - 1] + c0) * D + e]);
-      const float b = c1 - c0 > 1 ? bf16_to_f32(Pb[(size_t)(geo.off[l - 1] + c0 + 1) * D + e]) : 0.f;
-      float s, err;
-      two_sum(a, b, s, err);
-      Pb[(size_t)(geo.off[l] + node) * D + e] = bf16_mean(s, err, c1 - c0);
+    const int m = geo.M[l], mc = geo.M[l - 1];
+    const int total = m * CH;
+    const uint16_t* src = Pb + (size_t)geo.off[l - 1] * D;
+    uint16_t* dst = Pb + (size_t)geo.off[l] * D;
+    for (int base = threadIdx.x; base < total; base += THREADS * BATCH) {
+      uint4 va[BATCH], vb[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        va[u] = vb[u] = make_uint4(0, 0, 0, 0);
+        if (idx < total) {
+          const int node = idx / CH, c = idx - node * CH;
+          va[u] = *reinterpret_cast<const uint4*>(src + (size_t)(2 * node) * D + 8 * c);
+          if (2 * node + 1 < mc) vb[u] = *reinterpret_cast<const uint4*>(src + (size_t)(2 * node + 1) * D + 8 * c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx >= total) continue;
+        const int node = idx / CH, c = idx - node * CH;
+        const int cnt = 2 * node + 1 < mc ? 2 : 1;
+        const uint32_t wa[4] = {va[u].x, va[u].y, va[u].z, va[u].w}, wb[4] = {vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+        uint32_t packed[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float s0, e0, s1, e1;
+          two_sum(bf16_lo(wa[k]), cnt > 1 ? bf16_lo(wb[k]) : 0.f, s0, e0);
+          two_sum(bf16_hi(wa[k]), cnt > 1 ? bf16_hi(wb[k]) : 0.f, s1, e1);
+          packed[k] = (uint32_t)bf16_mean(s0, e0, cnt) | ((uint32_t)bf16_mean(s1, e1, cnt) << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + (size_t)node * D + 8 * c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
     }
     __syncthreads();
   }
