@@ -234,7 +234,7 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   if (launch_stage1(Q, P, S2, cb, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_cluster(S2, cb, p, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_leaf_lse(Q, K, cb, score, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
-  if (launch_topk(S2, score, idx, p, geo, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (launch_topk(S2, score, idx, p, geo, st->num_sms, s) != cudaSuccess) return PISA_ERR_CUDA;
   return PISA_OK;
 }
 

@@ -48,7 +48,7 @@ cudaError_t launch_leaf_lse(const uint16_t* Q, const uint16_t* K, const ClusterB
 
 // Final top-K with the own block kept; idx rows ascending, -1 padded.
 cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx, const Problem& p,
-                        const Geometry& geo, cudaStream_t s);
+                        const Geometry& geo, int num_sms, cudaStream_t s);
 
 // Block-sparse attention over idx.
 cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,

@@ -24,19 +24,41 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
   const int st_bh = (int)(nwarps / nq), st_t = (int)(nwarps % nq);  // grid stride as (bh, t) steps
   const int twoK = 2 * Ksel;
   const int keep_n = causal ? Ksel - 1 : Ksel;
-  for (int bh = (int)(gw / nq), t = t_lo + (int)(gw % nq); bh < BH;) {
-    const long long item = (long long)bh * N + t;
-    const int own = causal ? t / 64 : -1;
+  // lane s reads slot s of an item: its level-2 survivor and its leaf score (both in bounds;
+  // the score of an empty slot is never used), and the next item's pair is read while the
+  // current item is ranked
+  auto fetch = [&](int fbh, int ft, int& node, float& sc) {
+    node = -1;
+    sc = NEG_INF;
+    if (fbh < BH && lane < twoK) {
+      const long long fitem = (long long)fbh * N + ft;
+      node = S2[fitem * Ksel + (lane >> 1)];
+      sc = score[fitem * twoK + lane];
+    }
+  };
+  int bh = (int)(gw / nq), t = t_lo + (int)(gw % nq);
+  int node_n;
+  float sc_n;
+  fetch(bh, t, node_n, sc_n);
+  while (bh < BH) {
+    const int node = node_n, cbh = bh, ct = t;
+    const float sc_raw = sc_n;
+    t += st_t;
+    bh += st_bh;
+    if (t >= t_lo + nq) {
+      t -= nq;
+      ++bh;
+    }
+    fetch(bh, t, node_n, sc_n);
+    const long long item = (long long)cbh * N + ct;
+    const int own = causal ? ct / 64 : -1;
     int leaf = -1;
     float sc = NEG_INF;
-    if (lane < twoK) {
-      const int node = S2[item * Ksel + (lane >> 1)];
-      if (node >= 0) {
-        const int j = 2 * node + (lane & 1);
-        if (j < M1 && (!causal || j <= t / 64) && j != own) {
-          leaf = j;
-          sc = score[item * twoK + lane];
-        }
+    if (node >= 0) {
+      const int j = 2 * node + (lane & 1);
+      if (j < M1 && (!causal || j <= ct / 64) && j != own) {
+        leaf = j;
+        sc = sc_raw;
       }
     }
     // The survivors, hence the slots, are in ascending block order, so ranking by (score
@@ -67,24 +89,20 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
     if (causal && lane == 0) out[__popc(km & below)] = own;
     const int filled = __popc(km) + (causal ? 1 : 0);
     if (lane >= filled && lane < Ksel) out[lane] = -1;
-    t += st_t;
-    bh += st_bh;
-    if (t >= t_lo + nq) {
-      t -= nq;
-      ++bh;
-    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx, const Problem& p,
-                        const Geometry& geo, cudaStream_t s) {
+                        const Geometry& geo, int num_sms, cudaStream_t s) {
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * nq;
   if (total <= 0) return cudaSuccess;
+  // one wave of resident CTAs, each warp walking items with a grid stride (so that the next
+  // item's rows are in flight while the current one is ranked)
   long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
-  if (blocks > 65535LL * 8) blocks = 65535LL * 8;
+  if (blocks > (long long)num_sms * 8) blocks = (long long)num_sms * 8;
   topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1], p.causal);
   return cudaGetLastError();
 }
