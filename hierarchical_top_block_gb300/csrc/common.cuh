@@ -301,7 +301,6 @@ __device__ __forceinline__ void st_b32_hint(void* p, uint32_t v, uint64_t policy
 }
 
 // Fetch the 128-byte line holding p into L1 (no register result).
-__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // 16-byte read-only global load.

@@ -106,16 +106,6 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       const int tc = t >> (l + 4);  // the same for level-(l-1) nodes
       const uint16_t* Pl = Pb + (size_t)geo.off[l - 1] * D;
       const int Mc = geo.M[l - 1];
-      // lane i starts candidate i's two (adjacent) child rows on their way to L1, so the level
-      // costs one memory round trip
-      if (lane < nc) {
-        const int ch = 2 * cand;
-        const bool v1 = ch + 1 < Mc && (!causal || ch + 1 <= tc);
-        const uint16_t* row = Pl + (size_t)ch * D;
-#pragma unroll
-        for (int o = 0; o < (2 * D * 2) / 128; ++o)
-          if (o < (D * 2) / 128 || v1) prefetch_l1(row + o * 64);
-      }
       float my = NEG_INF;  // score of candidate `lane`
       const int nmt = (nc + 7) >> 3;
       for (int mt = 0; mt < nmt; ++mt) {
