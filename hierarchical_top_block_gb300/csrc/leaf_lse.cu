@@ -346,13 +346,20 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           // four independent partial sums; the mask is only needed inside the own block
           float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
           if (lim >= 63) {
+            // the scaling and the sums two lanes per instruction (packed fp32: same roundings
+            // and the same four partial sums as the scalar form)
+            const unsigned long long s2 = pack_f32x2(prm.sl2, prm.sl2);
+            unsigned long long acc01 = 0ull, acc23 = 0ull;
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
-              p0 += fast_exp2(__uint_as_float(v[j]) * prm.sl2);
-              p1 += fast_exp2(__uint_as_float(v[j + 1]) * prm.sl2);
-              p2 += fast_exp2(__uint_as_float(v[j + 2]) * prm.sl2);
-              p3 += fast_exp2(__uint_as_float(v[j + 3]) * prm.sl2);
+              float a, b, c, d;
+              unpack_f32x2(mul_f32x2(pack_u32x2(v[j], v[j + 1]), s2), a, b);
+              unpack_f32x2(mul_f32x2(pack_u32x2(v[j + 2], v[j + 3]), s2), c, d);
+              acc01 = add_f32x2(acc01, pack_f32x2(fast_exp2(a), fast_exp2(b)));
+              acc23 = add_f32x2(acc23, pack_f32x2(fast_exp2(c), fast_exp2(d)));
             }
+            unpack_f32x2(acc01, p0, p1);
+            unpack_f32x2(acc23, p2, p3);
           } else {
 #pragma unroll
             for (int j = 0; j < 64; j += 2) {
