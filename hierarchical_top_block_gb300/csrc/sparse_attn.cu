@@ -324,20 +324,32 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
       }
       // every processed half block holds a visible key, so m0 and m1 are finite here
       const float ms0 = -m0 * p.sl2, ms1 = -m1 * p.sl2;
+      // exponent arguments and row sums two lanes per instruction (packed fp32)
+      const unsigned long long sl2x2 = pack_f32x2(p.sl2, p.sl2);
+      const unsigned long long ms0x2 = pack_f32x2(ms0, ms0), ms1x2 = pack_f32x2(ms1, ms1);
+      unsigned long long lx0 = 0ull, lx1 = 0ull;
       uint32_t pa[KS / 16][4];
 #pragma unroll
       for (int nt = 0; nt < KS / 8; ++nt) {
-        const float p00 = fast_exp2(fmaf(s[nt][0], p.sl2, ms0));
-        const float p01 = fast_exp2(fmaf(s[nt][1], p.sl2, ms0));
-        const float p10 = fast_exp2(fmaf(s[nt][2], p.sl2, ms1));
-        const float p11 = fast_exp2(fmaf(s[nt][3], p.sl2, ms1));
-        l0 += p00 + p01;
-        l1 += p10 + p11;
+        float x00, x01, x10, x11;
+        unpack_f32x2(fma_f32x2(pack_f32x2(s[nt][0], s[nt][1]), sl2x2, ms0x2), x00, x01);
+        unpack_f32x2(fma_f32x2(pack_f32x2(s[nt][2], s[nt][3]), sl2x2, ms1x2), x10, x11);
+        const float p00 = fast_exp2(x00), p01 = fast_exp2(x01);
+        const float p10 = fast_exp2(x10), p11 = fast_exp2(x11);
+        lx0 = add_f32x2(lx0, pack_f32x2(p00, p01));
+        lx1 = add_f32x2(lx1, pack_f32x2(p10, p11));
         const int kk = nt >> 1, hi = nt & 1;
         pa[kk][hi ? 2 : 0] = pack_bf16x2(p00, p01);
         pa[kk][hi ? 3 : 1] = pack_bf16x2(p10, p11);
       }
 
+      {
+        float a0, b0, a1, b1;
+        unpack_f32x2(lx0, a0, b0);
+        unpack_f32x2(lx1, a1, b1);
+        l0 += a0 + b0;
+        l1 += a1 + b1;
+      }
       // ---------------- O += P V ----------------
       if (!mbar_wait_warp(&full[warp][cslot], cphase, err)) {
         ok = false;
