@@ -169,7 +169,7 @@ pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p)
 }
 
 struct SelectLayout {
-  size_t s2, score, counts, cursor, offsets, tile_off, block_sums, entries, tiles, totals, total_bytes;
+  size_t s2, score, counts, offsets, tile_off, block_sums, entries, tiles, totals, total_bytes;
   ClusterBuffers cb;  // sizes only; pointers filled by carve()
 };
 
@@ -200,7 +200,6 @@ SelectLayout select_layout(const Problem& p) {
   L.s2 = take(sizeof(int32_t) * total * p.K);
   L.score = take(sizeof(float) * total * 2 * p.K);
   L.counts = take(sizeof(int32_t) * cb.nkeys);
-  L.cursor = take(sizeof(int32_t) * cb.nkeys);
   L.offsets = take(sizeof(int32_t) * cb.nkeys);
   L.tile_off = take(sizeof(int32_t) * cb.nkeys);
   L.block_sums = take(sizeof(int32_t) * 2 * cb.nblocks);
@@ -222,7 +221,7 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   float* score = leaf_score ? leaf_score : reinterpret_cast<float*>(w + L.score);
   ClusterBuffers cb = L.cb;
   cb.counts = reinterpret_cast<int32_t*>(w + L.counts);
-  cb.cursor = reinterpret_cast<int32_t*>(w + L.cursor);
+  cb.rank = reinterpret_cast<int32_t*>(score);  // list places, until Stage 2 writes the scores
   cb.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
   cb.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
   cb.block_sums = reinterpret_cast<int32_t*>(w + L.block_sums);

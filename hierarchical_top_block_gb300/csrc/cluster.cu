@@ -6,7 +6,8 @@
 // Windows of consecutive queries keep the Q rows a tile gathers resident in L2.
 //
 //   count   : histogram of entries per key (atomics; accumulated by the Stage 1 walk as it
-//             writes each query's survivors, into counts zeroed before it)
+//             writes each query's survivors, into counts zeroed before it; the value each
+//             atomic returned is the entry's place k in its list, kept in cb.rank)
 //   scan    : exclusive scans of counts and of ceil(count / qt) (three small kernels)
 //   scatter : entries[offset[key] + k] = (t << 6) | slot   (order within a key arbitrary)
 //   tiles   : {bh, node, first entry, entry count <= qt} for every tile
@@ -132,7 +133,7 @@ __global__ void scatter_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb
     const int node = S2[((long long)bh * N + t) * Ksel + slot];
     if (node < 0) continue;
     const long long key = key_of(bh, t, node, cb);
-    const int pos = cb.offsets[key] + atomicAdd(&cb.cursor[key], 1);
+    const int pos = cb.offsets[key] + cb.rank[((long long)bh * N + t) * (2 * Ksel) + slot];
     cb.entries[pos] = (t << 6) | slot;
   }
 }
@@ -162,7 +163,6 @@ cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Pr
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * (nq > 0 ? nq : 0);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(cb.cursor, 0, sizeof(int32_t) * cb.nkeys, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cb.totals, 0, sizeof(int32_t) * 4, s)) != cudaSuccess) return e;  // [2] = tile counter
   scan_local_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
   scan_blocks_kernel<<<1, SCAN_THREADS, 0, s>>>(cb);

@@ -23,7 +23,8 @@ cudaError_t launch_pyramid(const uint16_t* K, uint16_t* P, const Problem& p, con
 // and Q tiles for Stage 2.
 struct ClusterBuffers {
   int32_t* counts;      // [nkeys]
-  int32_t* cursor;      // [nkeys]
+  int32_t* rank;        // [B * H_kv * N * 2K]  place of entry (t, slot) in its key's list, at
+                        // [(bh * N + t) * 2K + slot] (the leaf-score buffer, before Stage 2 fills it)
   int32_t* offsets;     // [nkeys]  exclusive scan of counts
   int32_t* tile_off;    // [nkeys]  exclusive scan of ceil(counts / qt)
   int32_t* block_sums;  // [2 * nblocks]

@@ -14,7 +14,8 @@
 // lane holds both children of one candidate and the pair LSE needs no exchange).  The d
 // index is permuted identically in A and B so that each lane loads 8 contiguous values per
 // row.  Candidate lists, LSE, head sums and a bitonic SelectK stay in registers and warp
-// shuffles: no query-key score matrix is materialised.
+// shuffles: no query-key score matrix is materialised.  Each survivor is also counted into
+// the clustering histogram, and the count returned is stored as its place in its list.
 #include "kernels.cuh"
 
 namespace pisa {
@@ -50,6 +51,9 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
   const int st_bh = (int)(nwarps / nq), st_t = (int)(nwarps % nq);
   const int t_end = t_lo + nq;
 
+  bool pend = false;  // this lane holds the list place of a survivor not yet stored
+  int pend_rank = 0;
+  long long pend_item = 0;
   for (int bh = (int)(gw / nq), t = t_lo + (int)(gw % nq); bh < BH;) {
     const long long item = (long long)bh * N + t;
     const int b = bh / H_kv, hk = bh - b * H_kv;
@@ -184,11 +188,19 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       __syncwarp();
     }
     if (lane < Ksel) S2[item * Ksel + lane] = lane < ns ? surv : -1;
-    // the clustering histogram: one entry per survivor in the list of key (b, h_kv, window, node)
-    if (lane < ns) atomicAdd(&cb.counts[((long long)bh * cb.nwin + t / cb.win) * cb.M2 + surv], 1);
+    // the clustering histogram: one entry per survivor in the list of key (b, h_kv, window,
+    // node); the count returned is the entry's place in that list, stored one item later so
+    // that the atomic's round trip overlaps the next walk
+    if (pend) cb.rank[pend_item * (2 * Ksel) + lane] = pend_rank;
+    pend = lane < ns;
+    if (pend) {
+      pend_rank = atomicAdd(&cb.counts[((long long)bh * cb.nwin + t / cb.win) * cb.M2 + surv], 1);
+      pend_item = item;
+    }
     bh = nbh;
     t = nt;
   }
+  if (pend) cb.rank[pend_item * (2 * Ksel) + lane] = pend_rank;
 }
 
 }  // namespace
