@@ -146,10 +146,31 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
         }
         // per head: the pair score (LSE or one of its truncations), log2 units; child 1 may be absent
         float part = 0.f;
-        if (2 * q < GQ) part += pair_score(a0[0], a0[2], v1, scale_log2, scoring);
-        if (2 * q + 1 < GQ) part += pair_score(a0[1], a0[3], v1, scale_log2, scoring);
-        if (8 + 2 * q < GQ) part += pair_score(a1[0], a1[2], v1, scale_log2, scoring);
-        if (9 + 2 * q < GQ) part += pair_score(a1[1], a1[3], v1, scale_log2, scoring);
+        if (scoring == 0 && GQ >= 16 && v1) {
+          // the four pair LSEs two heads per instruction (packed fp32, same roundings as the
+          // scalar form, summed in the same order)
+          const unsigned long long s2 = pack_f32x2(scale_log2, scale_log2);
+          const unsigned long long one2 = pack_f32x2(1.f, 1.f);
+          float r[4];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float* c = hh == 0 ? a0 : a1;
+            const float m0 = fmaxf(c[0], c[2]), m1 = fmaxf(c[1], c[3]);
+            const float n0 = fminf(c[0], c[2]), n1 = fminf(c[1], c[3]);
+            float d0, d1;
+            unpack_f32x2(mul_f32x2(add_f32x2(pack_f32x2(n0, n1), pack_f32x2(-m0, -m1)), s2), d0, d1);
+            float e0, e1;
+            unpack_f32x2(add_f32x2(one2, pack_f32x2(fast_exp2(d0), fast_exp2(d1))), e0, e1);
+            unpack_f32x2(fma_f32x2(pack_f32x2(m0, m1), s2, pack_f32x2(fast_log2(e0), fast_log2(e1))), r[2 * hh],
+                         r[2 * hh + 1]);
+          }
+          part = ((r[0] + r[1]) + r[2]) + r[3];
+        } else {
+          if (2 * q < GQ) part += pair_score(a0[0], a0[2], v1, scale_log2, scoring);
+          if (2 * q + 1 < GQ) part += pair_score(a0[1], a0[3], v1, scale_log2, scoring);
+          if (8 + 2 * q < GQ) part += pair_score(a1[0], a1[2], v1, scale_log2, scoring);
+          if (9 + 2 * q < GQ) part += pair_score(a1[1], a1[3], v1, scale_log2, scoring);
+        }
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         // candidate 8mt + r's score (held by lanes 4r..4r+3) to lane 8mt + r
