@@ -65,7 +65,8 @@ struct Params {
   float sl2;  // scale * log2(e)
 };
 
-template <int D>
+// SC >= 0: the block score fixed at compile time (else prm.scoring); R > 0: G_Q = RPQ = R
+template <int D, int SC, int R>
 __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                               const __grid_constant__ CUtensorMap mapK, Params prm,
                                                               uint32_t* err) {
@@ -261,8 +262,10 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     const int ew = warp - 2;
     const int grp = ew >> 2;
     const int quarter = warp & 3;
+    const int RPQ = R > 0 ? R : prm.RPQ, GQ = R > 0 ? R : prm.GQ;
+    const int scoring = SC >= 0 ? SC : prm.scoring;
     const int row = quarter * 32 + lane;
-    const int qi = row / prm.RPQ, h = row - qi * prm.RPQ;
+    const int qi = row / RPQ, h = row - qi * RPQ;
     const int twoK = 2 * prm.Ksel;
     for (int it = grp;; it += NACC) {
       const int qs = it % NQS;
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         if (prm.causal && (long long)t - key0 < lim64) lim64 = (long long)t - key0;
         const int lim = (int)(lim64 < 63 ? lim64 : 63);
         float lse2 = NEG_INF;
-        if (leaf_ok && h < prm.GQ && prm.scoring != 0) {
+        if (leaf_ok && h < GQ && scoring != 0) {
           // truncated forms over the m = lim + 1 visible keys, log2 units: log2 m + mean(x),
           // plus ln2/2 * Var(x) for the second order; x = logit * sl2, so the sums run on the
           // raw logits and are scaled once (Var by sl2^2)
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           }
           const float mean = ((a0 + a1) + (a2 + a3)) / m;  // raw logits
           lse2 = fast_log2(m) + mean * prm.sl2;
-          if (prm.scoring == 2) {
+          if (scoring == 2) {
             float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;
             if (lim >= 63) {
 #pragma unroll
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
             }
             lse2 += 0.5f * LN2 * prm.sl2 * prm.sl2 * ((q0 + q1) + (q2 + q3)) / m;
           }
-        } else if (leaf_ok && h < prm.GQ) {
+        } else if (leaf_ok && h < GQ) {
           // four independent partial sums; the mask is only needed inside the own block
           float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
           if (lim >= 63) {
@@ -383,8 +386,8 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           }
         }
         // sum over the G_Q head rows of each query (lanes of one query are contiguous)
-        float part = (leaf_ok && h < prm.GQ) ? lse2 : 0.f;
-        for (int o = 1; o < prm.RPQ; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        float part = (leaf_ok && h < GQ) ? lse2 : 0.f;
+        for (int o = 1; o < RPQ; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (vq && h == 0)
           prm.leaf_score[((size_t)bh * prm.N + t) * twoK + 2 * slot + leaf_c] = leaf_ok ? part * LN2 : NEG_INF;
       }
@@ -442,10 +445,14 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
   prm.scoring = p.scoring;
   prm.sl2 = p.scale * LOG2E;
   const size_t smem = (size_t)(NQS + NKS) * ROWS * D * 2 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(leaf_lse_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  leaf_lse_kernel<D><<<num_sms, THREADS, smem, s>>>(mapQ, mapK, prm, err);
-  return cudaGetLastError();
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<num_sms, THREADS, smem, s>>>(mapQ, mapK, prm, err);
+    return cudaGetLastError();
+  };
+  if (p.GQ == 16 && RPQ == 16) return p.scoring == 0 ? go(leaf_lse_kernel<D, 0, 16>) : go(leaf_lse_kernel<D, -1, 16>);
+  return p.scoring == 0 ? go(leaf_lse_kernel<D, 0, 0>) : go(leaf_lse_kernel<D, -1, 0>);
 }
 
 }  // namespace
