@@ -289,18 +289,15 @@ __global__ void __launch_bounds__(32 * NW, 1) sparse_attn_kernel(const __grid_co
           }
         }
       }
-      bool over = false;
+      // this lane's row maxima of the half block, then one test against the thresholds
+      float mx0 = fmaxf(s[0][0], s[0][1]), mx1 = fmaxf(s[0][2], s[0][3]);
 #pragma unroll
-      for (int nt = 0; nt < KS / 8; ++nt)
-        over |= (s[nt][0] > th0) | (s[nt][1] > th0) | (s[nt][2] > th1) | (s[nt][3] > th1);
-      if (__any_sync(0xffffffffu, over)) {
+      for (int nt = 1; nt < KS / 8; ++nt) {
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
+      if (__any_sync(0xffffffffu, (mx0 > th0) | (mx1 > th1))) {
         // exact row maxima of this half block; move the reference and rescale O and l
-        float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-        for (int nt = 0; nt < KS / 8; ++nt) {
-          mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-          mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-        }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
