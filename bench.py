@@ -38,8 +38,8 @@ KERNELS_PER_STEP = 11  # pyramid 2, stage 1 (with the clustering histogram), clu
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
 # as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "db6ccf34560184de3563f07297424221ef0688f486879703b180868f972d8e59",
-                "workload": "prefill_256k", "bytes": 14017314816 + 1090693376}
+ATTN_TRAFFIC = {"sources_sha256": "040ba5c75085c0959672db135df9813763a08899ce7902c0749c076d9a92f887",
+                "workload": "prefill_256k", "bytes": 13929120768 + 1089666816}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
