@@ -239,19 +239,39 @@ __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
         }
         // dS = P (dP - D), packed as bf16 A fragments (keys are the k index of dQ += dS K)
         uint32_t sa[2][4];
+        if (kbase + 31 <= last) {  // every key of the half block visible: packed fp32 pairs
+          const unsigned long long sl2x2 = pack_f32x2(p.sl2, p.sl2);
+          const unsigned long long nl0 = pack_f32x2(-lse2[0], -lse2[0]), nl1 = pack_f32x2(-lse2[1], -lse2[1]);
+          const unsigned long long nd0 = pack_f32x2(-dsum[0], -dsum[0]), nd1 = pack_f32x2(-dsum[1], -dsum[1]);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          float ds[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int key = kbase + 8 * nt + 2 * q + (u & 1);
-            const int rr = u >> 1;
-            const float pr = key <= last ? fast_exp2(fmaf(sacc[nt][u], p.sl2, -lse2[rr])) : 0.f;
-            ds[u] = pr * (pacc[nt][u] - dsum[rr]);
+          for (int nt = 0; nt < 4; ++nt) {
+            float x0, x1, x2, x3;
+            unpack_f32x2(fma_f32x2(pack_f32x2(sacc[nt][0], sacc[nt][1]), sl2x2, nl0), x0, x1);
+            unpack_f32x2(fma_f32x2(pack_f32x2(sacc[nt][2], sacc[nt][3]), sl2x2, nl1), x2, x3);
+            float d0, d1, d2, d3;
+            unpack_f32x2(mul_f32x2(pack_f32x2(fast_exp2(x0), fast_exp2(x1)),
+                                   add_f32x2(pack_f32x2(pacc[nt][0], pacc[nt][1]), nd0)), d0, d1);
+            unpack_f32x2(mul_f32x2(pack_f32x2(fast_exp2(x2), fast_exp2(x3)),
+                                   add_f32x2(pack_f32x2(pacc[nt][2], pacc[nt][3]), nd1)), d2, d3);
+            const int kk = nt >> 1, hi = nt & 1;
+            sa[kk][hi ? 2 : 0] = pack_bf16x2(d0, d1);
+            sa[kk][hi ? 3 : 1] = pack_bf16x2(d2, d3);
           }
-          const int kk = nt >> 1, hi = nt & 1;
-          sa[kk][hi ? 2 : 0] = pack_bf16x2(ds[0], ds[1]);
-          sa[kk][hi ? 3 : 1] = pack_bf16x2(ds[2], ds[3]);
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            float ds[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int key = kbase + 8 * nt + 2 * q + (u & 1);
+              const int rr = u >> 1;
+              const float pr = key <= last ? fast_exp2(fmaf(sacc[nt][u], p.sl2, -lse2[rr])) : 0.f;
+              ds[u] = pr * (pacc[nt][u] - dsum[rr]);
+            }
+            const int kk = nt >> 1, hi = nt & 1;
+            sa[kk][hi ? 2 : 0] = pack_bf16x2(ds[0], ds[1]);
+            sa[kk][hi ? 3 : 1] = pack_bf16x2(ds[2], ds[3]);
+          }
         }
         // dQ += dS K (K^T fragments by ldmatrix.trans on the K slot)
 #pragma unroll
@@ -387,21 +407,42 @@ __global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) 
     }
     // P^T and dS^T (rows: keys 16w + r, + 8; columns: heads 8 nt + 2q + {0, 1})
     uint32_t pa[4], sa[4];
+    if (key0 + 16 * warp + 15 <= last) {  // all of this warp's keys visible: packed fp32 pairs
+      const unsigned long long sl2x2 = pack_f32x2(p.sl2, p.sl2);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float pv[4], dsv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int key = key0 + 16 * warp + r + 8 * (u >> 1);
-        const int h = 8 * nt + 2 * q + (u & 1);
-        const float pr = key <= last ? fast_exp2(fmaf(sacc[nt][u], p.sl2, -lse2_s[bf][h])) : 0.f;
-        pv[u] = pr;
-        dsv[u] = pr * (pacc[nt][u] - dsum_s[bf][h]);
+      for (int nt = 0; nt < 2; ++nt) {
+        const int h0 = 8 * nt + 2 * q;
+        const unsigned long long nl = pack_f32x2(-lse2_s[bf][h0], -lse2_s[bf][h0 + 1]);
+        const unsigned long long nd = pack_f32x2(-dsum_s[bf][h0], -dsum_s[bf][h0 + 1]);
+        float x0, x1, x2, x3;
+        unpack_f32x2(fma_f32x2(pack_f32x2(sacc[nt][0], sacc[nt][1]), sl2x2, nl), x0, x1);
+        unpack_f32x2(fma_f32x2(pack_f32x2(sacc[nt][2], sacc[nt][3]), sl2x2, nl), x2, x3);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+        float d0, d1, d2, d3;
+        unpack_f32x2(mul_f32x2(pack_f32x2(p0, p1), add_f32x2(pack_f32x2(pacc[nt][0], pacc[nt][1]), nd)), d0, d1);
+        unpack_f32x2(mul_f32x2(pack_f32x2(p2, p3), add_f32x2(pack_f32x2(pacc[nt][2], pacc[nt][3]), nd)), d2, d3);
+        pa[nt ? 2 : 0] = pack_bf16x2(p0, p1);
+        pa[nt ? 3 : 1] = pack_bf16x2(p2, p3);
+        sa[nt ? 2 : 0] = pack_bf16x2(d0, d1);
+        sa[nt ? 3 : 1] = pack_bf16x2(d2, d3);
       }
-      pa[nt ? 2 : 0] = pack_bf16x2(pv[0], pv[1]);
-      pa[nt ? 3 : 1] = pack_bf16x2(pv[2], pv[3]);
-      sa[nt ? 2 : 0] = pack_bf16x2(dsv[0], dsv[1]);
-      sa[nt ? 3 : 1] = pack_bf16x2(dsv[2], dsv[3]);
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int key = key0 + 16 * warp + r + 8 * (u >> 1);
+          const int h = 8 * nt + 2 * q + (u & 1);
+          const float pr = key <= last ? fast_exp2(fmaf(sacc[nt][u], p.sl2, -lse2_s[bf][h])) : 0.f;
+          pv[u] = pr;
+          dsv[u] = pr * (pacc[nt][u] - dsum_s[bf][h]);
+        }
+        pa[nt ? 2 : 0] = pack_bf16x2(pv[0], pv[1]);
+        pa[nt ? 3 : 1] = pack_bf16x2(pv[2], pv[3]);
+        sa[nt ? 2 : 0] = pack_bf16x2(dsv[0], dsv[1]);
+        sa[nt ? 3 : 1] = pack_bf16x2(dsv[2], dsv[3]);
+      }
     }
     // dV_w += P^T dO and dK_w += dS^T Q (B fragments by ldmatrix.trans: k = head, n = d)
 #pragma unroll
