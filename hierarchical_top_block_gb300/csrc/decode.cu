@@ -50,6 +50,9 @@ __device__ __forceinline__ int level_size(long long n, int l) {
 // heads runs in one wave
 template <int D>
 __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint32_t* err) {
+  // L2 priorities: candidate K blocks may be read again by the attention (keep them), the
+  // attention's K and V reads are their last use (let them go first)
+  const uint64_t pol_keep = l2_evict_last_policy(), pol_last_use = l2_evict_first_policy();
   constexpr int NCH = D / 32;
   constexpr int NDT = D / 8;
   __shared__ int wlst[WARPS][32];
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       const uint16_t* krow = Kb + (size_t)(vis ? key : key0) * D;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        const uint4 kv = vis ? ldg16(krow + 32 * j + 8 * q) : make_uint4(0, 0, 0, 0);
+        const uint4 kv = vis ? ldg16_hint(krow + 32 * j + 8 * q, pol_keep) : make_uint4(0, 0, 0, 0);
         mma_bf16_16816(acc[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
         mma_bf16_16816(acc[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
       }
@@ -445,8 +448,8 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
         const int k = i / (D / 8), c = i % (D / 8);
         const long long key = key0 + k;
         const bool in = key <= T;
-        cp_async16(vmine + (c >> 3) * HSPAN + k * 128 + (((c & 7) ^ (k & 7)) << 4),
-                   Vb + (size_t)(in ? key : key0) * D + 8 * c, in ? 16 : 0);
+        cp_async16_hint(vmine + (c >> 3) * HSPAN + k * 128 + (((c & 7) ^ (k & 7)) << 4),
+                        Vb + (size_t)(in ? key : key0) * D + 8 * c, in ? 16 : 0, pol_last_use);
       }
       cp_async_commit();
       float s[4][4];
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
         const uint16_t* krow = Kb + (size_t)(key <= T ? key : key0) * D;
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          const uint4 kv = ldg16(krow + 32 * j + 8 * q);
+          const uint4 kv = ldg16_hint(krow + 32 * j + 8 * q, pol_last_use);
           mma_bf16_16816(s[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
           mma_bf16_16816(s[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
         }
