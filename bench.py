@@ -38,8 +38,8 @@ KERNELS_PER_STEP = 11  # pyramid 2, stage 1 (with the clustering histogram), clu
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
 # as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "040ba5c75085c0959672db135df9813763a08899ce7902c0749c076d9a92f887",
-                "workload": "prefill_256k", "bytes": 13929120768 + 1089666816}
+ATTN_TRAFFIC = {"sources_sha256": "d03e05ed471c5bfda7af2aab19eba736e33d70716d0f9dde0a54ac6e160b3a6c",
+                "workload": "prefill_256k", "bytes": 13713879552 + 1089932032}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
