@@ -38,7 +38,7 @@ KERNELS_PER_STEP = 11  # pyramid 2, stage 1 (with the clustering histogram), clu
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
 # as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "d03e05ed471c5bfda7af2aab19eba736e33d70716d0f9dde0a54ac6e160b3a6c",
+ATTN_TRAFFIC = {"sources_sha256": "88038b29dfd8dfe96aa900359165d4b75c6f7ef683facc058995e0ab9a07ce43",
                 "workload": "prefill_256k", "bytes": 13713879552 + 1089932032}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]

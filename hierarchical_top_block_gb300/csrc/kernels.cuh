@@ -48,7 +48,8 @@ cudaError_t launch_leaf_lse(const uint16_t* Q, const uint16_t* K, const ClusterB
                             const Problem& p, const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s);
 
 // Final top-K with the own block kept; idx rows ascending, -1 padded.
-cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx, const Problem& p,
+// Also writes -inf into the leaf-score slots of absent survivors.
+cudaError_t launch_topk(const int32_t* S2, float* leaf_score, int32_t* idx, const Problem& p,
                         const Geometry& geo, int num_sms, cudaStream_t s);
 
 // Block-sparse attention over idx.

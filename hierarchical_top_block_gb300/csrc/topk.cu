@@ -15,7 +15,7 @@ constexpr int THREADS = 256;
 
 
 __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict__ S2,
-                                                       const float* __restrict__ score, int32_t* __restrict__ idx,
+                                                       float* __restrict__ score, int32_t* __restrict__ idx,
                                                        int BH, int N, int t_lo, int nq, int Ksel, int M1, int causal) {
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
     fetch(bh, t, node_n, sc_n);
     const long long item = (long long)cbh * N + ct;
     const int own = causal ? ct / 64 : -1;
+    // slots of absent level-2 survivors hold no leaf: their score reads -inf
+    if (lane < twoK && node < 0) score[item * twoK + lane] = NEG_INF;
     int leaf = -1;
     float sc = NEG_INF;
     if (node >= 0) {
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
 
 }  // namespace
 
-cudaError_t launch_topk(const int32_t* S2, const float* leaf_score, int32_t* idx, const Problem& p,
+cudaError_t launch_topk(const int32_t* S2, float* leaf_score, int32_t* idx, const Problem& p,
                         const Geometry& geo, int num_sms, cudaStream_t s) {
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * nq;

@@ -79,6 +79,10 @@ def check_selection(o, Qb, Kb, Pb, K_sel, rows, gpu_idx, gpu_s2=None, gpu_score=
         with np.errstate(invalid="ignore"):
             diff = np.abs(np.where(valid, gpu_score - ref["cand_score"], 0.0))
         assert diff.max() <= SCORE_TOL, f"leaf score differs by {diff.max()}"
+        # slots without a candidate leaf (absent survivor, leaf past the end, or not yet
+        # visible) read -inf
+        empty = (ref["cand"] < 0) & same_s2[:, None]
+        assert np.all(np.isneginf(gpu_score[empty])), "a slot without a candidate leaf does not read -inf"
     return dict(rows=len(rows), ambiguous=int(amb.size), clear=int(clear.sum()))
 
 
