@@ -285,7 +285,10 @@ def run_pisa(args):
     if rank == 0:
         out["e2e"] = None if args.no_e2e else run_e2e(args, w, dev)
         if not args.no_secondary:
+            # K = 8 is the setting of the paper's selection-speed comparison (its Fig. 3)
             out["secondary"] = {"prefill_32k": secondary_prefill(W.WORKLOADS["prefill_32k"], dev),
+                                "prefill_32k_k8": secondary_prefill(W.WORKLOADS["prefill_32k"], dev, K_sel=8),
+                                "prefill_256k_k8": secondary_prefill(W.WORKLOADS["prefill_256k"], dev, K_sel=8),
                                 "decode_128k": secondary_decode(W.WORKLOADS["decode_128k"], dev),
                                 "selection_quality_32k": selection_quality_section(W.WORKLOADS["prefill_32k"], dev)}
         out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
@@ -386,36 +389,49 @@ def run_e2e(args, w, dev):
             "ms_per_step": dt * 1e3, "steps": args.e2e_steps, "api": "pisa_prefill_host (pinned host buffers)"}
 
 
-def secondary_prefill(w, dev, steps=5):
+def secondary_prefill(w, dev, steps=5, K_sel=None):
+    """Pyramid + selection + attention, and pyramid + selection alone, on a workload's inputs
+    (K_sel overrides the workload's K)."""
     import torch
 
     import hierarchical_top_block_gb300 as pisa
     import workloads as W
 
+    Ks = w.K if K_sel is None else K_sel
     Q, K, V = W.prefill_inputs(w, dev)
     P = pisa.pisa_build_pyramid(K)
     shape = pisa.make_shape(w.B, w.N, w.H_q, w.H_kv, w.d)
-    ws = torch.empty(pisa.pisa_select_workspace_bytes(shape, pisa.make_params(w.K)), dtype=torch.uint8, device=dev)
-    idx = torch.empty(w.B, w.H_kv, w.N, w.K, dtype=torch.int32, device=dev)
+    ws = torch.empty(pisa.pisa_select_workspace_bytes(shape, pisa.make_params(Ks)), dtype=torch.uint8, device=dev)
+    idx = torch.empty(w.B, w.H_kv, w.N, Ks, dtype=torch.int32, device=dev)
     O = torch.empty_like(Q)
     L = torch.empty(w.B, w.H_q, w.N, dtype=torch.float32, device=dev)
 
-    def step():
+    def select():
         pisa.pisa_build_pyramid(K, P=P)
-        pisa.pisa_select_prefill(Q, K, P, w.K, ws=ws, idx=idx)
+        pisa.pisa_select_prefill(Q, K, P, Ks, ws=ws, idx=idx)
+
+    def step():
+        select()
         pisa.pisa_sparse_attn_prefill(Q, K, V, idx, O=O, LSE=L)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms_per_step": ms, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv}
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms, sel_ms = timed(step), timed(select)
+    if pisa.pisa_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the secondary prefill")
+    return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms_per_step": ms,
+            "selection_tokens_per_s": w.B * w.N / (sel_ms * 1e-3), "select_ms": sel_ms,
+            "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "K": Ks}
 
 
 def selection_quality_section(w, dev, samples=96, seed=11):
