@@ -34,6 +34,17 @@ METRIC = "prefill tokens/s (select + sparse attn)"
 UNIT = "tokens/s"
 KERNELS_PER_STEP = 11  # pyramid 2, stage 1 (with the clustering histogram), clustering 5, leaf LSE, top-K, attention
 
+# The paper's own figures for this path (summary page "Block Sparse Attention with Log-Linear
+# Complexity", section "Experimental results", item 5, Fig. 3): context only.  They are ratios
+# against the authors' BSA selection on hardware the page does not name; no absolute latency,
+# throughput or decode time is given there.
+PAGES_REFERENCE = {
+    "selection_speedup_vs_bsa": {"64K": 2.86, "128K": 5.31, "256K": 9.95},
+    "setting": "block selection at C=64, K=8 (this bench times K=8 under secondary.prefill_*_k8)",
+    "hardware": "not stated on the page",
+    "note": "BSA is faster than PISA at 4K-16K on the page's figure",
+}
+
 # DRAM traffic of the attention kernel per launch on the 256K prefill (dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
 # by a hash of the kernel's sources: when the sources change the figure is stale and is reported
@@ -278,6 +289,7 @@ def run_pisa(args):
                                    "achieved_tbs": work["gather_bytes"] / (att_ms * 1e-3) / 1e12}},
         "clocks": clk,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "pages_reference": PAGES_REFERENCE,
     }
     if rank == 0 and not args.no_secondary:
         out["scoring_variants"] = scoring_variants(Q, K, P, w, ws, idx)
