@@ -72,7 +72,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="pisa", choices=["pisa", "reference"])
     ap.add_argument("--workload", default="prefill_256k")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true", help="skip the 32K prefill and decode measurements")
     ap.add_argument("--cpu-sample-rows", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
