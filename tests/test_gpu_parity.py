@@ -106,22 +106,26 @@ def test_argument_errors_are_synchronous():
     assert pisa.pisa_get_last_device_error() == 0
 
 
-def test_prefill_32k_sampled(oracle_impl):
+@pytest.mark.parametrize("K_sel", [16, 8])
+def test_prefill_32k_sampled(oracle_impl, K_sel):
+    """The long-prefill workload at its own K and at K = 8 (both timed by the benchmark)."""
     w = W.WORKLOADS["prefill_32k"]
     Q, K, V = _inputs(w)
-    rep = H.full_prefill_check(oracle_impl, Q, K, V, w.K, sample=192, seed=3)
+    rep = H.full_prefill_check(oracle_impl, Q, K, V, K_sel, sample=192, seed=3 + K_sel)
     assert rep["rows"] == 192
 
 
-def test_prefill_256k_sampled(oracle_impl):
-    """Full selection-scale size, the launch configuration the benchmark times; the oracle
-    computes sampled rows one by one.  Q is generated on the GPU and, for the sampled rows
-    only, on the CPU; K and V are generated on both and compared bit for bit."""
+@pytest.mark.parametrize("K_sel", [16, 8])
+def test_prefill_256k_sampled(oracle_impl, K_sel):
+    """Full selection-scale size, the launch configuration the benchmark times (at the
+    workload's K and at K = 8); the oracle computes sampled rows one by one.  Q is generated on
+    the GPU and, for the sampled rows only, on the CPU; K and V are generated on both and
+    compared bit for bit."""
     w = W.WORKLOADS["prefill_256k"]
     Q = W.make_q(w, "cuda")
     K = W.make_kv(w, "K", "cuda")
     V = W.make_kv(w, "V", "cuda")
-    res = H.run_gpu_prefill(Q, K, V, w.K)
+    res = H.run_gpu_prefill(Q, K, V, K_sel)
     Kc, Vc = W.make_kv(w, "K", "cpu"), W.make_kv(w, "V", "cpu")
     assert torch.equal(K.cpu().view(torch.int16), Kc.view(torch.int16))
     assert torch.equal(V.cpu().view(torch.int16), Vc.view(torch.int16))
@@ -135,7 +139,7 @@ def test_prefill_256k_sampled(oracle_impl):
     Qb[0, ts] = W.bits(qrows)
     assert torch.equal(Q[0, torch.as_tensor(ts, device="cuda")].cpu().view(torch.int16), qrows.view(torch.int16))
     rows = np.stack([np.zeros_like(ts), np.zeros_like(ts), ts], 1)
-    H.check_selection(oracle_impl, Qb, Kb, Pb, w.K, rows, res["idx"][0, 0, ts], res["s2"][0, 0, ts],
+    H.check_selection(oracle_impl, Qb, Kb, Pb, K_sel, rows, res["idx"][0, 0, ts], res["s2"][0, 0, ts],
                       res["score"][0, 0, ts])
     bt = np.unique(np.stack([np.zeros_like(ts), ts], 1), axis=0)
     O = res["O"][0, torch.as_tensor(bt[:, 1], device="cuda")].float().cpu().numpy()
