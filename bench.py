@@ -391,14 +391,18 @@ def run_e2e(args, w, dev):
     dws = torch.empty(pisa.pisa_prefill_host_workspace_bytes(shape, params), dtype=torch.uint8, device=dev)
     pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, dev_ws=dws, O_host=Oh, LSE_host=Lh, device=dev.index)
     torch.cuda.synchronize()
+    calls = []
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
+        tc = time.perf_counter()
         pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, dev_ws=dws, O_host=Oh, LSE_host=Lh, device=dev.index)
+        calls.append(round((time.perf_counter() - tc) * 1e3, 3))  # each call returns when all its work is done
     dt = (time.perf_counter() - t0) / args.e2e_steps
     h2d = Qh.numel() * 2 + Kh.numel() * 2 + Vh.numel() * 2
     d2h = Oh.numel() * 2 + Lh.numel() * 4
     return {"value": w.B * w.N / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": dt * 1e3, "steps": args.e2e_steps, "api": "pisa_prefill_host (pinned host buffers)"}
+            "ms_per_step": dt * 1e3, "steps": args.e2e_steps, "calls_ms": calls,
+            "api": "pisa_prefill_host (pinned host buffers)"}
 
 
 def secondary_prefill(w, dev, steps=5, K_sel=None):

@@ -29,24 +29,35 @@ struct HostPipe {
   cudaEvent_t ev[PIPE_EVENTS] = {};
 };
 
-// Query chunks of the host-buffer prefill: a short first chunk (the copy-in that precedes
-// any compute) and a short last chunk (the copy-out that follows it), growing threefold in
-// between up to a quarter of the sequence.  Sizes are multiples of 64 except the remainder.
+// Query chunks of the host-buffer prefill.  The chunks double from N/64 (at least 4096
+// queries) up to a quarter of the sequence and halve again at the end, with equal chunks of at
+// most N/4 between: a short first chunk shortens the copy-in that precedes any compute, and
+// the halving tail keeps each chunk's copy-out shorter than the compute of the chunks after
+// it, so only the last, small copy-out trails the compute.  Bounds are multiples of 64 except
+// where the remainder of a ragged N falls; at most 12 chunks.
 int plan_chunks(long long N, long long* bounds) {
-  long long lo = (N / 32 + 63) / 64 * 64;
+  long long lo = N / 64 / 64 * 64;
   if (lo < 4096) lo = 4096;
   long long cap = N / 4 / 64 * 64;
   if (cap < lo) cap = lo;
-  int n = 0;
-  long long t = 0, c = lo;
-  bounds[0] = 0;
-  while (t + c + lo < N && n < PIPE_MAX_CHUNKS - 2) {
-    t += c;
-    bounds[++n] = t;
-    c = 3 * c < cap ? 3 * c : cap;
+  long long ramp[8];
+  int nr = 0;
+  long long used = 0;
+  for (long long c = lo; c < cap && used + 2 * c <= N && nr < 8; c *= 2) {
+    ramp[nr++] = c;
+    used += 2 * c;
   }
-  if (N - t > lo) bounds[++n] = N - lo;
-  bounds[++n] = N;
+  const long long mid = N - used;
+  long long nm = mid > 0 ? (mid + cap - 1) / cap : 0;
+  if (nm > PIPE_MAX_CHUNKS - 2 * nr) nm = PIPE_MAX_CHUNKS - 2 * nr;
+  int n = 0;
+  long long t = 0;
+  bounds[0] = 0;
+  for (int i = 0; i < nr; ++i) bounds[++n] = (t += ramp[i]);
+  for (long long i = 1; i < nm; ++i) bounds[++n] = t + mid * i / nm / 64 * 64;
+  t += mid;
+  if (nm > 0) bounds[++n] = t;
+  for (int i = nr - 1; i >= 0; --i) bounds[++n] = (t += ramp[i]);
   return n;
 }
 
