@@ -60,6 +60,8 @@ def lib() -> ct.CDLL:
         L.pisa_sparse_attn_backward.argtypes = [_P] * 10 + [_P, ct.c_size_t, pisa_shape, pisa_params, _P]
         L.pisa_prefill_host_workspace_bytes.restype = ct.c_size_t
         L.pisa_prefill_host_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_prefill_host_chunks.restype = ct.c_int
+        L.pisa_prefill_host_chunks.argtypes = [ct.c_longlong, ct.POINTER(ct.c_longlong), ct.c_int]
         L.pisa_build_pyramid.restype = ct.c_int
         L.pisa_build_pyramid.argtypes = [_P, _P, pisa_shape, pisa_params, _P]
         L.pisa_select_prefill.restype = ct.c_int
@@ -129,6 +131,15 @@ def pisa_select_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
 
 def pisa_prefill_host_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
     return int(lib().pisa_prefill_host_workspace_bytes(shape, params))
+
+
+def pisa_prefill_host_chunks(N: int) -> list[int]:
+    """Chunk bounds [0, ..., N] of the host-buffer prefill for N positions."""
+    buf = (ct.c_longlong * 17)()
+    n = lib().pisa_prefill_host_chunks(N, buf, 17)
+    if n < 0:
+        raise ValueError(f"pisa_prefill_host_chunks({N}) failed")
+    return [int(buf[i]) for i in range(n + 1)]
 
 
 def pisa_status_string(status: int) -> str:

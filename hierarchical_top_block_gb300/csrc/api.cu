@@ -34,7 +34,7 @@ struct HostPipe {
 // most N/4 between: a short first chunk shortens the copy-in that precedes any compute, and
 // the halving tail keeps each chunk's copy-out shorter than the compute of the chunks after
 // it, so only the last, small copy-out trails the compute.  Bounds are multiples of 64 except
-// where the remainder of a ragged N falls; at most 12 chunks.
+// where the remainder of a ragged N falls; at most 11 chunks.
 int plan_chunks(long long N, long long* bounds) {
   long long lo = N / 64 / 64 * 64;
   if (lo < 4096) lo = 4096;
@@ -43,7 +43,7 @@ int plan_chunks(long long N, long long* bounds) {
   long long ramp[8];
   int nr = 0;
   long long used = 0;
-  for (long long c = lo; c < cap && used + 2 * c <= N && nr < 8; c *= 2) {
+  for (long long c = lo; c < cap && used + 2 * c <= N && nr < 6; c *= 2) {
     ramp[nr++] = c;
     used += 2 * c;
   }
@@ -365,6 +365,15 @@ pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, cons
   if ((rc = device_state(&st)) != PISA_OK) return rc;
   return cuda_status(launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+int pisa_prefill_host_chunks(long long N, long long* bounds, int max_bounds) {
+  if (!bounds || N < 0) return -1;
+  long long b[PIPE_MAX_CHUNKS + 1];
+  const int n = plan_chunks(N, b);
+  if (max_bounds < n + 1) return -1;
+  for (int i = 0; i <= n; ++i) bounds[i] = b[i];
+  return n;
 }
 
 size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params) {

@@ -167,7 +167,7 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
 
 /* Copies Q, K, V host -> device, builds the pyramid, selects, attends and copies O (and
  * LSE, idx when non-NULL) device -> host; returns when all of it has finished.  The work runs
- * in query chunks (at most 12: doubling from N/64 positions, at least 4096, up to N/4 and
+ * in query chunks (at most 11: doubling from N/64 positions, at least 4096, up to N/4 and
  * halving again towards the end, equal chunks of at most N/4 between) so that the host -> device copy of the next
  * chunk's Q, the device -> host copy of the previous chunk's O and the attention of one chunk
  * overlap the selection of the next: selection runs on `stream`, attention and the copies on
@@ -178,6 +178,11 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
  * and concurrent copies.  dev_ws is device scratch of at least
  * pisa_prefill_host_workspace_bytes().  N_cap must equal N. */
 PISA_API size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params);
+/* The query chunks pisa_prefill_host uses for a sequence of N positions (host only, no device
+ * work): writes the chunk bounds 0 = bounds[0] < bounds[1] < ... < bounds[n] = N into
+ * bounds[0..n] and returns n (0 for N = 0, at most 16).  Returns -1, writing nothing, when
+ * bounds is NULL, N < 0 or max_bounds < n + 1. */
+PISA_API int pisa_prefill_host_chunks(long long N, long long* bounds, int max_bounds);
 PISA_API pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, const uint16_t* V_host,
                               uint16_t* O_host, float* LSE_host, int32_t* idx_host, void* dev_ws, size_t ws_bytes,
                               pisa_shape shape, pisa_params params, pisa_stream stream);
