@@ -97,9 +97,29 @@ def _stream(t: torch.Tensor):
     return ct.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
-def _bf16(t, name):
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+def _bf16(t, name, dim=None):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or (dim is not None and t.dim() != dim):
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor" + (f" with {dim} dimensions" if dim else ""))
+
+
+def _expect(t, name, shape, dtype, device):
+    """The library reads and writes through raw pointers with the sizes the shape implies, so
+    every tensor must have exactly that shape, dtype and device, and be contiguous (None is
+    passed through as NULL where the C ABI allows it)."""
+    if t is None:
+        return
+    if t.dtype != dtype or t.device != torch.device(device) or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}; got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}{'' if t.is_contiguous() else ', not contiguous'}")
+
+
+def _workspace(ws, need, device):
+    """A caller's workspace if it is large enough, else a new one."""
+    if ws is not None and (ws.dtype != torch.uint8 or ws.device != torch.device(device) or not ws.is_contiguous()):
+        raise ValueError(f"workspace must be a contiguous uint8 tensor on {device}")
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return ws
 
 
 # block scores: the LSE (PISA) or its first- / second-order truncations (PISA-1, PISA-2)
@@ -158,36 +178,44 @@ def pisa_get_last_device_error(device=None) -> int:
 # ---- step 1 -----------------------------------------------------------------------------
 def pisa_build_pyramid(K: torch.Tensor, N: int | None = None, P: torch.Tensor | None = None) -> torch.Tensor:
     """K [B, H_kv, N_cap, d] bf16 -> P [B, H_kv, nodes(N_cap), d]; levels built from the first N rows."""
-    _bf16(K, "K")
+    _bf16(K, "K", 4)
     B, H_kv, N_cap, d = K.shape
     N = N_cap if N is None else N
     nodes = pisa_pyramid_nodes(N_cap)
     if P is None:
         P = torch.empty(B, H_kv, nodes, d, dtype=torch.bfloat16, device=K.device)
-    _bf16(P, "P")
+    _expect(P, "P", (B, H_kv, nodes, d), torch.bfloat16, K.device)
     shape = make_shape(B, N, H_kv, H_kv, d, N_cap)
     _check(lib().pisa_build_pyramid(_ptr(K), _ptr(P), shape, make_params(1), _stream(K)), "pisa_build_pyramid")
     return P
 
 
 # ---- step 2 -----------------------------------------------------------------------------
+def _select_inputs(Q, K, P):
+    """Q [B, N, H_q, d], K [B, H_kv, N, d] and P [B, H_kv, nodes(N), d], all bf16 on one device."""
+    _bf16(Q, "Q", 4)
+    _bf16(K, "K", 4)
+    B, N, H_q, d = Q.shape
+    H_kv = K.shape[1]
+    _expect(K, "K", (B, H_kv, N, d), torch.bfloat16, Q.device)
+    _expect(P, "P", (B, H_kv, pisa_pyramid_nodes(N), d), torch.bfloat16, Q.device)
+    return B, N, H_q, d, H_kv
+
+
 def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float = 0.0, want_scores: bool = False,
                         want_s2: bool = False, ws: torch.Tensor | None = None, idx: torch.Tensor | None = None,
                         scoring: int | str = 0):
     """Returns idx [B, H_kv, N, K_sel] int32 (and leaf_score, s2 if asked)."""
-    for t, n in ((Q, "Q"), (K, "K"), (P, "P")):
-        _bf16(t, n)
-    B, N, H_q, d = Q.shape
-    H_kv = K.shape[1]
+    B, N, H_q, d, H_kv = _select_inputs(Q, K, P)
     shape = make_shape(B, N, H_q, H_kv, d, N)
     params = make_params(K_sel, causal, scale, scoring=scoring)
     need = pisa_select_workspace_bytes(shape, params)
     if need == 0 and B * N > 0:
         raise PisaError(2, "pisa_select_prefill: unsupported shape or parameters")
-    if ws is None or ws.numel() < need:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    ws = _workspace(ws, need, Q.device)
     if idx is None:
         idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
+    _expect(idx, "idx", (B, H_kv, N, K_sel), torch.int32, Q.device)
     score = torch.empty(B, H_kv, N, 2 * K_sel, dtype=torch.float32, device=Q.device) if want_scores else None
     s2 = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device) if want_s2 else None
     _check(lib().pisa_select_prefill(_ptr(Q), _ptr(K), _ptr(P), _ptr(idx), _ptr(score), _ptr(s2), _ptr(ws),
@@ -205,12 +233,12 @@ def pisa_select_prefill_noalloc(Q, K, P, K_sel: int, causal: bool = True, scale:
     """pisa_select_prefill without a caller-supplied workspace: the library's fixed 32 MiB
     device scratch is used instead (for callers that cannot allocate device memory).
     Output tensors may be passed in so that the call itself allocates nothing."""
-    for t, n in ((Q, "Q"), (K, "K"), (P, "P")):
-        _bf16(t, n)
-    B, N, H_q, d = Q.shape
-    H_kv = K.shape[1]
+    B, N, H_q, d, H_kv = _select_inputs(Q, K, P)
     if idx is None:
         idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
+    _expect(idx, "idx", (B, H_kv, N, K_sel), torch.int32, Q.device)
+    _expect(leaf_score, "leaf_score", (B, H_kv, N, 2 * K_sel), torch.float32, Q.device)
+    _expect(s2, "s2", (B, H_kv, N, K_sel), torch.int32, Q.device)
     _check(lib().pisa_select_prefill_noalloc(_ptr(Q), _ptr(K), _ptr(P), _ptr(idx), _ptr(leaf_score), _ptr(s2),
                                              make_shape(B, N, H_q, H_kv, d, N),
                                              make_params(K_sel, causal, scale, scoring=scoring),
@@ -219,20 +247,32 @@ def pisa_select_prefill_noalloc(Q, K, P, K_sel: int, causal: bool = True, scale:
 
 
 # ---- step 4 -----------------------------------------------------------------------------
+def _attn_inputs(Q, K, V, idx):
+    """Q [B, N, H_q, d], K and V [B, H_kv, N_cap, d] bf16, idx [B, H_kv, N, K] int32, one device."""
+    _bf16(Q, "Q", 4)
+    _bf16(K, "K", 4)
+    B, N, H_q, d = Q.shape
+    H_kv, N_cap = K.shape[1], K.shape[2]
+    _expect(K, "K", (B, H_kv, N_cap, d), torch.bfloat16, Q.device)
+    _expect(V, "V", (B, H_kv, N_cap, d), torch.bfloat16, Q.device)
+    if idx.dim() != 4:
+        raise ValueError("idx must be [B, H_kv, N, K]")
+    _expect(idx, "idx", (B, H_kv, N, idx.shape[-1]), torch.int32, Q.device)
+    return B, N, H_q, d, H_kv, N_cap
+
+
 def pisa_sparse_attn_prefill(Q, K, V, idx, causal: bool = True, scale: float = 0.0, O=None, LSE=None,
                              want_lse: bool = True):
     """Returns O [B, N, H_q, d] bf16 and LSE [B, H_q, N] fp32 (None if not wanted)."""
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
-        _bf16(t, n)
-    if idx.dtype != torch.int32 or not idx.is_contiguous():
-        raise ValueError("idx must be contiguous int32")
-    B, N, H_q, d = Q.shape
-    H_kv = K.shape[1]
+    B, N, H_q, d, H_kv, N_cap = _attn_inputs(Q, K, V, idx)
     if O is None:
         O = torch.empty_like(Q)
     if want_lse and LSE is None:
         LSE = torch.empty(B, H_q, N, dtype=torch.float32, device=Q.device)
-    shape = make_shape(B, N, H_q, H_kv, d, K.shape[2])
+    _expect(O, "O", (B, N, H_q, d), torch.bfloat16, Q.device)
+    if want_lse:
+        _expect(LSE, "LSE", (B, H_q, N), torch.float32, Q.device)
+    shape = make_shape(B, N, H_q, H_kv, d, N_cap)
     params = make_params(idx.shape[-1], causal, scale)
     _check(lib().pisa_sparse_attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(O), _ptr(LSE if want_lse else None),
                                           shape, params, _stream(Q)), "pisa_sparse_attn_prefill")
@@ -246,24 +286,24 @@ def pisa_attn_backward_workspace_bytes(shape: pisa_shape, params: pisa_params) -
 def pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal: bool = True, scale: float = 0.0, ws=None,
                               dQ=None, dK=None, dV=None):
     """Gradients of pisa_sparse_attn_prefill: returns dQ [B, N, H_q, d], dK, dV [B, H_kv, N_cap, d] (fp32)."""
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (dO, "dO")):
-        _bf16(t, n)
-    if idx.dtype != torch.int32 or not idx.is_contiguous():
-        raise ValueError("idx must be contiguous int32")
-    if LSE.dtype != torch.float32 or not LSE.is_contiguous():
-        raise ValueError("LSE must be contiguous fp32")
-    B, N, H_q, d = Q.shape
-    H_kv, N_cap = K.shape[1], K.shape[2]
+    B, N, H_q, d, H_kv, N_cap = _attn_inputs(Q, K, V, idx)
+    for t, n in ((O, "O"), (dO, "dO")):
+        _expect(t, n, (B, N, H_q, d), torch.bfloat16, Q.device)
+    if LSE is None:
+        raise ValueError("LSE must be given")
+    _expect(LSE, "LSE", (B, H_q, N), torch.float32, Q.device)
     shape = make_shape(B, N, H_q, H_kv, d, N_cap)
     params = make_params(idx.shape[-1], causal, scale)
     need = pisa_attn_backward_workspace_bytes(shape, params)
     if need == 0 and B * N > 0:
         raise PisaError(2, "pisa_sparse_attn_backward: unsupported shape or parameters")
-    if ws is None or ws.numel() < need:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    ws = _workspace(ws, need, Q.device)
     dQ = torch.empty(B, N, H_q, d, dtype=torch.float32, device=Q.device) if dQ is None else dQ
     dK = torch.empty(B, H_kv, N_cap, d, dtype=torch.float32, device=Q.device) if dK is None else dK
     dV = torch.empty(B, H_kv, N_cap, d, dtype=torch.float32, device=Q.device) if dV is None else dV
+    _expect(dQ, "dQ", (B, N, H_q, d), torch.float32, Q.device)
+    _expect(dK, "dK", (B, H_kv, N_cap, d), torch.float32, Q.device)
+    _expect(dV, "dV", (B, H_kv, N_cap, d), torch.float32, Q.device)
     _check(lib().pisa_sparse_attn_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(O), _ptr(LSE), _ptr(dO),
                                            _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), shape, params,
                                            _stream(Q)), "pisa_sparse_attn_backward")
@@ -273,16 +313,25 @@ def pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal: bool = True, sca
 def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, scale: float = 0.0, dev_ws=None,
                       O_host=None, LSE_host=None, idx_host=None, device=None, scoring: int | str = 0):
     """Whole prefill from host (ideally pinned) tensors; copies happen inside the call."""
+    if Q_host.dim() != 4 or K_host.dim() != 4:
+        raise ValueError("Q_host must be [B, N, H_q, d] and K_host [B, H_kv, N, d]")
     B, N, H_q, d = Q_host.shape
     H_kv = K_host.shape[1]
-    shape = make_shape(B, N, H_q, H_kv, d, N)
-    params = make_params(K_sel, causal, scale, scoring=scoring)
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    need = pisa_prefill_host_workspace_bytes(shape, params)
-    if dev_ws is None or dev_ws.numel() < need:
-        dev_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    cpu = torch.device("cpu")
+    _expect(Q_host, "Q_host", (B, N, H_q, d), torch.bfloat16, cpu)
+    _expect(K_host, "K_host", (B, H_kv, N, d), torch.bfloat16, cpu)
+    _expect(V_host, "V_host", (B, H_kv, N, d), torch.bfloat16, cpu)
     if O_host is None:
         O_host = torch.empty_like(Q_host)
+    _expect(O_host, "O_host", (B, N, H_q, d), torch.bfloat16, cpu)
+    _expect(LSE_host, "LSE_host", (B, H_q, N), torch.float32, cpu)
+    _expect(idx_host, "idx_host", (B, H_kv, N, K_sel), torch.int32, cpu)
+    shape = make_shape(B, N, H_q, H_kv, d, N)
+    params = make_params(K_sel, causal, scale, scoring=scoring)
+    # the host buffers are all checked before anything touches the device
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    need = pisa_prefill_host_workspace_bytes(shape, params)
+    dev_ws = _workspace(dev_ws, need, dev)
     stream = ct.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     _check(lib().pisa_prefill_host(_ptr(Q_host), _ptr(K_host), _ptr(V_host), _ptr(O_host), _ptr(LSE_host),
                                    _ptr(idx_host), _ptr(dev_ws), dev_ws.numel(), shape, params, stream),
@@ -294,15 +343,24 @@ def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, s
 def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.0, o=None, lse=None, idx_out=None,
                      scoring: int | str = 0):
     """One decode step for every sequence; caches and seq_len are updated in place."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (Kc, "Kc"), (Vc, "Vc"), (Pc, "Pc")):
-        _bf16(t, n)
-    if seq_len.dtype != torch.int32 or not seq_len.is_cuda:
-        raise ValueError("seq_len must be an int32 CUDA tensor")
+    _bf16(q, "q", 3)
+    _bf16(k, "k", 3)
+    _bf16(Kc, "Kc", 4)
     B, H_q, d = q.shape
     H_kv = k.shape[1]
     N_cap = Kc.shape[2]
+    dev = q.device
+    for t, n in ((k, "k"), (v, "v")):
+        _expect(t, n, (B, H_kv, d), torch.bfloat16, dev)
+    for t, n in ((Kc, "Kc"), (Vc, "Vc")):
+        _expect(t, n, (B, H_kv, N_cap, d), torch.bfloat16, dev)
+    _expect(Pc, "Pc", (B, H_kv, pisa_pyramid_nodes(N_cap), d), torch.bfloat16, dev)
+    _expect(seq_len, "seq_len", (B,), torch.int32, dev)
     if o is None:
         o = torch.empty_like(q)
+    _expect(o, "o", (B, H_q, d), torch.bfloat16, dev)
+    _expect(lse, "lse", (B, H_q), torch.float32, dev)
+    _expect(idx_out, "idx_out", (B, H_kv, K_sel), torch.int32, dev)
     shape = make_shape(B, 0, H_q, H_kv, d, N_cap)
     _check(lib().pisa_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), _ptr(o),
                                   _ptr(lse), _ptr(idx_out), shape, make_params(K_sel, True, scale, scoring=scoring),

@@ -280,14 +280,14 @@ def test_decode_scoring_variants(oracle_impl, scoring):
 def test_prefill_host_matches_the_device_path(case):
     """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
     what the device-resident calls return on the same inputs.  The 35000-token cases run as six
-    query chunks (4096, 8704, 8704, 8704, 696, 4096) with two sequences per batch, so the
+    query chunks (4096, 8192, 5184, 5240, 8192, 4096) with two sequences per batch, so the
     chunked copies of Q, O, LSE and the selection rows are all strided; the last one also
     selects without the causal mask (every block of the sequence is a candidate for every
     chunk) and with the PISA-2 block score."""
     causal, scoring = True, 0
     if case == "4k_b2":
         w = W.WORKLOADS["prefill_4k"].with_(B=2)
-    elif case == "20000_d64_k4_chunked":  # d = 64, G_Q = 4, K = 4: chunks 4096, 4992, 4992, 1824, 4096
+    elif case == "20000_d64_k4_chunked":  # d = 64, G_Q = 4, K = 4: chunks 4096, 3904, 3968, 3936, 4096
         w = W.WORKLOADS["tiny"].with_(N=20000)
     else:
         w = W.WORKLOADS["prefill_32k"].with_(B=2, N=35000, H_q=8, H_kv=2)
