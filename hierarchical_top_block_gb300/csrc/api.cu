@@ -223,8 +223,13 @@ SelectLayout select_layout(const Problem& p) {
 
 pisa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA; }
 
+// The selection's clustering lists and the backward's block -> queries lists hold up to
+// B * H_kv * N * K entries and address them with 32-bit offsets.
+bool entry_lists_fit(const Problem& p) { return (long long)p.B * p.H_kv * p.N * p.K < (1LL << 31); }
+
 pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx, float* leaf_score,
                        int32_t* s2, void* ws, size_t ws_bytes, const Problem& p, DeviceState* st, cudaStream_t s) {
+  if (!entry_lists_fit(p)) return PISA_ERR_UNSUPPORTED;
   SelectLayout L = select_layout(p);
   if (ws_bytes < L.total_bytes) return PISA_ERR_WORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -297,7 +302,7 @@ long long pisa_pyramid_nodes(long long N, int C, int g) {
 
 size_t pisa_select_workspace_bytes(pisa_shape shape, pisa_params params) {
   Problem p;
-  if (check_params(shape, params, &p) != PISA_OK) return 0;
+  if (check_params(shape, params, &p) != PISA_OK || !entry_lists_fit(p)) return 0;
   return select_layout(p).total_bytes;
 }
 
@@ -319,6 +324,7 @@ pisa_status pisa_select_prefill(const uint16_t* Q, const uint16_t* K, const uint
   pisa_status rc = check_params(shape, params, &p);
   if (rc != PISA_OK) return rc;
   if (p.N_cap != p.N) return PISA_ERR_INVALID_ARG;
+  if (!entry_lists_fit(p)) return PISA_ERR_UNSUPPORTED;
   if (p.B == 0 || p.N == 0) return PISA_OK;
   if (!Q || !K || !P || !idx || !ws) return PISA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(P) || (reinterpret_cast<uintptr_t>(ws) & 255u)) return PISA_ERR_INVALID_ARG;
@@ -344,7 +350,7 @@ pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t* K, const
 
 size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params) {
   Problem p;
-  if (check_params(shape, params, &p) != PISA_OK) return 0;
+  if (check_params(shape, params, &p) != PISA_OK || !entry_lists_fit(p)) return 0;
   return attn_backward_workspace_bytes(p);
 }
 
@@ -355,6 +361,7 @@ pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, cons
   Problem p;
   pisa_status rc = check_params(shape, params, &p);
   if (rc != PISA_OK) return rc;
+  if (!entry_lists_fit(p)) return PISA_ERR_UNSUPPORTED;
   if (p.B == 0 || p.N == 0) return PISA_OK;
   if (!Q || !K || !V || !idx || !O || !LSE || !dO || !dQ || !dK || !dV || !ws) return PISA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
@@ -378,7 +385,7 @@ int pisa_prefill_host_chunks(long long N, long long* bounds, int max_bounds) {
 
 size_t pisa_prefill_host_workspace_bytes(pisa_shape shape, pisa_params params) {
   Problem p;
-  if (check_params(shape, params, &p) != PISA_OK) return 0;
+  if (check_params(shape, params, &p) != PISA_OK || !entry_lists_fit(p)) return 0;
   const size_t q = (size_t)p.B * p.N * p.H_q * p.d * 2;
   const size_t kv = (size_t)p.B * p.H_kv * p.N * p.d * 2;
   const size_t pyr = (size_t)p.B * p.H_kv * pisa_pyramid_nodes(p.N, 64, 2) * p.d * 2;
@@ -395,6 +402,7 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   pisa_status rc = check_params(shape, params, &p);
   if (rc != PISA_OK) return rc;
   if (p.N_cap != p.N) return PISA_ERR_INVALID_ARG;
+  if (!entry_lists_fit(p)) return PISA_ERR_UNSUPPORTED;
   if (p.B == 0 || p.N == 0) return PISA_OK;
   if (!Q_host || !K_host || !V_host || !O_host || !dev_ws) return PISA_ERR_INVALID_ARG;
   if (ws_bytes < pisa_prefill_host_workspace_bytes(shape, params)) return PISA_ERR_WORKSPACE;

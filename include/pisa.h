@@ -29,6 +29,10 @@
  *     Argument errors are reported synchronously, before anything is launched.
  *   - Supported: d in {64, 128}; C = 64; g = 2; 1 <= K <= 16; H_q % H_kv == 0 and
  *     G_Q = H_q / H_kv in {1, 2, 4, 8, 16}.  Other values return PISA_ERR_UNSUPPORTED.
+ *   - Sizes: N_cap < 2^25 and B * N_cap * H_q < 2^31 everywhere; the selection entry points
+ *     (pisa_select_prefill, pisa_select_prefill_noalloc, pisa_prefill_host) and the backward
+ *     also need B * H_kv * N * K < 2^31 (their per-block lists use 32-bit offsets).  Larger
+ *     shapes return PISA_ERR_UNSUPPORTED, and their workspace queries return 0.
  *   - Selected index rows are sorted ascending and padded with -1 at the end.
  *   - Kernels never trap: waits are bounded and out-of-range indices are skipped; either
  *     event sets a device error word that pisa_get_last_device_error() returns.

@@ -100,3 +100,22 @@ def test_prefill_host_chunk_plan(lib):
     assert lib.pisa_prefill_host_chunks(262144, None, 17) == -1
     assert lib.pisa_prefill_host_chunks(262144, buf, 11) == -1
     assert lib.pisa_prefill_host_chunks(262144, buf, 12) == 11
+
+
+def test_entry_list_limit(lib):
+    """The selection and the backward keep per-block lists of up to B * H_kv * N * K entries
+    with 32-bit offsets: a shape at 2^31 entries is refused before anything touches the
+    device (workspace queries give 0), one entry below it is accepted by the queries."""
+    N = 1 << 23
+    big = pisa.make_shape(1, N, 16, 16, 64, N)  # G_Q = 1, d = 64: B * N_cap * H_q = 2^27 passes the other checks
+    at, below = pisa.make_params(16), pisa.make_params(15)
+    assert pisa.pisa_select_workspace_bytes(big, at) == 0
+    assert pisa.pisa_attn_backward_workspace_bytes(big, at) == 0
+    assert pisa.pisa_prefill_host_workspace_bytes(big, at) == 0
+    assert pisa.pisa_select_workspace_bytes(big, below) > 0
+    assert pisa.pisa_attn_backward_workspace_bytes(big, below) > 0
+    fake = ct.c_void_p(1 << 20)  # aligned, never dereferenced: the call returns before using it
+    assert lib.pisa_select_prefill(fake, fake, fake, fake, None, None, fake, 1 << 40, big, at, None) == 2
+    assert lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, big, at, None) == 2
+    assert lib.pisa_sparse_attn_backward(*([fake] * 11), 1 << 40, big, at, None) == 2
+    assert lib.pisa_prefill_host(fake, fake, fake, fake, None, None, fake, 1 << 40, big, at, None) == 2
