@@ -224,8 +224,12 @@ SelectLayout select_layout(const Problem& p) {
 pisa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA; }
 
 // The selection's clustering lists and the backward's block -> queries lists hold up to
-// B * H_kv * N * K entries and address them with 32-bit offsets.
-bool entry_lists_fit(const Problem& p) { return (long long)p.B * p.H_kv * p.N * p.K < (1LL << 31); }
+// B * H_kv * N * K entries and address them with 32-bit offsets; the selection's tile
+// offsets are 32-bit as well.
+bool entry_lists_fit(const Problem& p) {
+  if ((long long)p.B * p.H_kv * p.N * p.K >= (1LL << 31)) return false;
+  return select_layout(p).cb.max_tiles < (1LL << 31);
+}
 
 pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx, float* leaf_score,
                        int32_t* s2, void* ws, size_t ws_bytes, const Problem& p, DeviceState* st, cudaStream_t s) {
