@@ -109,3 +109,45 @@ def test_host_prefill_buffers_checked_before_the_device_is_touched():
         pisa.pisa_prefill_host(Q, K[:, :, :-1].contiguous(), V, w.K)
     with pytest.raises(ValueError):
         pisa.pisa_prefill_host(Q.float(), K, V, w.K)
+
+
+def _empty_calls(dev, host_prefill):
+    """Every entry point on empty problems (N = 0, then B = 0), through the binding and the
+    library; each returns outputs of the right (empty) shape and launches nothing."""
+    for B, N in ((1, 0), (0, 256)):
+        Q = torch.empty(B, N, 16, 128, dtype=torch.bfloat16, device=dev)
+        K = torch.empty(B, 1, N, 128, dtype=torch.bfloat16, device=dev)
+        V = torch.empty_like(K)
+        P = pisa.pisa_build_pyramid(K)
+        assert P.shape == (B, 1, pisa.pisa_pyramid_nodes(N), 128)
+        idx, score = pisa.pisa_select_prefill(Q, K, P, 16, want_scores=True)
+        assert idx.shape == (B, 1, N, 16) and score.shape == (B, 1, N, 32)
+        O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx)
+        assert O.shape == Q.shape and LSE.shape == (B, 16, N)
+        dQ, dK, dV = pisa.pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, torch.empty_like(Q))
+        assert dQ.shape == Q.shape and dK.shape == K.shape and dV.shape == V.shape
+        if host_prefill:
+            Oh = pisa.pisa_prefill_host(Q.cpu(), K.cpu(), V.cpu(), 16, device=0)
+            assert Oh.shape == Q.shape and Oh.device.type == "cpu"
+    Kc = torch.empty(0, 2, 256, 64, dtype=torch.bfloat16, device=dev)
+    Pc = pisa.pisa_build_pyramid(Kc, N=0)
+    q = torch.empty(0, 8, 64, dtype=torch.bfloat16, device=dev)
+    kv = torch.empty(0, 2, 64, dtype=torch.bfloat16, device=dev)
+    o = pisa.pisa_decode_step(q, kv, kv.clone(), Kc, Kc.clone(), Pc, torch.empty(0, dtype=torch.int32, device=dev), 16)
+    assert o.shape == (0, 8, 64)
+
+
+def test_empty_problems(monkeypatch):
+    """The real library on CPU tensors: an empty problem returns before any device work, so the
+    whole path from the binding through the C entry points runs without a GPU."""
+    build()
+
+    def bf16_any_device(t, name, dim=None):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or (dim is not None and t.dim() != dim):
+            raise ValueError(name)
+
+    monkeypatch.setattr(pisa, "_bf16", bf16_any_device)
+    monkeypatch.setattr(pisa, "_stream", lambda t: None)
+    monkeypatch.setattr(pisa, "_workspace", lambda ws, need, dev: torch.empty(max(need, 256), dtype=torch.uint8))
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda dev=None: types.SimpleNamespace(cuda_stream=0))
+    _empty_calls("cpu", host_prefill=True)
