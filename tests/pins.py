@@ -313,6 +313,29 @@ def pin_backward_dense_autograd(o):
     assert np.abs(dV - v.grad.numpy()).max() < 1e-10
 
 
+
+def pin_backward_dense_autograd_noncausal(o):
+    """Without the causal mask and with K >= M_1, step 4 is dense attention over all keys: its
+    gradients equal PyTorch's autograd of the unmasked textbook formula (fp64)."""
+    import torch
+    N, H_q, H_kv, d, K_sel = 150, 4, 2, 16, 3       # M_1 = 3 leaves, the last one ragged
+    Q, K, V, dO = _bwd_case(53, N=N, H_q=H_q, H_kv=H_kv, d=d)
+    P = o.build_pyramid(K)
+    rows = np.array([[0, g, t] for g in range(H_kv) for t in range(N)], np.int64)
+    idx = o.select(Q, K, P, K_sel, rows, causal=False)["idx"].reshape(1, H_kv, N, K_sel)
+    dQ, dK, dV = o.sparse_attention_backward(Q, K, V, idx, dO, causal=False)
+    q = torch.tensor(b2f(Q), dtype=torch.float64, requires_grad=True)
+    k = torch.tensor(b2f(K), dtype=torch.float64, requires_grad=True)
+    v = torch.tensor(b2f(V), dtype=torch.float64, requires_grad=True)
+    G = H_q // H_kv
+    kk, vv = k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1)
+    s_ = torch.einsum("bthd,bhnd->bhtn", q, kk) / math.sqrt(d)
+    out = torch.einsum("bhtn,bhnd->bthd", torch.softmax(s_, dim=-1), vv)
+    out.backward(torch.tensor(b2f(dO)))
+    assert np.abs(dQ - q.grad.numpy()).max() < 1e-10
+    assert np.abs(dK - k.grad.numpy()).max() < 1e-10
+    assert np.abs(dV - v.grad.numpy()).max() < 1e-10
+
 def pin_backward_finite_differences(o):
     """Sparse selection (K=1: the own block only in causal mode, other blocks absent): the
     gradients match central differences of the oracle's own forward of L = sum(O * dO),
@@ -429,6 +452,30 @@ def pin_brute_force_topk(o):
                     assert abs(s - lse[int(j)]) < 1e-9, (t, j, s, lse[int(j)])
 
 
+
+def pin_brute_force_topk_noncausal(o):
+    """Without the causal mask every leaf of the sequence is a candidate and none is forced:
+    when no level prunes (M_1 <= g K) the selection is the plain top-K of the leaf LSE over
+    all keys of every leaf, ragged last leaf included (brute force, ties to the lower index)."""
+    for (N, H_q, H_kv, Ksel) in ((1024, 4, 1, 8), (64 * 11 + 9, 4, 2, 6)):
+        Q, K, V = _tiny_inputs(seed=13, N=N, H_q=H_q, H_kv=H_kv)
+        P = o.build_pyramid(K)
+        G = H_q // H_kv
+        scale = 1.0 / math.sqrt(Q.shape[-1])
+        rows = np.array([(0, g, t) for g in range(H_kv) for t in range(0, N, 11)])
+        r = o.select(Q, K, P, Ksel, rows, causal=False)
+        for i, (b, g, t) in enumerate(rows):
+            lse = brute_leaf_lse(b2f(Q[b, t, g * G:(g + 1) * G]), b2f(K[b, g]), scale, t, 64, causal=False)
+            assert len(lse) == (N + 63) // 64
+            want = sorted(sorted(lse, key=lambda j: (-lse[j], j))[:Ksel])
+            got = [x for x in r["idx"][i] if x >= 0]
+            assert got == want, (N, t, got, want)
+            for j, sc in zip(r["cand"][i], r["cand_score"][i]):
+                if j >= 0:
+                    assert abs(sc - lse[int(j)]) < 1e-9, (t, j, sc, lse[int(j)])
+        # queries early in the sequence select leaves after their own position
+        assert any(x * 64 > t for (_, _, t), row in zip(rows, r["idx"]) for x in row if x >= 0)
+
 def pin_final_set_invariants(o):
     """Final sets: ascending, unique, -1 padded at the end, own leaf present,
     |I_t| = min(K, #eligible leaves) when no level prunes; <= gK candidates; |S2| <= K."""
@@ -515,6 +562,31 @@ def pin_dense_equivalence(o):
                 assert np.abs(O[i, h] - out).max() < 1e-9, (t, h)
 
 
+
+def pin_dense_equivalence_noncausal(o):
+    """Without the causal mask and with K >= M_1 every leaf is selected, so the output of every
+    query is dense attention over all N keys (textbook softmax), ragged last leaf included."""
+    Q, K, V = _tiny_inputs(seed=17, N=64 * 5 + 21, H_q=4, H_kv=2)
+    N, H_q, d = Q.shape[1], Q.shape[2], Q.shape[3]
+    H_kv = 2
+    G = H_q // H_kv
+    Ksel = (N + 63) // 64
+    P = o.build_pyramid(K)
+    sel = o.select(Q, K, P, Ksel, np.array([(0, g, t) for g in range(H_kv) for t in range(N)]), causal=False)
+    idx = sel["idx"].reshape(1, H_kv, N, Ksel)
+    assert np.all(idx == np.arange(Ksel))
+    rows = np.array([(0, t) for t in range(0, N, 3)])
+    O, LSE, _ = o.sparse_attention(Q, K, V, idx, rows, causal=False)
+    scale = 1.0 / math.sqrt(d)
+    for i, (b, t) in enumerate(rows):
+        for h in range(H_q):
+            g = h // G
+            z = scale * (b2f(K[0, g]) @ b2f(Q[0, t, h]))
+            m = z.max()
+            w = np.exp(z - m)
+            assert abs(LSE[i, h] - (m + math.log(w.sum()))) < 1e-9, (t, h)
+            assert np.abs(O[i, h] - (w / w.sum()) @ b2f(V[0, g])).max() < 1e-9, (t, h)
+
 def pin_weights_sum_to_one(o):
     Q, K, V = _tiny_inputs(seed=9)
     N = Q.shape[1]
@@ -588,8 +660,10 @@ def pin_decode(o):
 ALL_PINS = [
     pin_level_sizes, pin_bf16_rounding, pin_pyramid_constant_keys, pin_pyramid_raw_mean,
     pin_pyramid_ragged_leaf_mean, pin_leaf_lse_closed_forms, pin_gqa_head_sum, pin_lse_beats_mean,
-    pin_ties_lower_index, pin_brute_force_topk, pin_final_set_invariants, pin_walk_prunes_by_summary_lse,
-    pin_dense_equivalence, pin_weights_sum_to_one, pin_single_block_at_start, pin_decode,
+    pin_ties_lower_index, pin_brute_force_topk, pin_brute_force_topk_noncausal, pin_final_set_invariants,
+    pin_walk_prunes_by_summary_lse, pin_dense_equivalence, pin_dense_equivalence_noncausal, pin_weights_sum_to_one,
+    pin_single_block_at_start, pin_decode,
     pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,
-    pin_backward_dense_autograd, pin_backward_finite_differences, pin_backward_sums,
+    pin_backward_dense_autograd, pin_backward_dense_autograd_noncausal, pin_backward_finite_differences,
+    pin_backward_sums,
 ]

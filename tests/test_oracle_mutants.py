@@ -62,6 +62,21 @@ MUTANTS["backward_dv_uses_dS"] = [("      dV[c * d + e] += P[i] * dO[e];", "    
 MUTANTS["backward_ignores_causal"] = [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;",
                                        "      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;")]
 
+# the non-causal mode (every block a candidate, none forced, no key masked)
+MUTANTS["noncausal_leaf_masked"] = [("if (!R.causal || c <= R.t) z.push_back(R.scale * dot_key(R, h, c));",
+                                     "if (c <= R.t) z.push_back(R.scale * dot_key(R, h, c));")]
+MUTANTS["noncausal_eligibility_masked"] = [("  if (!R.causal) return true;\n  return i * ipow(R.g, l - 1) * R.C <= R.t;",
+                                            "  return i * ipow(R.g, l - 1) * R.C <= R.t;")]
+MUTANTS["noncausal_own_forced"] = [
+    ("  long long own = R.causal ? R.t / R.C : -1;\n  for (size_t s = 0; s < out.cand.size(); ++s)\n    if (out.cand[s] >= 0 && out.cand[s] != own) {",
+     "  long long own = R.t / R.C;\n  for (size_t s = 0; s < out.cand.size(); ++s)\n    if (out.cand[s] >= 0 && out.cand[s] != own) {"),
+    ("fin = topk(ids, sc, R.causal ? R.K - 1 : R.K, &gap);", "fin = topk(ids, sc, R.K - 1, &gap);"),
+    ("  if (R.causal) fin.push_back(own);\n", "  fin.push_back(own);\n")]
+MUTANTS["attention_noncausal_masked"] = [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;",
+                                          "      if (c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;")]
+MUTANTS["backward_noncausal_masked"] = [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;",
+                                         "      if (c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;")]
+
 # "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
 MUTANTS["head_sum_drops_heads"] = [
     ("  double u = 0;\n  for (int h = 0; h < R.GQ; ++h) {\n    std::vector<double> z;\n    for (long long r",
