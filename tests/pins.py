@@ -657,12 +657,49 @@ def pin_decode(o):
                 assert np.array_equal(O[0], out[b]) and np.array_equal(L[0], lse[b]), (s, b)
 
 
+
+def pin_decode_scoring_variants(o):
+    """Decode under the PISA-1 and PISA-2 block scores: each step's selection and output equal
+    the prefill row over the same tokens under the same score (the walk prunes: M_1 > g K), and
+    on these inputs the two scores select differently from the LSE on some steps."""
+    rng = np.random.default_rng(29)
+    B, H_q, H_kv, d, Ksel, N0, steps, N_cap = 1, 4, 2, 32, 2, 64 * 9 + 5, 12, 1024
+    K0 = random_bf16(rng, (B, H_kv, N0, d))
+    V0 = random_bf16(rng, (B, H_kv, N0, d))
+    Qs = random_bf16(rng, (steps, B, H_q, d), 2.0)
+    ks = random_bf16(rng, (steps, B, H_kv, d))
+    vs = random_bf16(rng, (steps, B, H_kv, d))
+    picks = {}
+    for scoring in (0, 1, 2):
+        Kc = np.zeros((B, H_kv, N_cap, d), np.uint16)
+        Vc = np.zeros((B, H_kv, N_cap, d), np.uint16)
+        Kc[:, :, :N0], Vc[:, :, :N0] = K0, V0
+        Pc = o.build_pyramid(Kc, N=N0)
+        seq = np.array([N0], np.int32)
+        picks[scoring] = []
+        for s in range(steps):
+            n = int(seq[0]) + 1
+            out, lse, idx = o.decode_step(Qs[s], ks[s], vs[s], Kc, Vc, Pc, seq, Ksel, scoring=scoring)
+            picks[scoring].append(idx.copy())
+            Qp = np.zeros((1, n, H_q, d), np.uint16)
+            Qp[0, n - 1] = Qs[s, 0]
+            Kp, Vp = Kc[:, :, :n].copy(), Vc[:, :, :n].copy()
+            sel = o.select(Qp, Kp, o.build_pyramid(Kp), Ksel, np.array([(0, g, n - 1) for g in range(H_kv)]),
+                           scoring=scoring)
+            assert np.array_equal(sel["idx"], idx[0]), (scoring, s)
+            idxf = np.full((1, H_kv, n, Ksel), -1, np.int32)
+            idxf[0, :, n - 1] = sel["idx"]
+            O, L, _ = o.sparse_attention(Qp, Kp, Vp, idxf, np.array([(0, n - 1)]))
+            assert np.array_equal(O[0], out[0]) and np.array_equal(L[0], lse[0]), (scoring, s)
+    for scoring in (1, 2):
+        assert any(not np.array_equal(a, b) for a, b in zip(picks[0], picks[scoring])), scoring
+
 ALL_PINS = [
     pin_level_sizes, pin_bf16_rounding, pin_pyramid_constant_keys, pin_pyramid_raw_mean,
     pin_pyramid_ragged_leaf_mean, pin_leaf_lse_closed_forms, pin_gqa_head_sum, pin_lse_beats_mean,
     pin_ties_lower_index, pin_brute_force_topk, pin_brute_force_topk_noncausal, pin_final_set_invariants,
     pin_walk_prunes_by_summary_lse, pin_dense_equivalence, pin_dense_equivalence_noncausal, pin_weights_sum_to_one,
-    pin_single_block_at_start, pin_decode,
+    pin_single_block_at_start, pin_decode, pin_decode_scoring_variants,
     pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,
     pin_backward_dense_autograd, pin_backward_dense_autograd_noncausal, pin_backward_finite_differences,
     pin_backward_sums,

@@ -76,6 +76,8 @@ MUTANTS["attention_noncausal_masked"] = [("      if (causal && c > t) continue;\
                                           "      if (c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  for (int e = 0; e < d; ++e) o[e] = 0;")]
 MUTANTS["backward_noncausal_masked"] = [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;",
                                          "      if (c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;")]
+MUTANTS["decode_ignores_scoring"] = [("n, T, d, C, g, Ksel, GQ, 1, scale, scoring);\n      Selection S = select_row(R);",
+                                      "n, T, d, C, g, Ksel, GQ, 1, scale, 0);\n      Selection S = select_row(R);")]
 
 # "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
 MUTANTS["head_sum_drops_heads"] = [
