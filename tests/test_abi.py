@@ -119,3 +119,46 @@ def test_entry_list_limit(lib):
     assert lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, big, at, None) == 2
     assert lib.pisa_sparse_attn_backward(*([fake] * 11), 1 << 40, big, at, None) == 2
     assert lib.pisa_prefill_host(fake, fake, fake, fake, None, None, fake, 1 << 40, big, at, None) == 2
+
+
+def test_parameter_rules(lib):
+    """Each documented argument rule is enforced before anything touches the device (status 1
+    invalid argument, 2 unsupported, 6 workspace too small); the pointers are aligned fakes
+    that no refused call dereferences."""
+    fake = ct.c_void_p(1 << 20)
+    base = {"B": 1, "N": 4096, "H_q": 16, "H_kv": 1, "d": 128, "N_cap": 0}
+
+    def shape(**kw):
+        s = dict(base, **kw)
+        return pisa.make_shape(s["B"], s["N"], s["H_q"], s["H_kv"], s["d"], s["N_cap"])
+
+    def sel(sh, pr, ws=fake, Q=fake):
+        return lib.pisa_select_prefill(Q, fake, fake, fake, None, None, ws, 1 << 40, sh, pr, None)
+
+    p16 = pisa.make_params(16)
+    cases = [
+        (sel(shape(), pisa.make_params(0)), 2), (sel(shape(), pisa.make_params(17)), 2),
+        (sel(shape(H_q=12, H_kv=8), p16), 1), (sel(shape(H_q=3, H_kv=1), p16), 2), (sel(shape(H_q=32, H_kv=1), p16), 2),
+        (sel(shape(d=96), p16), 2), (sel(shape(B=-1), p16), 1), (sel(shape(H_q=0), p16), 1),
+        (sel(shape(N_cap=100), p16), 1), (sel(shape(N_cap=8192), p16), 1),
+        (sel(shape(N=1 << 25), p16), 2),
+        (sel(shape(B=64, N=1 << 24, H_q=16, H_kv=16), pisa.make_params(1)), 2),
+        (sel(shape(), pisa.make_params(16, scale=float("nan"))), 1),
+        (sel(shape(), pisa.pisa_params(64, 2, 16, 2, 0.0, 0)), 1),      # causal must be 0 or 1
+        (sel(shape(), pisa.make_params(16, scoring=3)), 1),
+        (sel(shape(), pisa.make_params(16, g=4)), 2),
+        (sel(shape(), p16, ws=ct.c_void_p((1 << 20) + 16)), 1),          # ws must be 256-byte aligned
+        (sel(shape(), p16, Q=ct.c_void_p((1 << 20) + 2)), 1),            # tensors 16-byte aligned
+        (lib.pisa_sparse_attn_prefill(fake, fake, fake, fake, fake, None, shape(N_cap=100), p16, None), 1),
+        (lib.pisa_sparse_attn_prefill(fake, fake, fake, ct.c_void_p((1 << 20) + 4), fake, None, shape(), p16, None), 1),
+        (lib.pisa_decode_step(*([fake] * 10), shape(N=0, N_cap=0), p16, None), 1),
+        (lib.pisa_decode_step(*([fake] * 10), shape(N=0, N_cap=4096), pisa.make_params(16, causal=False), None), 2),
+        (lib.pisa_prefill_host(fake, fake, fake, fake, None, None, fake, 1 << 40, shape(N_cap=8192), p16, None), 1),
+        (lib.pisa_prefill_host(fake, fake, fake, fake, None, None, ct.c_void_p((1 << 20) + 16), 1 << 40, shape(), p16,
+                               None), 1),
+        (lib.pisa_prefill_host(fake, fake, fake, fake, None, None, fake, 1024, shape(), p16, None), 6),
+        (lib.pisa_prefill_host(None, fake, fake, fake, None, None, fake, 1 << 40, shape(), p16, None), 1),
+        (lib.pisa_sparse_attn_backward(*([fake] * 11), 1024, shape(), p16, None), 6),
+        (lib.pisa_sparse_attn_backward(*([fake] * 10), ct.c_void_p((1 << 20) + 64), 1 << 40, shape(), p16, None), 1),
+    ]
+    assert [got for got, _ in cases] == [want for _, want in cases]
