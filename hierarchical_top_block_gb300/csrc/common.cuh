@@ -178,7 +178,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   }
 }
 
-// Warp-uniform bounded wait: every lane polls; all lanes get the same result.
+// Warp-uniform bounded wait: every lane polls; all lanes get the same verdict.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
   const bool ok = mbar_wait(bar, parity, err);
   return __all_sync(0xffffffffu, ok);
