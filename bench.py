@@ -452,7 +452,9 @@ def secondary_prefill(w, dev, steps=5, K_sel=None):
 
 def selection_quality_section(w, dev, samples=96, seed=11):
     """Recall@K against the exact leaf-LSE top-K and kept dense-attention mass, on the seeded
-    needle workload, for each block scoring and K = 8 (the pages' setting) and the workload's K."""
+    needle workload, for each block scoring and K = 8 (the pages' setting) and the workload's K;
+    and the needle-hit rate: the share of the query rows each planted needle was aimed at whose
+    selection holds the needle's block."""
     import numpy as np
     import torch
 
@@ -464,13 +466,16 @@ def selection_quality_section(w, dev, samples=96, seed=11):
     P = pisa.pisa_build_pyramid(K)
     rng = np.random.default_rng(seed)
     rows = sorted((int(rng.integers(0, w.B)), int(t)) for t in rng.integers(64, w.N, samples))
-    res = {"samples": samples, "workload": w.name,
+    targets = [(n.b, n.g, n.pos, t) for n in W.needles(w) for (t, _h) in n.rows]
+    res = {"samples": samples, "workload": w.name, "needle_rows": len(targets),
            "reference": "exact top-K of the head-summed leaf LSE over all eligible blocks (own block kept)"}
     for K_sel in sorted({8, w.K}):
         for name in ("lse", "pisa1", "pisa2"):
             idx = pisa.pisa_select_prefill(Q, K, P, K_sel, scoring=name)
             torch.cuda.synchronize()
-            res[f"K{K_sel}_{name}"] = quality.selection_quality(Q, K, idx, K_sel, rows)
+            rep = quality.selection_quality(Q, K, idx, K_sel, rows)
+            rep["needle_hit_rate"] = quality.needle_hit_rate(idx, targets)["hit_rate"]
+            res[f"K{K_sel}_{name}"] = rep
     del Q, K, V, P
     torch.cuda.empty_cache()
     return res

@@ -94,3 +94,19 @@ def selection_quality(Q, K, idx, K_sel: int, rows, C: int = 64, scale: float | N
     out["recall_by_position"] = [float(rec_t[(pos_t >= lo) & (pos_t < hi)].mean()) if ((pos_t >= lo) & (pos_t < hi)).any()
                                  else None for lo, hi in zip(edges[:-1], edges[1:])]
     return out
+
+
+def needle_hit_rate(idx, targets, C: int = 64) -> dict:
+    """Share of planted-needle query rows whose selected set holds the needle's block.
+
+    idx [B, H_kv, N, K_sel] from the selection under test (any device); targets: one
+    (b, h_kv, needle key position, t') per query row a needle was aimed at.  A row hits
+    when the block of the needle's key, position // C, is among the row's selected blocks.
+    Returns {"rows": number of rows, "hit_rate": share of hits, None without rows}."""
+    tg = torch.as_tensor([tuple(int(v) for v in x) for x in targets], dtype=torch.int64).reshape(-1, 4)
+    if tg.shape[0] == 0:
+        return {"rows": 0, "hit_rate": None}
+    tg = tg.to(idx.device)
+    sel = idx[tg[:, 0], tg[:, 1], tg[:, 3]].to(torch.int64)                 # [R, K_sel]
+    hit = (sel == (tg[:, 2] // C)[:, None]).any(dim=1)
+    return {"rows": int(tg.shape[0]), "hit_rate": float(hit.double().mean())}

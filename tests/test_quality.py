@@ -48,3 +48,36 @@ def test_recall_and_mass_of_exact_and_dense_selections(oracle_impl):
     rep6 = quality.selection_quality(Qt, Kt, torch.from_numpy(idx6), 6, rows)
     assert abs(rep6["kept_mass"] - 1.0) < 1e-12
     assert rep["kept_mass"] < 1.0
+
+
+def test_needle_hit_rate_counts_rows():
+    """Hand-built selections: a row hits when its set holds the needle key's block."""
+    idx = torch.full((2, 1, 300, 3), -1, dtype=torch.int32)
+    idx[0, 0, 200] = torch.tensor([0, 2, 3], dtype=torch.int32)      # holds block 2 (key 130)
+    idx[0, 0, 250] = torch.tensor([1, 3, -1], dtype=torch.int32)     # does not
+    idx[1, 0, 299] = torch.tensor([2, 4, -1], dtype=torch.int32)     # holds block 2 (key 191)
+    targets = [(0, 0, 130, 200), (0, 0, 130, 250), (1, 0, 191, 299), (1, 0, 192, 299)]
+    assert quality.needle_hit_rate(idx, targets) == {"rows": 4, "hit_rate": 0.5}
+    assert quality.needle_hit_rate(idx, []) == {"rows": 0, "hit_rate": None}
+
+
+def test_needle_hit_rate_equals_the_exact_reference_without_pruning(oracle_impl):
+    """On the small needle workload with g K >= M_1 nothing is pruned, so the oracle's needle
+    hits are those of the exact top-K reference, which holds every planted needle there."""
+    import workloads as W
+    o = oracle_impl
+    w = W.WORKLOADS["tiny"]                       # 16 leaves, 2 needles x 8 aimed rows
+    Q, K, V = W.prefill_inputs(w, "cpu")
+    Qb, Kb = (x.contiguous().view(torch.int16).numpy().view(np.uint16) for x in (Q, K))
+    nl = W.needles(w)
+    targets = [(n.b, n.g, n.pos, t) for n in nl for (t, _h) in n.rows]
+    rows = np.array([(b, g, t) for (b, g, _p, t) in targets], np.int64)
+    K_sel = 8
+    sel = o.select(Qb, Kb, o.build_pyramid(Kb), K_sel, rows)["idx"]
+    idx = torch.full((w.B, w.H_kv, w.N, K_sel), -1, dtype=torch.int32)
+    idx[rows[:, 0], rows[:, 1], rows[:, 2]] = torch.from_numpy(sel)
+    ref = torch.full_like(idx, -1)
+    for b, g, t in rows:
+        ref[b, g, t] = quality.exact_topk_blocks(Q, K, int(b), int(t), K_sel)[g].to(torch.int32)
+    assert torch.equal(idx, ref)
+    assert quality.needle_hit_rate(idx, targets) == quality.needle_hit_rate(ref, targets) == {"rows": 16, "hit_rate": 1.0}
