@@ -567,10 +567,11 @@ class OracleSample:
         ts = np.sort(self.ts_all[offset:offset + rows_n])
         t0 = time.perf_counter()
         P = self.o.build_pyramid(self.Kb)
-        rows = np.stack([np.zeros_like(ts), np.zeros_like(ts), ts], 1)
+        rows = np.array([(0, g, t) for g in range(w.H_kv) for t in ts], np.int64).reshape(-1, 3)
         sel = self.o.select(self.Qb, self.Kb, P, w.K, rows)
+        self.select_dt = time.perf_counter() - t0          # pyramid + selection alone
         idx = np.full((w.B, w.H_kv, w.N, w.K), -1, np.int32)
-        idx[0, 0, ts] = sel["idx"]
+        idx[rows[:, 0], rows[:, 1], rows[:, 2]] = sel["idx"]
         self.o.sparse_attention(self.Qb, self.Kb, self.Vb, idx, np.stack([np.zeros_like(ts), ts], 1))
         dt = time.perf_counter() - t0
         return len(ts) / dt, dt
@@ -578,12 +579,62 @@ class OracleSample:
 
 def cpu_baseline(args, w):
     try:
-        tps, dt = OracleSample(w, args.cpu_sample_rows).run(args.cpu_sample_rows)
+        sample = OracleSample(w, args.cpu_sample_rows)
+        tps, dt = sample.run(args.cpu_sample_rows)
     except Exception as e:  # the baseline is informational
         return {"value": None, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "error": str(e)}
-    return {"value": tps, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"full pyramid + selection and attention for {args.cpu_sample_rows} query positions of "
-                      f"{w.name} (N={w.N}), {dt:.1f} s wall on {os.cpu_count()} threads"}
+    out = {"value": tps, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"full pyramid + selection and attention for {args.cpu_sample_rows} query positions of "
+                     f"{w.name} (N={w.N}), {dt:.1f} s wall on {os.cpu_count()} threads",
+           "selection_only_tokens_per_s": args.cpu_sample_rows / sample.select_dt}
+    if not args.no_secondary:
+        out["secondary"] = oracle_secondary()
+    return out
+
+
+def oracle_secondary(rows_32k=2048, decode_steps=8):
+    """The oracle on bounded samples of the other workloads, as context: the 32K prefill
+    (selection alone and with attention, for a set of query positions) and the batched decode
+    step (the first sequence's first two KV heads for a few steps, scaled to the whole batch
+    by the number of (sequence, KV head) pairs, and labelled so)."""
+    import numpy as np
+
+    import oracle
+    import workloads as W
+
+    res = {}
+    try:
+        w = W.WORKLOADS["prefill_32k"]
+        sample = OracleSample(w, rows_32k)
+        tps, dt = sample.run(rows_32k)
+        res["prefill_32k"] = {"tokens_per_s": tps, "selection_tokens_per_s": rows_32k / sample.select_dt,
+                              "sample": f"full pyramid + {rows_32k} query positions, {dt:.1f} s wall"}
+    except Exception as e:  # informational
+        res["prefill_32k"] = {"error": str(e)}
+    try:
+        w = W.WORKLOADS["decode_128k"]
+        o = oracle.Oracle()
+        pairs = 2                                      # (sequence 0, KV heads 0 and 1)
+        N_cap = w.N + decode_steps
+        Kc = np.zeros((1, pairs, N_cap, w.d), np.uint16)
+        Vc = np.zeros_like(Kc)
+        for g in range(pairs):
+            Kc[0, g, :w.N] = W.bits(W.kv_slice(w, "K", 0, g))
+            Vc[0, g, :w.N] = W.bits(W.kv_slice(w, "V", 0, g))
+        Pc = o.build_pyramid(Kc, N=w.N)
+        seq = np.array([w.N], np.int32)
+        ins = [W.decode_step_inputs(w, s, "cpu") for s in range(decode_steps)]
+        t0 = time.perf_counter()
+        for q, k, v in ins:
+            o.decode_step(W.bits(q[:1, :pairs * w.G_Q]), W.bits(k[:1, :pairs]), W.bits(v[:1, :pairs]), Kc, Vc, Pc,
+                          seq, w.K)
+        per_pair = (time.perf_counter() - t0) / decode_steps / pairs
+        res["decode_128k"] = {"step_us_extrapolated": per_pair * w.B * w.H_kv * 1e6,
+                              "sample": f"{decode_steps} steps of {pairs} (sequence, KV head) pairs of "
+                                        f"{w.B * w.H_kv}, scaled by the pair count"}
+    except Exception as e:  # informational
+        res["decode_128k"] = {"error": str(e)}
+    return res
 
 
 def run_reference(args):
