@@ -9,6 +9,7 @@ import os
 import subprocess
 import sys
 import tempfile
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -94,6 +95,29 @@ def mutant_dir():
         yield d
 
 
+def _mutant_source(name):
+    src = open(oracle.SRC).read()
+    for old, new in MUTANTS[name]:
+        assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+        src = src.replace(old, new)
+    return src
+
+
+@pytest.fixture(scope="module")
+def mutant_libs(mutant_dir):
+    """Every mutant compiled once, the independent g++ runs side by side; each test takes its
+    own result (a missing mutation site raises there)."""
+    def build(name):
+        path = os.path.join(mutant_dir, f"{name}.cpp")
+        with open(path, "w") as f:
+            f.write(_mutant_source(name))
+        return oracle.compile_source(path, os.path.join(mutant_dir, f"lib{name}.so"))
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        futures = {name: ex.submit(build, name) for name in MUTANTS}
+        return {name: fut.exception() or fut.result() for name, fut in futures.items()}
+
+
 RUNNER = """
 import sys
 sys.path[:0] = [{root!r}, {here!r}]
@@ -105,20 +129,16 @@ for pin in pins.ALL_PINS:
         pin(o)
     except Exception as e:
         failed.append(pin.__name__)
+        break  # one failing pin is enough to catch the mutant
 print("FAILED_PINS", ",".join(failed))
 """
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_mutant_is_caught(name, mutant_dir):
-    src = open(oracle.SRC).read()
-    for old, new in MUTANTS[name]:
-        assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
-        src = src.replace(old, new)
-    path = os.path.join(mutant_dir, f"{name}.cpp")
-    with open(path, "w") as f:
-        f.write(src)
-    lib = oracle.compile_source(path, os.path.join(mutant_dir, f"lib{name}.so"))
+def test_mutant_is_caught(name, mutant_libs):
+    lib = mutant_libs[name]
+    if isinstance(lib, BaseException):
+        raise lib
     code = RUNNER.format(root=os.path.dirname(HERE), here=HERE, lib=lib)
     res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
     failed = [ln.split(" ", 1)[1] for ln in res.stdout.splitlines() if ln.startswith("FAILED_PINS ")]
