@@ -292,20 +292,30 @@ def run_pisa(args):
         "pages_reference": PAGES_REFERENCE,
     }
     if rank == 0 and not args.no_secondary:
-        out["scoring_variants"] = scoring_variants(Q, K, P, w, ws, idx)
-        out["backward"] = backward_section(Q, K, V, idx, O, LSE, w, work)
+        out["scoring_variants"] = section(scoring_variants, Q, K, P, w, ws, idx)
+        out["backward"] = section(backward_section, Q, K, V, idx, O, LSE, w, work)
     if rank == 0:
-        out["e2e"] = None if args.no_e2e else run_e2e(args, w, dev)
+        out["e2e"] = None if args.no_e2e else section(run_e2e, args, w, dev)
         if not args.no_secondary:
             # K = 8 is the setting of the paper's selection-speed comparison (its Fig. 3)
-            out["secondary"] = {"prefill_32k": secondary_prefill(W.WORKLOADS["prefill_32k"], dev),
-                                "prefill_32k_k8": secondary_prefill(W.WORKLOADS["prefill_32k"], dev, K_sel=8),
-                                "prefill_256k_k8": secondary_prefill(W.WORKLOADS["prefill_256k"], dev, K_sel=8),
-                                "decode_128k": secondary_decode(W.WORKLOADS["decode_128k"], dev),
-                                "selection_quality_32k": selection_quality_section(W.WORKLOADS["prefill_32k"], dev)}
+            out["secondary"] = {
+                "prefill_32k": section(secondary_prefill, W.WORKLOADS["prefill_32k"], dev),
+                "prefill_32k_k8": section(secondary_prefill, W.WORKLOADS["prefill_32k"], dev, K_sel=8),
+                "prefill_256k_k8": section(secondary_prefill, W.WORKLOADS["prefill_256k"], dev, K_sel=8),
+                "decode_128k": section(secondary_decode, W.WORKLOADS["decode_128k"], dev),
+                "selection_quality_32k": section(selection_quality_section, W.WORKLOADS["prefill_32k"], dev)}
         out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
         print(json.dumps(out), flush=True)
     barrier(world)
+
+
+def section(fn, *args, **kwargs):
+    """Runs one of the line's secondary sections; one that fails is reported in its place
+    ({"error": ...}) instead of costing the whole line (the timed step is checked before)."""
+    try:
+        return fn(*args, **kwargs)
+    except Exception as e:  # noqa: BLE001 - any failure of a secondary section is reported
+        return {"error": f"{type(e).__name__}: {e}"}
 
 
 def backward_section(Q, K, V, idx, O, LSE, w, work, steps=5, warmup=3):

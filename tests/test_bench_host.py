@@ -68,3 +68,10 @@ def test_secondary_decode_times_every_step(monkeypatch):
     assert len(seen) == 3 + 256 and seen[0][0] == 500
     assert all(pos < n_cap for pos, n_cap in seen) and seen[-1][0] == seen[-1][1] - 1   # the cache fills exactly
     assert res["step_us_mean"] == res["step_us_p50"] == 125.0
+
+
+def test_a_failing_section_is_reported_not_fatal():
+    def boom(x):
+        raise RuntimeError(f"device error word {x}")
+    assert bench.section(boom, 5) == {"error": "RuntimeError: device error word 5"}
+    assert bench.section(lambda a, b=0: a + b, 1, b=2) == 3
