@@ -414,6 +414,39 @@ def pin_ties_lower_index(o):
     assert list(r["idx"][1]) == [0, 1, 3], r["idx"]
 
 
+
+def pin_admissible_sets(o):
+    """The parity rule's admissibility check: the oracle's own selection is admissible; on rows
+    whose every SelectK has a gap well above the tolerance nothing else is (a set with one block
+    swapped for an unselected eligible one is refused); with exactly tied scores every choice
+    among the tied blocks is admissible, though the selection itself takes the lower index."""
+    Q, K, V = _tiny_inputs(seed=19)              # 16 leaves, K = 2: levels prune
+    P = o.build_pyramid(K)
+    N, Ksel = Q.shape[1], 2
+    rows = np.array([(0, 0, t) for t in range(200, N, 37)], np.int64)
+    r = o.select(Q, K, P, Ksel, rows)
+    assert np.all(o.admissible(Q, K, P, Ksel, rows, r["idx"]) == 1)
+    clear = np.where(r["min_gap"] > 0.05)[0]
+    assert clear.size >= 5, clear.size
+    for i in clear:
+        t = int(rows[i, 2])
+        row = list(r["idx"][i])
+        other = next(j for j in range(t // 64 + 1) if j not in row)      # an eligible, unselected leaf
+        swapped = sorted([b for b in row if b != t // 64][1:] + [other, t // 64])
+        assert o.admissible(Q, K, P, Ksel, rows[i:i + 1], np.array([swapped], np.int32))[0] == 0, (t, row, swapped)
+    # identical keys: all scores tie
+    d, N = 16, 64 * 6
+    Qt = np.zeros((1, N, 1, d), np.uint16)
+    Qt[0, :, 0, :] = f2b(np.full(d, 0.5))
+    Kt = np.zeros((1, 1, N, d), np.uint16)
+    Kt[0, 0, :, :] = f2b(np.full(d, 0.25))
+    Pt = o.build_pyramid(Kt)
+    row = np.array([[0, 0, N - 1]], np.int64)
+    assert list(o.select(Qt, Kt, Pt, 3, row)["idx"][0]) == [0, 1, 5]
+    for alt in ([0, 1, 5], [0, 4, 5], [2, 3, 5], [1, 4, 5]):
+        assert o.admissible(Qt, Kt, Pt, 3, row, np.array([alt], np.int32))[0] == 1, alt
+    assert o.admissible(Qt, Kt, Pt, 3, row, np.array([[0, 1, 4]], np.int32))[0] == 0   # the own block is forced
+
 def _tiny_inputs(seed=3, N=1024, H_q=4, H_kv=1, d=64, offsets=True):
     rng = np.random.default_rng(seed)
     Q = random_bf16(rng, (1, N, H_q, d))
@@ -697,7 +730,7 @@ def pin_decode_scoring_variants(o):
 ALL_PINS = [
     pin_level_sizes, pin_bf16_rounding, pin_pyramid_constant_keys, pin_pyramid_raw_mean,
     pin_pyramid_ragged_leaf_mean, pin_leaf_lse_closed_forms, pin_gqa_head_sum, pin_lse_beats_mean,
-    pin_ties_lower_index, pin_brute_force_topk, pin_brute_force_topk_noncausal, pin_final_set_invariants,
+    pin_ties_lower_index, pin_admissible_sets, pin_brute_force_topk, pin_brute_force_topk_noncausal, pin_final_set_invariants,
     pin_walk_prunes_by_summary_lse, pin_dense_equivalence, pin_dense_equivalence_noncausal, pin_weights_sum_to_one,
     pin_single_block_at_start, pin_decode, pin_decode_scoring_variants,
     pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,

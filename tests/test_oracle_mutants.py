@@ -80,6 +80,11 @@ MUTANTS["backward_noncausal_masked"] = [("      if (causal && c > t) continue;\n
 MUTANTS["decode_ignores_scoring"] = [("n, T, d, C, g, Ksel, GQ, 1, scale, scoring);\n      Selection S = select_row(R);",
                                       "n, T, d, C, g, Ksel, GQ, 1, scale, 0);\n      Selection S = select_row(R);")]
 
+# the admissibility check behind the parity rule for near-ties
+MUTANTS["admissible_accepts_anything"] = [("    if (f == target) return 1;", "    return 1;")]
+MUTANTS["admissible_without_tolerance"] = [("    if (mn >= mx - tol) {", "    if (mn > mx) {")]
+MUTANTS["admissible_drops_own_block"] = [("    if (R.causal) f.push_back(own);", "")]
+
 # "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
 MUTANTS["head_sum_drops_heads"] = [
     ("  double u = 0;\n  for (int h = 0; h < R.GQ; ++h) {\n    std::vector<double> z;\n    for (long long r",
