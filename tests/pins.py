@@ -276,6 +276,13 @@ def pin_mean_scoring_ranks_like_the_mean(o):
     P = o.build_pyramid(K)
     assert list(o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0, scoring=1)["idx"][0]) == [0, 3]
     assert list(o.select(Q, K, P, 2, np.array([[0, 0, N - 1]]), scale=1.0 / 8.0, scoring=0)["idx"][0]) == [1, 3]
+    # the admissibility check ranks by the same score: each scoring's own set is admissible under
+    # that scoring and the other scoring's set is not (the gaps are about 0.9)
+    row = np.array([[0, 0, N - 1]])
+    for scoring, mine, other in ((1, [0, 3], [1, 3]), (0, [1, 3], [0, 3])):
+        for target, want in ((mine, 1), (other, 0)):
+            got = o.admissible(Q, K, P, 2, row, np.array([target], np.int32), scale=1.0 / 8.0, scoring=scoring)[0]
+            assert got == want, (scoring, target, got)
 
 
 # ------------------------------------------------------------------------------------
@@ -506,6 +513,8 @@ def pin_brute_force_topk_noncausal(o):
             for j, sc in zip(r["cand"][i], r["cand_score"][i]):
                 if j >= 0:
                     assert abs(sc - lse[int(j)]) < 1e-9, (t, j, sc, lse[int(j)])
+        # the admissibility check without the mask accepts the plain top-K (no forced block)
+        assert np.all(o.admissible(Q, K, P, Ksel, rows, r["idx"], causal=False) == 1)
         # queries early in the sequence select leaves after their own position
         assert any(x * 64 > t for (_, _, t), row in zip(rows, r["idx"]) for x in row if x >= 0)
 

@@ -84,6 +84,12 @@ MUTANTS["decode_ignores_scoring"] = [("n, T, d, C, g, Ksel, GQ, 1, scale, scorin
 MUTANTS["admissible_accepts_anything"] = [("    if (f == target) return 1;", "    return 1;")]
 MUTANTS["admissible_without_tolerance"] = [("    if (mn >= mx - tol) {", "    if (mn > mx) {")]
 MUTANTS["admissible_drops_own_block"] = [("    if (R.causal) f.push_back(own);", "")]
+MUTANTS["admissible_ignores_scoring"] = [("GQ, causal, scale, scoring);\n      std::vector<long long> target;",
+                                          "GQ, causal, scale, 0);\n      std::vector<long long> target;")]
+MUTANTS["admissible_noncausal_forces_own"] = [
+    ("  long long own = R.causal ? R.t / R.C : -1;\n  for (long long p : S)", "  long long own = R.t / R.C;\n  for (long long p : S)"),
+    ("admissible_sets(ids, sc, R.causal ? R.K - 1 : R.K, tol, sets, 4096);", "admissible_sets(ids, sc, R.K - 1, tol, sets, 4096);"),
+    ("    if (R.causal) f.push_back(own);", "    f.push_back(own);")]
 
 # "head_sum_drops_heads" needs two edits (internal and leaf scores): sum only head 0
 MUTANTS["head_sum_drops_heads"] = [
