@@ -46,9 +46,9 @@ PAGES_REFERENCE = {
 }
 
 # DRAM traffic of the attention kernel per launch on the 256K prefill (dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture, profiles/dram_traffic_prefill_256k.md), keyed
-# by a hash of the kernel's sources: when the sources change the figure is stale and is reported
-# as null until it is taken again.
+# dram__bytes_write.sum from one ncu capture; the committed DRAM-traffic profile of that
+# workload), keyed by a hash of the kernel's sources: when the sources change the figure is
+# stale and is reported as null until it is taken again.
 ATTN_TRAFFIC = {"sources_sha256": "88038b29dfd8dfe96aa900359165d4b75c6f7ef683facc058995e0ab9a07ce43",
                 "workload": "prefill_256k", "bytes": 13713879552 + 1089932032}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
@@ -186,6 +186,116 @@ def attention_work(idx, N, H_q, H_kv, d, C=64):
             "blocks": blocks}
 
 
+def level_sizes(n, C=64, g=2):
+    """Nodes per pyramid level for n tokens: M_1 = ceil(n / C), M_{l+1} = ceil(M_l / g)."""
+    out = [-(-n // C)] if n > 0 else []
+    while out and out[-1] > 1:
+        out.append(-(-out[-1] // g))
+    return out
+
+
+def stage1_work(N, H_q, H_kv, d, K, B=1, C=64, causal=True):
+    """Child rows the level walk scores, summed over the queries, for a walk whose survivors
+    always have all their children (an upper bound of the realised walk, exact away from the
+    causal edge): at level l the candidates are min(eligible, 2 x survivors of level l + 1);
+    a level is scored when more than K remain, each candidate by its 2 children."""
+    import numpy as np
+
+    M = level_sizes(N, C)
+    L = len(M)
+    t = np.arange(N, dtype=np.int64)
+    surv = np.ones(N, dtype=np.int64)  # the root
+    rows = np.zeros(N, dtype=np.int64)
+    for lvl in range(L - 1, 1, -1):       # levels L-1 .. 2 (1-based); M[lvl - 1] nodes
+        span = C << (lvl - 1)             # keys covered by one level-lvl node
+        elig = np.minimum(M[lvl - 1], t // span + 1) if causal else np.full(N, M[lvl - 1])
+        cand = np.minimum(elig, 2 * surv)
+        scored = cand > K
+        rows += np.where(scored, 2 * cand, 0)
+        surv = np.minimum(cand, K)
+    G = H_q // H_kv
+    total_rows = int(rows.sum()) * B * H_kv
+    return {"child_rows": total_rows, "flops": 2.0 * d * G * total_rows, "l2_gather_bytes": total_rows * d * 2}
+
+
+def leaf_lse_work(s2, N, H_q, H_kv, d, C=64):
+    """Algorithmic work of Stage 2, counted from the realised level-2 survivors s2
+    [B, H_kv, N, K]: 2 d flops per (query head, visible key) of each eligible leaf child."""
+    import torch
+
+    t = torch.arange(N, device=s2.device, dtype=torch.int64).view(1, 1, N, 1)
+    node = s2.to(torch.int64)
+    keys = 0
+    for c in (0, 1):
+        leaf = 2 * node + c
+        vis = torch.clamp(torch.minimum(t, torch.tensor(N - 1, device=s2.device)) - leaf * C + 1, min=0, max=C)
+        keys += int((vis * (node >= 0)).sum().item())
+    return {"visible_keys": keys, "flops": 2.0 * d * keys * (H_q // H_kv)}
+
+
+def roofline_entry(kernel, ms, bound, work, pk):
+    """One kernel's roofline: algorithmic work per launch / its event-timed duration, against the
+    measured peak (HBM copy bandwidth, or bf16 dense burst)."""
+    if bound == "hbm":
+        ach = work / (ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "ms": ms, "algorithmic_bytes": work, "achieved": ach,
+                "peak": pk["hbm"], "unit": "GB/s", "frac": ach / pk["hbm"], "peak_source": pk["source"] + " copy"}
+    ach = work / (ms * 1e-3) / 1e12
+    return {"kernel": kernel, "bound": "tensor", "ms": ms, "algorithmic_flops": work, "achieved": ach,
+            "peak": pk["tensor"], "unit": "TFLOP/s", "frac": ach / pk["tensor"],
+            "peak_source": pk["source"] + " bf16 dense burst"}
+
+
+def phase_rooflines(w, step_fn, s2, attn_flops, steps=5):
+    """Runs `steps` more steps with the library's per-phase event timing on and returns a
+    roofline entry per kernel of the step (CUDA events recorded by the library on the
+    launching stream around each kernel phase)."""
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+
+    pisa.pisa_phase_timing(True)
+    for _ in range(steps):
+        step_fn()
+    torch.cuda.synchronize()
+    times = pisa.pisa_phase_times()
+    pisa.pisa_phase_timing(False)
+    ms = {k: v[0] / v[1] for k, v in times.items() if v[1] > 0}
+    pk = peaks()
+    B, N, H_q, H_kv, d, K = w.B, w.N, w.H_q, w.H_kv, w.d, w.K
+    nodes = sum(level_sizes(N))
+    q_bytes = B * N * H_q * d * 2
+    kv_bytes = B * H_kv * N * d * 2
+    sel_int = B * H_kv * N * K * 4
+    s1 = stage1_work(N, H_q, H_kv, d, K, B)
+    s2w = leaf_lse_work(s2, N, H_q, H_kv, d)
+    out = {}
+    if "pyramid" in ms:
+        out["pyramid"] = roofline_entry("pyramid_leaves_kernel + pyramid_upper_kernel", ms["pyramid"], "hbm",
+                                        kv_bytes + B * H_kv * nodes * d * 2, pk)
+    if "stage1" in ms:
+        e = roofline_entry("stage1_kernel", ms["stage1"], "hbm", q_bytes + 2 * sel_int, pk)
+        e["mma_flops"] = s1["flops"]
+        e["mma_tflops"] = s1["flops"] / (ms["stage1"] * 1e-3) / 1e12
+        e["l2_gather_bytes"] = s1["l2_gather_bytes"]
+        e["note"] = "HBM bytes: Q once, survivors and list places out; mma_flops: saturated-walk count"
+        out["stage1"] = e
+    if "cluster" in ms:
+        out["cluster"] = roofline_entry("cluster kernels (5)", ms["cluster"], "hbm", 3 * sel_int, pk)
+    if "leaf_lse" in ms:
+        e = roofline_entry("leaf_lse_kernel", ms["leaf_lse"], "tensor", s2w["flops"], pk)
+        e["visible_keys"] = s2w["visible_keys"]
+        out["leaf_lse"] = e
+    if "topk" in ms:
+        out["topk"] = roofline_entry("topk_kernel", ms["topk"], "hbm", sel_int + 2 * sel_int + sel_int, pk)
+    if "sparse_attn" in ms:
+        out["sparse_attn"] = roofline_entry("sparse_attn_kernel", ms["sparse_attn"], "tensor", attn_flops, pk)
+    out["timed_steps"] = steps
+    out["method"] = ("CUDA events the library records on the launching stream around each kernel phase "
+                     "(pisa_phase_timing), over separate steps after the timed region")
+    return out
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -225,13 +335,14 @@ def run_pisa(args):
     O = torch.empty_like(Q)
     LSE = torch.empty(w.B, w.H_q, w.N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    s2 = torch.empty(w.B, w.H_kv, w.N, w.K, dtype=torch.int32, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    def step(marks=None):
+    def step(marks=None, keep_s2=False):
         if marks is not None:
             marks[0].record(stream)
         pisa.pisa_build_pyramid(K, P=P)
-        pisa.pisa_select_prefill(Q, K, P, w.K, ws=ws, idx=idx)
+        pisa.pisa_select_prefill(Q, K, P, w.K, ws=ws, idx=idx, s2=s2 if keep_s2 else None)
         if marks is not None:
             marks[1].record(stream)
         pisa.pisa_sparse_attn_prefill(Q, K, V, idx, O=O, LSE=LSE)
@@ -268,6 +379,7 @@ def run_pisa(args):
     work = attention_work(idx, w.N, w.H_q, w.H_kv, w.d)
     flops = work["flops"]
     pk = peaks()
+    rooflines = section(phase_rooflines, w, lambda: step(keep_s2=True), s2, flops)
     achieved_tf = flops / (att_ms * 1e-3) / 1e12
     io_bytes = sum(x.numel() * x.element_size() for x in (Q, K, V, O, LSE, P, idx))
     traffic = ATTN_TRAFFIC["bytes"] if (ATTN_TRAFFIC["sources_sha256"] == attn_sources_sha256()
@@ -287,6 +399,7 @@ def run_pisa(args):
                      "peak_source": pk["source"] + " bf16 dense burst",
                      "l2_gather": {"bytes_per_launch": work["gather_bytes"], "blocks": work["blocks"],
                                    "achieved_tbs": work["gather_bytes"] / (att_ms * 1e-3) / 1e12}},
+        "rooflines": rooflines,
         "clocks": clk,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "pages_reference": PAGES_REFERENCE,
@@ -536,14 +649,13 @@ def secondary_decode(w, dev, steps=None, warmup=3):
 
 def decode_hbm_bytes(w, C=64, g=2):
     """Bytes one decode step must read at least, per (sequence, KV head): the child summaries
-    of every scored level (2K candidates x 2 children), the raw keys of the 2K leaf
-    candidates, and the raw keys and values of the K selected blocks; d bf16 values per row."""
+    of every scored level (2K candidates x 2 children), the raw keys of the 2K leaf candidates
+    (the selected blocks' keys are among them and are not counted again), and the raw values of
+    the K selected blocks; d bf16 values per row."""
     n = w.N + 1
-    sizes = [-(-n // C)]
-    while sizes[-1] > 1:
-        sizes.append(-(-sizes[-1] // g))
+    sizes = level_sizes(n, C, g)
     scored = sum(1 for m in sizes[1:-1] if m > w.K)  # levels 2.. whose candidates exceed K
-    rows = scored * 2 * w.K * g + 2 * w.K * C + w.K * C * 2
+    rows = scored * 2 * w.K * g + 2 * w.K * C + w.K * C
     return w.B * w.H_kv * rows * w.d * 2
 
 

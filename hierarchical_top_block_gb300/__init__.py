@@ -80,6 +80,12 @@ def lib() -> ct.CDLL:
         L.pisa_get_last_device_error.argtypes = [_P]
         L.pisa_version.restype = ct.c_char_p
         L.pisa_version.argtypes = []
+        L.pisa_phase_timing.restype = ct.c_int
+        L.pisa_phase_timing.argtypes = [ct.c_int]
+        L.pisa_phase_times.restype = ct.c_int
+        L.pisa_phase_times.argtypes = [ct.POINTER(ct.c_double), ct.POINTER(ct.c_longlong), ct.c_int]
+        L.pisa_phase_name.restype = ct.c_char_p
+        L.pisa_phase_name.argtypes = [ct.c_int]
         _lib = L
     return _lib
 
@@ -170,6 +176,26 @@ def pisa_version() -> str:
     return lib().pisa_version().decode()
 
 
+def pisa_phase_timing(enable: bool = True) -> None:
+    """Start (clearing the totals) or stop per-phase event timing on the current device."""
+    _check(lib().pisa_phase_timing(1 if enable else 0), "pisa_phase_timing")
+
+
+def pisa_phase_name(phase: int):
+    n = lib().pisa_phase_name(phase)
+    return None if n is None else n.decode()
+
+
+def pisa_phase_times() -> dict:
+    """{phase name: (total ms, timed launches)} of the current device since timing started."""
+    ms = (ct.c_double * 32)()
+    cnt = (ct.c_longlong * 32)()
+    n = lib().pisa_phase_times(ms, cnt, 32)
+    if n < 0:
+        raise PisaError(3, "pisa_phase_times")
+    return {pisa_phase_name(i): (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
 def pisa_get_last_device_error(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
     return lib().pisa_get_last_device_error(ct.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
@@ -204,8 +230,9 @@ def _select_inputs(Q, K, P):
 
 def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float = 0.0, want_scores: bool = False,
                         want_s2: bool = False, ws: torch.Tensor | None = None, idx: torch.Tensor | None = None,
-                        scoring: int | str = 0):
-    """Returns idx [B, H_kv, N, K_sel] int32 (and leaf_score, s2 if asked)."""
+                        scoring: int | str = 0, s2: torch.Tensor | None = None):
+    """Returns idx [B, H_kv, N, K_sel] int32 (and leaf_score, s2 if asked).  An s2 tensor passed in
+    receives the level-2 survivors without being returned."""
     B, N, H_q, d, H_kv = _select_inputs(Q, K, P)
     shape = make_shape(B, N, H_q, H_kv, d, N)
     params = make_params(K_sel, causal, scale, scoring=scoring)
@@ -217,7 +244,9 @@ def pisa_select_prefill(Q, K, P, K_sel: int, causal: bool = True, scale: float =
         idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
     _expect(idx, "idx", (B, H_kv, N, K_sel), torch.int32, Q.device)
     score = torch.empty(B, H_kv, N, 2 * K_sel, dtype=torch.float32, device=Q.device) if want_scores else None
-    s2 = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device) if want_s2 else None
+    if want_s2:
+        s2 = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
+    _expect(s2, "s2", (B, H_kv, N, K_sel), torch.int32, Q.device)
     _check(lib().pisa_select_prefill(_ptr(Q), _ptr(K), _ptr(P), _ptr(idx), _ptr(score), _ptr(s2), _ptr(ws),
                                      ws.numel(), shape, params, _stream(Q)), "pisa_select_prefill")
     out = [idx]

@@ -2,8 +2,10 @@
 // carving, per-device state and the launch sequence of each entry point.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "../../include/pisa.h"
 #include "kernels.cuh"
@@ -70,6 +72,100 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_dev[MAX_DEVICES];
+
+// ---- per-phase device time (profiling aid) ------------------------------------------------
+// While enabled, each entry point records a CUDA event on its stream at the start of its work
+// and after each kernel phase; pisa_phase_times() resolves the events and sums the phases.
+enum Phase { PH_PYRAMID, PH_STAGE1, PH_CLUSTER, PH_LEAF_LSE, PH_TOPK, PH_ATTN, PH_BSA, PH_DECODE, PH_BACKWARD, NPHASE };
+const char* const PHASE_NAMES[NPHASE] = {"pyramid", "stage1", "cluster", "leaf_lse", "topk",
+                                         "sparse_attn", "bsa_select", "decode", "attn_backward"};
+
+std::atomic<bool> g_timing{false};
+
+struct PhaseRec {
+  int phase;
+  cudaEvent_t a, b;
+  bool own_a;  // a opens a chain (else it is the previous record's b)
+};
+struct PhaseLog {
+  std::vector<cudaEvent_t> pool;
+  std::vector<PhaseRec> pending;
+  double ms[NPHASE] = {};
+  long long count[NPHASE] = {};
+};
+PhaseLog g_phase[MAX_DEVICES];  // guarded by g_mutex
+
+cudaEvent_t take_event(PhaseLog& log) {
+  if (!log.pool.empty()) {
+    cudaEvent_t e = log.pool.back();
+    log.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+}
+
+// Records the phases of one entry point's launch sequence on one stream (a no-op unless
+// timing is enabled).
+class PhaseTimer {
+ public:
+  explicit PhaseTimer(cudaStream_t s) : s_(s) {
+    if (!g_timing.load(std::memory_order_relaxed)) return;
+    if (cudaGetDevice(&dev_) != cudaSuccess || dev_ < 0 || dev_ >= MAX_DEVICES) return;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    last_ = take_event(g_phase[dev_]);
+    if (last_ && cudaEventRecord(last_, s_) != cudaSuccess) {
+      g_phase[dev_].pool.push_back(last_);
+      last_ = nullptr;
+    }
+  }
+  void mark(int phase) {
+    if (!last_) return;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    PhaseLog& log = g_phase[dev_];
+    cudaEvent_t e = take_event(log);
+    if (!e) return;
+    if (cudaEventRecord(e, s_) != cudaSuccess) {
+      log.pool.push_back(e);
+      return;
+    }
+    log.pending.push_back(PhaseRec{phase, last_, e, first_});
+    first_ = false;
+    last_ = e;
+  }
+  ~PhaseTimer() {
+    if (last_ && first_) {  // opened but no phase recorded: return the start event
+      std::lock_guard<std::mutex> lock(g_mutex);
+      g_phase[dev_].pool.push_back(last_);
+    }
+  }
+
+ private:
+  cudaStream_t s_;
+  int dev_ = -1;
+  cudaEvent_t last_ = nullptr;
+  bool first_ = true;
+};
+
+// Waits for the pending records of device dev and adds them to its totals (g_mutex held).
+bool resolve_phases(PhaseLog& log) {
+  bool ok = true;
+  for (const PhaseRec& r : log.pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      ok = false;
+      continue;
+    }
+    log.ms[r.phase] += ms;
+    log.count[r.phase] += 1;
+  }
+  for (const PhaseRec& r : log.pending) {
+    log.pool.push_back(r.b);
+    if (r.own_a) log.pool.push_back(r.a);
+  }
+  log.pending.clear();
+  return ok;
+}
 
 // Per-device set-up, done once per device with that device current.
 pisa_status device_state(DeviceState** out) {
@@ -249,11 +345,16 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   cb.tiles = reinterpret_cast<int4*>(w + L.tiles);
   cb.totals = reinterpret_cast<int32_t*>(w + L.totals);
   const Geometry geo = make_geometry(p.N, p.N);
+  PhaseTimer tm(s);
   if (cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * cb.nkeys, s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_stage1(Q, P, S2, cb, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
+  tm.mark(PH_STAGE1);
   if (launch_cluster(S2, cb, p, s) != cudaSuccess) return PISA_ERR_CUDA;
+  tm.mark(PH_CLUSTER);
   if (launch_leaf_lse(Q, K, cb, score, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
+  tm.mark(PH_LEAF_LSE);
   if (launch_topk(S2, score, idx, p, geo, st->num_sms, s) != cudaSuccess) return PISA_ERR_CUDA;
+  tm.mark(PH_TOPK);
   return PISA_OK;
 }
 
@@ -318,7 +419,10 @@ pisa_status pisa_build_pyramid(const uint16_t* K, uint16_t* P, pisa_shape shape,
   if (p.B == 0 || p.N == 0) return PISA_OK;
   if (!K || !P || !aligned16(K) || !aligned16(P)) return PISA_ERR_INVALID_ARG;
   const Geometry geo = make_geometry(p.N, p.N_cap);
-  return cuda_status(launch_pyramid(K, P, p, geo, static_cast<cudaStream_t>(stream)));
+  PhaseTimer tm(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_pyramid(K, P, p, geo, static_cast<cudaStream_t>(stream));
+  tm.mark(PH_PYRAMID);
+  return cuda_status(e);
 }
 
 pisa_status pisa_select_prefill(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx,
@@ -349,7 +453,10 @@ pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t* K, const
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(idx)) return PISA_ERR_INVALID_ARG;
   DeviceState* st;
   if ((rc = device_state(&st)) != PISA_OK) return rc;
-  return cuda_status(launch_sparse_attn(Q, K, V, idx, O, LSE, p, st->num_sms, st->err, static_cast<cudaStream_t>(stream)));
+  PhaseTimer tm(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_sparse_attn(Q, K, V, idx, O, LSE, p, st->num_sms, st->err, static_cast<cudaStream_t>(stream));
+  tm.mark(PH_ATTN);
+  return cuda_status(e);
 }
 
 size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params) {
@@ -374,8 +481,11 @@ pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, cons
   if (ws_bytes < attn_backward_workspace_bytes(p)) return PISA_ERR_WORKSPACE;
   DeviceState* st;
   if ((rc = device_state(&st)) != PISA_OK) return rc;
-  return cuda_status(launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms,
-                                          static_cast<cudaStream_t>(stream)));
+  PhaseTimer tm(static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms,
+                                             static_cast<cudaStream_t>(stream));
+  tm.mark(PH_BACKWARD);
+  return cuda_status(e);
 }
 
 int pisa_prefill_host_chunks(long long N, long long* bounds, int max_bounds) {
@@ -538,8 +648,11 @@ pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_
   DeviceState* st;
   if ((rc = device_state(&st)) != PISA_OK) return rc;
   const Geometry geo_cap = make_geometry(p.N_cap, p.N_cap);
-  return cuda_status(
-      launch_decode(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, st->err, static_cast<cudaStream_t>(stream)));
+  PhaseTimer tm(static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_decode(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, st->err, static_cast<cudaStream_t>(stream));
+  tm.mark(PH_DECODE);
+  return cuda_status(e);
 }
 
 const char* pisa_status_string(pisa_status status) {
@@ -570,6 +683,35 @@ pisa_status pisa_get_last_device_error(pisa_stream stream) {
   if (word & ERR_BAD_INDEX) return PISA_ERR_BAD_INDEX;
   return PISA_OK;
 }
+
+pisa_status pisa_phase_timing(int enable) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PISA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  PhaseLog& log = g_phase[dev];
+  const bool ok = resolve_phases(log);
+  for (int i = 0; i < NPHASE; ++i) {
+    log.ms[i] = 0.0;
+    log.count[i] = 0;
+  }
+  g_timing.store(enable != 0);
+  return ok ? PISA_OK : PISA_ERR_CUDA;
+}
+
+int pisa_phase_times(double* ms, long long* count, int n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return -1;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  PhaseLog& log = g_phase[dev];
+  if (!resolve_phases(log)) return -1;
+  for (int i = 0; i < n && i < NPHASE; ++i) {
+    if (ms) ms[i] = log.ms[i];
+    if (count) count[i] = log.count[i];
+  }
+  return NPHASE;
+}
+
+const char* pisa_phase_name(int phase) { return phase >= 0 && phase < NPHASE ? PHASE_NAMES[phase] : nullptr; }
 
 const char* pisa_version(void) { return "pisa-gb300 0.1 (sm_103a)"; }
 

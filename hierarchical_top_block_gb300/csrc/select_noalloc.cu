@@ -4,8 +4,8 @@
 // lists and tiles) that the caller allocates.  Some callers cannot do that: code running
 // under a memory pool they do not own, plugins of a host that hands out no allocator, or
 // code that must not call cudaMalloc between setup and a latency-critical loop.  For them
-// this file keeps one fixed scratch array in device global memory, sized at load time, and
-// runs the same selection kernels on it.
+// this file keeps one scratch array in device global memory, of fixed size (32 MiB) and
+// reserved when the module loads on a device, and runs the same selection kernels on it.
 //
 // Facts a caller has to know:
 //   - The array is SCRATCH_BYTES (32 MiB) on every GPU that loads this library, held until
@@ -53,7 +53,9 @@ extern "C" pisa_status pisa_select_prefill_noalloc(const uint16_t* Q, const uint
                                                    int32_t* idx, float* leaf_score, int32_t* s2, pisa_shape shape,
                                                    pisa_params params, pisa_stream stream) {
   const size_t need = pisa_select_workspace_bytes(shape, params);
-  if (need == 0 && (long long)shape.B * shape.N > 0) return PISA_ERR_UNSUPPORTED;
+  // no workspace size (an argument the selection refuses: it returns its own status before
+  // launching anything) or an empty problem (a no-op that touches no device)
+  if (need == 0 || (long long)shape.B * shape.N <= 0) return pisa_select_prefill(Q, K, P, idx, leaf_score, s2, nullptr, 0, shape, params, stream);
   if (need > SCRATCH_BYTES) return PISA_ERR_WORKSPACE;
   void* ws = nullptr;
   pisa_status rc = scratch_address(&ws);

@@ -7,11 +7,12 @@
 // The G_Q heads of one query share the selected blocks, so one warp owns one query: its
 // G_Q rows (padded to 16) form the M = 16 side of m16n8k16 MMAs; different queries
 // select different blocks, so there is no larger dense tile without wasted work.  The
-// kernel is bound by moving the selected K/V blocks into the SM.  Each of the 8 warps of a
-// CTA runs its own ring of 3 shared-memory slots filled by TMA (one 4-D box per 32-key
-// half block: rows x both 64-column halves of d, 128-byte swizzle, rows past N read as
-// zero); the ring keeps two loads in flight ahead of the one being multiplied, across
-// block and query boundaries, and skips half blocks that hold no visible key.
+// kernel is bound by moving the selected K/V blocks into the SM.  Each warp of a CTA (12
+// warps at d = 128, 16 at d = 64) runs its own ring of shared-memory slots (2 at d = 128,
+// 3 at d = 64) filled by TMA (one 4-D box per 32-key half block: rows x both 64-column
+// halves of d, 128-byte swizzle, rows past N read as zero); the ring keeps the next loads in
+// flight while the current slot is multiplied, across block and query boundaries, and
+// skips half blocks that hold no visible key.
 // S = Q K^T and O += P V use ldmatrix (.trans for V) on the swizzled slots; the softmax is
 // online in the exp2 domain against a lazy reference maximum per row: exact on the first half
 // block, then moved (and O and the running sum rescaled) only when a logit passes it by more

@@ -216,6 +216,23 @@ PISA_API const char* pisa_status_string(pisa_status status);
  * range, PISA_OK otherwise (PISA_ERR_CUDA if the CUDA calls themselves fail). */
 PISA_API pisa_status pisa_get_last_device_error(pisa_stream stream);
 
+/* ---- per-phase device time (a profiling aid; the paper has no counterpart) --------------- */
+
+/* While enabled, every compute entry point records a CUDA event on its stream when its work
+ * starts and after each of its kernel phases: pyramid, Stage 1 (with the clustering histogram),
+ * clustering, Stage 2 leaf LSE, top-K, sparse attention, BSA selection, decode step, attention
+ * backward.  The records cost a few microseconds per call and add no ordering beyond the
+ * stream's own.  Events are recorded on the device current at the call.
+ * pisa_phase_timing(1) enables recording and clears the current device's totals; (0) disables
+ * it (the totals are kept).  Returns PISA_ERR_CUDA if resolving earlier records failed.
+ * pisa_phase_times waits for the current device's recorded events and writes, for each phase
+ * i < n, the total milliseconds into ms[i] and the number of timed launches into count[i]
+ * (either may be NULL).  Returns the number of phases, or -1 on a CUDA error.
+ * pisa_phase_name returns a phase's name ("stage1", ...), or NULL past the last phase. */
+PISA_API pisa_status pisa_phase_timing(int enable);
+PISA_API int pisa_phase_times(double* ms, long long* count, int n);
+PISA_API const char* pisa_phase_name(int phase);
+
 /* Library version string. */
 PISA_API const char* pisa_version(void);
 

@@ -149,6 +149,12 @@ def test_parameter_rules(lib):
         (sel(shape(), pisa.make_params(16, g=4)), 2),
         (sel(shape(), p16, ws=ct.c_void_p((1 << 20) + 16)), 1),          # ws must be 256-byte aligned
         (sel(shape(), p16, Q=ct.c_void_p((1 << 20) + 2)), 1),            # tensors 16-byte aligned
+        # the allocation-free selection reports the same statuses as the workspace one
+        (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(H_q=12, H_kv=8), p16, None), 1),
+        (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(),
+                                         pisa.pisa_params(64, 2, 16, 2, 0.0, 0), None), 1),
+        (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(), pisa.make_params(17), None), 2),
+        (lib.pisa_select_prefill_noalloc(None, None, None, None, None, None, shape(B=0), p16, None), 0),
         (lib.pisa_sparse_attn_prefill(fake, fake, fake, fake, fake, None, shape(N_cap=100), p16, None), 1),
         (lib.pisa_sparse_attn_prefill(fake, fake, fake, ct.c_void_p((1 << 20) + 4), fake, None, shape(), p16, None), 1),
         (lib.pisa_decode_step(*([fake] * 10), shape(N=0, N_cap=0), p16, None), 1),

@@ -75,3 +75,44 @@ def test_a_failing_section_is_reported_not_fatal():
         raise RuntimeError(f"device error word {x}")
     assert bench.section(boom, 5) == {"error": "RuntimeError: device error word 5"}
     assert bench.section(lambda a, b=0: a + b, 1, b=2) == 3
+
+
+def test_work_counts():
+    """The algorithmic work the per-kernel rooflines divide by: decode bytes count the selected
+    blocks' keys once (they are among the 2K candidate leaves), the walk's child rows follow
+    the level geometry, and Stage 2's flops count the visible keys of each eligible leaf child."""
+    w = W.WORKLOADS["decode_128k"]
+    # 131073 tokens: 7 scored levels x 64 child rows, 32 candidate leaves of keys, 16 of values
+    assert bench.decode_hbm_bytes(w) == 64 * 8 * (7 * 64 + 32 * 64 + 16 * 64) * 128 * 2
+    assert bench.level_sizes(262144) == [4096 >> i for i in range(13)]
+    assert bench.level_sizes(65) == [2, 1] and bench.level_sizes(0) == []
+    r = bench.stage1_work(262144, 16, 1, 128, 16)
+    # the last query scores levels 8..2 (32 candidates each, 64 child rows): 448 rows; the
+    # first 17 * 64 queries see at most 16 leaves, and no level is scored
+    assert bench.stage1_work(64 * 17, 16, 1, 128, 16)["child_rows"] == 0
+    assert r["child_rows"] <= 448 * 262144 and r["flops"] == 2.0 * 128 * 16 * r["child_rows"]
+    tail = bench.stage1_work(262144, 16, 1, 128, 16)["child_rows"] - bench.stage1_work(262143, 16, 1, 128, 16)["child_rows"]
+    assert tail == 448
+    s2 = torch.full((1, 1, 200, 2), -1, dtype=torch.int32)
+    s2[0, 0, 10, 0] = 0      # t = 10: leaf 0 holds keys 0..10 visible, leaf 1 none
+    s2[0, 0, 199, 0] = 1     # t = 199: leaf 2 keys 128..199 -> 64 visible, leaf 3 (key 192..) 8 visible
+    got = bench.leaf_lse_work(s2, 200, 8, 2, 64)
+    assert got["visible_keys"] == 11 + 64 + 8 and got["flops"] == 2.0 * 64 * 4 * (11 + 64 + 8)
+
+
+def test_phase_rooflines_fields(monkeypatch):
+    times = {"pyramid": (0.1, 2), "stage1": (4.0, 2), "cluster": (0.2, 2), "leaf_lse": (5.0, 2), "topk": (0.3, 2),
+             "sparse_attn": (16.0, 2), "bsa_select": (0.0, 0), "decode": (0.0, 0), "attn_backward": (0.0, 0)}
+    state = []
+    monkeypatch.setattr(pisa, "pisa_phase_timing", lambda on=True: state.append(on))
+    monkeypatch.setattr(pisa, "pisa_phase_times", lambda: times)
+    _no_device(monkeypatch)
+    steps = []
+    w = W.WORKLOADS["tiny"]
+    s2 = torch.zeros(w.B, w.H_kv, w.N, w.K, dtype=torch.int32)
+    res = bench.phase_rooflines(w, lambda: steps.append(1), s2, attn_flops=1e9, steps=2)
+    assert state == [True, False] and len(steps) == 2
+    assert set(res) >= {"pyramid", "stage1", "cluster", "leaf_lse", "topk", "sparse_attn"}
+    assert res["stage1"]["ms"] == 2.0 and res["stage1"]["bound"] == "hbm" and res["leaf_lse"]["bound"] == "tensor"
+    a = res["sparse_attn"]
+    assert abs(a["achieved"] - 1e9 / 8e-3 / 1e12) < 1e-12 and abs(a["frac"] - a["achieved"] / a["peak"]) < 1e-12
