@@ -74,6 +74,8 @@ class Oracle:
         L.oracle_decode_step.restype = _I
         L.oracle_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _P, _P,
                                          _P, _I, _I]
+        L.oracle_select_bsa.restype = _I
+        L.oracle_select_bsa.argtypes = [_P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _I, _P, _P, _P, _P, _I]
         L.oracle_f64_to_bf16.restype = ct.c_uint16
         L.oracle_f64_to_bf16.argtypes = [_D]
 
@@ -122,6 +124,29 @@ class Oracle:
                                     int(scoring))
         assert rc == 0, rc
         return dict(idx=idx, s2=s2, cand=cand, cand_score=cs, min_gap=gap)
+
+    def select_bsa(self, Q, P, Ksel, rows, C=64, g=2, causal=True, scale=None, want_scores=False):
+        """BSA flat selection (one level of mean summaries, head-summed dot products, top-K):
+        Q uint16 [B,N,H_q,d]; P [B,H_kv,nodes,d] (level 1 = the leaf means); rows int64 [R,3].
+        Returns idx [R,K], min_gap [R] and, if asked, score [R,M_1] (-inf where not ranked)."""
+        B, N, H_q, d = Q.shape
+        H_kv = P.shape[1]
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        rows = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+        R = rows.shape[0]
+        M1 = (N + C - 1) // C
+        idx = np.zeros((R, Ksel), np.int32)
+        gap = np.zeros(R, np.float64)
+        score = np.zeros((R, M1), np.float64) if want_scores else None
+        rc = self.lib.oracle_select_bsa(_ptr(np.ascontiguousarray(Q, dtype=np.uint16)),
+                                        _ptr(np.ascontiguousarray(P, dtype=np.uint16)), B, N, H_q, H_kv, d, C, g, Ksel,
+                                        int(causal), scale, R, _ptr(rows), _ptr(idx), _ptr(score), _ptr(gap),
+                                        self.nthreads)
+        assert rc == 0, rc
+        out = dict(idx=idx, min_gap=gap)
+        if want_scores:
+            out["score"] = score
+        return out
 
     def admissible(self, Q, K, P, Ksel, rows, target_idx, tol=1e-3, C=64, g=2, causal=True, scale=None, scoring=0):
         B, N, H_q, d = Q.shape

@@ -423,6 +423,47 @@ int admissible_walk(const Row& R, int l, const std::vector<long long>& S, const 
   return 0;
 }
 
+// ---------------------------------------------------------------------------------------
+// BSA flat selection, the single-level baseline PISA is compared with (summary page,
+// "Prerequisites": block sparse attention keeps K blocks per query, chosen by the dot
+// product of the query with each block's summary, q . kbar_i / sqrt(d), over all
+// M = ceil(N / C) blocks; GQA: the group's heads share one selected set, their scores summed).
+// Readings: the summaries are the mean-pooled level-1 nodes of the pyramid (eqs 10-15);
+// causal eligibility, the forced own block and the tie rule are those of the PISA walk
+// (R2, R5, R6).
+// ---------------------------------------------------------------------------------------
+struct BsaSelection {
+  std::vector<long long> final_set;   // ascending
+  std::vector<double> score;          // per leaf: head-summed score, -inf if not ranked
+  double min_gap = POS_INF;           // K-th / (K+1)-th gap of the ranked blocks
+};
+
+BsaSelection select_bsa_row(const Row& R) {
+  BsaSelection out;
+  if (R.lv.L == 0) return out;
+  const long long M1 = R.lv.M[1];
+  out.score.assign((size_t)M1, NEG_INF);
+  const long long own = R.causal ? R.t / R.C : -1;
+  std::vector<long long> ids;
+  std::vector<double> sc;
+  for (long long j = 0; j < M1; ++j) {
+    if (!eligible(R, 1, j) || j == own) continue;
+    double u = 0;
+    for (int h = 0; h < R.GQ; ++h) u += R.scale * dot_node(R, h, 1, j);
+    ids.push_back(j);
+    sc.push_back(u);
+    out.score[(size_t)j] = u;
+  }
+  double gap;
+  const int keep = R.causal ? R.K - 1 : R.K;  // the own block takes one of the K places
+  std::vector<long long> ranked = topk(ids, sc, keep, &gap);
+  out.min_gap = gap;
+  if (R.causal) ranked.push_back(own);
+  std::sort(ranked.begin(), ranked.end());
+  out.final_set = ranked;
+  return out;
+}
+
 Row make_row(const uint16_t* Q_row /* GQ x d for this (b, t, group) */, const uint16_t* Kbg, const uint16_t* Pbg,
              const std::vector<long long>* off, long long n, long long t, int d, int C, int g, int K, int GQ,
              int causal, double scale, int scoring) {
@@ -600,6 +641,37 @@ int oracle_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int B
         for (int i = 0; i < g * Ksel; ++i) cand[r * g * Ksel + i] = (int32_t)S.cand[i];
       if (cand_score)
         for (int i = 0; i < g * Ksel; ++i) cand_score[r * g * Ksel + i] = S.cand_score[i];
+      if (min_gap) min_gap[r] = S.min_gap;
+    }
+  });
+  return bad.load();
+}
+
+// BSA flat selection for the given rows (b, h_kv, t): idx [nrows][K] (ascending, -1 padded),
+// score [nrows][M_1] nullable (head-summed score of every ranked block, -inf for blocks not
+// ranked: ineligible, or the forced own block), min_gap [nrows] nullable.
+int oracle_select_bsa(const uint16_t* Q, const uint16_t* P, int B, long long N, int H_q, int H_kv, int d, int C, int g,
+                      int Ksel, int causal, double scale, int nrows, const long long* rows, int32_t* idx,
+                      double* score, double* min_gap, int nthreads) {
+  if (H_kv <= 0 || H_q % H_kv != 0 || Ksel < 1) return 1;
+  const int GQ = H_q / H_kv;
+  std::vector<long long> off = level_offsets(N, C, g);
+  const long long nodes = oracle_pyramid_nodes(N, C, g);
+  const long long M1 = N > 0 ? (N + C - 1) / C : 0;
+  std::atomic<int> bad(0);
+  run_parallel(nrows, nthreads, [&](long long a, long long e) {
+    for (long long r = a; r < e; ++r) {
+      long long b = rows[3 * r], hk = rows[3 * r + 1], t = rows[3 * r + 2];
+      if (b < 0 || b >= B || hk < 0 || hk >= H_kv || t < 0 || t >= N) {
+        bad = 1;
+        continue;
+      }
+      const uint16_t* qrow = Q + ((b * N + t) * H_q + hk * GQ) * d;
+      Row R = make_row(qrow, nullptr, P + (b * H_kv + hk) * nodes * d, &off, N, t, d, C, g, Ksel, GQ, causal, scale, 0);
+      BsaSelection S = select_bsa_row(R);
+      for (int i = 0; i < Ksel; ++i) idx[r * Ksel + i] = i < (int)S.final_set.size() ? (int32_t)S.final_set[i] : -1;
+      if (score)
+        for (long long j = 0; j < M1; ++j) score[r * M1 + j] = S.score[(size_t)j];
       if (min_gap) min_gap[r] = S.min_gap;
     }
   });

@@ -736,6 +736,111 @@ def pin_decode_scoring_variants(o):
     for scoring in (1, 2):
         assert any(not np.array_equal(a, b) for a, b in zip(picks[0], picks[scoring])), scoring
 
+
+# ------------------------------------------------------------------------------------
+# BSA flat selection (the single-level baseline of the paper's selection-speed figure)
+# ------------------------------------------------------------------------------------
+def _bsa_constant_blocks(c, d=16, lanes=(0,)):
+    """Keys of block j all equal to sum over lane e of c[e][j] * unit vector e (bf16-exact), so
+    the block's mean summary is exactly that vector."""
+    M = len(c[0])
+    K = np.zeros((1, 1, 64 * M, d), np.float32)
+    for e, ce in zip(lanes, c):
+        for j in range(M):
+            K[0, 0, 64 * j:64 * (j + 1), e] = ce[j]
+    return f2b(K)
+
+
+def pin_bsa_closed_form(o):
+    """Blocks of constant keys c_j along one axis and queries along that axis: every BSA score is
+    G_Q * scale * (q . axis) * c_j, so the selection is the own block plus the K - 1 largest (or,
+    for a negative query, smallest) c_j among the earlier blocks; a second head on another axis
+    enters the head sum and changes the ranking."""
+    c = [3.0, -1.0, 5.0, 2.0, 7.0, 0.5, 4.0, 6.0]
+    d, N = 16, 64 * 8
+    K = _bsa_constant_blocks([c], d)
+    P = o.build_pyramid(K)
+    Q = np.zeros((1, N, 1, d), np.float32)
+    Q[0, :, 0, 0] = 1.0
+    Qp = f2b(Q)
+    rows = np.array([(0, 0, t) for t in (511, 200, 64, 10)], np.int64)
+    r = o.select_bsa(Qp, P, 3, rows, want_scores=True)
+    assert [list(x) for x in r["idx"]] == [[2, 4, 7], [0, 2, 3], [0, 1, -1], [0, -1, -1]], r["idx"]
+    assert abs(r["score"][0, 4] - 7.0 / 4.0) < 1e-12 and np.isneginf(r["score"][0, 7])   # own block not ranked
+    assert abs(r["min_gap"][0] - (5.0 - 4.0) / 4.0) < 1e-12
+    nc = o.select_bsa(Qp, P, 3, np.array([[0, 0, 0]]), causal=False)
+    assert list(nc["idx"][0]) == [2, 4, 7], nc["idx"]
+    Q[0, :, 0, 0] = -1.0
+    neg = o.select_bsa(f2b(Q), P, 3, rows[:1])
+    assert list(neg["idx"][0]) == [1, 5, 7], neg["idx"]
+    # two heads: head 0 along axis 0 (weight 2), head 1 along axis 1; block j's keys are
+    # c_j on axis 0 and b_j on axis 1, so the head sum ranks by 2 c_j + b_j
+    b = [9.0, 0.0, -6.0, 0.0, -8.0, 0.0, 0.0, 0.0]
+    K2 = _bsa_constant_blocks([c, b], d, lanes=(0, 1))
+    P2 = o.build_pyramid(K2)
+    Q2 = np.zeros((1, N, 2, d), np.float32)
+    Q2[0, :, 0, 0] = 2.0
+    Q2[0, :, 1, 1] = 1.0
+    r2 = o.select_bsa(f2b(Q2), P2, 3, rows[:1])
+    # 2c + b over blocks 0..6: 15, -2, 4, 4, 6, 1, 8 -> the best two are 0 and 6
+    assert list(r2["idx"][0]) == [0, 6, 7], r2["idx"]
+    # identical blocks: every score ties and the lower indices win
+    Kt = _bsa_constant_blocks([[2.0] * 8], d)
+    rt = o.select_bsa(Qp, o.build_pyramid(Kt), 3, rows)
+    assert [list(x) for x in rt["idx"]] == [[0, 1, 7], [0, 1, 3], [0, 1, -1], [0, -1, -1]], rt["idx"]
+
+
+def _bsa_exact_mean_inputs(seed, N, H_q, H_kv=1, d=32):
+    """Keys whose block means are exact bf16 values: each block holds an offset o_j and
+    pairs of keys o_j + r, o_j - r (all multiples of 1/64 below 4 in magnitude, exact in bf16),
+    so the fp64 mean over any complete block, and its bf16 summary, equal o_j exactly."""
+    rng = np.random.default_rng(seed)
+    M1 = (N + 63) // 64
+    o_ = rng.integers(-64, 65, size=(1, H_kv, M1, d)) / 64.0
+    r = rng.integers(-60, 61, size=(1, H_kv, M1, 32, d)) / 64.0
+    blk = np.concatenate([o_[:, :, :, None, :] + r, o_[:, :, :, None, :] - r], axis=3)   # [.., M1, 64, d]
+    K = blk.reshape(1, H_kv, M1 * 64, d)[:, :, :N].astype(np.float32)
+    Q = (rng.integers(-64, 65, size=(1, N, H_q, d)) / 32.0).astype(np.float32)
+    return f2b(Q), f2b(K)
+
+
+def pin_bsa_equals_pisa1_leaf_ranking(o):
+    """PISA-1 scores a leaf by log m + mean of its m visible logits = log m + scale q . mean(k)
+    (summary page, "Core method": mean scoring is the first-order truncation of the LSE); with
+    no pruning (M_1 <= g K every eligible leaf is a candidate) and full blocks (every ranked
+    block in causal mode ends before the query), PISA-1 ranks exactly by BSA's q . kbar.  With
+    keys whose block means are exact in bf16 the two selections must be identical."""
+    for (N, H_q, H_kv, Ksel, causal) in ((1024, 4, 1, 8, True), (64 * 12, 2, 2, 7, True), (64 * 11 + 64, 4, 1, 6, False)):
+        Q, K = _bsa_exact_mean_inputs(7 + N, N, H_q, H_kv)
+        P = o.build_pyramid(K)
+        M1 = (N + 63) // 64
+        assert M1 <= 2 * Ksel
+        rows = np.array([(0, g, t) for g in range(H_kv) for t in range(0, N, 5)], np.int64)
+        b = o.select_bsa(Q, P, Ksel, rows, causal=causal)
+        p1 = o.select(Q, K, P, Ksel, rows, causal=causal, scoring=1)
+        ok = (b["min_gap"] > 1e-9) & (p1["min_gap"] > 1e-9)
+        assert ok.mean() > 0.95, ok.mean()
+        assert np.array_equal(b["idx"][ok], p1["idx"][ok]), (N, np.where(~np.all(b["idx"] == p1["idx"], 1))[0][:3])
+
+
+def pin_bsa_invariants(o):
+    """Final sets ascending, unique, -1 padded at the end, own block present and every block
+    eligible (causal); |I_t| = min(K, #eligible); K >= M_1 selects every eligible block."""
+    Q, K, V = _tiny_inputs(seed=23)
+    P = o.build_pyramid(K)
+    N = Q.shape[1]
+    rows = np.array([(0, 0, t) for t in range(N)], np.int64)
+    for Ksel in (1, 5, 16):
+        r = o.select_bsa(Q, P, Ksel, rows)
+        for t in range(N):
+            row = list(r["idx"][t])
+            val = [x for x in row if x >= 0]
+            assert row == val + [-1] * (Ksel - len(val))
+            assert val == sorted(set(val)) and t // 64 in val and all(x * 64 <= t for x in val)
+            assert len(val) == min(Ksel, t // 64 + 1)
+            if Ksel >= 16:
+                assert val == list(range(t // 64 + 1))
+
 ALL_PINS = [
     pin_level_sizes, pin_bf16_rounding, pin_pyramid_constant_keys, pin_pyramid_raw_mean,
     pin_pyramid_ragged_leaf_mean, pin_leaf_lse_closed_forms, pin_gqa_head_sum, pin_lse_beats_mean,
@@ -744,5 +849,5 @@ ALL_PINS = [
     pin_single_block_at_start, pin_decode, pin_decode_scoring_variants,
     pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,
     pin_backward_dense_autograd, pin_backward_dense_autograd_noncausal, pin_backward_finite_differences,
-    pin_backward_sums,
+    pin_backward_sums, pin_bsa_closed_form, pin_bsa_equals_pisa1_leaf_ranking, pin_bsa_invariants,
 ]

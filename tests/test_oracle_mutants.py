@@ -100,6 +100,21 @@ MUTANTS["head_sum_drops_heads"] = [
 ]
 
 
+# the BSA flat selection (the baseline of the selection-speed comparison)
+MUTANTS["bsa_sign_flipped"] = [("    for (int h = 0; h < R.GQ; ++h) u += R.scale * dot_node(R, h, 1, j);",
+                                "    for (int h = 0; h < R.GQ; ++h) u -= R.scale * dot_node(R, h, 1, j);")]
+MUTANTS["bsa_level2_summaries"] = [("    for (int h = 0; h < R.GQ; ++h) u += R.scale * dot_node(R, h, 1, j);",
+                                    "    for (int h = 0; h < R.GQ; ++h) u += R.scale * dot_node(R, h, 2, j / 2);")]
+MUTANTS["bsa_first_head_only"] = [("    for (int h = 0; h < R.GQ; ++h) u += R.scale * dot_node(R, h, 1, j);",
+                                   "    for (int h = 0; h < 1; ++h) u += R.scale * dot_node(R, h, 1, j);")]
+MUTANTS["bsa_own_not_forced"] = [("    if (!eligible(R, 1, j) || j == own) continue;", "    if (!eligible(R, 1, j)) continue;"),
+                                 ("  const int keep = R.causal ? R.K - 1 : R.K;", "  const int keep = R.K;"),
+                                 ("  if (R.causal) ranked.push_back(own);", "")]
+MUTANTS["bsa_ignores_causal"] = [("    if (!eligible(R, 1, j) || j == own) continue;", "    if (j == own) continue;")]
+MUTANTS["bsa_ties_to_higher_index"] = [("    double u = 0;\n    for (int h = 0; h < R.GQ; ++h) u += R.scale",
+                                        "    double u = 1e-12 * j;\n    for (int h = 0; h < R.GQ; ++h) u += R.scale")]
+
+
 @pytest.fixture(scope="module")
 def mutant_dir():
     with tempfile.TemporaryDirectory() as d:
