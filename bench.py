@@ -416,6 +416,7 @@ def run_pisa(args):
                 "prefill_32k_k8": section(secondary_prefill, W.WORKLOADS["prefill_32k"], dev, K_sel=8),
                 "prefill_256k_k8": section(secondary_prefill, W.WORKLOADS["prefill_256k"], dev, K_sel=8),
                 "decode_128k": section(secondary_decode, W.WORKLOADS["decode_128k"], dev),
+                "bsa_vs_pisa_selection": section(bsa_vs_pisa_section, dev),
                 "selection_quality_32k": section(selection_quality_section, W.WORKLOADS["prefill_32k"], dev)}
         out["cpu_baseline"] = None if args.no_cpu else cpu_baseline(args, w)
         print(json.dumps(out), flush=True)
@@ -571,6 +572,57 @@ def secondary_prefill(w, dev, steps=5, K_sel=None):
     return {"tokens_per_s": w.B * w.N / (ms * 1e-3), "ms_per_step": ms,
             "selection_tokens_per_s": w.B * w.N / (sel_ms * 1e-3), "select_ms": sel_ms,
             "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "K": Ks}
+
+
+def bsa_vs_pisa_section(dev, Ns=(4096, 16384, 65536, 131072, 262144), K_sel=8, steps=10):
+    """Block-selection latency of PISA (pyramid + pisa_select_prefill) and of the BSA flat
+    selection (pyramid + pisa_select_bsa) at the pages' Fig. 3 setting (C = 64, K = 8) on the
+    selection-scale shape (H_q = 16, H_kv = 1, d = 128), for N from 4K to 256K; the ratio
+    BSA / PISA is the speed-up the pages report (2.86x, 5.31x, 9.95x at 64K, 128K, 256K)."""
+    import torch
+
+    import hierarchical_top_block_gb300 as pisa
+    import workloads as W
+
+    base = W.WORKLOADS["prefill_256k"]
+    rows = []
+    for N in Ns:
+        w = base.with_(N=N)
+        Q, K, V = W.prefill_inputs(w, dev)
+        del V
+        P = pisa.pisa_build_pyramid(K)
+        shape = pisa.make_shape(w.B, N, w.H_q, w.H_kv, w.d)
+        ws = torch.empty(pisa.pisa_select_workspace_bytes(shape, pisa.make_params(K_sel)), dtype=torch.uint8, device=dev)
+        wb = torch.empty(pisa.pisa_select_bsa_workspace_bytes(shape, pisa.make_params(K_sel)), dtype=torch.uint8,
+                         device=dev)
+        idx = torch.empty(w.B, w.H_kv, N, K_sel, dtype=torch.int32, device=dev)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(steps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / steps
+
+        pyr = timed(lambda: pisa.pisa_build_pyramid(K, P=P))
+        pisa_ms = timed(lambda: (pisa.pisa_build_pyramid(K, P=P), pisa.pisa_select_prefill(Q, K, P, K_sel, ws=ws, idx=idx)))
+        bsa_ms = timed(lambda: (pisa.pisa_build_pyramid(K, P=P), pisa.pisa_select_bsa(Q, P, K_sel, ws=wb, idx=idx)))
+        if pisa.pisa_get_last_device_error() != 0:
+            raise RuntimeError("device error word set while timing the selections")
+        rows.append({"N": N, "pyramid_ms": pyr, "pisa_select_ms": pisa_ms, "bsa_select_ms": bsa_ms,
+                     "pisa_speedup_over_bsa": bsa_ms / pisa_ms})
+        del Q, K, P, ws, wb, idx
+        torch.cuda.empty_cache()
+    return {"K": K_sel, "C": 64, "H_q": base.H_q, "H_kv": base.H_kv, "d": base.d, "rows": rows,
+            "includes": "pyramid build in both selections",
+            "pages_pisa_speedup_over_bsa": {"65536": 2.86, "131072": 5.31, "262144": 9.95},
+            "note": ("BSA's mean-summary score is linear in q, so the group's head sum folds into one "
+                     "query vector: one d-length dot product per (query, block) on the tensor cores")}
 
 
 def selection_quality_section(w, dev, samples=96, seed=11):

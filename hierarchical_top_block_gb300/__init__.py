@@ -68,6 +68,10 @@ def lib() -> ct.CDLL:
         L.pisa_select_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, ct.c_size_t, pisa_shape, pisa_params, _P]
         L.pisa_select_prefill_noalloc.restype = ct.c_int
         L.pisa_select_prefill_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
+        L.pisa_select_bsa_workspace_bytes.restype = ct.c_size_t
+        L.pisa_select_bsa_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_select_bsa.restype = ct.c_int
+        L.pisa_select_bsa.argtypes = [_P, _P, _P, _P, ct.c_size_t, pisa_shape, pisa_params, _P]
         L.pisa_sparse_attn_prefill.restype = ct.c_int
         L.pisa_sparse_attn_prefill.argtypes = [_P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
         L.pisa_prefill_host.restype = ct.c_int
@@ -80,6 +84,8 @@ def lib() -> ct.CDLL:
         L.pisa_get_last_device_error.argtypes = [_P]
         L.pisa_version.restype = ct.c_char_p
         L.pisa_version.argtypes = []
+        L.pisa_check_wait_timeout.restype = ct.c_int
+        L.pisa_check_wait_timeout.argtypes = [ct.c_ulonglong, _P]
         L.pisa_phase_timing.restype = ct.c_int
         L.pisa_phase_timing.argtypes = [ct.c_int]
         L.pisa_phase_times.restype = ct.c_int
@@ -174,6 +180,13 @@ def pisa_status_string(status: int) -> str:
 
 def pisa_version() -> str:
     return lib().pisa_version().decode()
+
+
+def pisa_check_wait_timeout(limit_ns: int = 1_000_000, device=None) -> None:
+    """Launch the kernel whose bounded waits run out after limit_ns (see include/pisa.h)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    _check(lib().pisa_check_wait_timeout(int(limit_ns), ct.c_void_p(torch.cuda.current_stream(dev).cuda_stream)),
+           "pisa_check_wait_timeout")
 
 
 def pisa_phase_timing(enable: bool = True) -> None:
@@ -272,6 +285,32 @@ def pisa_select_prefill_noalloc(Q, K, P, K_sel: int, causal: bool = True, scale:
                                              make_shape(B, N, H_q, H_kv, d, N),
                                              make_params(K_sel, causal, scale, scoring=scoring),
                                              _stream(Q)), "pisa_select_prefill_noalloc")
+    return idx
+
+
+# ---- baseline: BSA flat selection --------------------------------------------------------
+def pisa_select_bsa_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
+    return int(lib().pisa_select_bsa_workspace_bytes(shape, params))
+
+
+def pisa_select_bsa(Q, P, K_sel: int, causal: bool = True, scale: float = 0.0, ws=None, idx=None):
+    """BSA flat selection from the leaf summaries of P: returns idx [B, H_kv, N, K_sel] int32."""
+    _bf16(Q, "Q", 4)
+    _bf16(P, "P", 4)
+    B, N, H_q, d = Q.shape
+    H_kv = P.shape[1]
+    _expect(P, "P", (B, H_kv, pisa_pyramid_nodes(N), d), torch.bfloat16, Q.device)
+    shape = make_shape(B, N, H_q, H_kv, d, N)
+    params = make_params(K_sel, causal, scale)
+    need = pisa_select_bsa_workspace_bytes(shape, params)
+    if need == 0 and B * N > 0:
+        raise PisaError(2, "pisa_select_bsa: unsupported shape or parameters")
+    ws = _workspace(ws, need, Q.device)
+    if idx is None:
+        idx = torch.empty(B, H_kv, N, K_sel, dtype=torch.int32, device=Q.device)
+    _expect(idx, "idx", (B, H_kv, N, K_sel), torch.int32, Q.device)
+    _check(lib().pisa_select_bsa(_ptr(Q), _ptr(P), _ptr(idx), _ptr(ws), ws.numel(), shape, params, _stream(Q)),
+           "pisa_select_bsa")
     return idx
 
 

@@ -459,6 +459,41 @@ pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t* K, const
   return cuda_status(e);
 }
 
+// The BSA selection's query parts are addressed with 32-bit TMA row coordinates
+// (B * H_kv * 2 * N rows) and the summary rows likewise (B * H_kv * nodes).
+bool bsa_fits(const Problem& p) {
+  const long long bh = (long long)p.B * p.H_kv;
+  return bh * 2 * p.N < (1LL << 31) && bh * pisa_pyramid_nodes(p.N, 64, 2) < (1LL << 31);
+}
+
+size_t pisa_select_bsa_workspace_bytes(pisa_shape shape, pisa_params params) {
+  Problem p;
+  if (check_params(shape, params, &p) != PISA_OK || !bsa_fits(p)) return 0;
+  return round_up(bsa_workspace_bytes(p), 256);
+}
+
+pisa_status pisa_select_bsa(const uint16_t* Q, const uint16_t* P, int32_t* idx, void* ws, size_t ws_bytes,
+                            pisa_shape shape, pisa_params params, pisa_stream stream) {
+  Problem p;
+  pisa_status rc = check_params(shape, params, &p);
+  if (rc != PISA_OK) return rc;
+  if (p.N_cap != p.N) return PISA_ERR_INVALID_ARG;
+  if (!bsa_fits(p)) return PISA_ERR_UNSUPPORTED;
+  if (p.B == 0 || p.N == 0) return PISA_OK;
+  if (!Q || !P || !idx || !ws) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(P) || !aligned16(idx) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return PISA_ERR_INVALID_ARG;
+  if (ws_bytes < bsa_workspace_bytes(p)) return PISA_ERR_WORKSPACE;
+  DeviceState* st;
+  if ((rc = device_state(&st)) != PISA_OK) return rc;
+  const Geometry geo = make_geometry(p.N, p.N);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PhaseTimer tm(s);
+  const cudaError_t e = launch_bsa_select(Q, P, idx, ws, p, geo, st->num_sms, st->err, s);
+  tm.mark(PH_BSA);
+  return cuda_status(e);
+}
+
 size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params) {
   Problem p;
   if (check_params(shape, params, &p) != PISA_OK || !entry_lists_fit(p)) return 0;
@@ -653,6 +688,14 @@ pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_
       launch_decode(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, st->err, static_cast<cudaStream_t>(stream));
   tm.mark(PH_DECODE);
   return cuda_status(e);
+}
+
+pisa_status pisa_check_wait_timeout(unsigned long long limit_ns, pisa_stream stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull) return PISA_ERR_INVALID_ARG;
+  DeviceState* st;
+  pisa_status rc = device_state(&st);
+  if (rc != PISA_OK) return rc;
+  return cuda_status(launch_wait_check(limit_ns, st->err, static_cast<cudaStream_t>(stream)));
 }
 
 const char* pisa_status_string(pisa_status status) {

@@ -52,6 +52,12 @@ cudaError_t launch_leaf_lse(const uint16_t* Q, const uint16_t* K, const ClusterB
 cudaError_t launch_topk(const int32_t* S2, float* leaf_score, int32_t* idx, const Problem& p,
                         const Geometry& geo, int num_sms, cudaStream_t s);
 
+// BSA flat selection: head-summed query parts into ws (bsa_workspace_bytes), then the scoring
+// GEMM with a per-query top-K over every eligible leaf summary; idx rows ascending, -1 padded.
+size_t bsa_workspace_bytes(const Problem& p);
+cudaError_t launch_bsa_select(const uint16_t* Q, const uint16_t* P, int32_t* idx, void* ws, const Problem& p,
+                              const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s);
+
 // Block-sparse attention over idx.
 cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
                                uint16_t* O, float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s);
@@ -66,6 +72,9 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
                           uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
                           const Problem& p, const Geometry& geo_cap, uint32_t* err, cudaStream_t s);
+
+// One CTA whose bounded waits run out after limit_ns (checks the timeout path).
+cudaError_t launch_wait_check(uint64_t limit_ns, uint32_t* err, cudaStream_t s);
 
 // Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,

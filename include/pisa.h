@@ -138,6 +138,28 @@ PISA_API pisa_status pisa_select_prefill_noalloc(const uint16_t* Q, const uint16
                                                  int32_t* idx, float* leaf_score, int32_t* s2, pisa_shape shape,
                                                  pisa_params params, pisa_stream stream);
 
+/* ---- baseline: BSA flat selection ----------------------------------------------------- */
+
+/* The single-level selection PISA is compared with (summary page, "Prerequisites": block
+ * sparse attention ranks every block by the dot product of the query with the block's
+ * summary, q . kbar_j / sqrt(d), over all M = ceil(N / C) blocks, the G_Q heads of a group
+ * sharing one selection with their scores summed; "Experimental results", item 5, Fig. 3
+ * times this selection against PISA's).  The summaries are the leaf level of P (the mean of
+ * each block's keys, as built by pisa_build_pyramid).  In causal mode block j is eligible for
+ * query t iff j C <= t and the own block t / C always belongs to the set, counting toward K;
+ * ties go to the lower block index; non-causal mode is a plain top-K.  The head sum is taken
+ * in fp32 and the products on the tensor cores from a two-part bf16 split of it (score error
+ * below 1e-4 at the workloads' sizes).  Only params.K, causal and scale are used; the result
+ * does not depend on the scale's value (> 0).  Q, P as for pisa_select_prefill (N_cap must
+ * equal N).
+ *   idx  [B][H_kv][N][K] int32 out: ascending, -1 padded.
+ *   ws   device scratch of at least pisa_select_bsa_workspace_bytes(); 256-B aligned.
+ * Shapes with B * H_kv * 2 * N or B * H_kv * nodes(N) >= 2^31 return PISA_ERR_UNSUPPORTED
+ * (their workspace query returns 0). */
+PISA_API size_t pisa_select_bsa_workspace_bytes(pisa_shape shape, pisa_params params);
+PISA_API pisa_status pisa_select_bsa(const uint16_t* Q, const uint16_t* P, int32_t* idx, void* ws, size_t ws_bytes,
+                                     pisa_shape shape, pisa_params params, pisa_stream stream);
+
 /* ---- step 4: attention over the selected blocks --------------------------------------- */
 
 /* o_{t,h} = sum over keys c of the selected blocks of head h's group (c <= t if causal) of
@@ -232,6 +254,16 @@ PISA_API pisa_status pisa_get_last_device_error(pisa_stream stream);
 PISA_API pisa_status pisa_phase_timing(int enable);
 PISA_API int pisa_phase_times(double* ms, long long* count, int n);
 PISA_API const char* pisa_phase_name(int phase);
+
+/* ---- a check of the timeout path (no counterpart in the paper) ---------------------------- */
+
+/* Launches one CTA that holds tensor memory and waits, through the same bounded waits every
+ * kernel of the library uses, on an mbarrier that nothing completes.  Each wait gives up after
+ * limit_ns (1 us to 10 s; otherwise PISA_ERR_INVALID_ARG, nothing launched), sets the device
+ * error word, and the CTA frees its tensor memory and returns: pisa_get_last_device_error()
+ * then reports PISA_ERR_TIMEOUT and the device stays usable.  Lets a caller or a test exercise
+ * the timeout path without hanging a GPU.  Asynchronous on `stream`. */
+PISA_API pisa_status pisa_check_wait_timeout(unsigned long long limit_ns, pisa_stream stream);
 
 /* Library version string. */
 PISA_API const char* pisa_version(void);

@@ -136,3 +136,30 @@ def full_prefill_check(o, Q, K, V, K_sel, causal=True, sample=None, seed=0, scor
     LSE = np.transpose(res["LSE"], (0, 2, 1))[bt[:, 0], bt[:, 1]]
     rep.update(check_attention(o, Qb, Kb, Vb, res["idx"], bt, O, LSE, causal=causal))
     return rep
+
+
+def check_bsa(o, Qb, Pb, K_sel, rows, gpu_idx, causal=True):
+    """BSA selection parity: identical to the oracle's set where its K-th/(K+1)-th score gap is
+    >= 1e-3; elsewhere the GPU's set must be a top-K within 1e-3 of the oracle's fp64 scores
+    (own block present in causal mode, as many ranked blocks as the oracle's)."""
+    ref = o.select_bsa(Qb, Pb, K_sel, rows, causal=causal, want_scores=True)
+    clear = ref["min_gap"] >= GAP_TOL
+    same = np.all(ref["idx"] == gpu_idx, axis=1)
+    bad = np.where(clear & ~same)[0]
+    assert bad.size == 0, f"BSA idx differs on {bad.size} clear-gap rows, e.g. row {rows[bad[0]]}: " \
+                          f"gpu {gpu_idx[bad[0]]} oracle {ref['idx'][bad[0]]}"
+    for i in np.where(~same)[0]:
+        t = int(rows[i, 2])
+        own = t // 64 if causal else -1
+        got = [int(x) for x in gpu_idx[i] if x >= 0]
+        want = [int(x) for x in ref["idx"][i] if x >= 0]
+        assert got == sorted(set(got)) and len(got) == len(want), (rows[i], got, want)
+        if causal:
+            assert own in got, (rows[i], got)
+        sc = ref["score"][i]
+        chosen = [j for j in got if j != own]
+        assert all(np.isfinite(sc[j]) for j in chosen), (rows[i], got)
+        others = [j for j in range(sc.size) if np.isfinite(sc[j]) and j not in chosen]
+        if chosen and others:
+            assert min(sc[j] for j in chosen) >= max(sc[j] for j in others) - GAP_TOL, (rows[i], got, want)
+    return dict(rows=len(rows), ambiguous=int((~same).sum()), clear=int(clear.sum()))

@@ -165,6 +165,12 @@ def test_parameter_rules(lib):
         (lib.pisa_prefill_host(fake, fake, fake, fake, None, None, fake, 1024, shape(), p16, None), 6),
         (lib.pisa_prefill_host(None, fake, fake, fake, None, None, fake, 1 << 40, shape(), p16, None), 1),
         (lib.pisa_sparse_attn_backward(*([fake] * 11), 1024, shape(), p16, None), 6),
+        (lib.pisa_select_bsa(fake, fake, fake, fake, 1024, shape(), p16, None), 6),
+        (lib.pisa_select_bsa(fake, fake, fake, ct.c_void_p((1 << 20) + 16), 1 << 40, shape(), p16, None), 1),
+        (lib.pisa_select_bsa(fake, fake, fake, fake, 1 << 40, shape(N_cap=8192), p16, None), 1),
+        (lib.pisa_select_bsa(fake, fake, fake, fake, 1 << 40, shape(), pisa.make_params(17), None), 2),
+        (lib.pisa_select_bsa(None, None, None, None, 0, shape(B=0), p16, None), 0),
+        (lib.pisa_check_wait_timeout(999, None), 1), (lib.pisa_check_wait_timeout(10**10 + 1, None), 1),
         (lib.pisa_sparse_attn_backward(*([fake] * 10), ct.c_void_p((1 << 20) + 64), 1 << 40, shape(), p16, None), 1),
     ]
     assert [got for got, _ in cases] == [want for _, want in cases]

@@ -13,7 +13,7 @@ import workloads as W
 from hierarchical_top_block_gb300.build import build
 
 COMPUTE = ("pisa_build_pyramid", "pisa_select_prefill", "pisa_select_prefill_noalloc", "pisa_sparse_attn_prefill",
-           "pisa_sparse_attn_backward", "pisa_prefill_host", "pisa_decode_step")
+           "pisa_sparse_attn_backward", "pisa_prefill_host", "pisa_decode_step", "pisa_select_bsa")
 
 
 @pytest.fixture
@@ -63,6 +63,9 @@ def test_prefill_buffers(calls):
     _ok(calls, lambda: pisa.pisa_select_prefill(Q, K, P, w.K, idx=idx, want_scores=True, want_s2=True))
     _ok(calls, lambda: pisa.pisa_select_prefill_noalloc(Q, K, P, 8))
     _ok(calls, lambda: pisa.pisa_sparse_attn_prefill(Q, K, V, idx, O=O, LSE=LSE))
+    _ok(calls, lambda: pisa.pisa_select_bsa(Q, P, w.K, idx=idx))
+    _refused(calls, lambda: pisa.pisa_select_bsa(Q, P[:, :, :-1], w.K))
+    _refused(calls, lambda: pisa.pisa_select_bsa(Q, P, w.K, idx=idx[..., :8].contiguous()))
     _refused(calls, lambda: pisa.pisa_build_pyramid(K, P=P[:, :, :-1]))
     _refused(calls, lambda: pisa.pisa_select_prefill(Q, K[:, :, :-64].contiguous(), P, w.K))
     _refused(calls, lambda: pisa.pisa_select_prefill(Q, K, P, w.K, idx=idx[..., :8].contiguous()))
