@@ -165,13 +165,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: true once the phase with this parity completed; false (and the error
-// word set) after WAIT_LIMIT_NS.  Callers stop their work on false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+// word set) after limit_ns (WAIT_LIMIT_NS unless given).  Callers stop their work on false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       report_error(err, ERR_TIMEOUT);
       return false;
     }
@@ -179,8 +180,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // Warp-uniform bounded wait: every lane polls; all lanes get the same verdict.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  const bool ok = mbar_wait(bar, parity, err);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                               uint64_t limit_ns = WAIT_LIMIT_NS) {
+  const bool ok = mbar_wait(bar, parity, err, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

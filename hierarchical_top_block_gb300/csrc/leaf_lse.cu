@@ -26,7 +26,8 @@
 //   warps 2-13  epilogue: three groups of four (one warp per TMEM lane quarter), group g
 //               taking tiles g, g+3, ... in its own accumulator; each warp reduces both
 //               leaves of its rows.
-// Every wait is bounded; on timeout the error word is set and the CTA drains and exits.
+// Every wait is bounded; on timeout the error word is set, the MMAs and TMA loads still in
+// flight are waited for (bounded) and the CTA exits.
 #include "kernels.cuh"
 
 namespace pisa {
@@ -78,7 +79,8 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   uint8_t* sQ = smem;
   uint8_t* sK = smem + NQS * STAGE_BYTES;
 
-  __shared__ uint64_t q_info[NQS], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[NACC], acc_empty[NACC];
+  __shared__ uint64_t q_info[NQS], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[NACC], acc_empty[NACC],
+      drain;
   __shared__ TileInfo info[NQS];
   __shared__ int32_t ent[NQS][ROWS];
   __shared__ uint32_t tmem_base_s;
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
+    mbar_init(&drain, 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     uint32_t kload = 0;
     int prev_bh = -1, prev_node = -1, ks = 0;
     int next_tile = 0, chunk_end = 0, chunk_base = 0, chunk_e0 = 0;
+    bool failed = false;
     for (int it = 0;; ++it) {
       const int qs = it % NQS;
       if (next_tile >= chunk_end) {
@@ -139,7 +143,10 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           __syncwarp();
         }
       }
-      if (!mbar_wait_warp(&q_empty[qs], ((it / NQS) & 1) ^ 1, err)) break;
+      if (!mbar_wait_warp(&q_empty[qs], ((it / NQS) & 1) ^ 1, err)) {
+        failed = true;
+        break;
+      }
       if (next_tile >= ntiles) {  // no work left: pass an end marker down the pipeline
         if (lane == 0) {
           info[qs].tile = make_int4(0, 0, 0, -1);
@@ -165,7 +172,10 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       }
       __syncwarp();
       if (newk) {
-        if (!mbar_wait_warp(&k_empty[ks], ((kload / NKS) & 1) ^ 1, err)) break;
+        if (!mbar_wait_warp(&k_empty[ks], ((kload / NKS) & 1) ^ 1, err)) {
+          failed = true;
+          break;
+        }
         if (lane == 0) {
           mbar_arrive_expect_tx(&k_full[ks], STAGE_BYTES);
 #pragma unroll
@@ -178,15 +188,25 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         prev_node = node;
       }
     }
+    // after a timeout, K pairs still in flight land before shared memory goes away (bounded):
+    // the latest load of each stage completes its barrier's current phase
+    if (failed && lane == 0)
+      for (uint32_t k = kload > NKS ? kload - NKS : 0; k < kload; ++k) mbar_wait(&k_full[k % NKS], (k / NKS) & 1, err);
+    __syncwarp();
   } else if (warp >= LOAD_WARP0) {
     // ------------------------------ Q loaders ------------------------------
     // loader warp w issues the TMA boxes (RPQ rows x 64 columns, one per d half) of the tile's
     // queries w, w + LOAD_WARPS, ...; each warp arrives on the stage's barrier with the bytes
     // it expects, so the MMA issuer sees the stage full once every box has landed.
     const int lw = warp - LOAD_WARP0;
+    int issued = 0;  // iterations whose loads this warp has issued
+    bool failed = false;
     for (int it = 0;; ++it) {
       const int qs = it % NQS;
-      if (!mbar_wait_warp(&q_info[qs], (it / NQS) & 1, err)) break;
+      if (!mbar_wait_warp(&q_info[qs], (it / NQS) & 1, err)) {
+        failed = true;
+        break;
+      }
       const int4 tl = info[qs].tile;
       if (tl.w < 0) {  // end marker: pass it to the MMA issuer
         if (lane == 0) mbar_arrive(&q_full[qs]);
@@ -208,7 +228,13 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         const int row = (int)(((long long)b * prm.N + (ent[qs][i] >> 6)) * prm.H_q + (long long)hk * prm.GQ);
         tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h, row);
       }
+      issued = it + 1;
     }
+    // after a timeout, Q rows still in flight land before shared memory goes away (bounded);
+    // on the normal path every stage was consumed, and the end marker has reused one of them
+    if (failed && lane == 0)
+      for (int k = issued > NQS ? issued - NQS : 0; k < issued; ++k) mbar_wait(&q_full[k % NQS], (k / NQS) & 1, err);
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
@@ -251,6 +277,9 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         umma_commit(&acc_full[a]);
         umma_commit(&q_empty[qs]);
       }
+      // every MMA issued has completed before the tensor memory is released (bounded)
+      umma_commit(&drain);
+      mbar_wait(&drain, 0, err);
     }
     __syncwarp();
   } else {
