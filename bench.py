@@ -49,8 +49,8 @@ PAGES_REFERENCE = {
 # dram__bytes_write.sum from one ncu capture; the committed DRAM-traffic profile of that
 # workload), keyed by a hash of the kernel's sources: when the sources change the figure is
 # stale and is reported as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "88038b29dfd8dfe96aa900359165d4b75c6f7ef683facc058995e0ab9a07ce43",
-                "workload": "prefill_256k", "bytes": 13713879552 + 1089932032}
+ATTN_TRAFFIC = {"sources_sha256": "1dc1710457731f368d0419dc01b6a0a1b21a4c5d82e0a9f5012f84c1337ae04e",
+                "workload": "prefill_256k", "bytes": 13835122944 + 1089851648}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
@@ -77,6 +77,11 @@ def parse():
     ap.add_argument("--cpu-sample-rows", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
+    ap.add_argument("--profile-section", choices=["decode", "bsa"], default=None,
+                    help="run only the decode step or the PISA/BSA selection timing, at a reduced size, and print "
+                         "its JSON (for profiler captures; --steps and --warmup apply)")
+    ap.add_argument("--profile-batch", type=int, default=8, help="decode batch of --profile-section decode")
+    ap.add_argument("--profile-n", type=int, default=65536, help="sequence length of --profile-section bsa")
     return ap.parse_args()
 
 
@@ -839,8 +844,31 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile_section(args):
+    """One measurement alone at a reduced size, for profiler captures of its kernels: the batched
+    decode step with a smaller batch (the cache of 8 sequences is 2.1 GB), or the PISA and BSA
+    selections at one sequence length."""
+    import torch
+
+    import workloads as W
+    from hierarchical_top_block_gb300.build import build
+
+    build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.profile_section == "decode":
+        w = W.WORKLOADS["decode_128k"].with_(B=args.profile_batch)
+        out = secondary_decode(w, dev, steps=args.steps, warmup=args.warmup)
+    else:
+        out = bsa_vs_pisa_section(dev, Ns=(args.profile_n,), steps=args.steps)
+    print(json.dumps({"profile_section": args.profile_section, **out}), flush=True)
+
+
 def main():
     args = parse()
+    if args.profile_section:
+        run_profile_section(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
