@@ -246,7 +246,7 @@ Geometry make_geometry(long long n, long long n_cap) {
 pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p) {
   if (s.B < 0 || s.N < 0 || s.H_q <= 0 || s.H_kv <= 0 || s.d <= 0) return PISA_ERR_INVALID_ARG;
   if (pr.C != 64 || pr.g != 2 || (s.d != 64 && s.d != 128)) return PISA_ERR_UNSUPPORTED;
-  if (pr.K < 1 || pr.K > 16) return PISA_ERR_UNSUPPORTED;
+  if (pr.K < 1 || pr.K > 32) return PISA_ERR_UNSUPPORTED;  // a query's 2K candidates fit two per lane
   if (pr.causal != 0 && pr.causal != 1) return PISA_ERR_INVALID_ARG;
   if (pr.scoring < 0 || pr.scoring > 2) return PISA_ERR_INVALID_ARG;
   if (s.H_q % s.H_kv != 0) return PISA_ERR_INVALID_ARG;

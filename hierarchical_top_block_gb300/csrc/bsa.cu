@@ -270,8 +270,10 @@ __global__ void __launch_bounds__(THREADS, 1) bsa_select_kernel(const __grid_con
       tile_of(p, i, bh, t0, nbt);
       const int t = t0 + row;
       const bool valid = t < p.N;
+      // a warp's 32 queries lie in one block of 64 keys, so the own block and the causal limit
+      // are the same for all its lanes (lanes past N are never written)
       const int own = p.causal ? (t >> 6) : -1;
-      const int jlim = !valid ? 0 : (p.causal ? min(p.M1, (t >> 6) + 1) : p.M1);
+      const int jlim = p.causal ? min(p.M1, (t >> 6) + 1) : p.M1;
       float sv[KM];
       int si[KM];
 #pragma unroll
@@ -290,23 +292,32 @@ __global__ void __launch_bounds__(THREADS, 1) bsa_select_kernel(const __grid_con
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          const int j0 = jt * BN + c * 32;
+          if (j0 >= jlim) break;  // the rest of the tile is past the eligible blocks
           uint32_t v[32];
           tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + ac * BN + c * 32, v);
           tmem_wait_ld();
-          const int j0 = jt * BN + c * 32;
-          bool any = false;
+          // bit k: block j0 + k beats the current K-th best (masks only where a chunk reaches past
+          // the eligible blocks or holds the own block)
+          uint32_t cand = 0;
+          if (j0 + 32 <= jlim && (own < j0 || own >= j0 + 32)) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int j = j0 + k;
-            const float s = (j < jlim && j != own) ? __uint_as_float(v[k]) : NEG_INF;
-            v[k] = __float_as_uint(s);
-            any |= s > thr;
+            for (int k = 0; k < 32; ++k) cand |= (__uint_as_float(v[k]) > thr ? 1u : 0u) << k;
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int j = j0 + k;
+              cand |= ((j < jlim && j != own && __uint_as_float(v[k]) > thr) ? 1u : 0u) << k;
+            }
           }
-          if (any) {  // rare after the first blocks: insert the winners in block order
+          if (__any_sync(0xffffffffu, cand != 0)) {
+            // the winners, in block order, through shared memory (a register array cannot be
+            // indexed by a runtime bit position)
 #pragma unroll
             for (int k = 0; k < 32; ++k) my_spill[k * BQ] = __uint_as_float(v[k]);
-#pragma unroll 1
-            for (int k = 0; k < 32; ++k) {
+            while (cand) {
+              const int k = __ffs(cand) - 1;
+              cand &= cand - 1;
               const float s = my_spill[k * BQ];
               if (s > thr) {
                 list_insert(sv, si, s, j0 + k);
@@ -314,6 +325,7 @@ __global__ void __launch_bounds__(THREADS, 1) bsa_select_kernel(const __grid_con
               }
             }
           }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
@@ -398,7 +410,8 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* P, int32_t* idx, uint16_
     return cudaGetLastError();
   };
   if (p.K <= 8) return go(bsa_select_kernel<D, 8>);
-  return go(bsa_select_kernel<D, 16>);
+  if (p.K <= 16) return go(bsa_select_kernel<D, 16>);
+  return go(bsa_select_kernel<D, 32>);
 }
 
 }  // namespace

@@ -144,6 +144,55 @@ __device__ __forceinline__ float pair_score(float a, float b, bool has_b, float 
   return r;
 }
 
+// ---- warp ranking of up to 64 entries ---------------------------------------------------
+// Entry e of lane l sits at position 32 e + l.  Ranks the warp's 64 (score, key, id) entries by
+// (score desc, key asc) with a bitonic network and stops once positions 0..31 (entry 0 of every
+// lane) hold the best 32 in rank order: both halves are sorted (opposite directions), the
+// first merge step keeps the better of positions p and p + 32 in entry 0 (the best 32 as a set),
+// and the last five steps sort entry 0.  Lets a warp take a top-K of 2K candidates for K <= 32.
+__device__ __forceinline__ bool rank_before(float va, int ka, float vb, int kb) {
+  return va > vb || (va == vb && ka < kb);
+}
+__device__ __forceinline__ void warp_top32_of64(float (&v)[2], int (&key)[2], int (&id)[2]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v[e], j);
+        const int ok = __shfl_xor_sync(0xffffffffu, key[e], j);
+        const int oi = __shfl_xor_sync(0xffffffffu, id[e], j);
+        const int pos = 32 * e + lane;
+        const bool lower = (pos & j) == 0, desc = (pos & k) == 0;
+        if ((lower == desc) == rank_before(ov, ok, v[e], key[e])) {
+          v[e] = ov;
+          key[e] = ok;
+          id[e] = oi;
+        }
+      }
+    }
+  }
+  if (rank_before(v[1], key[1], v[0], key[0])) {  // positions p and p + 32: the better to entry 0
+    v[0] = v[1];
+    key[0] = key[1];
+    id[0] = id[1];
+  }
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v[0], j);
+    const int ok = __shfl_xor_sync(0xffffffffu, key[0], j);
+    const int oi = __shfl_xor_sync(0xffffffffu, id[0], j);
+    const bool lower = (lane & j) == 0;
+    if (lower == rank_before(ov, ok, v[0], key[0])) {
+      v[0] = ov;
+      key[0] = ok;
+      id[0] = oi;
+    }
+  }
+}
+
 // ---- mbarrier --------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

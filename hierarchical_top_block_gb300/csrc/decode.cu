@@ -47,18 +47,19 @@ __device__ __forceinline__ int level_size(long long n, int l) {
 }
 
 // 4 CTAs per SM (<= 128 registers, 33 KB of shared memory): a batch of 64 sequences x 8 KV
-// heads runs in one wave
-template <int D>
+// heads runs in one wave.  W: candidates per lane, 1 for K <= 16 (2K <= 32 per level and 2K
+// leaf slots), 2 for K in 17..32 (lane l also holds candidate or slot l + 32).
+template <int D, int W>
 __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint32_t* err) {
   // L2 priorities: candidate K blocks may be read again by the attention (keep them), the
   // attention's K and V reads are their last use (let them go first)
   const uint64_t pol_keep = l2_evict_last_policy(), pol_last_use = l2_evict_first_policy();
   constexpr int NCH = D / 32;
   constexpr int NDT = D / 8;
-  __shared__ int wlst[WARPS][32];
-  __shared__ float lvl_score[2][32];
-  __shared__ int cand_leaf[32];
-  __shared__ float cand_score[32];
+  __shared__ int wlst[WARPS][32 * W];
+  __shared__ float lvl_score[2][32 * W];
+  __shared__ int cand_leaf[32 * W];
+  __shared__ float cand_score[32 * W];
   __shared__ int ncand_s, nsel_s;
   __shared__ int sel[32];
   __shared__ float part_m[WARPS][16], part_l[WARPS][16];
@@ -179,8 +180,10 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       if (e1) mylst[pos + (e0 ? 1 : 0)] = c1;
       __syncwarp();
       const int cand = lane < nc ? mylst[lane] : -1;
+      int cand_hi = -1;  // candidates 32..63 (W == 2)
+      if constexpr (W == 2) cand_hi = lane + 32 < nc ? mylst[lane + 32] : -1;
       __syncwarp();
-      if (nc <= p.Ksel) {
+      if (nc <= p.Ksel) {  // Ksel <= 32: the candidates fit one per lane
         surv = cand;
         ns = nc;
         continue;
@@ -188,9 +191,9 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       const int Mc = level_size(n, l - 1);
       const int tc = (int)(T >> (l + 4));
       const uint16_t* Pl = Pb + (size_t)p.off[l - 1] * D;
-      if (8 * warp < nc) {
-        const int ci = 8 * warp + r;
-        const int cnode = __shfl_sync(0xffffffffu, cand, ci);
+      for (int mt = warp; 8 * mt < nc; mt += WARPS) {  // groups of 8 candidates over the warps
+        const int ci = 8 * mt + r;
+        const int cnode = __shfl_sync(0xffffffffu, mt >= 4 ? cand_hi : cand, ci & 31);
         const bool vc = ci < nc;
         const int ch = 2 * cnode;
         const bool v1 = vc && ch + 1 < Mc && ch + 1 <= tc;
@@ -226,6 +229,24 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
         if (q == 0) lvl_score[par][ci] = vc ? part : NEG_INF;
       }
       __syncthreads();
+      if constexpr (W == 2) {
+        // SelectK over up to 64 candidates (every warp, same result), kept ones compacted in
+        // list (ascending node) order
+        float sv2[2] = {lane < nc ? lvl_score[par][lane] : NEG_INF, lane + 32 < nc ? lvl_score[par][lane + 32] : NEG_INF};
+        int key2[2] = {lane, lane + 32}, id2[2] = {lane, lane + 32};
+        par ^= 1;
+        warp_top32_of64(sv2, key2, id2);
+        const bool take = lane < p.Ksel;
+        const unsigned k0 = __reduce_or_sync(0xffffffffu, take && id2[0] < 32 ? (1u << id2[0]) : 0u);
+        const unsigned k1 = __reduce_or_sync(0xffffffffu, take && id2[0] >= 32 ? (1u << (id2[0] - 32)) : 0u);
+        if ((k0 >> lane) & 1u) mylst[__popc(k0 & lt_mask)] = cand;
+        if ((k1 >> lane) & 1u) mylst[__popc(k0) + __popc(k1 & lt_mask)] = cand_hi;
+        __syncwarp();
+        ns = __popc(k0) + __popc(k1);
+        surv = lane < ns ? mylst[lane] : -1;
+        __syncwarp();
+        continue;
+      }
       // SelectK (every warp, same result): bitonic sort of (score desc, index asc)
       float sv = lane < nc ? lvl_score[par][lane] : NEG_INF;
       int si = lane;
@@ -255,10 +276,14 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
     if (warp == 0) {
       // leaf candidates: eligible children of the level-2 survivors, slot 2i + c
       const int M1 = level_size(n, 1);
-      const int node = __shfl_sync(0xffffffffu, surv, (lane >> 1) & 31);
-      if (lane < 2 * p.Ksel) {
-        const int j = 2 * node + (lane & 1);
-        cand_leaf[lane] = (node >= 0 && j < M1 && (long long)j * 64 <= T) ? j : -1;
+#pragma unroll
+      for (int e = 0; e < W; ++e) {
+        const int slot = 32 * e + lane;
+        const int node = __shfl_sync(0xffffffffu, surv, (slot >> 1) & 31);
+        if (slot < 2 * p.Ksel) {
+          const int j = 2 * node + (slot & 1);
+          cand_leaf[slot] = (node >= 0 && j < M1 && (long long)j * 64 <= T) ? j : -1;
+        }
       }
       if (lane == 0) ncand_s = 2 * p.Ksel;
     }
@@ -387,7 +412,39 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
   // The candidate slots hold their leaves in ascending order; rank the other leaves by
   // (score desc, index asc) with a bitonic sort over the 32 lanes, keep K-1, and write the
   // kept leaves plus the own block in ascending order.
-  if (warp == 0) {
+  if (W == 2 && warp == 0) {
+    // 2K > 32 slots: two per lane, ranked by (score desc, leaf index asc) with the 64-entry
+    // bitonic ranking; kept leaves and the own block written ascending
+    const int own = (int)(T >> 6);
+    int leaf[2];
+    float v2[2];
+    int key2[2], id2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int slot = 32 * e + lane;
+      leaf[e] = slot < nslots ? cand_leaf[slot] : -1;
+      if (leaf[e] == own) leaf[e] = -1;
+      v2[e] = leaf[e] >= 0 ? cand_score[slot] : NEG_INF;
+      key2[e] = leaf[e] >= 0 ? leaf[e] : 0x7fffffff;
+      id2[e] = slot;
+    }
+    const unsigned valid0 = __ballot_sync(0xffffffffu, leaf[0] >= 0), valid1 = __ballot_sync(0xffffffffu, leaf[1] >= 0);
+    warp_top32_of64(v2, key2, id2);
+    const bool take = lane < p.Ksel - 1;
+    const unsigned k0 = __reduce_or_sync(0xffffffffu, take && id2[0] < 32 ? (1u << id2[0]) : 0u) & valid0;
+    const unsigned k1 = __reduce_or_sync(0xffffffffu, take && id2[0] >= 32 ? (1u << (id2[0] - 32)) : 0u) & valid1;
+    const int n0 = __popc(k0);
+    const unsigned b0 = __ballot_sync(0xffffffffu, leaf[0] >= 0 && leaf[0] < own);
+    const unsigned b1 = __ballot_sync(0xffffffffu, leaf[1] >= 0 && leaf[1] < own);
+    if ((k0 >> lane) & 1u) sel[__popc(k0 & lt_mask) + (own < leaf[0] ? 1 : 0)] = leaf[0];
+    if ((k1 >> lane) & 1u) sel[n0 + __popc(k1 & lt_mask) + (own < leaf[1] ? 1 : 0)] = leaf[1];
+    if (lane == 0) {
+      sel[__popc(k0 & b0) + __popc(k1 & b1)] = own;
+      nsel_s = n0 + __popc(k1) + 1;
+    }
+    __syncwarp();
+    if (p.idx_out && lane < p.Ksel) p.idx_out[(size_t)bh * p.Ksel + lane] = lane < nsel_s ? sel[lane] : -1;
+  } else if (warp == 0) {
     const int own = (int)(T >> 6);
     int leaf = lane < nslots ? cand_leaf[lane] : -1;
     if (leaf == own) leaf = -1;
@@ -604,9 +661,14 @@ cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
   for (int l = 0; l <= MAX_LEVELS; ++l) p.off[l] = geo_cap.off[l];
   // V staging [WARPS][32 keys x D] bf16, also the merge buffer [WARPS][16][D] fp32
   const size_t smem = (size_t)WARPS * 32 * D * 2 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<pr.B * pr.H_kv, THREADS, smem, s>>>(p, err);
+    return cudaGetLastError();
+  };
+  cudaError_t e = pr.K > 16 ? go(decode_kernel<D, 2>) : go(decode_kernel<D, 1>);
   if (e != cudaSuccess) return e;
-  decode_kernel<D><<<pr.B * pr.H_kv, THREADS, smem, s>>>(p, err);
   advance_seq_len_kernel<<<(pr.B + 127) / 128, 128, 0, s>>>(seq_len, pr.B, pr.N_cap);
   return cudaGetLastError();
 }

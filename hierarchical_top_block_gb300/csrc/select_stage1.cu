@@ -28,8 +28,9 @@ constexpr int MIN_BLOCKS_128 = 5, MIN_BLOCKS_64 = 6;
 
 
 // SC: the block score (0 LSE, 1 log m + mean, 2 log m + mean + variance / 2), fixed at compile
-// time so that the pair score carries no branch
-template <int D, int SC>
+// time so that the pair score carries no branch.  W: candidates per lane, 1 for K <= 16 (2K <= 32
+// candidates per level), 2 for K in 17..32 (lane l also holds candidate l + 32).
+template <int D, int SC, int W>
 __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCKS_64) stage1_kernel(const uint16_t* __restrict__ Q,
                                                          const uint16_t* __restrict__ P, int32_t* __restrict__ S2,
                                                          ClusterBuffers cb,
@@ -38,7 +39,7 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
   constexpr int scoring = SC;
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
   constexpr int KH = NCH / 2;      // chunks loaded together
-  __shared__ int lists[THREADS / 32][32];
+  __shared__ int lists[THREADS / 32][32 * W];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = lane >> 2, q = lane & 3;
@@ -96,8 +97,10 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       if (e1) lst[pos + (e0 ? 1 : 0)] = c1;
       __syncwarp();
       const int cand = lane < nc ? lst[lane] : -1;
+      int cand_hi = -1;  // candidates 32..63 (W == 2)
+      if constexpr (W == 2) cand_hi = lane + 32 < nc ? lst[lane + 32] : -1;
       __syncwarp();
-      if (nc <= Ksel) {
+      if (nc <= Ksel) {  // Ksel <= 32: the candidates fit one per lane
         surv = cand;
         ns = nc;
         continue;
@@ -110,11 +113,14 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
       const int tc = t >> (l + 4);  // the same for level-(l-1) nodes
       const uint16_t* Pl = Pb + (size_t)geo.off[l - 1] * D;
       const int Mc = geo.M[l - 1];
-      float my = NEG_INF;  // score of candidate `lane`
+      float my = NEG_INF;     // score of candidate `lane`
+      float my_hi = NEG_INF;  // score of candidate `lane + 32` (W == 2)
       const int nmt = (nc + 7) >> 3;
       for (int mt = 0; mt < nmt; ++mt) {
         const int ci = 8 * mt + r;
-        const int cnode = __shfl_sync(0xffffffffu, cand, ci);
+        int cnode;
+        if constexpr (W == 2) cnode = __shfl_sync(0xffffffffu, mt >= 4 ? cand_hi : cand, ci & 31);
+        else cnode = __shfl_sync(0xffffffffu, cand, ci);
         const bool vc = ci < nc;
         const int ch = 2 * cnode;
         const bool v1 = vc && ch + 1 < Mc && (!causal || ch + 1 <= tc);
@@ -176,8 +182,28 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
         // candidate 8mt + r's score (held by lanes 4r..4r+3) to lane 8mt + r
         const float val = __shfl_sync(0xffffffffu, part, 4 * (lane & 7));
         if ((lane >> 3) == mt) my = val;
+        if constexpr (W == 2)
+          if ((lane >> 3) == mt - 4) my_hi = val;
       }
       if (lane >= nc) my = NEG_INF;
+      if constexpr (W == 2) {
+        if (lane + 32 >= nc) my_hi = NEG_INF;
+        // SelectK over up to 64 candidates (ranked by score desc, list position asc), then the
+        // kept ones compacted in list (ascending node) order
+        float sv2[2] = {my, my_hi};
+        int key2[2] = {lane, lane + 32}, id2[2] = {lane, lane + 32};
+        warp_top32_of64(sv2, key2, id2);
+        const bool take = lane < Ksel;
+        const unsigned k0 = __reduce_or_sync(0xffffffffu, take && id2[0] < 32 ? (1u << id2[0]) : 0u);
+        const unsigned k1 = __reduce_or_sync(0xffffffffu, take && id2[0] >= 32 ? (1u << (id2[0] - 32)) : 0u);
+        if ((k0 >> lane) & 1u) lst[__popc(k0 & lt_mask)] = cand;
+        if ((k1 >> lane) & 1u) lst[__popc(k0) + __popc(k1 & lt_mask)] = cand_hi;
+        __syncwarp();
+        ns = __popc(k0) + __popc(k1);
+        surv = lane < ns ? lst[lane] : -1;
+        __syncwarp();
+        continue;
+      }
       // SelectK: bitonic sort of the 32 (score desc, index asc) pairs; the first Ksel lanes
       // then hold the kept candidates.  For Ksel = 16 the network stops after the first merge
       // step of the last stage: the two sorted halves then face each other, so each of lanes
@@ -246,14 +272,24 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
                                          nq, geo);
     return cudaGetLastError();
   };
-  if (p.d == 128) {
-    if (p.scoring == 1) return go(stage1_kernel<128, 1>);
-    if (p.scoring == 2) return go(stage1_kernel<128, 2>);
-    return go(stage1_kernel<128, 0>);
+  if (p.K > 16) {  // 2K > 32 candidates per level: two per lane
+    if (p.d == 128) {
+      if (p.scoring == 1) return go(stage1_kernel<128, 1, 2>);
+      if (p.scoring == 2) return go(stage1_kernel<128, 2, 2>);
+      return go(stage1_kernel<128, 0, 2>);
+    }
+    if (p.scoring == 1) return go(stage1_kernel<64, 1, 2>);
+    if (p.scoring == 2) return go(stage1_kernel<64, 2, 2>);
+    return go(stage1_kernel<64, 0, 2>);
   }
-  if (p.scoring == 1) return go(stage1_kernel<64, 1>);
-  if (p.scoring == 2) return go(stage1_kernel<64, 2>);
-  return go(stage1_kernel<64, 0>);
+  if (p.d == 128) {
+    if (p.scoring == 1) return go(stage1_kernel<128, 1, 1>);
+    if (p.scoring == 2) return go(stage1_kernel<128, 2, 1>);
+    return go(stage1_kernel<128, 0, 1>);
+  }
+  if (p.scoring == 1) return go(stage1_kernel<64, 1, 1>);
+  if (p.scoring == 2) return go(stage1_kernel<64, 2, 1>);
+  return go(stage1_kernel<64, 0, 1>);
 }
 
 }  // namespace pisa

@@ -5,7 +5,7 @@
 // block index); the row is written ascending and padded with -1.
 //
 // One warp per (b, h_kv, t); lane s owns candidate slot s = 2i + c (child c of the i-th
-// level-2 survivor), so g*K <= 32 slots fit one warp.
+// level-2 survivor), so g*K <= 32 slots fit one warp; for K up to 32 each lane owns two.
 #include "kernels.cuh"
 
 namespace pisa {
@@ -94,6 +94,65 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
   }
 }
 
+// The same for K in 17..32: lane l owns slots l and l + 32 (g*K <= 64), ranked with the
+// warp's 64-entry bitonic ranking.
+__global__ void __launch_bounds__(THREADS) topk64_kernel(const int32_t* __restrict__ S2,
+                                                         float* __restrict__ score, int32_t* __restrict__ idx,
+                                                         int BH, int N, int t_lo, int nq, int Ksel, int M1, int causal) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const long long gw = (long long)blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5);
+  const long long nwarps = (long long)gridDim.x * (THREADS / 32);
+  const int twoK = 2 * Ksel;
+  const int keep_n = causal ? Ksel - 1 : Ksel;
+  for (long long it = gw; it < (long long)BH * nq; it += nwarps) {
+    const int bh = (int)(it / nq), t = t_lo + (int)(it - (long long)bh * nq);
+    const long long item = (long long)bh * N + t;
+    const int own = causal ? t / 64 : -1;
+    float v[2];
+    int key[2], id[2], leaf[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int slot = 32 * e + lane;
+      int node = -1;
+      float sc = NEG_INF;
+      if (slot < twoK) {
+        node = S2[item * Ksel + (slot >> 1)];
+        sc = score[item * twoK + slot];
+        // slots of absent level-2 survivors hold no leaf: their score reads -inf
+        if (node < 0) score[item * twoK + slot] = NEG_INF;
+      }
+      leaf[e] = -1;
+      v[e] = NEG_INF;
+      if (node >= 0) {
+        const int j = 2 * node + (slot & 1);
+        if (j < M1 && (!causal || j <= own) && j != own) {
+          leaf[e] = j;
+          v[e] = sc;
+        }
+      }
+      key[e] = slot;  // slots are in ascending block order: ties go to the lower block
+      id[e] = slot;
+    }
+    const unsigned valid0 = __ballot_sync(0xffffffffu, leaf[0] >= 0), valid1 = __ballot_sync(0xffffffffu, leaf[1] >= 0);
+    warp_top32_of64(v, key, id);
+    // kept slots: the first keep_n ranked entries that hold a leaf
+    const bool take = lane < keep_n;
+    const unsigned k0 = __reduce_or_sync(0xffffffffu, take && id[0] < 32 ? (1u << id[0]) : 0u) & valid0;
+    const unsigned k1 = __reduce_or_sync(0xffffffffu, take && id[0] >= 32 ? (1u << (id[0] - 32)) : 0u) & valid1;
+    int32_t* out = idx + item * Ksel;
+    const int n0 = __popc(k0);
+    const unsigned b0 = __ballot_sync(0xffffffffu, leaf[0] >= 0 && leaf[0] < own);
+    const unsigned b1 = __ballot_sync(0xffffffffu, leaf[1] >= 0 && leaf[1] < own);
+    // output position = kept blocks with a smaller index (+1 if the own block is smaller)
+    if ((k0 >> lane) & 1u) out[__popc(k0 & lt_mask) + ((causal && own < leaf[0]) ? 1 : 0)] = leaf[0];
+    if ((k1 >> lane) & 1u) out[n0 + __popc(k1 & lt_mask) + ((causal && own < leaf[1]) ? 1 : 0)] = leaf[1];
+    if (causal && lane == 0) out[__popc(k0 & b0) + __popc(k1 & b1)] = own;
+    const int filled = n0 + __popc(k1) + (causal ? 1 : 0);
+    if (lane >= filled && lane < Ksel) out[lane] = -1;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const int32_t* S2, float* leaf_score, int32_t* idx, const Problem& p,
@@ -105,7 +164,12 @@ cudaError_t launch_topk(const int32_t* S2, float* leaf_score, int32_t* idx, cons
   // item's rows are in flight while the current one is ranked)
   long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
   if (blocks > (long long)num_sms * 8) blocks = (long long)num_sms * 8;
-  topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1], p.causal);
+  if (p.K > 16)
+    topk64_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1],
+                                                  p.causal);
+  else
+    topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1],
+                                                p.causal);
   return cudaGetLastError();
 }
 

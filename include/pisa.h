@@ -27,7 +27,7 @@
  *              idx [B][H_kv][N][K] int32; LSE [B][H_q][N] fp32 (natural log).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *     Argument errors are reported synchronously, before anything is launched.
- *   - Supported: d in {64, 128}; C = 64; g = 2; 1 <= K <= 16; H_q % H_kv == 0 and
+ *   - Supported: d in {64, 128}; C = 64; g = 2; 1 <= K <= 32; H_q % H_kv == 0 and
  *     G_Q = H_q / H_kv in {1, 2, 4, 8, 16}.  Other values return PISA_ERR_UNSUPPORTED.
  *   - Sizes: N_cap < 2^25 and B * N_cap * H_q < 2^31 everywhere; the selection entry points
  *     (pisa_select_prefill, pisa_select_prefill_noalloc, pisa_prefill_host) and the backward

@@ -52,7 +52,8 @@ def test_workspace_query(lib):
     ok = pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 262144, 16, 1, 128), pisa.make_params(16))
     assert ok > 0 and ok % 256 == 0
     assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 16, 1, 96), pisa.make_params(16)) == 0
-    assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 16, 1, 128), pisa.make_params(17)) == 0
+    assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 16, 1, 128), pisa.make_params(33)) == 0
+    assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 16, 1, 128), pisa.make_params(32)) > 0
     assert pisa.pisa_select_workspace_bytes(pisa.make_shape(1, 4096, 12, 4, 128), pisa.make_params(8)) == 0
 
 
@@ -137,7 +138,7 @@ def test_parameter_rules(lib):
 
     p16 = pisa.make_params(16)
     cases = [
-        (sel(shape(), pisa.make_params(0)), 2), (sel(shape(), pisa.make_params(17)), 2),
+        (sel(shape(), pisa.make_params(0)), 2), (sel(shape(), pisa.make_params(33)), 2),
         (sel(shape(H_q=12, H_kv=8), p16), 1), (sel(shape(H_q=3, H_kv=1), p16), 2), (sel(shape(H_q=32, H_kv=1), p16), 2),
         (sel(shape(d=96), p16), 2), (sel(shape(B=-1), p16), 1), (sel(shape(H_q=0), p16), 1),
         (sel(shape(N_cap=100), p16), 1), (sel(shape(N_cap=8192), p16), 1),
@@ -153,7 +154,7 @@ def test_parameter_rules(lib):
         (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(H_q=12, H_kv=8), p16, None), 1),
         (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(),
                                          pisa.pisa_params(64, 2, 16, 2, 0.0, 0), None), 1),
-        (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(), pisa.make_params(17), None), 2),
+        (lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, shape(), pisa.make_params(33), None), 2),
         (lib.pisa_select_prefill_noalloc(None, None, None, None, None, None, shape(B=0), p16, None), 0),
         (lib.pisa_sparse_attn_prefill(fake, fake, fake, fake, fake, None, shape(N_cap=100), p16, None), 1),
         (lib.pisa_sparse_attn_prefill(fake, fake, fake, ct.c_void_p((1 << 20) + 4), fake, None, shape(), p16, None), 1),
@@ -168,7 +169,7 @@ def test_parameter_rules(lib):
         (lib.pisa_select_bsa(fake, fake, fake, fake, 1024, shape(), p16, None), 6),
         (lib.pisa_select_bsa(fake, fake, fake, ct.c_void_p((1 << 20) + 16), 1 << 40, shape(), p16, None), 1),
         (lib.pisa_select_bsa(fake, fake, fake, fake, 1 << 40, shape(N_cap=8192), p16, None), 1),
-        (lib.pisa_select_bsa(fake, fake, fake, fake, 1 << 40, shape(), pisa.make_params(17), None), 2),
+        (lib.pisa_select_bsa(fake, fake, fake, fake, 1 << 40, shape(), pisa.make_params(33), None), 2),
         (lib.pisa_select_bsa(None, None, None, None, 0, shape(B=0), p16, None), 0),
         (lib.pisa_check_wait_timeout(999, None), 1), (lib.pisa_check_wait_timeout(10**10 + 1, None), 1),
         (lib.pisa_sparse_attn_backward(*([fake] * 10), ct.c_void_p((1 << 20) + 64), 1 << 40, shape(), p16, None), 1),

@@ -96,3 +96,8 @@ def test_backward_multi_chunk_blocks(oracle_impl):
     _close("dQ", dQ.cpu().numpy(), rQ)
     _close("dK", dK.cpu().numpy(), rK)
     _close("dV", dV.cpu().numpy(), rV)
+
+
+def test_backward_k32(oracle_impl):
+    w = W.WORKLOADS["prefill_4k"].with_(B=1, N=64 * 40 + 9, H_q=16, H_kv=1, K=32)
+    _check(oracle_impl, w, 32, seed=3)

@@ -52,6 +52,7 @@ def test_bsa_tiny_all_rows(oracle_impl, K_sel):
 @pytest.mark.parametrize("N,GQ,H_kv,d,K_sel,causal", [
     (1, 4, 1, 64, 4, True), (63, 2, 2, 128, 3, True), (129, 8, 1, 128, 5, True), (64 * 130 + 7, 16, 1, 128, 16, True),
     (64 * 70 + 1, 1, 2, 64, 16, True), (300, 4, 1, 64, 4, False), (64 * 200 + 5, 16, 1, 128, 8, False),
+    (64 * 300 + 9, 16, 1, 128, 32, True), (64 * 90, 4, 2, 64, 20, False),
 ])
 def test_bsa_ragged_shapes(oracle_impl, N, GQ, H_kv, d, K_sel, causal):
     w = W.WORKLOADS["prefill_4k"].with_(B=2, N=N, H_q=GQ * H_kv, H_kv=H_kv, d=d, K=K_sel, needles=0)

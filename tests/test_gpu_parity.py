@@ -121,7 +121,7 @@ def test_argument_errors_are_synchronous():
     w = W.WORKLOADS["tiny"]
     Q, K, V = _inputs(w)
     with pytest.raises(pisa.PisaError):
-        pisa.pisa_select_prefill(Q, K, pisa.pisa_build_pyramid(K), 17)  # K > 16 unsupported
+        pisa.pisa_select_prefill(Q, K, pisa.pisa_build_pyramid(K), 33)  # K > 32 unsupported
     assert pisa.pisa_get_last_device_error() == 0
 
 
@@ -331,3 +331,29 @@ def test_prefill_host_matches_the_device_path(case):
     assert torch.equal(Ih, idx.cpu())
     assert torch.equal(Oh, O.cpu())
     assert torch.equal(Lh, LSE.cpu())
+
+
+# ---- K up to 32 (the pages' continued-pretraining setting): 2K candidates, two per lane -----
+@pytest.mark.parametrize("N,GQ,H_kv,d,K_sel", [
+    (16384 + 37, 16, 1, 128, 32),    # levels with 64 candidates are scored (walk, top-K, attention)
+    (64 * 200 + 5, 8, 2, 64, 24),
+    (64 * 150, 4, 1, 128, 17),
+])
+def test_k_up_to_32_sampled(oracle_impl, N, GQ, H_kv, d, K_sel):
+    w = W.WORKLOADS["prefill_4k"].with_(B=1, N=N, H_q=GQ * H_kv, H_kv=H_kv, d=d, K=K_sel, needles=4)
+    Q, K, V = _inputs(w)
+    rep = H.full_prefill_check(oracle_impl, Q, K, V, K_sel, sample=768, seed=K_sel)
+    assert rep["rows"] == 768
+
+
+def test_k32_tiny_all_rows_dense(oracle_impl):
+    """K = 32 >= M_1 = 16: every eligible leaf is selected (dense causal attention)."""
+    w = W.WORKLOADS["tiny"].with_(K=32)
+    Q, K, V = _inputs(w)
+    H.full_prefill_check(oracle_impl, Q, K, V, 32)
+
+
+def test_decode_k32(oracle_impl):
+    # 64 candidates at the scored levels of the walk and 64 leaf slots
+    w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=8, H_kv=2, K=32)
+    _decode_check(oracle_impl, w, N0=64 * 160 + 50, steps=4, N_cap=16384)
