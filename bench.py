@@ -49,8 +49,8 @@ PAGES_REFERENCE = {
 # dram__bytes_write.sum from one ncu capture; the committed DRAM-traffic profile of that
 # workload), keyed by a hash of the kernel's sources: when the sources change the figure is
 # stale and is reported as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "1dc1710457731f368d0419dc01b6a0a1b21a4c5d82e0a9f5012f84c1337ae04e",
-                "workload": "prefill_256k", "bytes": 13835122944 + 1089851648}
+ATTN_TRAFFIC = {"sources_sha256": "2eea854f4fa2701d2a6afffc3395e46f4909a0f887c1cc3d66384afe0a8332b7",
+                "workload": "prefill_256k", "bytes": 14015405312 + 1090564352}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
