@@ -127,6 +127,8 @@ def _empty_calls(dev, host_prefill):
         assert idx.shape == (B, 1, N, 16) and score.shape == (B, 1, N, 32)
         O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx)
         assert O.shape == Q.shape and LSE.shape == (B, 16, N)
+        assert pisa.pisa_select_bsa(Q, P, 8).shape == (B, 1, N, 8)
+        assert pisa.pisa_select_prefill(Q, K, P, 32).shape == (B, 1, N, 32)
         dQ, dK, dV = pisa.pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, torch.empty_like(Q))
         assert dQ.shape == Q.shape and dK.shape == K.shape and dV.shape == V.shape
         if host_prefill:

@@ -299,7 +299,8 @@ def test_decode_scoring_variants(oracle_impl, scoring):
     _decode_check(oracle_impl, w, N0=2040, steps=12, N_cap=2304, scoring=scoring)
 
 
-@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked", "35000_noncausal_pisa2_chunked", "20000_d64_k4_chunked"])
+@pytest.mark.parametrize("case", ["4k_b2", "35000_b2_chunked", "35000_noncausal_pisa2_chunked", "20000_d64_k4_chunked",
+                                  "35000_k32_chunked"])
 def test_prefill_host_matches_the_device_path(case):
     """The whole prefill from pinned host buffers (the end-to-end entry point) returns exactly
     what the device-resident calls return on the same inputs.  The 35000-token cases run as six
@@ -316,6 +317,8 @@ def test_prefill_host_matches_the_device_path(case):
         w = W.WORKLOADS["prefill_32k"].with_(B=2, N=35000, H_q=8, H_kv=2)
         if case == "35000_noncausal_pisa2_chunked":
             causal, scoring = False, 2
+        if case == "35000_k32_chunked":  # two candidates per lane in every chunk
+            w = w.with_(K=32)
     Q, K, V = _inputs(w)
     P = pisa.pisa_build_pyramid(K)
     idx = pisa.pisa_select_prefill(Q, K, P, w.K, causal=causal, scoring=scoring)
@@ -351,6 +354,19 @@ def test_k32_tiny_all_rows_dense(oracle_impl):
     w = W.WORKLOADS["tiny"].with_(K=32)
     Q, K, V = _inputs(w)
     H.full_prefill_check(oracle_impl, Q, K, V, 32)
+
+
+@pytest.mark.parametrize("N,d,K_sel", [(64 * 40 + 3, 64, 32), (64 * 150 + 17, 128, 20)])
+def test_k_up_to_32_non_causal(oracle_impl, N, d, K_sel):
+    """Without the mask every leaf is a candidate; 64-candidate levels at N > 64 * 128."""
+    w = W.WORKLOADS["tiny"].with_(N=N, d=d, H_q=8, H_kv=2)
+    Q, K, V = _inputs(w)
+    H.full_prefill_check(oracle_impl, Q, K, V, K_sel, causal=False, sample=600, seed=N)
+
+
+def test_decode_k32_d64_gq16(oracle_impl):
+    w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=16, H_kv=1, d=64, K=32)
+    _decode_check(oracle_impl, w, N0=64 * 140 + 60, steps=5, N_cap=16384)
 
 
 def test_decode_k32(oracle_impl):
