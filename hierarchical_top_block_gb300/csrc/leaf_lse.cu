@@ -10,20 +10,22 @@
 // per leaf to log-sum-exp (causal mask inside the query's own block), and the G_Q rows of
 // a query are summed with lane shuffles in a fixed order.
 //
-// Persistent, warp-specialised CTA (one per SM):
+// Persistent, warp-specialised CTA (one per SM, 17 warps):
 //   warp 0      scheduler: tiles come in runs of consecutive tiles from an atomic counter
 //               (a run's tile records and entries are staged in shared memory in one round
-//               trip); per tile it publishes the record and the query list of a Q stage and
-//               loads the K pair by TMA (3-D map, rows past N read as zero) into a 2-stage
-//               ring, reused across consecutive tiles of the same pair.
-//   warps 14-17 Q loaders: the tile's query rows by TMA into a 4-stage ring, the tile's
-//               queries spread over the four warps (with small boxes the issue cost per box
-//               dominates; one warp issuing all of them was the pipeline's bottleneck).  For
-//               d = 128 and G_Q a multiple of 8 one 4-D box per query (8-row groups with both
-//               d halves), else one 2-D box of RPQ rows per d half; 128-byte swizzle.
-//   warp 1      owns TMEM (3 x 128 columns of accumulators, one per epilogue group); one thread
-//               issues the d/16 MMAs of a tile and commits to mbarriers.
-//   warps 2-13  epilogue: three groups of four (one warp per TMEM lane quarter), group g
+//               trip); it publishes each tile's record and query list into a 16-slot ring
+//               that runs ahead of the Q stages, and loads each new K pair by TMA (3-D map,
+//               rows past N read as zero) into a 2-stage ring, reused across consecutive
+//               tiles of the same pair.
+//   warps 2-3   Q loaders: once a tile's record is out and its Q stage (4-stage ring) is
+//               free, the tile's query rows by TMA, the queries split over the two warps.
+//               For d = 128 and G_Q a multiple of 8 one 4-D box per query (8-row groups with
+//               both d halves), else one 2-D box of RPQ rows per d half; 128-byte swizzle.
+//   warp 1, 16  MMA issuers: lane 0 of each issues the d/16 MMAs of alternate tiles (an
+//               issuing thread stalls while the tensor pipe's queue is full, so the other
+//               prepares its next tile meanwhile) and commits to mbarriers; warp 1 owns TMEM
+//               (3 x 128 columns of accumulators, one per epilogue group).
+//   warps 4-15  epilogue: three groups of four (one warp per TMEM lane quarter), group g
 //               taking tiles g, g+3, ... in its own accumulator; each warp reduces both
 //               leaves of its rows.
 // Every wait is bounded; on timeout the error word is set, the MMAs and TMA loads still in
@@ -34,15 +36,32 @@ namespace pisa {
 namespace {
 
 constexpr int NQS = 4;            // Q stages
+constexpr int NREC = 16;          // tile records, published ahead of the Q stages and read by the epilogue
 constexpr int NKS = 2;            // K-pair stages
 constexpr int ROWS = 128;         // MMA M (query-head rows)
 constexpr int KEYS = 128;         // MMA N (two leaves of 64 keys)
-constexpr int EPI_WARPS = 12;
 constexpr int NACC = 3;           // accumulator buffers = epilogue groups
-constexpr int LOAD_WARPS = 4;
-constexpr int LOAD_WARP0 = 2 + EPI_WARPS;
-constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * LOAD_WARPS;
+constexpr int EPI_WARPS = 4 * NACC;
+constexpr int LOAD_WARPS = 2;
+constexpr int LOAD_WARP0 = 2;
+constexpr int EPI_WARP0 = 4;      // a warpgroup boundary, so warp & 3 is the TMEM lane quarter
+constexpr int MMA2_WARP = EPI_WARP0 + EPI_WARPS;  // the second MMA issuer (the first is warp 1)
+constexpr int THREADS = 32 * (MMA2_WARP + 1);     // 544: 96 registers a thread
+
+// Accumulator buffer a = t % NACC holds tile t; MMA issuer t & 1 issues it.  Use m = t / NACC
+// of buffer a waits for the release of use m - 1, which the epilogue group signals on the
+// empty barrier of the issuer of use m, so each issuer waits every phase of its own barriers
+// in order (a parity wait never runs two phases ahead of its barrier).  Returns the phase
+// index of that release among the releases on the barrier, or -1 when no wait is needed.
+__device__ __forceinline__ int acc_release_phase(int t) {
+  const int a = t % NACC, m = t / NACC;
+  if (m == 0) return -1;
+  if (NACC % 2 == 0) return m - 1;            // every use of the buffer has the same issuer
+  const int j0 = ((t & 1) + a + 1) & 1;        // first earlier use whose successor is t's issuer
+  return (m - 1 - j0) >> 1;
+}
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int QT_MAX = ROWS / 8;  // queries per tile (G_Q rows each, padded to 8)
 
 
 
@@ -79,10 +98,10 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   uint8_t* sQ = smem;
   uint8_t* sK = smem + NQS * STAGE_BYTES;
 
-  __shared__ uint64_t q_info[NQS], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS], acc_full[NACC], acc_empty[NACC],
-      drain;
-  __shared__ TileInfo info[NQS];
-  __shared__ int32_t ent[NQS][ROWS];
+  __shared__ uint64_t rec_full[NREC], rec_empty[NREC], q_full[NQS], q_empty[NQS], k_full[NKS], k_empty[NKS],
+      acc_full[NACC], acc_empty[NACC][2], drain;
+  __shared__ TileInfo rec[NREC];
+  __shared__ int32_t rec_ent[NREC][QT_MAX];
   __shared__ uint32_t tmem_base_s;
   __shared__ int done_it_s;  // iteration index of the end marker
   __shared__ int4 chunk_tiles[SCHED_CHUNK];        // producer staging of the current chunk
@@ -91,20 +110,24 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     done_it_s = 0x7fffffff;
+    for (int i = 0; i < NREC; ++i) {
+      mbar_init(&rec_full[i], 1);
+      mbar_init(&rec_empty[i], LOAD_WARPS + 4 + 2);  // read by the Q loaders, an epilogue group, both MMA issuers
+    }
     for (int i = 0; i < NQS; ++i) {
-      mbar_init(&q_info[i], 1);
       mbar_init(&q_full[i], LOAD_WARPS);
-      mbar_init(&q_empty[i], 1 + 4);
+      mbar_init(&q_empty[i], 1);
     }
     for (int i = 0; i < NKS; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+      mbar_init(&k_empty[i], 2);  // both MMA issuers
     }
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i][0], 4);  // released for the next use by issuer 0 / 1
+      mbar_init(&acc_empty[i][1], 4);
     }
-    mbar_init(&drain, 1);
+    mbar_init(&drain, 2);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -116,15 +139,88 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
   const uint32_t tmem_base = tmem_base_s;
   const int ntiles = prm.totals[1];
 
+  // ------------------------------ MMA issuers ------------------------------
+  // Two threads (lane 0 of warp 1 and of the last warp) issue the MMAs of alternate tiles, so
+  // one waits for its next tile's Q stage, K pair and accumulator while the other's MMAs run
+  // (an issuing thread stalls while the tensor pipe's queue is full).  Each reads every tile
+  // record, so both follow the K-stage sequence, and commits its own MMAs on k_empty when the
+  // pair changes (k_empty counts both).  A tile's MMAs complete -> its Q stage is free and
+  // its accumulator goes to the epilogue group; the record stays in its ring slot until the
+  // loaders, both issuers and the group have read it.
+  auto mma_issuer = [&](const int par) {
+    constexpr uint32_t idesc = idesc_bf16_f32(ROWS, KEYS);
+    uint32_t kload = 0;
+    int cur_ks = -1;
+    bool kwait = false;  // the current K pair has not been waited for by this thread
+    // Every K load is waited for in order, also those of pairs without a tile of this thread,
+    // so no parity wait runs two phases ahead of k_full (the scheduler publishes a record
+    // before the stage it names is free).
+    auto wait_k = [&]() -> bool {
+      if (!kwait) return true;
+      kwait = false;
+      return mbar_wait(&k_full[cur_ks], ((kload - 1) / NKS) & 1, err);
+    };
+    auto wait_acc = [&](int t) -> bool {
+      const int ph = acc_release_phase(t);
+      return ph < 0 || mbar_wait(&acc_empty[t % NACC][par], (ph & 1), err);
+    };
+    for (int it = 0;; ++it) {
+      const int qs = it % NQS, rs = it % NREC;
+      if (!mbar_wait(&rec_full[rs], (it / NREC) & 1, err)) break;
+      const TileInfo ti = rec[rs];
+      if (ti.tile.w < 0) {  // end marker: tell the groups of this thread's parity once their buffers are free
+        done_it_s = it;     // both issuers write the same value
+        __threadfence_block();
+        for (int k = 0; k < NACC; ++k) {
+          const int i2 = it + k;
+          if ((i2 & 1) != par) continue;
+          if (!wait_acc(i2)) break;
+          mbar_arrive(&acc_full[i2 % NACC]);
+        }
+        break;
+      }
+      mbar_arrive(&rec_empty[rs]);
+      if (ti.newk) {
+        if (!wait_k()) break;
+        if (cur_ks >= 0) umma_commit(&k_empty[cur_ks]);
+        ++kload;
+        cur_ks = ti.ks;
+        kwait = true;
+      }
+      if ((it & 1) != par) continue;
+      if (!wait_k() || !mbar_wait(&q_full[qs], (it / NQS) & 1, err) || !wait_acc(it)) break;
+      const int a = it % NACC;
+      tc_fence_after();
+      const uint32_t qbase = smem_u32(sQ + qs * STAGE_BYTES);
+      const uint32_t kbase = smem_u32(sK + ti.ks * STAGE_BYTES);
+#pragma unroll
+      for (int s = 0; s < KSTEPS; ++s) {
+        const uint32_t off = (s >> 2) * (ROWS * 128) + (s & 3) * 32;
+        // grouped Q: d half h of 8-row group g at g * 2048 + h * 1024
+        const uint32_t qoff = prm.qgrp ? (s >> 2) * 1024 + (s & 3) * 32 : off;
+        umma_bf16(tmem_base + a * KEYS, smem_desc_sw128(qbase + qoff, 16, prm.qgrp ? 2048 : 1024),
+                  smem_desc_sw128(kbase + off, 16, 1024), idesc, s > 0 ? 1u : 0u);
+      }
+      umma_commit(&acc_full[a]);
+      umma_commit(&q_empty[qs]);
+    }
+    // every MMA issued by either thread has completed before the tensor memory is released
+    // (bounded)
+    umma_commit(&drain);
+    mbar_wait(&drain, 0, err);
+  };
+
   if (warp == 0) {
     // ------------------------------ scheduler ------------------------------
+    // Publishes tile records into a ring that runs up to NREC tiles ahead of the Q stages,
+    // and loads each new K pair.
     const uint64_t keep_policy = l2_evict_last_policy();  // K pairs are reused by later windows
     uint32_t kload = 0;
     int prev_bh = -1, prev_node = -1, ks = 0;
     int next_tile = 0, chunk_end = 0, chunk_base = 0, chunk_e0 = 0;
     bool failed = false;
     for (int it = 0;; ++it) {
-      const int qs = it % NQS;
+      const int rs = it % NREC;
       if (next_tile >= chunk_end) {
         // grab the next run of consecutive tiles (mostly one K pair) and stage their tile
         // records and entries in shared memory with one round trip each
@@ -143,15 +239,14 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
           __syncwarp();
         }
       }
-      if (!mbar_wait_warp(&q_empty[qs], ((it / NQS) & 1) ^ 1, err)) {
+      if (!mbar_wait_warp(&rec_empty[rs], ((it / NREC) & 1) ^ 1, err)) {
         failed = true;
         break;
       }
       if (next_tile >= ntiles) {  // no work left: pass an end marker down the pipeline
         if (lane == 0) {
-          info[qs].tile = make_int4(0, 0, 0, -1);
-          __threadfence_block();
-          mbar_arrive(&q_info[qs]);
+          rec[rs].tile = make_int4(0, 0, 0, -1);
+          mbar_arrive(&rec_full[rs]);
         }
         break;
       }
@@ -161,14 +256,13 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       const int newk = (bh != prev_bh || node != prev_node) ? 1 : 0;
       if (newk) ks = kload % NKS;
       // publish the tile first: its Q loads need not wait for a free K stage
-      for (int i = lane; i < cnt; i += 32) ent[qs][i] = chunk_ent[start - chunk_e0 + i];
+      if (lane < cnt) rec_ent[rs][lane] = chunk_ent[start - chunk_e0 + lane];
       __syncwarp();
       if (lane == 0) {
-        info[qs].tile = tl;
-        info[qs].ks = ks;
-        info[qs].newk = newk;
-        __threadfence_block();
-        mbar_arrive(&q_info[qs]);
+        rec[rs].tile = tl;
+        rec[rs].ks = ks;
+        rec[rs].newk = newk;
+        mbar_arrive(&rec_full[rs]);  // release: the record is visible to whoever waits
       }
       __syncwarp();
       if (newk) {
@@ -193,21 +287,29 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     if (failed && lane == 0)
       for (uint32_t k = kload > NKS ? kload - NKS : 0; k < kload; ++k) mbar_wait(&k_full[k % NKS], (k / NKS) & 1, err);
     __syncwarp();
-  } else if (warp >= LOAD_WARP0) {
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(0);
+    __syncwarp();
+  } else if (warp == MMA2_WARP) {
+    if (lane == 0) mma_issuer(1);
+    __syncwarp();
+  } else if (warp >= LOAD_WARP0 && warp < LOAD_WARP0 + LOAD_WARPS) {
     // ------------------------------ Q loaders ------------------------------
-    // loader warp w issues the TMA boxes (RPQ rows x 64 columns, one per d half) of the tile's
-    // queries w, w + LOAD_WARPS, ...; each warp arrives on the stage's barrier with the bytes
-    // it expects, so the MMA issuer sees the stage full once every box has landed.
+    // Each loader waits for the tile's record and for the Q stage to be free, then issues
+    // the TMA boxes (one per query, or RPQ rows x 64 columns per d half) of the tile's
+    // queries w, w + LOAD_WARPS, ...; each warp arrives on the stage's barrier with the
+    // bytes it expects, so the MMA issuer sees the stage full once every box has landed.
     const int lw = warp - LOAD_WARP0;
     int issued = 0;  // iterations whose loads this warp has issued
     bool failed = false;
     for (int it = 0;; ++it) {
-      const int qs = it % NQS;
-      if (!mbar_wait_warp(&q_info[qs], (it / NQS) & 1, err)) {
+      const int qs = it % NQS, rs = it % NREC;
+      if (!mbar_wait_warp(&rec_full[rs], (it / NREC) & 1, err) ||
+          !mbar_wait_warp(&q_empty[qs], ((it / NQS) & 1) ^ 1, err)) {
         failed = true;
         break;
       }
-      const int4 tl = info[qs].tile;
+      const int4 tl = rec[rs].tile;
       if (tl.w < 0) {  // end marker: pass it to the MMA issuer
         if (lane == 0) mbar_arrive(&q_full[qs]);
         break;
@@ -215,18 +317,30 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
       const int bh = tl.x, cnt = tl.w;
       const int b = bh / prm.H_kv, hk = bh - b * prm.H_kv;
       const int mine = cnt > lw ? (cnt - lw + LOAD_WARPS - 1) / LOAD_WARPS : 0;  // queries of this warp
-      if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], (uint32_t)mine * prm.RPQ * D * 2);
+      int t_mine = 0;
+      if (lane < mine) t_mine = rec_ent[rs][lw + LOAD_WARPS * lane] >> 6;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&rec_empty[rs]);
+        mbar_arrive_expect_tx(&q_full[qs], (uint32_t)mine * prm.RPQ * D * 2);
+      }
       __syncwarp();
       if (prm.qgrp) {  // the query's 8-row groups with both d halves in one box
         if (lane < mine) {
           const int i = lw + LOAD_WARPS * lane;
-          const long long row = ((long long)b * prm.N + (ent[qs][i] >> 6)) * prm.H_q + (long long)hk * prm.GQ;
+          const long long row = ((long long)b * prm.N + t_mine) * prm.H_q + (long long)hk * prm.GQ;
           tma_load_4d(sQ + qs * STAGE_BYTES + i * prm.RPQ * 256, &mapQ, &q_full[qs], 0, 0, 0, (int)(row >> 3));
         }
-      } else if (lane < mine * HALVES) {
-        const int i = lw + LOAD_WARPS * (lane / HALVES), h = lane % HALVES;
-        const int row = (int)(((long long)b * prm.N + (ent[qs][i] >> 6)) * prm.H_q + (long long)hk * prm.GQ);
-        tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h, row);
+      } else {
+        // lane j of the first mine * HALVES issues d half j % HALVES of query j / HALVES
+        const int src = lane / HALVES, h = lane % HALVES;
+        const int t = __shfl_sync(0xffffffffu, t_mine, src < 32 ? src : 0);
+        if (lane < mine * HALVES) {
+          const int i = lw + LOAD_WARPS * src;
+          const int row = (int)(((long long)b * prm.N + t) * prm.H_q + (long long)hk * prm.GQ);
+          tma_load_2d(sQ + qs * STAGE_BYTES + h * (ROWS * 128) + i * prm.RPQ * 128, &mapQ, &q_full[qs], 64 * h,
+                      row);
+        }
       }
       issued = it + 1;
     }
@@ -235,60 +349,13 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     if (failed && lane == 0)
       for (int k = issued > NQS ? issued - NQS : 0; k < issued; ++k) mbar_wait(&q_full[k % NQS], (k / NQS) & 1, err);
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(ROWS, KEYS);
-      uint32_t kload = 0;
-      int cur_ks = -1;
-      for (int it = 0;; ++it) {
-        const int qs = it % NQS;
-        if (!mbar_wait(&q_full[qs], (it / NQS) & 1, err)) break;
-        const TileInfo ti = info[qs];
-        if (ti.tile.w < 0) {  // end marker: tell both epilogue groups once their buffers are free
-          done_it_s = it;
-          __threadfence_block();
-          for (int k = 0; k < NACC; ++k) {
-            const int i2 = it + k, a = i2 % NACC;
-            if (!mbar_wait(&acc_empty[a], ((i2 / NACC) & 1) ^ 1, err)) break;
-            mbar_arrive(&acc_full[a]);
-          }
-          break;
-        }
-        if (ti.newk) {
-          if (cur_ks >= 0) umma_commit(&k_empty[cur_ks]);
-          if (!mbar_wait(&k_full[ti.ks], (kload / NKS) & 1, err)) break;
-          ++kload;
-          cur_ks = ti.ks;
-        }
-        const int a = it % NACC;
-        if (!mbar_wait(&acc_empty[a], ((it / NACC) & 1) ^ 1, err)) break;
-        tc_fence_after();
-        const uint32_t qbase = smem_u32(sQ + qs * STAGE_BYTES);
-        const uint32_t kbase = smem_u32(sK + ti.ks * STAGE_BYTES);
-#pragma unroll
-        for (int s = 0; s < KSTEPS; ++s) {
-          const uint32_t off = (s >> 2) * (ROWS * 128) + (s & 3) * 32;
-          // grouped Q: d half h of 8-row group g at g * 2048 + h * 1024
-          const uint32_t qoff = prm.qgrp ? (s >> 2) * 1024 + (s & 3) * 32 : off;
-          umma_bf16(tmem_base + a * KEYS, smem_desc_sw128(qbase + qoff, 16, prm.qgrp ? 2048 : 1024),
-                    smem_desc_sw128(kbase + off, 16, 1024), idesc, s > 0 ? 1u : 0u);
-        }
-        umma_commit(&acc_full[a]);
-        umma_commit(&q_empty[qs]);
-      }
-      // every MMA issued has completed before the tensor memory is released (bounded)
-      umma_commit(&drain);
-      mbar_wait(&drain, 0, err);
-    }
-    __syncwarp();
   } else {
     // ------------------------------ epilogue ------------------------------
-    // Three groups of four warps, one warp per TMEM lane quarter: group g takes the tiles
-    // g, g + 3, ... (accumulator buffer g) and reduces both leaves of each, so the epilogue
+    // NACC groups of four warps, one warp per TMEM lane quarter: group g takes the tiles
+    // g, g + NACC, ... (accumulator buffer g) and reduces both leaves of each, so the epilogue
     // warps sharing a scheduler partition work on different tiles and hide each other's
     // TMEM loads, shuffles and stores.
-    const int ew = warp - 2;
+    const int ew = warp - EPI_WARP0;
     const int grp = ew >> 2;
     const int quarter = warp & 3;
     const int RPQ = R > 0 ? R : prm.RPQ, GQ = R > 0 ? R : prm.GQ;
@@ -297,16 +364,18 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
     const int qi = row / RPQ, h = row - qi * RPQ;
     const int twoK = 2 * prm.Ksel;
     for (int it = grp;; it += NACC) {
-      const int qs = it % NQS;
-      const int a = grp;
+      const int a = grp, rs = it % NREC;
       if (!mbar_wait_warp(&acc_full[a], (it / NACC) & 1, err)) break;
       if (it >= *(volatile int*)&done_it_s) break;
       tc_fence_after();
-      const int4 tl = info[qs].tile;
+      // the record's publication, acquired directly (it completed before the MMAs were issued,
+      // and the slot cannot be reused before this group frees it, so this returns at once)
+      if (!mbar_wait_warp(&rec_full[rs], (it / NREC) & 1, err)) break;
+      const int4 tl = rec[rs].tile;
       const bool vq = qi < tl.w;
-      const int e = vq ? ent[qs][qi] : 0;
+      const int e = vq ? rec_ent[rs][qi] : 0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&q_empty[qs]);
+      if (lane == 0) mbar_arrive(&rec_empty[rs]);
       const int t = e >> 6, slot = e & 63;
       const int bh = tl.x, node = tl.y;
 #pragma unroll 1
@@ -319,7 +388,7 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
         if (leaf_c == 1) {  // the accumulator is read out: the MMA may reuse it
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[a]);
+          if (lane == 0) mbar_arrive(&acc_empty[a][(it + NACC) & 1]);  // for the issuer of the next use
         }
         const int leaf = 2 * node + leaf_c;
         const long long key0 = (long long)leaf * 64;
@@ -477,6 +546,9 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if (fa.maxThreadsPerBlock < THREADS) return cudaErrorLaunchOutOfResources;  // registers x threads
     kern<<<num_sms, THREADS, smem, s>>>(mapQ, mapK, prm, err);
     return cudaGetLastError();
   };
