@@ -71,6 +71,9 @@ class Oracle:
         L.oracle_sparse_attention_backward.restype = _I
         L.oracle_sparse_attention_backward.argtypes = [_P, _P, _P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I, _D, _P,
                                                        _P, _P, _I]
+        L.oracle_sparse_attention_backward_sampled.restype = _I
+        L.oracle_sparse_attention_backward_sampled.argtypes = [_P, _P, _P, _P, _P, _I, _LL, _I, _I, _I, _I, _I, _I,
+                                                               _D, _P, _I, _P, _I, _P, _P, _P, _I]
         L.oracle_decode_step.restype = _I
         L.oracle_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _LL, _I, _I, _I, _I, _I, _I, _I, _D, _P, _P,
                                          _P, _I, _I]
@@ -194,6 +197,27 @@ class Oracle:
         rc = self.lib.oracle_sparse_attention_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(dO), B, N, H_q,
                                                        H_kv, d, C, Ksel, int(causal), scale, _ptr(dQ), _ptr(dK),
                                                        _ptr(dV), self.nthreads)
+        assert rc == 0, rc
+        return dQ, dK, dV
+
+    def sparse_attention_backward_sampled(self, Q, K, V, idx, dO, rows, blocks, C=64, causal=True, scale=None):
+        """The backward at samples: rows = flat (b * N + t) query positions -> dQ [nrows, H_q, d];
+        blocks = flat ((b * H_kv + h_kv) * M1 + j) key blocks -> dK, dV [nblocks, C, d] (fp64), equal
+        to the corresponding values of sparse_attention_backward."""
+        B, N, H_q, d = Q.shape
+        H_kv = K.shape[1]
+        Ksel = idx.shape[-1]
+        scale = 1.0 / math.sqrt(d) if scale is None else scale
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        blocks = np.ascontiguousarray(blocks, dtype=np.int64)
+        dQ = np.zeros((len(rows), H_q, d), np.float64)
+        dK = np.zeros((len(blocks), C, d), np.float64)
+        dV = np.zeros((len(blocks), C, d), np.float64)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        dO = np.ascontiguousarray(dO, dtype=np.uint16)
+        rc = self.lib.oracle_sparse_attention_backward_sampled(
+            _ptr(Q), _ptr(K), _ptr(V), _ptr(idx), _ptr(dO), B, N, H_q, H_kv, d, C, Ksel, int(causal), scale, _ptr(rows),
+            len(rows), _ptr(blocks), len(blocks), _ptr(dQ), _ptr(dK), _ptr(dV), self.nthreads)
         assert rc == 0, rc
         return dQ, dK, dV
 

@@ -528,6 +528,7 @@ double attend(const uint16_t* qh, const uint16_t* Kbg, const uint16_t* Vbg, long
 // give no backward): with the forward's visible positions c, s_c = scale q.k_c,
 // P_c = exp(s_c - lse), O = sum P_c v_c, D = dO.O, dP_c = dO.v_c, dS_c = P_c (dP_c - D):
 // dq += scale sum dS_c k_c, dk_c += scale dS_c q, dv_c += P_c dO.  dO is d values (fp64).
+// dK and dV may be null (only dq wanted).
 void attend_backward(const uint16_t* qh, const uint16_t* Kbg, const uint16_t* Vbg, long long n, long long t, int d,
                      int C, bool causal, double scale, const int32_t* blocks, int nb, const double* dO, double* dq,
                      double* dK, double* dV) {
@@ -565,8 +566,8 @@ void attend_backward(const uint16_t* qh, const uint16_t* Kbg, const uint16_t* Vb
     const double dS = P[i] * (dP - D);
     for (int e = 0; e < d; ++e) {
       dq[e] += scale * dS * bf16_to_f64(Kbg[c * d + e]);
-      dK[c * d + e] += scale * dS * q[e];
-      dV[c * d + e] += P[i] * dO[e];
+      if (dK) dK[c * d + e] += scale * dS * q[e];
+      if (dV) dV[c * d + e] += P[i] * dO[e];
     }
   }
 }
@@ -756,6 +757,77 @@ int oracle_sparse_attention_backward(const uint16_t* Q, const uint16_t* K, const
           for (int x = 0; x < d; ++x) go[x] = bf16_to_f64(dO[row + x]);
           attend_backward(Q + row, K + bg * N * d, V + bg * N * d, N, t, d, C, causal != 0, scale,
                           idx + (bg * N + t) * Ksel, Ksel, go.data(), dQ + row, dK + bg * N * d, dV + bg * N * d);
+        }
+    }
+  });
+  return 0;
+}
+
+// The same backward restricted to samples, for parity checks at sizes where the full one
+// takes too long: dQ of the listed query positions (row = b * N + t, every head) and dK, dV of
+// the listed key blocks (block = (b * H_kv + h_kv) * M1 + j, its C rows).  Every value is
+// accumulated from the same rows, in the same (t, head) order, as oracle_sparse_attention_backward
+// does, so the two functions give equal values.  Outputs fp64, overwritten:
+// dQ_rows [nrows][H_q][d], dK_blk and dV_blk [nblocks][C][d] (rows past N stay zero).
+int oracle_sparse_attention_backward_sampled(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                                             const int32_t* idx, const uint16_t* dO, int B, long long N, int H_q,
+                                             int H_kv, int d, int C, int Ksel, int causal, double scale,
+                                             const long long* rows, int nrows, const long long* blocks, int nblocks,
+                                             double* dQ_rows, double* dK_blk, double* dV_blk, int nthreads) {
+  if (H_kv <= 0 || H_q % H_kv != 0) return 1;
+  const int GQ = H_q / H_kv;
+  const long long M1 = (N + C - 1) / C;
+  for (int i = 0; i < nrows; ++i)
+    if (rows[i] < 0 || rows[i] >= (long long)B * N) return 2;
+  for (int i = 0; i < nblocks; ++i)
+    if (blocks[i] < 0 || blocks[i] >= (long long)B * H_kv * M1) return 3;
+  std::fill(dQ_rows, dQ_rows + (size_t)nrows * H_q * d, 0.0);
+  std::fill(dK_blk, dK_blk + (size_t)nblocks * C * d, 0.0);
+  std::fill(dV_blk, dV_blk + (size_t)nblocks * C * d, 0.0);
+  // dQ: each listed position, every head
+  run_parallel(nrows, nthreads, [&](long long a, long long e) {
+    std::vector<double> go(d);
+    for (long long i = a; i < e; ++i) {
+      const long long b = rows[i] / N, t = rows[i] % N;
+      for (int hk = 0; hk < H_kv; ++hk) {
+        const long long bg = b * H_kv + hk;
+        for (int g = 0; g < GQ; ++g) {
+          const long long h = (long long)hk * GQ + g;
+          const size_t row = ((size_t)(b * N + t) * H_q + h) * d;
+          for (int x = 0; x < d; ++x) go[x] = bf16_to_f64(dO[row + x]);
+          attend_backward(Q + row, K + bg * N * d, V + bg * N * d, N, t, d, C, causal != 0, scale,
+                          idx + (bg * N + t) * Ksel, Ksel, go.data(), dQ_rows + ((size_t)i * H_q + h) * d, nullptr,
+                          nullptr);
+        }
+      }
+    }
+  });
+  // dK, dV: for each listed block, every (t, head) whose selection holds it, in order
+  run_parallel(nblocks, nthreads, [&](long long a, long long e) {
+    std::vector<double> go(d), dq(d), sk((size_t)N * d), sv((size_t)N * d);
+    for (long long i = a; i < e; ++i) {
+      const long long bg = blocks[i] / M1, j = blocks[i] % M1;
+      const long long b = bg / H_kv, hk = bg % H_kv;
+      std::fill(sk.begin(), sk.end(), 0.0);
+      std::fill(sv.begin(), sv.end(), 0.0);
+      for (long long t = 0; t < N; ++t) {
+        const int32_t* sel = idx + (bg * N + t) * Ksel;
+        bool has = false;
+        for (int k = 0; k < Ksel; ++k) has = has || sel[k] == j;
+        if (!has) continue;
+        for (int g = 0; g < GQ; ++g) {
+          const long long h = hk * GQ + g;
+          const size_t row = ((size_t)(b * N + t) * H_q + h) * d;
+          for (int x = 0; x < d; ++x) go[x] = bf16_to_f64(dO[row + x]);
+          std::fill(dq.begin(), dq.end(), 0.0);
+          attend_backward(Q + row, K + bg * N * d, V + bg * N * d, N, t, d, C, causal != 0, scale, sel, Ksel,
+                          go.data(), dq.data(), sk.data(), sv.data());
+        }
+      }
+      for (long long c = j * C; c < std::min<long long>(N, j * C + C); ++c)
+        for (int x = 0; x < d; ++x) {
+          dK_blk[((size_t)i * C + (c - j * C)) * d + x] = sk[c * d + x];
+          dV_blk[((size_t)i * C + (c - j * C)) * d + x] = sv[c * d + x];
         }
     }
   });

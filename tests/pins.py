@@ -408,6 +408,35 @@ def pin_backward_sums(o):
     assert np.abs(dK).max() > 1e-3
 
 
+def pin_backward_sampled_equals_full(o):
+    """The sampled backward (dQ of listed positions, dK and dV of listed key blocks) gives the
+    full backward's values exactly: the same rows accumulate in the same order.  Pruned
+    selections (K = 2 of 7 leaves, ragged N), causal and not, two sequences, G_Q = 2."""
+    N, H_q, H_kv, d = 64 * 6 + 29, 4, 2, 16
+    rng = np.random.default_rng(61)
+    for causal in (True, False):
+        Q, K, V = (random_bf16(rng, s, 0.5) for s in ((2, N, H_q, d), (2, H_kv, N, d), (2, H_kv, N, d)))
+        dO = random_bf16(rng, (2, N, H_q, d))
+        P = o.build_pyramid(K)
+        rows = np.array([[b, g, t] for b in range(2) for g in range(H_kv) for t in range(N)], np.int64)
+        idx = o.select(Q, K, P, 2, rows, causal=causal)["idx"].reshape(2, H_kv, N, 2)
+        dQ, dK, dV = o.sparse_attention_backward(Q, K, V, idx, dO, causal=causal)
+        M1 = (N + 63) // 64
+        srows = np.array([0, 5, 63, 64, N - 1, N, N + 200, 2 * N - 1], np.int64)          # b * N + t
+        sblocks = np.array([0, M1 - 1, M1 + 2, 2 * M1 + 1, 4 * M1 - 1], np.int64)          # (b * H_kv + h) * M1 + j
+        sq, sk, sv = o.sparse_attention_backward_sampled(Q, K, V, idx, dO, srows, sblocks, causal=causal)
+        for i, r in enumerate(srows):
+            assert np.array_equal(sq[i], dQ[r // N, r % N]), (causal, r)
+        for i, blk in enumerate(sblocks):
+            bg, j = divmod(int(blk), M1)
+            b, h = divmod(bg, H_kv)
+            n = min(64, N - 64 * j)
+            assert np.array_equal(sk[i, :n], dK[b, h, 64 * j:64 * j + n]), (causal, blk)
+            assert np.array_equal(sv[i, :n], dV[b, h, 64 * j:64 * j + n]), (causal, blk)
+            assert not sk[i, n:].any() and not sv[i, n:].any()
+        assert np.abs(sk).max() > 1e-3 and np.abs(sq).max() > 1e-3
+
+
 def pin_ties_lower_index(o):
     """Identical keys everywhere: equal scores rank the lower block index first."""
     d, C, N = 16, 64, 64 * 6
@@ -849,5 +878,5 @@ ALL_PINS = [
     pin_single_block_at_start, pin_decode, pin_decode_scoring_variants,
     pin_scoring_variants_closed_forms, pin_scoring_variants_order, pin_mean_scoring_ranks_like_the_mean,
     pin_backward_dense_autograd, pin_backward_dense_autograd_noncausal, pin_backward_finite_differences,
-    pin_backward_sums, pin_bsa_closed_form, pin_bsa_equals_pisa1_leaf_ranking, pin_bsa_invariants,
+    pin_backward_sums, pin_backward_sampled_equals_full, pin_bsa_closed_form, pin_bsa_equals_pisa1_leaf_ranking, pin_bsa_invariants,
 ]

@@ -101,3 +101,71 @@ def test_backward_multi_chunk_blocks(oracle_impl):
 def test_backward_k32(oracle_impl):
     w = W.WORKLOADS["prefill_4k"].with_(B=1, N=64 * 40 + 9, H_q=16, H_kv=1, K=32)
     _check(oracle_impl, w, 32, seed=3)
+
+
+def _pick_blocks(idx_np, M1, rng, per_bg, cap_rows):
+    """Key blocks to check, per (sequence, KV head): the first and the last block and random
+    selected ones across the range of selection counts, while the queries selecting the chosen
+    blocks stay within cap_rows in total (the oracle recomputes each of them)."""
+    B, H_kv = idx_np.shape[:2]
+    out, rows = [], 0
+    for bg in range(B * H_kv):
+        sel = idx_np.reshape(B * H_kv, -1)[bg]
+        cnt = np.bincount(sel[sel >= 0], minlength=M1)
+        chosen = [j for j in (0, M1 - 1) if cnt[j] > 0]
+        order = np.argsort(cnt, kind="stable")
+        picked = [int(j) for j in order[cnt[order] > 0]]
+        # spread over the count distribution: quantiles of the selected blocks
+        for qn in np.linspace(0.05, 0.95, per_bg):
+            chosen.append(picked[int(qn * (len(picked) - 1))])
+        chosen += [int(j) for j in rng.choice(picked, size=2, replace=False)]
+        for j in dict.fromkeys(chosen):
+            if cnt[j] <= cap_rows // 4 and rows + cnt[j] <= cap_rows:
+                out.append(bg * M1 + j)
+                rows += int(cnt[j])
+    return np.array(out, np.int64), rows
+
+
+def _check_sampled(oracle_impl, w, n_rows, per_bg, cap_rows, seed):
+    Q, K, V = W.prefill_inputs(w, "cuda")
+    gen = torch.Generator(device="cpu").manual_seed(4321 + seed)
+    dO = (torch.randn(Q.shape, generator=gen) * 0.5).to(torch.bfloat16).to("cuda")
+    P = pisa.pisa_build_pyramid(K)
+    idx = pisa.pisa_select_prefill(Q, K, P, w.K)
+    O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx)
+    dQ, dK, dV = pisa.pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO)
+    torch.cuda.synchronize()
+    assert pisa.pisa_get_last_device_error() == 0
+    N, M1 = w.N, (w.N + 63) // 64
+    idx_np = idx.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    t = np.unique(np.concatenate([rng.choice(N, n_rows, replace=False), [0, 1, 63, 64, 65, N - 64, N - 1]]))
+    rows = np.concatenate([b * N + t for b in range(w.B)]).astype(np.int64)
+    blocks, nsel = _pick_blocks(idx_np, M1, rng, per_bg, cap_rows)
+    assert len(blocks) >= 4 and nsel > 0
+    rQ, rK, rV = oracle_impl.sparse_attention_backward_sampled(H.to_np_bits(Q), H.to_np_bits(K), H.to_np_bits(V),
+                                                               idx_np, H.to_np_bits(dO), rows, blocks)
+    gQ = dQ.reshape(w.B * N, w.H_q, w.d)[torch.from_numpy(rows).to("cuda")].cpu().numpy()
+    _close("dQ (sampled positions)", gQ, rQ)
+    bg, j = blocks // M1, blocks % M1
+    keys = (j[:, None] * 64 + np.arange(64)[None, :])
+    valid = keys < N
+    gK = dK.reshape(w.B * w.H_kv, N, w.d).cpu().numpy()
+    gV = dV.reshape(w.B * w.H_kv, N, w.d).cpu().numpy()
+    kk = np.minimum(keys, N - 1)
+    _close("dK (sampled blocks)", gK[bg[:, None], kk][valid], rK[valid])
+    _close("dV (sampled blocks)", gV[bg[:, None], kk][valid], rV[valid])
+
+
+def test_backward_32k_sampled(oracle_impl):
+    """The benchmark's 32K shape (B = 1, N = 32768, H_q = 32, H_kv = 2, d = 128, K = 16) on the
+    GPU's own selection, through the full-size chunked path: dQ on about 1000 sampled positions
+    (every head) and dK, dV of key blocks across the range of selection counts (the first and
+    last block included), against the oracle's sampled backward."""
+    _check_sampled(oracle_impl, W.WORKLOADS["prefill_32k"], n_rows=1000, per_bg=5, cap_rows=4000, seed=5)
+
+
+def test_backward_256k_sampled(oracle_impl):
+    """The bench's 256K shape (B = 1, N = 262144, H_q = 16, H_kv = 1, d = 128, K = 16): dQ on
+    about 500 sampled positions and dK, dV of a few key blocks, as above."""
+    _check_sampled(oracle_impl, W.WORKLOADS["prefill_256k"], n_rows=500, per_bg=5, cap_rows=12000, seed=6)

@@ -58,8 +58,9 @@ MUTANTS["pisa1_adds_variance"] = [("  if (scoring == 2) {", "  if (scoring >= 1)
 
 # the backward of step 4
 MUTANTS["backward_drops_D"] = [("    const double dS = P[i] * (dP - D);", "    const double dS = P[i] * dP;")]
-MUTANTS["backward_dk_without_scale"] = [("      dK[c * d + e] += scale * dS * q[e];", "      dK[c * d + e] += dS * q[e];")]
-MUTANTS["backward_dv_uses_dS"] = [("      dV[c * d + e] += P[i] * dO[e];", "      dV[c * d + e] += dS * dO[e];")]
+MUTANTS["backward_dk_without_scale"] = [("      if (dK) dK[c * d + e] += scale * dS * q[e];",
+                                         "      if (dK) dK[c * d + e] += dS * q[e];")]
+MUTANTS["backward_dv_uses_dS"] = [("      if (dV) dV[c * d + e] += P[i] * dO[e];", "      if (dV) dV[c * d + e] += dS * dO[e];")]
 MUTANTS["backward_ignores_causal"] = [("      if (causal && c > t) continue;\n      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;",
                                        "      double z = 0;\n      for (int e = 0; e < d; ++e) z += q[e] * bf16_to_f64(Kbg[c * d + e]);\n      pos.push_back(c);\n      s.push_back(scale * z);\n    }\n  if (pos.empty()) return;")]
 
