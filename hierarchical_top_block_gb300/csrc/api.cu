@@ -31,15 +31,15 @@ struct HostPipe {
   cudaEvent_t ev[PIPE_EVENTS] = {};
 };
 
-// Query chunks of the host-buffer prefill.  The chunks double from N/64 (at least 4096
+// Query chunks of the host-buffer prefill.  The chunks double from N/32 (at least 8192
 // queries) up to a quarter of the sequence and halve again at the end, with equal chunks of at
 // most N/4 between: a short first chunk shortens the copy-in that precedes any compute, and
 // the halving tail keeps each chunk's copy-out shorter than the compute of the chunks after
 // it, so only the last, small copy-out trails the compute.  Bounds are multiples of 64 except
 // where the remainder of a ragged N falls; at most 11 chunks.
 int plan_chunks(long long N, long long* bounds) {
-  long long lo = N / 64 / 64 * 64;
-  if (lo < 4096) lo = 4096;
+  long long lo = N / 32 / 64 * 64;
+  if (lo < 8192) lo = 8192;
   long long cap = N / 4 / 64 * 64;
   if (cap < lo) cap = lo;
   long long ramp[8];

@@ -193,7 +193,7 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
 
 /* Copies Q, K, V host -> device, builds the pyramid, selects, attends and copies O (and
  * LSE, idx when non-NULL) device -> host; returns when all of it has finished.  The work runs
- * in query chunks (at most 11: doubling from N/64 positions, at least 4096, up to N/4 and
+ * in query chunks (at most 11: doubling from N/32 positions, at least 8192, up to N/4 and
  * halving again towards the end, equal chunks of at most N/4 between) so that the host -> device copy of the next
  * chunk's Q, the device -> host copy of the previous chunk's O and the attention of one chunk
  * overlap the selection of the next: selection runs on `stream`, attention and the copies on

@@ -75,16 +75,16 @@ def test_argument_errors_without_a_gpu(lib):
 
 def test_prefill_host_chunk_plan(lib):
     """The host-buffer prefill's query chunks: they tile [0, N) in order, there are at most 11,
-    they double from N/64 (at least 4096) up to N/4 and halve again at the end, and a short
+    they double from N/32 (at least 8192) up to N/4 and halve again at the end, and a short
     sequence runs as one chunk."""
     assert pisa.pisa_prefill_host_chunks(0) == [0]
-    for n in (1, 63, 4096):
+    for n in (1, 63, 4096, 8192):
         assert pisa.pisa_prefill_host_chunks(n) == [0, n]
-    for n in (4097, 20000, 35000, 65536, 245633, 262144, 262207, 1 << 20, (1 << 24) + 5, 10**10 + 7):
+    for n in (8193, 20000, 35000, 65536, 245633, 262144, 262207, 1 << 20, (1 << 24) + 5, 10**10 + 7):
         b = pisa.pisa_prefill_host_chunks(n)
         sizes = [hi - lo for lo, hi in zip(b, b[1:])]
         assert b[0] == 0 and b[-1] == n and min(sizes) > 0 and len(sizes) <= 11, (n, sizes)
-        lo = max(n // 64 // 64 * 64, 4096)
+        lo = max(n // 32 // 64 * 64, 8192)
         cap = max(n // 4 // 64 * 64, lo)
         assert max(sizes) <= cap + 64, (n, sizes)
         # the rising ramp and the falling one mirror each other
@@ -94,13 +94,13 @@ def test_prefill_host_chunk_plan(lib):
         assert sizes[len(sizes) - r:] == sizes[:r][::-1], (n, sizes)
     # the 256K plan the benchmark's end-to-end leg runs
     sizes = [hi - lo for lo, hi in zip(pisa.pisa_prefill_host_chunks(262144), pisa.pisa_prefill_host_chunks(262144)[1:])]
-    assert sizes == [4096, 8192, 16384, 32768, 46400, 46400, 46464, 32768, 16384, 8192, 4096]
+    assert sizes == [8192, 16384, 32768, 49152, 49152, 49152, 32768, 16384, 8192]
     # errors: negative N, NULL bounds, too small a buffer
     buf = (ct.c_longlong * 17)()
     assert lib.pisa_prefill_host_chunks(-1, buf, 17) == -1
     assert lib.pisa_prefill_host_chunks(262144, None, 17) == -1
-    assert lib.pisa_prefill_host_chunks(262144, buf, 11) == -1
-    assert lib.pisa_prefill_host_chunks(262144, buf, 12) == 11
+    assert lib.pisa_prefill_host_chunks(262144, buf, 9) == -1
+    assert lib.pisa_prefill_host_chunks(262144, buf, 10) == 9
 
 
 def test_entry_list_limit(lib):
