@@ -682,13 +682,16 @@ def secondary_decode(w, dev, steps=None, warmup=3):
     ins = [W.decode_step_inputs(w, s, dev) for s in range(warmup + steps)]
     o = torch.empty(w.B, w.H_q, w.d, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.B, w.H_q, dtype=torch.float32, device=dev)
+    # the leaf logits scratch of pisa_decode_step_ws, allocated once
+    ws = torch.empty(pisa.pisa_decode_workspace_bytes(pisa.make_shape(w.B, 0, w.H_q, w.H_kv, w.d, N_cap),
+                                                      pisa.make_params(w.K)), dtype=torch.uint8, device=dev)
     for s in range(warmup):
-        pisa.pisa_decode_step(*ins[s], Kc, Vc, Pc, seq, w.K, o=o, lse=lse)
+        pisa.pisa_decode_step(*ins[s], Kc, Vc, Pc, seq, w.K, o=o, lse=lse, ws=ws)
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for s in range(steps):
         evs[s][0].record()
-        pisa.pisa_decode_step(*ins[warmup + s], Kc, Vc, Pc, seq, w.K, o=o, lse=lse)
+        pisa.pisa_decode_step(*ins[warmup + s], Kc, Vc, Pc, seq, w.K, o=o, lse=lse, ws=ws)
         evs[s][1].record()
     torch.cuda.synchronize()
     us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)

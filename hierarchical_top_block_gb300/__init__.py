@@ -78,6 +78,11 @@ def lib() -> ct.CDLL:
         L.pisa_prefill_host.argtypes = [_P, _P, _P, _P, _P, _P, _P, ct.c_size_t, pisa_shape, pisa_params, _P]
         L.pisa_decode_step.restype = ct.c_int
         L.pisa_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, pisa_shape, pisa_params, _P]
+        L.pisa_decode_workspace_bytes.restype = ct.c_size_t
+        L.pisa_decode_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_decode_step_ws.restype = ct.c_int
+        L.pisa_decode_step_ws.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ct.c_size_t, pisa_shape,
+                                          pisa_params, _P]
         L.pisa_status_string.restype = ct.c_char_p
         L.pisa_status_string.argtypes = [ct.c_int]
         L.pisa_get_last_device_error.restype = ct.c_int
@@ -408,9 +413,22 @@ def pisa_prefill_host(Q_host, K_host, V_host, K_sel: int, causal: bool = True, s
 
 
 # ---- step 3 -----------------------------------------------------------------------------
+def pisa_decode_workspace_bytes(shape, params) -> int:
+    """Bytes of the decode step's logits scratch (0 for arguments the step refuses)."""
+    return int(lib().pisa_decode_workspace_bytes(shape, params))
+
+
+def pisa_decode_step_ws(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, ws=None, **kw):
+    """pisa_decode_step with the logits scratch ws (allocated when None or too small)."""
+    return pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel, ws=ws, keep_logits=True, **kw)
+
+
 def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.0, o=None, lse=None, idx_out=None,
-                     scoring: int | str = 0):
-    """One decode step for every sequence; caches and seq_len are updated in place."""
+                     scoring: int | str = 0, ws=None, keep_logits: bool = True):
+    """One decode step for every sequence; caches and seq_len are updated in place.  With
+    keep_logits (pisa_decode_step_ws) the leaf scoring's logits are kept in ws (a uint8 device
+    tensor, allocated when None or too small) and the attention reads them instead of the
+    selected blocks' K rows; without it, pisa_decode_step.  The results are the same."""
     _bf16(q, "q", 3)
     _bf16(k, "k", 3)
     _bf16(Kc, "Kc", 4)
@@ -430,8 +448,16 @@ def pisa_decode_step(q, k, v, Kc, Vc, Pc, seq_len, K_sel: int, scale: float = 0.
     _expect(lse, "lse", (B, H_q), torch.float32, dev)
     _expect(idx_out, "idx_out", (B, H_kv, K_sel), torch.int32, dev)
     shape = make_shape(B, 0, H_q, H_kv, d, N_cap)
-    _check(lib().pisa_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), _ptr(o),
-                                  _ptr(lse), _ptr(idx_out), shape, make_params(K_sel, True, scale, scoring=scoring),
-                                  _stream(q)),
-           "pisa_decode_step")
+    params = make_params(K_sel, True, scale, scoring=scoring)
+    if not keep_logits:
+        _check(lib().pisa_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), _ptr(o),
+                                      _ptr(lse), _ptr(idx_out), shape, params, _stream(q)),
+               "pisa_decode_step")
+        return o
+    need = lib().pisa_decode_workspace_bytes(shape, params)
+    ws = _workspace(ws, need, dev) if need > 0 else None  # 0: arguments the call refuses with its own status
+    _check(lib().pisa_decode_step_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(Kc), _ptr(Vc), _ptr(Pc), _ptr(seq_len), _ptr(o),
+                                     _ptr(lse), _ptr(idx_out), _ptr(ws), 0 if ws is None else ws.numel(), shape, params,
+                                     _stream(q)),
+           "pisa_decode_step_ws")
     return o

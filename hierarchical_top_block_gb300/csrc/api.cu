@@ -665,9 +665,24 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   return PISA_OK;
 }
 
+size_t pisa_decode_workspace_bytes(pisa_shape shape, pisa_params params) {
+  pisa_shape sh = shape;
+  if (sh.N_cap <= 0) return 0;
+  sh.N = 0;
+  Problem p;
+  if (check_params(sh, params, &p) != PISA_OK || p.causal != 1) return 0;
+  return decode_logits_bytes(p);
+}
+
 pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
                              uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
                              pisa_shape shape, pisa_params params, pisa_stream stream) {
+  return pisa_decode_step_ws(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, nullptr, 0, shape, params, stream);
+}
+
+pisa_status pisa_decode_step_ws(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
+                                uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out, void* ws,
+                                size_t ws_bytes, pisa_shape shape, pisa_params params, pisa_stream stream) {
   pisa_shape sh = shape;
   if (sh.N_cap <= 0) return PISA_ERR_INVALID_ARG;
   sh.N = 0;
@@ -676,6 +691,10 @@ pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_
   if (rc != PISA_OK) return rc;
   if (p.causal != 1) return PISA_ERR_UNSUPPORTED;
   if (p.B == 0) return PISA_OK;
+  if (ws) {
+    if (ws_bytes < decode_logits_bytes(p)) return PISA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return PISA_ERR_INVALID_ARG;
+  }
   if (!q || !k || !v || !Kc || !Vc || !Pc || !seq_len || !o) return PISA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(Pc) ||
       !aligned16(o))
@@ -685,7 +704,8 @@ pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_
   const Geometry geo_cap = make_geometry(p.N_cap, p.N_cap);
   PhaseTimer tm(static_cast<cudaStream_t>(stream));
   const cudaError_t e =
-      launch_decode(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, st->err, static_cast<cudaStream_t>(stream));
+      launch_decode(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, static_cast<float*>(ws), p, geo_cap, st->err,
+                    static_cast<cudaStream_t>(stream));
   tm.mark(PH_DECODE);
   return cuda_status(e);
 }

@@ -402,6 +402,19 @@ __device__ __forceinline__ uint4 ldg16_hint(const void* p, uint64_t policy) {
   return v;
 }
 
+// 8-byte global store and load with an L2 eviction-priority policy (coherent: the values are
+// written and read back by the same kernel).
+__device__ __forceinline__ void st_f2_hint(float2* p, float2 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(v.x), "f"(v.y), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ float2 ld_f2_hint(const float2* p, uint64_t policy) {
+  float2 v;
+  asm volatile("ld.global.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;" : "=f"(v.x), "=f"(v.y) : "l"(p), "l"(policy)
+               : "memory");
+  return v;
+}
+
 // ---- pyramid geometry (passed by value to kernels) ------------------------------------
 constexpr int MAX_LEVELS = 40;
 struct Geometry {

@@ -32,6 +32,12 @@ struct DecodeParams {
   uint16_t* o;
   float* lse;
   int32_t* idx_out;
+  // logits of the leaf candidates, kept for the attention (nullable): per (sequence, KV head)
+  // [2K slots][8 key octets][sc_halves][sc_lanes] float2, in the MMA accumulator layout (lane
+  // 4r + q holds head r; the lanes of heads past G_Q are not kept)
+  float2* sc;
+  int sc_halves;  // 2 when G_Q > 8 (rows r + 8 hold heads), else 1
+  int sc_lanes;   // 4 min(G_Q, 8)
   int H_q, H_kv, GQ, Ksel, N_cap;
   int scoring;  // 0 LSE, 1 log m + mean, 2 log m + mean + variance / 2
   float sl2;
@@ -62,6 +68,7 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
   __shared__ float cand_score[32 * W];
   __shared__ int ncand_s, nsel_s;
   __shared__ int sel[32];
+  __shared__ int sel_slot[32];  // the candidate slot of each selected block, -1 if none
   __shared__ float part_m[WARPS][16], part_l[WARPS][16];
   extern __shared__ __align__(1024) uint8_t vbuf_raw[];
   uint8_t* vbuf = (uint8_t*)(((uintptr_t)vbuf_raw + 1023) & ~(uintptr_t)1023);  // [WARPS][32 x D bf16]
@@ -292,6 +299,8 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
 
   // ---- exact leaf LSE of the candidates (slots split over the warps) ----
   const int nslots = ncand_s;
+  // with the logits kept, the attention reads no candidate's K rows again: no need to keep them
+  const uint64_t pol_leaf_k = p.sc ? pol_last_use : pol_keep;
   for (int sidx = warp; sidx < nslots; sidx += WARPS) {
     const int leaf = cand_leaf[sidx];
     if (leaf < 0) continue;
@@ -305,12 +314,21 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       const uint16_t* krow = Kb + (size_t)(vis ? key : key0) * D;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        const uint4 kv = vis ? ldg16_hint(krow + 32 * j + 8 * q, pol_keep) : make_uint4(0, 0, 0, 0);
+        const uint4 kv = vis ? ldg16_hint(krow + 32 * j + 8 * q, pol_leaf_k) : make_uint4(0, 0, 0, 0);
         mma_bf16_16816(acc[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
         mma_bf16_16816(acc[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
       }
     }
     // acc[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0, 1}
+    if (p.sc && lane < p.sc_lanes) {  // keep the logits: the attention over this leaf, if selected, reuses them
+      const int nl = p.sc_lanes;
+      float2* dst = p.sc + (((size_t)bh * 2 * p.Ksel + sidx) * 8) * p.sc_halves * nl + lane;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        st_f2_hint(dst + (size_t)nt * p.sc_halves * nl, make_float2(acc[nt][0], acc[nt][1]), pol_keep);
+        if (p.sc_halves == 2) st_f2_hint(dst + (size_t)(nt * 2 + 1) * nl, make_float2(acc[nt][2], acc[nt][3]), pol_keep);
+      }
+    }
     float lse2_0, lse2_1;
     if (p.scoring != 0) {
       // truncated forms over the m visible keys, log2 units: log2 m + mean (+ ln2/2 Var)
@@ -436,10 +454,22 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
     const int n0 = __popc(k0);
     const unsigned b0 = __ballot_sync(0xffffffffu, leaf[0] >= 0 && leaf[0] < own);
     const unsigned b1 = __ballot_sync(0xffffffffu, leaf[1] >= 0 && leaf[1] < own);
-    if ((k0 >> lane) & 1u) sel[__popc(k0 & lt_mask) + (own < leaf[0] ? 1 : 0)] = leaf[0];
-    if ((k1 >> lane) & 1u) sel[n0 + __popc(k1 & lt_mask) + (own < leaf[1] ? 1 : 0)] = leaf[1];
+    if ((k0 >> lane) & 1u) {
+      const int at = __popc(k0 & lt_mask) + (own < leaf[0] ? 1 : 0);
+      sel[at] = leaf[0];
+      sel_slot[at] = lane;
+    }
+    if ((k1 >> lane) & 1u) {
+      const int at = n0 + __popc(k1 & lt_mask) + (own < leaf[1] ? 1 : 0);
+      sel[at] = leaf[1];
+      sel_slot[at] = 32 + lane;
+    }
+    const unsigned own0 = __ballot_sync(0xffffffffu, lane < nslots && cand_leaf[lane] == own);
+    const unsigned own1 = __ballot_sync(0xffffffffu, 32 + lane < nslots && cand_leaf[32 + lane] == own);
     if (lane == 0) {
-      sel[__popc(k0 & b0) + __popc(k1 & b1)] = own;
+      const int at = __popc(k0 & b0) + __popc(k1 & b1);
+      sel[at] = own;
+      sel_slot[at] = own0 ? __ffs(own0) - 1 : own1 ? 32 + __ffs(own1) - 1 : -1;
       nsel_s = n0 + __popc(k1) + 1;
     }
     __syncwarp();
@@ -470,9 +500,14 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
     const bool keep = (km >> lane) & 1u;
     const int pos = __popc(km & lt_mask);
     const int below = __popc(km & __ballot_sync(0xffffffffu, leaf >= 0 && leaf < own));
-    if (keep) sel[pos + (own < leaf ? 1 : 0)] = leaf;
+    if (keep) {
+      sel[pos + (own < leaf ? 1 : 0)] = leaf;
+      sel_slot[pos + (own < leaf ? 1 : 0)] = lane;
+    }
+    const unsigned own_at = __ballot_sync(0xffffffffu, lane < nslots && cand_leaf[lane] == own);
     if (lane == 0) {
       sel[below] = own;
+      sel_slot[below] = own_at ? __ffs(own_at) - 1 : -1;
       nsel_s = __popc(km) + 1;
     }
     __syncwarp();
@@ -495,6 +530,7 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
   const uint32_t vs = smem_u32(vmine);
   for (int si = warp; si < nsel; si += WARPS) {
     const int blk = sel[si];
+    const int slot = p.sc ? sel_slot[si] : -1;  // the leaf phase kept this block's logits
 #pragma unroll 1
     for (int hb = 0; hb < 2; ++hb) {
       const long long key0 = (long long)blk * 64 + HKEYS * hb;
@@ -510,16 +546,32 @@ __global__ void __launch_bounds__(THREADS, 4) decode_kernel(DecodeParams p, uint
       }
       cp_async_commit();
       float s[4][4];
+      if (slot >= 0) {  // the same products the leaf phase computed, in the same layout
+        const int nl = p.sc_lanes;
+        const bool kept = lane < nl;  // rows of heads past G_Q read as zero (their outputs are not written)
+        const float2* src = p.sc + (((size_t)bh * 2 * p.Ksel + slot) * 8 + 4 * hb) * p.sc_halves * nl + (kept ? lane : 0);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        const long long key = key0 + 8 * nt + r;
-        const uint16_t* krow = Kb + (size_t)(key <= T ? key : key0) * D;
+        for (int nt = 0; nt < 4; ++nt) {
+          const float2 a = kept ? ld_f2_hint(src + (size_t)nt * p.sc_halves * nl, pol_last_use) : make_float2(0.f, 0.f);
+          const float2 c = p.sc_halves == 2 ? ld_f2_hint(src + (size_t)(nt * 2 + 1) * nl, pol_last_use)
+                                            : make_float2(0.f, 0.f);
+          s[nt][0] = a.x;
+          s[nt][1] = a.y;
+          s[nt][2] = c.x;
+          s[nt][3] = c.y;
+        }
+      } else {
 #pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-          const uint4 kv = ldg16_hint(krow + 32 * j + 8 * q, pol_last_use);
-          mma_bf16_16816(s[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
-          mma_bf16_16816(s[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+        for (int nt = 0; nt < 4; ++nt) {
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          const long long key = key0 + 8 * nt + r;
+          const uint16_t* krow = Kb + (size_t)(key <= T ? key : key0) * D;
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            const uint4 kv = ldg16_hint(krow + 32 * j + 8 * q, pol_last_use);
+            mma_bf16_16816(s[nt], qa[j].x, qb[j].x, qa[j].y, qb[j].y, kv.x, kv.y);
+            mma_bf16_16816(s[nt], qa[j].z, qb[j].z, qa[j].w, qb[j].w, kv.z, kv.w);
+          }
         }
       }
       // s[nt]: rows (r | r+8) x keys key0 + 8nt + 2q + {0,1}  (the n index maps key order 1:1)
@@ -637,8 +689,8 @@ __global__ void advance_seq_len_kernel(int32_t* seq_len, int B, int N_cap) {
 
 template <int D>
 cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
-                     uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out, const Problem& pr,
-                     const Geometry& geo_cap, uint32_t* err, cudaStream_t s) {
+                     uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out, float* logits,
+                     const Problem& pr, const Geometry& geo_cap, uint32_t* err, cudaStream_t s) {
   DecodeParams p;
   p.q = q;
   p.k = k;
@@ -650,6 +702,9 @@ cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
   p.o = o;
   p.lse = lse;
   p.idx_out = idx_out;
+  p.sc = reinterpret_cast<float2*>(logits);
+  p.sc_halves = pr.GQ > 8 ? 2 : 1;
+  p.sc_lanes = 4 * (pr.GQ < 8 ? pr.GQ : 8);
   p.H_q = pr.H_q;
   p.H_kv = pr.H_kv;
   p.GQ = pr.GQ;
@@ -675,11 +730,15 @@ cudaError_t launch_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
 
 }  // namespace
 
+size_t decode_logits_bytes(const Problem& p) {
+  return (size_t)p.B * p.H_kv * 2 * p.K * 8 * (p.GQ > 8 ? 2 : 1) * 4 * (p.GQ < 8 ? p.GQ : 8) * sizeof(float2);
+}
+
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
-                          uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
+                          uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out, float* logits,
                           const Problem& p, const Geometry& geo_cap, uint32_t* err, cudaStream_t s) {
-  if (p.d == 128) return launch_d<128>(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, err, s);
-  return launch_d<64>(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, p, geo_cap, err, s);
+  if (p.d == 128) return launch_d<128>(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, logits, p, geo_cap, err, s);
+  return launch_d<64>(q, k, v, Kc, Vc, Pc, seq_len, o, lse, idx_out, logits, p, geo_cap, err, s);
 }
 
 }  // namespace pisa

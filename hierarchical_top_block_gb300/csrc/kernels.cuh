@@ -68,9 +68,11 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
                                  const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
                                  float* dV, void* ws, const Problem& p, int num_sms, cudaStream_t s);
 
-// Fused decode step.
+// Fused decode step.  logits (nullable, decode_logits_bytes(p) bytes) keeps the leaf
+// candidates' logits for the attention, which then reads no K rows of the selected blocks.
+size_t decode_logits_bytes(const Problem& p);
 cudaError_t launch_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
-                          uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
+                          uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out, float* logits,
                           const Problem& p, const Geometry& geo_cap, uint32_t* err, cudaStream_t s);
 
 // One CTA whose bounded waits run out after limit_ns (checks the timeout path).

@@ -228,6 +228,19 @@ PISA_API pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K
 PISA_API pisa_status pisa_decode_step(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc, uint16_t* Vc,
                              uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse, int32_t* idx_out,
                              pisa_shape shape, pisa_params params, pisa_stream stream);
+/* The same step with device scratch: ws (256-byte aligned, at least
+ * pisa_decode_workspace_bytes() bytes, owned by the caller, not to be used by other work
+ * until the step has run) keeps the exact leaf scoring's logits of every candidate block,
+ * B * H_kv * 2K * 64 keys * G' heads fp32 (G' = G_Q up to 8, 16 above), and the attention takes the selected
+ * blocks' logits from there instead of reading their K rows again.  The logits are the same
+ * products in the same order, so o, lse and idx equal pisa_decode_step's bit for bit.
+ * ws = NULL runs pisa_decode_step; ws_bytes below the size returns PISA_ERR_WORKSPACE.
+ * pisa_decode_workspace_bytes returns 0 for arguments pisa_decode_step refuses. */
+PISA_API size_t pisa_decode_workspace_bytes(pisa_shape shape, pisa_params params);
+PISA_API pisa_status pisa_decode_step_ws(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* Kc,
+                                         uint16_t* Vc, uint16_t* Pc, int32_t* seq_len, uint16_t* o, float* lse,
+                                         int32_t* idx_out, void* ws, size_t ws_bytes, pisa_shape shape,
+                                         pisa_params params, pisa_stream stream);
 
 /* ---- status ---------------------------------------------------------------------------- */
 

@@ -160,6 +160,13 @@ def test_parameter_rules(lib):
         (lib.pisa_sparse_attn_prefill(fake, fake, fake, ct.c_void_p((1 << 20) + 4), fake, None, shape(), p16, None), 1),
         (lib.pisa_decode_step(*([fake] * 10), shape(N=0, N_cap=0), p16, None), 1),
         (lib.pisa_decode_step(*([fake] * 10), shape(N=0, N_cap=4096), pisa.make_params(16, causal=False), None), 2),
+        # the decode step with the logits scratch: too small, misaligned, refused arguments
+        (lib.pisa_decode_step_ws(*([fake] * 10), fake, 1024, shape(N=0, N_cap=4096), p16, None), 6),
+        (lib.pisa_decode_step_ws(*([fake] * 10), ct.c_void_p((1 << 20) + 16), 1 << 40, shape(N=0, N_cap=4096), p16,
+                                 None), 1),
+        (lib.pisa_decode_step_ws(*([fake] * 10), fake, 1 << 40, shape(N=0, N_cap=0), p16, None), 1),
+        (lib.pisa_decode_step_ws(*([fake] * 10), fake, 1 << 40, shape(N=0, N_cap=4096), pisa.make_params(33), None), 2),
+        (lib.pisa_decode_step_ws(*([None] * 11), 0, shape(B=0, N=0, N_cap=4096), p16, None), 0),
         (lib.pisa_prefill_host(fake, fake, fake, fake, None, None, fake, 1 << 40, shape(N_cap=8192), p16, None), 1),
         (lib.pisa_prefill_host(fake, fake, fake, fake, None, None, ct.c_void_p((1 << 20) + 16), 1 << 40, shape(), p16,
                                None), 1),
@@ -175,3 +182,17 @@ def test_parameter_rules(lib):
         (lib.pisa_sparse_attn_backward(*([fake] * 10), ct.c_void_p((1 << 20) + 64), 1 << 40, shape(), p16, None), 1),
     ]
     assert [got for got, _ in cases] == [want for _, want in cases]
+
+
+def test_decode_workspace_bytes(lib):
+    """The decode step's logits scratch: B * H_kv * 2K candidate leaves * 8 key octets * 4 lanes
+    per head (G_Q heads up to 8, all 32 lanes twice when G_Q > 8: the second MMA row tile) of
+    fp32 pairs; 0 for the arguments the step refuses."""
+    def need(B, H_q, H_kv, K, N_cap=4096, causal=True):
+        return pisa.pisa_decode_workspace_bytes(pisa.make_shape(B, 0, H_q, H_kv, 128, N_cap),
+                                                pisa.make_params(K, causal=causal))
+    assert need(64, 32, 8, 16, N_cap=131072 + 300) == 64 * 8 * 32 * 8 * 16 * 8 == 16777216
+    assert need(4, 64, 4, 32) == 4 * 4 * 64 * 8 * 2 * 32 * 8
+    assert need(3, 24, 3, 5) == 3 * 3 * 10 * 8 * 32 * 8
+    assert need(2, 4, 4, 16) == 2 * 4 * 32 * 8 * 4 * 8
+    assert need(2, 16, 2, 33) == 0 and need(2, 16, 2, 16, N_cap=0) == 0 and need(2, 16, 2, 16, causal=False) == 0

@@ -13,7 +13,7 @@ import workloads as W
 from hierarchical_top_block_gb300.build import build
 
 COMPUTE = ("pisa_build_pyramid", "pisa_select_prefill", "pisa_select_prefill_noalloc", "pisa_sparse_attn_prefill",
-           "pisa_sparse_attn_backward", "pisa_prefill_host", "pisa_decode_step", "pisa_select_bsa")
+           "pisa_sparse_attn_backward", "pisa_prefill_host", "pisa_decode_step", "pisa_decode_step_ws", "pisa_select_bsa")
 
 
 @pytest.fixture
@@ -95,6 +95,10 @@ def test_decode_buffers(calls):
     _refused(calls, lambda: pisa.pisa_decode_step(q, k, v, Kc, Kc[:, :, :256].contiguous(), Pc, seq, w.K))
     _refused(calls, lambda: pisa.pisa_decode_step(q, k, v, Kc, Kc.clone(), Pc, seq, w.K, idx_out=idx[..., :4]))
     _refused(calls, lambda: pisa.pisa_decode_step(q, k[:, :1].contiguous(), v, Kc, Kc.clone(), Pc, seq, w.K))
+    # the same checks with the logits scratch off (pisa_decode_step) and through pisa_decode_step_ws
+    _ok(calls, lambda: pisa.pisa_decode_step(q, k, v, Kc, Kc.clone(), Pc, seq, w.K, keep_logits=False))
+    _ok(calls, lambda: pisa.pisa_decode_step_ws(q, k, v, Kc, Kc.clone(), Pc, seq, w.K, lse=lse))
+    _refused(calls, lambda: pisa.pisa_decode_step_ws(q, k, v, Kc, Kc.clone(), Pc, seq[:2], w.K))
 
 
 def test_host_prefill_buffers_checked_before_the_device_is_touched():

@@ -373,3 +373,39 @@ def test_decode_k32(oracle_impl):
     # 64 candidates at the scored levels of the walk and 64 leaf slots
     w = W.WORKLOADS["decode_128k"].with_(B=2, H_q=8, H_kv=2, K=32)
     _decode_check(oracle_impl, w, N0=64 * 160 + 50, steps=4, N_cap=16384)
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,K_sel,N0", [(8, 2, 128, 6, 2040), (16, 1, 128, 16, 64 * 37 + 61),
+                                                 (16, 1, 64, 32, 64 * 40 + 5), (4, 4, 128, 16, 3000)])
+def test_decode_kept_logits_equal_recomputed(H_q, H_kv, d, K_sel, N0):
+    """The decode step that keeps the leaf scoring's logits for the attention (pisa_decode_step_ws)
+    gives the same o, lse, idx, caches and lengths, bit for bit, as the one that reads the
+    selected blocks' K rows again (G_Q 4, 16 and 1; d 128 and 64; K up to 32; leaf boundaries
+    crossed)."""
+    w = W.WORKLOADS["decode_128k"].with_(B=3, H_q=H_q, H_kv=H_kv, d=d, K=K_sel)
+    N_cap = N0 + 128
+    wk = w.with_(N=N0)
+    Kc = torch.zeros(w.B, H_kv, N_cap, d, dtype=torch.bfloat16, device="cuda")
+    Vc = torch.zeros_like(Kc)
+    for b in range(w.B):
+        for g in range(H_kv):
+            Kc[b, g, :N0] = W.kv_slice(wk, "K", b, g, device="cuda")
+            Vc[b, g, :N0] = W.kv_slice(wk, "V", b, g, device="cuda")
+    Pc = pisa.pisa_build_pyramid(Kc, N=N0)
+    seq = torch.full((w.B,), N0, dtype=torch.int32, device="cuda")
+    state = {kept: [Kc.clone(), Vc.clone(), Pc.clone(), seq.clone()] for kept in (False, True)}
+    for s in range(70):  # crosses the leaf boundaries after N0
+        q, k, v = W.decode_step_inputs(w, s, "cuda")
+        outs = {}
+        for kept, (kc, vc, pc, sl) in state.items():
+            o = torch.empty(w.B, H_q, d, dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty(w.B, H_q, dtype=torch.float32, device="cuda")
+            idx = torch.empty(w.B, H_kv, K_sel, dtype=torch.int32, device="cuda")
+            pisa.pisa_decode_step(q, k, v, kc, vc, pc, sl, K_sel, o=o, lse=lse, idx_out=idx, keep_logits=kept)
+            outs[kept] = (o, lse, idx)
+        torch.cuda.synchronize()
+        assert pisa.pisa_get_last_device_error() == 0
+        for a, b in zip(outs[False], outs[True]):
+            assert torch.equal(a, b), s
+    for a, b in zip(state[False], state[True]):
+        assert torch.equal(a, b)
