@@ -55,8 +55,11 @@ def test_selection_quality_section_reports_needle_hits(monkeypatch, oracle_impl)
 def test_secondary_decode_times_every_step(monkeypatch):
     seen = []
 
-    def decode(q, k, v, Kc, Vc, Pc, seq, K_sel, o=None, lse=None):
-        seen.append((int(seq[0]), Kc.shape[2]))
+    def decode(q, k, v, Kc, Vc, Pc, seq, K_sel, o=None, lse=None, ws=None):
+        # the logits scratch is allocated once, at the size the library asks for
+        assert ws is not None and ws.numel() == pisa.pisa_decode_workspace_bytes(
+            pisa.make_shape(w.B, 0, w.H_q, w.H_kv, w.d, Kc.shape[2]), pisa.make_params(w.K)) > 0
+        seen.append((int(seq[0]), Kc.shape[2], ws.data_ptr()))
         seq += 1
 
     monkeypatch.setattr(pisa, "pisa_build_pyramid", lambda K, N=None: torch.empty(0))
@@ -66,7 +69,8 @@ def test_secondary_decode_times_every_step(monkeypatch):
     res = bench.secondary_decode(w, "cpu")
     assert res["steps"] == w.decode_steps == 256
     assert len(seen) == 3 + 256 and seen[0][0] == 500
-    assert all(pos < n_cap for pos, n_cap in seen) and seen[-1][0] == seen[-1][1] - 1   # the cache fills exactly
+    assert all(pos < n_cap for pos, n_cap, _ in seen) and seen[-1][0] == seen[-1][1] - 1   # the cache fills exactly
+    assert len({p for _, _, p in seen}) == 1
     assert res["step_us_mean"] == res["step_us_p50"] == 125.0
 
 
