@@ -517,7 +517,7 @@ pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, cons
   DeviceState* st;
   if ((rc = device_state(&st)) != PISA_OK) return rc;
   PhaseTimer tm(static_cast<cudaStream_t>(stream));
-  const cudaError_t e = launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms,
+  const cudaError_t e = launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms, st->err,
                                              static_cast<cudaStream_t>(stream));
   tm.mark(PH_BACKWARD);
   return cuda_status(e);

@@ -66,7 +66,7 @@ cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint1
 size_t attn_backward_workspace_bytes(const Problem& p);
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
                                  const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
-                                 float* dV, void* ws, const Problem& p, int num_sms, cudaStream_t s);
+                                 float* dV, void* ws, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s);
 
 // Fused decode step.  logits (nullable, decode_logits_bytes(p) bytes) keeps the leaf
 // candidates' logits for the attention, which then reads no K rows of the selected blocks.

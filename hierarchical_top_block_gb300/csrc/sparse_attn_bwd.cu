@@ -478,8 +478,350 @@ __global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) 
   }
 }
 
+// (4') dK, dV on tcgen05 (d = 128, G_Q of 8 or 16).  Persistent CTAs take the chunks with a
+// stride.  Per chunk: the block's K and V by TMA; per tile of 128 query-head rows (the next
+// 128 / G_Q queries of the chunk, their Q and dO rows by one 4-D TMA box each):
+//   S = Q K^T, dP = dO V^T       M 128 rows x N 64 keys x K = d, fp32 in TMEM
+//   epilogue (4 warps, one row a thread): P = exp2(S sl2 - LSE2), dS = P (dP - D), written as
+//     bf16 rows of 64 keys to shared memory (keys past t or N, and rows of absent queries, 0)
+//   dV^T += dO^T P, dK^T += Q^T dS   M 128 (d) x N 64 keys x K = rows: the Q / dO tile read
+//     as a d-major A operand and P / dS as a key-major B operand (both MN-major)
+// After the chunk's last tile the epilogue warps (TMEM lane = d) add dV^T and scale dK^T into
+// dV and dK.  Stages are double-buffered (Q/dO tiles, S/dP accumulators, P/dS tiles), and the
+// MMA thread issues a tile's S and dP before the previous tile's dV and dK, so the tensor pipe
+// has work while the epilogue turns S into P.  Every wait is bounded.
+namespace tcb {
+constexpr int THREADS = 192;                    // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int ROWS = 128, KEYS = 64;
+constexpr uint32_t QT_BYTES = ROWS * 128 * 2;   // a Q or dO tile, 32 KB
+constexpr uint32_t KV_BYTES = KEYS * 128 * 2;   // a K or V block, 16 KB
+constexpr uint32_t PS_BYTES = ROWS * KEYS * 2;  // a P or dS tile, 16 KB
+constexpr size_t SMEM = 4 * QT_BYTES + 2 * KV_BYTES + 4 * PS_BYTES + 1024;
+constexpr uint32_t COL_DV = 256, COL_DK = 320;  // TMEM: S of buffer b at 128 b, dP at 128 b + 64
+}  // namespace tcb
+
+__device__ __forceinline__ void tmem_ld32_cols(uint32_t taddr, float (&f)[32]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+}
+
+__global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                                     const __grid_constant__ CUtensorMap mapO,
+                                                                     const __grid_constant__ CUtensorMap mapK,
+                                                                     const __grid_constant__ CUtensorMap mapV,
+                                                                     BwdParams p, uint32_t* err) {
+  using namespace tcb;
+  constexpr int D = 128;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem;                        // stage st: Q at 2 st, dO at 2 st + 1 (QT_BYTES each)
+  uint8_t* sK = smem + 4 * QT_BYTES;
+  uint8_t* sV = sK + KV_BYTES;
+  uint8_t* sP = sV + KV_BYTES;               // buffer b: P at 2 b, dS at 2 b + 1 (PS_BYTES each)
+  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2],
+      acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_base_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunks = *p.nchunks;
+  const int RPQ = p.GQ, QPT = ROWS / p.GQ;  // rows per query, queries per tile
+
+  // stale rows of a partial tile must be finite: zero both Q/dO stages once
+  for (uint32_t i = threadIdx.x; i < 4 * QT_BYTES / 16; i += THREADS)
+    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async();
+  if (threadIdx.x == 0) {
+    mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 4);
+    mbar_init(&drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_empty[i], 1);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_s;
+
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    bool failed = false;
+    uint32_t tt = 0, cc = 0;
+    for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
+      const int4 ch = p.chunks[ci];
+      const int bh = ch.x, blk = ch.y, first = ch.z, cnt = ch.w;
+      const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+      if (!mbar_wait_warp(&kv_empty, (cc & 1) ^ 1, err)) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&kv_full, 2 * KV_BYTES);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(sK + h * (KEYS * 128), &mapK, &kv_full, 64 * h, blk * KEYS, bh);
+          tma_load_3d(sV + h * (KEYS * 128), &mapV, &kv_full, 64 * h, blk * KEYS, bh);
+        }
+        if (ci + (int)gridDim.x < nchunks) {  // the next chunk's block towards L2
+          const int4 nx = p.chunks[ci + gridDim.x];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_prefetch_3d(&mapK, 64 * h, nx.y * KEYS, nx.x);
+            tma_prefetch_3d(&mapV, 64 * h, nx.y * KEYS, nx.x);
+          }
+        }
+      }
+      // the rows of the tile after the next one towards L2, while the next ones load
+      auto prefetch_tile = [&](int kk) {
+        if (kk < cnt && lane < min(QPT, cnt - kk)) {
+          const int t = p.entries[first + kk + lane];
+          const long long row = ((long long)b * p.N + t) * p.H_q + (long long)hk * p.GQ;
+          tma_prefetch_4d(&mapQ, 0, 0, 0, (int)(row >> 3));
+          tma_prefetch_4d(&mapO, 0, 0, 0, (int)(row >> 3));
+        }
+      };
+      prefetch_tile(0);
+      prefetch_tile(QPT);
+      for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
+        const int st = tt & 1;
+        if (!mbar_wait_warp(&q_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
+          failed = true;
+          break;
+        }
+        const int nq = min(QPT, cnt - k0);
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[st], (uint32_t)nq * 2 * RPQ * 256);
+        __syncwarp();
+        if (lane < nq) {
+          const int t = p.entries[first + k0 + lane];
+          const long long row = ((long long)b * p.N + t) * p.H_q + (long long)hk * p.GQ;
+          tma_load_4d(sQ + (2 * st) * QT_BYTES + lane * RPQ * 256, &mapQ, &q_full[st], 0, 0, 0, (int)(row >> 3));
+          tma_load_4d(sQ + (2 * st + 1) * QT_BYTES + lane * RPQ * 256, &mapO, &q_full[st], 0, 0, 0, (int)(row >> 3));
+        }
+        prefetch_tile(k0 + 2 * QPT);
+      }
+    }
+    // after a timeout, copies still in flight land before shared memory goes away (bounded)
+    if (failed && lane == 0) {
+      if (cc > 0) mbar_wait(&kv_full, (cc - 1) & 1, err, 100000000ull);
+      for (uint32_t u = tt > 2 ? tt - 2 : 0; u < tt; ++u) mbar_wait(&q_full[u & 1], (u >> 1) & 1, err, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16_f32(ROWS, KEYS);
+      constexpr uint32_t id_mn = id_kk | (1u << 15) | (1u << 16);  // A and B MN-major
+      bool failed = false;
+      // a tile's dV and dK products, issued after the next tile's S and dP
+      int pend = -1;             // tile index tt of the pending products, or -1
+      bool pend_first = false, pend_last = false;
+      uint32_t pend_cc = 0;
+      auto dvdk = [&](uint32_t u, bool first_of_chunk, bool last_of_chunk, uint32_t c) -> bool {
+        const int su = u & 1;
+        if (!mbar_wait(&p_full[su], (u >> 1) & 1, err)) return false;
+        if (first_of_chunk && !mbar_wait(&acc_empty, (c & 1) ^ 1, err)) return false;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(sQ + (2 * su) * QT_BYTES), ob = smem_u32(sQ + (2 * su + 1) * QT_BYTES);
+        const uint32_t pb = smem_u32(sP + (2 * su) * PS_BYTES), db = smem_u32(sP + (2 * su + 1) * PS_BYTES);
+#pragma unroll
+        for (int s = 0; s < ROWS / 16; ++s) {  // K = rows: 16 rows = two 8-row groups per step
+          const uint32_t acc = (first_of_chunk && s == 0) ? 0u : 1u;
+          umma_bf16(tmem_base + COL_DV, smem_desc_sw128(ob + s * 4096, 1024, 2048), smem_desc_sw128(pb + s * 2048, 8192, 1024),
+                    id_mn, acc);
+          umma_bf16(tmem_base + COL_DK, smem_desc_sw128(qb + s * 4096, 1024, 2048), smem_desc_sw128(db + s * 2048, 8192, 1024),
+                    id_mn, acc);
+        }
+        umma_commit(&p_empty[su]);
+        umma_commit(&q_empty[su]);
+        if (last_of_chunk) umma_commit(&acc_full);
+        return true;
+      };
+      uint32_t tt = 0, cc = 0;
+      for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
+        const int cnt = p.chunks[ci].w;
+        if (!mbar_wait(&kv_full, cc & 1, err)) {
+          failed = true;
+          break;
+        }
+        const uint32_t kb = smem_u32(sK), vb = smem_u32(sV);
+        for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
+          const int st = tt & 1;
+          if (!mbar_wait(&q_full[st], (tt >> 1) & 1, err) || !mbar_wait(&s_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qb = smem_u32(sQ + (2 * st) * QT_BYTES), ob = smem_u32(sQ + (2 * st + 1) * QT_BYTES);
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s) {  // K = d; grouped rows: d half h of 8-row group g at g 2048 + h 1024
+            const uint32_t aoff = (s >> 2) * 1024 + (s & 3) * 32, boff = (s >> 2) * (KEYS * 128) + (s & 3) * 32;
+            umma_bf16(tmem_base + st * 128, smem_desc_sw128(qb + aoff, 16, 2048), smem_desc_sw128(kb + boff, 16, 1024),
+                      id_kk, s > 0 ? 1u : 0u);
+            umma_bf16(tmem_base + st * 128 + 64, smem_desc_sw128(ob + aoff, 16, 2048), smem_desc_sw128(vb + boff, 16, 1024),
+                      id_kk, s > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[st]);
+          if (k0 + QPT >= cnt) umma_commit(&kv_empty);  // the block's K and V are no longer read
+          if (pend >= 0 && !dvdk((uint32_t)pend, pend_first, pend_last, pend_cc)) {
+            failed = true;
+            break;
+          }
+          pend = (int)tt;
+          pend_first = k0 == 0;
+          pend_last = k0 + QPT >= cnt;
+          pend_cc = cc;
+        }
+      }
+      if (!failed && pend >= 0) dvdk((uint32_t)pend, pend_first, pend_last, pend_cc);
+      // every MMA issued has completed before the tensor memory is released (bounded)
+      umma_commit(&drain);
+      mbar_wait(&drain, 0, err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;       // TMEM lane: query-head row for S / dP, d for dV^T / dK^T
+    const int qi = row / RPQ, h = row - qi * RPQ;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    uint32_t tt = 0, cc = 0;
+    bool failed = false;
+    for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
+      const int4 ch = p.chunks[ci];
+      const int bh = ch.x, blk = ch.y, first = ch.z, cnt = ch.w;
+      const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+      const int key0 = blk * KEYS;
+      for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
+        const int st = tt & 1;
+        const bool vq = k0 + qi < cnt;
+        const int t = vq ? p.entries[first + k0 + qi] : 0;
+        float lse2 = POS_INF, dsum = 0.f;
+        if (vq) {
+          const size_t li = ((size_t)b * p.H_q + (size_t)hk * p.GQ + h) * p.N + t;
+          const float l = p.LSE[li];
+          lse2 = l == NEG_INF ? POS_INF : l * LOG2E;
+          dsum = p.Dsum[li];
+        }
+        const int last = vq ? (p.causal ? min(t, p.N - 1) : p.N - 1) - key0 : -1;  // visible keys j <= last
+        if (!mbar_wait_warp(&s_full[st], (tt >> 1) & 1, err)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        float pv[64], dpv[64];
+        uint32_t pk[32];
+        // S (64 columns) in one round trip, then P; then dP likewise, and dS = P (dP - D)
+        tmem_ld32_cols(lane_base + st * 128, *reinterpret_cast<float(*)[32]>(&pv[0]));
+        tmem_ld32_cols(lane_base + st * 128 + 32, *reinterpret_cast<float(*)[32]>(&pv[32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 64; ++j) pv[j] = (j <= last) ? fast_exp2(fmaf(pv[j], p.sl2, -lse2)) : 0.f;
+        tmem_ld32_cols(lane_base + st * 128 + 64, *reinterpret_cast<float(*)[32]>(&dpv[0]));
+        tmem_ld32_cols(lane_base + st * 128 + 96, *reinterpret_cast<float(*)[32]>(&dpv[32]));
+        tmem_wait_ld();
+        uint32_t dk2[32];
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) dk2[j / 2] = pack_bf16x2(pv[j] * (dpv[j] - dsum), pv[j + 1] * (dpv[j + 1] - dsum));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(pv[2 * j], pv[2 * j + 1]);
+        // S and dP are read out: the MMA may reuse this buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[st]);
+        if (!mbar_wait_warp(&p_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
+          failed = true;
+          break;
+        }
+        uint8_t* prow = sP + (2 * st) * PS_BYTES + row * 128;
+        uint8_t* drow = sP + (2 * st + 1) * PS_BYTES + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c (keys 8c .. 8c + 7), 128-byte swizzle
+          const uint32_t off = (uint32_t)((c ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+        }
+        fence_proxy_async();  // the MMA reads the tiles through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[st]);
+      }
+      if (failed) break;
+      // the chunk's dV^T and dK^T (lane = d): add into dV and scale x dK (keys past N carry none)
+      if (!mbar_wait_warp(&acc_full, cc & 1, err)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      float* dKg = p.dK + ((size_t)bh * p.N_cap) * D;
+      float* dVg = p.dV + ((size_t)bh * p.N_cap) * D;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float v32[32], k32[32];
+        tmem_ld32_cols(lane_base + COL_DV + 32 * c, v32);
+        tmem_ld32_cols(lane_base + COL_DK + 32 * c, k32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int key = key0 + 32 * c + j;
+          if (key < p.N) {
+            red_add(dVg + (size_t)key * D + row, v32[j]);
+            red_add(dKg + (size_t)key * D + row, k32[j] * p.scale);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+cudaError_t launch_dkv_tc(BwdParams& p, long long max_chunks, int num_sms, uint32_t* err, cudaStream_t s) {
+  constexpr int D = 128;
+  CUtensorMap mapQ, mapO, mapK, mapV;
+  const long long rows = (long long)p.B * p.N * p.H_q;
+  {
+    // one box per query: (64 columns, 8 rows, 2 d halves, G_Q / 8 row groups), lands as
+    // [row group][half][8 rows][64]
+    const uint64_t dims[4] = {64, 8, 2, (uint64_t)(rows / 8)};
+    const uint64_t strides[3] = {(uint64_t)D * 2, 128, (uint64_t)8 * D * 2};
+    const uint32_t box[4] = {64, 8, 2, (uint32_t)(p.GQ / 8)};
+    if (!encode_tensor_map(&mapQ, p.Q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_tensor_map(&mapO, p.dO, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.N, (uint64_t)p.B * p.H_kv};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.N_cap * D * 2};
+    const uint32_t box[3] = {64, (uint32_t)tcb::KEYS, 1};
+    if (!encode_tensor_map(&mapK, p.K, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_tensor_map(&mapV, p.V, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcb::SMEM);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<long long>(max_chunks, (long long)num_sms);
+  if (grid > 0) bwd_dkv_tc_kernel<<<grid, tcb::THREADS, tcb::SMEM, s>>>(mapQ, mapO, mapK, mapV, p, err);
+  return cudaGetLastError();
+}
+
 template <int D>
-cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_chunks, int num_sms, cudaStream_t s) {
+cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_chunks, int num_sms, uint32_t* err,
+                     cudaStream_t s) {
   cudaError_t e;
   const long long rows = (long long)p.B * p.N * p.H_q;
   const long long ents = (long long)p.B * p.H_kv * p.N * p.Ksel;
@@ -501,6 +843,7 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) !=
       cudaSuccess)
     return e;
+  if (D == 128 && (p.GQ == 8 || p.GQ == 16) && p.H_q % 8 == 0) return launch_dkv_tc(p, max_chunks, num_sms, err, s);
   if (max_chunks > 0) bwd_dkv_kernel<D><<<(int)max_chunks, 32 * KV_WARPS, smem_kv, s>>>(p);
   return cudaGetLastError();
 }
@@ -519,7 +862,7 @@ size_t attn_backward_workspace_bytes(const Problem& p) {
 
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
                                  const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
-                                 float* dV, void* ws, const Problem& pr, int num_sms, cudaStream_t s) {
+                                 float* dV, void* ws, const Problem& pr, int num_sms, uint32_t* err, cudaStream_t s) {
   BwdParams p;
   p.Q = Q;
   p.K = K;
@@ -567,8 +910,8 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   if ((e = cudaMemsetAsync(p.cursor, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dK, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dV, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
-  if (pr.d == 128) return launch_d<128>(p, (int)nkeys, chunk_off, max_chunks, num_sms, s);
-  return launch_d<64>(p, (int)nkeys, chunk_off, max_chunks, num_sms, s);
+  if (pr.d == 128) return launch_d<128>(p, (int)nkeys, chunk_off, max_chunks, num_sms, err, s);
+  return launch_d<64>(p, (int)nkeys, chunk_off, max_chunks, num_sms, err, s);
 }
 
 }  // namespace pisa

@@ -60,6 +60,18 @@ def test_backward_non_causal(oracle_impl):
     _check(oracle_impl, w, 3, causal=False, seed=2)
 
 
+def test_backward_non_causal_gq16(oracle_impl):
+    # the tensor-core dK/dV path (G_Q = 16, d = 128) without the causal mask, ragged N
+    w = W.WORKLOADS["prefill_4k"].with_(B=1, N=64 * 12 + 17, H_q=16, H_kv=1, K=5)
+    _check(oracle_impl, w, 5, causal=False, seed=4)
+
+
+def test_backward_gq8_two_sequences(oracle_impl):
+    # G_Q = 8 (16 queries a tile on the tensor-core path), two sequences, two KV heads
+    w = W.WORKLOADS["prefill_4k"].with_(B=2, N=64 * 20 + 3, H_q=16, H_kv=2, K=7)
+    _check(oracle_impl, w, 7, seed=5)
+
+
 def _planted_selection(N, K_sel, seed):
     """Every query keeps its own block, blocks 0 and 1 (when eligible) and random other eligible
     blocks up to K: blocks 0 and 1 are then selected by every query, more than the 256 queries
