@@ -482,30 +482,29 @@ __global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) 
 // stride.  Per chunk: the block's K and V by TMA; per tile of 128 query-head rows (the next
 // 128 / G_Q queries of the chunk, their Q and dO rows by one 4-D TMA box each):
 //   S = Q K^T, dP = dO V^T       M 128 rows x N 64 keys x K = d, fp32 in TMEM
-//   epilogue (4 warps, one row a thread): P = exp2(S sl2 - LSE2), dS = P (dP - D), written as
-//     bf16 rows of 64 keys to shared memory (keys past t or N, and rows of absent queries, 0)
+//   epilogue (one row a thread): P = exp2(S sl2 - LSE2), dS = P (dP - D), written as bf16 rows
+//     of 64 keys to shared memory (keys past t or N, and rows of absent queries, 0)
 //   dV^T += dO^T P, dK^T += Q^T dS   M 128 (d) x N 64 keys x K = rows: the Q / dO tile read
 //     as a d-major A operand and P / dS as a key-major B operand (both MN-major)
-// After the chunk's last tile the epilogue warps (TMEM lane = d) add dV^T and scale dK^T into
-// dV and dK.  Stages are double-buffered (Q/dO tiles, S/dP accumulators, P/dS tiles), and the
-// MMA thread issues a tile's S and dP before the previous tile's dV and dK, so the tensor pipe
-// has work while the epilogue turns S into P.  Every wait is bounded.
+// After the chunk's last tile, TMEM lane = d, dV^T is added into dV and scale x dK^T into dK.
+// Roles: a producer warp (TMA), one thread issuing every tile's S and dP, another issuing the
+// dV and dK products, and two epilogue groups of eight warps taking alternate tiles (two warps
+// a TMEM lane quarter, 32 keys each), so that one tile's S and dP run on the tensor pipe while
+// the other group turns the previous tile's into P and dS.  Stages are double-buffered (Q/dO tiles, S/dP accumulators and P/dS tiles,
+// stage = tile parity = epilogue group) and so are the dV/dK accumulators (set = chunk
+// parity; the group of that parity adds a chunk's set into dV and dK while the other chunk's
+// tiles go on).  Every wait is bounded.
 namespace tcb {
-constexpr int THREADS = 192;                    // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int THREADS = 608;                    // warp 0 producer, warps 1-2 MMA issuers, 3-18 epilogue
+constexpr int EPI_WARP0 = 3, EPI_GROUP_WARPS = 8;
 constexpr int ROWS = 128, KEYS = 64;
 constexpr uint32_t QT_BYTES = ROWS * 128 * 2;   // a Q or dO tile, 32 KB
 constexpr uint32_t KV_BYTES = KEYS * 128 * 2;   // a K or V block, 16 KB
 constexpr uint32_t PS_BYTES = ROWS * KEYS * 2;  // a P or dS tile, 16 KB
 constexpr size_t SMEM = 4 * QT_BYTES + 2 * KV_BYTES + 4 * PS_BYTES + 1024;
-constexpr uint32_t COL_DV = 256, COL_DK = 320;  // TMEM: S of buffer b at 128 b, dP at 128 b + 64
+// TMEM columns: S of stage b at 128 b, dP at 128 b + 64; dV^T of set a at 256 + 128 a, dK^T 64 further
+constexpr uint32_t COL_ACC = 256;
 }  // namespace tcb
-
-__device__ __forceinline__ void tmem_ld32_cols(uint32_t taddr, float (&f)[32]) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-#pragma unroll
-  for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
-}
 
 __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                                      const __grid_constant__ CUtensorMap mapO,
@@ -519,9 +518,10 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
   uint8_t* sQ = smem;                        // stage st: Q at 2 st, dO at 2 st + 1 (QT_BYTES each)
   uint8_t* sK = smem + 4 * QT_BYTES;
   uint8_t* sV = sK + KV_BYTES;
-  uint8_t* sP = sV + KV_BYTES;               // buffer b: P at 2 b, dS at 2 b + 1 (PS_BYTES each)
-  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2],
-      acc_full, acc_empty, drain;
+  uint8_t* sP = sV + KV_BYTES;               // stage st: P at 2 st, dS at 2 st + 1 (PS_BYTES each)
+  // q_full[st]: the stage's Q rows landed; o_full[st]: its dO rows
+  __shared__ uint64_t kv_full, kv_empty, q_full[2], o_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2],
+      p_empty[2], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_base_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = *p.nchunks;
@@ -534,16 +534,17 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
   if (threadIdx.x == 0) {
     mbar_init(&kv_full, 1);
     mbar_init(&kv_empty, 1);
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 4);
-    mbar_init(&drain, 1);
+    mbar_init(&drain, 2);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
+      mbar_init(&o_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_empty[i], EPI_GROUP_WARPS);
+      mbar_init(&p_full[i], EPI_GROUP_WARPS);
       mbar_init(&p_empty[i], 1);
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], EPI_GROUP_WARPS);
     }
     mbar_fence_init();
   }
@@ -583,72 +584,57 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
           }
         }
       }
-      // the rows of the tile after the next one towards L2, while the next ones load
-      auto prefetch_tile = [&](int kk) {
-        if (kk < cnt && lane < min(QPT, cnt - kk)) {
-          const int t = p.entries[first + kk + lane];
-          const long long row = ((long long)b * p.N + t) * p.H_q + (long long)hk * p.GQ;
-          tma_prefetch_4d(&mapQ, 0, 0, 0, (int)(row >> 3));
-          tma_prefetch_4d(&mapO, 0, 0, 0, (int)(row >> 3));
+      // lane l's query of the tile starting at entry kk (-1 past the chunk); a tile's queries
+      // are read two tiles ahead, when its rows are prefetched towards L2
+      auto entry = [&](int kk) -> int {
+        return (kk < cnt && lane < min(QPT, cnt - kk)) ? p.entries[first + kk + lane] : -1;
+      };
+      auto q_row = [&](int t) -> int { return (int)((((long long)b * p.N + t) * p.H_q + (long long)hk * p.GQ) >> 3); };
+      auto prefetch_rows = [&](int t) {
+        if (t >= 0) {
+          tma_prefetch_4d(&mapQ, 0, 0, 0, q_row(t));
+          tma_prefetch_4d(&mapO, 0, 0, 0, q_row(t));
         }
       };
-      prefetch_tile(0);
-      prefetch_tile(QPT);
+      int t_cur = entry(0), t_next = entry(QPT);
+      prefetch_rows(t_cur);
+      prefetch_rows(t_next);
       for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
         const int st = tt & 1;
+        const int t_after = entry(k0 + 2 * QPT);  // in flight while the stage frees
         if (!mbar_wait_warp(&q_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
           failed = true;
           break;
         }
         const int nq = min(QPT, cnt - k0);
-        if (lane == 0) mbar_arrive_expect_tx(&q_full[st], (uint32_t)nq * 2 * RPQ * 256);
-        __syncwarp();
-        if (lane < nq) {
-          const int t = p.entries[first + k0 + lane];
-          const long long row = ((long long)b * p.N + t) * p.H_q + (long long)hk * p.GQ;
-          tma_load_4d(sQ + (2 * st) * QT_BYTES + lane * RPQ * 256, &mapQ, &q_full[st], 0, 0, 0, (int)(row >> 3));
-          tma_load_4d(sQ + (2 * st + 1) * QT_BYTES + lane * RPQ * 256, &mapO, &q_full[st], 0, 0, 0, (int)(row >> 3));
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[st], (uint32_t)nq * RPQ * 256);
+          mbar_arrive_expect_tx(&o_full[st], (uint32_t)nq * RPQ * 256);
         }
-        prefetch_tile(k0 + 2 * QPT);
+        __syncwarp();
+        // the Q rows first: S starts on them while the dO rows land
+        if (lane < nq) tma_load_4d(sQ + (2 * st) * QT_BYTES + lane * RPQ * 256, &mapQ, &q_full[st], 0, 0, 0, q_row(t_cur));
+        if (lane < nq) tma_load_4d(sQ + (2 * st + 1) * QT_BYTES + lane * RPQ * 256, &mapO, &o_full[st], 0, 0, 0, q_row(t_cur));
+        prefetch_rows(t_after);
+        t_cur = t_next;
+        t_next = t_after;
       }
     }
     // after a timeout, copies still in flight land before shared memory goes away (bounded)
     if (failed && lane == 0) {
       if (cc > 0) mbar_wait(&kv_full, (cc - 1) & 1, err, 100000000ull);
-      for (uint32_t u = tt > 2 ? tt - 2 : 0; u < tt; ++u) mbar_wait(&q_full[u & 1], (u >> 1) & 1, err, 100000000ull);
+      for (uint32_t u = tt > 2 ? tt - 2 : 0; u < tt; ++u) {
+        mbar_wait(&q_full[u & 1], (u >> 1) & 1, err, 100000000ull);
+        mbar_wait(&o_full[u & 1], (u >> 1) & 1, err, 100000000ull);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
+    // ------------------- MMA issuer: S = Q K^T and dP = dO V^T -------------------
     if (lane == 0) {
       constexpr uint32_t id_kk = idesc_bf16_f32(ROWS, KEYS);
-      constexpr uint32_t id_mn = id_kk | (1u << 15) | (1u << 16);  // A and B MN-major
-      bool failed = false;
-      // a tile's dV and dK products, issued after the next tile's S and dP
-      int pend = -1;             // tile index tt of the pending products, or -1
-      bool pend_first = false, pend_last = false;
-      uint32_t pend_cc = 0;
-      auto dvdk = [&](uint32_t u, bool first_of_chunk, bool last_of_chunk, uint32_t c) -> bool {
-        const int su = u & 1;
-        if (!mbar_wait(&p_full[su], (u >> 1) & 1, err)) return false;
-        if (first_of_chunk && !mbar_wait(&acc_empty, (c & 1) ^ 1, err)) return false;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(sQ + (2 * su) * QT_BYTES), ob = smem_u32(sQ + (2 * su + 1) * QT_BYTES);
-        const uint32_t pb = smem_u32(sP + (2 * su) * PS_BYTES), db = smem_u32(sP + (2 * su + 1) * PS_BYTES);
-#pragma unroll
-        for (int s = 0; s < ROWS / 16; ++s) {  // K = rows: 16 rows = two 8-row groups per step
-          const uint32_t acc = (first_of_chunk && s == 0) ? 0u : 1u;
-          umma_bf16(tmem_base + COL_DV, smem_desc_sw128(ob + s * 4096, 1024, 2048), smem_desc_sw128(pb + s * 2048, 8192, 1024),
-                    id_mn, acc);
-          umma_bf16(tmem_base + COL_DK, smem_desc_sw128(qb + s * 4096, 1024, 2048), smem_desc_sw128(db + s * 2048, 8192, 1024),
-                    id_mn, acc);
-        }
-        umma_commit(&p_empty[su]);
-        umma_commit(&q_empty[su]);
-        if (last_of_chunk) umma_commit(&acc_full);
-        return true;
-      };
       uint32_t tt = 0, cc = 0;
+      bool failed = false;
       for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
         const int cnt = p.chunks[ci].w;
         if (!mbar_wait(&kv_full, cc & 1, err)) {
@@ -664,38 +650,75 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
           }
           tc_fence_after();
           const uint32_t qb = smem_u32(sQ + (2 * st) * QT_BYTES), ob = smem_u32(sQ + (2 * st + 1) * QT_BYTES);
+          // K = d; grouped rows: d half h of 8-row group g at g 2048 + h 1024
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s) {  // K = d; grouped rows: d half h of 8-row group g at g 2048 + h 1024
-            const uint32_t aoff = (s >> 2) * 1024 + (s & 3) * 32, boff = (s >> 2) * (KEYS * 128) + (s & 3) * 32;
-            umma_bf16(tmem_base + st * 128, smem_desc_sw128(qb + aoff, 16, 2048), smem_desc_sw128(kb + boff, 16, 1024),
-                      id_kk, s > 0 ? 1u : 0u);
-            umma_bf16(tmem_base + st * 128 + 64, smem_desc_sw128(ob + aoff, 16, 2048), smem_desc_sw128(vb + boff, 16, 1024),
-                      id_kk, s > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[st]);
-          if (k0 + QPT >= cnt) umma_commit(&kv_empty);  // the block's K and V are no longer read
-          if (pend >= 0 && !dvdk((uint32_t)pend, pend_first, pend_last, pend_cc)) {
+          for (int s = 0; s < D / 16; ++s)
+            umma_bf16(tmem_base + st * 128, smem_desc_sw128(qb + (s >> 2) * 1024 + (s & 3) * 32, 16, 2048),
+                      smem_desc_sw128(kb + (s >> 2) * (KEYS * 128) + (s & 3) * 32, 16, 1024), id_kk, s > 0 ? 1u : 0u);
+          if (!mbar_wait(&o_full[st], (tt >> 1) & 1, err)) {
             failed = true;
             break;
           }
-          pend = (int)tt;
-          pend_first = k0 == 0;
-          pend_last = k0 + QPT >= cnt;
-          pend_cc = cc;
+          tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s)
+            umma_bf16(tmem_base + st * 128 + 64, smem_desc_sw128(ob + (s >> 2) * 1024 + (s & 3) * 32, 16, 2048),
+                      smem_desc_sw128(vb + (s >> 2) * (KEYS * 128) + (s & 3) * 32, 16, 1024), id_kk, s > 0 ? 1u : 0u);
+          umma_commit(&s_full[st]);
+          if (k0 + QPT >= cnt) umma_commit(&kv_empty);  // the block's K and V are no longer read
         }
       }
-      if (!failed && pend >= 0) dvdk((uint32_t)pend, pend_first, pend_last, pend_cc);
       // every MMA issued has completed before the tensor memory is released (bounded)
+      umma_commit(&drain);
+      mbar_wait(&drain, 0, err);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------ MMA issuer: dV^T += dO^T P and dK^T += Q^T dS ------------------
+    if (lane == 0) {
+      constexpr uint32_t id_mn = idesc_bf16_f32(ROWS, KEYS) | (1u << 15) | (1u << 16);  // A and B MN-major
+      uint32_t tt = 0, cc = 0;
+      bool failed = false;
+      for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
+        const int cnt = p.chunks[ci].w;
+        const int a = cc & 1;
+        const uint32_t col = tmem_base + COL_ACC + 128 * a;
+        for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
+          const int st = tt & 1;
+          if (!mbar_wait(&p_full[st], (tt >> 1) & 1, err) ||
+              (k0 == 0 && !mbar_wait(&acc_empty[a], ((cc >> 1) & 1) ^ 1, err))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qb = smem_u32(sQ + (2 * st) * QT_BYTES), ob = smem_u32(sQ + (2 * st + 1) * QT_BYTES);
+          const uint32_t pb = smem_u32(sP + (2 * st) * PS_BYTES), db = smem_u32(sP + (2 * st + 1) * PS_BYTES);
+#pragma unroll
+          for (int s = 0; s < ROWS / 16; ++s) {  // K = rows: 16 rows = two 8-row groups per step
+            const uint32_t acc = (k0 == 0 && s == 0) ? 0u : 1u;
+            umma_bf16(col, smem_desc_sw128(ob + s * 4096, 1024, 2048), smem_desc_sw128(pb + s * 2048, 8192, 1024), id_mn,
+                      acc);
+            umma_bf16(col + 64, smem_desc_sw128(qb + s * 4096, 1024, 2048), smem_desc_sw128(db + s * 2048, 8192, 1024),
+                      id_mn, acc);
+          }
+          umma_commit(&p_empty[st]);
+          umma_commit(&q_empty[st]);
+          if (k0 + QPT >= cnt) umma_commit(&acc_full[a]);
+        }
+      }
       umma_commit(&drain);
       mbar_wait(&drain, 0, err);
     }
     __syncwarp();
   } else {
     // ------------------------------ epilogue ------------------------------
+    const int g = (warp - EPI_WARP0) / EPI_GROUP_WARPS;  // group: the tiles (and the stage) of parity g
+    const int kh = ((warp - EPI_WARP0) % EPI_GROUP_WARPS) >> 2;  // keys 32 kh .. 32 kh + 31 of the block
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;       // TMEM lane: query-head row for S / dP, d for dV^T / dK^T
     const int qi = row / RPQ, h = row - qi * RPQ;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const int st = g;
     uint32_t tt = 0, cc = 0;
     bool failed = false;
     for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
@@ -704,7 +727,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
       const int key0 = blk * KEYS;
       for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
-        const int st = tt & 1;
+        if ((int)(tt & 1) != g) continue;
         const bool vq = k0 + qi < cnt;
         const int t = vq ? p.entries[first + k0 + qi] : 0;
         float lse2 = POS_INF, dsum = 0.f;
@@ -720,69 +743,76 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
           break;
         }
         tc_fence_after();
-        float pv[64], dpv[64];
-        uint32_t pk[32];
-        // S (64 columns) in one round trip, then P; then dP likewise, and dS = P (dP - D)
-        tmem_ld32_cols(lane_base + st * 128, *reinterpret_cast<float(*)[32]>(&pv[0]));
-        tmem_ld32_cols(lane_base + st * 128 + 32, *reinterpret_cast<float(*)[32]>(&pv[32]));
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 64; ++j) pv[j] = (j <= last) ? fast_exp2(fmaf(pv[j], p.sl2, -lse2)) : 0.f;
-        tmem_ld32_cols(lane_base + st * 128 + 64, *reinterpret_cast<float(*)[32]>(&dpv[0]));
-        tmem_ld32_cols(lane_base + st * 128 + 96, *reinterpret_cast<float(*)[32]>(&dpv[32]));
-        tmem_wait_ld();
-        uint32_t dk2[32];
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) dk2[j / 2] = pack_bf16x2(pv[j] * (dpv[j] - dsum), pv[j + 1] * (dpv[j + 1] - dsum));
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(pv[2 * j], pv[2 * j + 1]);
-        // S and dP are read out: the MMA may reuse this buffer
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[st]);
+        // P and dS go to this stage's tiles once the previous tile of the stage has been consumed
         if (!mbar_wait_warp(&p_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
           failed = true;
           break;
         }
         uint8_t* prow = sP + (2 * st) * PS_BYTES + row * 128;
         uint8_t* drow = sP + (2 * st + 1) * PS_BYTES + row * 128;
+        // this warp's 32 keys, 16 at a time: S and dP in one round trip, then P and dS = P (dP - D)
+        // as bf16 into two 16-byte chunks of each row (128-byte swizzle)
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int j0 = 32 * kh + 16 * hf;  // first key of the step
+          uint32_t sr[16], dr[16];
+          tmem_ld16(lane_base + st * 128 + j0, sr);
+          tmem_ld16(lane_base + st * 128 + 64 + j0, dr);
+          tmem_wait_ld();
+          if (hf == 1) {  // S and dP are read out: the MMA may reuse this buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[st]);
+          }
+          uint32_t pk[8], dk2[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c (keys 8c .. 8c + 7), 128-byte swizzle
-          const uint32_t off = (uint32_t)((c ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+          for (int j = 0; j < 16; j += 2) {
+            const float p0 = (j0 + j <= last) ? fast_exp2(fmaf(__uint_as_float(sr[j]), p.sl2, -lse2)) : 0.f;
+            const float p1 = (j0 + j + 1 <= last) ? fast_exp2(fmaf(__uint_as_float(sr[j + 1]), p.sl2, -lse2)) : 0.f;
+            pk[j / 2] = pack_bf16x2(p0, p1);
+            dk2[j / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[j]) - dsum), p1 * (__uint_as_float(dr[j + 1]) - dsum));
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {  // 16-byte chunk j0 / 8 + c of the row
+            const uint32_t off = (uint32_t)(((j0 / 8 + c) ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+          }
         }
         fence_proxy_async();  // the MMA reads the tiles through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[st]);
       }
       if (failed) break;
+      if ((int)(cc & 1) != g) continue;
       // the chunk's dV^T and dK^T (lane = d): add into dV and scale x dK (keys past N carry none)
-      if (!mbar_wait_warp(&acc_full, cc & 1, err)) {
+      if (!mbar_wait_warp(&acc_full[g], (cc >> 1) & 1, err)) {
         failed = true;
         break;
       }
       tc_fence_after();
       float* dKg = p.dK + ((size_t)bh * p.N_cap) * D;
       float* dVg = p.dV + ((size_t)bh * p.N_cap) * D;
+      const uint32_t col = lane_base + COL_ACC + 128 * g;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v32[32], k32[32];
-        tmem_ld32_cols(lane_base + COL_DV + 32 * c, v32);
-        tmem_ld32_cols(lane_base + COL_DK + 32 * c, k32);
+      for (int c = 0; c < 2; ++c) {  // this warp's 32 keys, 16 at a time
+        const int j0 = 32 * kh + 16 * c;
+        uint32_t vr[16], kr[16];
+        tmem_ld16(col + j0, vr);
+        tmem_ld16(col + 64 + j0, kr);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int key = key0 + 32 * c + j;
+        for (int j = 0; j < 16; ++j) {
+          const int key = key0 + j0 + j;
           if (key < p.N) {
-            red_add(dVg + (size_t)key * D + row, v32[j]);
-            red_add(dKg + (size_t)key * D + row, k32[j] * p.scale);
+            red_add(dVg + (size_t)key * D + row, __uint_as_float(vr[j]));
+            red_add(dKg + (size_t)key * D + row, __uint_as_float(kr[j]) * p.scale);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[g]);
     }
   }
   __syncthreads();
@@ -814,6 +844,9 @@ cudaError_t launch_dkv_tc(BwdParams& p, long long max_chunks, int num_sms, uint3
   }
   cudaError_t e = cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tcb::SMEM);
   if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, bwd_dkv_tc_kernel)) != cudaSuccess) return e;
+  if (fa.maxThreadsPerBlock < tcb::THREADS) return cudaErrorLaunchOutOfResources;  // registers x threads
   const int grid = (int)std::min<long long>(max_chunks, (long long)num_sms);
   if (grid > 0) bwd_dkv_tc_kernel<<<grid, tcb::THREADS, tcb::SMEM, s>>>(mapQ, mapO, mapK, mapV, p, err);
   return cudaGetLastError();
