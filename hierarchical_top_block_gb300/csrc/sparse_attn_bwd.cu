@@ -519,9 +519,9 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
   uint8_t* sK = smem + 4 * QT_BYTES;
   uint8_t* sV = sK + KV_BYTES;
   uint8_t* sP = sV + KV_BYTES;               // stage st: P at 2 st, dS at 2 st + 1 (PS_BYTES each)
-  // q_full[st]: the stage's Q rows landed; o_full[st]: its dO rows
-  __shared__ uint64_t kv_full, kv_empty, q_full[2], o_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2],
-      p_empty[2], acc_full[2], acc_empty[2], drain;
+  // q_full / o_full[st]: the stage's Q / dO rows landed; q_empty / o_empty[st]: no longer read
+  __shared__ uint64_t kv_full, kv_empty, q_full[2], o_full[2], q_empty[2], o_empty[2], s_full[2], s_empty[2],
+      p_full[2], p_empty[2], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_base_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = *p.nchunks;
@@ -539,6 +539,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       mbar_init(&q_full[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&q_empty[i], 1);
+      mbar_init(&o_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], EPI_GROUP_WARPS);
       mbar_init(&p_full[i], EPI_GROUP_WARPS);
@@ -602,18 +603,23 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
         const int st = tt & 1;
         const int t_after = entry(k0 + 2 * QPT);  // in flight while the stage frees
+        const int nq = min(QPT, cnt - k0);
+        // the Q rows as soon as the previous tile's dK products are done (S starts on them),
+        // the dO rows once its dV products are
         if (!mbar_wait_warp(&q_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
           failed = true;
           break;
         }
-        const int nq = min(QPT, cnt - k0);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[st], (uint32_t)nq * RPQ * 256);
-          mbar_arrive_expect_tx(&o_full[st], (uint32_t)nq * RPQ * 256);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[st], (uint32_t)nq * RPQ * 256);
         __syncwarp();
-        // the Q rows first: S starts on them while the dO rows land
         if (lane < nq) tma_load_4d(sQ + (2 * st) * QT_BYTES + lane * RPQ * 256, &mapQ, &q_full[st], 0, 0, 0, q_row(t_cur));
+        if (!mbar_wait_warp(&o_empty[st], ((tt >> 1) & 1) ^ 1, err)) {
+          if (lane == 0) mbar_wait(&q_full[st], (tt >> 1) & 1, err, 100000000ull);  // this tile's Q rows
+          failed = true;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&o_full[st], (uint32_t)nq * RPQ * 256);
+        __syncwarp();
         if (lane < nq) tma_load_4d(sQ + (2 * st + 1) * QT_BYTES + lane * RPQ * 256, &mapO, &o_full[st], 0, 0, 0, q_row(t_cur));
         prefetch_rows(t_after);
         t_cur = t_next;
@@ -693,16 +699,18 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
           tc_fence_after();
           const uint32_t qb = smem_u32(sQ + (2 * st) * QT_BYTES), ob = smem_u32(sQ + (2 * st + 1) * QT_BYTES);
           const uint32_t pb = smem_u32(sP + (2 * st) * PS_BYTES), db = smem_u32(sP + (2 * st + 1) * PS_BYTES);
+          // K = rows: 16 rows = two 8-row groups per step; dK^T first, so that the Q rows free early
 #pragma unroll
-          for (int s = 0; s < ROWS / 16; ++s) {  // K = rows: 16 rows = two 8-row groups per step
-            const uint32_t acc = (k0 == 0 && s == 0) ? 0u : 1u;
-            umma_bf16(col, smem_desc_sw128(ob + s * 4096, 1024, 2048), smem_desc_sw128(pb + s * 2048, 8192, 1024), id_mn,
-                      acc);
+          for (int s = 0; s < ROWS / 16; ++s)
             umma_bf16(col + 64, smem_desc_sw128(qb + s * 4096, 1024, 2048), smem_desc_sw128(db + s * 2048, 8192, 1024),
-                      id_mn, acc);
-          }
-          umma_commit(&p_empty[st]);
+                      id_mn, (k0 == 0 && s == 0) ? 0u : 1u);
           umma_commit(&q_empty[st]);
+#pragma unroll
+          for (int s = 0; s < ROWS / 16; ++s)
+            umma_bf16(col, smem_desc_sw128(ob + s * 4096, 1024, 2048), smem_desc_sw128(pb + s * 2048, 8192, 1024), id_mn,
+                      (k0 == 0 && s == 0) ? 0u : 1u);
+          umma_commit(&o_empty[st]);
+          umma_commit(&p_empty[st]);
           if (k0 + QPT >= cnt) umma_commit(&acc_full[a]);
         }
       }
