@@ -10,10 +10,11 @@
 // Kernels: (1) D per (b, t, h) from the stored O and dO; (2) an inverse index, block ->
 // the queries that selected it, cut into chunks of at most QC queries; (3) dQ, one warp per
 // query over its selected blocks in 32-key halves (the forward's structure, with dP = dO V^T
-// and dQ += dS K in place of P V); (4) dK and dV, one 4-warp CTA per chunk, each warp owning
-// 16 keys of the block and accumulating over the chunk's queries (their Q and dO rows staged
-// three ahead in a 4-buffer ring), then adding into fp32 dK and dV (a block selected by many
-// queries spans several chunks).
+// and dQ += dS K in place of P V); (4) dK and dV per chunk, added into fp32 dK and dV (a
+// block selected by many queries spans several chunks): for d = 128 and G_Q of 8 or 16 on
+// tcgen05 with the chunk's queries in tiles of 128 query-head rows (4'), otherwise one 4-warp
+// CTA per chunk, each warp owning 16 keys of the block and accumulating over the chunk's
+// queries by mma.sync (their Q and dO rows staged three ahead in a 4-buffer ring).
 #include "kernels.cuh"
 
 namespace pisa {
