@@ -21,7 +21,7 @@ constexpr int MAX_DEVICES = 64;
 
 // Streams and events of the host-buffer prefill pipeline (created on first use).
 constexpr int PIPE_MAX_CHUNKS = 16;
-constexpr int PIPE_EVENTS = 4 + 3 * PIPE_MAX_CHUNKS;
+constexpr int PIPE_EVENTS = 4 + 4 * PIPE_MAX_CHUNKS;
 
 struct HostPipe {
   bool ready = false;
@@ -585,9 +585,13 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   const size_t sel_bytes = select_layout(p).total_bytes;
 
   // Query chunks: selection and attention of chunk j need Q rows of chunk j only (plus all
-  // of K and V), so the copy-in of chunk j+1 and the copy-out of chunk j-1 overlap the
-  // compute of chunk j; attention of chunk j (its own stream) also overlaps selection of
-  // chunk j+1, which fills the tail of each persistent kernel with the next one's CTAs.
+  // of K, and V up to the chunk's last position when causal), so the copy-in of chunk j+1
+  // and the copy-out of chunk j-1 overlap the compute of chunk j; attention of chunk j (its
+  // own stream) also overlaps selection of chunk j+1, which fills the tail of each
+  // persistent kernel with the next one's CTAs.  K goes first (the pyramid needs all of it);
+  // then each chunk's Q rows and, when causal, the V rows of the same positions (the chunk
+  // bounds are multiples of 64 but the last, so the attention of chunk j reads no V row past
+  // its last position: its blocks end there); without causality V goes whole after Q0.
   // The two share only idx, whose rows of different chunks are disjoint; selection scratch
   // is reused from chunk to chunk in the order of `stream`.  Q and O are [B][N][H_q][d]: a
   // chunk is one row band per sequence.
@@ -598,6 +602,7 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   cudaEvent_t* e_q = ev + 4;
   cudaEvent_t* e_sel = ev + 4 + PIPE_MAX_CHUNKS;
   cudaEvent_t* e_attn = ev + 4 + 2 * PIPE_MAX_CHUNKS;
+  cudaEvent_t* e_vs = ev + 4 + 3 * PIPE_MAX_CHUNKS;  // V rows of chunks 0..j in place (causal)
   const size_t q_row = (size_t)p.H_q * p.d * 2;  // bytes of one query position, all heads
   auto copy_q = [&](int j) {
     const long long lo = bounds[j], hi = bounds[j + 1];
@@ -611,20 +616,29 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   chk(cudaEventRecord(e_start, s));
   chk(cudaStreamWaitEvent(hp->in, e_start, 0));
   chk(cudaStreamWaitEvent(hp->attn, e_start, 0));
+  const size_t kv_row = (size_t)p.d * 2;  // bytes of one key position of one KV head
+  auto copy_v = [&](long long lo, long long hi) {  // positions lo .. hi - 1 of every (b, h_kv)
+    return cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(dV) + lo * kv_row, p.N * kv_row,
+                             reinterpret_cast<const uint8_t*>(V_host) + lo * kv_row, p.N * kv_row, (hi - lo) * kv_row,
+                             (size_t)p.B * p.H_kv, cudaMemcpyHostToDevice, hp->in);
+  };
   chk(cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, hp->in));
   chk(cudaEventRecord(e_k, hp->in));
-  chk(copy_q(0));
-  chk(cudaEventRecord(e_q[0], hp->in));
-  chk(cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, hp->in));
-  chk(cudaEventRecord(e_v, hp->in));
-  for (int j = 1; j < nchunks && ok; ++j) {
+  for (int j = 0; j < nchunks && ok; ++j) {
     chk(copy_q(j));
     chk(cudaEventRecord(e_q[j], hp->in));
+    if (p.causal) {
+      chk(copy_v(bounds[j], bounds[j + 1]));
+      chk(cudaEventRecord(e_vs[j], hp->in));
+    } else if (j == 0) {
+      chk(cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, hp->in));
+      chk(cudaEventRecord(e_v, hp->in));
+    }
   }
   const Geometry geo = make_geometry(p.N, p.N);
   chk(cudaStreamWaitEvent(s, e_k, 0));
   if (ok) chk(launch_pyramid(dK, dP, p, geo, s));
-  chk(cudaStreamWaitEvent(hp->attn, e_v, 0));
+  if (!p.causal) chk(cudaStreamWaitEvent(hp->attn, e_v, 0));
   for (int j = 0; j < nchunks && ok; ++j) {
     Problem pc = p;
     pc.t_lo = (int)bounds[j];
@@ -637,6 +651,7 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
     }
     chk(cudaEventRecord(e_sel[j], s));
     chk(cudaStreamWaitEvent(hp->attn, e_sel[j], 0));
+    if (p.causal) chk(cudaStreamWaitEvent(hp->attn, e_vs[j], 0));
     if (ok) chk(launch_sparse_attn(dQ, dK, dV, dIdx, dO, dL, pc, st->num_sms, st->err, hp->attn));
     chk(cudaEventRecord(e_attn[j], hp->attn));
     // copy-out of chunk j: O rows, and the LSE / selection columns of every head

@@ -307,7 +307,9 @@ def test_prefill_host_matches_the_device_path(case):
     query chunks (4096, 8192, 5184, 5240, 8192, 4096) with two sequences per batch, so the
     chunked copies of Q, O, LSE and the selection rows are all strided; the last one also
     selects without the causal mask (every block of the sequence is a candidate for every
-    chunk) and with the PISA-2 block score."""
+    chunk) and with the PISA-2 block score.  The device scratch starts as all-ones bytes (NaN
+    in bf16 and fp32): in causal mode V arrives in the same chunks as Q, and a V row read
+    before its chunk's copy would put NaN into O."""
     causal, scoring = True, 0
     if case == "4k_b2":
         w = W.WORKLOADS["prefill_4k"].with_(B=2)
@@ -328,7 +330,11 @@ def test_prefill_host_matches_the_device_path(case):
     Oh = torch.empty(Q.shape, dtype=torch.bfloat16).pin_memory()
     Lh = torch.empty(LSE.shape, dtype=torch.float32).pin_memory()
     Ih = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
-    pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, causal=causal, O_host=Oh, LSE_host=Lh, idx_host=Ih, scoring=scoring)
+    shape = pisa.make_shape(w.B, w.N, w.H_q, w.H_kv, w.d, w.N)
+    params = pisa.make_params(w.K, causal, 0.0, scoring=scoring)
+    ws = torch.full((pisa.pisa_prefill_host_workspace_bytes(shape, params),), 0xFF, dtype=torch.uint8, device="cuda")
+    pisa.pisa_prefill_host(Qh, Kh, Vh, w.K, causal=causal, dev_ws=ws, O_host=Oh, LSE_host=Lh, idx_host=Ih,
+                           scoring=scoring)
     torch.cuda.synchronize()
     assert pisa.pisa_get_last_device_error() == 0
     assert torch.equal(Ih, idx.cpu())
