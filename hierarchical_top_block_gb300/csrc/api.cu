@@ -589,9 +589,10 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   // and the copy-out of chunk j-1 overlap the compute of chunk j; attention of chunk j (its
   // own stream) also overlaps selection of chunk j+1, which fills the tail of each
   // persistent kernel with the next one's CTAs.  K goes first (the pyramid needs all of it);
-  // then each chunk's Q rows and, when causal, the V rows of the same positions (the chunk
-  // bounds are multiples of 64 but the last, so the attention of chunk j reads no V row past
-  // its last position: its blocks end there); without causality V goes whole after Q0.
+  // then each chunk's Q rows and, when causal, the V rows up to the end of the 64-key block
+  // that holds the chunk's last position (the attention of chunk j reads V rows of blocks
+  // that start at or before its positions, and no further); without causality V goes whole
+  // after Q0.
   // The two share only idx, whose rows of different chunks are disjoint; selection scratch
   // is reused from chunk to chunk in the order of `stream`.  Q and O are [B][N][H_q][d]: a
   // chunk is one row band per sequence.
@@ -628,7 +629,8 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
     chk(copy_q(j));
     chk(cudaEventRecord(e_q[j], hp->in));
     if (p.causal) {
-      chk(copy_v(bounds[j], bounds[j + 1]));
+      auto block_end = [&](long long t) { return std::min<long long>((long long)p.N, (t + 63) / 64 * 64); };
+      chk(copy_v(block_end(bounds[j]), block_end(bounds[j + 1])));
       chk(cudaEventRecord(e_vs[j], hp->in));
     } else if (j == 0) {
       chk(cudaMemcpyAsync(dV, V_host, kv, cudaMemcpyHostToDevice, hp->in));

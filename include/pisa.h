@@ -197,8 +197,9 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
  * halving again towards the end, equal chunks of at most N/4 between) so that the host -> device copy of the next
  * chunk's Q, the device -> host copy of the previous chunk's O and the attention of one chunk
  * overlap the selection of the next (K is copied first, whole; in causal mode V follows in
- * the same chunks as Q, since a chunk's attention reads no later position; otherwise V is
- * copied whole after the first chunk's Q): selection runs on `stream`, attention and the copies on
+ * the same chunks as Q, each extended to the end of the 64-key block of its last position,
+ * since a chunk's attention reads no later block; otherwise V is copied whole after the
+ * first chunk's Q): selection runs on `stream`, attention and the copies on
  * three streams of the library's own (ordered after the work queued on `stream` before the
  * call), and all of them are idle again on return.  Results equal those of pisa_build_pyramid + pisa_select_prefill +
  * pisa_sparse_attn_prefill on the same inputs.  One call at a time per device (calls from
