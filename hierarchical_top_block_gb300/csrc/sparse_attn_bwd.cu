@@ -481,20 +481,22 @@ __global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) 
 
 // (4') dK, dV on tcgen05 (d = 128, G_Q of 8 or 16).  Persistent CTAs take the chunks with a
 // stride.  Per chunk: the block's K and V by TMA; per tile of 128 query-head rows (the next
-// 128 / G_Q queries of the chunk, their Q and dO rows by one 4-D TMA box each):
+// 128 / G_Q queries of the chunk, their Q rows and their dO rows by one 4-D TMA box each, on
+// separate barriers so that S starts on the Q rows while the dO rows land):
 //   S = Q K^T, dP = dO V^T       M 128 rows x N 64 keys x K = d, fp32 in TMEM
 //   epilogue (one row a thread): P = exp2(S sl2 - LSE2), dS = P (dP - D), written as bf16 rows
 //     of 64 keys to shared memory (keys past t or N, and rows of absent queries, 0)
-//   dV^T += dO^T P, dK^T += Q^T dS   M 128 (d) x N 64 keys x K = rows: the Q / dO tile read
-//     as a d-major A operand and P / dS as a key-major B operand (both MN-major)
+//   dK^T += Q^T dS, dV^T += dO^T P   M 128 (d) x N 64 keys x K = rows: the Q / dO tile read
+//     as a d-major A operand and dS / P as a key-major B operand (both MN-major); dK^T first,
+//     so that the stage's Q rows are free for the next tile before its dO rows
 // After the chunk's last tile, TMEM lane = d, dV^T is added into dV and scale x dK^T into dK.
 // Roles: a producer warp (TMA), one thread issuing every tile's S and dP, another issuing the
-// dV and dK products, and two epilogue groups of eight warps taking alternate tiles (two warps
+// dK and dV products, and two epilogue groups of eight warps taking alternate tiles (two warps
 // a TMEM lane quarter, 32 keys each), so that one tile's S and dP run on the tensor pipe while
-// the other group turns the previous tile's into P and dS.  Stages are double-buffered (Q/dO tiles, S/dP accumulators and P/dS tiles,
-// stage = tile parity = epilogue group) and so are the dV/dK accumulators (set = chunk
-// parity; the group of that parity adds a chunk's set into dV and dK while the other chunk's
-// tiles go on).  Every wait is bounded.
+// the other group turns the previous tile's into P and dS.  Stages are double-buffered (Q/dO
+// tiles, S/dP accumulators and P/dS tiles; stage = tile parity = epilogue group) and so are
+// the dV/dK accumulators (set = chunk parity; the group of that parity adds a chunk's set into
+// dV and dK while the other chunk's tiles go on).  Every wait is bounded.
 namespace tcb {
 constexpr int THREADS = 608;                    // warp 0 producer, warps 1-2 MMA issuers, 3-18 epilogue
 constexpr int EPI_WARP0 = 3, EPI_GROUP_WARPS = 8;
