@@ -31,7 +31,8 @@ struct BwdParams {
   const int32_t* idx;
   const float* LSE;
   float *dQ, *dK, *dV, *Dsum;
-  int32_t *counts, *cursor, *offsets, *entries;
+  uint16_t* dS;  // tcgen05 path: dS of every (query, selected block), [B][H_kv][N][K][G_Q][64] bf16
+  int32_t *counts, *cursor, *offsets, *entries;  // entries: (t << 5) | selection slot
   int4* chunks;
   int32_t* nchunks;
   int B, N, N_cap, H_q, H_kv, GQ, Ksel, M1, causal;
@@ -135,7 +136,7 @@ __global__ void bwd_scatter_kernel(BwdParams p) {
     const int blk = p.idx[i];
     if (!valid_block(p, blk, t)) continue;
     const long long key = (long long)bh * p.M1 + blk;
-    p.entries[p.offsets[key] + atomicAdd(&p.cursor[key], 1)] = t;
+    p.entries[p.offsets[key] + atomicAdd(&p.cursor[key], 1)] = (t << 5) | (int)(i - item * p.Ksel);
   }
 }
 
@@ -303,6 +304,91 @@ __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
   }
 }
 
+// (3') dQ from the dS rows the tcgen05 dK/dV kernel wrote (d = 128): one warp per (b, h_kv, t)
+// over its selected blocks in 32-key halves, dQ += dS K, the K half staged by cp.async and
+// the dS fragments read straight from the rows (one query's rows are contiguous, in slot order)
+constexpr int DQS_WARPS = 16;
+
+__global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(BwdParams p) {
+  constexpr int D = 128, NDT = D / 8, CPR = D / 8;
+  constexpr int HALF = HK * 128;             // bytes of one 64-column half of a slot
+  constexpr int SLOT = HK * D * 2;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
+  uint8_t* ks = smem + (size_t)warp * SLOT;
+  const uint32_t kb = smem_u32(ks);
+  const long long total = (long long)p.B * p.H_kv * p.N;
+  for (long long item = (long long)blockIdx.x * DQS_WARPS + warp; item < total;
+       item += (long long)gridDim.x * DQS_WARPS) {
+    const int bh = (int)(item / p.N), t = (int)(item - (long long)bh * p.N);
+    const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
+    const int last = p.causal ? min(t, p.N - 1) : p.N - 1;
+    int v = lane < p.Ksel ? p.idx[item * p.Ksel + lane] : -1;
+    if (!valid_block(p, v, t)) v = -1;
+    unsigned mask = __ballot_sync(0xffffffffu, v >= 0);
+    const size_t row0 = ((size_t)b * p.N + t) * p.H_q + (size_t)hk * p.GQ;
+    float dq[NDT][4];
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
+    for (; mask; mask &= mask - 1) {
+      const int sl = __ffs(mask) - 1;
+      const int blk = __shfl_sync(0xffffffffu, v, sl);
+      const uint16_t* dsr = p.dS + ((size_t)item * p.Ksel + sl) * (size_t)(p.GQ * 64);  // [G_Q][64]
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {
+        const int kbase = blk * 64 + HK * hb;
+        if (kbase > last) break;
+        // K rows kbase .. kbase + 31 (rows past the last visible key become zero; their dS is 0)
+        const uint16_t* Kg = p.K + ((size_t)bh * p.N_cap) * D;
+        for (int i = lane; i < HK * CPR; i += 32) {
+          const int k = i / CPR, c = i - k * CPR;
+          const int key = kbase + k;
+          const bool in = key <= last;
+          cp_async16(ks + swz(HALF, k, c), Kg + (size_t)(in ? key : kbase) * D + 8 * c, in ? 16 : 0);
+        }
+        cp_async_commit();
+        // dS as bf16 A fragments: rows r, r+8 (heads; zero past G_Q), keys 32 hb + 16 kk + {2q, 2q + 8}
+        uint32_t sa[2][4];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int c0 = HK * hb + 16 * kk + 2 * q;
+          sa[kk][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + c0) : 0u;
+          sa[kk][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + c0) : 0u;
+          sa[kk][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + c0 + 8) : 0u;
+          sa[kk][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + c0 + 8) : 0u;
+        }
+        cp_async_wait_all();
+        __syncwarp();
+        // dQ += dS K (K^T fragments by ldmatrix.trans on the K slot)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
+#pragma unroll
+          for (int np = 0; np < NDT / 2; ++np) {
+            const int d0 = 8 * (2 * np + (lane >> 4));
+            const uint32_t addr = kb + (d0 >> 6) * HALF + key * 128 + ((((d0 & 63) >> 3) ^ (key & 7)) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+            mma_bf16_16816(dq[2 * np], sa[kk][0], sa[kk][1], sa[kk][2], sa[kk][3], b0, b1);
+            mma_bf16_16816(dq[2 * np + 1], sa[kk][0], sa[kk][1], sa[kk][2], sa[kk][3], b2, b3);
+          }
+        }
+        __syncwarp();  // every lane is done with the slot before the next copy
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NDT; ++i) {
+      const int col = 8 * i + 2 * q;
+      if (r < p.GQ)
+        *reinterpret_cast<float2*>(p.dQ + (row0 + r) * D + col) = make_float2(dq[i][0] * p.scale, dq[i][1] * p.scale);
+      if (r + 8 < p.GQ)
+        *reinterpret_cast<float2*>(p.dQ + (row0 + r + 8) * D + col) =
+            make_float2(dq[i][2] * p.scale, dq[i][3] * p.scale);
+    }
+  }
+}
+
 __device__ __forceinline__ void red_add(float* a, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(a), "f"(v) : "memory");
 }
@@ -343,7 +429,7 @@ __global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) 
   }
   // one query's Q and dO rows (heads past G_Q become zero), log2 LSE and D, into buffer bf
   auto stage = [&](int i, int bf) {
-    const int t = p.entries[first + i];
+    const int t = p.entries[first + i] >> 5;
     const size_t row0 = ((size_t)b * p.N + t) * p.H_q + (size_t)hk * p.GQ;
     for (int j = threadIdx.x; j < 16 * CPR; j += blockDim.x) {
       const int h = j / CPR, c = j - h * CPR;
@@ -591,7 +677,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       // lane l's query of the tile starting at entry kk (-1 past the chunk); a tile's queries
       // are read two tiles ahead, when its rows are prefetched towards L2
       auto entry = [&](int kk) -> int {
-        return (kk < cnt && lane < min(QPT, cnt - kk)) ? p.entries[first + kk + lane] : -1;
+        return (kk < cnt && lane < min(QPT, cnt - kk)) ? p.entries[first + kk + lane] >> 5 : -1;
       };
       auto q_row = [&](int t) -> int { return (int)((((long long)b * p.N + t) * p.H_q + (long long)hk * p.GQ) >> 3); };
       auto prefetch_rows = [&](int t) {
@@ -740,7 +826,10 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
         if ((int)(tt & 1) != g) continue;
         const bool vq = k0 + qi < cnt;
-        const int t = vq ? p.entries[first + k0 + qi] : 0;
+        const int ent = vq ? p.entries[first + k0 + qi] : 0;
+        const int t = ent >> 5;
+        // this row's dS (64 keys) in the dS rows the dQ kernel reads
+        uint16_t* ds_row = p.dS + (((size_t)bh * p.N + t) * p.Ksel + (ent & 31)) * (size_t)(p.GQ * 64) + (size_t)h * 64;
         float lse2 = POS_INF, dsum = 0.f;
         if (vq) {
           const size_t li = ((size_t)b * p.H_q + (size_t)hk * p.GQ + h) * p.N + t;
@@ -788,6 +877,9 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
             const uint32_t off = (uint32_t)(((j0 / 8 + c) ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+            if (vq)
+              *reinterpret_cast<uint4*>(ds_row + j0 + 8 * c) =
+                  make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
           }
         }
         fence_proxy_async();  // the MMA reads the tiles through the async proxy
@@ -877,22 +969,38 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   bwd_scatter_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
   bwd_chunks_kernel<<<(nkeys + 255) / 256, 256, 0, s>>>(p, nkeys, chunk_off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const long long items = (long long)p.B * p.H_kv * p.N;
+  if (p.dS) {  // tcgen05 dK/dV writes dS, then dQ reads it
+    if ((e = launch_dkv_tc(p, max_chunks, num_sms, err, s)) != cudaSuccess) return e;
+    const size_t smem_ds = (size_t)DQS_WARPS * HK * 128 * 2 + 1024;
+    if ((e = cudaFuncSetAttribute(bwd_dq_ds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_ds)) !=
+        cudaSuccess)
+      return e;
+    const long long gds = std::min<long long>((items + DQS_WARPS - 1) / DQS_WARPS, (long long)num_sms);
+    bwd_dq_ds_kernel<<<(int)gds, 32 * DQS_WARPS, smem_ds, s>>>(p);
+    return cudaGetLastError();
+  }
   const size_t smem_q = (size_t)DQ_WARPS * 2 * HK * D * 2 + 1024;
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q)) != cudaSuccess)
     return e;
-  const long long items = (long long)p.B * p.H_kv * p.N;
   const long long gq = std::min<long long>((items + DQ_WARPS - 1) / DQ_WARPS, (long long)num_sms);
   bwd_dq_kernel<D><<<(int)gq, 32 * DQ_WARPS, smem_q, s>>>(p);
   const size_t smem_kv = (size_t)2 * 64 * D * 2 + (size_t)2 * KV_NBUF * 16 * D * 2 + 1024;
   if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) !=
       cudaSuccess)
     return e;
-  if (D == 128 && (p.GQ == 8 || p.GQ == 16) && p.H_q % 8 == 0) return launch_dkv_tc(p, max_chunks, num_sms, err, s);
   if (max_chunks > 0) bwd_dkv_kernel<D><<<(int)max_chunks, 32 * KV_WARPS, smem_kv, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+// dK and dV on tcgen05 (and dQ from the dS rows it writes) for d = 128 and G_Q of 8 or 16
+bool bwd_tc_path(const Problem& p) { return p.d == 128 && (p.GQ == 8 || p.GQ == 16) && p.H_q % 8 == 0; }
+
+size_t bwd_ds_bytes(const Problem& p) {
+  return bwd_tc_path(p) ? (size_t)p.B * p.H_kv * p.N * p.K * p.GQ * 64 * 2 : 0;
+}
 
 size_t attn_backward_workspace_bytes(const Problem& p) {
   const long long M1 = (p.N + 63) / 64;
@@ -901,7 +1009,7 @@ size_t attn_backward_workspace_bytes(const Problem& p) {
   const long long max_chunks = nkeys + ents / QC + 1;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + up((size_t)(nkeys + 1) * 4) +
-         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4);
+         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(bwd_ds_bytes(p));
 }
 
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
@@ -949,6 +1057,8 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   p.chunks = reinterpret_cast<int4*>(w);
   w += up((size_t)max_chunks * 16);
   p.nchunks = reinterpret_cast<int32_t*>(w);
+  w += up(4);
+  p.dS = bwd_tc_path(pr) ? reinterpret_cast<uint16_t*>(w) : nullptr;
   cudaError_t e;
   if ((e = cudaMemsetAsync(p.counts, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.cursor, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
