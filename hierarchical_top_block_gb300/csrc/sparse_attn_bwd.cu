@@ -25,6 +25,8 @@ constexpr int HK = 32;      // keys per half block (dQ kernel)
 constexpr int DQ_WARPS = 8;
 constexpr int KV_WARPS = 4;
 constexpr int KV_NBUF = 4;  // staged queries per dK/dV CTA (three prefetched ahead)
+constexpr int SORT_CAP = 16384;   // block lists up to this length are sorted by query position
+constexpr int NBUCKETS = 1024;    // position buckets for the chunk order
 
 struct BwdParams {
   const uint16_t *Q, *K, *V, *O, *dO;
@@ -35,6 +37,9 @@ struct BwdParams {
   int32_t *counts, *cursor, *offsets, *entries;  // entries: (t << 5) | selection slot
   int4* chunks;
   int32_t* nchunks;
+  int4* chunks_by_t;            // the chunks reordered by their first query position
+  int32_t *bucket_count, *bucket_start, *bucket_cursor;
+  int bucket_shift;             // position bucket = t >> bucket_shift (< NBUCKETS)
   int B, N, N_cap, H_q, H_kv, GQ, Ksel, M1, causal;
   float scale, sl2;
 };
@@ -147,6 +152,73 @@ __global__ void bwd_chunks_kernel(BwdParams p, int nkeys, const int32_t* chunk_o
     const int bh = key / p.M1, blk = key - bh * p.M1;
     for (int j = 0; j * QC < c; ++j)
       p.chunks[chunk_off[key] + j] = make_int4(bh, blk, p.offsets[key] + j * QC, min(QC, c - j * QC));
+  }
+}
+
+// (2e) each block's query list in increasing position (a list longer than SORT_CAP keeps its
+// order), so that a chunk covers a narrow band of positions: one CTA per list, bitonic sort in
+// shared memory.  The entries (t << 5 | slot) are distinct, so the order is unique.
+__global__ void __launch_bounds__(512) bwd_sort_lists_kernel(BwdParams p) {
+  extern __shared__ int32_t sbuf[];
+  const int key = blockIdx.x;
+  const int lo = p.offsets[key], n = p.offsets[key + 1] - lo;
+  if (n <= 1 || n > SORT_CAP) return;
+  int np = 2;
+  while (np < n) np <<= 1;
+  for (int i = threadIdx.x; i < np; i += blockDim.x) sbuf[i] = i < n ? p.entries[lo + i] : INT_MAX;
+  __syncthreads();
+  for (int k = 2; k <= np; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < np; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const int a = sbuf[i], b = sbuf[l];
+          if ((a > b) == ((i & k) == 0)) {
+            sbuf[i] = b;
+            sbuf[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) p.entries[lo + i] = sbuf[i];
+}
+
+// (2f) the chunks in order of their first query position (counting sort by position bucket;
+// order inside a bucket arbitrary): the persistent dK/dV CTAs then work on chunks whose
+// queries lie close together, and their Q and dO rows are re-read from the L2
+__device__ __forceinline__ int chunk_bucket(const BwdParams& p, int ci) {
+  return (p.entries[p.chunks[ci].z] >> 5) >> p.bucket_shift;
+}
+
+__global__ void bwd_bucket_count_kernel(BwdParams p) {
+  const int n = *p.nchunks;
+  for (int ci = blockIdx.x * blockDim.x + threadIdx.x; ci < n; ci += gridDim.x * blockDim.x)
+    atomicAdd(&p.bucket_count[chunk_bucket(p, ci)], 1);
+}
+
+__global__ void __launch_bounds__(NBUCKETS) bwd_bucket_scan_kernel(BwdParams p) {
+  __shared__ int32_t ws[NBUCKETS / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = p.bucket_count[threadIdx.x];
+  int a = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, a, o);
+    if (lane >= o) a += y;
+  }
+  if (lane == 31) ws[warp] = a;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += ws[w];
+  p.bucket_start[threadIdx.x] = base + a - c;
+}
+
+__global__ void bwd_bucket_scatter_kernel(BwdParams p) {
+  const int n = *p.nchunks;
+  for (int ci = blockIdx.x * blockDim.x + threadIdx.x; ci < n; ci += gridDim.x * blockDim.x) {
+    const int b = chunk_bucket(p, ci);
+    p.chunks_by_t[p.bucket_start[b] + atomicAdd(&p.bucket_cursor[b], 1)] = p.chunks[ci];
   }
 }
 
@@ -969,6 +1041,17 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   bwd_scatter_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
   bwd_chunks_kernel<<<(nkeys + 255) / 256, 256, 0, s>>>(p, nkeys, chunk_off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // lists by position, chunks by their first position
+  if ((e = cudaFuncSetAttribute(bwd_sort_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(SORT_CAP * sizeof(int32_t)))) != cudaSuccess)
+    return e;
+  if (nkeys > 0) bwd_sort_lists_kernel<<<nkeys, 512, SORT_CAP * sizeof(int32_t), s>>>(p);
+  const int gc = (int)std::min<long long>((max_chunks + 255) / 256, (long long)num_sms * 8);
+  bwd_bucket_count_kernel<<<gc > 0 ? gc : 1, 256, 0, s>>>(p);
+  bwd_bucket_scan_kernel<<<1, NBUCKETS, 0, s>>>(p);
+  bwd_bucket_scatter_kernel<<<gc > 0 ? gc : 1, 256, 0, s>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  p.chunks = p.chunks_by_t;
   const long long items = (long long)p.B * p.H_kv * p.N;
   if (p.dS) {  // tcgen05 dK/dV writes dS, then dQ reads it
     if ((e = launch_dkv_tc(p, max_chunks, num_sms, err, s)) != cudaSuccess) return e;
@@ -1009,7 +1092,8 @@ size_t attn_backward_workspace_bytes(const Problem& p) {
   const long long max_chunks = nkeys + ents / QC + 1;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + up((size_t)(nkeys + 1) * 4) +
-         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(bwd_ds_bytes(p));
+         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(bwd_ds_bytes(p)) +
+         up((size_t)max_chunks * 16) + 3 * up((size_t)NBUCKETS * 4);
 }
 
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
@@ -1059,9 +1143,21 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   p.nchunks = reinterpret_cast<int32_t*>(w);
   w += up(4);
   p.dS = bwd_tc_path(pr) ? reinterpret_cast<uint16_t*>(w) : nullptr;
+  w += up(bwd_ds_bytes(pr));
+  p.chunks_by_t = reinterpret_cast<int4*>(w);
+  w += up((size_t)max_chunks * 16);
+  p.bucket_count = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)NBUCKETS * 4);
+  p.bucket_start = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)NBUCKETS * 4);
+  p.bucket_cursor = reinterpret_cast<int32_t*>(w);
+  p.bucket_shift = 0;
+  while ((((long long)pr.N - 1) >> p.bucket_shift) >= NBUCKETS) ++p.bucket_shift;
   cudaError_t e;
   if ((e = cudaMemsetAsync(p.counts, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.cursor, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.bucket_count, 0, (size_t)NBUCKETS * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.bucket_cursor, 0, (size_t)NBUCKETS * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dK, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dV, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
   if (pr.d == 128) return launch_d<128>(p, (int)nkeys, chunk_off, max_chunks, num_sms, err, s);
