@@ -949,14 +949,19 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
             const uint32_t off = (uint32_t)(((j0 / 8 + c) ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             *reinterpret_cast<uint4*>(drow + off) = make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
-            if (vq)
-              *reinterpret_cast<uint4*>(ds_row + j0 + 8 * c) =
-                  make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
           }
         }
         fence_proxy_async();  // the MMA reads the tiles through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[st]);
+        // then, off the MMA's path, this thread's 32 keys of dS from the tile to the dS rows (the
+        // tile is only read until the stage comes back to this group)
+        if (vq) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(ds_row + 32 * kh + 8 * c) =
+                *reinterpret_cast<const uint4*>(drow + (((4 * kh + c) ^ (row & 7)) << 4));
+        }
       }
       if (failed) break;
       if ((int)(cc & 1) != g) continue;
