@@ -377,22 +377,93 @@ __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
 }
 
 // (3') dQ from the dS rows the tcgen05 dK/dV kernel wrote (d = 128): one warp per (b, h_kv, t)
-// over its selected blocks in 32-key halves, dQ += dS K, the K half staged by cp.async and
-// the dS fragments read straight from the rows (one query's rows are contiguous, in slot order)
-constexpr int DQS_WARPS = 16;
+// over its selected blocks in 32-key halves, dQ += dS K, the dS fragments read straight from
+// the rows (one query's rows are contiguous, in slot order).  Each warp streams the K halves of
+// its queries' selections through a ring of shared-memory slots filled by TMA (one box per half
+// block: 32 rows x both 64-column halves of d, 128-byte swizzle, rows past N read as zero): a
+// cursor walks the same sequence of half blocks DQS_SLOTS - 1 ahead of the multiplications,
+// across query boundaries.  All waits are bounded.
+constexpr int DQS_WARPS = 12, DQS_SLOTS = 2;
 
-__global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(BwdParams p) {
-  constexpr int D = 128, NDT = D / 8, CPR = D / 8;
+struct DqCursor {
+  long long item;  // (bh, t) as bh * N + t; >= total once exhausted
+  unsigned mask;   // selection positions of the item not yet passed (the current block first)
+  int val;         // this lane's selection entry of the item (-1 if not a valid block)
+  int hb;          // half of the current block
+  int last;        // last visible key of the item's query
+};
+
+// positions the cursor on the first visible half block of item `it` or of a later item
+__device__ __forceinline__ void dq_seek(DqCursor& c, const BwdParams& p, long long it, long long total, long long stride) {
+  const int lane = threadIdx.x & 31;
+  for (; it < total; it += stride) {
+    const int t = (int)(it % p.N);
+    int v = lane < p.Ksel ? p.idx[it * p.Ksel + lane] : -1;
+    if (!valid_block(p, v, t)) v = -1;
+    const unsigned m = __ballot_sync(0xffffffffu, v >= 0);
+    if (m) {
+      c.item = it;
+      c.mask = m;
+      c.val = v;
+      c.hb = 0;
+      c.last = p.causal ? min(t, p.N - 1) : p.N - 1;
+      return;
+    }
+  }
+  c.item = total;
+}
+
+__device__ __forceinline__ int dq_block(const DqCursor& c) { return __shfl_sync(0xffffffffu, c.val, __ffs(c.mask) - 1); }
+
+__device__ __forceinline__ void dq_next(DqCursor& c, const BwdParams& p, long long total, long long stride) {
+  if (c.hb == 0 && dq_block(c) * 64 + HK <= c.last) {
+    c.hb = 1;
+    return;
+  }
+  c.hb = 0;
+  c.mask &= c.mask - 1;
+  if (!c.mask) dq_seek(c, p, c.item + stride, total, stride);
+}
+
+__global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __grid_constant__ CUtensorMap mapK, BwdParams p,
+                                                                    uint32_t* err) {
+  constexpr int D = 128, NDT = D / 8;
   constexpr int HALF = HK * 128;             // bytes of one 64-column half of a slot
   constexpr int SLOT = HK * D * 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t bar[DQS_WARPS][DQS_SLOTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
-  uint8_t* ks = smem + (size_t)warp * SLOT;
-  const uint32_t kb = smem_u32(ks);
+  uint8_t* slots = smem + (size_t)warp * DQS_SLOTS * SLOT;
+  if (lane == 0) {
+    for (int i = 0; i < DQS_SLOTS; ++i) mbar_init(&bar[warp][i], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
   const long long total = (long long)p.B * p.H_kv * p.N;
-  for (long long item = (long long)blockIdx.x * DQS_WARPS + warp; item < total;
-       item += (long long)gridDim.x * DQS_WARPS) {
+  const long long stride = (long long)gridDim.x * DQS_WARPS;
+  const long long first = (long long)blockIdx.x * DQS_WARPS + warp;
+  // the copy of one K half block into a slot (its previous contents were read by ldmatrix whose
+  // results fed MMAs issued before this point, so those reads are complete)
+  auto issue = [&](const DqCursor& c, int slot) {
+    const int bh = (int)(c.item / p.N);
+    const int row = dq_block(c) * 64 + HK * c.hb;
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar[warp][slot], SLOT);
+      tma_load_4d(slots + slot * SLOT, &mapK, &bar[warp][slot], 0, row, 0, bh);
+    }
+  };
+  DqCursor ck;  // the next K half block to load
+  dq_seek(ck, p, first, total, stride);
+  long long nk = 0, h = 0;  // half blocks issued, half blocks consumed
+  for (; nk < DQS_SLOTS - 1 && ck.item < total; ++nk) {
+    issue(ck, (int)(nk % DQS_SLOTS));
+    dq_next(ck, p, total, stride);
+  }
+
+  bool ok = true;
+  for (long long item = first; item < total && ok; item += stride) {
     const int bh = (int)(item / p.N), t = (int)(item - (long long)bh * p.N);
     const int b = bh / p.H_kv, hk = bh - b * p.H_kv;
     const int last = p.causal ? min(t, p.N - 1) : p.N - 1;
@@ -403,23 +474,19 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(BwdParams 
     float dq[NDT][4];
 #pragma unroll
     for (int i = 0; i < NDT; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
-    for (; mask; mask &= mask - 1) {
+    for (; mask && ok; mask &= mask - 1) {
       const int sl = __ffs(mask) - 1;
       const int blk = __shfl_sync(0xffffffffu, v, sl);
       const uint16_t* dsr = p.dS + ((size_t)item * p.Ksel + sl) * (size_t)(p.GQ * 64);  // [G_Q][64]
 #pragma unroll 1
       for (int hb = 0; hb < 2; ++hb) {
-        const int kbase = blk * 64 + HK * hb;
-        if (kbase > last) break;
-        // K rows kbase .. kbase + 31 (rows past the last visible key become zero; their dS is 0)
-        const uint16_t* Kg = p.K + ((size_t)bh * p.N_cap) * D;
-        for (int i = lane; i < HK * CPR; i += 32) {
-          const int k = i / CPR, c = i - k * CPR;
-          const int key = kbase + k;
-          const bool in = key <= last;
-          cp_async16(ks + swz(HALF, k, c), Kg + (size_t)(in ? key : kbase) * D + 8 * c, in ? 16 : 0);
+        if (blk * 64 + HK * hb > last) break;
+        // keep DQS_SLOTS - 1 half blocks in flight beyond this one
+        if (ck.item < total) {
+          issue(ck, (int)(nk % DQS_SLOTS));
+          dq_next(ck, p, total, stride);
+          ++nk;
         }
-        cp_async_commit();
         // dS as bf16 A fragments: rows r, r+8 (heads; zero past G_Q), keys 32 hb + 16 kk + {2q, 2q + 8}
         uint32_t sa[2][4];
 #pragma unroll
@@ -430,9 +497,13 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(BwdParams 
           sa[kk][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + c0 + 8) : 0u;
           sa[kk][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + c0 + 8) : 0u;
         }
-        cp_async_wait_all();
-        __syncwarp();
-        // dQ += dS K (K^T fragments by ldmatrix.trans on the K slot)
+        const int slot = (int)(h % DQS_SLOTS);
+        if (!mbar_wait_warp(&bar[warp][slot], (uint32_t)(h / DQS_SLOTS) & 1u, err)) {
+          ok = false;
+          break;
+        }
+        // dQ += dS K (K^T fragments by ldmatrix.trans on the slot)
+        const uint32_t kb = smem_u32(slots + slot * SLOT);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
@@ -446,9 +517,10 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(BwdParams 
             mma_bf16_16816(dq[2 * np + 1], sa[kk][0], sa[kk][1], sa[kk][2], sa[kk][3], b2, b3);
           }
         }
-        __syncwarp();  // every lane is done with the slot before the next copy
+        ++h;
       }
     }
+    if (!ok) break;
 #pragma unroll
     for (int i = 0; i < NDT; ++i) {
       const int col = 8 * i + 2 * q;
@@ -459,6 +531,10 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(BwdParams 
             make_float2(dq[i][2] * p.scale, dq[i][3] * p.scale);
     }
   }
+  // after a timeout, copies still in flight land before shared memory goes away (bounded)
+  if (!ok)
+    for (long long u = h; u < nk; ++u)
+      mbar_wait_warp(&bar[warp][u % DQS_SLOTS], (uint32_t)(u / DQS_SLOTS) & 1u, err, 100000000ull);
 }
 
 __device__ __forceinline__ void red_add(float* a, float v) {
@@ -1060,12 +1136,20 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   const long long items = (long long)p.B * p.H_kv * p.N;
   if (p.dS) {  // tcgen05 dK/dV writes dS, then dQ reads it
     if ((e = launch_dkv_tc(p, max_chunks, num_sms, err, s)) != cudaSuccess) return e;
-    const size_t smem_ds = (size_t)DQS_WARPS * HK * 128 * 2 + 1024;
+    // K half blocks by TMA: dims (64 columns, rows, d half, b*h_kv), both d halves in one box
+    CUtensorMap mapK;
+    {
+      const uint64_t dims[4] = {64, (uint64_t)p.N, 2, (uint64_t)p.B * p.H_kv};
+      const uint64_t strides[3] = {128 * 2, 128, (uint64_t)p.N_cap * 128 * 2};
+      const uint32_t box[4] = {64, (uint32_t)HK, 2, 1};
+      if (!encode_tensor_map(&mapK, p.K, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    const size_t smem_ds = (size_t)DQS_WARPS * DQS_SLOTS * HK * 128 * 2 + 1024;
     if ((e = cudaFuncSetAttribute(bwd_dq_ds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_ds)) !=
         cudaSuccess)
       return e;
     const long long gds = std::min<long long>((items + DQS_WARPS - 1) / DQS_WARPS, (long long)num_sms);
-    bwd_dq_ds_kernel<<<(int)gds, 32 * DQS_WARPS, smem_ds, s>>>(p);
+    bwd_dq_ds_kernel<<<(int)gds, 32 * DQS_WARPS, smem_ds, s>>>(mapK, p, err);
     return cudaGetLastError();
   }
   const size_t smem_q = (size_t)DQ_WARPS * 2 * HK * D * 2 + 1024;
