@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
 // block: 32 rows x both 64-column halves of d, 128-byte swizzle, rows past N read as zero): a
 // cursor walks the same sequence of half blocks DQS_SLOTS - 1 ahead of the multiplications,
 // across query boundaries.  All waits are bounded.
-constexpr int DQS_WARPS = 12, DQS_SLOTS = 2;
+constexpr int DQS_WARPS = 14, DQS_SLOTS = 2;
 
 struct DqCursor {
   long long item;  // (bh, t) as bh * N + t; >= total once exhausted
