@@ -8,13 +8,15 @@
 // (dk_c and dv_c summed over every query head of the group that selected c's block).
 //
 // Kernels: (1) D per (b, t, h) from the stored O and dO; (2) an inverse index, block ->
-// the queries that selected it, cut into chunks of at most QC queries; (3) dQ, one warp per
-// query over its selected blocks in 32-key halves (the forward's structure, with dP = dO V^T
-// and dQ += dS K in place of P V); (4) dK and dV per chunk, added into fp32 dK and dV (a
-// block selected by many queries spans several chunks): for d = 128 and G_Q of 8 or 16 on
-// tcgen05 with the chunk's queries in tiles of 128 query-head rows (4'), otherwise one 4-warp
-// CTA per chunk, each warp owning 16 keys of the block and accumulating over the chunk's
-// queries by mma.sync (their Q and dO rows staged three ahead in a 4-buffer ring).
+// the queries that selected it, each list sorted by position and cut into chunks of at most QC
+// queries, the chunks ordered by their first position; then for d = 128 and G_Q of 8 or 16:
+// (4') dK and dV on tcgen05, the chunk's queries in tiles of 128 query-head rows, which also
+// writes dS of every (query, block) pair, and (3') dQ = scale dS K, one warp per query;
+// otherwise (3) dQ, one warp per query over its selected blocks in 32-key halves (the
+// forward's structure, with dP = dO V^T and dQ += dS K in place of P V) and (4) dK and dV, one
+// 4-warp CTA per chunk, each warp owning 16 keys of the block and accumulating over the chunk's
+// queries by mma.sync (their Q and dO rows staged three ahead in a 4-buffer ring).  dK and dV
+// are added into fp32 (a block selected by many queries spans several chunks).
 #include "kernels.cuh"
 
 namespace pisa {
