@@ -35,7 +35,9 @@ struct BwdParams {
   const int32_t* idx;
   const float* LSE;
   float *dQ, *dK, *dV, *Dsum;
-  uint16_t* dS;  // tcgen05 path: dS of every (query, selected block), [B][H_kv][N][K][G_Q][64] bf16
+  uint16_t* dS;  // tcgen05 path: dS of every (query, selected block) by entry, [entries][G_Q][64] bf16,
+                 // 16-byte chunks swizzled by head (chunk c of head h at c ^ (h & 7))
+  int32_t* epos;  // tcgen05 path: entry of (b, h_kv, t, selection slot)
   int32_t *counts, *cursor, *offsets, *entries;  // entries: (t << 5) | selection slot
   int4* chunks;
   int32_t* nchunks;
@@ -164,7 +166,14 @@ __global__ void __launch_bounds__(512) bwd_sort_lists_kernel(BwdParams p) {
   extern __shared__ int32_t sbuf[];
   const int key = blockIdx.x;
   const int lo = p.offsets[key], n = p.offsets[key + 1] - lo;
-  if (n <= 1 || n > SORT_CAP) return;
+  const long long bh = key / p.M1;
+  auto place = [&](int i, int e) {  // where entry lo + i (= e) sits, for the dQ kernel
+    if (p.epos) p.epos[((long long)bh * p.N + (e >> 5)) * p.Ksel + (e & 31)] = lo + i;
+  };
+  if (n <= 1 || n > SORT_CAP) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) place(i, p.entries[lo + i]);
+    return;
+  }
   int np = 2;
   while (np < n) np <<= 1;
   for (int i = threadIdx.x; i < np; i += blockDim.x) sbuf[i] = i < n ? p.entries[lo + i] : INT_MAX;
@@ -183,7 +192,10 @@ __global__ void __launch_bounds__(512) bwd_sort_lists_kernel(BwdParams p) {
       }
       __syncthreads();
     }
-  for (int i = threadIdx.x; i < n; i += blockDim.x) p.entries[lo + i] = sbuf[i];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    p.entries[lo + i] = sbuf[i];
+    place(i, sbuf[i]);
+  }
 }
 
 // (2f) the chunks in order of their first query position (counting sort by position bucket;
@@ -479,7 +491,8 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
     for (; mask && ok; mask &= mask - 1) {
       const int sl = __ffs(mask) - 1;
       const int blk = __shfl_sync(0xffffffffu, v, sl);
-      const uint16_t* dsr = p.dS + ((size_t)item * p.Ksel + sl) * (size_t)(p.GQ * 64);  // [G_Q][64]
+      // this pair's dS rows: [G_Q][64] at its entry, 16-byte chunk c of head h at c ^ (h & 7)
+      const uint16_t* dsr = p.dS + (size_t)p.epos[item * p.Ksel + sl] * (size_t)(p.GQ * 64);
 #pragma unroll 1
       for (int hb = 0; hb < 2; ++hb) {
         if (blk * 64 + HK * hb > last) break;
@@ -489,15 +502,16 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
           dq_next(ck, p, total, stride);
           ++nk;
         }
-        // dS as bf16 A fragments: rows r, r+8 (heads; zero past G_Q), keys 32 hb + 16 kk + {2q, 2q + 8}
+        // dS as bf16 A fragments: rows r, r+8 (heads; zero past G_Q), keys 32 hb + 16 kk + {2q, 2q + 8}:
+        // chunk 4 hb + 2 kk (+1), element 2q of it; rows r and r + 8 share the chunk swizzle (h & 7 = r)
         uint32_t sa[2][4];
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-          const int c0 = HK * hb + 16 * kk + 2 * q;
-          sa[kk][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + c0) : 0u;
-          sa[kk][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + c0) : 0u;
-          sa[kk][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + c0 + 8) : 0u;
-          sa[kk][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + c0 + 8) : 0u;
+          const int o0 = (((4 * hb + 2 * kk) ^ r) << 3) + 2 * q, o1 = (((4 * hb + 2 * kk + 1) ^ r) << 3) + 2 * q;
+          sa[kk][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + o0) : 0u;
+          sa[kk][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + o0) : 0u;
+          sa[kk][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + o1) : 0u;
+          sa[kk][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + o1) : 0u;
         }
         const int slot = (int)(h % DQS_SLOTS);
         if (!mbar_wait_warp(&bar[warp][slot], (uint32_t)(h / DQS_SLOTS) & 1u, err)) {
@@ -782,7 +796,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], EPI_GROUP_WARPS);
       mbar_init(&p_full[i], EPI_GROUP_WARPS);
-      mbar_init(&p_empty[i], 1);
+      mbar_init(&p_empty[i], 2);  // the dK/dV products done, and the dS tile copied out
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], EPI_GROUP_WARPS);
     }
@@ -925,7 +939,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       uint32_t tt = 0, cc = 0;
       bool failed = false;
       for (int ci = blockIdx.x; ci < nchunks && !failed; ci += gridDim.x, ++cc) {
-        const int cnt = p.chunks[ci].w;
+        const int first = p.chunks[ci].z, cnt = p.chunks[ci].w;
         const int a = cc & 1;
         const uint32_t col = tmem_base + COL_ACC + 128 * a;
         for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
@@ -950,9 +964,17 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
                       (k0 == 0 && s == 0) ? 0u : 1u);
           umma_commit(&o_empty[st]);
           umma_commit(&p_empty[st]);
+          // the tile's dS rows (the first nq queries' rows, in the entries' order) to the workspace
+          const int nq = min(QPT, cnt - k0);
+          bulk_store(p.dS + (size_t)(first + k0) * (size_t)(RPQ * 64), sP + (2 * st + 1) * PS_BYTES,
+                     (uint32_t)(nq * RPQ * 128));
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(&p_empty[st]);
           if (k0 + QPT >= cnt) umma_commit(&acc_full[a]);
         }
       }
+      bulk_wait();  // the dS tiles are in global memory
       umma_commit(&drain);
       mbar_wait(&drain, 0, err);
     }
@@ -976,10 +998,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       for (int k0 = 0; k0 < cnt; k0 += QPT, ++tt) {
         if ((int)(tt & 1) != g) continue;
         const bool vq = k0 + qi < cnt;
-        const int ent = vq ? p.entries[first + k0 + qi] : 0;
-        const int t = ent >> 5;
-        // this row's dS (64 keys) in the dS rows the dQ kernel reads
-        uint16_t* ds_row = p.dS + (((size_t)bh * p.N + t) * p.Ksel + (ent & 31)) * (size_t)(p.GQ * 64) + (size_t)h * 64;
+        const int t = vq ? p.entries[first + k0 + qi] >> 5 : 0;
         float lse2 = POS_INF, dsum = 0.f;
         if (vq) {
           const size_t li = ((size_t)b * p.H_q + (size_t)hk * p.GQ + h) * p.N + t;
@@ -1032,14 +1051,6 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
         fence_proxy_async();  // the MMA reads the tiles through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[st]);
-        // then, off the MMA's path, this thread's 32 keys of dS from the tile to the dS rows (the
-        // tile is only read until the stage comes back to this group)
-        if (vq) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(ds_row + 32 * kh + 8 * c) =
-                *reinterpret_cast<const uint4*>(drow + (((4 * kh + c) ^ (row & 7)) << 4));
-        }
       }
       if (failed) break;
       if ((int)(cc & 1) != g) continue;
@@ -1184,7 +1195,7 @@ size_t attn_backward_workspace_bytes(const Problem& p) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + up((size_t)(nkeys + 1) * 4) +
          up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(bwd_ds_bytes(p)) +
-         up((size_t)max_chunks * 16) + 3 * up((size_t)NBUCKETS * 4);
+         up((size_t)max_chunks * 16) + 3 * up((size_t)NBUCKETS * 4) + (bwd_tc_path(p) ? up((size_t)ents * 4) : 0);
 }
 
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
@@ -1242,6 +1253,8 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   p.bucket_start = reinterpret_cast<int32_t*>(w);
   w += up((size_t)NBUCKETS * 4);
   p.bucket_cursor = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)NBUCKETS * 4);
+  p.epos = bwd_tc_path(pr) ? reinterpret_cast<int32_t*>(w) : nullptr;
   p.bucket_shift = 0;
   while ((((long long)pr.N - 1) >> p.bucket_shift) >= NBUCKETS) ++p.bucket_shift;
   cudaError_t e;
