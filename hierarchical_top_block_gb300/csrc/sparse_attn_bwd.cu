@@ -553,6 +553,18 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
       mbar_wait_warp(&bar[warp][u % DQS_SLOTS], (uint32_t)(u / DQS_SLOTS) & 1u, err, 100000000ull);
 }
 
+// Bulk copy shared -> global of `bytes` (a multiple of 16; both addresses 16-byte aligned),
+// tracked in the issuing thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the thread's committed bulk copies have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and finished writing global memory
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void red_add(float* a, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(a), "f"(v) : "memory");
 }
