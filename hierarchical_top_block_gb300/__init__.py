@@ -56,6 +56,8 @@ def lib() -> ct.CDLL:
         L.pisa_select_workspace_bytes.argtypes = [pisa_shape, pisa_params]
         L.pisa_attn_backward_workspace_bytes.restype = ct.c_size_t
         L.pisa_attn_backward_workspace_bytes.argtypes = [pisa_shape, pisa_params]
+        L.pisa_attn_backward_min_workspace_bytes.restype = ct.c_size_t
+        L.pisa_attn_backward_min_workspace_bytes.argtypes = [pisa_shape, pisa_params]
         L.pisa_sparse_attn_backward.restype = ct.c_int
         L.pisa_sparse_attn_backward.argtypes = [_P] * 10 + [_P, ct.c_size_t, pisa_shape, pisa_params, _P]
         L.pisa_prefill_host_workspace_bytes.restype = ct.c_size_t
@@ -356,9 +358,16 @@ def pisa_attn_backward_workspace_bytes(shape: pisa_shape, params: pisa_params) -
     return lib().pisa_attn_backward_workspace_bytes(shape, params)
 
 
+def pisa_attn_backward_min_workspace_bytes(shape: pisa_shape, params: pisa_params) -> int:
+    return lib().pisa_attn_backward_min_workspace_bytes(shape, params)
+
+
 def pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal: bool = True, scale: float = 0.0, ws=None,
                               dQ=None, dK=None, dV=None):
-    """Gradients of pisa_sparse_attn_prefill: returns dQ [B, N, H_q, d], dK, dV [B, H_kv, N_cap, d] (fp32)."""
+    """Gradients of pisa_sparse_attn_prefill: returns dQ [B, N, H_q, d], dK, dV [B, H_kv, N_cap, d] (fp32).
+    A caller's ws of at least pisa_attn_backward_min_workspace_bytes() is used as it is (below
+    pisa_attn_backward_workspace_bytes() the dQ kernel forms S and dP again instead of reading dS);
+    without one, the full size is allocated."""
     B, N, H_q, d, H_kv, N_cap = _attn_inputs(Q, K, V, idx)
     for t, n in ((O, "O"), (dO, "dO")):
         _expect(t, n, (B, N, H_q, d), torch.bfloat16, Q.device)
@@ -370,7 +379,8 @@ def pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal: bool = True, sca
     need = pisa_attn_backward_workspace_bytes(shape, params)
     if need == 0 and B * N > 0:
         raise PisaError(2, "pisa_sparse_attn_backward: unsupported shape or parameters")
-    ws = _workspace(ws, need, Q.device)
+    least = pisa_attn_backward_min_workspace_bytes(shape, params)
+    ws = _workspace(ws, need if ws is None else least, Q.device)
     dQ = torch.empty(B, N, H_q, d, dtype=torch.float32, device=Q.device) if dQ is None else dQ
     dK = torch.empty(B, H_kv, N_cap, d, dtype=torch.float32, device=Q.device) if dK is None else dK
     dV = torch.empty(B, H_kv, N_cap, d, dtype=torch.float32, device=Q.device) if dV is None else dV

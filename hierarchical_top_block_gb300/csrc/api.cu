@@ -497,7 +497,13 @@ pisa_status pisa_select_bsa(const uint16_t* Q, const uint16_t* P, int32_t* idx, 
 size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params) {
   Problem p;
   if (check_params(shape, params, &p) != PISA_OK || !entry_lists_fit(p)) return 0;
-  return attn_backward_workspace_bytes(p);
+  return attn_backward_workspace_bytes(p, true);
+}
+
+size_t pisa_attn_backward_min_workspace_bytes(pisa_shape shape, pisa_params params) {
+  Problem p;
+  if (check_params(shape, params, &p) != PISA_OK || !entry_lists_fit(p)) return 0;
+  return attn_backward_workspace_bytes(p, false);
 }
 
 pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
@@ -513,12 +519,13 @@ pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, cons
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
       !aligned16(dK) || !aligned16(dV) || ((uintptr_t)ws & 255))
     return PISA_ERR_INVALID_ARG;
-  if (ws_bytes < attn_backward_workspace_bytes(p)) return PISA_ERR_WORKSPACE;
+  if (ws_bytes < attn_backward_workspace_bytes(p, false)) return PISA_ERR_WORKSPACE;
+  const bool with_ds = ws_bytes >= attn_backward_workspace_bytes(p, true);
   DeviceState* st;
   if ((rc = device_state(&st)) != PISA_OK) return rc;
   PhaseTimer tm(static_cast<cudaStream_t>(stream));
-  const cudaError_t e = launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, p, st->num_sms, st->err,
-                                             static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_attn_backward(Q, K, V, idx, O, LSE, dO, dQ, dK, dV, ws, with_ds, p, st->num_sms,
+                                             st->err, static_cast<cudaStream_t>(stream));
   tm.mark(PH_BACKWARD);
   return cuda_status(e);
 }

@@ -63,10 +63,13 @@ cudaError_t launch_sparse_attn(const uint16_t* Q, const uint16_t* K, const uint1
                                uint16_t* O, float* LSE, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s);
 
 // Backward of the attention over the selected blocks (dQ, dK, dV).
-size_t attn_backward_workspace_bytes(const Problem& p);
+// with_ds: room for dS of every (query, block) pair (where the tcgen05 path writes it), which
+// spares the dQ kernel forming S and dP again
+size_t attn_backward_workspace_bytes(const Problem& p, bool with_ds);
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
                                  const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
-                                 float* dV, void* ws, const Problem& p, int num_sms, uint32_t* err, cudaStream_t s);
+                                 float* dV, void* ws, bool with_ds, const Problem& p, int num_sms, uint32_t* err,
+                                 cudaStream_t s);
 
 // Fused decode step.  logits (nullable, decode_logits_bytes(p) bytes) keeps the leaf
 // candidates' logits for the attention, which then reads no K rows of the selected blocks.

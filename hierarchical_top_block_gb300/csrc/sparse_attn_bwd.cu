@@ -45,6 +45,7 @@ struct BwdParams {
   int32_t *bucket_count, *bucket_start, *bucket_cursor;
   int bucket_shift;             // position bucket = t >> bucket_shift (< NBUCKETS)
   int B, N, N_cap, H_q, H_kv, GQ, Ksel, M1, causal;
+  int tc;  // dK and dV on tcgen05 (with dS written out when dS is not null)
   float scale, sl2;
 };
 
@@ -808,7 +809,7 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], EPI_GROUP_WARPS);
       mbar_init(&p_full[i], EPI_GROUP_WARPS);
-      mbar_init(&p_empty[i], 2);  // the dK/dV products done, and the dS tile copied out
+      mbar_init(&p_empty[i], p.dS ? 2 : 1);  // the dK/dV products done (and the dS tile copied out)
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], EPI_GROUP_WARPS);
     }
@@ -976,13 +977,14 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
                       (k0 == 0 && s == 0) ? 0u : 1u);
           umma_commit(&o_empty[st]);
           umma_commit(&p_empty[st]);
-          // the tile's dS rows (the first nq queries' rows, in the entries' order) to the workspace
-          const int nq = min(QPT, cnt - k0);
-          bulk_store(p.dS + (size_t)(first + k0) * (size_t)(RPQ * 64), sP + (2 * st + 1) * PS_BYTES,
-                     (uint32_t)(nq * RPQ * 128));
-          bulk_commit();
-          bulk_wait_read();
-          mbar_arrive(&p_empty[st]);
+          if (p.dS) {  // the tile's dS rows (the first nq queries' rows, in the entries' order) out
+            const int nq = min(QPT, cnt - k0);
+            bulk_store(p.dS + (size_t)(first + k0) * (size_t)(RPQ * 64), sP + (2 * st + 1) * PS_BYTES,
+                       (uint32_t)(nq * RPQ * 128));
+            bulk_commit();
+            bulk_wait_read();
+            mbar_arrive(&p_empty[st]);
+          }
           if (k0 + QPT >= cnt) umma_commit(&acc_full[a]);
         }
       }
@@ -1159,8 +1161,8 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.chunks = p.chunks_by_t;
   const long long items = (long long)p.B * p.H_kv * p.N;
-  if (p.dS) {  // tcgen05 dK/dV writes dS, then dQ reads it
-    if ((e = launch_dkv_tc(p, max_chunks, num_sms, err, s)) != cudaSuccess) return e;
+  if (p.tc && (e = launch_dkv_tc(p, max_chunks, num_sms, err, s)) != cudaSuccess) return e;
+  if (p.dS) {  // the tcgen05 dK/dV kernel wrote dS: dQ = scale dS K
     // K half blocks by TMA: dims (64 columns, rows, d half, b*h_kv), both d halves in one box
     CUtensorMap mapK;
     {
@@ -1182,6 +1184,7 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
     return e;
   const long long gq = std::min<long long>((items + DQ_WARPS - 1) / DQ_WARPS, (long long)num_sms);
   bwd_dq_kernel<D><<<(int)gq, 32 * DQ_WARPS, smem_q, s>>>(p);
+  if (p.tc) return cudaGetLastError();
   const size_t smem_kv = (size_t)2 * 64 * D * 2 + (size_t)2 * KV_NBUF * 16 * D * 2 + 1024;
   if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) !=
       cudaSuccess)
@@ -1195,24 +1198,30 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
 // dK and dV on tcgen05 (and dQ from the dS rows it writes) for d = 128 and G_Q of 8 or 16
 bool bwd_tc_path(const Problem& p) { return p.d == 128 && (p.GQ == 8 || p.GQ == 16) && p.H_q % 8 == 0; }
 
+// dS of every (query, block) pair, written by the tcgen05 dK/dV kernel for the dQ kernel, up to
+// 64 GB of scratch; above that the dQ kernel forms S and dP again instead
+constexpr size_t DS_MAX_BYTES = (size_t)1 << 36;
 size_t bwd_ds_bytes(const Problem& p) {
-  return bwd_tc_path(p) ? (size_t)p.B * p.H_kv * p.N * p.K * p.GQ * 64 * 2 : 0;
+  const size_t b = (size_t)p.B * p.H_kv * p.N * p.K * p.GQ * 64 * 2;
+  return bwd_tc_path(p) && b <= DS_MAX_BYTES ? b : 0;
 }
 
-size_t attn_backward_workspace_bytes(const Problem& p) {
+size_t attn_backward_workspace_bytes(const Problem& p, bool with_ds) {
+  const size_t ds = with_ds ? bwd_ds_bytes(p) : 0;
   const long long M1 = (p.N + 63) / 64;
   const long long nkeys = (long long)p.B * p.H_kv * M1;
   const long long ents = (long long)p.B * p.H_kv * p.N * p.K;
   const long long max_chunks = nkeys + ents / QC + 1;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + up((size_t)(nkeys + 1) * 4) +
-         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(bwd_ds_bytes(p)) +
-         up((size_t)max_chunks * 16) + 3 * up((size_t)NBUCKETS * 4) + (bwd_tc_path(p) ? up((size_t)ents * 4) : 0);
+         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(ds) + up((size_t)max_chunks * 16) +
+         3 * up((size_t)NBUCKETS * 4) + (ds ? up((size_t)ents * 4) : 0);
 }
 
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
                                  const uint16_t* O, const float* LSE, const uint16_t* dO, float* dQ, float* dK,
-                                 float* dV, void* ws, const Problem& pr, int num_sms, uint32_t* err, cudaStream_t s) {
+                                 float* dV, void* ws, bool with_ds, const Problem& pr, int num_sms, uint32_t* err,
+                                 cudaStream_t s) {
   BwdParams p;
   p.Q = Q;
   p.K = K;
@@ -1256,8 +1265,10 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   w += up((size_t)max_chunks * 16);
   p.nchunks = reinterpret_cast<int32_t*>(w);
   w += up(4);
-  p.dS = bwd_tc_path(pr) ? reinterpret_cast<uint16_t*>(w) : nullptr;
-  w += up(bwd_ds_bytes(pr));
+  p.tc = bwd_tc_path(pr) ? 1 : 0;
+  const size_t ds = with_ds ? bwd_ds_bytes(pr) : 0;
+  p.dS = ds ? reinterpret_cast<uint16_t*>(w) : nullptr;
+  w += up(ds);
   p.chunks_by_t = reinterpret_cast<int4*>(w);
   w += up((size_t)max_chunks * 16);
   p.bucket_count = reinterpret_cast<int32_t*>(w);
@@ -1266,7 +1277,7 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   w += up((size_t)NBUCKETS * 4);
   p.bucket_cursor = reinterpret_cast<int32_t*>(w);
   w += up((size_t)NBUCKETS * 4);
-  p.epos = bwd_tc_path(pr) ? reinterpret_cast<int32_t*>(w) : nullptr;
+  p.epos = p.dS ? reinterpret_cast<int32_t*>(w) : nullptr;
   p.bucket_shift = 0;
   while ((((long long)pr.N - 1) >> p.bucket_shift) >= NBUCKETS) ++p.bucket_shift;
   cudaError_t e;

@@ -180,12 +180,17 @@ PISA_API pisa_status pisa_sparse_attn_prefill(const uint16_t* Q, const uint16_t*
  * forward; only params.K, causal and scale are used.
  *   O, dO [B][N][H_q][d] bf16 (O and LSE from the forward);  LSE [B][H_q][N] fp32.
  *   dQ [B][N][H_q][d] fp32 out;  dK, dV [B][H_kv][N_cap][d] fp32 out (rows >= N are zero).
- *   ws  device scratch of at least pisa_attn_backward_workspace_bytes(); 256-B aligned.  For
- *       d = 128 and G_Q of 8 or 16 it also holds dS of every (query, selected block) in bf16
- *       (B * H_kv * N * K * G_Q * 64 * 2 bytes, 8.6 GB at N = 262144, H_kv = 1, G_Q = K = 16):
- *       the dK/dV kernel writes it and the dQ kernel reads it instead of forming S and dP again.
+ *   ws  device scratch, 256-B aligned, of ws_bytes >= pisa_attn_backward_min_workspace_bytes()
+ *       (else PISA_ERR_WORKSPACE).  With ws_bytes >= pisa_attn_backward_workspace_bytes(), and
+ *       for d = 128 and G_Q of 8 or 16, it also holds dS of every (query, selected block) in
+ *       bf16 (B * H_kv * N * K * G_Q * 64 * 2 bytes, 8.6 GB at N = 262144, H_kv = 1,
+ *       G_Q = K = 16; up to 64 GB): the dK/dV kernel writes it and the dQ kernel reads it
+ *       instead of forming S and dP again.  The results are the same either way up to the
+ *       rounding order of the fp32 sums.
  * dK and dV accumulate with fp32 atomic adds, so their last bits may vary between runs. */
 PISA_API size_t pisa_attn_backward_workspace_bytes(pisa_shape shape, pisa_params params);
+/* The least scratch pisa_sparse_attn_backward runs with (no dS scratch); 0 where it refuses. */
+PISA_API size_t pisa_attn_backward_min_workspace_bytes(pisa_shape shape, pisa_params params);
 PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V,
                                                const int32_t* idx, const uint16_t* O, const float* LSE,
                                                const uint16_t* dO, float* dQ, float* dK, float* dV, void* ws,

@@ -115,6 +115,8 @@ def test_entry_list_limit(lib):
     assert pisa.pisa_prefill_host_workspace_bytes(big, at) == 0
     assert pisa.pisa_select_workspace_bytes(big, below) > 0
     assert pisa.pisa_attn_backward_workspace_bytes(big, below) > 0
+    assert pisa.pisa_attn_backward_min_workspace_bytes(big, at) == 0
+    assert pisa.pisa_attn_backward_min_workspace_bytes(big, below) > 0
     fake = ct.c_void_p(1 << 20)  # aligned, never dereferenced: the call returns before using it
     assert lib.pisa_select_prefill(fake, fake, fake, fake, None, None, fake, 1 << 40, big, at, None) == 2
     assert lib.pisa_select_prefill_noalloc(fake, fake, fake, fake, None, None, big, at, None) == 2
@@ -196,3 +198,20 @@ def test_decode_workspace_bytes(lib):
     assert need(3, 24, 3, 5) == 3 * 3 * 10 * 8 * 32 * 8
     assert need(2, 4, 4, 16) == 2 * 4 * 32 * 8 * 4 * 8
     assert need(2, 16, 2, 33) == 0 and need(2, 16, 2, 16, N_cap=0) == 0 and need(2, 16, 2, 16, causal=False) == 0
+
+
+def test_backward_workspace_with_and_without_ds():
+    """With d = 128 and G_Q of 8 or 16 the full backward scratch adds dS of every (query,
+    selected block) pair (bf16, G_Q x 64 per pair) and a 4-byte entry per pair to the least
+    scratch; elsewhere the two sizes are equal."""
+    B, N, K = 1, 4096, 16
+    for H_q, H_kv, d, extra in ((16, 1, 128, True), (32, 4, 128, True), (16, 4, 128, False), (16, 1, 64, False)):
+        shape, params = pisa.make_shape(B, N, H_q, H_kv, d, N), pisa.make_params(K)
+        full = pisa.pisa_attn_backward_workspace_bytes(shape, params)
+        least = pisa.pisa_attn_backward_min_workspace_bytes(shape, params)
+        if extra:
+            pairs = B * H_kv * N * K
+            assert full - least >= pairs * (H_q // H_kv) * 64 * 2 + pairs * 4
+            assert full - least <= pairs * (H_q // H_kv) * 64 * 2 + pairs * 4 + 512
+        else:
+            assert full == least > 0

@@ -29,14 +29,21 @@ def _close(name, got, ref):
     assert H.rel_l2(got, ref) <= 1e-2, f"{name}: relative L2 {H.rel_l2(got, ref)}"
 
 
-def _check(oracle_impl, w, K_sel, causal=True, seed=0):
+def _check(oracle_impl, w, K_sel, causal=True, seed=0, least_ws=False):
     Q, K, V = W.prefill_inputs(w, "cuda")
     gen = torch.Generator(device="cpu").manual_seed(1234 + seed)
     dO = (torch.randn(Q.shape, generator=gen) * 0.5).to(torch.bfloat16).to("cuda")
     P = pisa.pisa_build_pyramid(K)
     idx = pisa.pisa_select_prefill(Q, K, P, K_sel, causal=causal)
     O, LSE = pisa.pisa_sparse_attn_prefill(Q, K, V, idx, causal=causal)
-    dQ, dK, dV = pisa.pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal=causal)
+    ws = None
+    if least_ws:  # the least scratch: no dS rows, the dQ kernel forms S and dP again
+        shape = pisa.make_shape(w.B, w.N, w.H_q, w.H_kv, w.d, w.N)
+        params = pisa.make_params(K_sel, causal)
+        least = pisa.pisa_attn_backward_min_workspace_bytes(shape, params)
+        assert 0 < least < pisa.pisa_attn_backward_workspace_bytes(shape, params)
+        ws = torch.empty(least, dtype=torch.uint8, device="cuda")
+    dQ, dK, dV = pisa.pisa_sparse_attn_backward(Q, K, V, idx, O, LSE, dO, causal=causal, ws=ws)
     torch.cuda.synchronize()
     assert pisa.pisa_get_last_device_error() == 0
     rQ, rK, rV = oracle_impl.sparse_attention_backward(H.to_np_bits(Q), H.to_np_bits(K), H.to_np_bits(V),
@@ -53,6 +60,13 @@ def test_backward_tiny(oracle_impl):
 def test_backward_ragged_gq16_d128(oracle_impl):
     w = W.WORKLOADS["prefill_4k"].with_(B=1, N=2048 + 33, H_q=32, H_kv=2, K=8)
     _check(oracle_impl, w, 8, seed=1)
+
+
+def test_backward_ragged_gq16_d128_least_workspace(oracle_impl):
+    """The same shape with only the least scratch: dK/dV on tcgen05 without writing dS, and dQ
+    forming S and dP itself."""
+    w = W.WORKLOADS["prefill_4k"].with_(B=1, N=2048 + 33, H_q=32, H_kv=2, K=8)
+    _check(oracle_impl, w, 8, seed=1, least_ws=True)
 
 
 def test_backward_non_causal(oracle_impl):
