@@ -49,8 +49,8 @@ PAGES_REFERENCE = {
 # dram__bytes_write.sum from one ncu capture; the committed DRAM-traffic profile of that
 # workload), keyed by a hash of the kernel's sources: when the sources change the figure is
 # stale and is reported as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "007a9b7683a8c5aa095a4aa40fe8fea5eaa8c6f685d3f8ee165b25f35b12fc7f",
-                "workload": "prefill_256k", "bytes": 14263950080 + 1091918592}
+ATTN_TRAFFIC = {"sources_sha256": "fadf057976a670244f117a313678167481639d2c2f94de60b8df70bfb9d2be0d",
+                "workload": "prefill_256k", "bytes": 14240070912 + 1092140800}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 
