@@ -398,12 +398,13 @@ __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
 // block: 32 rows x both 64-column halves of d, 128-byte swizzle, rows past N read as zero): a
 // cursor walks the same sequence of half blocks DQS_SLOTS - 1 ahead of the multiplications,
 // across query boundaries.  All waits are bounded.
-constexpr int DQS_WARPS = 14, DQS_SLOTS = 2;
+constexpr int DQS_WARPS = 11, DQS_SLOTS = 2;
 
 struct DqCursor {
   long long item;  // (bh, t) as bh * N + t; >= total once exhausted
   unsigned mask;   // selection positions of the item not yet passed (the current block first)
   int val;         // this lane's selection entry of the item (-1 if not a valid block)
+  int ent;         // the dS entry of this lane's selection slot
   int hb;          // half of the current block
   int last;        // last visible key of the item's query
 };
@@ -420,6 +421,7 @@ __device__ __forceinline__ void dq_seek(DqCursor& c, const BwdParams& p, long lo
       c.item = it;
       c.mask = m;
       c.val = v;
+      c.ent = v >= 0 ? p.epos[it * p.Ksel + lane] : 0;
       c.hb = 0;
       c.last = p.causal ? min(t, p.N - 1) : p.N - 1;
       return;
@@ -445,11 +447,12 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
   constexpr int D = 128, NDT = D / 8;
   constexpr int HALF = HK * 128;             // bytes of one 64-column half of a slot
   constexpr int SLOT = HK * D * 2;
+  constexpr int SLOT_ALL = SLOT + 16 * 128;  // the K half block, then the pair's dS rows (up to 16 x 64)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t bar[DQS_WARPS][DQS_SLOTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
-  uint8_t* slots = smem + (size_t)warp * DQS_SLOTS * SLOT;
+  uint8_t* slots = smem + (size_t)warp * DQS_SLOTS * SLOT_ALL;
   if (lane == 0) {
     for (int i = 0; i < DQS_SLOTS; ++i) mbar_init(&bar[warp][i], 1);
     mbar_fence_init();
@@ -463,10 +466,17 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
   auto issue = [&](const DqCursor& c, int slot) {
     const int bh = (int)(c.item / p.N);
     const int row = dq_block(c) * 64 + HK * c.hb;
+    const int ent = __shfl_sync(0xffffffffu, c.ent, __ffs(c.mask) - 1);
+    const uint32_t ds_bytes = (uint32_t)(p.GQ * 128);
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bar[warp][slot], SLOT);
-      tma_load_4d(slots + slot * SLOT, &mapK, &bar[warp][slot], 0, row, 0, bh);
+      mbar_arrive_expect_tx(&bar[warp][slot], SLOT + ds_bytes);
+      tma_load_4d(slots + slot * SLOT_ALL, &mapK, &bar[warp][slot], 0, row, 0, bh);
+      asm volatile(  // the pair's dS rows (swizzled as stored)
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_u32(slots + slot * SLOT_ALL + SLOT)),
+          "l"(p.dS + (size_t)ent * (size_t)(p.GQ * 64)), "r"(ds_bytes), "r"(smem_u32(&bar[warp][slot]))
+          : "memory");
     }
   };
   DqCursor ck;  // the next K half block to load
@@ -492,8 +502,6 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
     for (; mask && ok; mask &= mask - 1) {
       const int sl = __ffs(mask) - 1;
       const int blk = __shfl_sync(0xffffffffu, v, sl);
-      // this pair's dS rows: [G_Q][64] at its entry, 16-byte chunk c of head h at c ^ (h & 7)
-      const uint16_t* dsr = p.dS + (size_t)p.epos[item * p.Ksel + sl] * (size_t)(p.GQ * 64);
 #pragma unroll 1
       for (int hb = 0; hb < 2; ++hb) {
         if (blk * 64 + HK * hb > last) break;
@@ -503,24 +511,25 @@ __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __gr
           dq_next(ck, p, total, stride);
           ++nk;
         }
-        // dS as bf16 A fragments: rows r, r+8 (heads; zero past G_Q), keys 32 hb + 16 kk + {2q, 2q + 8}:
-        // chunk 4 hb + 2 kk (+1), element 2q of it; rows r and r + 8 share the chunk swizzle (h & 7 = r)
-        uint32_t sa[2][4];
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const int o0 = (((4 * hb + 2 * kk) ^ r) << 3) + 2 * q, o1 = (((4 * hb + 2 * kk + 1) ^ r) << 3) + 2 * q;
-          sa[kk][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + o0) : 0u;
-          sa[kk][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + o0) : 0u;
-          sa[kk][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + r * 64 + o1) : 0u;
-          sa[kk][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsr + (r + 8) * 64 + o1) : 0u;
-        }
         const int slot = (int)(h % DQS_SLOTS);
         if (!mbar_wait_warp(&bar[warp][slot], (uint32_t)(h / DQS_SLOTS) & 1u, err)) {
           ok = false;
           break;
         }
+        // dS as bf16 A fragments from the slot's dS rows: rows r, r+8 (heads; zero past G_Q), keys
+        // 32 hb + 16 kk + {2q, 2q + 8}: chunk 4 hb + 2 kk (+1) at its swizzled place (h & 7 = r)
+        const uint8_t* dsm = slots + slot * SLOT_ALL + SLOT;
+        uint32_t sa[2][4];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int o0 = (((4 * hb + 2 * kk) ^ r) << 4) + 4 * q, o1 = (((4 * hb + 2 * kk + 1) ^ r) << 4) + 4 * q;
+          sa[kk][0] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsm + r * 128 + o0) : 0u;
+          sa[kk][1] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsm + (r + 8) * 128 + o0) : 0u;
+          sa[kk][2] = r < p.GQ ? *reinterpret_cast<const uint32_t*>(dsm + r * 128 + o1) : 0u;
+          sa[kk][3] = r + 8 < p.GQ ? *reinterpret_cast<const uint32_t*>(dsm + (r + 8) * 128 + o1) : 0u;
+        }
         // dQ += dS K (K^T fragments by ldmatrix.trans on the slot)
-        const uint32_t kb = smem_u32(slots + slot * SLOT);
+        const uint32_t kb = smem_u32(slots + slot * SLOT_ALL);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int key = 16 * kk + 8 * ((lane >> 3) & 1) + (lane & 7);
@@ -1171,7 +1180,7 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
       const uint32_t box[4] = {64, (uint32_t)HK, 2, 1};
       if (!encode_tensor_map(&mapK, p.K, 4, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    const size_t smem_ds = (size_t)DQS_WARPS * DQS_SLOTS * HK * 128 * 2 + 1024;
+    const size_t smem_ds = (size_t)DQS_WARPS * DQS_SLOTS * (HK * 128 * 2 + 16 * 128) + 1024;
     if ((e = cudaFuncSetAttribute(bwd_dq_ds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_ds)) !=
         cudaSuccess)
       return e;
