@@ -392,12 +392,13 @@ __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
 }
 
 // (3') dQ from the dS rows the tcgen05 dK/dV kernel wrote (d = 128): one warp per (b, h_kv, t)
-// over its selected blocks in 32-key halves, dQ += dS K, the dS fragments read straight from
-// the rows (one query's rows are contiguous, in slot order).  Each warp streams the K halves of
-// its queries' selections through a ring of shared-memory slots filled by TMA (one box per half
-// block: 32 rows x both 64-column halves of d, 128-byte swizzle, rows past N read as zero): a
-// cursor walks the same sequence of half blocks DQS_SLOTS - 1 ahead of the multiplications,
-// across query boundaries.  All waits are bounded.
+// over its selected blocks in 32-key halves, dQ += dS K.  Each warp streams its queries'
+// selections through a ring of shared-memory slots: per half block, the K rows by TMA (one box:
+// 32 rows x both 64-column halves of d, 128-byte swizzle, rows past N read as zero) and the
+// (query, block) pair's dS rows by a bulk copy (stored by entry, swizzled as the dK/dV kernel's
+// tile was; found through the (query, slot) -> entry map), on one barrier.  A cursor walks the
+// same sequence of half blocks DQS_SLOTS - 1 ahead of the multiplications, across query
+// boundaries, so the dS reads from DRAM are off the path.  All waits are bounded.
 constexpr int DQS_WARPS = 11, DQS_SLOTS = 2;
 
 struct DqCursor {
