@@ -69,6 +69,14 @@ def test_backward_ragged_gq16_d128_least_workspace(oracle_impl):
     _check(oracle_impl, w, 8, seed=1, least_ws=True)
 
 
+@pytest.mark.parametrize("N,K_sel", [(37, 1), (64 * 3 + 1, 2)])
+def test_backward_short_sequences_gq16_d128(oracle_impl, N, K_sel):
+    """The tcgen05 path on sequences of one partial block and of a single key past three full
+    blocks: K and V rows past N read as zero, partial tiles of a chunk."""
+    w = W.WORKLOADS["prefill_4k"].with_(B=1, N=N, H_q=16, H_kv=1, K=K_sel)
+    _check(oracle_impl, w, K_sel, seed=N)
+
+
 def test_backward_non_causal(oracle_impl):
     w = W.WORKLOADS["tiny"].with_(N=64 * 9 + 5, H_q=8, H_kv=2, d=128)
     _check(oracle_impl, w, 3, causal=False, seed=2)
