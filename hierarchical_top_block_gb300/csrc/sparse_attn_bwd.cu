@@ -54,23 +54,32 @@ __device__ __forceinline__ uint32_t swz(int half_bytes, int k, int c) {
   return (c >> 3) * half_bytes + k * 128 + ((((c & 7) ^ (k & 7))) << 4);
 }
 
-// (1) D[b][h][t] = sum_e dO[b,t,h,e] O[b,t,h,e]
+// (1) D[b][h][t] = sum_e dO[b,t,h,e] O[b,t,h,e]: D / 8 lanes per row, 16 bytes of dO and of O
+// each (coalesced: a warp reads 32 x 16 contiguous bytes of each), a shuffle tree per row
 template <int D>
 __global__ void bwd_dsum_kernel(BwdParams p) {
+  constexpr int LPR = D / 8, RPW = 32 / LPR;  // lanes per row (16 at d = 128), rows per warp
   const long long rows = (long long)p.B * p.N * p.H_q;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += (long long)gridDim.x * blockDim.x) {
-    const uint4* a = reinterpret_cast<const uint4*>(p.dO + i * D);
-    const uint4* o = reinterpret_cast<const uint4*>(p.O + i * D);
+  const int lane = threadIdx.x & 31, sub = lane % LPR;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+  // warp-uniform loop (the shuffles need every lane): rows RPW w .. RPW w + RPW - 1
+  for (long long w = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w * RPW < rows; w += nwarps) {
+    const long long i = w * RPW + lane / LPR;
+    const bool ok = i < rows;
     float s = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < D / 8; ++j) {
-      const uint4 x = __ldg(a + j), y = __ldg(o + j);
+    if (ok) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(p.dO + i * D) + sub);
+      const uint4 y = __ldg(reinterpret_cast<const uint4*>(p.O + i * D) + sub);
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u) s += bf16_lo(xs[u]) * bf16_lo(ys[u]) + bf16_hi(xs[u]) * bf16_hi(ys[u]);
     }
-    const long long h = i % p.H_q, bt = i / p.H_q, t = bt % p.N, b = bt / p.N;
-    p.Dsum[(b * p.H_q + h) * p.N + t] = s;
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (ok && sub == 0) {
+      const long long h = i % p.H_q, bt = i / p.H_q, t = bt % p.N, b = bt / p.N;
+      p.Dsum[(b * p.H_q + h) * p.N + t] = s;
+    }
   }
 }
 
@@ -1151,7 +1160,7 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   cudaError_t e;
   const long long rows = (long long)p.B * p.N * p.H_q;
   const long long ents = (long long)p.B * p.H_kv * p.N * p.Ksel;
-  const int g1 = (int)std::min<long long>((rows + 255) / 256, (long long)num_sms * 16);
+  const int g1 = (int)std::min<long long>((rows * (D / 8) + 255) / 256, (long long)num_sms * 32);
   const int g2 = (int)std::min<long long>((ents + 255) / 256, (long long)num_sms * 16);
   bwd_dsum_kernel<D><<<g1 > 0 ? g1 : 1, 256, 0, s>>>(p);
   bwd_count_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
