@@ -38,7 +38,8 @@ struct BwdParams {
   uint16_t* dS;  // tcgen05 path: dS of every (query, selected block) by entry, [entries][G_Q][64] bf16,
                  // 16-byte chunks swizzled by head (chunk c of head h at c ^ (h & 7))
   int32_t* epos;  // tcgen05 path: entry of (b, h_kv, t, selection slot)
-  int32_t *counts, *cursor, *offsets, *entries;  // entries: (t << 5) | selection slot
+  int32_t *counts, *offsets, *entries;  // entries: (t << 5) | selection slot
+  int32_t* rank;  // each selection entry's place in its block's list (from the counting atomics)
   int4* chunks;
   int32_t* nchunks;
   int4* chunks_by_t;            // the chunks reordered by their first query position
@@ -87,14 +88,15 @@ __device__ __forceinline__ bool valid_block(const BwdParams& p, int blk, int t) 
   return blk >= 0 && blk < p.M1 && (!p.causal || blk * 64 <= t);
 }
 
-// (2a) per (bh, block): how many queries selected it
+// (2a) per (bh, block): how many queries selected it; the value each atomic returns is the
+// entry's place in the block's list
 __global__ void bwd_count_kernel(BwdParams p) {
   const long long total = (long long)p.B * p.H_kv * p.N * p.Ksel;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
     const long long item = i / p.Ksel;
     const int t = (int)(item % p.N), bh = (int)(item / p.N);
     const int blk = p.idx[i];
-    if (valid_block(p, blk, t)) atomicAdd(&p.counts[(long long)bh * p.M1 + blk], 1);
+    if (valid_block(p, blk, t)) p.rank[i] = atomicAdd(&p.counts[(long long)bh * p.M1 + blk], 1);
   }
 }
 
@@ -155,7 +157,7 @@ __global__ void bwd_scatter_kernel(BwdParams p) {
     const int blk = p.idx[i];
     if (!valid_block(p, blk, t)) continue;
     const long long key = (long long)bh * p.M1 + blk;
-    p.entries[p.offsets[key] + atomicAdd(&p.cursor[key], 1)] = (t << 5) | (int)(i - item * p.Ksel);
+    p.entries[p.offsets[key] + p.rank[i]] = (t << 5) | (int)(i - item * p.Ksel);
   }
 }
 
@@ -1232,9 +1234,9 @@ size_t attn_backward_workspace_bytes(const Problem& p, bool with_ds) {
   const long long ents = (long long)p.B * p.H_kv * p.N * p.K;
   const long long max_chunks = nkeys + ents / QC + 1;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + up((size_t)(nkeys + 1) * 4) +
-         up((size_t)ents * 4) + up((size_t)max_chunks * 16) + up(4) + up(ds) + up((size_t)max_chunks * 16) +
-         3 * up((size_t)NBUCKETS * 4) + (ds ? up((size_t)ents * 4) : 0);
+  return up((size_t)p.B * p.H_q * p.N * 4) + 3 * up((size_t)(nkeys + 1) * 4) + 2 * up((size_t)ents * 4) +
+         up((size_t)max_chunks * 16) + up(4) + up(ds) + up((size_t)max_chunks * 16) + 3 * up((size_t)NBUCKETS * 4) +
+         (ds ? up((size_t)ents * 4) : 0);
 }
 
 cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uint16_t* V, const int32_t* idx,
@@ -1272,8 +1274,8 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   w += up((size_t)pr.B * pr.H_q * pr.N * 4);
   p.counts = reinterpret_cast<int32_t*>(w);
   w += up((size_t)(nkeys + 1) * 4);
-  p.cursor = reinterpret_cast<int32_t*>(w);
-  w += up((size_t)(nkeys + 1) * 4);
+  p.rank = reinterpret_cast<int32_t*>(w);
+  w += up((size_t)ents * 4);
   p.offsets = reinterpret_cast<int32_t*>(w);
   w += up((size_t)(nkeys + 1) * 4);
   int32_t* chunk_off = reinterpret_cast<int32_t*>(w);
@@ -1301,7 +1303,6 @@ cudaError_t launch_attn_backward(const uint16_t* Q, const uint16_t* K, const uin
   while ((((long long)pr.N - 1) >> p.bucket_shift) >= NBUCKETS) ++p.bucket_shift;
   cudaError_t e;
   if ((e = cudaMemsetAsync(p.counts, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(p.cursor, 0, (size_t)(nkeys + 1) * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.bucket_count, 0, (size_t)NBUCKETS * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.bucket_cursor, 0, (size_t)NBUCKETS * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(dK, 0, (size_t)pr.B * pr.H_kv * pr.N_cap * pr.d * 4, s)) != cudaSuccess) return e;
