@@ -49,8 +49,8 @@ PAGES_REFERENCE = {
 # dram__bytes_write.sum from one ncu capture; the committed DRAM-traffic profile of that
 # workload), keyed by a hash of the kernel's sources: when the sources change the figure is
 # stale and is reported as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "fadf057976a670244f117a313678167481639d2c2f94de60b8df70bfb9d2be0d",
-                "workload": "prefill_256k", "bytes": 14240070912 + 1092140800}
+ATTN_TRAFFIC = {"sources_sha256": "d08e674a5394644a64eaa3641d85d3ece26482e276766945bbdb48aeb47ec65c",
+                "workload": "prefill_256k", "bytes": 14254132736 + 1091767040}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 

@@ -306,7 +306,7 @@ SelectLayout select_layout(const Problem& p) {
   };
   L.s2 = take(sizeof(int32_t) * total * p.K);
   L.score = take(sizeof(float) * total * 2 * p.K);
-  L.counts = take(sizeof(int32_t) * cb.nkeys);
+  L.counts = take(sizeof(int32_t) * (cb.nkeys + 1));  // the histogram, then Stage 1's item counter
   L.offsets = take(sizeof(int32_t) * cb.nkeys);
   L.tile_off = take(sizeof(int32_t) * cb.nkeys);
   L.block_sums = take(sizeof(int32_t) * 2 * cb.nblocks);
@@ -337,6 +337,7 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   float* score = leaf_score ? leaf_score : reinterpret_cast<float*>(w + L.score);
   ClusterBuffers cb = L.cb;
   cb.counts = reinterpret_cast<int32_t*>(w + L.counts);
+  cb.sched = cb.counts + cb.nkeys;
   cb.rank = reinterpret_cast<int32_t*>(score);  // list places, until Stage 2 writes the scores
   cb.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
   cb.tile_off = reinterpret_cast<int32_t*>(w + L.tile_off);
@@ -346,7 +347,7 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   cb.totals = reinterpret_cast<int32_t*>(w + L.totals);
   const Geometry geo = make_geometry(p.N, p.N);
   PhaseTimer tm(s);
-  if (cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * cb.nkeys, s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * (cb.nkeys + 1), s) != cudaSuccess) return PISA_ERR_CUDA;
   if (launch_stage1(Q, P, S2, cb, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
   tm.mark(PH_STAGE1);
   if (launch_cluster(S2, cb, p, s) != cudaSuccess) return PISA_ERR_CUDA;

@@ -31,12 +31,13 @@ struct ClusterBuffers {
   int32_t* entries;     // [B * H_kv * N * K]   (t << 6) | slot
   int4* tiles;          // [max_tiles]          {bh, node, entry start, entry count}
   int32_t* totals;      // [4] {entries, tiles, ...}
+  int32_t* sched;       // [1] Stage 1 item counter, zeroed with counts
   long long nkeys;
   int nwin, win, M2, qt, nblocks;
   long long max_tiles;
 };
 // Stage 1: level walk for every (b, h_kv, t); writes the level-2 survivors S2 [.., K] and adds
-// each survivor to the clustering histogram cb.counts (zeroed by the caller).
+// each survivor to the clustering histogram cb.counts (zeroed by the caller, with cb.sched).
 cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, const ClusterBuffers& cb, const Problem& p,
                           const Geometry& geo, int num_sms, uint32_t* err, cudaStream_t s);
 

@@ -7,7 +7,7 @@
 // the set of level-2 survivors S2 (<= K nodes); their eligible children are the leaf
 // candidates that Stage 2 scores exactly.
 //
-// One warp owns one (b, h_kv, t) at a time.  The group's G_Q query rows (padded to 16)
+// One warp owns one (b, h_kv, t) at a time, claimed from a counter.  The group's G_Q query rows (padded to 16)
 // stay in registers as mma.sync B fragments for the whole walk; each scored level gathers
 // the <= 2K x 2 child summaries straight from L2/L1 into registers with 16-byte loads and
 // multiplies them with m16n8k16 (the two children of 8 candidates x 8 heads per MMA, so a
@@ -46,24 +46,31 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
   const unsigned lt_mask = (1u << lane) - 1u;
   int* lst = lists[warp];
   const int BH = B * H_kv;
-  // items (bh, t), t in [t_lo, t_lo + nq), with a grid stride applied as (bh, t) increments
-  const long long gw = (long long)blockIdx.x * (THREADS / 32) + warp;
-  const long long nwarps = (long long)gridDim.x * (THREADS / 32);
-  const int st_bh = (int)(nwarps / nq), st_t = (int)(nwarps % nq);
-  const int t_end = t_lo + nq;
+  // Items i = bh * nq + (t - t_lo) are claimed one at a time from a counter, so that CTAs
+  // that start late (their SM still held by a kernel of another stream) take fewer of them
+  // and the kernel ends on a tail of one walk.  The claim of the item after next is issued
+  // as a walk starts and read when it ends, so its round trip overlaps the walk.  The count
+  // fits 32 bits: the clustering lists already bound B * H_kv * N * K below 2^31.
+  const int total = BH * nq;
+  auto claim = [&]() {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(cb.sched, 1);
+    return __shfl_sync(0xffffffffu, v, 0);
+  };
+  int cur = claim();
+  int nxt = claim();
 
   bool pend = false;  // this lane holds the list place of a survivor not yet stored
   int pend_rank = 0;
-  long long pend_item = 0;
-  for (int bh = (int)(gw / nq), t = t_lo + (int)(gw % nq); bh < BH;) {
+  int pend_item = 0;  // bh * N + t, below B * H_kv * N < 2^31
+  while (cur < total) {
+    int fut = 0;
+    if (lane == 0) fut = atomicAdd(cb.sched, 1);
+    const int bh = cur / nq, t = t_lo + (cur - bh * nq);
     const long long item = (long long)bh * N + t;
     const int b = bh / H_kv, hk = bh - b * H_kv;
-    int nbh = bh + st_bh, nt = t + st_t;  // the next item
-    if (nt >= t_end) {
-      nt -= nq;
-      ++nbh;
-    }
-    if (nbh < BH) {  // move its Q rows towards L2 while this walk runs (128 bytes per lane)
+    if (nxt < total) {  // move the next item's Q rows towards L2 while this walk runs (128 bytes per lane)
+      const int nbh = nxt / nq, nt = t_lo + (nxt - nbh * nq);
       const int nb = nbh / H_kv, nhk = nbh - nb * H_kv;
       const uint16_t* nq = Q + (((size_t)nb * N + nt) * H_q + (size_t)nhk * GQ) * D;
       if (lane * 64 < GQ * D) prefetch_l2(nq + (size_t)lane * 64);
@@ -238,16 +245,16 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
     // the clustering histogram: one entry per survivor in the list of key (b, h_kv, window,
     // node); the count returned is the entry's place in that list, stored one item later so
     // that the atomic's round trip overlaps the next walk
-    if (pend) cb.rank[pend_item * (2 * Ksel) + lane] = pend_rank;
+    if (pend) cb.rank[(long long)pend_item * (2 * Ksel) + lane] = pend_rank;
     pend = lane < ns;
     if (pend) {
       pend_rank = atomicAdd(&cb.counts[((long long)bh * cb.nwin + t / cb.win) * cb.M2 + surv], 1);
-      pend_item = item;
+      pend_item = (int)item;
     }
-    bh = nbh;
-    t = nt;
+    cur = nxt;
+    nxt = __shfl_sync(0xffffffffu, fut, 0);
   }
-  if (pend) cb.rank[pend_item * (2 * Ksel) + lane] = pend_rank;
+  if (pend) cb.rank[(long long)pend_item * (2 * Ksel) + lane] = pend_rank;
 }
 
 }  // namespace
@@ -258,8 +265,8 @@ cudaError_t launch_stage1(const uint16_t* Q, const uint16_t* P, int32_t* S2, con
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * nq;
   if (total <= 0) return cudaSuccess;
-  // persistent grid: exactly the CTAs that are resident at once, each walking items with a
-  // grid stride, so no second partial wave
+  // persistent grid: exactly the CTAs that are resident at once, each warp claiming items from
+  // the counter, so no second partial wave
   auto go = [&](auto kern) -> cudaError_t {
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, 0);
