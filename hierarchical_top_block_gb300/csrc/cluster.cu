@@ -8,12 +8,16 @@
 //   count   : histogram of entries per key (atomics; accumulated by the Stage 1 walk as it
 //             writes each query's survivors, into counts zeroed before it; the value each
 //             atomic returned is the entry's place k in its list, kept in cb.rank)
-//   scan    : exclusive scans of counts and of ceil(count / qt) (three small kernels)
+//   scan    : exclusive scans of counts and of ceil(count / qt) (three small kernels; the
+//             second also zeroes Stage 2's tile counter)
 //   scatter : entries[offset[key] + k] = (t << 6) | slot   (order within a key arbitrary)
 //   tiles   : {bh, node, first entry, entry count <= qt} for every tile
+//             (scatter and tiles are independent: one launch, split by block)
+// Each kernel is launched as a programmatic dependent of the one before it on the stream.
 // The order of entries inside a list does not change any result: each entry is scored
 // on its own and written to its own (t, slot) location.
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace pisa {
 namespace {
@@ -60,6 +64,8 @@ __device__ int2 block_excl_scan(int2 v, int2* total) {
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) scan_local_kernel(ClusterBuffers cb) {
+  pdl_trigger();
+  pdl_wait();
   const long long base = (long long)blockIdx.x * SCAN_CHUNK + (long long)threadIdx.x * SCAN_PER_THREAD;
   int2 vals[SCAN_PER_THREAD];
   int2 sum = make_int2(0, 0);
@@ -90,6 +96,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_local_kernel(ClusterBuffers
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) scan_blocks_kernel(ClusterBuffers cb) {
+  pdl_trigger();
+  pdl_wait();
   // single block: exclusive scan of the block totals in chunks, carrying the running sum
   int2 carry = make_int2(0, 0);
   for (int base = 0; base < cb.nblocks; base += SCAN_THREADS) {
@@ -107,10 +115,14 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_blocks_kernel(ClusterBuffer
   if (threadIdx.x == 0) {
     cb.totals[0] = carry.x;
     cb.totals[1] = carry.y;
+    cb.totals[2] = 0;  // Stage 2's tile counter
+    cb.totals[3] = 0;
   }
 }
 
 __global__ void __launch_bounds__(SCAN_THREADS) scan_add_kernel(ClusterBuffers cb) {
+  pdl_trigger();
+  pdl_wait();
   const int bx = blockIdx.x;
   const int ax = cb.block_sums[2 * bx], ay = cb.block_sums[2 * bx + 1];
   const long long base = (long long)bx * SCAN_CHUNK;
@@ -123,10 +135,27 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_add_kernel(ClusterBuffers c
   }
 }
 
-__global__ void scatter_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int t_lo, int nq, int Ksel,
-                               long long total) {
+// blocks [0, nb_scatter) place the entries, the others write the tile list
+__global__ void scatter_tiles_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb, int N, int t_lo, int nq, int Ksel,
+                                     long long total, int nb_scatter) {
+  pdl_trigger();
+  pdl_wait();
+  if ((int)blockIdx.x >= nb_scatter) {
+    const long long nb_tiles = (long long)gridDim.x - nb_scatter;
+    for (long long k = ((long long)blockIdx.x - nb_scatter) * blockDim.x + threadIdx.x; k < cb.nkeys;
+         k += nb_tiles * blockDim.x) {
+      const int n = cb.counts[k];
+      if (n == 0) continue;
+      const int node = (int)(k % cb.M2);
+      const int bh = (int)(k / ((long long)cb.nwin * cb.M2));
+      const int e0 = cb.offsets[k];
+      int tix = cb.tile_off[k];
+      for (int s = 0; s < n; s += cb.qt, ++tix) cb.tiles[tix] = make_int4(bh, node, e0 + s, min(cb.qt, n - s));
+    }
+    return;
+  }
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total * Ksel;
-       e += (long long)gridDim.x * blockDim.x) {
+       e += (long long)nb_scatter * blockDim.x) {
     const long long item = e / Ksel;
     const int slot = (int)(e - item * Ksel);
     const int bh = (int)(item / nq), t = t_lo + (int)(item % nq);
@@ -135,19 +164,6 @@ __global__ void scatter_kernel(const int32_t* __restrict__ S2, ClusterBuffers cb
     const long long key = key_of(bh, t, node, cb);
     const int pos = cb.offsets[key] + cb.rank[((long long)bh * N + t) * (2 * Ksel) + slot];
     cb.entries[pos] = (t << 6) | slot;
-  }
-}
-
-__global__ void tiles_kernel(ClusterBuffers cb) {
-  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < cb.nkeys;
-       k += (long long)gridDim.x * blockDim.x) {
-    const int n = cb.counts[k];
-    if (n == 0) continue;
-    const int node = (int)(k % cb.M2);
-    const int bh = (int)(k / ((long long)cb.nwin * cb.M2));
-    const int e0 = cb.offsets[k];
-    int tix = cb.tile_off[k];
-    for (int s = 0; s < n; s += cb.qt, ++tix) cb.tiles[tix] = make_int4(bh, node, e0 + s, min(cb.qt, n - s));
   }
 }
 
@@ -163,13 +179,12 @@ cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Pr
   const int nq = p.t_hi - p.t_lo;
   const long long total = (long long)p.B * p.H_kv * (nq > 0 ? nq : 0);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(cb.totals, 0, sizeof(int32_t) * 4, s)) != cudaSuccess) return e;  // [2] = tile counter
-  scan_local_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
-  scan_blocks_kernel<<<1, SCAN_THREADS, 0, s>>>(cb);
-  scan_add_kernel<<<cb.nblocks, SCAN_THREADS, 0, s>>>(cb);
-  scatter_kernel<<<grid_for(total * p.K, THREADS), THREADS, 0, s>>>(S2, cb, p.N, p.t_lo, nq, p.K, total);
-  tiles_kernel<<<grid_for(cb.nkeys, THREADS), THREADS, 0, s>>>(cb);
-  return cudaGetLastError();
+  if ((e = launch_pdl(scan_local_kernel, dim3(cb.nblocks), dim3(SCAN_THREADS), 0, s, cb)) != cudaSuccess) return e;
+  if ((e = launch_pdl(scan_blocks_kernel, dim3(1), dim3(SCAN_THREADS), 0, s, cb)) != cudaSuccess) return e;
+  if ((e = launch_pdl(scan_add_kernel, dim3(cb.nblocks), dim3(SCAN_THREADS), 0, s, cb)) != cudaSuccess) return e;
+  const int nb_scatter = grid_for(total * p.K, THREADS), nb_tiles = grid_for(cb.nkeys, THREADS);
+  return launch_pdl(scatter_tiles_kernel, dim3(nb_scatter + nb_tiles), dim3(THREADS), 0, s, S2, cb, p.N, p.t_lo, nq,
+                    p.K, total, nb_scatter);
 }
 
 }  // namespace pisa

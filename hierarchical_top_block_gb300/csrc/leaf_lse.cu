@@ -29,8 +29,10 @@
 //               taking tiles g, g+3, ... in its own accumulator; each warp reduces both
 //               leaves of its rows.
 // Every wait is bounded; on timeout the error word is set, the MMAs and TMA loads still in
-// flight are waited for (bounded) and the CTA exits.
+// flight are waited for (bounded) and the CTA exits.  Launched as a programmatic dependent of
+// the clustering's last kernel.
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace pisa {
 namespace {
@@ -90,6 +92,8 @@ template <int D, int SC, int R>
 __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                               const __grid_constant__ CUtensorMap mapK, Params prm,
                                                               uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();  // the tile list and its counts come from the kernel before
   constexpr int HALVES = D / 64;
   constexpr uint32_t STAGE_BYTES = ROWS * D * 2;   // also the K-pair stage size (KEYS == ROWS)
   constexpr int KSTEPS = D / 16;
@@ -549,8 +553,7 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
     if (fa.maxThreadsPerBlock < THREADS) return cudaErrorLaunchOutOfResources;  // registers x threads
-    kern<<<num_sms, THREADS, smem, s>>>(mapQ, mapK, prm, err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(THREADS), smem, s, mapQ, mapK, prm, err);
   };
   if (p.GQ == 16 && RPQ == 16) return p.scoring == 0 ? go(leaf_lse_kernel<D, 0, 16>) : go(leaf_lse_kernel<D, -1, 16>);
   return p.scoring == 0 ? go(leaf_lse_kernel<D, 0, 0>) : go(leaf_lse_kernel<D, -1, 0>);

@@ -17,6 +17,7 @@
 // shuffles: no query-key score matrix is materialised.  Each survivor is also counted into
 // the clustering histogram, and the count returned is stored as its place in its list.
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace pisa {
 namespace {
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(THREADS, D == 128 ? MIN_BLOCKS_128 : MIN_BLOCK
                                                          ClusterBuffers cb,
                                                          int B, int N, int H_q, int H_kv, int GQ, int Ksel, int causal,
                                                          float scale_log2, int t_lo, int nq, Geometry geo) {
+  pdl_trigger();  // the clustering's first kernel may launch (it waits for this one to end)
   constexpr int scoring = SC;
   constexpr int NCH = D / 32;  // 32-wide d chunks; each feeds two k16 steps
   constexpr int KH = NCH / 2;      // chunks loaded together

@@ -7,6 +7,7 @@
 // One warp per (b, h_kv, t); lane s owns candidate slot s = 2i + c (child c of the i-th
 // level-2 survivor), so g*K <= 32 slots fit one warp; for K up to 32 each lane owns two.
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace pisa {
 namespace {
@@ -17,6 +18,8 @@ constexpr int THREADS = 256;
 __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict__ S2,
                                                        float* __restrict__ score, int32_t* __restrict__ idx,
                                                        int BH, int N, int t_lo, int nq, int Ksel, int M1, int causal) {
+  pdl_trigger();
+  pdl_wait();  // the leaf scores come from Stage 2
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
   const long long gw = (long long)blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5);
@@ -99,6 +102,8 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const int32_t* __restrict
 __global__ void __launch_bounds__(THREADS) topk64_kernel(const int32_t* __restrict__ S2,
                                                          float* __restrict__ score, int32_t* __restrict__ idx,
                                                          int BH, int N, int t_lo, int nq, int Ksel, int M1, int causal) {
+  pdl_trigger();
+  pdl_wait();  // the leaf scores come from Stage 2
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
   const long long gw = (long long)blockIdx.x * (THREADS / 32) + (threadIdx.x >> 5);
@@ -164,13 +169,9 @@ cudaError_t launch_topk(const int32_t* S2, float* leaf_score, int32_t* idx, cons
   // item's rows are in flight while the current one is ranked)
   long long blocks = (total + (THREADS / 32) - 1) / (THREADS / 32);
   if (blocks > (long long)num_sms * 8) blocks = (long long)num_sms * 8;
-  if (p.K > 16)
-    topk64_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1],
-                                                  p.causal);
-  else
-    topk_kernel<<<(int)blocks, THREADS, 0, s>>>(S2, leaf_score, idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1],
-                                                p.causal);
-  return cudaGetLastError();
+  // a programmatic dependent of Stage 2
+  return launch_pdl(p.K > 16 ? topk64_kernel : topk_kernel, dim3((unsigned)blocks), dim3(THREADS), 0, s, S2, leaf_score,
+                    idx, p.B * p.H_kv, p.N, p.t_lo, nq, p.K, geo.M[1], p.causal);
 }
 
 }  // namespace pisa
