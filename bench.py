@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s (select + sparse attn)"
 UNIT = "tokens/s"
-KERNELS_PER_STEP = 11  # pyramid 2, stage 1 (with the clustering histogram), clustering 5, leaf LSE, top-K, attention
+KERNELS_PER_STEP = 10  # pyramid 2, stage 1 (with the clustering histogram), clustering 4 (three scans, scatter and tiles in one), leaf LSE, top-K, attention
 
 # The paper's own figures for this path (summary page "Block Sparse Attention with Log-Linear
 # Complexity", section "Experimental results", item 5, Fig. 3): context only.  They are ratios
