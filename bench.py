@@ -49,8 +49,8 @@ PAGES_REFERENCE = {
 # dram__bytes_write.sum from one ncu capture; the committed DRAM-traffic profile of that
 # workload), keyed by a hash of the kernel's sources: when the sources change the figure is
 # stale and is reported as null until it is taken again.
-ATTN_TRAFFIC = {"sources_sha256": "d08e674a5394644a64eaa3641d85d3ece26482e276766945bbdb48aeb47ec65c",
-                "workload": "prefill_256k", "bytes": 14254132736 + 1091767040}
+ATTN_TRAFFIC = {"sources_sha256": "9ed724c54f00616b0cb692bf96f4336023006022014a0b1f66ec429cbc54faf3",
+                "workload": "prefill_256k", "bytes": 14359143936 + 1091798784}
 ATTN_SOURCES = ["hierarchical_top_block_gb300/csrc/sparse_attn.cu", "hierarchical_top_block_gb300/csrc/common.cuh",
                 "hierarchical_top_block_gb300/csrc/kernels.cuh"]
 

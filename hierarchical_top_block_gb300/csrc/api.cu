@@ -21,13 +21,14 @@ constexpr int MAX_DEVICES = 64;
 
 // Streams and events of the host-buffer prefill pipeline (created on first use).
 constexpr int PIPE_MAX_CHUNKS = 16;
-constexpr int PIPE_EVENTS = 4 + 4 * PIPE_MAX_CHUNKS;
+constexpr int PIPE_EVENTS = 4 + 6 * PIPE_MAX_CHUNKS;
 
 struct HostPipe {
   bool ready = false;
   std::mutex run;                                    // one host-buffer prefill at a time per device
   cudaStream_t in = nullptr, out = nullptr;          // host->device and device->host copies
   cudaStream_t attn = nullptr;                       // attention of chunk j beside selection of j+1
+  cudaStream_t pyr = nullptr;                        // pyramid over each chunk's key slice (causal)
   cudaEvent_t ev[PIPE_EVENTS] = {};
 };
 
@@ -191,6 +192,7 @@ pisa_status host_pipe(DeviceState* st, HostPipe** out) {
     if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&hp.attn, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&hp.pyr, cudaStreamNonBlocking) != cudaSuccess) return PISA_ERR_CUDA;
     for (cudaEvent_t& e : hp.ev)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return PISA_ERR_CUDA;
     hp.ready = true;
@@ -241,6 +243,22 @@ Geometry make_geometry(long long n, long long n_cap) {
   }
   g.nodes = off;
   return g;
+}
+
+// Keys [0, x) that the causal selection and attention of queries t < T read, x returned.  The
+// level walk reads the child summaries of a level-l candidate (l >= 2: 2^(l+5) keys, starting at
+// or before t) only at levels where more than K candidates can be eligible, i.e. where
+// ((T - 1) >> (l + 5)) + 1 > K; Stage 2 reads the 128 keys of level-2 nodes that start at or before
+// t, and the attention the 64-key blocks that do.  So x is the end of the last eligible node at
+// the highest level with more than K of them, or of the last eligible level-2 node.
+long long causal_key_prefix(long long T, int Ksel, const Geometry& g, long long N) {
+  if (T <= 0) return 0;
+  long long x = (((T - 1) >> 7) + 1) << 7;
+  for (int l = 2; l <= g.L - 1; ++l) {  // the levels the walk may score
+    const long long cnt = ((T - 1) >> (l + 5)) + 1;
+    if (cnt > Ksel) x = std::max(x, cnt << (l + 5));
+  }
+  return std::min(x, N);
 }
 
 pisa_status check_params(const pisa_shape& s, const pisa_params& pr, Problem* p) {
@@ -592,15 +610,18 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   w += round_up(lseb, 256);
   const size_t sel_bytes = select_layout(p).total_bytes;
 
-  // Query chunks: selection and attention of chunk j need Q rows of chunk j only (plus all
-  // of K, and V up to the chunk's last position when causal), so the copy-in of chunk j+1
-  // and the copy-out of chunk j-1 overlap the compute of chunk j; attention of chunk j (its
-  // own stream) also overlaps selection of chunk j+1, which fills the tail of each
-  // persistent kernel with the next one's CTAs.  K goes first (the pyramid needs all of it);
-  // then each chunk's Q rows and, when causal, the V rows up to the end of the 64-key block
-  // that holds the chunk's last position (the attention of chunk j reads V rows of blocks
-  // that start at or before its positions, and no further); without causality V goes whole
-  // after Q0.
+  // Query chunks: selection and attention of chunk j need Q rows of chunk j only (plus K, and
+  // V up to the chunk's last position when causal), so the copy-in of chunk j+1 and the
+  // copy-out of chunk j-1 overlap the compute of chunk j; attention of chunk j (its own
+  // stream) also overlaps selection of chunk j+1, which fills the tail of each persistent
+  // kernel with the next one's CTAs.  When causal, each chunk's K rows come first: those below
+  // the prefix its selection reads (causal_key_prefix; the last chunk's slice ends at N), and a
+  // fourth stream builds the pyramid nodes that meet the slice while the chunks before are
+  // computed (none of them reads those nodes: each meets keys past their prefixes); then the
+  // chunk's Q rows and the V rows up to the end of the 64-key block that holds its last
+  // position (the attention of chunk j reads V rows of blocks that start at or before its
+  // positions, and no further).  Without causality every node is eligible: K goes whole and
+  // first, the pyramid follows on `stream`, and V goes whole after Q0.
   // The two share only idx, whose rows of different chunks are disjoint; selection scratch
   // is reused from chunk to chunk in the order of `stream`.  Q and O are [B][N][H_q][d]: a
   // chunk is one row band per sequence.
@@ -612,6 +633,13 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   cudaEvent_t* e_sel = ev + 4 + PIPE_MAX_CHUNKS;
   cudaEvent_t* e_attn = ev + 4 + 2 * PIPE_MAX_CHUNKS;
   cudaEvent_t* e_vs = ev + 4 + 3 * PIPE_MAX_CHUNKS;  // V rows of chunks 0..j in place (causal)
+  cudaEvent_t* e_ks = ev + 4 + 4 * PIPE_MAX_CHUNKS;  // K rows below kpre[j + 1] in place (causal)
+  cudaEvent_t* e_py = ev + 4 + 5 * PIPE_MAX_CHUNKS;  // pyramid nodes below kpre[j + 1] exact (causal)
+  const Geometry geo = make_geometry(p.N, p.N);
+  long long kpre[PIPE_MAX_CHUNKS + 1];  // chunk j reads keys [0, kpre[j + 1])
+  kpre[0] = 0;
+  for (int j = 0; j < nchunks; ++j)
+    kpre[j + 1] = j + 1 == nchunks ? p.N : std::max(kpre[j], causal_key_prefix(bounds[j + 1], p.K, geo, p.N));
   const size_t q_row = (size_t)p.H_q * p.d * 2;  // bytes of one query position, all heads
   auto copy_q = [&](int j) {
     const long long lo = bounds[j], hi = bounds[j + 1];
@@ -625,15 +653,27 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   chk(cudaEventRecord(e_start, s));
   chk(cudaStreamWaitEvent(hp->in, e_start, 0));
   chk(cudaStreamWaitEvent(hp->attn, e_start, 0));
+  chk(cudaStreamWaitEvent(hp->pyr, e_start, 0));
   const size_t kv_row = (size_t)p.d * 2;  // bytes of one key position of one KV head
   auto copy_v = [&](long long lo, long long hi) {  // positions lo .. hi - 1 of every (b, h_kv)
     return cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(dV) + lo * kv_row, p.N * kv_row,
                              reinterpret_cast<const uint8_t*>(V_host) + lo * kv_row, p.N * kv_row, (hi - lo) * kv_row,
                              (size_t)p.B * p.H_kv, cudaMemcpyHostToDevice, hp->in);
   };
-  chk(cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, hp->in));
-  chk(cudaEventRecord(e_k, hp->in));
+  auto copy_k = [&](long long lo, long long hi) {  // positions lo .. hi - 1 of every (b, h_kv)
+    return cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(dK) + lo * kv_row, p.N * kv_row,
+                             reinterpret_cast<const uint8_t*>(K_host) + lo * kv_row, p.N * kv_row, (hi - lo) * kv_row,
+                             (size_t)p.B * p.H_kv, cudaMemcpyHostToDevice, hp->in);
+  };
+  if (!p.causal) {
+    chk(cudaMemcpyAsync(dK, K_host, kv, cudaMemcpyHostToDevice, hp->in));
+    chk(cudaEventRecord(e_k, hp->in));
+  }
   for (int j = 0; j < nchunks && ok; ++j) {
+    if (p.causal) {
+      if (kpre[j + 1] > kpre[j]) chk(copy_k(kpre[j], kpre[j + 1]));
+      chk(cudaEventRecord(e_ks[j], hp->in));
+    }
     chk(copy_q(j));
     chk(cudaEventRecord(e_q[j], hp->in));
     if (p.causal) {
@@ -645,14 +685,22 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
       chk(cudaEventRecord(e_v, hp->in));
     }
   }
-  const Geometry geo = make_geometry(p.N, p.N);
-  chk(cudaStreamWaitEvent(s, e_k, 0));
-  if (ok) chk(launch_pyramid(dK, dP, p, geo, s));
+  if (p.causal) {
+    for (int j = 0; j < nchunks && ok; ++j) {
+      chk(cudaStreamWaitEvent(hp->pyr, e_ks[j], 0));
+      if (ok) chk(launch_pyramid_range(dK, dP, p, geo, kpre[j], kpre[j + 1], hp->pyr));
+      chk(cudaEventRecord(e_py[j], hp->pyr));
+    }
+  } else {
+    chk(cudaStreamWaitEvent(s, e_k, 0));
+    if (ok) chk(launch_pyramid(dK, dP, p, geo, s));
+  }
   if (!p.causal) chk(cudaStreamWaitEvent(hp->attn, e_v, 0));
   for (int j = 0; j < nchunks && ok; ++j) {
     Problem pc = p;
     pc.t_lo = (int)bounds[j];
     pc.t_hi = (int)bounds[j + 1];
+    if (p.causal) chk(cudaStreamWaitEvent(s, e_py[j], 0));
     chk(cudaStreamWaitEvent(s, e_q[j], 0));
     if (!ok) break;
     if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, pc, st, s)) != PISA_OK) {
@@ -682,10 +730,11 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
   const cudaError_t e_rec = cudaEventRecord(e_end, hp->out);
   if (e_rec == cudaSuccess) cudaStreamWaitEvent(s, e_end, 0);
   const cudaError_t e_in = cudaStreamSynchronize(hp->in), e_at = cudaStreamSynchronize(hp->attn);
+  const cudaError_t e_py_sync = cudaStreamSynchronize(hp->pyr);
   const cudaError_t e_out = cudaStreamSynchronize(hp->out), e_s = cudaStreamSynchronize(s);
   if (rc != PISA_OK) return rc;
   if (!ok || e_rec != cudaSuccess || e_in != cudaSuccess || e_at != cudaSuccess || e_out != cudaSuccess ||
-      e_s != cudaSuccess)
+      e_s != cudaSuccess || e_py_sync != cudaSuccess)
     return PISA_ERR_CUDA;
   return PISA_OK;
 }

@@ -18,6 +18,10 @@ struct Problem {
 
 // Builds pyramid levels 1..geo.L from the first N rows of K (layout capacity N_cap).
 cudaError_t launch_pyramid(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s);
+// Rewrites the nodes whose span meets keys [key_lo, key_hi); builds over consecutive ranges,
+// each run once the keys below its key_hi are in place, leave the nodes below the last key_hi exact.
+cudaError_t launch_pyramid_range(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, long long key_lo,
+                                 long long key_hi, cudaStream_t s);
 
 // Clustering of (query, level-2 survivor) entries into per-(b, h_kv, window, node) lists
 // and Q tiles for Stage 2.

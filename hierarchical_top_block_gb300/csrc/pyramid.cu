@@ -9,6 +9,10 @@
 // HBM streaming: K is read once with 16-byte coalesced loads (one warp per leaf);
 // each CTA owns a 16-leaf subtree and writes levels 1..5 of it from shared memory; a
 // second small kernel builds the levels above (one CTA per (b, h_kv)).
+// A build can be limited to a key range [lo, hi): it rewrites every node whose span meets the
+// range (from K rows that may be incomplete past hi).  A sequence of builds over consecutive
+// ranges, each run once the keys below its hi are in place, leaves every node whose span ends
+// at or below the last hi exact: the last build that met its span ran with all its keys.
 #include "kernels.cuh"
 
 namespace pisa {
@@ -21,13 +25,13 @@ constexpr int THREADS = 256;
 template <int D>
 __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t* __restrict__ K,
                                                                  uint16_t* __restrict__ P, int N, int N_cap,
-                                                                 Geometry geo, int top_level) {
+                                                                 Geometry geo, int top_level, int sub0, long long key_lo) {
   constexpr int LPR = D / 8;        // lanes per key row (16 bytes each)
   constexpr int RPI = 32 / LPR;     // rows per warp iteration
   __shared__ __align__(16) uint16_t buf[2][LPB][D];
 
   const int bh = blockIdx.y;
-  const int sub = blockIdx.x;
+  const int sub = sub0 + (int)blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint16_t* Kb = K + (size_t)bh * N_cap * D;
   uint16_t* Pb = P + (size_t)bh * geo.nodes * D;
@@ -79,7 +83,8 @@ __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t*
         packed[k] = (uint32_t)a | ((uint32_t)b << 16);
       }
       uint4 out = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      *reinterpret_cast<uint4*>(Pb + (size_t)(geo.off[1] + leaf) * D + col) = out;
+      // nodes below the range are exact already (and may be read meanwhile): not rewritten
+      if ((long long)(leaf + 1) * 64 > key_lo) *reinterpret_cast<uint4*>(Pb + (size_t)(geo.off[1] + leaf) * D + col) = out;
       *reinterpret_cast<uint4*>(&buf[0][li][col]) = out;
     }
   }
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t*
       float s, err;
       two_sum(a, b, s, err);
       const uint16_t v = bf16_mean(s, err, c1 - c0);
-      Pb[(size_t)(geo.off[l] + node) * D + e] = v;
+      if (((long long)(node + 1) << (l + 5)) > key_lo) Pb[(size_t)(geo.off[l] + node) * D + e] = v;
       buf[cur ^ 1][i][e] = v;
     }
     __syncthreads();
@@ -114,13 +119,16 @@ __global__ void __launch_bounds__(THREADS) pyramid_leaves_kernel(const uint16_t*
 // stores, so a level costs about one memory round trip per batch instead of one per value.
 template <int D>
 __global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __restrict__ P, Geometry geo,
-                                                                int first_level) {
+                                                                int first_level, long long key_lo, long long key_hi) {
   constexpr int CH = D / 8;   // chunks per row
   constexpr int BATCH = 8;
   uint16_t* Pb = P + (size_t)blockIdx.x * geo.nodes * D;
   for (int l = first_level; l <= geo.L; ++l) {
     const int m = geo.M[l], mc = geo.M[l - 1];
-    const int total = m * CH;
+    // the nodes whose span (2^(l+5) keys) meets [key_lo, key_hi)
+    const int n0 = (int)(key_lo >> (l + 5));
+    const int n1 = (int)min((long long)m, ((key_hi - 1) >> (l + 5)) + 1);
+    const int total = (n1 - n0) * CH;
     const uint16_t* src = Pb + (size_t)geo.off[l - 1] * D;
     uint16_t* dst = Pb + (size_t)geo.off[l] * D;
     for (int base = threadIdx.x; base < total; base += THREADS * BATCH) {
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __rest
         const int idx = base + u * THREADS;
         va[u] = vb[u] = make_uint4(0, 0, 0, 0);
         if (idx < total) {
-          const int node = idx / CH, c = idx - node * CH;
+          const int node = n0 + idx / CH, c = idx - (idx / CH) * CH;
           va[u] = *reinterpret_cast<const uint4*>(src + (size_t)(2 * node) * D + 8 * c);
           if (2 * node + 1 < mc) vb[u] = *reinterpret_cast<const uint4*>(src + (size_t)(2 * node + 1) * D + 8 * c);
         }
@@ -139,7 +147,7 @@ __global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __rest
       for (int u = 0; u < BATCH; ++u) {
         const int idx = base + u * THREADS;
         if (idx >= total) continue;
-        const int node = idx / CH, c = idx - node * CH;
+        const int node = n0 + idx / CH, c = idx - (idx / CH) * CH;
         const int cnt = 2 * node + 1 < mc ? 2 : 1;
         const uint32_t wa[4] = {va[u].x, va[u].y, va[u].z, va[u].w}, wb[4] = {vb[u].x, vb[u].y, vb[u].z, vb[u].w};
         uint32_t packed[4];
@@ -158,20 +166,29 @@ __global__ void __launch_bounds__(THREADS) pyramid_upper_kernel(uint16_t* __rest
 }
 
 template <int D>
-cudaError_t launch_pyramid_d(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s) {
-  if (geo.L == 0) return cudaSuccess;
+cudaError_t launch_pyramid_d(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, long long key_lo,
+                             long long key_hi, cudaStream_t s) {
+  if (geo.L == 0 || key_hi <= key_lo) return cudaSuccess;
   const int top = geo.L < SUB_LEVELS ? geo.L : SUB_LEVELS;
-  dim3 grid((geo.M[1] + LPB - 1) / LPB, p.B * p.H_kv);
-  pyramid_leaves_kernel<D><<<grid, THREADS, 0, s>>>(K, P, p.N, p.N_cap, geo, top);
-  if (geo.L > top) pyramid_upper_kernel<D><<<p.B * p.H_kv, THREADS, 0, s>>>(P, geo, top + 1);
+  // the 16-leaf subtrees (1024 keys) that meet the range
+  const int sub0 = (int)(key_lo / (64 * LPB)), sub1 = (int)((key_hi - 1) / (64 * LPB)) + 1;
+  dim3 grid(sub1 - sub0, p.B * p.H_kv);
+  pyramid_leaves_kernel<D><<<grid, THREADS, 0, s>>>(K, P, p.N, p.N_cap, geo, top, sub0, key_lo);
+  if (geo.L > top) pyramid_upper_kernel<D><<<p.B * p.H_kv, THREADS, 0, s>>>(P, geo, top + 1, key_lo, key_hi);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+cudaError_t launch_pyramid_range(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, long long key_lo,
+                                 long long key_hi, cudaStream_t s) {
+  if (key_hi > p.N) key_hi = p.N;
+  if (p.d == 128) return launch_pyramid_d<128>(K, P, p, geo, key_lo, key_hi, s);
+  return launch_pyramid_d<64>(K, P, p, geo, key_lo, key_hi, s);
+}
+
 cudaError_t launch_pyramid(const uint16_t* K, uint16_t* P, const Problem& p, const Geometry& geo, cudaStream_t s) {
-  if (p.d == 128) return launch_pyramid_d<128>(K, P, p, geo, s);
-  return launch_pyramid_d<64>(K, P, p, geo, s);
+  return launch_pyramid_range(K, P, p, geo, 0, p.N, s);
 }
 
 }  // namespace pisa

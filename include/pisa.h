@@ -204,12 +204,15 @@ PISA_API pisa_status pisa_sparse_attn_backward(const uint16_t* Q, const uint16_t
  * in query chunks (at most 11: doubling from N/32 positions, at least 8192, up to N/4 and
  * halving again towards the end, equal chunks of at most N/4 between) so that the host -> device copy of the next
  * chunk's Q, the device -> host copy of the previous chunk's O and the attention of one chunk
- * overlap the selection of the next (K is copied first, whole; in causal mode V follows in
- * the same chunks as Q, each extended to the end of the 64-key block of its last position,
- * since a chunk's attention reads no later block; otherwise V is copied whole after the
- * first chunk's Q): selection runs on `stream`, attention and the copies on
- * three streams of the library's own (ordered after the work queued on `stream` before the
- * call), and all of them are idle again on return.  Results equal those of pisa_build_pyramid + pisa_select_prefill +
+ * overlap the selection of the next.  In causal mode each chunk's K rows go first: the keys
+ * its selection can read (the summaries of the levels where more than K candidates can be
+ * eligible, and the leaf pairs and blocks that start at or before its last position), with
+ * the pyramid nodes over them built on a stream of their own while earlier chunks are
+ * computed; V follows in the same chunks as Q, each extended to the end of the 64-key block of
+ * its last position, since a chunk's attention reads no later block.  Otherwise K is copied
+ * first and whole, and V whole after the first chunk's Q.  Selection runs on `stream`;
+ * attention, the copies and the pyramid on four streams of the library's own (ordered after
+ * the work queued on `stream` before the call), and all of them are idle again on return.  Results equal those of pisa_build_pyramid + pisa_select_prefill +
  * pisa_sparse_attn_prefill on the same inputs.  One call at a time per device (calls from
  * several threads are serialised).  Host buffers should be pinned for full copy bandwidth
  * and concurrent copies.  dev_ws is device scratch of at least
