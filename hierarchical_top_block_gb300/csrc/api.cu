@@ -345,8 +345,11 @@ bool entry_lists_fit(const Problem& p) {
   return select_layout(p).cb.max_tiles < (1LL << 31);
 }
 
+// counts_zero: the scratch's histogram and Stage 1's item counter are zero already (Stage 2 of a
+// selection over the same scratch leaves them so), and the memset before Stage 1 is skipped.
 pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, int32_t* idx, float* leaf_score,
-                       int32_t* s2, void* ws, size_t ws_bytes, const Problem& p, DeviceState* st, cudaStream_t s) {
+                       int32_t* s2, void* ws, size_t ws_bytes, const Problem& p, DeviceState* st, cudaStream_t s,
+                       bool counts_zero = false) {
   if (!entry_lists_fit(p)) return PISA_ERR_UNSUPPORTED;
   SelectLayout L = select_layout(p);
   if (ws_bytes < L.total_bytes) return PISA_ERR_WORKSPACE;
@@ -365,7 +368,8 @@ pisa_status run_select(const uint16_t* Q, const uint16_t* K, const uint16_t* P, 
   cb.totals = reinterpret_cast<int32_t*>(w + L.totals);
   const Geometry geo = make_geometry(p.N, p.N);
   PhaseTimer tm(s);
-  if (cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * (cb.nkeys + 1), s) != cudaSuccess) return PISA_ERR_CUDA;
+  if (!counts_zero && cudaMemsetAsync(cb.counts, 0, sizeof(int32_t) * (cb.nkeys + 1), s) != cudaSuccess)
+    return PISA_ERR_CUDA;
   if (launch_stage1(Q, P, S2, cb, p, geo, st->num_sms, st->err, s) != cudaSuccess) return PISA_ERR_CUDA;
   tm.mark(PH_STAGE1);
   if (launch_cluster(S2, cb, p, s) != cudaSuccess) return PISA_ERR_CUDA;
@@ -703,7 +707,8 @@ pisa_status pisa_prefill_host(const uint16_t* Q_host, const uint16_t* K_host, co
     if (p.causal) chk(cudaStreamWaitEvent(s, e_py[j], 0));
     chk(cudaStreamWaitEvent(s, e_q[j], 0));
     if (!ok) break;
-    if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, pc, st, s)) != PISA_OK) {
+    // after the first chunk the histogram is zero: the previous chunk's Stage 2 left it so
+    if ((rc = run_select(dQ, dK, dP, dIdx, nullptr, nullptr, w, sel_bytes, pc, st, s, j > 0)) != PISA_OK) {
       ok = false;
       break;
     }

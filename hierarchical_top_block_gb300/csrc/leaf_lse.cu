@@ -85,6 +85,8 @@ struct Params {
   int qgrp;   // 1: one 4-D box per query, stage layout [query][8-row group][d half][8][64]
   int scoring;  // 0 LSE, 1 log m + mean, 2 log m + mean + variance / 2
   float sl2;  // scale * log2(e)
+  int32_t* counts;     // the clustering histogram and Stage 1's item counter: zeroed here
+  long long ncounts;
 };
 
 // SC >= 0: the block score fixed at compile time (else prm.scoring); R > 0: G_Q = RPQ = R
@@ -94,6 +96,11 @@ __global__ void __launch_bounds__(THREADS, 1) leaf_lse_kernel(const __grid_const
                                                               uint32_t* err) {
   pdl_trigger();
   pdl_wait();  // the tile list and its counts come from the kernel before
+  // nothing reads the histogram (or Stage 1's item counter) after the tile list: left zeroed,
+  // so a next selection over the same scratch may skip its memset
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < prm.ncounts;
+       i += (long long)gridDim.x * blockDim.x)
+    prm.counts[i] = 0;
   constexpr int HALVES = D / 64;
   constexpr uint32_t STAGE_BYTES = ROWS * D * 2;   // also the K-pair stage size (KEYS == ROWS)
   constexpr int KSTEPS = D / 16;
@@ -546,6 +553,8 @@ cudaError_t launch_d(const uint16_t* Q, const uint16_t* K, const ClusterBuffers&
   prm.causal = p.causal;
   prm.scoring = p.scoring;
   prm.sl2 = p.scale * LOG2E;
+  prm.counts = cb.counts;
+  prm.ncounts = cb.nkeys + 1;
   const size_t smem = (size_t)(NQS + NKS) * ROWS * D * 2 + 1024;
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
