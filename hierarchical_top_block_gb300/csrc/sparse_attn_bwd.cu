@@ -18,6 +18,7 @@
 // queries by mma.sync (their Q and dO rows staged three ahead in a 4-buffer ring).  dK and dV
 // are added into fp32 (a block selected by many queries spans several chunks).
 #include "kernels.cuh"
+#include "pdl.cuh"
 
 namespace pisa {
 namespace {
@@ -59,6 +60,8 @@ __device__ __forceinline__ uint32_t swz(int half_bytes, int k, int c) {
 // each (coalesced: a warp reads 32 x 16 contiguous bytes of each), a shuffle tree per row
 template <int D>
 __global__ void bwd_dsum_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   constexpr int LPR = D / 8, RPW = 32 / LPR;  // lanes per row (16 at d = 128), rows per warp
   const long long rows = (long long)p.B * p.N * p.H_q;
   const int lane = threadIdx.x & 31, sub = lane % LPR;
@@ -91,6 +94,8 @@ __device__ __forceinline__ bool valid_block(const BwdParams& p, int blk, int t) 
 // (2a) per (bh, block): how many queries selected it; the value each atomic returns is the
 // entry's place in the block's list
 __global__ void bwd_count_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   const long long total = (long long)p.B * p.H_kv * p.N * p.Ksel;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
     const long long item = i / p.Ksel;
@@ -102,6 +107,8 @@ __global__ void bwd_count_kernel(BwdParams p) {
 
 // (2b) exclusive scans of the counts and of the per-block chunk counts (one CTA)
 __global__ void bwd_scan_kernel(BwdParams p, int nkeys, int32_t* chunk_off) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   __shared__ int32_t carry_s[2];
   __shared__ int32_t warp_s[2][32];
   if (threadIdx.x == 0) carry_s[0] = carry_s[1] = 0;
@@ -150,6 +157,8 @@ __global__ void bwd_scan_kernel(BwdParams p, int nkeys, int32_t* chunk_off) {
 
 // (2c) each selection entry's query position into its block's list
 __global__ void bwd_scatter_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   const long long total = (long long)p.B * p.H_kv * p.N * p.Ksel;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
     const long long item = i / p.Ksel;
@@ -163,6 +172,8 @@ __global__ void bwd_scatter_kernel(BwdParams p) {
 
 // (2d) chunk records {bh, block, first entry, count}
 __global__ void bwd_chunks_kernel(BwdParams p, int nkeys, const int32_t* chunk_off) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   for (int key = blockIdx.x * blockDim.x + threadIdx.x; key < nkeys; key += gridDim.x * blockDim.x) {
     const int c = p.counts[key];
     const int bh = key / p.M1, blk = key - bh * p.M1;
@@ -175,6 +186,8 @@ __global__ void bwd_chunks_kernel(BwdParams p, int nkeys, const int32_t* chunk_o
 // order), so that a chunk covers a narrow band of positions: one CTA per list, bitonic sort in
 // shared memory.  The entries (t << 5 | slot) are distinct, so the order is unique.
 __global__ void __launch_bounds__(512) bwd_sort_lists_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   extern __shared__ int32_t sbuf[];
   const int key = blockIdx.x;
   const int lo = p.offsets[key], n = p.offsets[key + 1] - lo;
@@ -218,12 +231,16 @@ __device__ __forceinline__ int chunk_bucket(const BwdParams& p, int ci) {
 }
 
 __global__ void bwd_bucket_count_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   const int n = *p.nchunks;
   for (int ci = blockIdx.x * blockDim.x + threadIdx.x; ci < n; ci += gridDim.x * blockDim.x)
     atomicAdd(&p.bucket_count[chunk_bucket(p, ci)], 1);
 }
 
 __global__ void __launch_bounds__(NBUCKETS) bwd_bucket_scan_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   __shared__ int32_t ws[NBUCKETS / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = p.bucket_count[threadIdx.x];
@@ -241,6 +258,8 @@ __global__ void __launch_bounds__(NBUCKETS) bwd_bucket_scan_kernel(BwdParams p) 
 }
 
 __global__ void bwd_bucket_scatter_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   const int n = *p.nchunks;
   for (int ci = blockIdx.x * blockDim.x + threadIdx.x; ci < n; ci += gridDim.x * blockDim.x) {
     const int b = chunk_bucket(p, ci);
@@ -251,6 +270,8 @@ __global__ void bwd_bucket_scatter_kernel(BwdParams p) {
 // (3) dQ: one warp per (b, h_kv, t)
 template <int D>
 __global__ void __launch_bounds__(32 * DQ_WARPS) bwd_dq_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   constexpr int KST = D / 16, NDT = D / 8, CPR = D / 8;
   constexpr int HALF = HK * 128;             // bytes of one 64-column half of a slot
   constexpr int SLOT = HK * D * 2;
@@ -456,6 +477,8 @@ __device__ __forceinline__ void dq_next(DqCursor& c, const BwdParams& p, long lo
 
 __global__ void __launch_bounds__(32 * DQS_WARPS, 1) bwd_dq_ds_kernel(const __grid_constant__ CUtensorMap mapK, BwdParams p,
                                                                     uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   constexpr int D = 128, NDT = D / 8;
   constexpr int HALF = HK * 128;             // bytes of one 64-column half of a slot
   constexpr int SLOT = HK * D * 2;
@@ -595,6 +618,8 @@ __device__ __forceinline__ void red_add(float* a, float v) {
 template <int D>
 // 3 CTAs per SM (<= 168 registers): the per-query chain is latency-bound, more warps hide it
 __global__ void __launch_bounds__(32 * KV_WARPS, 3) bwd_dkv_kernel(BwdParams p) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   constexpr int KST = D / 16, NDT = D / 8, CPR = D / 8;
   constexpr int KHALF = 64 * 128;            // K/V tiles: [half][64 keys][64]
   constexpr int QHALF = 16 * 128;            // Q/dO tiles: [half][16 heads][64]
@@ -798,6 +823,8 @@ __global__ void __launch_bounds__(tcb::THREADS, 1) bwd_dkv_tc_kernel(const __gri
                                                                      const __grid_constant__ CUtensorMap mapK,
                                                                      const __grid_constant__ CUtensorMap mapV,
                                                                      BwdParams p, uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();  // the kernel before on the stream has completed
   using namespace tcb;
   constexpr int D = 128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1152,8 +1179,9 @@ cudaError_t launch_dkv_tc(BwdParams& p, long long max_chunks, int num_sms, uint3
   if ((e = cudaFuncGetAttributes(&fa, bwd_dkv_tc_kernel)) != cudaSuccess) return e;
   if (fa.maxThreadsPerBlock < tcb::THREADS) return cudaErrorLaunchOutOfResources;  // registers x threads
   const int grid = (int)std::min<long long>(max_chunks, (long long)num_sms);
-  if (grid > 0) bwd_dkv_tc_kernel<<<grid, tcb::THREADS, tcb::SMEM, s>>>(mapQ, mapO, mapK, mapV, p, err);
-  return cudaGetLastError();
+  if (grid > 0)
+    return launch_pdl(bwd_dkv_tc_kernel, dim3(grid), dim3(tcb::THREADS), tcb::SMEM, s, mapQ, mapO, mapK, mapV, p, err);
+  return cudaSuccess;
 }
 
 template <int D>
@@ -1164,22 +1192,26 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
   const long long ents = (long long)p.B * p.H_kv * p.N * p.Ksel;
   const int g1 = (int)std::min<long long>((rows * (D / 8) + 255) / 256, (long long)num_sms * 32);
   const int g2 = (int)std::min<long long>((ents + 255) / 256, (long long)num_sms * 16);
+  // after the first, every kernel is a programmatic dependent of the one before (each waits for
+  // it to complete before its first access)
   bwd_dsum_kernel<D><<<g1 > 0 ? g1 : 1, 256, 0, s>>>(p);
-  bwd_count_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
-  bwd_scan_kernel<<<1, 1024, 0, s>>>(p, nkeys, chunk_off);
-  bwd_scatter_kernel<<<g2 > 0 ? g2 : 1, 256, 0, s>>>(p);
-  bwd_chunks_kernel<<<(nkeys + 255) / 256, 256, 0, s>>>(p, nkeys, chunk_off);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_count_kernel, dim3(g2 > 0 ? g2 : 1), dim3(256), 0, s, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_scan_kernel, dim3(1), dim3(1024), 0, s, p, nkeys, chunk_off)) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_scatter_kernel, dim3(g2 > 0 ? g2 : 1), dim3(256), 0, s, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_chunks_kernel, dim3((nkeys + 255) / 256), dim3(256), 0, s, p, nkeys, chunk_off)) != cudaSuccess)
+    return e;
   // lists by position, chunks by their first position
   if ((e = cudaFuncSetAttribute(bwd_sort_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)(SORT_CAP * sizeof(int32_t)))) != cudaSuccess)
     return e;
-  if (nkeys > 0) bwd_sort_lists_kernel<<<nkeys, 512, SORT_CAP * sizeof(int32_t), s>>>(p);
+  if (nkeys > 0 &&
+      (e = launch_pdl(bwd_sort_lists_kernel, dim3(nkeys), dim3(512), SORT_CAP * sizeof(int32_t), s, p)) != cudaSuccess)
+    return e;
   const int gc = (int)std::min<long long>((max_chunks + 255) / 256, (long long)num_sms * 8);
-  bwd_bucket_count_kernel<<<gc > 0 ? gc : 1, 256, 0, s>>>(p);
-  bwd_bucket_scan_kernel<<<1, NBUCKETS, 0, s>>>(p);
-  bwd_bucket_scatter_kernel<<<gc > 0 ? gc : 1, 256, 0, s>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_bucket_count_kernel, dim3(gc > 0 ? gc : 1), dim3(256), 0, s, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_bucket_scan_kernel, dim3(1), dim3(NBUCKETS), 0, s, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(bwd_bucket_scatter_kernel, dim3(gc > 0 ? gc : 1), dim3(256), 0, s, p)) != cudaSuccess) return e;
   p.chunks = p.chunks_by_t;
   const long long items = (long long)p.B * p.H_kv * p.N;
   if (p.tc && (e = launch_dkv_tc(p, max_chunks, num_sms, err, s)) != cudaSuccess) return e;
@@ -1197,20 +1229,21 @@ cudaError_t launch_d(BwdParams& p, int nkeys, int32_t* chunk_off, long long max_
         cudaSuccess)
       return e;
     const long long gds = std::min<long long>((items + DQS_WARPS - 1) / DQS_WARPS, (long long)num_sms);
-    bwd_dq_ds_kernel<<<(int)gds, 32 * DQS_WARPS, smem_ds, s>>>(mapK, p, err);
-    return cudaGetLastError();
+    return launch_pdl(bwd_dq_ds_kernel, dim3((unsigned)gds), dim3(32 * DQS_WARPS), smem_ds, s, mapK, p, err);
   }
   const size_t smem_q = (size_t)DQ_WARPS * 2 * HK * D * 2 + 1024;
   if ((e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q)) != cudaSuccess)
     return e;
   const long long gq = std::min<long long>((items + DQ_WARPS - 1) / DQ_WARPS, (long long)num_sms);
-  bwd_dq_kernel<D><<<(int)gq, 32 * DQ_WARPS, smem_q, s>>>(p);
-  if (p.tc) return cudaGetLastError();
+  if ((e = launch_pdl(bwd_dq_kernel<D>, dim3((unsigned)gq), dim3(32 * DQ_WARPS), smem_q, s, p)) != cudaSuccess) return e;
+  if (p.tc) return cudaSuccess;
   const size_t smem_kv = (size_t)2 * 64 * D * 2 + (size_t)2 * KV_NBUF * 16 * D * 2 + 1024;
   if ((e = cudaFuncSetAttribute(bwd_dkv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv)) !=
       cudaSuccess)
     return e;
-  if (max_chunks > 0) bwd_dkv_kernel<D><<<(int)max_chunks, 32 * KV_WARPS, smem_kv, s>>>(p);
+  if (max_chunks > 0 &&
+      (e = launch_pdl(bwd_dkv_kernel<D>, dim3((unsigned)max_chunks), dim3(32 * KV_WARPS), smem_kv, s, p)) != cudaSuccess)
+    return e;
   return cudaGetLastError();
 }
 
