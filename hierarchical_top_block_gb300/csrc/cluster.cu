@@ -141,16 +141,30 @@ __global__ void scatter_tiles_kernel(const int32_t* __restrict__ S2, ClusterBuff
   pdl_trigger();
   pdl_wait();
   if ((int)blockIdx.x >= nb_scatter) {
-    const long long nb_tiles = (long long)gridDim.x - nb_scatter;
-    for (long long k = ((long long)blockIdx.x - nb_scatter) * blockDim.x + threadIdx.x; k < cb.nkeys;
-         k += nb_tiles * blockDim.x) {
-      const int n = cb.counts[k];
-      if (n == 0) continue;
-      const int node = (int)(k % cb.M2);
-      const int bh = (int)(k / ((long long)cb.nwin * cb.M2));
-      const int e0 = cb.offsets[k];
-      int tix = cb.tile_off[k];
-      for (int s = 0; s < n; s += cb.qt, ++tix) cb.tiles[tix] = make_int4(bh, node, e0 + s, min(cb.qt, n - s));
+    // a warp takes 32 keys at a time (one per lane) and writes the tiles of each of them with all
+    // its lanes, so a key that many queries of a window selected (hundreds of tiles) costs no
+    // more than a few stores per lane
+    const int lane = threadIdx.x & 31;
+    const long long nw = ((long long)gridDim.x - nb_scatter) * (blockDim.x / 32);
+    const long long gw = ((long long)blockIdx.x - nb_scatter) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    for (long long k0 = gw * 32; k0 < cb.nkeys; k0 += nw * 32) {
+      const long long k = k0 + lane;
+      const int n = k < cb.nkeys ? cb.counts[k] : 0;
+      const int e0 = n ? cb.offsets[k] : 0, t0 = n ? cb.tile_off[k] : 0;
+      unsigned busy = __ballot_sync(0xffffffffu, n > 0);
+      while (busy) {
+        const int j = __ffs(busy) - 1;
+        busy &= busy - 1;
+        const int nj = __shfl_sync(0xffffffffu, n, j), ej = __shfl_sync(0xffffffffu, e0, j);
+        const int tj = __shfl_sync(0xffffffffu, t0, j);
+        const long long kj = k0 + j;
+        const int node = (int)(kj % cb.M2);
+        const int bh = (int)(kj / ((long long)cb.nwin * cb.M2));
+        for (int i = lane; i * cb.qt < nj; i += 32) {
+          const int s = i * cb.qt;
+          cb.tiles[tj + i] = make_int4(bh, node, ej + s, min(cb.qt, nj - s));
+        }
+      }
     }
     return;
   }
@@ -182,7 +196,7 @@ cudaError_t launch_cluster(const int32_t* S2, const ClusterBuffers& cb, const Pr
   if ((e = launch_pdl(scan_local_kernel, dim3(cb.nblocks), dim3(SCAN_THREADS), 0, s, cb)) != cudaSuccess) return e;
   if ((e = launch_pdl(scan_blocks_kernel, dim3(1), dim3(SCAN_THREADS), 0, s, cb)) != cudaSuccess) return e;
   if ((e = launch_pdl(scan_add_kernel, dim3(cb.nblocks), dim3(SCAN_THREADS), 0, s, cb)) != cudaSuccess) return e;
-  const int nb_scatter = grid_for(total * p.K, THREADS), nb_tiles = grid_for(cb.nkeys, THREADS);
+  const int nb_scatter = grid_for(total * p.K, THREADS), nb_tiles = grid_for((cb.nkeys + 31) / 32, THREADS / 32);
   return launch_pdl(scatter_tiles_kernel, dim3(nb_scatter + nb_tiles), dim3(THREADS), 0, s, S2, cb, p.N, p.t_lo, nq,
                     p.K, total, nb_scatter);
 }
